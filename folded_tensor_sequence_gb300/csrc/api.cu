@@ -1,0 +1,633 @@
+// libtsp C ABI: plan validation, workspace layout and the orchestration of
+// one TSP transformer layer on one GPU.
+//
+// Schedule of the layer (ai-trends.today, "Zyphra Introduces Tensor and
+// Sequence Parallelism (TSP)", section "How to Fold a Book"; edge.aivizor.me
+// TSP news post), with the D ranks emulated as partitions of device memory:
+//   1. zigzag permute: rank r's tokens are chunks r and 2D-1-r;
+//   2. attention: for every weight shard s, every rank projects its local
+//      tokens with {W_Q, W_K, W_V}^s, K/V are all-gathered into natural
+//      order, causal attention runs, and O_s W_O^s is accumulated locally.
+//      Here: one projection GEMM over all shards (N = 3h) whose epilogue does
+//      the gather, the zigzag-balanced attention kernel, and one output GEMM
+//      whose K loop is the sum over shards (+ residual);
+//   3. gated MLP ring: each rank accumulates SiLU(H W_g^j)(H W_u^j) W_d^j over
+//      the shards j passing around the ring, with no all-reduce.  Here: one
+//      gate/up GEMM with the SiLU*up epilogue and one down GEMM whose K loop is
+//      the ring's sum over shards (+ residual);
+//   4. unpermute back to natural order.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <initializer_list>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace tsp {
+
+__device__ unsigned int g_dev_error_word = 0;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+thread_local tsp_status t_fail_status = TSP_OK;
+thread_local int t_fail_count = 0;
+
+tsp_status fail(tsp_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+tsp_status fail(tsp_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+tsp_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return TSP_OK;
+  return fail(TSP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Consumes one armed injected failure, if any.
+bool injected(tsp_status* out) {
+  if (t_fail_count > 0) {
+    --t_fail_count;
+    *out = fail(t_fail_status, "injected failure (tsp_debug_fail_next)");
+    return true;
+  }
+  return false;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t esize(const tsp_plan* p) { return p->dtype == TSP_BF16 ? 2 : 4; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Offsets of the layer's activations inside one buffer (the `saved` buffer
+// for the backward and the forward's workspace share this layout).
+struct Layout {
+  size_t xz, qz, k, v, oz, lse, hz, gu, mz, yz;  // yz: forward workspace only
+  size_t saved_end, fwd_end;
+};
+
+Layout layer_layout(const tsp_plan* p, int batch) {
+  const size_t T = (size_t)batch * p->seq, h = p->hidden, F = p->ffn, e = esize(p);
+  Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.xz = take(T * h * e);
+  L.qz = take(T * h * e);
+  L.k = take(T * h * e);
+  L.v = take(T * h * e);
+  L.oz = take(T * h * e);
+  L.lse = take((size_t)batch * p->heads * p->seq * 4);
+  L.hz = take(T * h * e);
+  L.gu = take(T * 2 * F * e);
+  L.mz = take(T * F * e);
+  L.saved_end = o;
+  L.yz = take(T * h * e);
+  L.fwd_end = o;
+  return L;
+}
+
+struct BwdLayout {
+  size_t dyz, wd_c, dgu, dyzT, mzT, wgu_T, dhz, dguT, hzT, wo_c, doz, dhzT, ozT, dq, dk, dv, dsum, dqkv, wqkv_T,
+      dxz, dqkvT, xzT, end;
+};
+
+BwdLayout bwd_layout(const tsp_plan* p, int batch) {
+  const size_t T = (size_t)batch * p->seq, h = p->hidden, F = p->ffn, e = esize(p);
+  BwdLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.dyz = take(T * h * e);
+  L.wd_c = take(F * h * e);
+  L.dgu = take(T * 2 * F * e);
+  L.dyzT = take(T * h * e);
+  L.mzT = take(T * F * e);
+  L.wgu_T = take(2 * F * h * e);
+  L.dhz = take(T * h * e);
+  L.dguT = take(T * 2 * F * e);
+  L.hzT = take(T * h * e);
+  L.wo_c = take(h * h * e);
+  L.doz = take(T * h * e);
+  L.dhzT = take(T * h * e);
+  L.ozT = take(T * h * e);
+  L.dq = take(T * h * e);
+  L.dk = take(T * h * e);
+  L.dv = take(T * h * e);
+  L.dsum = take((size_t)batch * p->heads * p->seq * 4);
+  L.dqkv = take(T * 3 * h * e);
+  L.wqkv_T = take(3 * h * h * e);
+  L.dxz = take(T * h * e);
+  L.dqkvT = take(T * 3 * h * e);
+  L.xzT = take(T * h * e);
+  L.end = o;
+  return L;
+}
+
+size_t attn_ws_bytes(const tsp_plan* p, int batch) {
+  const size_t T = (size_t)batch * p->seq, h = p->hidden, e = esize(p);
+  return 4 * align256(T * h * e);
+}
+
+size_t mlp_ws_bytes(const tsp_plan* p, int batch) {
+  const size_t T = (size_t)batch * p->seq, F = p->ffn, e = esize(p);
+  return align256(T * F * e) + align256(T * 2 * F * e);
+}
+
+tsp_status check_plan_batch(const tsp_plan* p, int batch) {
+  if (!p) return fail(TSP_ERR_INVALID_ARG, "plan is NULL");
+  if (batch < 0) return fail(TSP_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if ((int64_t)batch * p->seq > (int64_t)INT32_MAX / 4)
+    return fail(TSP_ERR_UNSUPPORTED, "batch*seq = %lld too large", (long long)batch * p->seq);
+  return TSP_OK;
+}
+
+tsp_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
+  for (const void* q : ptrs) {
+    if (!q) return fail(TSP_ERR_INVALID_ARG, "%s: NULL pointer", what);
+    if (!aligned16(q)) return fail(TSP_ERR_INVALID_ARG, "%s: pointer %p not 16-byte aligned", what, q);
+  }
+  return TSP_OK;
+}
+
+tsp_status check_bf16_shapes(const tsp_plan* p) {
+  if (p->dtype != TSP_BF16) return TSP_OK;
+  if (p->hidden % 256 || p->ffn % 256)
+    return fail(TSP_ERR_UNSUPPORTED, "bf16 kernels need hidden %% 256 == 0 and ffn %% 256 == 0 (got %d, %d)",
+                p->hidden, p->ffn);
+  if (p->head_dim != 128) return fail(TSP_ERR_UNSUPPORTED, "bf16 attention needs head_dim 128 (got %d)", p->head_dim);
+  return TSP_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// ---- the layer pieces ------------------------------------------------------
+
+EpiParams base_epi(const tsp_plan* p, int batch) {
+  EpiParams ep;
+  ep.D = p->D;
+  ep.B = batch;
+  ep.S = (int)p->seq;
+  ep.C = (int)p->chunk;
+  ep.H = p->heads;
+  ep.dh = p->head_dim;
+  ep.h = p->hidden;
+  ep.err = dev_error_word();
+  return ep;
+}
+
+tsp_status run_gemm(const tsp_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K,
+                    EpiKind epi, const EpiParams& ep, cudaStream_t st, const char* what) {
+  tsp_status s = p->dtype == TSP_BF16
+                     ? gemm_bf16_tc(A, lda, B, ldb, M, N, K, epi, ep, st)
+                     : gemm_f32_simt(static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb, M, N, K,
+                                     epi, ep, st);
+  if (s != TSP_OK) return fail(s, "%s GEMM (M=%d N=%d K=%d) failed: %s", what, M, N, K, tsp_status_string(s));
+  return TSP_OK;
+}
+
+// a_out = (Attn(xz Wq, xz Wk, xz Wv)) Wo [+ resid]
+tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const tsp_weights* w, void* a_out,
+                          const void* resid, float* lse, char* qz, char* k, char* v, char* oz, cudaStream_t st) {
+  const int T = batch * (int)p->seq, h = p->hidden;
+  EpiParams ep = base_epi(p, batch);
+  ep.q = qz;
+  ep.k = k;
+  ep.v = v;
+  tsp_status s = run_gemm(p, xz, h, w->qkv, h, T, 3 * h, h, EPI_QKV, ep, st, "QKV projection");
+  if (s != TSP_OK) return s;
+  AttnParams ap;
+  ap.q = qz;
+  ap.k = k;
+  ap.v = v;
+  ap.o = oz;
+  ap.lse = lse;
+  ap.D = p->D;
+  ap.B = batch;
+  ap.H = p->heads;
+  ap.dh = p->head_dim;
+  ap.S = p->seq;
+  ap.C = p->chunk;
+  s = p->dtype == TSP_BF16 ? attn_fwd_bf16(ap, st) : attn_fwd_f32(ap, st);
+  if (s != TSP_OK) return fail(s, "attention kernel failed: %s", tsp_status_string(s));
+  EpiParams eo = base_epi(p, batch);
+  eo.out = a_out;
+  eo.ldo = h;
+  eo.resid = resid;
+  eo.ldr = h;
+  return run_gemm(p, oz, h, w->o, h, T, h, h, resid ? EPI_RESID : EPI_STORE, eo, st, "output projection");
+}
+
+// out = (SiLU(hz Wg) * (hz Wu)) Wd [+ resid]; optionally keeps the raw gate/up in gu_save
+tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weights* w, void* out, const void* resid,
+                    char* mz, char* gu, bool save_gu, cudaStream_t st) {
+  const int T = batch * (int)p->seq, h = p->hidden, F = p->ffn;
+  tsp_status s;
+  if (p->dtype == TSP_BF16) {
+    EpiParams eg = base_epi(p, batch);
+    eg.out = mz;
+    eg.ldo = F;
+    eg.aux = save_gu ? gu : nullptr;
+    eg.ldx = 2 * F;
+    s = run_gemm(p, hz, h, w->gate_up, h, T, 2 * F, h, EPI_SWIGLU, eg, st, "gate/up projection");
+  } else {
+    EpiParams eg = base_epi(p, batch);
+    eg.out = gu;
+    eg.ldo = 2 * F;
+    s = run_gemm(p, hz, h, w->gate_up, h, T, 2 * F, h, EPI_STORE, eg, st, "gate/up projection");
+    if (s == TSP_OK)
+      s = cuda_status(launch_swiglu_f32(reinterpret_cast<const float*>(gu), reinterpret_cast<float*>(mz), T, F, st),
+                      "swiglu");
+  }
+  if (s != TSP_OK) return s;
+  EpiParams ed = base_epi(p, batch);
+  ed.out = out;
+  ed.ldo = h;
+  ed.resid = resid;
+  ed.ldr = h;
+  return run_gemm(p, mz, F, w->down, F, T, h, F, resid ? EPI_RESID : EPI_STORE, ed, st, "down projection");
+}
+
+}  // namespace
+
+unsigned int* dev_error_word() {
+  static unsigned int* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_dev_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(a);
+  }
+  return ptrs[dev];
+}
+
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace tsp
+
+using namespace tsp;
+
+extern "C" {
+
+const char* tsp_status_string(tsp_status s) {
+  switch (s) {
+    case TSP_OK: return "TSP_OK";
+    case TSP_ERR_INVALID_ARG: return "TSP_ERR_INVALID_ARG";
+    case TSP_ERR_UNSUPPORTED: return "TSP_ERR_UNSUPPORTED";
+    case TSP_ERR_CUDA: return "TSP_ERR_CUDA";
+    case TSP_ERR_TIMEOUT: return "TSP_ERR_TIMEOUT";
+    case TSP_ERR_WORKSPACE: return "TSP_ERR_WORKSPACE";
+  }
+  return "TSP_ERR_UNKNOWN";
+}
+
+const char* tsp_last_error_message(void) { return t_last_error; }
+
+void tsp_debug_fail_next(tsp_status status, int count) {
+  t_fail_status = status;
+  t_fail_count = count > 0 ? count : 0;
+}
+
+tsp_status tsp_plan_create(int D, int64_t seq, int hidden, int heads, int head_dim, int ffn, tsp_dtype dtype,
+                           tsp_plan** out) {
+  if (!out) return fail(TSP_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (D < 1) return fail(TSP_ERR_INVALID_ARG, "D = %d < 1", D);
+  if (seq < 2 * (int64_t)D || seq % (2 * (int64_t)D))
+    return fail(TSP_ERR_INVALID_ARG, "seq %lld not a positive multiple of 2D = %d", (long long)seq, 2 * D);
+  if (heads < 1 || head_dim < 1 || hidden != heads * head_dim)
+    return fail(TSP_ERR_INVALID_ARG, "hidden %d != heads %d * head_dim %d", hidden, heads, head_dim);
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128)
+    return fail(TSP_ERR_INVALID_ARG, "head_dim %d not in {32, 64, 128}", head_dim);
+  if (heads % D) return fail(TSP_ERR_INVALID_ARG, "heads %d not divisible by D %d", heads, D);
+  if (ffn < 1 || ffn % D) return fail(TSP_ERR_INVALID_ARG, "ffn %d not a positive multiple of D %d", ffn, D);
+  if (hidden % 8) return fail(TSP_ERR_INVALID_ARG, "hidden %d not a multiple of 8", hidden);
+  if (ffn % 128) return fail(TSP_ERR_INVALID_ARG, "ffn %d not a multiple of 128", ffn);
+  if (dtype != TSP_F32 && dtype != TSP_BF16) return fail(TSP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (seq > (int64_t)INT32_MAX / 4) return fail(TSP_ERR_UNSUPPORTED, "seq %lld too large", (long long)seq);
+  tsp_plan* p = new (std::nothrow) tsp_plan;
+  if (!p) return fail(TSP_ERR_INVALID_ARG, "out of host memory");
+  p->D = D;
+  p->seq = seq;
+  p->hidden = hidden;
+  p->heads = heads;
+  p->head_dim = head_dim;
+  p->ffn = ffn;
+  p->dtype = dtype;
+  p->chunk = seq / (2 * D);
+  *out = p;
+  return TSP_OK;
+}
+
+void tsp_plan_destroy(tsp_plan* plan) { delete plan; }
+
+size_t tsp_workspace_bytes(const tsp_plan* p, int batch, tsp_op op) {
+  if (!p || batch < 0) return 0;
+  switch (op) {
+    case TSP_OP_ATTENTION_FWD: return attn_ws_bytes(p, batch);
+    case TSP_OP_GATED_MLP_FWD: return mlp_ws_bytes(p, batch);
+    case TSP_OP_LAYER_FWD: return layer_layout(p, batch).fwd_end;
+    case TSP_OP_LAYER_BWD: return bwd_layout(p, batch).end;
+  }
+  return 0;
+}
+
+size_t tsp_saved_bytes(const tsp_plan* p, int batch) {
+  if (!p || batch < 0) return 0;
+  return layer_layout(p, batch).saved_end;
+}
+
+tsp_status tsp_pack_weights(const tsp_plan* p, const void* const canonical[7], const tsp_weight_grads* packed,
+                            void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if (!p || !canonical || !packed) return fail(TSP_ERR_INVALID_ARG, "NULL argument");
+  if ((s = check_ptrs({canonical[0], canonical[1], canonical[2], canonical[3], canonical[4], canonical[5],
+                       canonical[6], packed->qkv, packed->o, packed->gate_up, packed->down},
+                      "tsp_pack_weights")) != TSP_OK)
+    return s;
+  return cuda_status(launch_pack_weights(p, canonical, packed, false, as_stream(stream)), "pack weights");
+}
+
+tsp_status tsp_unpack_weights(const tsp_plan* p, const tsp_weights* packed, void* const canonical[7], void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if (!p || !canonical || !packed) return fail(TSP_ERR_INVALID_ARG, "NULL argument");
+  if ((s = check_ptrs({canonical[0], canonical[1], canonical[2], canonical[3], canonical[4], canonical[5],
+                       canonical[6], packed->qkv, packed->o, packed->gate_up, packed->down},
+                      "tsp_unpack_weights")) != TSP_OK)
+    return s;
+  tsp_weight_grads w{const_cast<void*>(packed->qkv), const_cast<void*>(packed->o), const_cast<void*>(packed->gate_up),
+                     const_cast<void*>(packed->down)};
+  return cuda_status(launch_pack_weights(p, const_cast<const void* const*>(canonical), &w, true, as_stream(stream)),
+                     "unpack weights");
+}
+
+tsp_status tsp_zigzag_permute(const tsp_plan* p, int batch, const void* x, void* xz, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if ((s = check_ptrs({x, xz}, "tsp_zigzag_permute")) != TSP_OK) return s;
+  return cuda_status(
+      launch_zigzag_rows(x, xz, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, true, as_stream(stream)),
+      "zigzag permute");
+}
+
+tsp_status tsp_zigzag_unpermute(const tsp_plan* p, int batch, const void* xz, void* x, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if ((s = check_ptrs({x, xz}, "tsp_zigzag_unpermute")) != TSP_OK) return s;
+  return cuda_status(
+      launch_zigzag_rows(xz, x, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, false, as_stream(stream)),
+      "zigzag unpermute");
+}
+
+tsp_status tsp_kv_gather(const tsp_plan* p, int batch, const void* kz, const void* vz, void* k, void* v,
+                         void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if ((s = check_ptrs({kz, vz, k, v}, "tsp_kv_gather")) != TSP_OK) return s;
+  return cuda_status(launch_kv_gather(kz, vz, k, v, (int)esize(p), p->D, batch, p->seq, p->heads, p->head_dim,
+                                      as_stream(stream)),
+                     "kv gather");
+}
+
+tsp_status tsp_attention_fwd(const tsp_plan* p, int batch, const void* xz, const tsp_weights* w, void* a_out,
+                             void* lse, void* ws, size_t ws_bytes, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if (!w) return fail(TSP_ERR_INVALID_ARG, "weights is NULL");
+  if ((s = check_ptrs({xz, a_out, w->qkv, w->o, ws}, "tsp_attention_fwd")) != TSP_OK) return s;
+  if (lse && !aligned16(lse)) return fail(TSP_ERR_INVALID_ARG, "lse not 16-byte aligned");
+  if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
+  if (ws_bytes < attn_ws_bytes(p, batch))
+    return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, attn_ws_bytes(p, batch));
+  const size_t blk = attn_ws_bytes(p, batch) / 4;
+  char* base = static_cast<char*>(ws);
+  return attention_impl(p, batch, xz, w, a_out, nullptr, static_cast<float*>(lse), base, base + blk, base + 2 * blk,
+                        base + 3 * blk, as_stream(stream));
+}
+
+tsp_status tsp_gated_mlp_fwd(const tsp_plan* p, int batch, const void* hz, const tsp_weights* w, void* m_out,
+                             void* ws, size_t ws_bytes, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if (!w) return fail(TSP_ERR_INVALID_ARG, "weights is NULL");
+  if ((s = check_ptrs({hz, m_out, w->gate_up, w->down, ws}, "tsp_gated_mlp_fwd")) != TSP_OK) return s;
+  if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
+  if (ws_bytes < mlp_ws_bytes(p, batch))
+    return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, mlp_ws_bytes(p, batch));
+  const size_t T = (size_t)batch * p->seq;
+  char* mz = static_cast<char*>(ws);
+  char* gu = mz + align256(T * p->ffn * esize(p));
+  return mlp_impl(p, batch, hz, w, m_out, nullptr, mz, gu, false, as_stream(stream));
+}
+
+tsp_status tsp_layer_fwd(const tsp_plan* p, int batch, const void* x, const tsp_weights* w, void* y, void* saved,
+                         void* ws, size_t ws_bytes, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if (!w) return fail(TSP_ERR_INVALID_ARG, "weights is NULL");
+  if ((s = check_ptrs({x, y, w->qkv, w->o, w->gate_up, w->down, ws}, "tsp_layer_fwd")) != TSP_OK) return s;
+  if (saved && !aligned16(saved)) return fail(TSP_ERR_INVALID_ARG, "saved not 16-byte aligned");
+  if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
+  const Layout L = layer_layout(p, batch);
+  if (ws_bytes < L.fwd_end) return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, L.fwd_end);
+  cudaStream_t st = as_stream(stream);
+  char* wsb = static_cast<char*>(ws);
+  char* act = saved ? static_cast<char*>(saved) : wsb;  // where the saved activations go
+  char* xz = act + L.xz;
+  char* yz = wsb + L.yz;
+  if ((s = cuda_status(launch_zigzag_rows(x, xz, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, true, st),
+                       "zigzag permute")) != TSP_OK)
+    return s;
+  s = attention_impl(p, batch, xz, w, act + L.hz, xz, saved ? reinterpret_cast<float*>(act + L.lse) : nullptr,
+                     act + L.qz, act + L.k, act + L.v, act + L.oz, st);
+  if (s != TSP_OK) return s;
+  s = mlp_impl(p, batch, act + L.hz, w, yz, act + L.hz, act + L.mz, act + L.gu, saved != nullptr, st);
+  if (s != TSP_OK) return s;
+  return cuda_status(launch_zigzag_rows(yz, y, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, false, st),
+                     "zigzag unpermute");
+}
+
+tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_weights* w, const void* saved,
+                         const void* dy, void* dx, const tsp_weight_grads* dw, void* ws, size_t ws_bytes,
+                         void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if (!w || !dw) return fail(TSP_ERR_INVALID_ARG, "weights or grads is NULL");
+  if ((s = check_ptrs({x, saved, dy, dx, w->qkv, w->o, w->gate_up, w->down, dw->qkv, dw->o, dw->gate_up, dw->down,
+                       ws},
+                      "tsp_layer_bwd")) != TSP_OK)
+    return s;
+  if (p->dtype != TSP_BF16) return fail(TSP_ERR_UNSUPPORTED, "layer backward is implemented for bf16 plans");
+  if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
+  const int64_t T64 = (int64_t)batch * p->seq;
+  if (T64 % 64) return fail(TSP_ERR_UNSUPPORTED, "backward needs batch*seq %% 64 == 0 (got %lld)", (long long)T64);
+  const BwdLayout L = bwd_layout(p, batch);
+  if (ws_bytes < L.end) return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, L.end);
+  const Layout A = layer_layout(p, batch);
+  cudaStream_t st = as_stream(stream);
+  const char* sv = static_cast<const char*>(saved);
+  char* wb = static_cast<char*>(ws);
+  const int T = (int)T64, h = p->hidden, F = p->ffn;
+  const int64_t eb = (int64_t)esize(p);
+  auto tr = [&](const void* src, size_t dst_off, int64_t rows, int64_t cols, const char* what) {
+    return cuda_status(launch_transpose(src, wb + dst_off, rows, cols, (int)eb, st), what);
+  };
+#define TSP_TRY(expr)              \
+  do {                             \
+    if ((s = (expr)) != TSP_OK) return s; \
+  } while (0)
+  // MLP backward
+  TSP_TRY(cuda_status(launch_zigzag_rows(dy, wb + L.dyz, h * eb, p->D, batch, p->seq, true, st), "permute dy"));
+  TSP_TRY(tr(w->down, L.wd_c, h, F, "transpose W_down"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = wb + L.dgu;
+    e.ldo = 2 * F;
+    e.resid = sv + A.gu;
+    e.ldr = 2 * F;
+    TSP_TRY(run_gemm(p, wb + L.dyz, h, wb + L.wd_c, h, T, F, h, EPI_DSWIGLU, e, st, "dM = dY Wd^T"));
+  }
+  TSP_TRY(tr(wb + L.dyz, L.dyzT, T, h, "transpose dY"));
+  TSP_TRY(tr(sv + A.mz, L.mzT, T, F, "transpose M"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = dw->down;
+    e.ldo = F;
+    TSP_TRY(run_gemm(p, wb + L.dyzT, T, wb + L.mzT, T, h, F, T, EPI_STORE, e, st, "dW_down"));
+  }
+  TSP_TRY(tr(w->gate_up, L.wgu_T, 2 * F, h, "transpose W_gate_up"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = wb + L.dhz;
+    e.ldo = h;
+    e.resid = wb + L.dyz;
+    e.ldr = h;
+    TSP_TRY(run_gemm(p, wb + L.dgu, 2 * F, wb + L.wgu_T, 2 * F, T, h, 2 * F, EPI_RESID, e, st, "dH"));
+  }
+  TSP_TRY(tr(wb + L.dgu, L.dguT, T, 2 * F, "transpose dGU"));
+  TSP_TRY(tr(sv + A.hz, L.hzT, T, h, "transpose H"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = dw->gate_up;
+    e.ldo = h;
+    TSP_TRY(run_gemm(p, wb + L.dguT, T, wb + L.hzT, T, 2 * F, h, T, EPI_STORE, e, st, "dW_gate_up"));
+  }
+  // attention output projection backward
+  TSP_TRY(tr(w->o, L.wo_c, h, h, "transpose W_O"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = wb + L.doz;
+    e.ldo = h;
+    TSP_TRY(run_gemm(p, wb + L.dhz, h, wb + L.wo_c, h, T, h, h, EPI_STORE, e, st, "dO"));
+  }
+  TSP_TRY(tr(wb + L.dhz, L.dhzT, T, h, "transpose dH"));
+  TSP_TRY(tr(sv + A.oz, L.ozT, T, h, "transpose O"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = dw->o;
+    e.ldo = h;
+    TSP_TRY(run_gemm(p, wb + L.dhzT, T, wb + L.ozT, T, h, h, T, EPI_STORE, e, st, "dW_O"));
+  }
+  // attention core backward
+  {
+    AttnBwdParams ab;
+    ab.q = sv + A.qz;
+    ab.k = sv + A.k;
+    ab.v = sv + A.v;
+    ab.o = sv + A.oz;
+    ab.dO = wb + L.doz;
+    ab.lse = reinterpret_cast<const float*>(sv + A.lse);
+    ab.dsum = reinterpret_cast<float*>(wb + L.dsum);
+    ab.dq = wb + L.dq;
+    ab.dk = wb + L.dk;
+    ab.dv = wb + L.dv;
+    ab.D = p->D;
+    ab.B = batch;
+    ab.H = p->heads;
+    ab.dh = p->head_dim;
+    ab.S = p->seq;
+    ab.C = p->chunk;
+    s = attn_bwd_bf16(ab, st);
+    if (s != TSP_OK) return fail(s, "attention backward failed: %s", tsp_status_string(s));
+  }
+  TSP_TRY(cuda_status(launch_assemble_dqkv(wb + L.dq, wb + L.dk, wb + L.dv, wb + L.dqkv, p->D, batch, p->seq,
+                                           p->heads, p->head_dim, st),
+                      "assemble dQKV"));
+  TSP_TRY(tr(w->qkv, L.wqkv_T, 3 * h, h, "transpose W_QKV"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = wb + L.dxz;
+    e.ldo = h;
+    e.resid = wb + L.dhz;
+    e.ldr = h;
+    TSP_TRY(run_gemm(p, wb + L.dqkv, 3 * h, wb + L.wqkv_T, 3 * h, T, h, 3 * h, EPI_RESID, e, st, "dx"));
+  }
+  TSP_TRY(tr(wb + L.dqkv, L.dqkvT, T, 3 * h, "transpose dQKV"));
+  TSP_TRY(tr(sv + A.xz, L.xzT, T, h, "transpose xz"));
+  {
+    EpiParams e = base_epi(p, batch);
+    e.out = dw->qkv;
+    e.ldo = h;
+    TSP_TRY(run_gemm(p, wb + L.dqkvT, T, wb + L.xzT, T, 3 * h, h, T, EPI_STORE, e, st, "dW_QKV"));
+  }
+  return cuda_status(launch_zigzag_rows(wb + L.dxz, dx, h * eb, p->D, batch, p->seq, false, st), "unpermute dx");
+#undef TSP_TRY
+}
+
+tsp_status tsp_sync_check(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return fail(TSP_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(TSP_ERR_CUDA, "pending CUDA error: %s", cudaGetErrorString(e));
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_dev_error_word, sizeof(word));
+  if (e != cudaSuccess) return fail(TSP_ERR_CUDA, "reading device error word: %s", cudaGetErrorString(e));
+  if (word) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_dev_error_word, &zero, sizeof(zero));
+    return fail(TSP_ERR_TIMEOUT, "device wait gave up (kernel %u, site %u)", word >> 8, word & 0xFF);
+  }
+  return TSP_OK;
+}
+
+}  // extern "C"

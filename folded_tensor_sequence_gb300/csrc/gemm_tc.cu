@@ -1,0 +1,389 @@
+// Persistent bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// C[M][N] = sum_k A[m][k] * B[n][k], both operands K-major bf16, fp32
+// accumulation in tensor memory, fused epilogues for the TSP layer:
+//   - QKV projection over all weight shards at once (N = 3h): the epilogue
+//     writes Q in zigzag token order and scatters K/V straight into gathered
+//     natural order per head, which is the zigzag K/V all-gather of the TSP
+//     attention schedule done for free (ai-trends.today TSP article, "How to
+//     Fold a Book");
+//   - output projection and down projection, whose K loop walks every weight
+//     shard in turn: the row-sharded partial products X_s W_s are summed in
+//     the TMEM accumulator, never leaving the SM (the per-rank accumulation of
+//     partial outputs that replaces the all-reduce; row split XW = X1W1 + X2W2,
+//     r007 chapter "Распределенное обучение", section "Тензорный параллелизм"),
+//     plus the residual add;
+//   - gate/up projection with SiLU(gate) * up computed from one TMEM tile that
+//     holds matching gate and up columns.
+//
+// Tile 128 x 256 x 64, 4-stage TMA ring (128-byte swizzle), one CTA per SM,
+// persistent over tiles.  Warp roles: warp 0 = TMA producer, warp 1 = MMA
+// issuer (and TMEM owner), warps 2..5 = epilogue (one TMEM lane quadrant each).
+// Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
+// tile overlap the main loop of the next.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace tsp {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;  // 32 KB
+constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int GROUP_M = 16;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct GemmShape {
+  int M, N, K;
+  int num_m, num_n, num_tiles, kblocks;
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmShape& s, int& mt, int& nt) {
+  const int per_group = GROUP_M * s.num_n;
+  const int group = t / per_group;
+  const int first_m = group * GROUP_M;
+  const int gsz = min(s.num_m - first_m, GROUP_M);
+  const int in_g = t - group * per_group;
+  mt = first_m + in_g % gsz;
+  nt = in_g / gsz;
+}
+
+__device__ __forceinline__ void store32_bf16(void* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  }
+}
+
+__device__ __forceinline__ void load32_bf16(const void* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = s[i];
+    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+    v[8 * i + 0] = a.x; v[8 * i + 1] = a.y; v[8 * i + 2] = b.x; v[8 * i + 3] = b.y;
+    v[8 * i + 4] = c.x; v[8 * i + 5] = c.y; v[8 * i + 6] = d.x; v[8 * i + 7] = d.y;
+  }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// Zigzag row m of [D][B][2C] -> (batch b, natural position p).
+__device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep, int& b, int64_t& p) {
+  const int64_t twoC = 2 * (int64_t)ep.C;
+  const int64_t per_rank = (int64_t)ep.B * twoC;
+  const int r = (int)(m / per_rank);
+  const int64_t rem = m - (int64_t)r * per_rank;
+  b = (int)(rem / twoC);
+  const int64_t k = rem - (int64_t)b * twoC;
+  p = (k < ep.C) ? (int64_t)r * ep.C + k : (int64_t)(2 * ep.D - 1 - r) * ep.C + (k - ep.C);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmShape shape, const EpiParams ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES * A_STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < shape.num_tiles && ok; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, shape, mt, nt);
+        for (int kb = 0; kb < shape.kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+          tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, mt * BM, &full[s]);
+          tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
+        }
+      }
+      // Before leaving, make sure every copy this thread issued has landed
+      // (always true on the normal path, bounded on the abort path).
+      const uint32_t issued = it;
+      const uint32_t first = issued > (uint32_t)STAGES ? issued - STAGES : 0;
+      for (uint32_t j = first; j < issued; ++j) {
+        volatile int dummy = 0;
+        mbar_wait(&full[j % STAGES], (j / STAGES) & 1, &dummy, ep.err, (KID_GEMM_TC << 8) | 2);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      uint32_t it = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < shape.num_tiles && ok; t += gridDim.x, ++tl) {
+        const int acc = tl & 1;
+        const uint32_t aph = (tl >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 3)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < shape.kblocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&full[s], ph, abort_flag, ep.err, (KID_GEMM_TC << 8) | 4)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smA + s * A_STAGE_BYTES));
+          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smB + s * B_STAGE_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // +32 bytes along K inside the 128-byte swizzle atom = +2 in the >>4 address field.
+            umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+      // Drain: wait until every MMA issued above has completed before TMEM is freed.
+      umma_commit(drain);
+      volatile int dummy = 0;
+      mbar_wait(drain, 0, &dummy, ep.err, (KID_GEMM_TC << 8) | 5);
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
+    const int row = quad * 32 + lane;
+    uint32_t tl = 0;
+    for (int t = blockIdx.x; t < shape.num_tiles; t += gridDim.x, ++tl) {
+      int mt, nt;
+      tile_coords(t, shape, mt, nt);
+      const int acc = tl & 1;
+      const uint32_t aph = (tl >> 1) & 1;
+      // Warp-uniform decision: tcgen05.ld below needs every lane of the warp.
+      const bool got = mbar_wait(&tfull[acc], aph, abort_flag, ep.err, (KID_GEMM_TC << 8) | 6);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int64_t m = (int64_t)mt * BM + row;
+      const bool valid = m < shape.M;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float g[32], u[32];
+          tmem_ld32(tbase + c * 32, g);
+          tmem_ld32(tbase + 128 + c * 32, u);
+          if (valid) {
+            if (ep.aux) {
+              __nv_bfloat16* aux = reinterpret_cast<__nv_bfloat16*>(ep.aux) + m * ep.ldx + (int64_t)nt * BN;
+              store32_bf16(aux + c * 32, g);
+              store32_bf16(aux + 128 + c * 32, u);
+            }
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = silu_f(g[i]) * u[i];
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + (int64_t)nt * (BN / 2);
+            store32_bf16(out + c * 32, o);
+          }
+        }
+      } else {
+        int b = 0;
+        int64_t p = 0;
+        if constexpr (EPI == EPI_QKV) {
+          if (valid) zigzag_row_to_pos(m, ep, b, p);
+        }
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          if (!valid) continue;
+          const int64_t n = (int64_t)nt * BN + c * 32;
+          if constexpr (EPI == EPI_STORE) {
+            store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + n, v);
+          } else if constexpr (EPI == EPI_RESID) {
+            float r[32];
+            load32_bf16(reinterpret_cast<const __nv_bfloat16*>(ep.resid) + m * ep.ldr + n, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += r[i];
+            store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + n, v);
+          } else if constexpr (EPI == EPI_QKV) {
+            // packed column n -> (shard s, which of q/k/v, head, d)
+            const int hs = ep.h / ep.D;  // columns of one projection in one shard
+            const int s = (int)(n / (3 * hs));
+            const int within = (int)(n - (int64_t)s * 3 * hs);
+            const int which = within / hs;
+            const int cin = within - which * hs;
+            const int head = s * (ep.H / ep.D) + cin / ep.dh;
+            const int d = cin % ep.dh;
+            if (which == 0) {
+              store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.q) + m * ep.h + head * ep.dh + d, v);
+            } else {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 1 ? ep.k : ep.v);
+              store32_bf16(dst + (((int64_t)b * ep.H + head) * ep.S + p) * ep.dh + d, v);
+            }
+          } else if constexpr (EPI == EPI_DSWIGLU) {
+            // n indexes F; the saved G/U and the dGU output use the packed gate_up order.
+            const int64_t blk = n / 128, off = n % 128;
+            const int64_t gcol = blk * 256 + off, ucol = gcol + 128;
+            const __nv_bfloat16* gu = reinterpret_cast<const __nv_bfloat16*>(ep.resid) + m * ep.ldr;
+            float g[32], u[32], dg[32], du[32];
+            load32_bf16(gu + gcol, g);
+            load32_bf16(gu + ucol, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float sg = 1.0f / (1.0f + __expf(-g[i]));
+              const float sl = g[i] * sg;
+              du[i] = v[i] * sl;
+              dg[i] = v[i] * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+            }
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo;
+            store32_bf16(out + gcol, dg);
+            store32_bf16(out + ucol, du);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix with row stride
+// `ld` elements; box = 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& s, const EpiParams& ep,
+                       cudaStream_t stream) {
+  static bool configured = false;  // per-process; attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = s.num_tiles < num_sms() ? s.num_tiles : num_sms();
+  gemm_bf16_tc_kernel<EPI><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, s, ep);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K, EpiKind epi,
+                        const EpiParams& ep, cudaStream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return TSP_OK;
+  if (N % BN || K % BK || lda % 8 || ldb % 8) return TSP_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) return TSP_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  if (!make_map_bf16(&ta, A, M, K, lda, BM) || !make_map_bf16(&tb, B, N, K, ldb, BN)) return TSP_ERR_CUDA;
+  GemmShape s;
+  s.M = M;
+  s.N = N;
+  s.K = K;
+  s.num_m = (M + BM - 1) / BM;
+  s.num_n = N / BN;
+  s.num_tiles = s.num_m * s.num_n;
+  s.kblocks = K / BK;
+  cudaError_t e;
+  switch (epi) {
+    case EPI_STORE: e = launch_epi<EPI_STORE>(ta, tb, s, ep, stream); break;
+    case EPI_RESID: e = launch_epi<EPI_RESID>(ta, tb, s, ep, stream); break;
+    case EPI_QKV: e = launch_epi<EPI_QKV>(ta, tb, s, ep, stream); break;
+    case EPI_SWIGLU: e = launch_epi<EPI_SWIGLU>(ta, tb, s, ep, stream); break;
+    case EPI_DSWIGLU: e = launch_epi<EPI_DSWIGLU>(ta, tb, s, ep, stream); break;
+    default: return TSP_ERR_INVALID_ARG;
+  }
+  return e == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
+}
+
+}  // namespace tsp

@@ -1,0 +1,102 @@
+// Internal declarations shared by the libtsp translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tsp.h"
+
+struct tsp_plan {
+  int D;
+  int64_t seq;
+  int hidden;
+  int heads;
+  int head_dim;
+  int ffn;
+  tsp_dtype dtype;
+  int64_t chunk;  // seq / (2D)
+};
+
+namespace tsp {
+
+// Epilogues of the projection GEMMs (C = A * B^T, A [M][K], B [N][K]).
+enum EpiKind : int {
+  EPI_STORE = 0,    // out[m][n] = acc
+  EPI_RESID = 1,    // out[m][n] = resid[m][n] + acc
+  EPI_QKV = 2,      // scatter packed Q|K|V columns: Q to zigzag rows, K/V gathered per head
+  EPI_SWIGLU = 3,   // gate/up 128-column blocks -> out[m][f] = SiLU(g) * u; optional raw copy to aux
+  EPI_DSWIGLU = 4,  // acc = dM[m][f]; reads saved G/U (resid, packed gate_up order) -> dGU to out
+};
+
+struct EpiParams {
+  void* out = nullptr;
+  int64_t ldo = 0;
+  const void* resid = nullptr;
+  int64_t ldr = 0;
+  void* aux = nullptr;
+  int64_t ldx = 0;
+  void* q = nullptr;
+  void* k = nullptr;
+  void* v = nullptr;
+  int D = 1, B = 1, S = 0, C = 0, H = 1, dh = 1, h = 0;
+  unsigned int* err = nullptr;  // device error word
+};
+
+int num_sms();
+unsigned int* dev_error_word();  // device address of this device's error word (nullptr on failure)
+
+// bf16 tcgen05 GEMM: C[M][N] = sum_k A[m][k] B[n][k] with fp32 accumulation in
+// tensor memory; row strides lda/ldb in elements.  Needs N % 256 == 0,
+// K % 64 == 0, 16-byte aligned rows.
+tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K,
+                        EpiKind epi, const EpiParams& ep, cudaStream_t stream);
+
+// fp32 SIMT GEMM, same contract (any M, N, K; SWIGLU/DSWIGLU not supported).
+tsp_status gemm_f32_simt(const float* A, int64_t lda, const float* B, int64_t ldb, int M, int N, int K,
+                         EpiKind epi, const EpiParams& ep, cudaStream_t stream);
+
+// Elementwise / layout kernels.
+cudaError_t launch_zigzag_rows(const void* src, void* dst, int64_t row_bytes, int D, int B, int64_t S,
+                               bool to_zigzag, cudaStream_t stream);
+cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
+                             int64_t S, int H, int dh, cudaStream_t stream);
+cudaError_t launch_swiglu_f32(const float* gu, float* m, int64_t T, int F, cudaStream_t stream);
+cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols, int elem_bytes,
+                             cudaStream_t stream);
+cudaError_t launch_pack_weights(const tsp_plan* p, const void* const c[7], const tsp_weight_grads* w, bool unpack,
+                                cudaStream_t stream);
+
+// Attention.
+struct AttnParams {
+  const void* q;  // zigzag rows [T][h]
+  const void* k;  // [B][H][S][dh]
+  const void* v;
+  void* o;        // zigzag rows [T][h]
+  float* lse;     // [B][H][S] natural log, may be null
+  int D, B, H, dh;
+  int64_t S, C;
+};
+tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream);
+tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream);
+
+struct AttnBwdParams {
+  const void* q;   // zigzag [T][h]
+  const void* k;   // [B][H][S][dh]
+  const void* v;
+  const void* o;   // zigzag [T][h]
+  const void* dO;  // zigzag [T][h]
+  const float* lse;
+  float* dsum;     // [B][H][S] scratch
+  void* dq;        // zigzag [T][h]
+  void* dk;        // [B][H][S][dh]
+  void* dv;
+  int D, B, H, dh;
+  int64_t S, C;
+};
+tsp_status attn_bwd_bf16(const AttnBwdParams& p, cudaStream_t stream);
+
+// Backward helpers.
+cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
+                                 int64_t S, int H, int dh, cudaStream_t stream);
+
+}  // namespace tsp

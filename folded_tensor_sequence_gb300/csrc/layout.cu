@@ -1,0 +1,278 @@
+// Memory-bound layout kernels: zigzag token permutation, the K/V all-gather
+// into natural order, weight packing, transposes and small elementwise steps.
+//
+// Zigzag partition (ai-trends.today TSP article, "How to Fold a Book": K/V
+// are reordered with a zigzag scheme so causal attention work is balanced):
+// the sequence is cut into 2D chunks of C tokens; virtual rank r holds chunk r
+// then chunk 2D-1-r.  Zigzag row (r*B + b)*2C + k holds natural position
+// pos(r,k) = r*C + k (k < C) or (2D-1-r)*C + (k-C) (k >= C).
+//
+// All copies move 16-byte vectors, consecutive threads touching consecutive
+// vectors of one row, over a grid of (SM count x 8) CTAs striding the work.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tsp {
+
+namespace {
+
+__device__ __forceinline__ int64_t zigzag_pos(int64_t r, int64_t k, int64_t C, int D) {
+  return k < C ? r * C + k : (2 * D - 1 - r) * C + (k - C);
+}
+
+// Natural position p -> (rank, local index).
+__device__ __forceinline__ void pos_to_zigzag(int64_t p, int64_t C, int D, int64_t& r, int64_t& k) {
+  const int64_t c = p / C;
+  const int64_t off = p - c * C;
+  if (c < D) {
+    r = c;
+    k = off;
+  } else {
+    r = 2 * D - 1 - c;
+    k = C + off;
+  }
+}
+
+// One 16-byte vector per thread-iteration; rows of `vecs_per_row` vectors.
+__global__ void zigzag_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t vecs_per_row,
+                                   int D, int B, int64_t S, bool to_zigzag) {
+  const int64_t C = S / (2 * D);
+  const int64_t twoC = 2 * C;
+  const int64_t total = (int64_t)B * S * vecs_per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t zrow = i / vecs_per_row;  // zigzag row index
+    const int64_t v = i - zrow * vecs_per_row;
+    const int64_t r = zrow / (B * twoC);
+    const int64_t rem = zrow - r * (B * twoC);
+    const int64_t b = rem / twoC;
+    const int64_t k = rem - b * twoC;
+    const int64_t nrow = b * S + zigzag_pos(r, k, C, D);  // natural row
+    if (to_zigzag)
+      dst[zrow * vecs_per_row + v] = __ldg(&src[nrow * vecs_per_row + v]);
+    else
+      dst[nrow * vecs_per_row + v] = __ldg(&src[zrow * vecs_per_row + v]);
+  }
+}
+
+// Gathered [B][H][S][dh] <- zigzag [T][h]; iterates over destination vectors.
+__global__ void kv_gather_kernel(const uint4* __restrict__ kz, const uint4* __restrict__ vz, uint4* __restrict__ k,
+                                 uint4* __restrict__ v, int vec_per_head, int D, int B, int64_t S, int H) {
+  const int64_t C = S / (2 * D);
+  const int64_t twoC = 2 * C;
+  const int64_t vec_per_row = (int64_t)H * vec_per_head;
+  const int64_t total = (int64_t)B * H * S * vec_per_head;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t dv = i % vec_per_head;
+    const int64_t rest = i / vec_per_head;
+    const int64_t p = rest % S;
+    const int64_t bh = rest / S;
+    const int64_t head = bh % H;
+    const int64_t b = bh / H;
+    int64_t r, kk;
+    pos_to_zigzag(p, C, D, r, kk);
+    const int64_t zrow = (r * B + b) * twoC + kk;
+    const int64_t s_idx = zrow * vec_per_row + head * vec_per_head + dv;
+    k[i] = __ldg(&kz[s_idx]);
+    v[i] = __ldg(&vz[s_idx]);
+  }
+}
+
+// dqkv [T][3h] in packed column order <- dq zigzag [T][h], dk/dv gathered [B][H][S][dh].
+__global__ void assemble_dqkv_kernel(const uint4* __restrict__ dq, const uint4* __restrict__ dk,
+                                     const uint4* __restrict__ dv, uint4* __restrict__ out, int vec_per_head, int D,
+                                     int B, int64_t S, int H) {
+  const int64_t C = S / (2 * D);
+  const int64_t twoC = 2 * C;
+  const int hpv = H / D;                             // heads per shard
+  const int64_t vec_per_proj = (int64_t)H * vec_per_head;  // h columns
+  const int64_t vec_per_row = 3 * vec_per_proj;
+  const int64_t total = (int64_t)B * S * vec_per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t zrow = i / vec_per_row;
+    const int64_t cv = i - zrow * vec_per_row;  // packed column vector index
+    const int64_t shard_w = 3 * (int64_t)hpv * vec_per_head;
+    const int64_t s = cv / shard_w;
+    const int64_t within = cv - s * shard_w;
+    const int64_t which = within / ((int64_t)hpv * vec_per_head);
+    const int64_t cin = within - which * hpv * vec_per_head;
+    const int64_t head = s * hpv + cin / vec_per_head;
+    const int64_t d = cin % vec_per_head;
+    if (which == 0) {
+      out[i] = __ldg(&dq[zrow * vec_per_proj + head * vec_per_head + d]);
+    } else {
+      const int64_t r = zrow / (B * twoC);
+      const int64_t rem = zrow - r * (B * twoC);
+      const int64_t b = rem / twoC;
+      const int64_t kk = rem - b * twoC;
+      const int64_t p = zigzag_pos(r, kk, C, D);
+      const int64_t g = ((b * H + head) * S + p) * vec_per_head + d;
+      out[i] = __ldg(which == 1 ? &dk[g] : &dv[g]);
+    }
+  }
+}
+
+// 32x32 tiles through shared memory, element type T.
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows, int64_t cols) {
+  __shared__ T tile[32][33];
+  const int64_t tiles_c = (cols + 31) / 32;
+  const int64_t tiles_r = (rows + 31) / 32;
+  for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
+    const int64_t r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+      const int64_t r = r0 + j, c = c0 + threadIdx.x;
+      if (r < rows && c < cols) tile[j][threadIdx.x] = src[r * cols + c];
+    }
+    __syncthreads();
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+      const int64_t c = c0 + j, r = r0 + threadIdx.x;
+      if (r < rows && c < cols) dst[c * rows + r] = tile[threadIdx.x][j];
+    }
+    __syncthreads();
+  }
+}
+
+// gu [T][2F] packed gate/up (128-blocks) -> m [T][F] = SiLU(g) * u, fp32.
+__global__ void swiglu_f32_kernel(const float* __restrict__ gu, float* __restrict__ m, int64_t T, int F) {
+  const int64_t total = T * F;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / F;
+    const int f = (int)(i - t * F);
+    const int64_t gcol = (int64_t)(f / 128) * 256 + (f % 128);
+    const float g = gu[t * 2 * F + gcol];
+    const float u = gu[t * 2 * F + gcol + 128];
+    m[i] = g / (1.0f + expf(-g)) * u;
+  }
+}
+
+// Packs canonical weights into (or unpacks from) the layouts of tsp.h.
+// Each packed element (row n, column k) maps to one canonical element.
+template <typename T>
+__global__ void pack_kernel(const T* __restrict__ Wq, const T* __restrict__ Wk, const T* __restrict__ Wv,
+                            const T* __restrict__ Wo, const T* __restrict__ Wg, const T* __restrict__ Wu,
+                            const T* __restrict__ Wd, T* __restrict__ Pqkv, T* __restrict__ Po,
+                            T* __restrict__ Pgu, T* __restrict__ Pd, int h, int F, int D, bool unpack) {
+  const int64_t n_qkv = 3LL * h * h, n_o = (int64_t)h * h, n_gu = 2LL * F * h, n_d = (int64_t)h * F;
+  const int64_t total = n_qkv + n_o + n_gu + n_d;
+  const int hs = h / D;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    T* packed;
+    const T* canon;
+    int64_t pidx, cidx;
+    if (i < n_qkv) {
+      const int64_t n = i / h, k = i % h;  // packed row n, column k
+      const int64_t s = n / (3 * hs), within = n % (3 * hs);
+      const int64_t which = within / hs, col = s * hs + within % hs;
+      canon = which == 0 ? Wq : (which == 1 ? Wk : Wv);
+      cidx = k * h + col;
+      packed = Pqkv;
+      pidx = i;
+    } else if (i < n_qkv + n_o) {
+      const int64_t j = i - n_qkv, n = j / h, k = j % h;
+      canon = Wo;
+      cidx = k * h + n;
+      packed = Po;
+      pidx = j;
+    } else if (i < n_qkv + n_o + n_gu) {
+      const int64_t j = i - n_qkv - n_o, n = j / h, k = j % h;
+      const int64_t blk = n / 256, off = n % 256;
+      const int64_t f = blk * 128 + (off % 128);
+      canon = off < 128 ? Wg : Wu;
+      cidx = k * F + f;
+      packed = Pgu;
+      pidx = j;
+    } else {
+      const int64_t j = i - n_qkv - n_o - n_gu, n = j / F, k = j % F;
+      canon = Wd;
+      cidx = k * h + n;
+      packed = Pd;
+      pidx = j;
+    }
+    if (unpack)
+      const_cast<T*>(canon)[cidx] = packed[pidx];
+    else
+      packed[pidx] = canon[cidx];
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  return blocks < 1 ? 1 : (int)blocks;
+}
+
+}  // namespace
+
+cudaError_t launch_zigzag_rows(const void* src, void* dst, int64_t row_bytes, int D, int B, int64_t S,
+                               bool to_zigzag, cudaStream_t stream) {
+  const int64_t vpr = row_bytes / 16;
+  const int64_t total = (int64_t)B * S * vpr;
+  if (total == 0) return cudaSuccess;
+  zigzag_rows_kernel<<<grid_for(total, 256), 256, 0, stream>>>(static_cast<const uint4*>(src),
+                                                               static_cast<uint4*>(dst), vpr, D, B, S, to_zigzag);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
+                             int64_t S, int H, int dh, cudaStream_t stream) {
+  const int vph = dh * elem_bytes / 16;
+  const int64_t total = (int64_t)B * H * S * vph;
+  if (total == 0) return cudaSuccess;
+  kv_gather_kernel<<<grid_for(total, 256), 256, 0, stream>>>(static_cast<const uint4*>(kz),
+                                                             static_cast<const uint4*>(vz), static_cast<uint4*>(k),
+                                                             static_cast<uint4*>(v), vph, D, B, S, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
+                                 int64_t S, int H, int dh, cudaStream_t stream) {
+  const int vph = dh * 2 / 16;
+  const int64_t total = (int64_t)B * S * 3 * H * vph;
+  if (total == 0) return cudaSuccess;
+  assemble_dqkv_kernel<<<grid_for(total, 256), 256, 0, stream>>>(
+      static_cast<const uint4*>(dq), static_cast<const uint4*>(dk), static_cast<const uint4*>(dv),
+      static_cast<uint4*>(dqkv), vph, D, B, S, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols, int elem_bytes,
+                             cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+  const int grid = (int)(tiles < (int64_t)num_sms() * 16 ? tiles : (int64_t)num_sms() * 16);
+  dim3 block(32, 8);
+  if (elem_bytes == 2)
+    transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<const uint16_t*>(src),
+                                                           static_cast<uint16_t*>(dst), rows, cols);
+  else
+    transpose_kernel<uint32_t><<<grid, block, 0, stream>>>(static_cast<const uint32_t*>(src),
+                                                           static_cast<uint32_t*>(dst), rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_f32(const float* gu, float* m, int64_t T, int F, cudaStream_t stream) {
+  const int64_t total = T * F;
+  if (total == 0) return cudaSuccess;
+  swiglu_f32_kernel<<<grid_for(total, 256), 256, 0, stream>>>(gu, m, T, F);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights(const tsp_plan* p, const void* const c[7], const tsp_weight_grads* w, bool unpack,
+                                cudaStream_t stream) {
+  const int h = p->hidden, F = p->ffn, D = p->D;
+  const int64_t total = 4LL * h * h + 3LL * h * F;
+  if (p->dtype == TSP_BF16)
+    pack_kernel<uint16_t><<<grid_for(total, 256), 256, 0, stream>>>(
+        (const uint16_t*)c[0], (const uint16_t*)c[1], (const uint16_t*)c[2], (const uint16_t*)c[3],
+        (const uint16_t*)c[4], (const uint16_t*)c[5], (const uint16_t*)c[6], (uint16_t*)w->qkv, (uint16_t*)w->o,
+        (uint16_t*)w->gate_up, (uint16_t*)w->down, h, F, D, unpack);
+  else
+    pack_kernel<uint32_t><<<grid_for(total, 256), 256, 0, stream>>>(
+        (const uint32_t*)c[0], (const uint32_t*)c[1], (const uint32_t*)c[2], (const uint32_t*)c[3],
+        (const uint32_t*)c[4], (const uint32_t*)c[5], (const uint32_t*)c[6], (uint32_t*)w->qkv, (uint32_t*)w->o,
+        (uint32_t*)w->gate_up, (uint32_t*)w->down, h, F, D, unpack);
+  return cudaGetLastError();
+}
+
+}  // namespace tsp

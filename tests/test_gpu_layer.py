@@ -1,0 +1,131 @@
+"""Layer-level parity of the CUDA path against the fp64 oracle (small and mid sizes).
+
+Tolerances: fp32 plans, normwise max relative error <= 1e-4; bf16 plans,
+relative Frobenius error <= 2e-2 per output tensor.  Outputs are checked both
+with and without the residual (A, MLP, Y) so the residual cannot hide errors.
+"""
+import numpy as np
+import pytest
+
+from folded_tensor_sequence_gb300 import synth
+from folded_tensor_sequence_gb300.configs import MID_BF16, TINY_F32, LayerConfig
+from oracle import tsp_oracle as O
+
+from helpers import check, rel_frob, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tsp():
+    import __graft_entry__ as g
+
+    g.build()
+    from folded_tensor_sequence_gb300 import tsp as T
+
+    return T
+
+
+def setup(tsp, cfg, inp=None, seed=0):
+    import torch
+
+    inp = inp if inp is not None else synth.layer_inputs(cfg, seed=seed)
+    plan = tsp.tsp_plan_create(cfg.D, cfg.seq, cfg.hidden, cfg.heads, cfg.head_dim, cfg.ffn, cfg.dtype)
+    canon = {k: to_dev(inp[k], cfg.dtype) for k in tsp.CANONICAL}
+    packed = tsp.empty_packed(plan)
+    tsp.tsp_pack_weights(plan, canon, packed)
+    x = to_dev(inp["x"], cfg.dtype)
+    return plan, packed, x, inp
+
+
+def run_pieces(tsp, cfg, plan, packed, x):
+    """Runs attention_fwd, gated_mlp_fwd and layer_fwd; returns natural-order A, MLP(H_ref-free), Y, lse."""
+    import torch
+
+    B = cfg.batch
+    xz = torch.empty_like(x)
+    tsp.tsp_zigzag_permute(plan, B, x, xz)
+    a = torch.empty_like(x)
+    lse = torch.empty(B, cfg.heads, cfg.seq, dtype=torch.float32, device="cuda")
+    tsp.tsp_attention_fwd(plan, B, xz, packed, a, lse, tsp.workspace(plan, B, tsp.TSP_OP_ATTENTION_FWD))
+    y = torch.empty_like(x)
+    tsp.tsp_layer_fwd(plan, B, x, packed, y, None, tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD))
+    tsp.tsp_sync_check()
+    a_nat = O.zigzag_unpermute(to_np(a).reshape(cfg.D, B, -1, cfg.hidden), cfg.D)
+    return a_nat, to_np(y), to_np(lse)
+
+
+def mlp_piece(tsp, cfg, plan, packed, H_np):
+    """gated_mlp_fwd on the given natural-order H (values exact in the plan dtype)."""
+    import torch
+
+    B = cfg.batch
+    Hd = to_dev(H_np, cfg.dtype)
+    hz = torch.empty_like(Hd)
+    tsp.tsp_zigzag_permute(plan, B, Hd, hz)
+    m = torch.empty_like(Hd)
+    tsp.tsp_gated_mlp_fwd(plan, B, hz, packed, m, tsp.workspace(plan, B, tsp.TSP_OP_GATED_MLP_FWD))
+    tsp.tsp_sync_check()
+    return O.zigzag_unpermute(to_np(m).reshape(cfg.D, B, -1, cfg.hidden), cfg.D)
+
+
+def round_to(a, dtype):
+    return synth.round_bf16(a) if dtype == "bf16" else a.astype(np.float32).astype(np.float64)
+
+
+def full_check(tsp, cfg, seed=0):
+    plan, packed, x, inp = setup(tsp, cfg, seed=seed)
+    w = {k: inp[k] for k in tsp.CANONICAL}
+    ref = O.layer_fwd(inp["x"], w, cfg.heads)
+    a, y, lse = run_pieces(tsp, cfg, plan, packed, x)
+    errs = {"A": check(a, ref["A"], cfg.dtype, f"{cfg.name} A"), "Y": check(y, ref["Y"], cfg.dtype, f"{cfg.name} Y")}
+    # lse is fp32 in both paths; bf16 inputs to QK^T are exact, so it must be close
+    assert np.max(np.abs(lse - ref["lse"])) < (2e-2 if cfg.dtype == "bf16" else 1e-4)
+    Hr = round_to(ref["H"], cfg.dtype)
+    mref = O.gated_mlp(Hr, w)
+    errs["MLP"] = check(mlp_piece(tsp, cfg, plan, packed, Hr), mref, cfg.dtype, f"{cfg.name} MLP")
+    return errs, y
+
+
+
+def test_tiny_f32_matches_oracle(tsp):
+    full_check(tsp, TINY_F32)
+
+
+@pytest.mark.parametrize("D", [1, 4])
+def test_tiny_f32_other_D(tsp, D):
+    full_check(tsp, TINY_F32.with_(D=D, name=f"tiny_f32_D{D}"))
+
+
+SMALL_BF16 = [
+    # ragged query tiles (C = 80) and a ragged 64-row GEMM tail (T = 320)
+    LayerConfig("bf16_D2_s320", D=2, batch=1, seq=320, hidden=256, heads=2, head_dim=128, ffn=512, dtype="bf16"),
+    # several tiles in every GEMM dimension, two batches
+    LayerConfig("bf16_D4_b2_s1024", D=4, batch=2, seq=1024, hidden=512, heads=4, head_dim=128, ffn=768, dtype="bf16"),
+    # D = 8 with one head per shard
+    LayerConfig("bf16_D8_s2048", D=8, batch=1, seq=2048, hidden=1024, heads=8, head_dim=128, ffn=1024, dtype="bf16"),
+    # odd D, chunk not a multiple of the 128-row query tile
+    LayerConfig("bf16_D3_s1152", D=3, batch=1, seq=1152, hidden=768, heads=6, head_dim=128, ffn=1536, dtype="bf16"),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL_BF16, ids=lambda c: c.name)
+def test_small_bf16_matches_oracle(tsp, cfg):
+    full_check(tsp, cfg)
+
+
+def test_mid_bf16_matches_oracle(tsp):
+    full_check(tsp, MID_BF16)
+
+
+def test_outputs_agree_across_D(tsp):
+    base = LayerConfig("xD", D=1, batch=1, seq=2048, hidden=1024, heads=8, head_dim=128, ffn=1024, dtype="bf16")
+    inp = synth.layer_inputs(base, seed=3)
+    ys = {}
+    for D in (1, 2, 4, 8):
+        cfg = base.with_(D=D)
+        plan, packed, x, _ = setup(tsp, cfg, inp=inp)
+        _, y, _ = run_pieces(tsp, cfg, plan, packed, x)
+        ys[D] = y
+    for D in (2, 4, 8):
+        assert rel_frob(ys[D], ys[1]) <= 2e-2
