@@ -1,0 +1,384 @@
+#!/usr/bin/env python3
+"""Throughput of one TSP transformer layer forward (bf16) on GB300.
+
+One step = one tsp_layer_fwd call on the whole workload: zigzag permute, the
+QKV projection over all weight shards with the fused K/V gather, the
+zigzag-balanced causal flash attention, the output projection accumulated over
+shards (+ residual), the gate/up projection with the fused SiLU*up epilogue,
+the down projection accumulated over the MLP ring's shards (+ residual) and
+the unpermute.  Default workload: D = 8 virtual ranks, batch 2, seq 16384,
+hidden 4096, 32 heads x 128, SwiGLU ffn 14336 (the 7B dense decoder shape).
+
+Prints one JSON line.  `value` is layer-forward TFLOP/s with inputs resident
+in device memory; `e2e` repeats the measurement through the public API with
+the input copied from pinned host memory and the output copied back inside
+the timed region.  `--impl reference` times the fp64 CPU oracle instead (on a
+bounded prefix of the same workload, single-threaded).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from folded_tensor_sequence_gb300.configs import BY_NAME, LAYER_7B_S16K  # noqa: E402
+
+METRIC = "TSP layer fwd TFLOP/s & tokens/s (bf16) at 1 GB300; % of dense bf16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# each step's kernel, scaled to the default workload, and the sha256 of the
+# kernel source the counters were taken on; a mismatch reports null.
+NCU_TRAFFIC: dict[str, tuple[float, str]] = {}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def step_work(cfg):
+    """Algorithmic work per launch of each step: (flops, bytes)."""
+    B, S, h, F, H, dh = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
+    T = B * S
+    e = 2 if cfg.dtype == "bf16" else 4
+    return {
+        "zigzag permute": (0, 2 * T * h * e),
+        "QKV projection": (2 * T * h * 3 * h, (T * h + 3 * h * h + 3 * T * h) * e),
+        "attention": (4 * B * H * dh * S * (S + 1) // 2, 4 * T * h * e),
+        "output projection": (2 * T * h * h, (3 * T * h + h * h) * e),
+        "gate/up projection": (2 * T * h * 2 * F, (T * h + 2 * F * h + T * F) * e),
+        "down projection": (2 * T * F * h, (T * F + F * h + 2 * T * h) * e),
+        "zigzag unpermute": (0, 2 * T * h * e),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        self.out = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.gpu], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.seek(0)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.out.read().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def sample_flops(cfg, prefix: int) -> int:
+    h, F, H, dh = cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
+    return prefix * (8 * h * h + 6 * h * F) + 4 * H * dh * prefix * (prefix + 1) // 2
+
+
+def run_oracle_sample(cfg, prefix: int, repeats: int, timeout: float = 1800.0):
+    """Times the fp64 oracle, single-threaded, `repeats` times on the first `prefix` positions of batch 0.
+
+    Causality makes the layer's outputs at those positions depend only on that
+    prefix, so the sample is an exact slice of the workload.  Runs in a fresh
+    interpreter with BLAS pinned to one thread; inputs are drawn once, outside
+    the timed calls.  Returns (list of seconds, error text).
+    """
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np, torch
+from folded_tensor_sequence_gb300 import synth
+from folded_tensor_sequence_gb300.configs import BY_NAME
+from oracle import tsp_oracle as O
+cfg = BY_NAME[{cfg.name!r}]
+h, F, P = cfg.hidden, cfg.ffn, {prefix}
+shapes = {{"Wq": (h, h), "Wk": (h, h), "Wv": (h, h), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}}
+w = {{k: synth.tensor_torch(k, s, (F if k == "Wd" else h) ** -0.5, cfg.dtype, 0, "cpu").double().numpy()
+      for k, s in shapes.items()}}
+x = synth.tensor_torch("x", (1, P, h), 1.0, cfg.dtype, 0, "cpu").double().numpy()
+secs = []
+for _ in range({repeats}):
+    t0 = time.perf_counter()
+    out = O.layer_fwd(x, w, cfg.heads)
+    secs.append(time.perf_counter() - t0)
+    assert np.isfinite(out["Y"]).all()
+print(json.dumps({{"seconds": secs}}))
+"""
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=timeout)
+    except subprocess.TimeoutExpired:
+        return None, "timed out"
+    if r.returncode != 0:
+        return None, r.stderr[-2000:]
+    return json.loads(r.stdout.strip().splitlines()[-1])["seconds"], None
+
+
+def cpu_baseline(cfg, prefix: int):
+    secs, err = run_oracle_sample(cfg, prefix, 1)
+    if secs is None:
+        return None, err
+    fl = sample_flops(cfg, prefix)
+    return {"value": round(fl / secs[0] / 1e12, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, 1 thread, positions 0..{prefix - 1} of batch 0 "
+                      f"({fl / 1e9:.1f} GFLOP algorithmic, {secs[0]:.1f} s)",
+            "tokens_per_s": round(prefix / secs[0], 2)}, None
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    prefix = args.ref_prefix
+    secs, err = run_oracle_sample(cfg, prefix, args.warmup + args.steps)
+    if secs is None:
+        print(json.dumps({"impl": "reference", "unavailable": f"oracle run failed: {err.strip()[-200:]}"}))
+        return 0
+    timed = secs[args.warmup:]
+    fl = sample_flops(cfg, prefix)
+    total = sum(timed)
+    value = fl * len(timed) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(timed),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "D": cfg.D, "batch": cfg.batch, "seq": cfg.seq, "hidden": cfg.hidden,
+                   "heads": cfg.heads, "head_dim": cfg.head_dim, "ffn": cfg.ffn,
+                   "sample": f"each step: positions 0..{prefix - 1} of batch 0 (causal prefix, exact slice)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"fp64 numpy oracle, 1 thread, causal prefix of {prefix} tokens per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tsp", choices=["tsp", "reference"])
+    ap.add_argument("--config", default=LAYER_7B_S16K.name, choices=sorted(BY_NAME))
+    ap.add_argument("--cpu-prefix", type=int, default=512, help="tokens of the oracle's CPU baseline sample")
+    ap.add_argument("--ref-prefix", type=int, default=64, help="tokens per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = BY_NAME[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    # The CPU baseline runs first, in its own interpreter, before this process
+    # does any heavy GPU work (rank 0 at N = 1 only).
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu, err = cpu_baseline(cfg, args.cpu_prefix)
+        if cpu is None:
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {err[-300:]}"}
+
+    import __graft_entry__ as g
+
+    g.build()
+    from folded_tensor_sequence_gb300 import synth, tsp
+
+    B, S, h, F = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn
+    plan = tsp.tsp_plan_create(cfg.D, S, h, cfg.heads, cfg.head_dim, F, cfg.dtype)
+    shapes = {"Wq": (h, h), "Wk": (h, h), "Wv": (h, h), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}
+    canon = {k: synth.tensor_torch(k, s, (F if k == "Wd" else h) ** -0.5, cfg.dtype, 0, dev) for k, s in shapes.items()}
+    packed = tsp.empty_packed(plan, dev)
+    tsp.tsp_pack_weights(plan, canon, packed)
+    del canon
+    x = synth.tensor_torch("x", (B, S, h), 1.0, cfg.dtype, 0, dev)
+    y = torch.empty_like(x)
+    work = tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        tsp.tsp_layer_fwd(plan, B, x, packed, y, None, work, stream)
+
+    for _ in range(args.warmup):
+        step()
+    tsp.tsp_sync_check(stream)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- device-resident timing ------------------------------------------
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = [t.strip() for t in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if t.strip()]
+    gpu_id = vis[dev.index] if dev.index < len(vis) else str(dev.index)
+    with ClockSampler(gpu_id) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    ms = ev0.elapsed_time(ev1)
+    tsp.tsp_sync_check(stream)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+    flops = cfg.fwd_flops()
+    ms_step = ms / args.steps
+    value = ws * flops * args.steps / (ms / 1e3) / 1e12
+    tokens_s = ws * B * S * args.steps / (ms / 1e3)
+
+    # ---- per-kernel timing (same stream, separate pass) ---------------------
+    tsp.tsp_profile_enable(True)
+    for _ in range(args.steps):
+        step()
+    rows = tsp.tsp_profile_report()
+    tsp.tsp_profile_enable(False)
+    wk = step_work(cfg)
+    kernels = {}
+    for name, tot, cnt in rows:
+        fl, by = wk.get(name, (0, 0))
+        avg = tot / cnt
+        kernels[name] = {"ms": round(avg, 4), "tflops": round(fl / avg / 1e9, 1) if fl else None,
+                         "gbs": round(by / avg / 1e6, 1)}
+    dom = max(rows, key=lambda r: r[1])
+    peaks, peak_src = load_peaks()
+    dname, dtot, dcnt = dom
+    dfl, dby = wk.get(dname, (0, 0))
+    davg_s = dtot / dcnt / 1e3
+    traffic = NCU_TRAFFIC.get(dname, (None, None))[0]
+    if dfl:
+        peak = peaks["bf16_tflops_sustained"]
+        ach = dfl / davg_s / 1e12
+        roof = {"bound": "tensor", "kernel": dname, "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
+                "algorithmic": f"{dfl / 1e12:.3f} TFLOP per launch"}
+    else:
+        peak = peaks["hbm_gbs"]
+        ach = dby / davg_s / 1e9
+        roof = {"bound": "hbm", "kernel": dname, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
+
+    # ---- end to end through the API with host buffers -----------------------
+    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_host.copy_(x)
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    ems = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([ems], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ems = float(t.item())
+    tsp.tsp_sync_check(stream)
+    e2e = {"value": round(ws * flops * args.steps / (ems / 1e3) / 1e12, 2), "unit": UNIT,
+           "h2d_bytes_per_step": x.numel() * x.element_size(), "d2h_bytes_per_step": y.numel() * y.element_size(),
+           "tokens_per_s": round(ws * B * S * args.steps / (ems / 1e3), 1)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (splitmix64 + Box-Muller, seed 0)",
+            "tokens_per_s": round(tokens_s, 1),
+            "pct_of_peak": {"burst": round(value / ws / peaks["bf16_tflops"], 4),
+                            "sustained": round(value / ws / peaks["bf16_tflops_sustained"], 4),
+                            "source": peak_src},
+            "config": {"workload": cfg.name, "D": cfg.D, "batch": B, "seq": S, "hidden": h, "heads": cfg.heads,
+                       "head_dim": cfg.head_dim, "ffn": F, "parallelism": f"replicas x{ws}" if ws > 1 else "single",
+                       "l2": "inputs larger than L2 (x %d MB, packed weights %d MB)" % (
+                           x.numel() * x.element_size() >> 20,
+                           sum(t.numel() * t.element_size() for t in (packed.qkv, packed.o, packed.gate_up,
+                                                                        packed.down)) >> 20)},
+            "roofline": roof,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": sum(1 for _ in wk) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

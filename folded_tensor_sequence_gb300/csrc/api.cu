@@ -21,7 +21,9 @@
 #include <string.h>
 
 #include <initializer_list>
+#include <mutex>
 #include <new>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -174,6 +176,56 @@ tsp_status check_bf16_shapes(const tsp_plan* p) {
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// ---- optional per-step timing (tsp_profile_*) --------------------------------
+// When enabled, each launched step is bracketed by two CUDA events on its
+// stream; tsp_profile_report() sums the elapsed times per step name.
+struct ProfState {
+  std::mutex mu;
+  bool enabled = false;
+  struct Rec {
+    const char* name;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t get() {
+    cudaEvent_t e = nullptr;
+    if (!pool.empty()) {
+      e = pool.back();
+      pool.pop_back();
+    } else if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+    }
+    return e;
+  }
+};
+ProfState& prof() {
+  static ProfState* s = new ProfState;  // never destroyed: events may outlive static teardown order
+  return *s;
+}
+
+struct Prof {
+  const char* name;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  Prof(const char* n, cudaStream_t s) : name(n), st(s) {
+    ProfState& P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    if (!P.enabled) return;
+    a = P.get();
+    if (a) cudaEventRecord(a, st);
+  }
+  ~Prof() {
+    if (!a) return;
+    ProfState& P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    cudaEvent_t b = P.get();
+    if (!b) return;
+    cudaEventRecord(b, st);
+    P.recs.push_back({name, a, b});
+  }
+};
+
 // ---- the layer pieces ------------------------------------------------------
 
 EpiParams base_epi(const tsp_plan* p, int batch) {
@@ -191,6 +243,7 @@ EpiParams base_epi(const tsp_plan* p, int batch) {
 
 tsp_status run_gemm(const tsp_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K,
                     EpiKind epi, const EpiParams& ep, cudaStream_t st, const char* what) {
+  Prof pr(what, st);
   tsp_status s = p->dtype == TSP_BF16
                      ? gemm_bf16_tc(A, lda, B, ldb, M, N, K, epi, ep, st)
                      : gemm_f32_simt(static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb, M, N, K,
@@ -221,7 +274,10 @@ tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const ts
   ap.dh = p->head_dim;
   ap.S = p->seq;
   ap.C = p->chunk;
-  s = p->dtype == TSP_BF16 ? attn_fwd_bf16(ap, st) : attn_fwd_f32(ap, st);
+  {
+    Prof pr("attention", st);
+    s = p->dtype == TSP_BF16 ? attn_fwd_bf16(ap, st) : attn_fwd_f32(ap, st);
+  }
   if (s != TSP_OK) return fail(s, "attention kernel failed: %s", tsp_status_string(s));
   EpiParams eo = base_epi(p, batch);
   eo.out = a_out;
@@ -248,6 +304,7 @@ tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weig
     eg.out = gu;
     eg.ldo = 2 * F;
     s = run_gemm(p, hz, h, w->gate_up, h, T, 2 * F, h, EPI_STORE, eg, st, "gate/up projection");
+    Prof pr("swiglu", st);
     if (s == TSP_OK)
       s = cuda_status(launch_swiglu_f32(reinterpret_cast<const float*>(gu), reinterpret_cast<float*>(mz), T, F, st),
                       "swiglu");
@@ -473,14 +530,18 @@ tsp_status tsp_layer_fwd(const tsp_plan* p, int batch, const void* x, const tsp_
   char* act = saved ? static_cast<char*>(saved) : wsb;  // where the saved activations go
   char* xz = act + L.xz;
   char* yz = wsb + L.yz;
-  if ((s = cuda_status(launch_zigzag_rows(x, xz, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, true, st),
-                       "zigzag permute")) != TSP_OK)
-    return s;
+  {
+    Prof pr("zigzag permute", st);
+    s = cuda_status(launch_zigzag_rows(x, xz, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, true, st),
+                    "zigzag permute");
+  }
+  if (s != TSP_OK) return s;
   s = attention_impl(p, batch, xz, w, act + L.hz, xz, saved ? reinterpret_cast<float*>(act + L.lse) : nullptr,
                      act + L.qz, act + L.k, act + L.v, act + L.oz, st);
   if (s != TSP_OK) return s;
   s = mlp_impl(p, batch, act + L.hz, w, yz, act + L.hz, act + L.mz, act + L.gu, saved != nullptr, st);
   if (s != TSP_OK) return s;
+  Prof pr("zigzag unpermute", st);
   return cuda_status(launch_zigzag_rows(yz, y, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, false, st),
                      "zigzag unpermute");
 }
@@ -510,6 +571,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   const int T = (int)T64, h = p->hidden, F = p->ffn;
   const int64_t eb = (int64_t)esize(p);
   auto tr = [&](const void* src, size_t dst_off, int64_t rows, int64_t cols, const char* what) {
+    Prof pr(what, st);
     return cuda_status(launch_transpose(src, wb + dst_off, rows, cols, (int)eb, st), what);
   };
 #define TSP_TRY(expr)              \
@@ -517,7 +579,10 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     if ((s = (expr)) != TSP_OK) return s; \
   } while (0)
   // MLP backward
-  TSP_TRY(cuda_status(launch_zigzag_rows(dy, wb + L.dyz, h * eb, p->D, batch, p->seq, true, st), "permute dy"));
+  {
+    Prof pr("permute dy", st);
+    TSP_TRY(cuda_status(launch_zigzag_rows(dy, wb + L.dyz, h * eb, p->D, batch, p->seq, true, st), "permute dy"));
+  }
   TSP_TRY(tr(w->down, L.wd_c, h, F, "transpose W_down"));
   {
     EpiParams e = base_epi(p, batch);
@@ -587,9 +652,13 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     ab.dh = p->head_dim;
     ab.S = p->seq;
     ab.C = p->chunk;
-    s = attn_bwd_bf16(ab, st);
+    {
+      Prof pr("attention bwd", st);
+      s = attn_bwd_bf16(ab, st);
+    }
     if (s != TSP_OK) return fail(s, "attention backward failed: %s", tsp_status_string(s));
   }
+  Prof pr_asm("assemble dQKV", st);
   TSP_TRY(cuda_status(launch_assemble_dqkv(wb + L.dq, wb + L.dk, wb + L.dv, wb + L.dqkv, p->D, batch, p->seq,
                                            p->heads, p->head_dim, st),
                       "assemble dQKV"));
@@ -610,8 +679,45 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     e.ldo = h;
     TSP_TRY(run_gemm(p, wb + L.dqkvT, T, wb + L.xzT, T, 3 * h, h, T, EPI_STORE, e, st, "dW_QKV"));
   }
+  Prof pr_dx("unpermute dx", st);
   return cuda_status(launch_zigzag_rows(wb + L.dxz, dx, h * eb, p->D, batch, p->seq, false, st), "unpermute dx");
 #undef TSP_TRY
+}
+
+void tsp_profile_enable(int on) {
+  ProfState& P = prof();
+  std::lock_guard<std::mutex> g(P.mu);
+  P.enabled = on != 0;
+}
+
+int tsp_profile_report(const char** names, double* total_ms, int* counts, int max_entries) {
+  ProfState& P = prof();
+  std::lock_guard<std::mutex> g(P.mu);
+  std::vector<const char*> nm;
+  std::vector<double> ms;
+  std::vector<int> cnt;
+  for (auto& r : P.recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess) cudaEventElapsedTime(&t, r.a, r.b);
+    size_t i = 0;
+    while (i < nm.size() && strcmp(nm[i], r.name) != 0) ++i;
+    if (i == nm.size()) {
+      nm.push_back(r.name);
+      ms.push_back(0.0);
+      cnt.push_back(0);
+    }
+    ms[i] += t;
+    cnt[i] += 1;
+    P.pool.push_back(r.a);
+    P.pool.push_back(r.b);
+  }
+  P.recs.clear();
+  for (size_t i = 0; i < nm.size() && (int)i < max_entries; ++i) {
+    if (names) names[i] = nm[i];
+    if (total_ms) total_ms[i] = ms[i];
+    if (counts) counts[i] = cnt[i];
+  }
+  return (int)nm.size();
 }
 
 tsp_status tsp_sync_check(void* stream) {

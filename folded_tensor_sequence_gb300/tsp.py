@@ -24,7 +24,7 @@ EXPORTS = [
     "tsp_plan_create", "tsp_plan_destroy", "tsp_workspace_bytes", "tsp_saved_bytes", "tsp_status_string",
     "tsp_last_error_message", "tsp_pack_weights", "tsp_unpack_weights", "tsp_zigzag_permute",
     "tsp_zigzag_unpermute", "tsp_kv_gather", "tsp_attention_fwd", "tsp_gated_mlp_fwd", "tsp_layer_fwd",
-    "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next",
+    "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next", "tsp_profile_enable", "tsp_profile_report",
 ]
 
 
@@ -79,6 +79,11 @@ def lib() -> ctypes.CDLL:
         L.tsp_sync_check.argtypes = [vp]
         L.tsp_debug_fail_next.argtypes = [i32, i32]
         L.tsp_debug_fail_next.restype = None
+        L.tsp_profile_enable.argtypes = [i32]
+        L.tsp_profile_enable.restype = None
+        L.tsp_profile_report.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_int), i32]
+        L.tsp_profile_report.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -157,6 +162,19 @@ def tsp_sync_check(stream=None) -> None:
 
 def tsp_debug_fail_next(status: int, count: int = 1) -> None:
     lib().tsp_debug_fail_next(status, count)
+
+
+def tsp_profile_enable(on: bool) -> None:
+    lib().tsp_profile_enable(1 if on else 0)
+
+
+def tsp_profile_report(max_entries: int = 64):
+    """[(step name, total ms, launches)] since the last report (waits for the GPU)."""
+    names = (ctypes.c_char_p * max_entries)()
+    ms = (ctypes.c_double * max_entries)()
+    cnt = (ctypes.c_int * max_entries)()
+    n = lib().tsp_profile_report(names, ms, cnt, max_entries)
+    return [(names[i].decode(), ms[i], cnt[i]) for i in range(min(n, max_entries))]
 
 
 # ---- weights -------------------------------------------------------------------

@@ -184,6 +184,18 @@ tsp_status tsp_sync_check(void* stream);
  * this thread return `status` before enqueuing anything (count 0 disarms). */
 void tsp_debug_fail_next(tsp_status status, int count);
 
+/* ---- measurement ----------------------------------------------------------- */
+
+/* Per-step timing for measurement (off by default).  While enabled, every
+ * kernel step a tsp_* call enqueues is bracketed by two CUDA events on the
+ * call's stream (a small gap between kernels).  Thread-safe. */
+void tsp_profile_enable(int on);
+/* Waits for the recorded events, then writes up to max_entries rows of
+ * (step name, total milliseconds, launch count) aggregated by name in
+ * first-seen order; names point to static strings of the library.  Returns
+ * the number of distinct names and clears the records. */
+int tsp_profile_report(const char** names, double* total_ms, int* counts, int max_entries);
+
 #ifdef __cplusplus
 }
 #endif
