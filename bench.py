@@ -36,10 +36,26 @@ METRIC = "TSP layer fwd TFLOP/s & tokens/s (bf16) at 1 GB300; % of dense bf16 te
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
-# each step's kernel, scaled to the default workload, and the sha256 of the
-# kernel source the counters were taken on; a mismatch reports null.
-NCU_TRAFFIC: dict[str, tuple[float, str]] = {}
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch
+# of a step's kernel on the default workload, with the kernel source file and
+# the first 16 hex digits of its sha256 when the counters were taken; if the
+# source has changed since, the traffic is reported as null.
+#   attention: 201.5 MB + 48.8 MB captured at seq 8192 (batch 1); K/V of a head
+#   are re-read from L2, so DRAM bytes scale with tokens: x4 for batch 2 x 16384.
+NCU_TRAFFIC = {
+    "attention": (4 * (201.52e6 + 48.84e6), "folded_tensor_sequence_gb300/csrc/attn_fwd.cu", "014e0d2509343901"),
+}
+
+
+def ncu_traffic(step: str):
+    ent = NCU_TRAFFIC.get(step)
+    if not ent:
+        return None
+    import hashlib
+
+    with open(os.path.join(ROOT, ent[1]), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return ent[0] if sha == ent[2] else None
 
 
 def load_peaks():
@@ -315,7 +331,7 @@ def main():
     dname, dtot, dcnt = dom
     dfl, dby = wk.get(dname, (0, 0))
     davg_s = dtot / dcnt / 1e3
-    traffic = NCU_TRAFFIC.get(dname, (None, None))[0]
+    traffic = ncu_traffic(dname)
     if dfl:
         peak = peaks["bf16_tflops_sustained"]
         ach = dfl / davg_s / 1e12
