@@ -320,6 +320,8 @@ tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weig
 
 }  // namespace
 
+tsp_status report_error(tsp_status s, const char* msg) { return fail(s, "%s", msg); }
+
 unsigned int* dev_error_word() {
   static unsigned int* ptrs[64] = {};
   int dev = 0;

@@ -43,6 +43,8 @@ struct EpiParams {
 };
 
 int num_sms();
+// Records `msg` as this thread's tsp_last_error_message() and returns `s`.
+tsp_status report_error(tsp_status s, const char* msg);
 unsigned int* dev_error_word();  // device address of this device's error word (nullptr on failure)
 
 // bf16 tcgen05 GEMM: C[M][N] = sum_k A[m][k] B[n][k] with fp32 accumulation in

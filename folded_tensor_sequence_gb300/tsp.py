@@ -25,6 +25,7 @@ EXPORTS = [
     "tsp_last_error_message", "tsp_pack_weights", "tsp_unpack_weights", "tsp_zigzag_permute",
     "tsp_zigzag_unpermute", "tsp_kv_gather", "tsp_attention_fwd", "tsp_gated_mlp_fwd", "tsp_layer_fwd",
     "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next", "tsp_profile_enable", "tsp_profile_report",
+    "tsp_attention_fwd_static",
 ]
 
 
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.tsp_sync_check.argtypes = [vp]
         L.tsp_debug_fail_next.argtypes = [i32, i32]
         L.tsp_debug_fail_next.restype = None
+        L.tsp_attention_fwd_static.argtypes = [vp, i32, vp, ctypes.POINTER(_Weights), vp, vp, vp]
         L.tsp_profile_enable.argtypes = [i32]
         L.tsp_profile_enable.restype = None
         L.tsp_profile_report.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
@@ -244,6 +246,13 @@ def tsp_attention_fwd(plan: Plan, batch: int, xz, weights: PackedWeights, a_out,
     wp, wn = _ws_args(workspace)
     _check(lib().tsp_attention_fwd(plan.handle, batch, _ptr(xz), ctypes.byref(w), _ptr(a_out), _ptr(lse), wp, wn,
                                    _stream(stream)), "tsp_attention_fwd")
+
+
+def tsp_attention_fwd_static(plan: Plan, batch: int, xz, weights: PackedWeights, a_out, lse, stream=None):
+    """tsp_attention_fwd without a workspace: scratch comes from the library's static device array."""
+    w = weights.c()
+    _check(lib().tsp_attention_fwd_static(plan.handle, batch, _ptr(xz), ctypes.byref(w), _ptr(a_out), _ptr(lse),
+                                          _stream(stream)), "tsp_attention_fwd_static")
 
 
 def tsp_gated_mlp_fwd(plan: Plan, batch: int, hz, weights: PackedWeights, m_out, workspace, stream=None):

@@ -184,6 +184,31 @@ tsp_status tsp_sync_check(void* stream);
  * this thread return `status` before enqueuing anything (count 0 disarms). */
 void tsp_debug_fail_next(tsp_status status, int count);
 
+/* ---- attention without a caller workspace -------------------------------- */
+
+/* Size of the static scratch array behind tsp_attention_fwd_static. */
+#define TSP_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* Same computation and arguments as tsp_attention_fwd, minus the workspace:
+ * for callers that cannot allocate device memory (a plug-in inside a host
+ * application that owns all device allocations, or a latency-critical loop
+ * that must not call cudaMalloc, which can synchronize the device).  The
+ * scratch (Q, K, V, O) lives in one static device array of
+ * TSP_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the library is unloaded; the call allocates and frees nothing.
+ * - A batch whose tsp_workspace_bytes(plan, batch, TSP_OP_ATTENTION_FWD)
+ *   exceeds TSP_STATIC_SCRATCH_BYTES is rejected with TSP_ERR_WORKSPACE
+ *   before anything is enqueued.
+ * - All calls share the array: calls whose GPU work overlaps (other streams,
+ *   unordered host threads) race and corrupt each other; order them.  Each
+ *   call writes all the scratch it reads, so nothing needs clearing.
+ * - The first call on a device looks up the array's address on that device
+ *   (cudaGetSymbolAddress, with the device current); make it before any
+ *   stream capture starts.
+ * The TSP posts have no counterpart of this entry point. */
+tsp_status tsp_attention_fwd_static(const tsp_plan* plan, int batch, const void* xz,
+                                    const tsp_weights* weights, void* a_out, void* lse, void* stream);
+
 /* ---- measurement ----------------------------------------------------------- */
 
 /* Per-step timing for measurement (off by default).  While enabled, every
