@@ -101,7 +101,7 @@ Layout layer_layout(const tsp_plan* p, int batch) {
 
 struct BwdLayout {
   size_t dyz, wd_c, dgu, dyzT, mzT, wgu_T, dhz, dguT, hzT, wo_c, doz, dhzT, ozT, dq, dk, dv, dsum, dqkv, wqkv_T,
-      dxz, dqkvT, xzT, end;
+      dxz, dqkvT, xzT, vnat, end;
 };
 
 BwdLayout bwd_layout(const tsp_plan* p, int batch) {
@@ -135,6 +135,7 @@ BwdLayout bwd_layout(const tsp_plan* p, int batch) {
   L.dxz = take(T * h * e);
   L.dqkvT = take(T * 3 * h * e);
   L.xzT = take(T * h * e);
+  L.vnat = take(T * h * e);  // V in [B][H][S][dh] when the forward saved it transposed
   L.end = o;
   return L;
 }
@@ -241,6 +242,12 @@ EpiParams base_epi(const tsp_plan* p, int batch) {
   return ep;
 }
 
+// The tcgen05 attention kernel reads V transposed ([B][H][dh][S]); the QKV
+// epilogue writes V in that layout whenever that kernel will run.
+bool use_tc_attention(const tsp_plan* p) {
+  return p->dtype == TSP_BF16 && attn_tc_supported(p->head_dim, p->chunk);
+}
+
 tsp_status run_gemm(const tsp_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K,
                     EpiKind epi, const EpiParams& ep, cudaStream_t st, const char* what) {
   Prof pr(what, st);
@@ -260,6 +267,7 @@ tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const ts
   ep.q = qz;
   ep.k = k;
   ep.v = v;
+  ep.v_transposed = use_tc_attention(p);
   tsp_status s = run_gemm(p, xz, h, w->qkv, h, T, 3 * h, h, EPI_QKV, ep, st, "QKV projection");
   if (s != TSP_OK) return s;
   AttnParams ap;
@@ -276,7 +284,8 @@ tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const ts
   ap.C = p->chunk;
   {
     Prof pr("attention", st);
-    s = p->dtype == TSP_BF16 ? attn_fwd_bf16(ap, st) : attn_fwd_f32(ap, st);
+    s = p->dtype != TSP_BF16 ? attn_fwd_f32(ap, st)
+                             : (use_tc_attention(p) ? attn_fwd_bf16_tc(ap, st) : attn_fwd_bf16(ap, st));
   }
   if (s != TSP_OK) return fail(s, "attention kernel failed: %s", tsp_status_string(s));
   EpiParams eo = base_epi(p, batch);
@@ -574,7 +583,9 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   const int64_t eb = (int64_t)esize(p);
   auto tr = [&](const void* src, size_t dst_off, int64_t rows, int64_t cols, const char* what) {
     Prof pr(what, st);
-    return cuda_status(launch_transpose(src, wb + dst_off, rows, cols, (int)eb, st), what);
+    // V^T is one [dh][S] matrix per (batch, head); everything else is a single matrix
+    const int nb = (rows == p->head_dim && cols == p->seq && src == sv + A.v) ? batch * p->heads : 1;
+    return cuda_status(launch_transpose(src, wb + dst_off, rows, cols, (int)eb, st, nb), what);
   };
 #define TSP_TRY(expr)              \
   do {                             \
@@ -636,11 +647,16 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     TSP_TRY(run_gemm(p, wb + L.dhzT, T, wb + L.ozT, T, h, h, T, EPI_STORE, e, st, "dW_O"));
   }
   // attention core backward
+  const void* v_nat = sv + A.v;
+  if (use_tc_attention(p)) {
+    TSP_TRY(tr(sv + A.v, L.vnat, p->head_dim, p->seq, "transpose V^T"));
+    v_nat = wb + L.vnat;
+  }
   {
     AttnBwdParams ab;
     ab.q = sv + A.qz;
     ab.k = sv + A.k;
-    ab.v = sv + A.v;
+    ab.v = v_nat;
     ab.o = sv + A.oz;
     ab.dO = wb + L.doz;
     ab.lse = reinterpret_cast<const float*>(sv + A.lse);

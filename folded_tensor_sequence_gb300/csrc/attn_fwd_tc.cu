@@ -1,0 +1,408 @@
+// Causal flash attention forward on the 5th-generation tensor cores
+// (tcgen05 + TMEM), zigzag token layout, head_dim 128, bf16 in, fp32 softmax.
+//
+// Queries come from the zigzag rows of the rank that owns them; keys and
+// values from the gathered natural-order tensors (K as [B][H][S][128], V
+// transposed as [B][H][128][S]) -- the K/V all-gather of the TSP attention
+// schedule (ai-trends.today TSP article, "How to Fold a Book").  Online
+// softmax as in FlashAttention / ring attention (r007 chapter, "Параллелизм по
+// контексту: Ring Attention против Ulysses").
+//
+// Work unit: a 256-query block (two 128-row tiles A and B) of one (batch,
+// head).  Block G needs key tiles 0..2G+1 (tile A stops one earlier); only
+// each tile's last key tile crosses the diagonal and is masked.  A CTA takes
+// the mirror pair of blocks (G, 2D*nb-1-G), which lie in chunks c and 2D-1-c
+// of the same rank, so every CTA does the same number of key tiles.
+//
+// Per CTA: warp 8 issues TMA loads (Q tiles, then K_j / V_j^T tiles through a
+// 3-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
+// are the softmax warpgroups of tiles A and B.  TMEM (512 columns): S_A, S_B,
+// O_A, O_B, 128 fp32 columns each.  Issue order per key tile j:
+//   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+// so the tensor core works on one tile while the other tile's softmax runs.
+// P = exp2(S*log2e/sqrt(dh) - m) is written as bf16 to shared memory in the
+// 128-byte-swizzled K-major layout the MMA reads.  The running max is only
+// raised (and O rescaled in TMEM) when it grows by more than 2^8, which keeps
+// P <= 256 and makes the rescale rare.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tsp {
+
+namespace {
+
+constexpr int QT = 128;    // rows per query tile (MMA M)
+constexpr int KT = 128;    // keys per key tile
+constexpr int HD = 128;    // head dim
+constexpr int STAGES = 3;  // K / V^T tile ring
+constexpr int THREADS = 320;
+constexpr uint32_t SUB_BYTES = 128 * 64 * 2;     // one [128][64] bf16 swizzled sub-tile
+constexpr uint32_t TILE_BYTES = 2 * SUB_BYTES;   // [128][128]
+constexpr size_t SMEM_BYTES = 1024 + (2 + STAGES + 2) * (size_t)TILE_BYTES + 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct FaParams {
+  int B, H, D, nb;  // nb = 256-query blocks per chunk
+  int64_t S, C;
+  int h;
+  __nv_bfloat16* o;
+  float* lse;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+struct BlockGeo {
+  int64_t zrow0;  // zigzag row of the block's first query
+  int64_t p0;     // global position of the block's first query
+  int nB;         // key tiles for tile B (tile A uses nB - 1)
+};
+
+__device__ __forceinline__ BlockGeo block_geo(int G, const FaParams& p, int b) {
+  const int c = G / p.nb, i = G % p.nb;
+  const int64_t r = c < p.D ? c : 2 * p.D - 1 - c;
+  const int64_t k0 = (c < p.D ? 0 : p.C) + (int64_t)i * 2 * QT;
+  BlockGeo g;
+  g.zrow0 = (r * p.B + b) * 2 * p.C + k0;
+  g.p0 = (int64_t)c * p.C + (int64_t)i * 2 * QT;
+  g.nB = (int)(g.p0 / KT) + 2;
+  return g;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmVt, const FaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Qs = smem;                                   // [2] tiles
+  uint8_t* KVs = smem + 2 * TILE_BYTES;                 // [STAGES] tiles
+  uint8_t* Ps = smem + (2 + STAGES) * TILE_BYTES;       // [2] tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + STAGES + 2) * TILE_BYTES);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;             // [STAGES]
+  uint64_t* kv_empty = kv_full + STAGES;    // [STAGES]
+  uint64_t* s_full = kv_empty + STAGES;     // [2]
+  uint64_t* p_full = s_full + 2;            // [2]
+  uint64_t* o_done = p_full + 2;            // [2]
+  uint64_t* drain = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int head = blockIdx.y, b = blockIdx.z;
+  const int total_blocks = 2 * p.D * p.nb;
+  // the CTA's two blocks: heavy (late in the sequence) first, then its mirror
+  auto blk_id = [&](int blk) { return blk == 0 ? total_blocks - 1 - (int)blockIdx.x : (int)blockIdx.x; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_done[x], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmVt);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const unsigned code = KID_ATTN_FWD << 8;
+
+  if (warp == 8) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      const int64_t kv_row0 = ((int64_t)b * p.H + head) * p.S;   // K rows of this head
+      const int64_t vt_row0 = ((int64_t)b * p.H + head) * HD;    // V^T rows of this head
+      uint32_t item = 0, q_armed = 0;
+      bool ok = true;
+      for (int blk = 0; blk < 2 && ok; ++blk) {
+        const BlockGeo g = block_geo(blk_id(blk), p, b);
+        if (!mbar_wait(q_empty, (blk & 1) ^ 1, abort_flag, p.err, code | 1)) break;
+        mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
+        ++q_armed;
+        for (int x = 0; x < 2; ++x)
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)(g.zrow0 + x * QT),
+                        q_full);
+        for (int j = 0; j < g.nB && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++item) {
+            const int s = item % STAGES;
+            if (!mbar_wait(&kv_empty[s], ((item / STAGES) & 1) ^ 1, abort_flag, p.err, code | 2)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&kv_full[s], TILE_BYTES);
+            uint8_t* dst = KVs + s * TILE_BYTES;
+            if (kv == 0) {
+              for (int c = 0; c < 2; ++c)
+                tma_load_2d(dst + c * SUB_BYTES, &tmK, c * 64, (int)(kv_row0 + (int64_t)j * KT), &kv_full[s]);
+            } else {
+              for (int c = 0; c < 2; ++c)
+                tma_load_2d(dst + c * SUB_BYTES, &tmVt, j * KT + c * 64, (int)vt_row0, &kv_full[s]);
+            }
+          }
+        }
+      }
+      // wait for the copies still in flight (bounded) before the CTA may exit
+      const uint32_t first = item > (uint32_t)STAGES ? item - STAGES : 0;
+      volatile int dummy = 0;
+      for (uint32_t n = first; n < item; ++n) mbar_wait(&kv_full[n % STAGES], (n / STAGES) & 1, &dummy, p.err, code | 3);
+      if (q_armed) mbar_wait(q_full, (q_armed - 1) & 1, &dummy, p.err, code | 3);
+    }
+  } else if (warp == 9) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(QT, KT);
+      uint32_t item = 0;
+      uint32_t pcnt0 = 0, pcnt1 = 0;
+      bool ok = true;
+      auto mma_s = [&](int x, int s) {  // S_x = Q_x K^T, K = head dim
+        const uint32_t qa = smem_u32(Qs + x * TILE_BYTES), kb = smem_u32(KVs + s * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t a = sdesc_kmajor_sw128(qa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
+          const uint64_t bb = sdesc_kmajor_sw128(kb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
+          umma_bf16(tmem_base + x * 128, a, bb, idesc, k > 0);
+        }
+      };
+      auto mma_pv = [&](int x, int s, bool acc) {  // O_x += P_x V, K = keys
+        const uint32_t pa = smem_u32(Ps + x * TILE_BYTES), vb = smem_u32(KVs + s * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < KT / 16; ++k) {
+          const uint64_t a = sdesc_kmajor_sw128(pa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
+          const uint64_t bb = sdesc_kmajor_sw128(vb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
+          umma_bf16(tmem_base + 256 + x * 128, a, bb, idesc, (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      auto wait_item = [&](uint32_t n) {
+        return mbar_wait(&kv_full[n % STAGES], (n / STAGES) & 1, abort_flag, p.err, code | 4);
+      };
+      auto wait_p = [&](int x) {
+        uint32_t& cnt = x == 0 ? pcnt0 : pcnt1;
+        const bool r = mbar_wait(&p_full[x], cnt & 1, abort_flag, p.err, code | 5);
+        ++cnt;
+        return r;
+      };
+      for (int blk = 0; blk < 2 && ok; ++blk) {
+        const BlockGeo g = block_geo(blk_id(blk), p, b);
+        const int nB = g.nB, nA = g.nB - 1;
+        if (!mbar_wait(q_full, blk & 1, abort_flag, p.err, code | 6)) break;
+        tc_fence_after();
+        const uint32_t base = item;  // K_j = base + 2j, V_j = base + 2j + 1
+        if (!wait_item(base)) break;
+        tc_fence_after();
+        mma_s(0, base % STAGES);
+        umma_commit(&s_full[0]);
+        mma_s(1, base % STAGES);
+        umma_commit(&s_full[1]);
+        umma_commit(&kv_empty[base % STAGES]);
+        for (int j = 0; j < nB && ok; ++j) {
+          const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+          bool k_next_ready = false;
+          if (!wait_item(iv)) { ok = false; break; }
+          if (j < nA) {
+            if (!wait_p(0)) { ok = false; break; }
+            tc_fence_after();
+            mma_pv(0, iv % STAGES, j > 0);
+            if (j + 1 < nA) {
+              if (!wait_item(ik)) { ok = false; break; }
+              k_next_ready = true;
+              tc_fence_after();
+              mma_s(0, ik % STAGES);
+              umma_commit(&s_full[0]);
+            } else {
+              umma_commit(&o_done[0]);
+            }
+          }
+          if (!wait_p(1)) { ok = false; break; }
+          tc_fence_after();
+          mma_pv(1, iv % STAGES, j > 0);
+          umma_commit(&kv_empty[iv % STAGES]);
+          if (j + 1 < nB) {
+            if (!k_next_ready) {
+              if (!wait_item(ik)) { ok = false; break; }
+              tc_fence_after();
+            }
+            mma_s(1, ik % STAGES);
+            umma_commit(&s_full[1]);
+            umma_commit(&kv_empty[ik % STAGES]);
+          } else {
+            umma_commit(&o_done[1]);
+          }
+        }
+        item = base + 2 * nB;
+        umma_commit(q_empty);
+      }
+      umma_commit(drain);
+      volatile int dummy = 0;
+      mbar_wait(drain, 0, &dummy, p.err, code | 7);
+    }
+  } else {
+    // ------------------------- softmax warpgroups (warps 0-7) -------------------------
+    const int x = warp / 4;  // 0: tile A, 1: tile B
+    const int quad = warp % 4;
+    const int row = quad * 32 + lane;  // TMEM lane == row of the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off + x * 128;
+    const uint32_t tO = tmem_base + lane_off + 256 + x * 128;
+    uint8_t* Pbuf = Ps + x * TILE_BYTES;
+    const float sl2 = kLog2e * rsqrtf((float)HD);
+    uint32_t scnt = 0;
+    for (int blk = 0; blk < 2; ++blk) {
+      const BlockGeo g = block_geo(blk_id(blk), p, b);
+      const int n = g.nB - 1 + x;
+      float m_used = -INFINITY, l = 0.f;
+      bool alive = true;
+      for (int j = 0; j < n; ++j) {
+        const bool got = mbar_wait(&s_full[x], scnt & 1, abort_flag, p.err, code | 8);
+        ++scnt;
+        if (!__all_sync(0xffffffffu, got)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld128(tS, sr);
+        const bool diag = (j == n - 1);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          float v = __uint_as_float(sr[c]);
+          if (diag && c > row) v = -INFINITY;
+          sr[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+        const float m_new = mx * sl2;
+        const bool need = m_new > m_used + kRescaleThreshold;
+        const float factor = need ? ex2f(m_used - m_new) : 1.0f;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float ov[32];
+            uint32_t part[32];
+            tmem_ld32(tO + c4 * 32, ov);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) part[c] = __float_as_uint(ov[c] * factor);
+            tmem_st32(tO + c4 * 32, part);
+          }
+        }
+        if (need) {
+          l *= factor;
+          m_used = m_new;
+        }
+        const float neg_m = -m_used;
+        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          float e[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) e[t] = ex2f(fmaf(__uint_as_float(sr[q * 8 + t]), sl2, neg_m));
+          ls0 += e[0] + e[4];
+          ls1 += e[1] + e[5];
+          ls2 += e[2] + e[6];
+          ls3 += e[3] + e[7];
+          const uint4 pk = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
+                                      pack_bf16x2(e[6], e[7]));
+          const int sub = q >> 3, cc = q & 7;
+          *reinterpret_cast<uint4*>(Pbuf + sub * SUB_BYTES + row * 128 + ((cc ^ (row & 7)) << 4)) = pk;
+        }
+        l += (ls0 + ls1) + (ls2 + ls3);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
+      }
+      if (!alive) break;
+      const bool got = mbar_wait(&o_done[x], blk & 1, abort_flag, p.err, code | 9);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      uint32_t orr[128];
+      tmem_ld128(tO, orr);
+      const float inv = 1.0f / l;
+      const int64_t zrow = g.zrow0 + x * QT + row;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + zrow * p.h + head * HD);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        dst[q] = make_uint4(pack_bf16x2(__uint_as_float(orr[q * 8 + 0]) * inv, __uint_as_float(orr[q * 8 + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(orr[q * 8 + 2]) * inv, __uint_as_float(orr[q * 8 + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(orr[q * 8 + 4]) * inv, __uint_as_float(orr[q * 8 + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(orr[q * 8 + 6]) * inv, __uint_as_float(orr[q * 8 + 7]) * inv));
+      }
+      if (p.lse) p.lse[((int64_t)b * p.H + head) * p.S + g.p0 + x * QT + row] = (m_used + __log2f(l)) * kLn2;
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace
+
+bool attn_tc_supported(int head_dim, int64_t chunk) { return head_dim == HD && chunk % (2 * QT) == 0; }
+
+tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
+  if (!attn_tc_supported(a.dh, a.C)) return TSP_ERR_UNSUPPORTED;
+  if (a.B * a.S == 0) return TSP_OK;
+  const int64_t T = (int64_t)a.B * a.S;
+  const int h = a.H * HD;
+  CUtensorMap mq, mk, mv;
+  if (!make_tma_2d_bf16(&mq, a.q, T, h, h, 128) ||
+      !make_tma_2d_bf16(&mk, a.k, (int64_t)a.B * a.H * a.S, HD, HD, 128) ||
+      !make_tma_2d_bf16(&mv, a.v, (int64_t)a.B * a.H * HD, a.S, a.S, 128))
+    return TSP_ERR_CUDA;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
+        cudaSuccess)
+      return TSP_ERR_CUDA;
+    configured = true;
+  }
+  FaParams p;
+  p.B = a.B;
+  p.H = a.H;
+  p.D = a.D;
+  p.nb = (int)(a.C / (2 * QT));
+  p.S = a.S;
+  p.C = a.C;
+  p.h = h;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.err = dev_error_word();
+  dim3 grid(a.D * p.nb, a.H, a.B);
+  attn_fwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
+}
+
+}  // namespace tsp

@@ -268,9 +268,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int d = cin % ep.dh;
             if (which == 0) {
               store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.q) + m * ep.h + head * ep.dh + d, v);
-            } else {
+            } else if (which == 1 || !ep.v_transposed) {
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 1 ? ep.k : ep.v);
               store32_bf16(dst + (((int64_t)b * ep.H + head) * ep.S + p) * ep.dh + d, v);
+            } else {
+              // V^T [B][H][dh][S]: lanes hold consecutive positions, so each store is coalesced
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(ep.v) +
+                                   (((int64_t)b * ep.H + head) * ep.dh + d) * ep.S + p;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) dst[(int64_t)i * ep.S] = __float2bfloat16_rn(v[i]);
             }
           } else if constexpr (EPI == EPI_DSWIGLU) {
             // n indexes F; the saved G/U and the dGU output use the packed gate_up order.
@@ -328,9 +334,11 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix with row stride
 // `ld` elements; box = 64 columns x box_rows rows, 128-byte swizzle.
-bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+bool make_tma_2d_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -341,6 +349,8 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int EPI>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& s, const EpiParams& ep,
@@ -365,7 +375,7 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   if (N % BN || K % BK || lda % 8 || ldb % 8) return TSP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) return TSP_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
-  if (!make_map_bf16(&ta, A, M, K, lda, BM) || !make_map_bf16(&tb, B, N, K, ldb, BN)) return TSP_ERR_CUDA;
+  if (!make_tma_2d_bf16(&ta, A, M, K, lda, BM) || !make_tma_2d_bf16(&tb, B, N, K, ldb, BN)) return TSP_ERR_CUDA;
   GemmShape s;
   s.M = M;
   s.N = N;

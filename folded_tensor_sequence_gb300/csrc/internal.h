@@ -1,6 +1,7 @@
 // Internal declarations shared by the libtsp translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,6 +41,7 @@ struct EpiParams {
   void* v = nullptr;
   int D = 1, B = 1, S = 0, C = 0, H = 1, dh = 1, h = 0;
   unsigned int* err = nullptr;  // device error word
+  bool v_transposed = false;    // EPI_QKV: write V as [B][H][dh][S] instead of [B][H][S][dh]
 };
 
 int num_sms();
@@ -53,6 +55,10 @@ unsigned int* dev_error_word();  // device address of this device's error word (
 tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K,
                         EpiKind epi, const EpiParams& ep, cudaStream_t stream);
 
+// 2-D bf16 TMA descriptor: row-major [rows][cols], row stride ld elements,
+// box = 64 columns x box_rows rows, 128-byte swizzle.
+bool make_tma_2d_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows);
+
 // fp32 SIMT GEMM, same contract (any M, N, K; SWIGLU/DSWIGLU not supported).
 tsp_status gemm_f32_simt(const float* A, int64_t lda, const float* B, int64_t ldb, int M, int N, int K,
                          EpiKind epi, const EpiParams& ep, cudaStream_t stream);
@@ -64,7 +70,7 @@ cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, i
                              int64_t S, int H, int dh, cudaStream_t stream);
 cudaError_t launch_swiglu_f32(const float* gu, float* m, int64_t T, int F, cudaStream_t stream);
 cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols, int elem_bytes,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int batch = 1);
 cudaError_t launch_pack_weights(const tsp_plan* p, const void* const c[7], const tsp_weight_grads* w, bool unpack,
                                 cudaStream_t stream);
 
@@ -80,6 +86,9 @@ struct AttnParams {
 };
 tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream);
 tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream);
+// tcgen05 attention (V given transposed, [B][H][dh][S]); needs head_dim 128 and chunk % 256 == 0.
+bool attn_tc_supported(int head_dim, int64_t chunk);
+tsp_status attn_fwd_bf16_tc(const AttnParams& p, cudaStream_t stream);
 
 struct AttnBwdParams {
   const void* q;   // zigzag [T][h]

@@ -115,6 +115,8 @@ __global__ void assemble_dqkv_kernel(const uint4* __restrict__ dq, const uint4* 
 template <typename T>
 __global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows, int64_t cols) {
   __shared__ T tile[32][33];
+  src += (int64_t)blockIdx.y * rows * cols;  // batch of matrices along grid y
+  dst += (int64_t)blockIdx.y * rows * cols;
   const int64_t tiles_c = (cols + 31) / 32;
   const int64_t tiles_r = (rows + 31) / 32;
   for (int64_t t = blockIdx.x; t < tiles_r * tiles_c; t += gridDim.x) {
@@ -237,10 +239,11 @@ cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv,
 }
 
 cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols, int elem_bytes,
-                             cudaStream_t stream) {
-  if (rows == 0 || cols == 0) return cudaSuccess;
+                             cudaStream_t stream, int batch) {
+  if (rows == 0 || cols == 0 || batch == 0) return cudaSuccess;
   const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
-  const int grid = (int)(tiles < (int64_t)num_sms() * 16 ? tiles : (int64_t)num_sms() * 16);
+  const int64_t cap = ((int64_t)num_sms() * 16 + batch - 1) / batch;
+  dim3 grid((unsigned)(tiles < cap ? tiles : cap), (unsigned)batch);
   dim3 block(32, 8);
   if (elem_bytes == 2)
     transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<const uint16_t*>(src),

@@ -48,6 +48,9 @@ BWD_CASES = [
     LayerConfig("bwd_D4_b2_s1024", D=4, batch=2, seq=1024, hidden=512, heads=4, head_dim=128, ffn=768, dtype="bf16"),
     LayerConfig("bwd_D8_s2048", D=8, batch=1, seq=2048, hidden=1024, heads=8, head_dim=128, ffn=1024, dtype="bf16"),
     LayerConfig("bwd_D3_s1152", D=3, batch=1, seq=1152, hidden=768, heads=6, head_dim=128, ffn=1536, dtype="bf16"),
+    # forward through the tcgen05 attention kernel (V saved transposed)
+    LayerConfig("bwd_D2_b2_s1024", D=2, batch=2, seq=1024, hidden=256, heads=2, head_dim=128, ffn=512, dtype="bf16"),
+    LayerConfig("bwd_D4_s2048", D=4, batch=1, seq=2048, hidden=512, heads=4, head_dim=128, ffn=768, dtype="bf16"),
 ]
 
 
