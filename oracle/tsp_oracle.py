@@ -177,7 +177,14 @@ def layer_fwd(x, w, heads: int, rows=None):
     return {k: np.stack(v) for k, v in out.items()}
 
 
-def layer_bwd(x, w, heads: int, dY):
+def _head_probs(Q, K, sl, scale, mask):
+    """Causal softmax probabilities of one head (rows: queries, columns: keys)."""
+    s = np.where(mask, (Q[:, sl] @ K[:, sl].T) * scale, -np.inf)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    return p / p.sum(axis=1, keepdims=True)
+
+
+def layer_bwd(x, w, heads: int, dY, return_y: bool = False):
     """Exact gradient of ``layer_fwd``'s Y with respect to x and all weights, fp64.
 
     The posts do not describe the TSP backward; its plainest reading is the
@@ -194,22 +201,20 @@ def layer_bwd(x, w, heads: int, dY):
     scale = 1.0 / math.sqrt(dh)
     grads = {k: np.zeros_like(v) for k, v in w.items()}
     dx = np.zeros_like(x)
+    Y = np.zeros_like(x) if return_y else None
     mask = np.tril(np.ones((S, S), dtype=bool))
     for b in range(B):
         xb = x[b]
         Q, K, V = xb @ w["Wq"], xb @ w["Wk"], xb @ w["Wv"]
         O = np.zeros((S, h))
-        Ps = []
         for e in range(heads):
             sl = slice(e * dh, (e + 1) * dh)
-            s = np.where(mask, (Q[:, sl] @ K[:, sl].T) * scale, -np.inf)
-            p = np.exp(s - s.max(axis=1, keepdims=True))
-            p /= p.sum(axis=1, keepdims=True)
-            Ps.append(p)
-            O[:, sl] = p @ V[:, sl]
+            O[:, sl] = _head_probs(Q, K, sl, scale, mask) @ V[:, sl]
         Hb = xb + O @ w["Wo"]
         G, U = Hb @ w["Wg"], Hb @ w["Wu"]
         M = silu(G) * U
+        if return_y:
+            Y[b] = Hb + M @ w["Wd"]
         dYb = dY[b]
         dM = dYb @ w["Wd"].T
         grads["Wd"] += M.T @ dYb
@@ -225,7 +230,7 @@ def layer_bwd(x, w, heads: int, dY):
         dV = np.zeros((S, h))
         for e in range(heads):
             sl = slice(e * dh, (e + 1) * dh)
-            p = Ps[e]
+            p = _head_probs(Q, K, sl, scale, mask)  # recomputed per head to bound memory
             dV[:, sl] = p.T @ dO[:, sl]
             dP = dO[:, sl] @ V[:, sl].T
             dS = p * (dP - (dP * p).sum(axis=1, keepdims=True))
@@ -235,6 +240,8 @@ def layer_bwd(x, w, heads: int, dY):
         grads["Wk"] += xb.T @ dK
         grads["Wv"] += xb.T @ dV
         dx[b] = dH + dQ @ w["Wq"].T + dK @ w["Wk"].T + dV @ w["Wv"].T
+    if return_y:
+        return dx, grads, Y
     return dx, grads
 
 

@@ -34,8 +34,10 @@ def max_rel(got, ref):
 def check(got, ref, dtype: str, what: str):
     if dtype == "bf16":
         e = rel_frob(got, ref)
+        print(f"PARITY {what}: relative Frobenius {e:.3e} (bound {BF16_TOL})")
         assert e <= BF16_TOL, f"{what}: relative Frobenius error {e:.3e} > {BF16_TOL}"
     else:
         e = max_rel(got, ref)
+        print(f"PARITY {what}: max relative {e:.3e} (bound {F32_TOL})")
         assert e <= F32_TOL, f"{what}: max relative error {e:.3e} > {F32_TOL}"
     return e

@@ -45,3 +45,16 @@ def test_backward_matches_finite_differences():
         fdw = fd_of(w[k], lambda: loss(x, w))
         err = np.linalg.norm(fdw - g[k]) / np.linalg.norm(g[k])
         assert err < 1e-6, (k, err)
+
+
+def test_backward_returns_forward_output():
+    rng = np.random.default_rng(8)
+    B, S, h, heads, F = 2, 6, 4, 2, 8
+    x = rng.standard_normal((B, S, h))
+    w = {k: rng.standard_normal(s) * 0.5 for k, s in
+         {"Wq": (h, h), "Wk": (h, h), "Wv": (h, h), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}.items()}
+    dY = rng.standard_normal((B, S, h))
+    dx, g, Y = O.layer_bwd(x, w, heads, dY, return_y=True)
+    dx2, g2 = O.layer_bwd(x, w, heads, dY)
+    assert np.allclose(Y, O.layer_fwd(x, w, heads)["Y"], rtol=1e-13, atol=1e-13)
+    assert np.array_equal(dx, dx2) and all(np.array_equal(g[k], g2[k]) for k in g)
