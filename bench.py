@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 from folded_tensor_sequence_gb300.configs import BY_NAME, LAYER_7B_S16K  # noqa: E402
 
 METRIC = "TSP layer fwd TFLOP/s & tokens/s (bf16) at 1 GB300; % of dense bf16 tensor peak"
+# (for the training workload the same metric counts the step's model flops, 3x the forward)
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -69,19 +70,50 @@ def load_peaks():
 
 
 def step_work(cfg):
-    """Algorithmic work per launch of each step: (flops, bytes)."""
+    """Algorithmic work per launch of each step: (flops, bytes, kernels launched)."""
     B, S, h, F, H, dh = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
     T = B * S
     e = 2 if cfg.dtype == "bf16" else 4
-    return {
-        "zigzag permute": (0, 2 * T * h * e),
-        "QKV projection": (2 * T * h * 3 * h, (T * h + 3 * h * h + 3 * T * h) * e),
-        "attention": (4 * B * H * dh * S * (S + 1) // 2, 4 * T * h * e),
-        "output projection": (2 * T * h * h, (3 * T * h + h * h) * e),
-        "gate/up projection": (2 * T * h * 2 * F, (T * h + 2 * F * h + T * F) * e),
-        "down projection": (2 * T * F * h, (T * F + F * h + 2 * T * h) * e),
-        "zigzag unpermute": (0, 2 * T * h * e),
+    attn = 4 * B * H * dh * S * (S + 1) // 2
+    w = {
+        "zigzag permute": (0, 2 * T * h * e, 1),
+        "QKV projection": (2 * T * h * 3 * h, (T * h + 3 * h * h + 3 * T * h) * e, 1),
+        "attention": (attn, 4 * T * h * e, 1),
+        "output projection": (2 * T * h * h, (3 * T * h + h * h) * e, 1),
+        "gate/up projection": (2 * T * h * 2 * F, (T * h + 2 * F * h + T * F) * e, 1),
+        "down projection": (2 * T * F * h, (T * F + F * h + 2 * T * h) * e, 1),
+        "zigzag unpermute": (0, 2 * T * h * e, 1),
     }
+    if cfg.backward:
+        tr = lambda r, c: (0, 2 * r * c * e, 1)  # noqa: E731
+        w.update({
+            "permute dy": (0, 2 * T * h * e, 1),
+            "transpose W_down": tr(h, F),
+            "dM = dY Wd^T": (2 * T * h * F, (T * h + F * h + 4 * T * F) * e, 1),
+            "transpose dY": tr(T, h),
+            "transpose M": tr(T, F),
+            "dW_down": (2 * h * F * T, (T * h + T * F + h * F) * e, 1),
+            "transpose W_gate_up": tr(2 * F, h),
+            "dH": (2 * T * 2 * F * h, (2 * T * F + 2 * F * h + 2 * T * h) * e, 1),
+            "transpose dGU": tr(T, 2 * F),
+            "transpose H": tr(T, h),
+            "dW_gate_up": (2 * 2 * F * h * T, (2 * T * F + T * h + 2 * F * h) * e, 1),
+            "transpose W_O": tr(h, h),
+            "dO": (2 * T * h * h, (2 * T * h + h * h) * e, 1),
+            "transpose dH": tr(T, h),
+            "transpose O": tr(T, h),
+            "dW_O": (2 * h * h * T, (2 * T * h + h * h) * e, 1),
+            "transpose V^T": tr(T, h),
+            "attention bwd": (2 * attn, 7 * T * h * e, 3),
+            "assemble dQKV": (0, 6 * T * h * e, 1),
+            "transpose W_QKV": tr(3 * h, h),
+            "dx": (2 * T * 3 * h * h, (3 * T * h + 3 * h * h + 2 * T * h) * e, 1),
+            "transpose dQKV": tr(T, 3 * h),
+            "transpose xz": tr(T, h),
+            "dW_QKV": (2 * 3 * h * h * T, (3 * T * h + T * h + 3 * h * h) * e, 1),
+            "unpermute dx": (0, 2 * T * h * e, 1),
+        })
+    return w
 
 
 class ClockSampler:
@@ -277,9 +309,20 @@ def main():
     y = torch.empty_like(x)
     work = tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD, dev)
     stream = torch.cuda.current_stream(dev)
+    if cfg.backward:
+        # training step (no optimizer): forward keeping activations, then the full backward
+        dy = synth.tensor_torch("dY", (B, S, h), 1.0, cfg.dtype, 0, dev)
+        dx = torch.empty_like(x)
+        grads = tsp.empty_packed(plan, dev)
+        saved = torch.empty(tsp.tsp_saved_bytes(plan, B), dtype=torch.uint8, device=dev)
+        bwork = tsp.workspace(plan, B, tsp.TSP_OP_LAYER_BWD, dev)
 
-    def step():
-        tsp.tsp_layer_fwd(plan, B, x, packed, y, None, work, stream)
+        def step():
+            tsp.tsp_layer_fwd(plan, B, x, packed, y, saved, work, stream)
+            tsp.tsp_layer_bwd(plan, B, x, packed, saved, dy, dx, grads, bwork, stream)
+    else:
+        def step():
+            tsp.tsp_layer_fwd(plan, B, x, packed, y, None, work, stream)
 
     for _ in range(args.warmup):
         step()
@@ -308,7 +351,7 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     clocks = clk.summary()
-    flops = cfg.fwd_flops()
+    flops = cfg.fwd_flops() * (3 if cfg.backward else 1)  # training step: model flops = 3x forward
     ms_step = ms / args.steps
     value = ws * flops * args.steps / (ms / 1e3) / 1e12
     tokens_s = ws * B * S * args.steps / (ms / 1e3)
@@ -321,15 +364,17 @@ def main():
     tsp.tsp_profile_enable(False)
     wk = step_work(cfg)
     kernels = {}
+    launches_per_step = 0
     for name, tot, cnt in rows:
-        fl, by = wk.get(name, (0, 0))
+        fl, by, nk = wk.get(name, (0, 0, 1))
+        launches_per_step += nk * cnt / args.steps
         avg = tot / cnt
         kernels[name] = {"ms": round(avg, 4), "tflops": round(fl / avg / 1e9, 1) if fl else None,
                          "gbs": round(by / avg / 1e6, 1)}
     dom = max(rows, key=lambda r: r[1])
     peaks, peak_src = load_peaks()
     dname, dtot, dcnt = dom
-    dfl, dby = wk.get(dname, (0, 0))
+    dfl, dby, _ = wk.get(dname, (0, 0, 1))
     davg_s = dtot / dcnt / 1e3
     traffic = ncu_traffic(dname)
     if dfl:
@@ -346,16 +391,20 @@ def main():
                 "frac": round(ach / peak, 4), "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
 
     # ---- end to end through the API with host buffers -----------------------
-    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    x_host.copy_(x)
-    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    ins = [x, dy] if cfg.backward else [x]          # per-step inputs copied in
+    out = dx if cfg.backward else y                   # per-step result copied out
+    ins_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
+    for th, t in zip(ins_host, ins):
+        th.copy_(t)
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        x.copy_(x_host, non_blocking=True)
+        for t, th in zip(ins, ins_host):
+            t.copy_(th, non_blocking=True)
         step()
-        y_host.copy_(y, non_blocking=True)
+        out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     barrier()
     ems = e0.elapsed_time(e1)
@@ -365,7 +414,8 @@ def main():
         ems = float(t.item())
     tsp.tsp_sync_check(stream)
     e2e = {"value": round(ws * flops * args.steps / (ems / 1e3) / 1e12, 2), "unit": UNIT,
-           "h2d_bytes_per_step": x.numel() * x.element_size(), "d2h_bytes_per_step": y.numel() * y.element_size(),
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in ins),
+           "d2h_bytes_per_step": out.numel() * out.element_size(),
            "tokens_per_s": round(ws * B * S * args.steps / (ems / 1e3), 1)}
 
     if rank == 0:
@@ -387,7 +437,7 @@ def main():
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": sum(1 for _ in wk) * args.steps,
+            "gpu_launches": int(round(launches_per_step)) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line))
