@@ -78,40 +78,42 @@ __global__ void kv_gather_kernel(const uint4* __restrict__ kz, const uint4* __re
 }
 
 // dqkv [T][3h] in packed column order <- dq zigzag [T][h], dk/dv gathered [B][H][S][dh].
+// One CTA per zigzag row: the row's (rank, batch, position) is decoded once.
 __global__ void assemble_dqkv_kernel(const uint4* __restrict__ dq, const uint4* __restrict__ dk,
                                      const uint4* __restrict__ dv, uint4* __restrict__ out, int vec_per_head, int D,
                                      int B, int64_t S, int H) {
   const int64_t C = S / (2 * D);
   const int64_t twoC = 2 * C;
-  const int hpv = H / D;                             // heads per shard
-  const int64_t vec_per_proj = (int64_t)H * vec_per_head;  // h columns
-  const int64_t vec_per_row = 3 * vec_per_proj;
-  const int64_t total = (int64_t)B * S * vec_per_row;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t zrow = i / vec_per_row;
-    const int64_t cv = i - zrow * vec_per_row;  // packed column vector index
-    const int64_t shard_w = 3 * (int64_t)hpv * vec_per_head;
-    const int64_t s = cv / shard_w;
-    const int64_t within = cv - s * shard_w;
-    const int64_t which = within / ((int64_t)hpv * vec_per_head);
-    const int64_t cin = within - which * hpv * vec_per_head;
-    const int64_t head = s * hpv + cin / vec_per_head;
-    const int64_t d = cin % vec_per_head;
+  const int64_t zrow = blockIdx.x;
+  const int64_t r = zrow / (B * twoC);
+  const int64_t rem = zrow - r * (B * twoC);
+  const int64_t b = rem / twoC;
+  const int64_t kk = rem - b * twoC;
+  const int64_t p = zigzag_pos(r, kk, C, D);
+  const int hpv = H / D;                       // heads per shard
+  const int proj = hpv * vec_per_head;         // vectors of one projection in one shard
+  const int vec_per_proj = H * vec_per_head;   // vectors of h columns
+  const uint4* dq_row = dq + zrow * vec_per_proj;
+  uint4* out_row = out + zrow * 3 * (int64_t)vec_per_proj;
+  for (int cv = threadIdx.x; cv < 3 * vec_per_proj; cv += blockDim.x) {
+    const int s = cv / (3 * proj);
+    const int within = cv - s * 3 * proj;
+    const int which = within / proj;
+    const int cin = within - which * proj;
+    const int head = s * hpv + cin / vec_per_head;
+    const int d = cin % vec_per_head;
+    uint4 v;
     if (which == 0) {
-      out[i] = __ldg(&dq[zrow * vec_per_proj + head * vec_per_head + d]);
+      v = __ldg(&dq_row[head * vec_per_head + d]);
     } else {
-      const int64_t r = zrow / (B * twoC);
-      const int64_t rem = zrow - r * (B * twoC);
-      const int64_t b = rem / twoC;
-      const int64_t kk = rem - b * twoC;
-      const int64_t p = zigzag_pos(r, kk, C, D);
       const int64_t g = ((b * H + head) * S + p) * vec_per_head + d;
-      out[i] = __ldg(which == 1 ? &dk[g] : &dv[g]);
+      v = __ldg(which == 1 ? &dk[g] : &dv[g]);
     }
+    out_row[cv] = v;
   }
 }
 
-// 32x32 tiles through shared memory, element type T.
+// 32x32 tiles through shared memory, element type T (used for 4-byte elements).
 template <typename T>
 __global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows, int64_t cols) {
   __shared__ T tile[32][33];
@@ -129,6 +131,48 @@ __global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst,
     for (int j = threadIdx.y; j < 32; j += blockDim.y) {
       const int64_t c = c0 + j, r = r0 + threadIdx.x;
       if (r < rows && c < cols) dst[c * rows + r] = tile[threadIdx.x][j];
+    }
+    __syncthreads();
+  }
+}
+
+// 2-byte elements, both dimensions multiples of 64: 64x64 tiles moved with
+// 16-byte global loads and stores.  Shared memory holds the tile as 64 rows
+// of eight 16-byte chunks, chunk c of row r stored at position c ^ ((r/8)%8),
+// so both the row-vector writes and the column gathers are free of bank
+// conflicts.  256 threads: each writes two row vectors, then gathers two
+// 8-element column vectors.
+__global__ void __launch_bounds__(256) transpose_b16_kernel(const uint16_t* __restrict__ src,
+                                                            uint16_t* __restrict__ dst, int rows, int cols) {
+  __shared__ __align__(16) uint16_t tile[64 * 64];
+  src += (int64_t)blockIdx.y * rows * cols;
+  dst += (int64_t)blockIdx.y * rows * cols;
+  const int tiles_c = cols / 64;
+  const int ntiles = (rows / 64) * tiles_c;
+  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int r0 = (t / tiles_c) * 64, c0 = (t % tiles_c) * 64;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int idx = threadIdx.x + it * 256;  // 64 rows x 8 chunks
+      const int r = idx / 8, cv = idx % 8;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(r0 + r) * cols + c0 + cv * 8));
+      *reinterpret_cast<uint4*>(&tile[r * 64 + ((cv ^ ((r / 8) & 7)) * 8)]) = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int idx = threadIdx.x + it * 256;  // output: 64 rows (source columns) x 8 chunks
+      const int c = idx / 8, rv = idx % 8;     // source column c, source rows rv*8 .. rv*8+7
+      const int pos = (((c / 8) ^ rv) * 8) + (c % 8);
+      uint16_t e[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) e[k] = tile[(rv * 8 + k) * 64 + pos];
+      uint4 v;
+      v.x = e[0] | (uint32_t(e[1]) << 16);
+      v.y = e[2] | (uint32_t(e[3]) << 16);
+      v.z = e[4] | (uint32_t(e[5]) << 16);
+      v.w = e[6] | (uint32_t(e[7]) << 16);
+      *reinterpret_cast<uint4*>(dst + (int64_t)(c0 + c) * rows + r0 + rv * 8) = v;
     }
     __syncthreads();
   }
@@ -230,11 +274,11 @@ cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, i
 cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
                                  int64_t S, int H, int dh, cudaStream_t stream) {
   const int vph = dh * 2 / 16;
-  const int64_t total = (int64_t)B * S * 3 * H * vph;
-  if (total == 0) return cudaSuccess;
-  assemble_dqkv_kernel<<<grid_for(total, 256), 256, 0, stream>>>(
-      static_cast<const uint4*>(dq), static_cast<const uint4*>(dk), static_cast<const uint4*>(dv),
-      static_cast<uint4*>(dqkv), vph, D, B, S, H);
+  const int64_t T = (int64_t)B * S;
+  if (T == 0) return cudaSuccess;
+  assemble_dqkv_kernel<<<(unsigned)T, 256, 0, stream>>>(static_cast<const uint4*>(dq), static_cast<const uint4*>(dk),
+                                                         static_cast<const uint4*>(dv), static_cast<uint4*>(dqkv),
+                                                         vph, D, B, S, H);
   return cudaGetLastError();
 }
 
@@ -245,7 +289,13 @@ cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t c
   const int64_t cap = ((int64_t)num_sms() * 16 + batch - 1) / batch;
   dim3 grid((unsigned)(tiles < cap ? tiles : cap), (unsigned)batch);
   dim3 block(32, 8);
-  if (elem_bytes == 2)
+  if (elem_bytes == 2 && rows % 64 == 0 && cols % 64 == 0 && rows * cols < (int64_t(1) << 31)) {
+    const int64_t t64 = (rows / 64) * (cols / 64);
+    const int64_t cap64 = ((int64_t)num_sms() * 8 + batch - 1) / batch;
+    dim3 g64((unsigned)(t64 < cap64 ? t64 : cap64), (unsigned)batch);
+    transpose_b16_kernel<<<g64, 256, 0, stream>>>(static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst),
+                                                 (int)rows, (int)cols);
+  } else if (elem_bytes == 2)
     transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<const uint16_t*>(src),
                                                            static_cast<uint16_t*>(dst), rows, cols);
   else
