@@ -101,7 +101,7 @@ Layout layer_layout(const tsp_plan* p, int batch) {
 
 struct BwdLayout {
   size_t dyz, wd_c, dgu, dyzT, mzT, wgu_T, dhz, dguT, hzT, wo_c, doz, dhzT, ozT, dq, dk, dv, dsum, dqkv, wqkv_T,
-      dxz, dqkvT, xzT, vnat, end;
+      dxz, dqkvT, xzT, vnat, qT, doT, kT, end;
 };
 
 BwdLayout bwd_layout(const tsp_plan* p, int batch) {
@@ -136,6 +136,9 @@ BwdLayout bwd_layout(const tsp_plan* p, int batch) {
   L.dqkvT = take(T * 3 * h * e);
   L.xzT = take(T * h * e);
   L.vnat = take(T * h * e);  // V in [B][H][S][dh] when the forward saved it transposed
+  L.qT = take(T * h * e);    // transposed copies for the tensor-core attention backward
+  L.doT = take(T * h * e);
+  L.kT = take(T * h * e);
   L.end = o;
   return L;
 }
@@ -581,11 +584,10 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   char* wb = static_cast<char*>(ws);
   const int T = (int)T64, h = p->hidden, F = p->ffn;
   const int64_t eb = (int64_t)esize(p);
-  auto tr = [&](const void* src, size_t dst_off, int64_t rows, int64_t cols, const char* what) {
+  // transposes `nmat` consecutive [rows][cols] matrices into workspace
+  auto tr = [&](const void* src, size_t dst_off, int64_t rows, int64_t cols, const char* what, int nmat = 1) {
     Prof pr(what, st);
-    // V^T is one [dh][S] matrix per (batch, head); everything else is a single matrix
-    const int nb = (rows == p->head_dim && cols == p->seq && src == sv + A.v) ? batch * p->heads : 1;
-    return cuda_status(launch_transpose(src, wb + dst_off, rows, cols, (int)eb, st, nb), what);
+    return cuda_status(launch_transpose(src, wb + dst_off, rows, cols, (int)eb, st, nmat), what);
   };
 #define TSP_TRY(expr)              \
   do {                             \
@@ -649,10 +651,39 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   // attention core backward
   const void* v_nat = sv + A.v;
   if (use_tc_attention(p)) {
-    TSP_TRY(tr(sv + A.v, L.vnat, p->head_dim, p->seq, "transpose V^T"));
+    TSP_TRY(tr(sv + A.v, L.vnat, p->head_dim, p->seq, "transpose V^T", batch * p->heads));
     v_nat = wb + L.vnat;
   }
-  {
+  if (attn_bwd_tc_supported(p->head_dim, p->chunk)) {
+    TSP_TRY(tr(sv + A.qz, L.qT, T, h, "transpose Q"));
+    TSP_TRY(tr(wb + L.doz, L.doT, T, h, "transpose dO"));
+    TSP_TRY(tr(sv + A.k, L.kT, p->seq, p->head_dim, "transpose K", batch * p->heads));
+    Prof pr("attention bwd", st);
+    TSP_TRY(cuda_status(launch_attn_dsum(sv + A.oz, wb + L.doz, reinterpret_cast<float*>(wb + L.dsum), p->D, batch,
+                                         p->heads, p->seq, p->chunk, st),
+                        "attention dsum"));
+    AttnBwdTcArgs ab;
+    ab.q = sv + A.qz;
+    ab.k = sv + A.k;
+    ab.v = v_nat;
+    ab.dO = wb + L.doz;
+    ab.qT = wb + L.qT;
+    ab.dOT = wb + L.doT;
+    ab.kT = wb + L.kT;
+    ab.lse = reinterpret_cast<const float*>(sv + A.lse);
+    ab.dsum = reinterpret_cast<const float*>(wb + L.dsum);
+    ab.dq = wb + L.dq;
+    ab.dk = wb + L.dk;
+    ab.dv = wb + L.dv;
+    ab.D = p->D;
+    ab.B = batch;
+    ab.H = p->heads;
+    ab.dh = p->head_dim;
+    ab.S = p->seq;
+    ab.C = p->chunk;
+    s = attn_bwd_bf16_tc(ab, st);
+    if (s != TSP_OK) return fail(s, "attention backward (tensor cores) failed: %s", tsp_status_string(s));
+  } else {
     AttnBwdParams ab;
     ab.q = sv + A.qz;
     ab.k = sv + A.k;
@@ -676,10 +707,12 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     }
     if (s != TSP_OK) return fail(s, "attention backward failed: %s", tsp_status_string(s));
   }
-  Prof pr_asm("assemble dQKV", st);
-  TSP_TRY(cuda_status(launch_assemble_dqkv(wb + L.dq, wb + L.dk, wb + L.dv, wb + L.dqkv, p->D, batch, p->seq,
-                                           p->heads, p->head_dim, st),
-                      "assemble dQKV"));
+  {
+    Prof pr_asm("assemble dQKV", st);
+    TSP_TRY(cuda_status(launch_assemble_dqkv(wb + L.dq, wb + L.dk, wb + L.dv, wb + L.dqkv, p->D, batch, p->seq,
+                                             p->heads, p->head_dim, st),
+                        "assemble dQKV"));
+  }
   TSP_TRY(tr(w->qkv, L.wqkv_T, 3 * h, h, "transpose W_QKV"));
   {
     EpiParams e = base_epi(p, batch);

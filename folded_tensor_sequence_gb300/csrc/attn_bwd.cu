@@ -374,6 +374,16 @@ __global__ void __launch_bounds__(BT) attn_dq_kernel(AttnBwdParams p, int n_tile
 
 }  // namespace
 
+cudaError_t launch_attn_dsum(const void* o, const void* dO, float* dsum, int D, int B, int H, int64_t S, int64_t C,
+                             cudaStream_t stream) {
+  const int64_t rows = (int64_t)B * H * S;
+  if (rows == 0) return cudaSuccess;
+  dsum_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                              static_cast<const __nv_bfloat16*>(dO), dsum, D, B, H,
+                                                              S, C);
+  return cudaGetLastError();
+}
+
 tsp_status attn_bwd_bf16(const AttnBwdParams& p, cudaStream_t stream) {
   if (p.dh != DH) return TSP_ERR_UNSUPPORTED;
   if (p.B * p.S == 0) return TSP_OK;

@@ -1,0 +1,668 @@
+// Causal flash-attention backward on the 5th-generation tensor cores
+// (tcgen05 + TMEM), head_dim 128, bf16 in, fp32 accumulation.
+//
+// Exact gradient of the forward (the TSP posts do not describe a backward):
+//   P = exp(S/sqrt(dh) - lse),  dP = dO V^T,  dS = P * (dP - rowsum(dO * O)),
+//   dV = P^T dO,  dK = dS^T Q / sqrt(dh),  dQ = dS K / sqrt(dh).
+// Two kernels, no atomics; every tensor-core operand is K-major and arrives
+// by TMA:
+//   dK/dV: one CTA per mirror pair of 128-key tiles (j, nk-1-j: together they
+//     see a constant number of query blocks).  K and V of the tile stay in
+//     shared memory; query blocks of 64 stream through a 2-stage ring holding
+//     Q, dO (for S^T = K Q^T, dP^T = V dO^T) and their transposes Q^T, dO^T
+//     (for dV += P^T dO, dK += dS^T Q).  TMEM: S^T and dP^T double-buffered
+//     (4 x 64 columns), dV and dK accumulators (2 x 128 columns).
+//   dQ: one CTA per mirror pair of 128-query tiles (the forward's zigzag
+//     pairing: both tiles on the same rank).  Q and dO stay in shared memory;
+//     key blocks of 64 stream K, V (for S = Q K^T, dP = dO V^T) and K^T (for
+//     dQ += dS K).  TMEM: S and dP double-buffered, dQ accumulator.
+// In both, warps 0-3 turn scores into P and dS (one TMEM lane = one row per
+// thread) and write them as bf16 in the 128-byte-swizzled layout the MMA
+// reads, warp 4 issues TMA, warp 5 issues tcgen05.mma from one thread; the
+// tensor core computes block i+1's scores while the elementwise warps work on
+// block i.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tsp {
+
+namespace {
+
+constexpr int HD = 128;
+constexpr int THREADS = 192;
+constexpr uint32_t SUB64 = 64 * 64 * 2;     // [64 rows][64 cols] bf16, 8 KB
+constexpr uint32_t SUB128 = 128 * 64 * 2;   // [128 rows][64 cols] bf16, 16 KB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned CODE_DKDV = KID_ATTN_BWD << 8;
+constexpr unsigned CODE_DQ = (KID_ATTN_BWD << 8) | 0x80;
+
+struct BwdTcParams {
+  int B, H, D;
+  int64_t S, C;
+  int h;
+  const float* lse;   // [B][H][S], natural log
+  const float* dsum;  // [B][H][S]
+  __nv_bfloat16* dq;  // zigzag [T][h]
+  __nv_bfloat16* dk;  // [B][H][S][dh]
+  __nv_bfloat16* dv;
+  unsigned int* err;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ int64_t zz_row(int64_t pos, int64_t C, int D, int B, int b) {
+  const int64_t c = pos / C, off = pos - c * C;
+  const int64_t r = c < D ? c : 2 * D - 1 - c;
+  return (r * B + b) * 2 * C + (c < D ? off : C + off);
+}
+
+// Writes 64 bf16 values (one row of a [rows][64] swizzled K-major sub-tile).
+__device__ __forceinline__ void store_row64(uint8_t* sub, int row, const float (&v)[64]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 pk = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                                pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+    *reinterpret_cast<uint4*>(sub + row * 128 + ((q ^ (row & 7)) << 4)) = pk;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  float a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = a[i];
+    v[32 + i] = b[i];
+  }
+}
+
+// ===========================================================================
+// dK, dV
+// ===========================================================================
+constexpr int KB_QB = 64;  // queries per block
+constexpr uint32_t KV_STAGE_BYTES = 4 * SUB64 + 2 * SUB128;  // Q, dO (2 sub each) + Q^T, dO^T
+constexpr size_t DKDV_SMEM = 1024 + 2 * 2 * SUB128 + 2 * (size_t)KV_STAGE_BYTES + 2 * SUB128 + 256;
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                        const __grid_constant__ CUtensorMap tmQT, const __grid_constant__ CUtensorMap tmdOT,
+                        const BwdTcParams p, int nk) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ks = smem;                    // 2 x SUB128
+  uint8_t* Vs = smem + 2 * SUB128;       // 2 x SUB128
+  uint8_t* stg = smem + 4 * SUB128;      // [2] stages
+  uint8_t* Pt = stg + 2 * KV_STAGE_BYTES;
+  uint8_t* dSt = Pt + SUB128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dSt + SUB128);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_free = bars + 1;
+  uint64_t* q_full = bars + 2;   // [2]
+  uint64_t* q_free = bars + 4;   // [2]
+  uint64_t* s_full = bars + 6;   // [2]
+  uint64_t* ds_full = bars + 8;
+  uint64_t* pds_free = bars + 9;
+  uint64_t* o_done = bars + 10;
+  uint64_t* drain = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int head = blockIdx.y, b = blockIdx.z;
+  const int64_t bh = (int64_t)b * p.H + head;
+  auto tile_of = [&](int t) { return t == 0 ? (int)blockIdx.x : nk - 1 - (int)blockIdx.x; };
+  const int ntile = (nk - 1 - (int)blockIdx.x == (int)blockIdx.x) ? 1 : 2;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_free, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_free[s], 1);
+      mbar_init(&s_full[s], 1);
+    }
+    mbar_init(ds_full, 128);
+    mbar_init(pds_free, 1);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmQT);
+    tma_prefetch_desc(&tmdOT);
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // TMEM columns: S^T[x] at 64x, dP^T[x] at 128 + 64x, dV at 256, dK at 384
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t qi = 0;
+      int kv_armed = 0;
+      bool ok = true;
+      for (int t = 0; t < ntile && ok; ++t) {
+        const int kt = tile_of(t);
+        const int64_t k0 = (int64_t)kt * 128;
+        if (!mbar_wait(kv_free, (t & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 1)) break;
+        mbar_arrive_expect_tx(kv_full, 4 * SUB128);
+        ++kv_armed;
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(Ks + c * SUB128, &tmK, c * 64, (int)(bh * p.S + k0), kv_full);
+          tma_load_2d(Vs + c * SUB128, &tmV, c * 64, (int)(bh * p.S + k0), kv_full);
+        }
+        const int nq = (int)((p.S - k0) / KB_QB);
+        for (int i = 0; i < nq; ++i, ++qi) {
+          const int s = qi & 1;
+          if (!mbar_wait(&q_free[s], ((qi >> 1) & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 2)) {
+            ok = false;
+            break;
+          }
+          const int64_t zr = zz_row(k0 + (int64_t)i * KB_QB, p.C, p.D, p.B, b);
+          uint8_t* st = stg + s * KV_STAGE_BYTES;
+          mbar_arrive_expect_tx(&q_full[s], KV_STAGE_BYTES);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(st + c * SUB64, &tmQ, head * HD + c * 64, (int)zr, &q_full[s]);
+            tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmdO, head * HD + c * 64, (int)zr, &q_full[s]);
+          }
+          tma_load_2d(st + 4 * SUB64, &tmQT, (int)zr, head * HD, &q_full[s]);
+          tma_load_2d(st + 4 * SUB64 + SUB128, &tmdOT, (int)zr, head * HD, &q_full[s]);
+        }
+      }
+      volatile int dummy = 0;
+      const uint32_t first = qi > 2 ? qi - 2 : 0;
+      for (uint32_t n = first; n < qi; ++n) mbar_wait(&q_full[n & 1], (n >> 1) & 1, &dummy, p.err, CODE_DKDV | 3);
+      if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_DKDV | 3);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, KB_QB);  // M = keys, N = queries
+      constexpr uint32_t id_o = idesc_bf16_f32(128, HD);     // M = keys, N = head dim
+      uint32_t qi = 0, scnt0 = 0, scnt1 = 0;
+      bool ok = true;
+      auto scores = [&](uint32_t n, int x) {  // S^T = K Q^T, dP^T = V dO^T for query block n
+        uint8_t* st = stg + (n & 1) * KV_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
+          const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
+          umma_bf16(tmem_base + 64 * x, ak, bq, id_s, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
+          const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
+          umma_bf16(tmem_base + 128 + 64 * x, av, bo, id_s, k > 0);
+        }
+        umma_commit(&s_full[x]);
+      };
+      auto accumulate = [&](uint32_t n, bool acc) {  // dV += P^T dO, dK += dS^T Q for query block n
+        uint8_t* st = stg + (n & 1) * KV_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < KB_QB / 16; ++k) {
+          const uint64_t ap = sdesc_kmajor_sw128(smem_u32(Pt)) + 2 * k;
+          const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64 + SUB128)) + 2 * k;
+          umma_bf16(tmem_base + 256, ap, bo, id_o, (acc || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < KB_QB / 16; ++k) {
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(dSt)) + 2 * k;
+          const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
+          umma_bf16(tmem_base + 384, ad, bq, id_o, (acc || k > 0) ? 1u : 0u);
+        }
+        umma_commit(pds_free);
+        umma_commit(&q_free[n & 1]);
+      };
+      uint32_t dscnt = 0;
+      for (int t = 0; t < ntile && ok; ++t) {
+        const int64_t k0 = (int64_t)tile_of(t) * 128;
+        const int nq = (int)((p.S - k0) / KB_QB);
+        if (!mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_DKDV | 4)) break;
+        for (int i = 0; i < nq; ++i) {
+          const uint32_t n = qi + i;
+          if (!mbar_wait(&q_full[n & 1], (n >> 1) & 1, abort_flag, p.err, CODE_DKDV | 5)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          scores(n, i & 1);
+          if (i & 1) ++scnt1; else ++scnt0;
+          if (i > 0) {
+            if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DKDV | 6)) {
+              ok = false;
+              break;
+            }
+            ++dscnt;
+            tc_fence_after();
+            accumulate(n - 1, i - 1 > 0);
+          }
+        }
+        if (!ok) break;
+        if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DKDV | 6)) break;
+        ++dscnt;
+        tc_fence_after();
+        accumulate(qi + nq - 1, nq - 1 > 0);
+        umma_commit(o_done);
+        umma_commit(kv_free);
+        qi += nq;
+      }
+      (void)scnt0;
+      (void)scnt1;
+      umma_commit(drain);
+      volatile int dummy = 0;
+      mbar_wait(drain, 0, &dummy, p.err, CODE_DKDV | 7);
+    }
+  } else {
+    // ---------------- elementwise warps 0-3: one key row per thread ----------------
+    const int row = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = kLog2e * rsqrtf((float)HD);
+    const float scale = rsqrtf((float)HD);
+    const float* lse_bh = p.lse + bh * p.S;
+    const float* ds_bh = p.dsum + bh * p.S;
+    uint32_t scnt[2] = {0, 0};
+    uint32_t freecnt = 0;
+    bool alive = true;
+    for (int t = 0; t < ntile && alive; ++t) {
+      const int64_t k0 = (int64_t)tile_of(t) * 128;
+      const int nq = (int)((p.S - k0) / KB_QB);
+      const int64_t key = k0 + row;
+      for (int i = 0; i < nq; ++i) {
+        const int x = i & 1;
+        const bool got = mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DKDV | 8);
+        ++scnt[x];
+        if (!__all_sync(0xffffffffu, got)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[64], dp[64];
+        tmem_ld64(tmem_base + lane_off + 64 * x, sv);
+        tmem_ld64(tmem_base + lane_off + 128 + 64 * x, dp);
+        const int64_t q0 = k0 + (int64_t)i * KB_QB;
+        const bool diag = i < 2;
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_bh + q0) + c4);
+          const float4 d4 = __ldg(reinterpret_cast<const float4*>(ds_bh + q0) + c4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 * 4 + e;
+            float pv = ex2f(fmaf(sv[c], sl2, -lv[e] * kLog2e));
+            if (diag && q0 + c < key) pv = 0.f;
+            sv[c] = pv;
+            dp[c] = pv * (dp[c] - dv4[e]);
+          }
+        }
+        // P^T and dS^T smem must be free of the previous block's MMAs
+        const bool fr = mbar_wait(pds_free, (freecnt & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 9);
+        ++freecnt;
+        if (!__all_sync(0xffffffffu, fr)) {
+          alive = false;
+          break;
+        }
+        store_row64(Pt, row, sv);
+        store_row64(dSt, row, dp);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!alive) break;
+      const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DKDV | 10);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bh * p.S + key) * HD);
+      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bh * p.S + key) * HD);
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        float a[32], d[32];
+        tmem_ld32(tmem_base + lane_off + 256 + 32 * c32, a);
+        tmem_ld32(tmem_base + lane_off + 384 + 32 * c32, d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dvrow[c32 * 4 + q] = make_uint4(pack_bf16x2(a[q * 8 + 0], a[q * 8 + 1]), pack_bf16x2(a[q * 8 + 2], a[q * 8 + 3]),
+                                          pack_bf16x2(a[q * 8 + 4], a[q * 8 + 5]), pack_bf16x2(a[q * 8 + 6], a[q * 8 + 7]));
+          dkrow[c32 * 4 + q] = make_uint4(
+              pack_bf16x2(d[q * 8 + 0] * scale, d[q * 8 + 1] * scale), pack_bf16x2(d[q * 8 + 2] * scale, d[q * 8 + 3] * scale),
+              pack_bf16x2(d[q * 8 + 4] * scale, d[q * 8 + 5] * scale), pack_bf16x2(d[q * 8 + 6] * scale, d[q * 8 + 7] * scale));
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ===========================================================================
+// dQ
+// ===========================================================================
+constexpr int DQ_KB = 64;  // keys per block
+constexpr uint32_t DQ_STAGE_BYTES = 4 * SUB64 + SUB128;  // K, V (2 sub each) + K^T
+constexpr size_t DQ_SMEM = 1024 + 4 * (size_t)SUB128 + 2 * (size_t)DQ_STAGE_BYTES + SUB128 + 256;
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmKT, const BwdTcParams p, int n_tiles) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Qs = smem;                  // 2 x SUB128
+  uint8_t* dOs = smem + 2 * SUB128;    // 2 x SUB128
+  uint8_t* stg = smem + 4 * SUB128;    // [2] stages
+  uint8_t* dSs = stg + 2 * DQ_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dSs + SUB128);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_free = bars + 1;
+  uint64_t* k_full = bars + 2;   // [2]
+  uint64_t* k_free = bars + 4;   // [2]
+  uint64_t* s_full = bars + 6;   // [2]
+  uint64_t* ds_full = bars + 8;
+  uint64_t* ds_free = bars + 9;
+  uint64_t* o_done = bars + 10;
+  uint64_t* drain = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int head = blockIdx.y, b = blockIdx.z;
+  const int64_t bh = (int64_t)b * p.H + head;
+  const int total_tiles = 2 * p.D * n_tiles;
+  auto tile_of = [&](int t) { return t == 0 ? total_tiles - 1 - (int)blockIdx.x : (int)blockIdx.x; };
+  auto geo = [&](int g, int64_t& zrow0, int64_t& p0) {
+    const int c = g / n_tiles, i = g % n_tiles;
+    const int64_t r = c < p.D ? c : 2 * p.D - 1 - c;
+    const int64_t off = (int64_t)i * 128;
+    zrow0 = (r * p.B + b) * 2 * p.C + (c < p.D ? off : p.C + off);
+    p0 = (int64_t)c * p.C + off;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_free[s], 1);
+      mbar_init(&s_full[s], 1);
+    }
+    mbar_init(ds_full, 128);
+    mbar_init(ds_free, 1);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmKT);
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // TMEM columns: S[x] at 64x, dP[x] at 128 + 64x, dQ at 256
+
+  if (warp == 4) {
+    if (lane == 0) {
+      uint32_t ki = 0;
+      int q_armed = 0;
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t) {
+        int64_t zrow0, p0;
+        geo(tile_of(t), zrow0, p0);
+        if (!mbar_wait(q_free, (t & 1) ^ 1, abort_flag, p.err, CODE_DQ | 1)) break;
+        mbar_arrive_expect_tx(q_full, 4 * SUB128);
+        ++q_armed;
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(Qs + c * SUB128, &tmQ, head * HD + c * 64, (int)zrow0, q_full);
+          tma_load_2d(dOs + c * SUB128, &tmdO, head * HD + c * 64, (int)zrow0, q_full);
+        }
+        const int nkb = (int)((p0 + 128) / DQ_KB);
+        for (int j = 0; j < nkb; ++j, ++ki) {
+          const int s = ki & 1;
+          if (!mbar_wait(&k_free[s], ((ki >> 1) & 1) ^ 1, abort_flag, p.err, CODE_DQ | 2)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = stg + s * DQ_STAGE_BYTES;
+          mbar_arrive_expect_tx(&k_full[s], DQ_STAGE_BYTES);
+          const int krow = (int)(bh * p.S + (int64_t)j * DQ_KB);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(st + c * SUB64, &tmK, c * 64, krow, &k_full[s]);
+            tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmV, c * 64, krow, &k_full[s]);
+          }
+          tma_load_2d(st + 4 * SUB64, &tmKT, j * DQ_KB, (int)(bh * HD), &k_full[s]);
+        }
+      }
+      volatile int dummy = 0;
+      const uint32_t first = ki > 2 ? ki - 2 : 0;
+      for (uint32_t n = first; n < ki; ++n) mbar_wait(&k_full[n & 1], (n >> 1) & 1, &dummy, p.err, CODE_DQ | 3);
+      if (q_armed) mbar_wait(q_full, (q_armed - 1) & 1, &dummy, p.err, CODE_DQ | 3);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, DQ_KB);
+      constexpr uint32_t id_o = idesc_bf16_f32(128, HD);
+      uint32_t ki = 0, dscnt = 0;
+      bool ok = true;
+      auto scores = [&](uint32_t n, int x) {  // S = Q K^T, dP = dO V^T for key block n
+        uint8_t* st = stg + (n & 1) * DQ_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t aq = sdesc_kmajor_sw128(smem_u32(Qs + (k / 4) * SUB128)) + 2 * (k % 4);
+          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
+          umma_bf16(tmem_base + 64 * x, aq, bk, id_s, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t ao = sdesc_kmajor_sw128(smem_u32(dOs + (k / 4) * SUB128)) + 2 * (k % 4);
+          const uint64_t bv = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
+          umma_bf16(tmem_base + 128 + 64 * x, ao, bv, id_s, k > 0);
+        }
+        umma_commit(&s_full[x]);
+      };
+      auto accumulate = [&](uint32_t n, bool acc) {  // dQ += dS K for key block n
+        uint8_t* st = stg + (n & 1) * DQ_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < DQ_KB / 16; ++k) {
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(dSs)) + 2 * k;
+          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
+          umma_bf16(tmem_base + 256, ad, bk, id_o, (acc || k > 0) ? 1u : 0u);
+        }
+        umma_commit(ds_free);
+        umma_commit(&k_free[n & 1]);
+      };
+      for (int t = 0; t < 2 && ok; ++t) {
+        int64_t zrow0, p0;
+        geo(tile_of(t), zrow0, p0);
+        const int nkb = (int)((p0 + 128) / DQ_KB);
+        if (!mbar_wait(q_full, t & 1, abort_flag, p.err, CODE_DQ | 4)) break;
+        for (int j = 0; j < nkb; ++j) {
+          const uint32_t n = ki + j;
+          if (!mbar_wait(&k_full[n & 1], (n >> 1) & 1, abort_flag, p.err, CODE_DQ | 5)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          scores(n, j & 1);
+          if (j > 0) {
+            if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DQ | 6)) {
+              ok = false;
+              break;
+            }
+            ++dscnt;
+            tc_fence_after();
+            accumulate(n - 1, j - 1 > 0);
+          }
+        }
+        if (!ok) break;
+        if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DQ | 6)) break;
+        ++dscnt;
+        tc_fence_after();
+        accumulate(ki + nkb - 1, nkb - 1 > 0);
+        umma_commit(o_done);
+        umma_commit(q_free);
+        ki += nkb;
+      }
+      umma_commit(drain);
+      volatile int dummy = 0;
+      mbar_wait(drain, 0, &dummy, p.err, CODE_DQ | 7);
+    }
+  } else {
+    const int row = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = kLog2e * rsqrtf((float)HD);
+    const float scale = rsqrtf((float)HD);
+    uint32_t scnt[2] = {0, 0};
+    uint32_t freecnt = 0;
+    bool alive = true;
+    for (int t = 0; t < 2 && alive; ++t) {
+      int64_t zrow0, p0;
+      geo(tile_of(t), zrow0, p0);
+      const int nkb = (int)((p0 + 128) / DQ_KB);
+      const int64_t qpos = p0 + row;
+      const float l2 = p.lse[bh * p.S + qpos] * kLog2e;
+      const float dsr = p.dsum[bh * p.S + qpos];
+      for (int j = 0; j < nkb; ++j) {
+        const int x = j & 1;
+        const bool got = mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DQ | 8);
+        ++scnt[x];
+        if (!__all_sync(0xffffffffu, got)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[64], dp[64];
+        tmem_ld64(tmem_base + lane_off + 64 * x, sv);
+        tmem_ld64(tmem_base + lane_off + 128 + 64 * x, dp);
+        const int64_t key0 = (int64_t)j * DQ_KB;
+        const bool diag = key0 + DQ_KB - 1 > p0;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float pv = ex2f(fmaf(sv[c], sl2, -l2));
+          if (diag && key0 + c > qpos) pv = 0.f;
+          dp[c] = pv * (dp[c] - dsr);
+        }
+        const bool fr = mbar_wait(ds_free, (freecnt & 1) ^ 1, abort_flag, p.err, CODE_DQ | 9);
+        ++freecnt;
+        if (!__all_sync(0xffffffffu, fr)) {
+          alive = false;
+          break;
+        }
+        store_row64(dSs, row, dp);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!alive) break;
+      const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DQ | 10);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      uint4* dst = reinterpret_cast<uint4*>(p.dq + (zrow0 + row) * p.h + head * HD);
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        float a[32];
+        tmem_ld32(tmem_base + lane_off + 256 + 32 * c32, a);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[c32 * 4 + q] = make_uint4(
+              pack_bf16x2(a[q * 8 + 0] * scale, a[q * 8 + 1] * scale), pack_bf16x2(a[q * 8 + 2] * scale, a[q * 8 + 3] * scale),
+              pack_bf16x2(a[q * 8 + 4] * scale, a[q * 8 + 5] * scale), pack_bf16x2(a[q * 8 + 6] * scale, a[q * 8 + 7] * scale));
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace
+
+bool attn_bwd_tc_supported(int head_dim, int64_t chunk) { return head_dim == HD && chunk % 128 == 0; }
+
+tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream) {
+  if (!attn_bwd_tc_supported(a.dh, a.C)) return TSP_ERR_UNSUPPORTED;
+  if ((int64_t)a.B * a.S == 0) return TSP_OK;
+  const int64_t T = (int64_t)a.B * a.S;
+  const int h = a.H * HD;
+  const int64_t kv_rows = (int64_t)a.B * a.H * a.S;
+  CUtensorMap mK128, mV128, mQ64, mdO64, mQT, mdOT, mQ128, mdO128, mK64, mV64, mKT;
+  if (!make_tma_2d_bf16(&mK128, a.k, kv_rows, HD, HD, 128) || !make_tma_2d_bf16(&mV128, a.v, kv_rows, HD, HD, 128) ||
+      !make_tma_2d_bf16(&mQ64, a.q, T, h, h, 64) || !make_tma_2d_bf16(&mdO64, a.dO, T, h, h, 64) ||
+      !make_tma_2d_bf16(&mQT, a.qT, h, T, T, 128) || !make_tma_2d_bf16(&mdOT, a.dOT, h, T, T, 128) ||
+      !make_tma_2d_bf16(&mQ128, a.q, T, h, h, 128) || !make_tma_2d_bf16(&mdO128, a.dO, T, h, h, 128) ||
+      !make_tma_2d_bf16(&mK64, a.k, kv_rows, HD, HD, 64) || !make_tma_2d_bf16(&mV64, a.v, kv_rows, HD, HD, 64) ||
+      !make_tma_2d_bf16(&mKT, a.kT, (int64_t)a.B * a.H * HD, a.S, a.S, 128))
+    return TSP_ERR_CUDA;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(attn_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DKDV_SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
+            cudaSuccess)
+      return TSP_ERR_CUDA;
+    configured = true;
+  }
+  BwdTcParams p;
+  p.B = a.B;
+  p.H = a.H;
+  p.D = a.D;
+  p.S = a.S;
+  p.C = a.C;
+  p.h = h;
+  p.lse = a.lse;
+  p.dsum = a.dsum;
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.err = dev_error_word();
+  const int nk = (int)(a.S / 128);
+  dim3 g1((nk + 1) / 2, a.H, a.B);
+  attn_dkdv_tc_kernel<<<g1, THREADS, DKDV_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, mQT, mdOT, p, nk);
+  if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
+  const int n_tiles = (int)(a.C / 128);
+  dim3 g2(a.D * n_tiles, a.H, a.B);
+  attn_dq_tc_kernel<<<g2, THREADS, DQ_SMEM, stream>>>(mQ128, mdO128, mK64, mV64, mKT, p, n_tiles);
+  return cudaGetLastError() == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
+}
+
+}  // namespace tsp

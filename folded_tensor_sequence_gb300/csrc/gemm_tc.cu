@@ -39,19 +39,23 @@ constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
-constexpr int GROUP_M = 16;
+// Raster: tiles are visited in bands of group_m m-tiles (all n-tiles of a band
+// before the next band), group_m chosen so one band of A is ~32 MB and stays
+// in L2 while the B operand streams past it.
+constexpr size_t kBandBytes = size_t(32) << 20;
 constexpr uint32_t TMEM_COLS = 512;
 
 struct GemmShape {
   int M, N, K;
   int num_m, num_n, num_tiles, kblocks;
+  int group_m;
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmShape& s, int& mt, int& nt) {
-  const int per_group = GROUP_M * s.num_n;
+  const int per_group = s.group_m * s.num_n;
   const int group = t / per_group;
-  const int first_m = group * GROUP_M;
-  const int gsz = min(s.num_m - first_m, GROUP_M);
+  const int first_m = group * s.group_m;
+  const int gsz = min(s.num_m - first_m, s.group_m);
   const int in_g = t - group * per_group;
   mt = first_m + in_g % gsz;
   nt = in_g / gsz;
@@ -384,6 +388,11 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   s.num_n = N / BN;
   s.num_tiles = s.num_m * s.num_n;
   s.kblocks = K / BK;
+  {
+    const size_t band_rows = kBandBytes / ((size_t)K * 2);
+    int gm = (int)(band_rows / BM);
+    s.group_m = gm < 1 ? 1 : (gm > s.num_m ? s.num_m : gm);
+  }
   cudaError_t e;
   switch (epi) {
     case EPI_STORE: e = launch_epi<EPI_STORE>(ta, tb, s, ep, stream); break;

@@ -105,6 +105,30 @@ struct AttnBwdParams {
   int64_t S, C;
 };
 tsp_status attn_bwd_bf16(const AttnBwdParams& p, cudaStream_t stream);
+// dsum[b][head][p] = rowsum(dO * O) (fp32), the softmax-Jacobian row term of the backward.
+cudaError_t launch_attn_dsum(const void* o, const void* dO, float* dsum, int D, int B, int H, int64_t S, int64_t C,
+                             cudaStream_t stream);
+
+// tcgen05 attention backward (head_dim 128, chunk % 128 == 0): needs the
+// transposed copies qT, dOT ([h][T], zigzag token columns) and kT ([B][H][dh][S]).
+struct AttnBwdTcArgs {
+  const void* q;    // zigzag [T][h]
+  const void* k;    // [B][H][S][dh]
+  const void* v;    // [B][H][S][dh]
+  const void* dO;   // zigzag [T][h]
+  const void* qT;   // [h][T]
+  const void* dOT;  // [h][T]
+  const void* kT;   // [B][H][dh][S]
+  const float* lse;
+  const float* dsum;
+  void* dq;
+  void* dk;
+  void* dv;
+  int D, B, H, dh;
+  int64_t S, C;
+};
+bool attn_bwd_tc_supported(int head_dim, int64_t chunk);
+tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream);
 
 // Backward helpers.
 cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
