@@ -62,6 +62,45 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Causal mask of the diagonal key tile: column c (key) > row (query) -> -inf.
+__device__ __forceinline__ void mask_half(uint32_t (&h)[64], int c0, int row) {
+#pragma unroll
+  for (int c = 0; c < 64; ++c)
+    if (c0 + c > row) h[c] = __float_as_uint(-INFINITY);
+}
+
+// Max of 64 values through 8 independent chains and a tree.
+__device__ __forceinline__ float max_half(const uint32_t (&h)[64]) {
+  float m[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) m[t] = __uint_as_float(h[t]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) m[t] = fmaxf(m[t], __uint_as_float(h[i * 8 + t]));
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+// p = 2^(s * sl2 - m) for 64 scores, written as bf16 to one [128][64]
+// swizzled K-major sub-tile row; returns the fp32 sum of p.
+__device__ __forceinline__ float exp_store_half(const uint32_t (&h)[64], uint8_t* sub, int row, float sl2,
+                                                float neg_m) {
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    float e[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      e[t] = ex2f(fmaf(__uint_as_float(h[q * 8 + t]), sl2, neg_m));
+      acc[t] += e[t];
+    }
+    const uint4 pk = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
+                                pack_bf16x2(e[6], e[7]));
+    *reinterpret_cast<uint4*>(sub + row * 128 + ((q ^ (row & 7)) << 4)) = pk;
+  }
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+}
+
 struct BlockGeo {
   int64_t zrow0;  // zigzag row of the block's first query
   int64_t p0;     // global position of the block's first query
@@ -289,52 +328,59 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld128(tS, sr);
         const bool diag = (j == n - 1);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float v = __uint_as_float(sr[c]);
-          if (diag && c > row) v = -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-        const float m_new = mx * sl2;
-        const bool need = m_new > m_used + kRescaleThreshold;
-        const float factor = need ? ex2f(m_used - m_new) : 1.0f;
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // Columns 0-63 are loaded and waited; columns 64-127 load while the
+        // first half is exponentiated.  Exponentials use the running max from
+        // earlier key tiles (speculation); only if this tile raises the max by
+        // more than the threshold are O rescaled and P recomputed from S.
+        uint32_t h0[64], h1[64];
+        tmem_ld64_issue(tS, h0);
+        tmem_wait_ld64(h0);
+        tmem_ld64_issue(tS + 64, h1);
+        if (diag) mask_half(h0, 0, row);
+        float sum = 0.f;
+        if (j == 0) {
+          tmem_wait_ld64(h1);
+          if (diag) mask_half(h1, 64, row);
+          m_used = fmaxf(max_half(h0), max_half(h1)) * sl2;
+          sum = exp_store_half(h0, Pbuf, row, sl2, -m_used) + exp_store_half(h1, Pbuf + SUB_BYTES, row, sl2, -m_used);
+        } else {
+          const float mx0 = max_half(h0);
+          const float s0 = exp_store_half(h0, Pbuf, row, sl2, -m_used);
+          tmem_wait_ld64(h1);
+          if (diag) mask_half(h1, 64, row);
+          const float mx1 = max_half(h1);
+          const float s1 = exp_store_half(h1, Pbuf + SUB_BYTES, row, sl2, -m_used);
+          sum = s0 + s1;
+          const float m_new = fmaxf(mx0, mx1) * sl2;
+          const bool need = m_new > m_used + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float factor = need ? ex2f(m_used - m_new) : 1.0f;
 #pragma unroll 1
-          for (int c4 = 0; c4 < 4; ++c4) {
-            float ov[32];
-            uint32_t part[32];
-            tmem_ld32(tO + c4 * 32, ov);
+            for (int c4 = 0; c4 < 4; ++c4) {
+              float ov[32];
+              uint32_t part[32];
+              tmem_ld32(tO + c4 * 32, ov);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) part[c] = __float_as_uint(ov[c] * factor);
-            tmem_st32(tO + c4 * 32, part);
+              for (int c = 0; c < 32; ++c) part[c] = __float_as_uint(ov[c] * factor);
+              tmem_st32(tO + c4 * 32, part);
+            }
+            if (need) {
+              l *= factor;
+              m_used = m_new;
+            }
+            tmem_ld64_issue(tS, h0);
+            tmem_wait_ld64(h0);
+            tmem_ld64_issue(tS + 64, h1);
+            tmem_wait_ld64(h1);
+            if (diag) {
+              mask_half(h0, 0, row);
+              mask_half(h1, 64, row);
+            }
+            sum = exp_store_half(h0, Pbuf, row, sl2, -m_used) + exp_store_half(h1, Pbuf + SUB_BYTES, row, sl2, -m_used);
           }
         }
-        if (need) {
-          l *= factor;
-          m_used = m_new;
-        }
-        const float neg_m = -m_used;
-        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          float e[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) e[t] = ex2f(fmaf(__uint_as_float(sr[q * 8 + t]), sl2, neg_m));
-          ls0 += e[0] + e[4];
-          ls1 += e[1] + e[5];
-          ls2 += e[2] + e[6];
-          ls3 += e[3] + e[7];
-          const uint4 pk = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
-                                      pack_bf16x2(e[6], e[7]));
-          const int sub = q >> 3, cc = q & 7;
-          *reinterpret_cast<uint4*>(Pbuf + sub * SUB_BYTES + row * 128 + ((cc ^ (row & 7)) << 4)) = pk;
-        }
-        l += (ls0 + ls1) + (ls2 + ls3);
+        l += sum;
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[x]);
