@@ -15,13 +15,14 @@
 // of the same rank, so every CTA does the same number of key tiles.
 //
 // Per CTA: warp 8 issues TMA loads (Q tiles, then K_j / V_j^T tiles through a
-// 3-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
+// 5-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
 // are the softmax warpgroups of tiles A and B.  TMEM (512 columns): S_A, S_B,
 // O_A, O_B, 128 fp32 columns each.  Issue order per key tile j:
 //   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 // so the tensor core works on one tile while the other tile's softmax runs.
-// P = exp2(S*log2e/sqrt(dh) - m) is written as bf16 to shared memory in the
-// 128-byte-swizzled K-major layout the MMA reads.  The running max is only
+// P = exp2(S*log2e/sqrt(dh) - m) is written as packed bf16 back into the first
+// 64 columns of S's TMEM and consumed from there by the PV MMA (A operand in
+// tensor memory), which leaves shared memory to a 5-deep K/V^T ring.  The running max is only
 // raised (and O rescaled in TMEM) when it grows by more than 2^8, which keeps
 // P <= 256 and makes the rescale rare.
 #include "common.cuh"
@@ -34,11 +35,11 @@ namespace {
 constexpr int QT = 128;    // rows per query tile (MMA M)
 constexpr int KT = 128;    // keys per key tile
 constexpr int HD = 128;    // head dim
-constexpr int STAGES = 3;  // K / V^T tile ring
+constexpr int STAGES = 5;  // K / V^T tile ring
 constexpr int THREADS = 320;
 constexpr uint32_t SUB_BYTES = 128 * 64 * 2;     // one [128][64] bf16 swizzled sub-tile
 constexpr uint32_t TILE_BYTES = 2 * SUB_BYTES;   // [128][128]
-constexpr size_t SMEM_BYTES = 1024 + (2 + STAGES + 2) * (size_t)TILE_BYTES + 256;
+constexpr size_t SMEM_BYTES = 1024 + (2 + STAGES) * (size_t)TILE_BYTES + 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -56,10 +57,6 @@ __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Causal mask of the diagonal key tile: column c (key) > row (query) -> -inf.
@@ -81,22 +78,17 @@ __device__ __forceinline__ float max_half(const uint32_t (&h)[64]) {
   return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
-// p = 2^(s * sl2 - m) for 64 scores, written as bf16 to one [128][64]
-// swizzled K-major sub-tile row; returns the fp32 sum of p.
-__device__ __forceinline__ float exp_store_half(const uint32_t (&h)[64], uint8_t* sub, int row, float sl2,
-                                                float neg_m) {
+// p = 2^(s * sl2 - m) for 64 scores, packed as 32 bf16 pairs (low half =
+// even key); returns the fp32 sum of p.
+__device__ __forceinline__ float exp_pack_half(const uint32_t (&h)[64], uint32_t* pk, float sl2, float neg_m) {
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    float e[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      e[t] = ex2f(fmaf(__uint_as_float(h[q * 8 + t]), sl2, neg_m));
-      acc[t] += e[t];
-    }
-    const uint4 pk = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
-                                pack_bf16x2(e[6], e[7]));
-    *reinterpret_cast<uint4*>(sub + row * 128 + ((q ^ (row & 7)) << 4)) = pk;
+  for (int q = 0; q < 32; ++q) {
+    const float e0 = ex2f(fmaf(__uint_as_float(h[2 * q]), sl2, neg_m));
+    const float e1 = ex2f(fmaf(__uint_as_float(h[2 * q + 1]), sl2, neg_m));
+    acc[(2 * q) & 7] += e0;
+    acc[(2 * q + 1) & 7] += e1;
+    pk[q] = pack_bf16x2(e0, e1);
   }
   return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
@@ -125,8 +117,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = smem;                                   // [2] tiles
   uint8_t* KVs = smem + 2 * TILE_BYTES;                 // [STAGES] tiles
-  uint8_t* Ps = smem + (2 + STAGES) * TILE_BYTES;       // [2] tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + STAGES + 2) * TILE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + STAGES) * TILE_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* kv_full = bars + 2;             // [STAGES]
@@ -232,13 +223,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           umma_bf16(tmem_base + x * 128, a, bb, idesc, k > 0);
         }
       };
-      auto mma_pv = [&](int x, int s, bool acc) {  // O_x += P_x V, K = keys
-        const uint32_t pa = smem_u32(Ps + x * TILE_BYTES), vb = smem_u32(KVs + s * TILE_BYTES);
+      auto mma_pv = [&](int x, int s, bool acc) {  // O_x += P_x V, K = keys; P_x in TMEM (S_x columns 0-63)
+        const uint32_t vb = smem_u32(KVs + s * TILE_BYTES);
 #pragma unroll
         for (int k = 0; k < KT / 16; ++k) {
-          const uint64_t a = sdesc_kmajor_sw128(pa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
           const uint64_t bb = sdesc_kmajor_sw128(vb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-          umma_bf16(tmem_base + 256 + x * 128, a, bb, idesc, (acc || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + 256 + x * 128, tmem_base + x * 128 + 8 * k, bb, idesc, (acc || k > 0) ? 1u : 0u);
         }
       };
       auto wait_item = [&](uint32_t n) {
@@ -312,7 +302,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + x * 128;
     const uint32_t tO = tmem_base + lane_off + 256 + x * 128;
-    uint8_t* Pbuf = Ps + x * TILE_BYTES;
     const float sl2 = kLog2e * rsqrtf((float)HD);
     uint32_t scnt = 0;
     for (int blk = 0; blk < 2; ++blk) {
@@ -334,6 +323,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // earlier key tiles (speculation); only if this tile raises the max by
         // more than the threshold are O rescaled and P recomputed from S.
         uint32_t h0[64], h1[64];
+        uint32_t pk[64];  // P as packed bf16 pairs: column c holds keys 2c, 2c+1
         tmem_ld64_issue(tS, h0);
         tmem_wait_ld64(h0);
         tmem_ld64_issue(tS + 64, h1);
@@ -343,14 +333,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_wait_ld64(h1);
           if (diag) mask_half(h1, 64, row);
           m_used = fmaxf(max_half(h0), max_half(h1)) * sl2;
-          sum = exp_store_half(h0, Pbuf, row, sl2, -m_used) + exp_store_half(h1, Pbuf + SUB_BYTES, row, sl2, -m_used);
+          sum = exp_pack_half(h0, pk, sl2, -m_used) + exp_pack_half(h1, pk + 32, sl2, -m_used);
         } else {
           const float mx0 = max_half(h0);
-          const float s0 = exp_store_half(h0, Pbuf, row, sl2, -m_used);
+          const float s0 = exp_pack_half(h0, pk, sl2, -m_used);
           tmem_wait_ld64(h1);
           if (diag) mask_half(h1, 64, row);
           const float mx1 = max_half(h1);
-          const float s1 = exp_store_half(h1, Pbuf + SUB_BYTES, row, sl2, -m_used);
+          const float s1 = exp_pack_half(h1, pk + 32, sl2, -m_used);
           sum = s0 + s1;
           const float m_new = fmaxf(mx0, mx1) * sl2;
           const bool need = m_new > m_used + kRescaleThreshold;
@@ -369,6 +359,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               l *= factor;
               m_used = m_new;
             }
+            // S is still intact (P has not been written over it yet): recompute
             tmem_ld64_issue(tS, h0);
             tmem_wait_ld64(h0);
             tmem_ld64_issue(tS + 64, h1);
@@ -377,11 +368,16 @@ __global__ void __launch_bounds__(THREADS, 1)
               mask_half(h0, 0, row);
               mask_half(h1, 64, row);
             }
-            sum = exp_store_half(h0, Pbuf, row, sl2, -m_used) + exp_store_half(h1, Pbuf + SUB_BYTES, row, sl2, -m_used);
+            sum = exp_pack_half(h0, pk, sl2, -m_used) + exp_pack_half(h1, pk + 32, sl2, -m_used);
           }
         }
         l += sum;
-        fence_async_smem();
+        // P over S's first 64 columns; the next S MMA into this buffer is
+        // issued after the PV MMA that reads P, and tensor-core MMAs of one
+        // CTA execute in issue order.
+        tmem_st32_nowait(tS, pk);
+        tmem_st32_nowait(tS + 32, pk + 32);
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[x]);
       }
