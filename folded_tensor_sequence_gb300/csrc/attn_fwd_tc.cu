@@ -14,15 +14,15 @@
 // the mirror pair of blocks (G, 2D*nb-1-G), which lie in chunks c and 2D-1-c
 // of the same rank, so every CTA does the same number of key tiles.
 //
-// Per CTA: warp 8 issues TMA loads (Q tiles, then K_j / V_j^T tiles through a
-// 5-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
+// Per CTA: warp 8 issues TMA loads (both blocks' Q tiles up front, then K_j /
+// V_j^T tiles through a 3-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
 // are the softmax warpgroups of tiles A and B.  TMEM (512 columns): S_A, S_B,
 // O_A, O_B, 128 fp32 columns each.  Issue order per key tile j:
 //   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 // so the tensor core works on one tile while the other tile's softmax runs.
 // P = exp2(S*log2e/sqrt(dh) - m) is written as packed bf16 back into the first
 // 64 columns of S's TMEM and consumed from there by the PV MMA (A operand in
-// tensor memory), which leaves shared memory to a 5-deep K/V^T ring.  The running max is only
+// tensor memory), which leaves shared memory for double-buffered Q tiles.  The running max is only
 // raised (and O rescaled in TMEM) when it grows by more than 2^8, which keeps
 // P <= 256 and makes the rescale rare.
 #include "common.cuh"
@@ -35,11 +35,11 @@ namespace {
 constexpr int QT = 128;    // rows per query tile (MMA M)
 constexpr int KT = 128;    // keys per key tile
 constexpr int HD = 128;    // head dim
-constexpr int STAGES = 5;  // K / V^T tile ring
+constexpr int STAGES = 3;  // K / V^T tile ring
 constexpr int THREADS = 320;
 constexpr uint32_t SUB_BYTES = 128 * 64 * 2;     // one [128][64] bf16 swizzled sub-tile
 constexpr uint32_t TILE_BYTES = 2 * SUB_BYTES;   // [128][128]
-constexpr size_t SMEM_BYTES = 1024 + (2 + STAGES) * (size_t)TILE_BYTES + 256;
+constexpr size_t SMEM_BYTES = 1024 + (4 + STAGES) * (size_t)TILE_BYTES + 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -115,11 +115,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                        const __grid_constant__ CUtensorMap tmVt, const FaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Qs = smem;                                   // [2] tiles
-  uint8_t* KVs = smem + 2 * TILE_BYTES;                 // [STAGES] tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + STAGES) * TILE_BYTES);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
+  uint8_t* Qs = smem;                                   // [2 blocks][2 tiles]
+  uint8_t* KVs = smem + 4 * TILE_BYTES;                 // [STAGES] tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (4 + STAGES) * TILE_BYTES);
+  uint64_t* q_full = bars + 0;              // [2] one per block
   uint64_t* kv_full = bars + 2;             // [STAGES]
   uint64_t* kv_empty = kv_full + STAGES;    // [STAGES]
   uint64_t* s_full = kv_empty + STAGES;     // [2]
@@ -136,8 +135,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto blk_id = [&](int blk) { return blk == 0 ? total_blocks - 1 - (int)blockIdx.x : (int)blockIdx.x; };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(&q_full[0], 1);
+    mbar_init(&q_full[1], 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -171,17 +170,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const int64_t kv_row0 = ((int64_t)b * p.H + head) * p.S;   // K rows of this head
       const int64_t vt_row0 = ((int64_t)b * p.H + head) * HD;    // V^T rows of this head
-      uint32_t item = 0, q_armed = 0;
+      uint32_t item = 0;
       bool ok = true;
-      for (int blk = 0; blk < 2 && ok; ++blk) {
+      // both blocks' query tiles first (each has its own buffer), so the
+      // second block never waits for the first to drain
+      for (int blk = 0; blk < 2; ++blk) {
         const BlockGeo g = block_geo(blk_id(blk), p, b);
-        if (!mbar_wait(q_empty, (blk & 1) ^ 1, abort_flag, p.err, code | 1)) break;
-        mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
-        ++q_armed;
+        mbar_arrive_expect_tx(&q_full[blk], 2 * TILE_BYTES);
         for (int x = 0; x < 2; ++x)
           for (int c = 0; c < 2; ++c)
-            tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)(g.zrow0 + x * QT),
-                        q_full);
+            tma_load_2d(Qs + (blk * 2 + x) * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64,
+                        (int)(g.zrow0 + x * QT), &q_full[blk]);
+      }
+      for (int blk = 0; blk < 2 && ok; ++blk) {
+        const BlockGeo g = block_geo(blk_id(blk), p, b);
         for (int j = 0; j < g.nB && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++item) {
             const int s = item % STAGES;
@@ -205,7 +207,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t first = item > (uint32_t)STAGES ? item - STAGES : 0;
       volatile int dummy = 0;
       for (uint32_t n = first; n < item; ++n) mbar_wait(&kv_full[n % STAGES], (n / STAGES) & 1, &dummy, p.err, code | 3);
-      if (q_armed) mbar_wait(q_full, (q_armed - 1) & 1, &dummy, p.err, code | 3);
+      mbar_wait(&q_full[0], 0, &dummy, p.err, code | 3);
+      mbar_wait(&q_full[1], 0, &dummy, p.err, code | 3);
     }
   } else if (warp == 9) {
     // ------------------------------ MMA issuer ------------------------------
@@ -214,8 +217,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t item = 0;
       uint32_t pcnt0 = 0, pcnt1 = 0;
       bool ok = true;
+      uint8_t* qbuf = Qs;
       auto mma_s = [&](int x, int s) {  // S_x = Q_x K^T, K = head dim
-        const uint32_t qa = smem_u32(Qs + x * TILE_BYTES), kb = smem_u32(KVs + s * TILE_BYTES);
+        const uint32_t qa = smem_u32(qbuf + x * TILE_BYTES), kb = smem_u32(KVs + s * TILE_BYTES);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t a = sdesc_kmajor_sw128(qa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
@@ -243,7 +247,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int blk = 0; blk < 2 && ok; ++blk) {
         const BlockGeo g = block_geo(blk_id(blk), p, b);
         const int nB = g.nB, nA = g.nB - 1;
-        if (!mbar_wait(q_full, blk & 1, abort_flag, p.err, code | 6)) break;
+        if (!mbar_wait(&q_full[blk], 0, abort_flag, p.err, code | 6)) break;
+        qbuf = Qs + blk * 2 * TILE_BYTES;
         tc_fence_after();
         const uint32_t base = item;  // K_j = base + 2j, V_j = base + 2j + 1
         if (!wait_item(base)) break;
@@ -288,7 +293,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         item = base + 2 * nB;
-        umma_commit(q_empty);
       }
       umma_commit(drain);
       volatile int dummy = 0;
