@@ -78,19 +78,82 @@ __device__ __forceinline__ float max_half(const uint32_t (&h)[64]) {
   return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
+// ---- packed fp32 pairs (f32x2 instructions) -----------------------------------
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^x on the FMA pipe for a pair (x <= ~127; x <= -125, including -inf,
+// gives about 2^-125).  Cody-Waite split x = j + f with j = round(x) taken
+// from the low mantissa bits of x + 1.5*2^23, f in [-0.5, 0.5]; 2^f by a cubic
+// fitted here for minimum relative error on that interval (max 7.5e-5, below
+// bf16's rounding of P); 2^j added to the exponent field as an integer.
+__device__ __forceinline__ void exp2_poly2(uint64_t x2, float& e0, float& e1) {
+  float x0, x1;
+  f2unpack(x2, x0, x1);
+  x0 = fmaxf(x0, -125.0f);
+  x1 = fmaxf(x1, -125.0f);
+  const uint64_t xc = f2pack(x0, x1);
+  const uint64_t magic = f2pack(12582912.0f, 12582912.0f);
+  const uint64_t t = f2add(xc, magic);
+  const uint64_t jf = f2add(t, f2pack(-12582912.0f, -12582912.0f));
+  float j0, j1;
+  f2unpack(jf, j0, j1);
+  const uint64_t f = f2add(xc, f2pack(-j0, -j1));
+  uint64_t pr = f2fma(f2pack(0.0551716648f, 0.0551716648f), f, f2pack(0.2426111251f, 0.2426111251f));
+  pr = f2fma(pr, f, f2pack(0.6932609677f, 0.6932609677f));
+  pr = f2fma(pr, f, f2pack(0.9999280572f, 0.9999280572f));
+  float p0, p1, t0, t1;
+  f2unpack(pr, p0, p1);
+  f2unpack(t, t0, t1);
+  e0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
+  e1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
+}
+
 // p = 2^(s * sl2 - m) for 64 scores, packed as 32 bf16 pairs (low half =
-// even key); returns the fp32 sum of p.
+// even key); returns the fp32 sum of p.  One pair in three goes through the
+// FMA-pipe polynomial, the rest through the MUFU ex2, to balance the two pipes.
 __device__ __forceinline__ float exp_pack_half(const uint32_t (&h)[64], uint32_t* pk, float sl2, float neg_m) {
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(neg_m, neg_m);
+  uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
-    const float e0 = ex2f(fmaf(__uint_as_float(h[2 * q]), sl2, neg_m));
-    const float e1 = ex2f(fmaf(__uint_as_float(h[2 * q + 1]), sl2, neg_m));
-    acc[(2 * q) & 7] += e0;
-    acc[(2 * q + 1) & 7] += e1;
+    const uint64_t x2 = f2fma(f2pack(__uint_as_float(h[2 * q]), __uint_as_float(h[2 * q + 1])), sl2x2, negm2);
+    float e0, e1;
+    if (q % 3 == 2) {
+      exp2_poly2(x2, e0, e1);
+    } else {
+      float x0, x1;
+      f2unpack(x2, x0, x1);
+      e0 = ex2f(x0);
+      e1 = ex2f(x1);
+    }
+    acc[q & 3] = f2add(acc[q & 3], f2pack(e0, e1));
     pk[q] = pack_bf16x2(e0, e1);
   }
-  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo, hi;
+    f2unpack(acc[i], lo, hi);
+    s += lo + hi;
+  }
+  return s;
 }
 
 struct BlockGeo {
