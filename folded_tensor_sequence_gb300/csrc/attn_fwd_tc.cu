@@ -59,25 +59,6 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// Causal mask of the diagonal key tile: column c (key) > row (query) -> -inf.
-__device__ __forceinline__ void mask_half(uint32_t (&h)[64], int c0, int row) {
-#pragma unroll
-  for (int c = 0; c < 64; ++c)
-    if (c0 + c > row) h[c] = __float_as_uint(-INFINITY);
-}
-
-// Max of 64 values through 8 independent chains and a tree.
-__device__ __forceinline__ float max_half(const uint32_t (&h)[64]) {
-  float m[8];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) m[t] = __uint_as_float(h[t]);
-#pragma unroll
-  for (int i = 1; i < 8; ++i)
-#pragma unroll
-    for (int t = 0; t < 8; ++t) m[t] = fmaxf(m[t], __uint_as_float(h[i * 8 + t]));
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-}
-
 // ---- packed fp32 pairs (f32x2 instructions) -----------------------------------
 __device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
   uint64_t r;
@@ -98,62 +79,43 @@ __device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
   return d;
 }
 
-// 2^x on the FMA pipe for a pair (x <= ~127; x <= -125, including -inf,
-// gives about 2^-125).  Cody-Waite split x = j + f with j = round(x) taken
-// from the low mantissa bits of x + 1.5*2^23, f in [-0.5, 0.5]; 2^f by a cubic
-// fitted here for minimum relative error on that interval (max 7.5e-5, below
-// bf16's rounding of P); 2^j added to the exponent field as an integer.
-__device__ __forceinline__ void exp2_poly2(uint64_t x2, float& e0, float& e1) {
-  float x0, x1;
-  f2unpack(x2, x0, x1);
-  x0 = fmaxf(x0, -125.0f);
-  x1 = fmaxf(x1, -125.0f);
-  const uint64_t xc = f2pack(x0, x1);
-  const uint64_t magic = f2pack(12582912.0f, 12582912.0f);
-  const uint64_t t = f2add(xc, magic);
-  const uint64_t jf = f2add(t, f2pack(-12582912.0f, -12582912.0f));
-  float j0, j1;
-  f2unpack(jf, j0, j1);
-  const uint64_t f = f2add(xc, f2pack(-j0, -j1));
-  uint64_t pr = f2fma(f2pack(0.0551716648f, 0.0551716648f), f, f2pack(0.2426111251f, 0.2426111251f));
-  pr = f2fma(pr, f, f2pack(0.6932609677f, 0.6932609677f));
-  pr = f2fma(pr, f, f2pack(0.9999280572f, 0.9999280572f));
-  float p0, p1, t0, t1;
-  f2unpack(pr, p0, p1);
-  f2unpack(t, t0, t1);
-  e0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
-  e1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
-// p = 2^(s * sl2 - m) for 64 scores, packed as 32 bf16 pairs (low half =
-// even key); returns the fp32 sum of p.  One pair in three goes through the
-// FMA-pipe polynomial, the rest through the MUFU ex2, to balance the two pipes.
-__device__ __forceinline__ float exp_pack_half(const uint32_t (&h)[64], uint32_t* pk, float sl2, float neg_m) {
-  const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(neg_m, neg_m);
-  uint64_t acc[4] = {0, 0, 0, 0};
+// Max of 32 raw scores (3-input max tree).
+__device__ __forceinline__ float max_quarter(const uint32_t (&h)[32]) {
+  float m[11];
 #pragma unroll
-  for (int q = 0; q < 32; ++q) {
+  for (int i = 0; i < 10; ++i)
+    m[i] = fmax3(__uint_as_float(h[3 * i]), __uint_as_float(h[3 * i + 1]), __uint_as_float(h[3 * i + 2]));
+  m[10] = fmaxf(__uint_as_float(h[30]), __uint_as_float(h[31]));
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]), c = fmax3(m[6], m[7], m[8]);
+  return fmax3(fmax3(a, b, c), m[9], m[10]);
+}
+
+// Causal mask of the diagonal key tile for 32 columns starting at c0.
+__device__ __forceinline__ void mask_quarter(uint32_t (&h)[32], int c0, int row) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    if (c0 + c > row) h[c] = __float_as_uint(-INFINITY);
+}
+
+// p = 2^(s * sl2 - m) for 32 scores, packed as 16 bf16 pairs (low half = even
+// key) into pk; accumulates the fp32 sum of p in acc (packed pairs).
+__device__ __forceinline__ void exp_pack_quarter(const uint32_t (&h)[32], uint32_t* pk, uint64_t sl2x2,
+                                                 uint64_t negm2, uint64_t (&acc)[2]) {
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
     const uint64_t x2 = f2fma(f2pack(__uint_as_float(h[2 * q]), __uint_as_float(h[2 * q + 1])), sl2x2, negm2);
-    float e0, e1;
-    if (q % 3 == 2) {
-      exp2_poly2(x2, e0, e1);
-    } else {
-      float x0, x1;
-      f2unpack(x2, x0, x1);
-      e0 = ex2f(x0);
-      e1 = ex2f(x1);
-    }
-    acc[q & 3] = f2add(acc[q & 3], f2pack(e0, e1));
+    float x0, x1;
+    f2unpack(x2, x0, x1);
+    const float e0 = ex2f(x0), e1 = ex2f(x1);
+    acc[q & 1] = f2add(acc[q & 1], f2pack(e0, e1));
     pk[q] = pack_bf16x2(e0, e1);
   }
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float lo, hi;
-    f2unpack(acc[i], lo, hi);
-    s += lo + hi;
-  }
-  return s;
 }
 
 struct BlockGeo {
@@ -389,53 +351,74 @@ __global__ void __launch_bounds__(THREADS, 1)
         // first half is exponentiated.  Exponentials use the running max from
         // earlier key tiles (speculation); only if this tile raises the max by
         // more than the threshold are O rescaled and P recomputed from S.
-        uint32_t h0[64], h1[64];
-        uint32_t pk[64];  // P as packed bf16 pairs: column c holds keys 2c, 2c+1
-        tmem_ld64_issue(tS, h0);
-        tmem_wait_ld64(h0);
-        tmem_ld64_issue(tS + 64, h1);
-        if (diag) mask_half(h0, 0, row);
-        float sum = 0.f;
-        if (j == 0) {
-          tmem_wait_ld64(h1);
-          if (diag) mask_half(h1, 64, row);
-          m_used = fmaxf(max_half(h0), max_half(h1)) * sl2;
-          sum = exp_pack_half(h0, pk, sl2, -m_used) + exp_pack_half(h1, pk + 32, sl2, -m_used);
-        } else {
-          const float mx0 = max_half(h0);
-          const float s0 = exp_pack_half(h0, pk, sl2, -m_used);
-          tmem_wait_ld64(h1);
-          if (diag) mask_half(h1, 64, row);
-          const float mx1 = max_half(h1);
-          const float s1 = exp_pack_half(h1, pk + 32, sl2, -m_used);
-          sum = s0 + s1;
-          const float m_new = fmaxf(mx0, mx1) * sl2;
-          const bool need = m_new > m_used + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            const float factor = need ? ex2f(m_used - m_new) : 1.0f;
+        // Four 32-column quarters of S: quarter k+1 loads while quarter k is
+        // processed.  Exponentials use the running max from earlier key tiles
+        // (speculation); only if this tile raises the max by more than the
+        // threshold are O rescaled and P recomputed from S (still in TMEM).
+        uint32_t pk[64];
+        if (j == 0) {  // first key tile of the block: the max has to come first
+          float mx = -INFINITY;
 #pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-              float ov[32];
-              uint32_t part[32];
-              tmem_ld32(tO + c4 * 32, ov);
+          for (int k = 0; k < 4; ++k) {
+            uint32_t hq[32];
+            tmem_ld32_issue(tS + 32 * k, hq);
+            tmem_wait_ld32(hq);
+            if (diag) mask_quarter(hq, 32 * k, row);
+            mx = fmaxf(mx, max_quarter(hq));
+          }
+          m_used = mx * sl2;
+        }
+        float sum = 0.f;
+        bool again = true;
+        for (int pass = 0; pass < 2 && again; ++pass) {
+          const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-m_used, -m_used);
+          uint64_t acc[2] = {0, 0};
+          float mx = -INFINITY;
+          uint32_t hq0[32], hq1[32];
+          tmem_ld32_issue(tS, hq0);
+          tmem_wait_ld32(hq0);
+          tmem_ld32_issue(tS + 32, hq1);
+          if (diag) mask_quarter(hq0, 0, row);
+          mx = max_quarter(hq0);
+          exp_pack_quarter(hq0, pk, sl2x2, negm2, acc);
+          tmem_wait_ld32(hq1);
+          tmem_ld32_issue(tS + 64, hq0);
+          if (diag) mask_quarter(hq1, 32, row);
+          mx = fmaxf(mx, max_quarter(hq1));
+          exp_pack_quarter(hq1, pk + 16, sl2x2, negm2, acc);
+          tmem_wait_ld32(hq0);
+          tmem_ld32_issue(tS + 96, hq1);
+          if (diag) mask_quarter(hq0, 64, row);
+          mx = fmaxf(mx, max_quarter(hq0));
+          exp_pack_quarter(hq0, pk + 32, sl2x2, negm2, acc);
+          tmem_wait_ld32(hq1);
+          if (diag) mask_quarter(hq1, 96, row);
+          mx = fmaxf(mx, max_quarter(hq1));
+          exp_pack_quarter(hq1, pk + 48, sl2x2, negm2, acc);
+          float a0, a1, a2, a3;
+          f2unpack(acc[0], a0, a1);
+          f2unpack(acc[1], a2, a3);
+          sum = (a0 + a1) + (a2 + a3);
+          const float m_new = mx * sl2;
+          const bool need = m_new > m_used + kRescaleThreshold;
+          again = __any_sync(0xffffffffu, need);
+          if (again) {
+            const float factor = need ? ex2f(m_used - m_new) : 1.0f;
+            if (j > 0) {
+#pragma unroll 1
+              for (int c4 = 0; c4 < 4; ++c4) {
+                float ov[32];
+                uint32_t part[32];
+                tmem_ld32(tO + c4 * 32, ov);
 #pragma unroll
-              for (int c = 0; c < 32; ++c) part[c] = __float_as_uint(ov[c] * factor);
-              tmem_st32(tO + c4 * 32, part);
+                for (int c = 0; c < 32; ++c) part[c] = __float_as_uint(ov[c] * factor);
+                tmem_st32(tO + c4 * 32, part);
+              }
             }
             if (need) {
               l *= factor;
               m_used = m_new;
             }
-            // S is still intact (P has not been written over it yet): recompute
-            tmem_ld64_issue(tS, h0);
-            tmem_wait_ld64(h0);
-            tmem_ld64_issue(tS + 64, h1);
-            tmem_wait_ld64(h1);
-            if (diag) {
-              mask_half(h0, 0, row);
-              mask_half(h1, 64, row);
-            }
-            sum = exp_pack_half(h0, pk, sl2, -m_used) + exp_pack_half(h1, pk + 32, sl2, -m_used);
           }
         }
         l += sum;
