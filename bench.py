@@ -38,13 +38,13 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch
-# of a step's kernel on the default workload, with the kernel source file and
-# the first 16 hex digits of its sha256 when the counters were taken; if the
-# source has changed since, the traffic is reported as null.
-#   attention: 201.5 MB + 48.8 MB captured at seq 8192 (batch 1); K/V of a head
-#   are re-read from L2, so DRAM bytes scale with tokens: x4 for batch 2 x 16384.
+# of a step's kernel on the default workload (D=8, batch 2, seq 16384), with
+# the kernel source file and the first 16 hex digits of its sha256 when the
+# counters were taken (one-pass capture of the full-size launch, see
+# profiles/); if the source has changed since, the traffic is reported as null.
 NCU_TRAFFIC = {
-    "attention": (4 * (201.52e6 + 48.84e6), "folded_tensor_sequence_gb300/csrc/attn_fwd.cu", "014e0d2509343901"),
+    "gate/up projection": (2.16e9 + 0.927e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "2be9988fc84071f1"),
+    "attention": (0.841e9 + 0.253e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "1401fedc4fa023e7"),
 }
 
 
