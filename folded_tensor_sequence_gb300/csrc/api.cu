@@ -32,6 +32,20 @@ namespace tsp {
 
 __device__ unsigned int g_dev_error_word = 0;
 
+// One warp waits (bounded) on a barrier that nothing will signal: the wait
+// gives up after timeout_ns, records the error word and the kernel returns.
+__global__ void wait_probe_kernel(unsigned int* err, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait_for(&bar, 0, &abort_flag, err, (KID_WAIT_PROBE << 8) | 1, timeout_ns);
+}
+
 namespace {
 
 thread_local char t_last_error[512] = "";
@@ -263,14 +277,18 @@ tsp_status run_gemm(const tsp_plan* p, const void* A, int64_t lda, const void* B
 }
 
 // a_out = (Attn(xz Wq, xz Wk, xz Wv)) Wo [+ resid]
+// x_natural: xz (and resid) are natural-order rows, read through the GEMMs'
+// zigzag row remapping instead of a separate permute.
 tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const tsp_weights* w, void* a_out,
-                          const void* resid, float* lse, char* qz, char* k, char* v, char* oz, cudaStream_t st) {
+                          const void* resid, float* lse, char* qz, char* k, char* v, char* oz, cudaStream_t st,
+                          bool x_natural = false) {
   const int T = batch * (int)p->seq, h = p->hidden;
   EpiParams ep = base_epi(p, batch);
   ep.q = qz;
   ep.k = k;
   ep.v = v;
   ep.v_transposed = use_tc_attention(p);
+  ep.a_natural = x_natural;
   tsp_status s = run_gemm(p, xz, h, w->qkv, h, T, 3 * h, h, EPI_QKV, ep, st, "QKV projection");
   if (s != TSP_OK) return s;
   AttnParams ap;
@@ -296,12 +314,14 @@ tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const ts
   eo.ldo = h;
   eo.resid = resid;
   eo.ldr = h;
+  eo.resid_natural = x_natural;
   return run_gemm(p, oz, h, w->o, h, T, h, h, resid ? EPI_RESID : EPI_STORE, eo, st, "output projection");
 }
 
 // out = (SiLU(hz Wg) * (hz Wu)) Wd [+ resid]; optionally keeps the raw gate/up in gu_save
+// out_natural: the down projection writes natural-order rows.
 tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weights* w, void* out, const void* resid,
-                    char* mz, char* gu, bool save_gu, cudaStream_t st) {
+                    char* mz, char* gu, bool save_gu, cudaStream_t st, bool out_natural = false) {
   const int T = batch * (int)p->seq, h = p->hidden, F = p->ffn;
   tsp_status s;
   if (p->dtype == TSP_BF16) {
@@ -327,6 +347,7 @@ tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weig
   ed.ldo = h;
   ed.resid = resid;
   ed.ldr = h;
+  ed.out_natural = out_natural;
   return run_gemm(p, mz, F, w->down, F, T, h, F, resid ? EPI_RESID : EPI_STORE, ed, st, "down projection");
 }
 
@@ -544,6 +565,16 @@ tsp_status tsp_layer_fwd(const tsp_plan* p, int batch, const void* x, const tsp_
   char* act = saved ? static_cast<char*>(saved) : wsb;  // where the saved activations go
   char* xz = act + L.xz;
   char* yz = wsb + L.yz;
+  if (!saved && p->dtype == TSP_BF16 && p->chunk % 128 == 0) {
+    // The zigzag permute and unpermute ride on the GEMMs: every 128-row tile
+    // of zigzag rows is one contiguous run of natural rows, so the QKV GEMM
+    // reads x through remapped TMA coordinates, the output projection adds x
+    // by remapped row, and the down projection writes y in natural order.
+    s = attention_impl(p, batch, x, w, act + L.hz, x, nullptr, act + L.qz, act + L.k, act + L.v, act + L.oz, st,
+                       true);
+    if (s != TSP_OK) return s;
+    return mlp_impl(p, batch, act + L.hz, w, y, act + L.hz, act + L.mz, act + L.gu, false, st, true);
+  }
   {
     Prof pr("zigzag permute", st);
     s = cuda_status(launch_zigzag_rows(x, xz, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, true, st),
@@ -733,6 +764,17 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   Prof pr_dx("unpermute dx", st);
   return cuda_status(launch_zigzag_rows(wb + L.dxz, dx, h * eb, p->D, batch, p->seq, false, st), "unpermute dx");
 #undef TSP_TRY
+}
+
+tsp_status tsp_debug_wait_timeout(unsigned int timeout_us, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if (timeout_us == 0 || timeout_us > 10000000u)
+    return fail(TSP_ERR_INVALID_ARG, "timeout_us %u not in (0, 10 s]", timeout_us);
+  unsigned int* err = dev_error_word();
+  if (!err) return fail(TSP_ERR_CUDA, "device error word unavailable");
+  wait_probe_kernel<<<1, 32, 0, as_stream(stream)>>>(err, (unsigned long long)timeout_us * 1000ull);
+  return cuda_status(cudaGetLastError(), "wait probe launch");
 }
 
 void tsp_profile_enable(int on) {

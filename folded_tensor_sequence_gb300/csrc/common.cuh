@@ -21,6 +21,7 @@ enum KernelId : unsigned int {
   KID_GEMM_TC = 1,
   KID_ATTN_FWD = 2,
   KID_ATTN_BWD = 3,
+  KID_WAIT_PROBE = 4,
 };
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
@@ -90,8 +91,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // kWaitTimeoutNs, or as soon as another role of the CTA has set *abort;
 // on its own timeout it sets *abort and records `code`.  Returns false on
 // giving up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* err, unsigned int code) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned int* err,
+                                              unsigned int code, unsigned long long timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
@@ -99,12 +100,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
       *abort = 1;
       record_dev_error(err, code);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* err, unsigned int code) {
+  return mbar_wait_for(bar, parity, abort, err, code, kWaitTimeoutNs);
 }
 
 // ---------------------------------------------------------------------------

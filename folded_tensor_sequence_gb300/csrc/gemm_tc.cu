@@ -83,6 +83,18 @@ __device__ __forceinline__ void load32_bf16(const void* src, float (&v)[32]) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
+// Zigzag row m of [D][B][2C] -> natural row b*S + pos.
+__device__ __forceinline__ int64_t zigzag_row_to_natural(int64_t m, const EpiParams& ep) {
+  const int64_t twoC = 2 * (int64_t)ep.C;
+  const int64_t per_rank = (int64_t)ep.B * twoC;
+  const int64_t r = m / per_rank;
+  const int64_t rem = m - r * per_rank;
+  const int64_t b = rem / twoC;
+  const int64_t k = rem - b * twoC;
+  const int64_t p = (k < ep.C) ? r * ep.C + k : (2 * ep.D - 1 - r) * ep.C + (k - ep.C);
+  return b * ep.S + p;
+}
+
 // Zigzag row m of [D][B][2C] -> (batch b, natural position p).
 __device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep, int& b, int64_t& p) {
   const int64_t twoC = 2 * (int64_t)ep.C;
@@ -155,7 +167,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-          tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, mt * BM, &full[s]);
+          const int arow = ep.a_natural ? (int)zigzag_row_to_natural((int64_t)mt * BM, ep) : mt * BM;
+          tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, &full[s]);
           tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
         }
       }
@@ -243,9 +256,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         int b = 0;
-        int64_t p = 0;
+        int64_t p = 0, nat = m;
         if constexpr (EPI == EPI_QKV) {
           if (valid) zigzag_row_to_pos(m, ep, b, p);
+        }
+        if constexpr (EPI == EPI_RESID) {
+          if (valid && (ep.resid_natural || ep.out_natural)) nat = zigzag_row_to_natural(m, ep);
         }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -257,10 +273,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + n, v);
           } else if constexpr (EPI == EPI_RESID) {
             float r[32];
-            load32_bf16(reinterpret_cast<const __nv_bfloat16*>(ep.resid) + m * ep.ldr + n, r);
+            load32_bf16(reinterpret_cast<const __nv_bfloat16*>(ep.resid) + (ep.resid_natural ? nat : m) * ep.ldr + n, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] += r[i];
-            store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + n, v);
+            store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + (ep.out_natural ? nat : m) * ep.ldo + n, v);
           } else if constexpr (EPI == EPI_QKV) {
             // packed column n -> (shard s, which of q/k/v, head, d)
             const int hs = ep.h / ep.D;  // columns of one projection in one shard

@@ -42,6 +42,12 @@ struct EpiParams {
   int D = 1, B = 1, S = 0, C = 0, H = 1, dh = 1, h = 0;
   unsigned int* err = nullptr;  // device error word
   bool v_transposed = false;    // EPI_QKV: write V as [B][H][dh][S] instead of [B][H][S][dh]
+  // Zigzag row m <-> natural row remapping (uses D, B, S, C; needs C % 128 == 0):
+  //   a_natural:     the A operand is natural-order rows; tile rows of zigzag
+  //                  rows m0.. are read from natural row nat(m0)..
+  //   resid_natural: EPI_RESID reads resid row nat(m)
+  //   out_natural:   EPI_RESID writes out row nat(m)
+  bool a_natural = false, resid_natural = false, out_natural = false;
 };
 
 int num_sms();

@@ -25,7 +25,7 @@ EXPORTS = [
     "tsp_last_error_message", "tsp_pack_weights", "tsp_unpack_weights", "tsp_zigzag_permute",
     "tsp_zigzag_unpermute", "tsp_kv_gather", "tsp_attention_fwd", "tsp_gated_mlp_fwd", "tsp_layer_fwd",
     "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next", "tsp_profile_enable", "tsp_profile_report",
-    "tsp_attention_fwd_static",
+    "tsp_attention_fwd_static", "tsp_debug_wait_timeout",
 ]
 
 
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.tsp_sync_check.argtypes = [vp]
         L.tsp_debug_fail_next.argtypes = [i32, i32]
         L.tsp_debug_fail_next.restype = None
+        L.tsp_debug_wait_timeout.argtypes = [ctypes.c_uint, vp]
         L.tsp_attention_fwd_static.argtypes = [vp, i32, vp, ctypes.POINTER(_Weights), vp, vp, vp]
         L.tsp_profile_enable.argtypes = [i32]
         L.tsp_profile_enable.restype = None
@@ -164,6 +165,10 @@ def tsp_sync_check(stream=None) -> None:
 
 def tsp_debug_fail_next(status: int, count: int = 1) -> None:
     lib().tsp_debug_fail_next(status, count)
+
+
+def tsp_debug_wait_timeout(timeout_us: int, stream=None) -> None:
+    _check(lib().tsp_debug_wait_timeout(timeout_us, _stream(stream)), "tsp_debug_wait_timeout")
 
 
 def tsp_profile_enable(on: bool) -> None:

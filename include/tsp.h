@@ -184,6 +184,13 @@ tsp_status tsp_sync_check(void* stream);
  * this thread return `status` before enqueuing anything (count 0 disarms). */
 void tsp_debug_fail_next(tsp_status status, int count);
 
+/* Failure-detection check: enqueues a one-warp kernel whose bounded wait on a
+ * barrier that nothing signals gives up after `timeout_us` microseconds
+ * (1 us .. 10 s), records the device error word and returns; the next
+ * tsp_sync_check on that stream reports TSP_ERR_TIMEOUT and clears the word.
+ * Nothing traps; the context stays usable. */
+tsp_status tsp_debug_wait_timeout(unsigned int timeout_us, void* stream);
+
 /* ---- attention without a caller workspace -------------------------------- */
 
 /* Size of the static scratch array behind tsp_attention_fwd_static. */

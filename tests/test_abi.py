@@ -111,3 +111,9 @@ def test_host_fault_injection(tsp):
     with pytest.raises(tsp.TspError) as ei:
         tsp.tsp_zigzag_permute(p, 1, None, None)
     assert ei.value.status == tsp.TSP_ERR_INVALID_ARG
+
+
+def test_wait_probe_validates_on_host(tsp):
+    L = tsp.lib()
+    assert L.tsp_debug_wait_timeout(0, None) == tsp.TSP_ERR_INVALID_ARG
+    assert L.tsp_debug_wait_timeout(20000000, None) == tsp.TSP_ERR_INVALID_ARG
