@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int t = blockIdx.x; t < shape.num_tiles && ok; t += gridDim.x) {
         int mt, nt;
         tile_coords(t, shape, mt, nt);
+        const int arow = ep.a_natural ? (int)zigzag_row_to_natural((int64_t)mt * BM, ep) : mt * BM;
         for (int kb = 0; kb < shape.kblocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -167,7 +168,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-          const int arow = ep.a_natural ? (int)zigzag_row_to_natural((int64_t)mt * BM, ep) : mt * BM;
           tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, &full[s]);
           tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
         }
