@@ -17,10 +17,11 @@
 //     key blocks of 64 stream K, V (for S = Q K^T, dP = dO V^T) and K^T (for
 //     dQ += dS K).  TMEM: S and dP double-buffered, dQ accumulator.
 // In both, warps 0-3 turn scores into P and dS (one TMEM lane = one row per
-// thread) and write them as bf16 in the 128-byte-swizzled layout the MMA
-// reads, warp 4 issues TMA, warp 5 issues tcgen05.mma from one thread; the
-// tensor core computes block i+1's scores while the elementwise warps work on
-// block i.
+// thread) and write them back into tensor memory as packed bf16, where the
+// accumulating MMAs read them as their A operand; lse and dsum of each query
+// block come in with the stage by bulk copy.  Warp 4 issues TMA, warp 5 issues
+// tcgen05.mma from one thread; the tensor core computes block i+1's scores
+// while the elementwise warps work on block i.
 #include "common.cuh"
 #include "internal.h"
 
@@ -54,22 +55,10 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
 __device__ __forceinline__ int64_t zz_row(int64_t pos, int64_t C, int D, int B, int b) {
   const int64_t c = pos / C, off = pos - c * C;
   const int64_t r = c < D ? c : 2 * D - 1 - c;
   return (r * B + b) * 2 * C + (c < D ? off : C + off);
-}
-
-// Writes 64 bf16 values (one row of a [rows][64] swizzled K-major sub-tile).
-__device__ __forceinline__ void store_row64(uint8_t* sub, int row, const float (&v)[64]) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint4 pk = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                                pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-    *reinterpret_cast<uint4*>(sub + row * 128 + ((q ^ (row & 7)) << 4)) = pk;
-  }
 }
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -87,8 +76,10 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // dK, dV
 // ===========================================================================
 constexpr int KB_QB = 64;  // queries per block
-constexpr uint32_t KV_STAGE_BYTES = 4 * SUB64 + 2 * SUB128;  // Q, dO (2 sub each) + Q^T, dO^T
-constexpr size_t DKDV_SMEM = 1024 + 2 * 2 * SUB128 + 2 * (size_t)KV_STAGE_BYTES + 2 * SUB128 + 256;
+// stage: Q, dO (2 sub-tiles each), Q^T, dO^T, then lse and dsum of the block (256 B each)
+constexpr uint32_t KV_STAGE_DATA = 4 * SUB64 + 2 * SUB128;
+constexpr uint32_t KV_STAGE_BYTES = KV_STAGE_DATA + 1024;  // keeps stages 1024-byte aligned
+constexpr size_t DKDV_SMEM = 1024 + 2 * 2 * SUB128 + 2 * (size_t)KV_STAGE_BYTES + 256;
 
 __global__ void __launch_bounds__(THREADS, 1)
     attn_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -100,16 +91,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* Ks = smem;                    // 2 x SUB128
   uint8_t* Vs = smem + 2 * SUB128;       // 2 x SUB128
   uint8_t* stg = smem + 4 * SUB128;      // [2] stages
-  uint8_t* Pt = stg + 2 * KV_STAGE_BYTES;
-  uint8_t* dSt = Pt + SUB128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dSt + SUB128);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * KV_STAGE_BYTES);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_free = bars + 1;
   uint64_t* q_full = bars + 2;   // [2]
   uint64_t* q_free = bars + 4;   // [2]
   uint64_t* s_full = bars + 6;   // [2]
   uint64_t* ds_full = bars + 8;
-  uint64_t* pds_free = bars + 9;
   uint64_t* o_done = bars + 10;
   uint64_t* drain = bars + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
@@ -130,7 +118,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&s_full[s], 1);
     }
     mbar_init(ds_full, 128);
-    mbar_init(pds_free, 1);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -152,7 +139,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // TMEM columns: S^T[x] at 64x, dP^T[x] at 128 + 64x, dV at 256, dK at 384
+  // TMEM columns: S^T[x] at 64x, dP^T[x] at 128 + 64x, dV at 256, dK at 384.
+  // P^T (bf16 pairs) is written over the first 32 columns of S^T[x] and dS^T
+  // over dP^T[x]; the accumulating MMAs read them from there (A operand in
+  // tensor memory).  The next score MMAs into buffer x are issued after those
+  // MMAs, and one CTA's tcgen05 MMAs execute in issue order.
 
   if (warp == 4) {
     // ---------------- TMA producer ----------------
@@ -179,13 +170,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const int64_t zr = zz_row(k0 + (int64_t)i * KB_QB, p.C, p.D, p.B, b);
           uint8_t* st = stg + s * KV_STAGE_BYTES;
-          mbar_arrive_expect_tx(&q_full[s], KV_STAGE_BYTES);
+          const int64_t q0 = k0 + (int64_t)i * KB_QB;
+          mbar_arrive_expect_tx(&q_full[s], KV_STAGE_DATA + 2 * KB_QB * 4);
           for (int c = 0; c < 2; ++c) {
             tma_load_2d(st + c * SUB64, &tmQ, head * HD + c * 64, (int)zr, &q_full[s]);
             tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmdO, head * HD + c * 64, (int)zr, &q_full[s]);
           }
           tma_load_2d(st + 4 * SUB64, &tmQT, (int)zr, head * HD, &q_full[s]);
           tma_load_2d(st + 4 * SUB64 + SUB128, &tmdOT, (int)zr, head * HD, &q_full[s]);
+          bulk_load(st + KV_STAGE_DATA, p.lse + bh * p.S + q0, KB_QB * 4, &q_full[s]);
+          bulk_load(st + KV_STAGE_DATA + KB_QB * 4, p.dsum + bh * p.S + q0, KB_QB * 4, &q_full[s]);
         }
       }
       volatile int dummy = 0;
@@ -216,21 +210,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         umma_commit(&s_full[x]);
       };
-      auto accumulate = [&](uint32_t n, bool acc) {  // dV += P^T dO, dK += dS^T Q for query block n
+      auto accumulate = [&](uint32_t n, int x, bool acc) {  // dV += P^T dO, dK += dS^T Q for query block n
         uint8_t* st = stg + (n & 1) * KV_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < KB_QB / 16; ++k) {
-          const uint64_t ap = sdesc_kmajor_sw128(smem_u32(Pt)) + 2 * k;
           const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64 + SUB128)) + 2 * k;
-          umma_bf16(tmem_base + 256, ap, bo, id_o, (acc || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 8 * k, bo, id_o, (acc || k > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < KB_QB / 16; ++k) {
-          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(dSt)) + 2 * k;
           const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
-          umma_bf16(tmem_base + 384, ad, bq, id_o, (acc || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * x + 8 * k, bq, id_o, (acc || k > 0) ? 1u : 0u);
         }
-        umma_commit(pds_free);
         umma_commit(&q_free[n & 1]);
       };
       uint32_t dscnt = 0;
@@ -254,14 +245,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             ++dscnt;
             tc_fence_after();
-            accumulate(n - 1, i - 1 > 0);
+            accumulate(n - 1, (i - 1) & 1, i - 1 > 0);
           }
         }
         if (!ok) break;
         if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DKDV | 6)) break;
         ++dscnt;
         tc_fence_after();
-        accumulate(qi + nq - 1, nq - 1 > 0);
+        accumulate(qi + nq - 1, (nq - 1) & 1, nq - 1 > 0);
         umma_commit(o_done);
         umma_commit(kv_free);
         qi += nq;
@@ -278,10 +269,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = kLog2e * rsqrtf((float)HD);
     const float scale = rsqrtf((float)HD);
-    const float* lse_bh = p.lse + bh * p.S;
-    const float* ds_bh = p.dsum + bh * p.S;
     uint32_t scnt[2] = {0, 0};
-    uint32_t freecnt = 0;
+    uint32_t qidx = 0;  // global query-block counter (stage = qidx & 1)
     bool alive = true;
     for (int t = 0; t < ntile && alive; ++t) {
       const int64_t k0 = (int64_t)tile_of(t) * 128;
@@ -301,31 +290,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld64(tmem_base + lane_off + 128 + 64 * x, dp);
         const int64_t q0 = k0 + (int64_t)i * KB_QB;
         const bool diag = i < 2;
+        // lse and dsum of this query block arrived with the stage (bulk copies)
+        const float* lse_s = reinterpret_cast<const float*>(stg + (qidx & 1) * KV_STAGE_BYTES + KV_STAGE_DATA);
+        const float* ds_s = lse_s + KB_QB;
+        uint32_t pk[32], dk2[32];
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_bh + q0) + c4);
-          const float4 d4 = __ldg(reinterpret_cast<const float4*>(ds_bh + q0) + c4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c4 * 4 + e;
-            float pv = ex2f(fmaf(sv[c], sl2, -lv[e] * kLog2e));
-            if (diag && q0 + c < key) pv = 0.f;
-            sv[c] = pv;
-            dp[c] = pv * (dp[c] - dv4[e]);
-          }
+        for (int c = 0; c < 64; c += 2) {
+          float pv0 = ex2f(fmaf(sv[c], sl2, -lse_s[c] * kLog2e));
+          float pv1 = ex2f(fmaf(sv[c + 1], sl2, -lse_s[c + 1] * kLog2e));
+          if (diag && q0 + c < key) pv0 = 0.f;
+          if (diag && q0 + c + 1 < key) pv1 = 0.f;
+          pk[c / 2] = pack_bf16x2(pv0, pv1);
+          dk2[c / 2] = pack_bf16x2(pv0 * (dp[c] - ds_s[c]), pv1 * (dp[c + 1] - ds_s[c + 1]));
         }
-        // P^T and dS^T smem must be free of the previous block's MMAs
-        const bool fr = mbar_wait(pds_free, (freecnt & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 9);
-        ++freecnt;
-        if (!__all_sync(0xffffffffu, fr)) {
-          alive = false;
-          break;
-        }
-        store_row64(Pt, row, sv);
-        store_row64(dSt, row, dp);
-        fence_async_smem();
+        ++qidx;
+        // P^T over S^T[x] and dS^T over dP^T[x] (first 32 columns each)
+        tmem_st32_nowait(tmem_base + lane_off + 64 * x, pk);
+        tmem_st32_nowait(tmem_base + lane_off + 128 + 64 * x, dk2);
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(ds_full);
       }
@@ -366,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ===========================================================================
 constexpr int DQ_KB = 64;  // keys per block
 constexpr uint32_t DQ_STAGE_BYTES = 4 * SUB64 + SUB128;  // K, V (2 sub each) + K^T
-constexpr size_t DQ_SMEM = 1024 + 4 * (size_t)SUB128 + 2 * (size_t)DQ_STAGE_BYTES + SUB128 + 256;
+constexpr size_t DQ_SMEM = 1024 + 4 * (size_t)SUB128 + 2 * (size_t)DQ_STAGE_BYTES + 256;
 
 __global__ void __launch_bounds__(THREADS, 1)
     attn_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -377,15 +359,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* Qs = smem;                  // 2 x SUB128
   uint8_t* dOs = smem + 2 * SUB128;    // 2 x SUB128
   uint8_t* stg = smem + 4 * SUB128;    // [2] stages
-  uint8_t* dSs = stg + 2 * DQ_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dSs + SUB128);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * DQ_STAGE_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* q_free = bars + 1;
   uint64_t* k_full = bars + 2;   // [2]
   uint64_t* k_free = bars + 4;   // [2]
   uint64_t* s_full = bars + 6;   // [2]
   uint64_t* ds_full = bars + 8;
-  uint64_t* ds_free = bars + 9;
   uint64_t* o_done = bars + 10;
   uint64_t* drain = bars + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
@@ -413,7 +393,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&s_full[s], 1);
     }
     mbar_init(ds_full, 128);
-    mbar_init(ds_free, 1);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -434,7 +413,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // TMEM columns: S[x] at 64x, dP[x] at 128 + 64x, dQ at 256
+  // TMEM columns: S[x] at 64x, dP[x] at 128 + 64x, dQ at 256.  dS (bf16
+  // pairs) is written over the first 32 columns of S[x] and read from there by
+  // the dQ MMA; MMAs of one CTA execute in issue order.
 
   if (warp == 4) {
     if (lane == 0) {
@@ -495,15 +476,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         umma_commit(&s_full[x]);
       };
-      auto accumulate = [&](uint32_t n, bool acc) {  // dQ += dS K for key block n
+      auto accumulate = [&](uint32_t n, int x, bool acc) {  // dQ += dS K for key block n
         uint8_t* st = stg + (n & 1) * DQ_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < DQ_KB / 16; ++k) {
-          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(dSs)) + 2 * k;
           const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
-          umma_bf16(tmem_base + 256, ad, bk, id_o, (acc || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 8 * k, bk, id_o, (acc || k > 0) ? 1u : 0u);
         }
-        umma_commit(ds_free);
         umma_commit(&k_free[n & 1]);
       };
       for (int t = 0; t < 2 && ok; ++t) {
@@ -526,14 +505,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             ++dscnt;
             tc_fence_after();
-            accumulate(n - 1, j - 1 > 0);
+            accumulate(n - 1, (j - 1) & 1, j - 1 > 0);
           }
         }
         if (!ok) break;
         if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DQ | 6)) break;
         ++dscnt;
         tc_fence_after();
-        accumulate(ki + nkb - 1, nkb - 1 > 0);
+        accumulate(ki + nkb - 1, (nkb - 1) & 1, nkb - 1 > 0);
         umma_commit(o_done);
         umma_commit(q_free);
         ki += nkb;
@@ -548,7 +527,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float sl2 = kLog2e * rsqrtf((float)HD);
     const float scale = rsqrtf((float)HD);
     uint32_t scnt[2] = {0, 0};
-    uint32_t freecnt = 0;
     bool alive = true;
     for (int t = 0; t < 2 && alive; ++t) {
       int64_t zrow0, p0;
@@ -571,20 +549,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld64(tmem_base + lane_off + 128 + 64 * x, dp);
         const int64_t key0 = (int64_t)j * DQ_KB;
         const bool diag = key0 + DQ_KB - 1 > p0;
+        uint32_t dsk[32];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float pv = ex2f(fmaf(sv[c], sl2, -l2));
-          if (diag && key0 + c > qpos) pv = 0.f;
-          dp[c] = pv * (dp[c] - dsr);
+        for (int c = 0; c < 64; c += 2) {
+          float pv0 = ex2f(fmaf(sv[c], sl2, -l2));
+          float pv1 = ex2f(fmaf(sv[c + 1], sl2, -l2));
+          if (diag && key0 + c > qpos) pv0 = 0.f;
+          if (diag && key0 + c + 1 > qpos) pv1 = 0.f;
+          dsk[c / 2] = pack_bf16x2(pv0 * (dp[c] - dsr), pv1 * (dp[c + 1] - dsr));
         }
-        const bool fr = mbar_wait(ds_free, (freecnt & 1) ^ 1, abort_flag, p.err, CODE_DQ | 9);
-        ++freecnt;
-        if (!__all_sync(0xffffffffu, fr)) {
-          alive = false;
-          break;
-        }
-        store_row64(dSs, row, dp);
-        fence_async_smem();
+        tmem_st32_nowait(tmem_base + lane_off + 64 * x, dsk);  // dS over S[x]
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(ds_full);
       }
