@@ -16,11 +16,11 @@
 //     pairing: both tiles on the same rank).  Q and dO stay in shared memory;
 //     key blocks of 64 stream K, V (for S = Q K^T, dP = dO V^T) and K^T (for
 //     dQ += dS K).  TMEM: S and dP double-buffered, dQ accumulator.
-// In both, warps 0-3 turn scores into P and dS (one TMEM lane = one row per
-// thread) and write them back into tensor memory as packed bf16, where the
-// accumulating MMAs read them as their A operand; lse and dsum of each query
-// block come in with the stage by bulk copy.  Warp 4 issues TMA, warp 5 issues
-// tcgen05.mma from one thread; the tensor core computes block i+1's scores
+// In both, warps 0-7 turn scores into P and dS (a TMEM lane = a row, split
+// over two threads of 32 columns each) and write them back into tensor memory
+// as packed bf16, where the accumulating MMAs read them as their A operand;
+// lse and dsum of each query block come in with the stage by bulk copy.
+// Warp 8 issues TMA, warp 9 issues tcgen05.mma from one thread; the tensor core computes block i+1's scores
 // while the elementwise warps work on block i.
 #include "common.cuh"
 #include "internal.h"
@@ -30,7 +30,7 @@ namespace tsp {
 namespace {
 
 constexpr int HD = 128;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;  // warps 0-7 elementwise (two per TMEM lane quadrant), 8 TMA, 9 MMA
 constexpr uint32_t SUB64 = 64 * 64 * 2;     // [64 rows][64 cols] bf16, 8 KB
 constexpr uint32_t SUB128 = 128 * 64 * 2;   // [128 rows][64 cols] bf16, 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -117,13 +117,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&q_free[s], 1);
       mbar_init(&s_full[s], 1);
     }
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmQ);
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmQT);
     tma_prefetch_desc(&tmdOT);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // tensor memory).  The next score MMAs into buffer x are issued after those
   // MMAs, and one CTA's tcgen05 MMAs execute in issue order.
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint32_t qi = 0;
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (uint32_t n = first; n < qi; ++n) mbar_wait(&q_full[n & 1], (n >> 1) & 1, &dummy, p.err, CODE_DKDV | 3);
       if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_DKDV | 3);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, KB_QB);  // M = keys, N = queries
@@ -215,12 +215,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < KB_QB / 16; ++k) {
           const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64 + SUB128)) + 2 * k;
-          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 8 * k, bo, id_o, (acc || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bo, id_o,
+                       (acc || k > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < KB_QB / 16; ++k) {
           const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
-          umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * x + 8 * k, bq, id_o, (acc || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * x + 32 * (k / 2) + 8 * (k % 2), bq, id_o,
+                       (acc || k > 0) ? 1u : 0u);
         }
         umma_commit(&q_free[n & 1]);
       };
@@ -264,9 +266,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(drain, 0, &dummy, p.err, CODE_DKDV | 7);
     }
   } else {
-    // ---------------- elementwise warps 0-3: one key row per thread ----------------
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ------- elementwise warps 0-7: one key row, 32 of the 64 query columns per thread -------
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = kLog2e * rsqrtf((float)HD);
     const float scale = rsqrtf((float)HD);
     uint32_t scnt[2] = {0, 0};
@@ -285,28 +288,38 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        float sv[64], dp[64];
-        tmem_ld64(tmem_base + lane_off + 64 * x, sv);
-        tmem_ld64(tmem_base + lane_off + 128 + 64 * x, dp);
-        const int64_t q0 = k0 + (int64_t)i * KB_QB;
+        const uint32_t cS = tmem_base + lane_off + 64 * x + 32 * half;
+        const uint32_t cdP = tmem_base + lane_off + 128 + 64 * x + 32 * half;
+        float sv[32], dp[32];
+        tmem_ld32(cS, sv);
+        tmem_ld32(cdP, dp);
+        const int64_t q0 = k0 + (int64_t)i * KB_QB + 32 * half;  // first query of this thread's columns
         const bool diag = i < 2;
         // lse and dsum of this query block arrived with the stage (bulk copies)
-        const float* lse_s = reinterpret_cast<const float*>(stg + (qidx & 1) * KV_STAGE_BYTES + KV_STAGE_DATA);
-        const float* ds_s = lse_s + KB_QB;
-        uint32_t pk[32], dk2[32];
+        const float4* lse4 = reinterpret_cast<const float4*>(stg + (qidx & 1) * KV_STAGE_BYTES + KV_STAGE_DATA) + 8 * half;
+        const float4* ds4 = lse4 + KB_QB / 4;
+        uint32_t pk[16], dk2[16];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float pv0 = ex2f(fmaf(sv[c], sl2, -lse_s[c] * kLog2e));
-          float pv1 = ex2f(fmaf(sv[c + 1], sl2, -lse_s[c + 1] * kLog2e));
-          if (diag && q0 + c < key) pv0 = 0.f;
-          if (diag && q0 + c + 1 < key) pv1 = 0.f;
-          pk[c / 2] = pack_bf16x2(pv0, pv1);
-          dk2[c / 2] = pack_bf16x2(pv0 * (dp[c] - ds_s[c]), pv1 * (dp[c + 1] - ds_s[c + 1]));
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = lse4[c4], d4 = ds4[c4];
+          const float lv[4] = {l4.x * kLog2e, l4.y * kLog2e, l4.z * kLog2e, l4.w * kLog2e};
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 * 4 + e;
+            pv[e] = ex2f(fmaf(sv[c], sl2, -lv[e]));
+            if (diag && q0 + c < key) pv[e] = 0.f;
+          }
+          pk[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+          pk[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk2[2 * c4] = pack_bf16x2(pv[0] * (dp[c4 * 4] - dv[0]), pv[1] * (dp[c4 * 4 + 1] - dv[1]));
+          dk2[2 * c4 + 1] = pack_bf16x2(pv[2] * (dp[c4 * 4 + 2] - dv[2]), pv[3] * (dp[c4 * 4 + 3] - dv[3]));
         }
         ++qidx;
-        // P^T over S^T[x] and dS^T over dP^T[x] (first 32 columns each)
-        tmem_st32_nowait(tmem_base + lane_off + 64 * x, pk);
-        tmem_st32_nowait(tmem_base + lane_off + 128 + 64 * x, dk2);
+        // P^T over the start of this thread's S^T columns, dS^T over its dP^T columns
+        tmem_st16_nowait(cS, pk);
+        tmem_st16_nowait(cdP, dk2);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(ds_full);
@@ -315,13 +328,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DKDV | 10);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bh * p.S + key) * HD);
-      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bh * p.S + key) * HD);
+      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bh * p.S + key) * HD) + 8 * half;
+      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bh * p.S + key) * HD) + 8 * half;
 #pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {
+      for (int c32 = 0; c32 < 2; ++c32) {
         float a[32], d[32];
-        tmem_ld32(tmem_base + lane_off + 256 + 32 * c32, a);
-        tmem_ld32(tmem_base + lane_off + 384 + 32 * c32, d);
+        tmem_ld32(tmem_base + lane_off + 256 + 64 * half + 32 * c32, a);
+        tmem_ld32(tmem_base + lane_off + 384 + 64 * half + 32 * c32, d);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           dvrow[c32 * 4 + q] = make_uint4(pack_bf16x2(a[q * 8 + 0], a[q * 8 + 1]), pack_bf16x2(a[q * 8 + 2], a[q * 8 + 3]),
@@ -337,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
@@ -392,20 +405,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&k_free[s], 1);
       mbar_init(&s_full[s], 1);
     }
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmdO);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmKT);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -417,7 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // pairs) is written over the first 32 columns of S[x] and read from there by
   // the dQ MMA; MMAs of one CTA execute in issue order.
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       uint32_t ki = 0;
       int q_armed = 0;
@@ -454,7 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (uint32_t n = first; n < ki; ++n) mbar_wait(&k_full[n & 1], (n >> 1) & 1, &dummy, p.err, CODE_DQ | 3);
       if (q_armed) mbar_wait(q_full, (q_armed - 1) & 1, &dummy, p.err, CODE_DQ | 3);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, DQ_KB);
       constexpr uint32_t id_o = idesc_bf16_f32(128, HD);
@@ -481,7 +494,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < DQ_KB / 16; ++k) {
           const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
-          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 8 * k, bk, id_o, (acc || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bk, id_o,
+                       (acc || k > 0) ? 1u : 0u);
         }
         umma_commit(&k_free[n & 1]);
       };
@@ -522,8 +536,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(drain, 0, &dummy, p.err, CODE_DQ | 7);
     }
   } else {
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ------- elementwise warps 0-7: one query row, 32 of the 64 key columns per thread -------
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = kLog2e * rsqrtf((float)HD);
     const float scale = rsqrtf((float)HD);
     uint32_t scnt[2] = {0, 0};
@@ -544,21 +560,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        float sv[64], dp[64];
-        tmem_ld64(tmem_base + lane_off + 64 * x, sv);
-        tmem_ld64(tmem_base + lane_off + 128 + 64 * x, dp);
-        const int64_t key0 = (int64_t)j * DQ_KB;
-        const bool diag = key0 + DQ_KB - 1 > p0;
-        uint32_t dsk[32];
+        const uint32_t cS = tmem_base + lane_off + 64 * x + 32 * half;
+        float sv[32], dp[32];
+        tmem_ld32(cS, sv);
+        tmem_ld32(tmem_base + lane_off + 128 + 64 * x + 32 * half, dp);
+        const int64_t key0 = (int64_t)j * DQ_KB + 32 * half;
+        const bool diag = key0 + 31 > p0;
+        uint32_t dsk[16];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < 32; c += 2) {
           float pv0 = ex2f(fmaf(sv[c], sl2, -l2));
           float pv1 = ex2f(fmaf(sv[c + 1], sl2, -l2));
           if (diag && key0 + c > qpos) pv0 = 0.f;
           if (diag && key0 + c + 1 > qpos) pv1 = 0.f;
           dsk[c / 2] = pack_bf16x2(pv0 * (dp[c] - dsr), pv1 * (dp[c + 1] - dsr));
         }
-        tmem_st32_nowait(tmem_base + lane_off + 64 * x, dsk);  // dS over S[x]
+        tmem_st16_nowait(cS, dsk);  // dS over the start of this thread's S columns
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(ds_full);
@@ -567,11 +584,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DQ | 10);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(p.dq + (zrow0 + row) * p.h + head * HD);
+      uint4* dst = reinterpret_cast<uint4*>(p.dq + (zrow0 + row) * p.h + head * HD) + 8 * half;
 #pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {
+      for (int c32 = 0; c32 < 2; ++c32) {
         float a[32];
-        tmem_ld32(tmem_base + lane_off + 256 + 32 * c32, a);
+        tmem_ld32(tmem_base + lane_off + 256 + 64 * half + 32 * c32, a);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           dst[c32 * 4 + q] = make_uint4(
@@ -584,7 +601,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
