@@ -115,7 +115,7 @@ Layout layer_layout(const tsp_plan* p, int batch) {
 
 struct BwdLayout {
   size_t dyz, wd_c, dgu, dyzT, mzT, wgu_T, dhz, dguT, hzT, wo_c, doz, dhzT, ozT, dq, dk, dv, dsum, dqkv, wqkv_T,
-      dxz, dqkvT, xzT, vnat, qT, doT, kT, end;
+      dxz, dqkvT, xzT, vnat, end;
 };
 
 BwdLayout bwd_layout(const tsp_plan* p, int batch) {
@@ -150,9 +150,6 @@ BwdLayout bwd_layout(const tsp_plan* p, int batch) {
   L.dqkvT = take(T * 3 * h * e);
   L.xzT = take(T * h * e);
   L.vnat = take(T * h * e);  // V in [B][H][S][dh] when the forward saved it transposed
-  L.qT = take(T * h * e);    // transposed copies for the tensor-core attention backward
-  L.doT = take(T * h * e);
-  L.kT = take(T * h * e);
   L.end = o;
   return L;
 }
@@ -686,9 +683,6 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     v_nat = wb + L.vnat;
   }
   if (attn_bwd_tc_supported(p->head_dim, p->chunk)) {
-    TSP_TRY(tr(sv + A.qz, L.qT, T, h, "transpose Q"));
-    TSP_TRY(tr(wb + L.doz, L.doT, T, h, "transpose dO"));
-    TSP_TRY(tr(sv + A.k, L.kT, p->seq, p->head_dim, "transpose K", batch * p->heads));
     Prof pr("attention bwd", st);
     TSP_TRY(cuda_status(launch_attn_dsum(sv + A.oz, wb + L.doz, reinterpret_cast<float*>(wb + L.dsum), p->D, batch,
                                          p->heads, p->seq, p->chunk, st),
@@ -698,9 +692,6 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     ab.k = sv + A.k;
     ab.v = v_nat;
     ab.dO = wb + L.doz;
-    ab.qT = wb + L.qT;
-    ab.dOT = wb + L.doT;
-    ab.kT = wb + L.kT;
     ab.lse = reinterpret_cast<const float*>(sv + A.lse);
     ab.dsum = reinterpret_cast<const float*>(wb + L.dsum);
     ab.dq = wb + L.dq;

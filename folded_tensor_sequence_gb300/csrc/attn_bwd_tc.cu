@@ -4,18 +4,18 @@
 // Exact gradient of the forward (the TSP posts do not describe a backward):
 //   P = exp(S/sqrt(dh) - lse),  dP = dO V^T,  dS = P * (dP - rowsum(dO * O)),
 //   dV = P^T dO,  dK = dS^T Q / sqrt(dh),  dQ = dS K / sqrt(dh).
-// Two kernels, no atomics; every tensor-core operand is K-major and arrives
-// by TMA:
+// Two kernels, no atomics; every tensor-core operand arrives by TMA:
 //   dK/dV: one CTA per mirror pair of 128-key tiles (j, nk-1-j: together they
 //     see a constant number of query blocks).  K and V of the tile stay in
-//     shared memory; query blocks of 64 stream through a 2-stage ring holding
-//     Q, dO (for S^T = K Q^T, dP^T = V dO^T) and their transposes Q^T, dO^T
-//     (for dV += P^T dO, dK += dS^T Q).  TMEM: S^T and dP^T double-buffered
-//     (4 x 64 columns), dV and dK accumulators (2 x 128 columns).
+//     shared memory; query blocks of 64 stream through a 4-stage ring holding
+//     Q and dO, read as K-major operands by S^T = K Q^T, dP^T = V dO^T and as
+//     MN-major operands by dV += P^T dO, dK += dS^T Q.  TMEM: S^T and dP^T
+//     double-buffered (4 x 64 columns), dV and dK accumulators (2 x 128).
 //   dQ: one CTA per mirror pair of 128-query tiles (the forward's zigzag
 //     pairing: both tiles on the same rank).  Q and dO stay in shared memory;
-//     key blocks of 64 stream K, V (for S = Q K^T, dP = dO V^T) and K^T (for
-//     dQ += dS K).  TMEM: S and dP double-buffered, dQ accumulator.
+//     key blocks of 64 stream K and V (4-stage ring) for S = Q K^T,
+//     dP = dO V^T, with the K tile read again as the MN-major operand of
+//     dQ += dS K.  TMEM: S and dP double-buffered, dQ accumulator.
 // In both, warps 0-7 turn scores into P and dS (a TMEM lane = a row, split
 // over two threads of 32 columns each) and write them back into tensor memory
 // as packed bf16, where the accumulating MMAs read them as their A operand;
@@ -76,31 +76,31 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // dK, dV
 // ===========================================================================
 constexpr int KB_QB = 64;  // queries per block
-// stage: Q, dO (2 sub-tiles each), Q^T, dO^T, then lse and dsum of the block (256 B each)
-constexpr uint32_t KV_STAGE_DATA = 4 * SUB64 + 2 * SUB128;
+// stage: Q, dO (2 sub-tiles each), then lse and dsum of the block (256 B each)
+constexpr int QSTG = 4;
+constexpr uint32_t KV_STAGE_DATA = 4 * SUB64;
 constexpr uint32_t KV_STAGE_BYTES = KV_STAGE_DATA + 1024;  // keeps stages 1024-byte aligned
-constexpr size_t DKDV_SMEM = 1024 + 2 * 2 * SUB128 + 2 * (size_t)KV_STAGE_BYTES + 256;
+constexpr size_t DKDV_SMEM = 1024 + 2 * 2 * SUB128 + QSTG * (size_t)KV_STAGE_BYTES + 256;
 
 __global__ void __launch_bounds__(THREADS, 1)
     attn_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-                        const __grid_constant__ CUtensorMap tmQT, const __grid_constant__ CUtensorMap tmdOT,
                         const BwdTcParams p, int nk) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Ks = smem;                    // 2 x SUB128
   uint8_t* Vs = smem + 2 * SUB128;       // 2 x SUB128
-  uint8_t* stg = smem + 4 * SUB128;      // [2] stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * KV_STAGE_BYTES);
+  uint8_t* stg = smem + 4 * SUB128;      // [QSTG] stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + QSTG * KV_STAGE_BYTES);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_free = bars + 1;
-  uint64_t* q_full = bars + 2;   // [2]
-  uint64_t* q_free = bars + 4;   // [2]
-  uint64_t* s_full = bars + 6;   // [2]
-  uint64_t* ds_full = bars + 8;
-  uint64_t* o_done = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* q_full = bars + 2;   // [QSTG]
+  uint64_t* q_free = bars + 6;   // [QSTG]
+  uint64_t* s_full = bars + 10;  // [2]
+  uint64_t* ds_full = bars + 12;
+  uint64_t* o_done = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -112,11 +112,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(kv_free, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < QSTG; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_free[s], 1);
-      mbar_init(&s_full[s], 1);
     }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(ds_full, 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -128,8 +129,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmdO);
-    tma_prefetch_desc(&tmQT);
-    tma_prefetch_desc(&tmdOT);
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
@@ -163,8 +162,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const int nq = (int)((p.S - k0) / KB_QB);
         for (int i = 0; i < nq; ++i, ++qi) {
-          const int s = qi & 1;
-          if (!mbar_wait(&q_free[s], ((qi >> 1) & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 2)) {
+          const int s = qi % QSTG;
+          if (!mbar_wait(&q_free[s], ((qi / QSTG) & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 2)) {
             ok = false;
             break;
           }
@@ -176,26 +175,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(st + c * SUB64, &tmQ, head * HD + c * 64, (int)zr, &q_full[s]);
             tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmdO, head * HD + c * 64, (int)zr, &q_full[s]);
           }
-          tma_load_2d(st + 4 * SUB64, &tmQT, (int)zr, head * HD, &q_full[s]);
-          tma_load_2d(st + 4 * SUB64 + SUB128, &tmdOT, (int)zr, head * HD, &q_full[s]);
           bulk_load(st + KV_STAGE_DATA, p.lse + bh * p.S + q0, KB_QB * 4, &q_full[s]);
           bulk_load(st + KV_STAGE_DATA + KB_QB * 4, p.dsum + bh * p.S + q0, KB_QB * 4, &q_full[s]);
         }
       }
       volatile int dummy = 0;
-      const uint32_t first = qi > 2 ? qi - 2 : 0;
-      for (uint32_t n = first; n < qi; ++n) mbar_wait(&q_full[n & 1], (n >> 1) & 1, &dummy, p.err, CODE_DKDV | 3);
+      const uint32_t first = qi > QSTG ? qi - QSTG : 0;
+      for (uint32_t n = first; n < qi; ++n) mbar_wait(&q_full[n % QSTG], (n / QSTG) & 1, &dummy, p.err, CODE_DKDV | 3);
       if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_DKDV | 3);
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, KB_QB);  // M = keys, N = queries
-      constexpr uint32_t id_o = idesc_bf16_f32(128, HD);     // M = keys, N = head dim
+      constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // M = keys, N = head dim (B MN-major)
       uint32_t qi = 0, scnt0 = 0, scnt1 = 0;
       bool ok = true;
       auto scores = [&](uint32_t n, int x) {  // S^T = K Q^T, dP^T = V dO^T for query block n
-        uint8_t* st = stg + (n & 1) * KV_STAGE_BYTES;
+        uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
@@ -210,21 +207,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         umma_commit(&s_full[x]);
       };
-      auto accumulate = [&](uint32_t n, int x, bool acc) {  // dV += P^T dO, dK += dS^T Q for query block n
-        uint8_t* st = stg + (n & 1) * KV_STAGE_BYTES;
+      // dV += P^T dO, dK += dS^T Q for query block n: the Q / dO tiles of the
+      // stage serve as MN-major B operands (rows = queries = K dimension)
+      auto accumulate = [&](uint32_t n, int x, bool acc) {
+        uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < KB_QB / 16; ++k) {
-          const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64 + SUB128)) + 2 * k;
+          const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB64) + 2048 * k, SUB64);
           umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bo, id_o,
                        (acc || k > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < KB_QB / 16; ++k) {
-          const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
+          const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
           umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * x + 32 * (k / 2) + 8 * (k % 2), bq, id_o,
                        (acc || k > 0) ? 1u : 0u);
         }
-        umma_commit(&q_free[n & 1]);
+        umma_commit(&q_free[n % QSTG]);
       };
       uint32_t dscnt = 0;
       for (int t = 0; t < ntile && ok; ++t) {
@@ -233,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_DKDV | 4)) break;
         for (int i = 0; i < nq; ++i) {
           const uint32_t n = qi + i;
-          if (!mbar_wait(&q_full[n & 1], (n >> 1) & 1, abort_flag, p.err, CODE_DKDV | 5)) {
+          if (!mbar_wait(&q_full[n % QSTG], (n / QSTG) & 1, abort_flag, p.err, CODE_DKDV | 5)) {
             ok = false;
             break;
           }
@@ -273,7 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float sl2 = kLog2e * rsqrtf((float)HD);
     const float scale = rsqrtf((float)HD);
     uint32_t scnt[2] = {0, 0};
-    uint32_t qidx = 0;  // global query-block counter (stage = qidx & 1)
+    uint32_t qidx = 0;  // global query-block counter (stage = qidx % QSTG)
     bool alive = true;
     for (int t = 0; t < ntile && alive; ++t) {
       const int64_t k0 = (int64_t)tile_of(t) * 128;
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int64_t q0 = k0 + (int64_t)i * KB_QB + 32 * half;  // first query of this thread's columns
         const bool diag = i < 2;
         // lse and dsum of this query block arrived with the stage (bulk copies)
-        const float4* lse4 = reinterpret_cast<const float4*>(stg + (qidx & 1) * KV_STAGE_BYTES + KV_STAGE_DATA) + 8 * half;
+        const float4* lse4 = reinterpret_cast<const float4*>(stg + (qidx % QSTG) * KV_STAGE_BYTES + KV_STAGE_DATA) + 8 * half;
         const float4* ds4 = lse4 + KB_QB / 4;
         uint32_t pk[16], dk2[16];
 #pragma unroll
@@ -360,28 +359,29 @@ __global__ void __launch_bounds__(THREADS, 1)
 // dQ
 // ===========================================================================
 constexpr int DQ_KB = 64;  // keys per block
-constexpr uint32_t DQ_STAGE_BYTES = 4 * SUB64 + SUB128;  // K, V (2 sub each) + K^T
-constexpr size_t DQ_SMEM = 1024 + 4 * (size_t)SUB128 + 2 * (size_t)DQ_STAGE_BYTES + 256;
+constexpr int KSTG = 4;
+constexpr uint32_t DQ_STAGE_BYTES = 4 * SUB64;  // K, V (2 sub-tiles each)
+constexpr size_t DQ_SMEM = 1024 + 4 * (size_t)SUB128 + KSTG * (size_t)DQ_STAGE_BYTES + 256;
 
 __global__ void __launch_bounds__(THREADS, 1)
     attn_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                      const __grid_constant__ CUtensorMap tmKT, const BwdTcParams p, int n_tiles) {
+                      const BwdTcParams p, int n_tiles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = smem;                  // 2 x SUB128
   uint8_t* dOs = smem + 2 * SUB128;    // 2 x SUB128
-  uint8_t* stg = smem + 4 * SUB128;    // [2] stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * DQ_STAGE_BYTES);
+  uint8_t* stg = smem + 4 * SUB128;    // [KSTG] stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + KSTG * DQ_STAGE_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* q_free = bars + 1;
-  uint64_t* k_full = bars + 2;   // [2]
-  uint64_t* k_free = bars + 4;   // [2]
-  uint64_t* s_full = bars + 6;   // [2]
-  uint64_t* ds_full = bars + 8;
-  uint64_t* o_done = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* k_full = bars + 2;   // [KSTG]
+  uint64_t* k_free = bars + 6;   // [KSTG]
+  uint64_t* s_full = bars + 10;  // [2]
+  uint64_t* ds_full = bars + 12;
+  uint64_t* o_done = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -400,11 +400,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_free, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KSTG; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_free[s], 1);
-      mbar_init(&s_full[s], 1);
     }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(ds_full, 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -416,7 +417,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmdO);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmKT);
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
@@ -447,8 +447,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const int nkb = (int)((p0 + 128) / DQ_KB);
         for (int j = 0; j < nkb; ++j, ++ki) {
-          const int s = ki & 1;
-          if (!mbar_wait(&k_free[s], ((ki >> 1) & 1) ^ 1, abort_flag, p.err, CODE_DQ | 2)) {
+          const int s = ki % KSTG;
+          if (!mbar_wait(&k_free[s], ((ki / KSTG) & 1) ^ 1, abort_flag, p.err, CODE_DQ | 2)) {
             ok = false;
             break;
           }
@@ -459,22 +459,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(st + c * SUB64, &tmK, c * 64, krow, &k_full[s]);
             tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmV, c * 64, krow, &k_full[s]);
           }
-          tma_load_2d(st + 4 * SUB64, &tmKT, j * DQ_KB, (int)(bh * HD), &k_full[s]);
         }
       }
       volatile int dummy = 0;
-      const uint32_t first = ki > 2 ? ki - 2 : 0;
-      for (uint32_t n = first; n < ki; ++n) mbar_wait(&k_full[n & 1], (n >> 1) & 1, &dummy, p.err, CODE_DQ | 3);
+      const uint32_t first = ki > KSTG ? ki - KSTG : 0;
+      for (uint32_t n = first; n < ki; ++n) mbar_wait(&k_full[n % KSTG], (n / KSTG) & 1, &dummy, p.err, CODE_DQ | 3);
       if (q_armed) mbar_wait(q_full, (q_armed - 1) & 1, &dummy, p.err, CODE_DQ | 3);
     }
   } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, DQ_KB);
-      constexpr uint32_t id_o = idesc_bf16_f32(128, HD);
+      constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // B (K tile) MN-major
       uint32_t ki = 0, dscnt = 0;
       bool ok = true;
       auto scores = [&](uint32_t n, int x) {  // S = Q K^T, dP = dO V^T for key block n
-        uint8_t* st = stg + (n & 1) * DQ_STAGE_BYTES;
+        uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t aq = sdesc_kmajor_sw128(smem_u32(Qs + (k / 4) * SUB128)) + 2 * (k % 4);
@@ -489,15 +488,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         umma_commit(&s_full[x]);
       };
-      auto accumulate = [&](uint32_t n, int x, bool acc) {  // dQ += dS K for key block n
-        uint8_t* st = stg + (n & 1) * DQ_STAGE_BYTES;
+      auto accumulate = [&](uint32_t n, int x, bool acc) {  // dQ += dS K for key block n (K tile as MN-major B)
+        uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < DQ_KB / 16; ++k) {
-          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + 4 * SUB64)) + 2 * k;
+          const uint64_t bk = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
           umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bk, id_o,
                        (acc || k > 0) ? 1u : 0u);
         }
-        umma_commit(&k_free[n & 1]);
+        umma_commit(&k_free[n % KSTG]);
       };
       for (int t = 0; t < 2 && ok; ++t) {
         int64_t zrow0, p0;
@@ -506,7 +505,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(q_full, t & 1, abort_flag, p.err, CODE_DQ | 4)) break;
         for (int j = 0; j < nkb; ++j) {
           const uint32_t n = ki + j;
-          if (!mbar_wait(&k_full[n & 1], (n >> 1) & 1, abort_flag, p.err, CODE_DQ | 5)) {
+          if (!mbar_wait(&k_full[n % KSTG], (n / KSTG) & 1, abort_flag, p.err, CODE_DQ | 5)) {
             ok = false;
             break;
           }
@@ -617,13 +616,11 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream) {
   const int64_t T = (int64_t)a.B * a.S;
   const int h = a.H * HD;
   const int64_t kv_rows = (int64_t)a.B * a.H * a.S;
-  CUtensorMap mK128, mV128, mQ64, mdO64, mQT, mdOT, mQ128, mdO128, mK64, mV64, mKT;
+  CUtensorMap mK128, mV128, mQ64, mdO64, mQ128, mdO128, mK64, mV64;
   if (!make_tma_2d_bf16(&mK128, a.k, kv_rows, HD, HD, 128) || !make_tma_2d_bf16(&mV128, a.v, kv_rows, HD, HD, 128) ||
       !make_tma_2d_bf16(&mQ64, a.q, T, h, h, 64) || !make_tma_2d_bf16(&mdO64, a.dO, T, h, h, 64) ||
-      !make_tma_2d_bf16(&mQT, a.qT, h, T, T, 128) || !make_tma_2d_bf16(&mdOT, a.dOT, h, T, T, 128) ||
       !make_tma_2d_bf16(&mQ128, a.q, T, h, h, 128) || !make_tma_2d_bf16(&mdO128, a.dO, T, h, h, 128) ||
-      !make_tma_2d_bf16(&mK64, a.k, kv_rows, HD, HD, 64) || !make_tma_2d_bf16(&mV64, a.v, kv_rows, HD, HD, 64) ||
-      !make_tma_2d_bf16(&mKT, a.kT, (int64_t)a.B * a.H * HD, a.S, a.S, 128))
+      !make_tma_2d_bf16(&mK64, a.k, kv_rows, HD, HD, 64) || !make_tma_2d_bf16(&mV64, a.v, kv_rows, HD, HD, 64))
     return TSP_ERR_CUDA;
   static bool configured = false;
   if (!configured) {
@@ -649,11 +646,11 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream) {
   p.err = dev_error_word();
   const int nk = (int)(a.S / 128);
   dim3 g1((nk + 1) / 2, a.H, a.B);
-  attn_dkdv_tc_kernel<<<g1, THREADS, DKDV_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, mQT, mdOT, p, nk);
+  attn_dkdv_tc_kernel<<<g1, THREADS, DKDV_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk);
   if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
   const int n_tiles = (int)(a.C / 128);
   dim3 g2(a.D * n_tiles, a.H, a.B);
-  attn_dq_tc_kernel<<<g2, THREADS, DQ_SMEM, stream>>>(mQ128, mdO128, mK64, mV64, mKT, p, n_tiles);
+  attn_dq_tc_kernel<<<g2, THREADS, DQ_SMEM, stream>>>(mQ128, mdO128, mK64, mV64, p, n_tiles);
   return cudaGetLastError() == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
 }
 

@@ -176,12 +176,27 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B, fp32 accumulator,
-// both operands K-major: D format (bits 4-5) = 1 (f32), A format (7-9) = 1
-// (bf16), B format (10-12) = 1 (bf16), N >> 3 at bits 17-22, M >> 4 at 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Descriptor for an MN-major operand tile stored with the 128-byte swizzle:
+// rows are K indices (128 B = 64 consecutive MN elements each), 8-row groups
+// 1024 B apart (stride byte offset), and the 64-element MN chunks `mn_chunk_bytes`
+// apart (leading byte offset).  Advancing K by 16 rows moves the start by 2048 B.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_chunk_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(mn_chunk_bytes >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B, fp32 accumulator:
+// D format (bits 4-5) = 1 (f32), A format (7-9) = 1 (bf16), B format (10-12)
+// = 1 (bf16), A / B MN-major flags (bits 15 / 16, K-major when clear),
+// N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

@@ -115,16 +115,12 @@ tsp_status attn_bwd_bf16(const AttnBwdParams& p, cudaStream_t stream);
 cudaError_t launch_attn_dsum(const void* o, const void* dO, float* dsum, int D, int B, int H, int64_t S, int64_t C,
                              cudaStream_t stream);
 
-// tcgen05 attention backward (head_dim 128, chunk % 128 == 0): needs the
-// transposed copies qT, dOT ([h][T], zigzag token columns) and kT ([B][H][dh][S]).
+// tcgen05 attention backward (head_dim 128, chunk % 128 == 0).
 struct AttnBwdTcArgs {
   const void* q;    // zigzag [T][h]
   const void* k;    // [B][H][S][dh]
   const void* v;    // [B][H][S][dh]
   const void* dO;   // zigzag [T][h]
-  const void* qT;   // [h][T]
-  const void* dOT;  // [h][T]
-  const void* kT;   // [B][H][dh][S]
   const float* lse;
   const float* dsum;
   void* dq;
