@@ -114,8 +114,7 @@ Layout layer_layout(const tsp_plan* p, int batch) {
 }
 
 struct BwdLayout {
-  size_t dyz, wd_c, dgu, dyzT, mzT, wgu_T, dhz, dguT, hzT, wo_c, doz, dhzT, ozT, dq, dk, dv, dsum, dqkv, wqkv_T,
-      dxz, dqkvT, xzT, vnat, end;
+  size_t dyz, dgu, dhz, doz, dq, dk, dv, dsum, dqkv, dxz, vnat, end;
 };
 
 BwdLayout bwd_layout(const tsp_plan* p, int batch) {
@@ -128,27 +127,15 @@ BwdLayout bwd_layout(const tsp_plan* p, int batch) {
     return at;
   };
   L.dyz = take(T * h * e);
-  L.wd_c = take(F * h * e);
   L.dgu = take(T * 2 * F * e);
-  L.dyzT = take(T * h * e);
-  L.mzT = take(T * F * e);
-  L.wgu_T = take(2 * F * h * e);
   L.dhz = take(T * h * e);
-  L.dguT = take(T * 2 * F * e);
-  L.hzT = take(T * h * e);
-  L.wo_c = take(h * h * e);
   L.doz = take(T * h * e);
-  L.dhzT = take(T * h * e);
-  L.ozT = take(T * h * e);
   L.dq = take(T * h * e);
   L.dk = take(T * h * e);
   L.dv = take(T * h * e);
   L.dsum = take((size_t)batch * p->heads * p->seq * 4);
   L.dqkv = take(T * 3 * h * e);
-  L.wqkv_T = take(3 * h * h * e);
   L.dxz = take(T * h * e);
-  L.dqkvT = take(T * 3 * h * e);
-  L.xzT = take(T * h * e);
   L.vnat = take(T * h * e);  // V in [B][H][S][dh] when the forward saved it transposed
   L.end = o;
   return L;
@@ -262,11 +249,14 @@ bool use_tc_attention(const tsp_plan* p) {
   return p->dtype == TSP_BF16 && attn_tc_supported(p->head_dim, p->chunk);
 }
 
+// a_mn / b_mn: operand stored [K][M] / [K][N] (tensor-core path only).
 tsp_status run_gemm(const tsp_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K,
-                    EpiKind epi, const EpiParams& ep, cudaStream_t st, const char* what) {
+                    EpiKind epi, const EpiParams& ep, cudaStream_t st, const char* what, bool a_mn = false,
+                    bool b_mn = false) {
   Prof pr(what, st);
+  if (p->dtype != TSP_BF16 && (a_mn || b_mn)) return fail(TSP_ERR_UNSUPPORTED, "%s: MN-major fp32 GEMM", what);
   tsp_status s = p->dtype == TSP_BF16
-                     ? gemm_bf16_tc(A, lda, B, ldb, M, N, K, epi, ep, st)
+                     ? gemm_bf16_tc(A, lda, B, ldb, M, N, K, epi, ep, st, a_mn, b_mn)
                      : gemm_f32_simt(static_cast<const float*>(A), lda, static_cast<const float*>(B), ldb, M, N, K,
                                      epi, ep, st);
   if (s != TSP_OK) return fail(s, "%s GEMM (M=%d N=%d K=%d) failed: %s", what, M, N, K, tsp_status_string(s));
@@ -626,55 +616,56 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     Prof pr("permute dy", st);
     TSP_TRY(cuda_status(launch_zigzag_rows(dy, wb + L.dyz, h * eb, p->D, batch, p->seq, true, st), "permute dy"));
   }
-  TSP_TRY(tr(w->down, L.wd_c, h, F, "transpose W_down"));
+  // Every weight and activation is read in the layout it is stored in: the
+  // GEMM takes operands stored [K][M] / [K][N] (MN-major) where the product
+  // needs their transpose.
   {
     EpiParams e = base_epi(p, batch);
     e.out = wb + L.dgu;
     e.ldo = 2 * F;
     e.resid = sv + A.gu;
     e.ldr = 2 * F;
-    TSP_TRY(run_gemm(p, wb + L.dyz, h, wb + L.wd_c, h, T, F, h, EPI_DSWIGLU, e, st, "dM = dY Wd^T"));
+    // dM = dY Wd^T: B = W_down^T, i.e. the packed down weight [h][F] read MN-major
+    TSP_TRY(run_gemm(p, wb + L.dyz, h, w->down, F, T, F, h, EPI_DSWIGLU, e, st, "dM = dY Wd^T", false, true));
   }
-  TSP_TRY(tr(wb + L.dyz, L.dyzT, T, h, "transpose dY"));
-  TSP_TRY(tr(sv + A.mz, L.mzT, T, F, "transpose M"));
   {
     EpiParams e = base_epi(p, batch);
     e.out = dw->down;
     e.ldo = F;
-    TSP_TRY(run_gemm(p, wb + L.dyzT, T, wb + L.mzT, T, h, F, T, EPI_STORE, e, st, "dW_down"));
+    // dWd^T = dY^T M: A = dY [T][h], B = M [T][F], both MN-major
+    TSP_TRY(run_gemm(p, wb + L.dyz, h, sv + A.mz, F, h, F, T, EPI_STORE, e, st, "dW_down", true, true));
   }
-  TSP_TRY(tr(w->gate_up, L.wgu_T, 2 * F, h, "transpose W_gate_up"));
   {
     EpiParams e = base_epi(p, batch);
     e.out = wb + L.dhz;
     e.ldo = h;
     e.resid = wb + L.dyz;
     e.ldr = h;
-    TSP_TRY(run_gemm(p, wb + L.dgu, 2 * F, wb + L.wgu_T, 2 * F, T, h, 2 * F, EPI_RESID, e, st, "dH"));
+    // dH = dY + dGU Wgu: B = packed gate_up [2F][h] read MN-major
+    TSP_TRY(run_gemm(p, wb + L.dgu, 2 * F, w->gate_up, h, T, h, 2 * F, EPI_RESID, e, st, "dH", false, true));
   }
-  TSP_TRY(tr(wb + L.dgu, L.dguT, T, 2 * F, "transpose dGU"));
-  TSP_TRY(tr(sv + A.hz, L.hzT, T, h, "transpose H"));
   {
     EpiParams e = base_epi(p, batch);
     e.out = dw->gate_up;
     e.ldo = h;
-    TSP_TRY(run_gemm(p, wb + L.dguT, T, wb + L.hzT, T, 2 * F, h, T, EPI_STORE, e, st, "dW_gate_up"));
+    // dWgu = dGU^T H: A = dGU [T][2F], B = H [T][h], both MN-major
+    TSP_TRY(run_gemm(p, wb + L.dgu, 2 * F, sv + A.hz, h, 2 * F, h, T, EPI_STORE, e, st, "dW_gate_up", true,
+                     true));
   }
   // attention output projection backward
-  TSP_TRY(tr(w->o, L.wo_c, h, h, "transpose W_O"));
   {
     EpiParams e = base_epi(p, batch);
     e.out = wb + L.doz;
     e.ldo = h;
-    TSP_TRY(run_gemm(p, wb + L.dhz, h, wb + L.wo_c, h, T, h, h, EPI_STORE, e, st, "dO"));
+    // dO = dH Wo^T: B = packed o [h][h] read MN-major
+    TSP_TRY(run_gemm(p, wb + L.dhz, h, w->o, h, T, h, h, EPI_STORE, e, st, "dO", false, true));
   }
-  TSP_TRY(tr(wb + L.dhz, L.dhzT, T, h, "transpose dH"));
-  TSP_TRY(tr(sv + A.oz, L.ozT, T, h, "transpose O"));
   {
     EpiParams e = base_epi(p, batch);
     e.out = dw->o;
     e.ldo = h;
-    TSP_TRY(run_gemm(p, wb + L.dhzT, T, wb + L.ozT, T, h, h, T, EPI_STORE, e, st, "dW_O"));
+    // dWo^T = dH^T O: A = dH [T][h], B = O [T][h], both MN-major
+    TSP_TRY(run_gemm(p, wb + L.dhz, h, sv + A.oz, h, h, h, T, EPI_STORE, e, st, "dW_O", true, true));
   }
   // attention core backward
   const void* v_nat = sv + A.v;
@@ -735,22 +726,21 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
                                              p->heads, p->head_dim, st),
                         "assemble dQKV"));
   }
-  TSP_TRY(tr(w->qkv, L.wqkv_T, 3 * h, h, "transpose W_QKV"));
   {
     EpiParams e = base_epi(p, batch);
     e.out = wb + L.dxz;
     e.ldo = h;
     e.resid = wb + L.dhz;
     e.ldr = h;
-    TSP_TRY(run_gemm(p, wb + L.dqkv, 3 * h, wb + L.wqkv_T, 3 * h, T, h, 3 * h, EPI_RESID, e, st, "dx"));
+    // dx = dH + dQKV Wqkv: B = packed qkv [3h][h] read MN-major
+    TSP_TRY(run_gemm(p, wb + L.dqkv, 3 * h, w->qkv, h, T, h, 3 * h, EPI_RESID, e, st, "dx", false, true));
   }
-  TSP_TRY(tr(wb + L.dqkv, L.dqkvT, T, 3 * h, "transpose dQKV"));
-  TSP_TRY(tr(sv + A.xz, L.xzT, T, h, "transpose xz"));
   {
     EpiParams e = base_epi(p, batch);
     e.out = dw->qkv;
     e.ldo = h;
-    TSP_TRY(run_gemm(p, wb + L.dqkvT, T, wb + L.xzT, T, 3 * h, h, T, EPI_STORE, e, st, "dW_QKV"));
+    // dWqkv = dQKV^T xz: A = dQKV [T][3h], B = xz [T][h], both MN-major
+    TSP_TRY(run_gemm(p, wb + L.dqkv, 3 * h, sv + A.xz, h, 3 * h, h, T, EPI_STORE, e, st, "dW_QKV", true, true));
   }
   Prof pr_dx("unpermute dx", st);
   return cuda_status(launch_zigzag_rows(wb + L.dxz, dx, h * eb, p->D, batch, p->seq, false, st), "unpermute dx");

@@ -106,7 +106,10 @@ __device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep
   p = (k < ep.C) ? (int64_t)r * ep.C + k : (int64_t)(2 * ep.D - 1 - r) * ep.C + (k - ep.C);
 }
 
-template <int EPI>
+// AMN / BMN: the operand is MN-major (global [K][M] / [K][N], M / N
+// contiguous), loaded as 64-wide boxes of [64 K rows][64 elements] into 8 KB
+// chunks and described with the MN-major 128-byte-swizzle descriptor.
+template <int EPI, bool AMN, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmShape shape, const EpiParams ep) {
@@ -168,8 +171,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-          tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, &full[s]);
-          tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
+          if constexpr (AMN) {
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              tma_load_2d(smA + s * A_STAGE_BYTES + c * 8192, &tmA, mt * BM + c * 64, kb * BK, &full[s]);
+          } else {
+            tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, &full[s]);
+          }
+          if constexpr (BMN) {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(smB + s * B_STAGE_BYTES + c * 8192, &tmB, nt * BN + c * 64, kb * BK, &full[s]);
+          } else {
+            tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
+          }
         }
       }
       // Before leaving, make sure every copy this thread issued has landed
@@ -184,7 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, AMN, BMN);
       uint32_t it = 0, tl = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < shape.num_tiles && ok; t += gridDim.x, ++tl) {
@@ -201,12 +216,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(smA + s * A_STAGE_BYTES));
-          const uint64_t bdesc = sdesc_kmajor_sw128(smem_u32(smB + s * B_STAGE_BYTES));
+          const uint32_t sa = smem_u32(smA + s * A_STAGE_BYTES), sb = smem_u32(smB + s * B_STAGE_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            // +32 bytes along K inside the 128-byte swizzle atom = +2 in the >>4 address field.
-            umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+            // K-major: +32 bytes along K inside the 128-byte swizzle atom (+2 in the >>4 field);
+            // MN-major: +16 K rows = +2048 bytes.
+            const uint64_t adesc = AMN ? sdesc_mn_sw128(sa + 2048 * k, 8192) : sdesc_kmajor_sw128(sa) + 2 * k;
+            const uint64_t bdesc = BMN ? sdesc_mn_sw128(sb + 2048 * k, 8192) : sdesc_kmajor_sw128(sb) + 2 * k;
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
           }
           umma_commit(&empty[s]);
         }
@@ -372,30 +389,33 @@ bool make_tma_2d_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t co
 
 namespace {
 
-template <int EPI>
+template <int EPI, bool AMN, bool BMN>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& s, const EpiParams& ep,
                        cudaStream_t stream) {
   static bool configured = false;  // per-process; attribute is per function
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, AMN, BMN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int grid = s.num_tiles < num_sms() ? s.num_tiles : num_sms();
-  gemm_bf16_tc_kernel<EPI><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, s, ep);
+  gemm_bf16_tc_kernel<EPI, AMN, BMN><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, s, ep);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K, EpiKind epi,
-                        const EpiParams& ep, cudaStream_t stream) {
+                        const EpiParams& ep, cudaStream_t stream, bool a_mn, bool b_mn) {
   if (M <= 0 || N <= 0 || K <= 0) return TSP_OK;
   if (N % BN || K % BK || lda % 8 || ldb % 8) return TSP_ERR_UNSUPPORTED;
+  if (a_mn && M % 64) return TSP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) return TSP_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
-  if (!make_tma_2d_bf16(&ta, A, M, K, lda, BM) || !make_tma_2d_bf16(&tb, B, N, K, ldb, BN)) return TSP_ERR_CUDA;
+  const bool ok_a = a_mn ? make_tma_2d_bf16(&ta, A, K, M, lda, 64) : make_tma_2d_bf16(&ta, A, M, K, lda, BM);
+  const bool ok_b = b_mn ? make_tma_2d_bf16(&tb, B, K, N, ldb, 64) : make_tma_2d_bf16(&tb, B, N, K, ldb, BN);
+  if (!ok_a || !ok_b) return TSP_ERR_CUDA;
   GemmShape s;
   s.M = M;
   s.N = N;
@@ -410,13 +430,18 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
     s.group_m = gm < 1 ? 1 : (gm > s.num_m ? s.num_m : gm);
   }
   cudaError_t e;
-  switch (epi) {
-    case EPI_STORE: e = launch_epi<EPI_STORE>(ta, tb, s, ep, stream); break;
-    case EPI_RESID: e = launch_epi<EPI_RESID>(ta, tb, s, ep, stream); break;
-    case EPI_QKV: e = launch_epi<EPI_QKV>(ta, tb, s, ep, stream); break;
-    case EPI_SWIGLU: e = launch_epi<EPI_SWIGLU>(ta, tb, s, ep, stream); break;
-    case EPI_DSWIGLU: e = launch_epi<EPI_DSWIGLU>(ta, tb, s, ep, stream); break;
-    default: return TSP_ERR_INVALID_ARG;
+  const int mode = (a_mn ? 2 : 0) | (b_mn ? 1 : 0);
+  switch (epi * 4 + mode) {
+    case EPI_STORE * 4 + 0: e = launch_epi<EPI_STORE, false, false>(ta, tb, s, ep, stream); break;
+    case EPI_STORE * 4 + 1: e = launch_epi<EPI_STORE, false, true>(ta, tb, s, ep, stream); break;
+    case EPI_STORE * 4 + 3: e = launch_epi<EPI_STORE, true, true>(ta, tb, s, ep, stream); break;
+    case EPI_RESID * 4 + 0: e = launch_epi<EPI_RESID, false, false>(ta, tb, s, ep, stream); break;
+    case EPI_RESID * 4 + 1: e = launch_epi<EPI_RESID, false, true>(ta, tb, s, ep, stream); break;
+    case EPI_QKV * 4 + 0: e = launch_epi<EPI_QKV, false, false>(ta, tb, s, ep, stream); break;
+    case EPI_SWIGLU * 4 + 0: e = launch_epi<EPI_SWIGLU, false, false>(ta, tb, s, ep, stream); break;
+    case EPI_DSWIGLU * 4 + 0: e = launch_epi<EPI_DSWIGLU, false, false>(ta, tb, s, ep, stream); break;
+    case EPI_DSWIGLU * 4 + 1: e = launch_epi<EPI_DSWIGLU, false, true>(ta, tb, s, ep, stream); break;
+    default: return TSP_ERR_UNSUPPORTED;
   }
   return e == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
 }

@@ -56,10 +56,13 @@ tsp_status report_error(tsp_status s, const char* msg);
 unsigned int* dev_error_word();  // device address of this device's error word (nullptr on failure)
 
 // bf16 tcgen05 GEMM: C[M][N] = sum_k A[m][k] B[n][k] with fp32 accumulation in
-// tensor memory; row strides lda/ldb in elements.  Needs N % 256 == 0,
-// K % 64 == 0, 16-byte aligned rows.
+// tensor memory.  A is stored [M][K] (row stride lda), or with a_mn [K][M]
+// (row stride lda, M contiguous); likewise B [N][K] or, with b_mn, [K][N].
+// Needs N % 256 == 0, K % 64 == 0 (and M % 64 == 0 with a_mn), 16-byte
+// aligned rows.
 tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, int M, int N, int K,
-                        EpiKind epi, const EpiParams& ep, cudaStream_t stream);
+                        EpiKind epi, const EpiParams& ep, cudaStream_t stream, bool a_mn = false,
+                        bool b_mn = false);
 
 // 2-D bf16 TMA descriptor: row-major [rows][cols], row stride ld elements,
 // box = 64 columns x box_rows rows, 128-byte swizzle.
