@@ -85,31 +85,18 @@ def step_work(cfg):
         "zigzag unpermute": (0, 2 * T * h * e, 1),
     }
     if cfg.backward:
-        tr = lambda r, c: (0, 2 * r * c * e, 1)  # noqa: E731
         w.update({
             "permute dy": (0, 2 * T * h * e, 1),
-            "transpose W_down": tr(h, F),
             "dM = dY Wd^T": (2 * T * h * F, (T * h + F * h + 4 * T * F) * e, 1),
-            "transpose dY": tr(T, h),
-            "transpose M": tr(T, F),
             "dW_down": (2 * h * F * T, (T * h + T * F + h * F) * e, 1),
-            "transpose W_gate_up": tr(2 * F, h),
             "dH": (2 * T * 2 * F * h, (2 * T * F + 2 * F * h + 2 * T * h) * e, 1),
-            "transpose dGU": tr(T, 2 * F),
-            "transpose H": tr(T, h),
             "dW_gate_up": (2 * 2 * F * h * T, (2 * T * F + T * h + 2 * F * h) * e, 1),
-            "transpose W_O": tr(h, h),
             "dO": (2 * T * h * h, (2 * T * h + h * h) * e, 1),
-            "transpose dH": tr(T, h),
-            "transpose O": tr(T, h),
             "dW_O": (2 * h * h * T, (2 * T * h + h * h) * e, 1),
-            "transpose V^T": tr(T, h),
+            "transpose V^T": (0, 2 * T * h * e, 1),
             "attention bwd": (2 * attn, 7 * T * h * e, 3),
             "assemble dQKV": (0, 6 * T * h * e, 1),
-            "transpose W_QKV": tr(3 * h, h),
             "dx": (2 * T * 3 * h * h, (3 * T * h + 3 * h * h + 2 * T * h) * e, 1),
-            "transpose dQKV": tr(T, 3 * h),
-            "transpose xz": tr(T, h),
             "dW_QKV": (2 * 3 * h * h * T, (3 * T * h + T * h + 3 * h * h) * e, 1),
             "unpermute dx": (0, 2 * T * h * e, 1),
         })
