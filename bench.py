@@ -95,6 +95,9 @@ def step_work(cfg):
             "dW_O": (2 * h * h * T, (2 * T * h + h * h) * e, 1),
             "transpose V^T": (0, 2 * T * h * e, 1),
             "attention bwd": (2 * attn, 7 * T * h * e, 3),
+            "attention bwd dsum": (0, 2 * T * h * e, 1),
+            "attention bwd dK/dV": (attn, 6 * T * h * e, 1),
+            "attention bwd dQ": (attn // 2, 5 * T * h * e, 1),
             "assemble dQKV": (0, 6 * T * h * e, 1),
             "dx": (2 * T * 3 * h * h, (3 * T * h + 3 * h * h + 2 * T * h) * e, 1),
             "dW_QKV": (2 * 3 * h * h * T, (3 * T * h + T * h + 3 * h * h) * e, 1),

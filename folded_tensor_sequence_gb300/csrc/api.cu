@@ -674,10 +674,12 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     v_nat = wb + L.vnat;
   }
   if (attn_bwd_tc_supported(p->head_dim, p->chunk)) {
-    Prof pr("attention bwd", st);
-    TSP_TRY(cuda_status(launch_attn_dsum(sv + A.oz, wb + L.doz, reinterpret_cast<float*>(wb + L.dsum), p->D, batch,
+    {
+      Prof pr("attention bwd dsum", st);
+      TSP_TRY(cuda_status(launch_attn_dsum(sv + A.oz, wb + L.doz, reinterpret_cast<float*>(wb + L.dsum), p->D, batch,
                                          p->heads, p->seq, p->chunk, st),
-                        "attention dsum"));
+                          "attention dsum"));
+    }
     AttnBwdTcArgs ab;
     ab.q = sv + A.qz;
     ab.k = sv + A.k;
@@ -694,7 +696,14 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     ab.dh = p->head_dim;
     ab.S = p->seq;
     ab.C = p->chunk;
-    s = attn_bwd_bf16_tc(ab, st);
+    {
+      Prof pr("attention bwd dK/dV", st);
+      s = attn_bwd_bf16_tc(ab, st, 1);
+    }
+    if (s == TSP_OK) {
+      Prof pr("attention bwd dQ", st);
+      s = attn_bwd_bf16_tc(ab, st, 2);
+    }
     if (s != TSP_OK) return fail(s, "attention backward (tensor cores) failed: %s", tsp_status_string(s));
   } else {
     AttnBwdParams ab;

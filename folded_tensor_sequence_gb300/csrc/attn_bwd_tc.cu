@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 bool attn_bwd_tc_supported(int head_dim, int64_t chunk) { return head_dim == HD && chunk % 128 == 0; }
 
-tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream) {
+tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int which) {
   if (!attn_bwd_tc_supported(a.dh, a.C)) return TSP_ERR_UNSUPPORTED;
   if ((int64_t)a.B * a.S == 0) return TSP_OK;
   const int64_t T = (int64_t)a.B * a.S;
@@ -646,8 +646,11 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream) {
   p.err = dev_error_word();
   const int nk = (int)(a.S / 128);
   dim3 g1((nk + 1) / 2, a.H, a.B);
-  attn_dkdv_tc_kernel<<<g1, THREADS, DKDV_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk);
-  if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
+  if (which & 1) {
+    attn_dkdv_tc_kernel<<<g1, THREADS, DKDV_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk);
+    if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
+  }
+  if (!(which & 2)) return TSP_OK;
   const int n_tiles = (int)(a.C / 128);
   dim3 g2(a.D * n_tiles, a.H, a.B);
   attn_dq_tc_kernel<<<g2, THREADS, DQ_SMEM, stream>>>(mQ128, mdO128, mK64, mV64, p, n_tiles);

@@ -133,7 +133,8 @@ struct AttnBwdTcArgs {
   int64_t S, C;
 };
 bool attn_bwd_tc_supported(int head_dim, int64_t chunk);
-tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream);
+// which: 1 = the dK/dV kernel, 2 = the dQ kernel, 3 = both.
+tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int which = 3);
 
 // Backward helpers.
 cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
