@@ -52,5 +52,9 @@ LAYER_7B_S64K = LayerConfig("bf16_D8_b1_s65536_h4096", D=8, batch=1, seq=65536, 
 TRAIN_7B_S8K = LayerConfig("bf16_fwdbwd_D8_b1_s8192_h4096", D=8, batch=1, seq=8192, hidden=4096,
                            heads=32, head_dim=128, ffn=14336, dtype="bf16", backward=True)
 
-ALL = [TINY_F32, MID_BF16, LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_S8K]
+# Backward at the 16K-token shape (training step, no optimizer).
+TRAIN_7B_S16K = LayerConfig("bf16_fwdbwd_D8_b2_s16384_h4096", D=8, batch=2, seq=16384, hidden=4096, heads=32,
+                            head_dim=128, ffn=14336, dtype="bf16", backward=True)
+
+ALL = [TINY_F32, MID_BF16, LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_S8K, TRAIN_7B_S16K]
 BY_NAME = {c.name: c for c in ALL}

@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 from folded_tensor_sequence_gb300 import synth
-from folded_tensor_sequence_gb300.configs import LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_S8K
+from folded_tensor_sequence_gb300.configs import LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_S8K, TRAIN_7B_S16K
 from oracle import tsp_oracle as O
 
 from helpers import check, rel_frob, to_np
@@ -139,3 +139,45 @@ def test_training_workload_backward(tsp):
     check(to_np(dx), rdx, "bf16", "dx")
     for k in tsp.CANONICAL:
         check(to_np(g[k]), rg[k], "bf16", f"d{k}")
+
+
+def gpu_backward(tsp, cfg, t, D):
+    import torch
+
+    B = cfg.batch
+    plan = tsp.tsp_plan_create(D, cfg.seq, cfg.hidden, cfg.heads, cfg.head_dim, cfg.ffn, "bf16")
+    canon = {k: t[k].cuda() for k in tsp.CANONICAL}
+    packed = tsp.empty_packed(plan)
+    tsp.tsp_pack_weights(plan, canon, packed)
+    x, dy = t["x"].cuda(), t["dY"].cuda()
+    y = torch.empty_like(x)
+    saved = torch.empty(tsp.tsp_saved_bytes(plan, B), dtype=torch.uint8, device="cuda")
+    tsp.tsp_layer_fwd(plan, B, x, packed, y, saved, tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD))
+    dx = torch.empty_like(x)
+    grads = tsp.empty_packed(plan)
+    tsp.tsp_layer_bwd(plan, B, x, packed, saved, dy, dx, grads, tsp.workspace(plan, B, tsp.TSP_OP_LAYER_BWD))
+    g = {k: torch.empty_like(v) for k, v in canon.items()}
+    tsp.tsp_unpack_weights(plan, grads, g)
+    tsp.tsp_sync_check()
+    out = {"dx": to_np(dx)}
+    out.update({k: to_np(v) for k, v in g.items()})
+    del saved, packed, canon
+    torch.cuda.empty_cache()
+    return out
+
+
+def test_backward_16k_tokens_agrees_across_D(tsp):
+    """Backward at batch 2 x 16384 tokens: D = 2 and 4 against D = 8 on dx and every weight gradient.
+
+    No fp64 reference at this size (its gradient would take hours); the
+    D = 8 run itself is pinned at 8K tokens by test_training_workload_backward.
+    """
+    cfg = TRAIN_7B_S16K
+    t = draw(cfg, with_dy=True)
+    ref = gpu_backward(tsp, cfg, t, 8)
+    for D in (2, 4):
+        got = gpu_backward(tsp, cfg, t, D)
+        for k in ref:
+            e = rel_frob(got[k], ref[k])
+            print(f"PARITY cross-D {D} vs 8 {k}: relative Frobenius {e:.3e}")
+            assert e <= 2e-2, (D, k, e)
