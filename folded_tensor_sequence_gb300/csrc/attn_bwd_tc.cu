@@ -97,10 +97,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* q_full = bars + 2;   // [QSTG]
   uint64_t* q_free = bars + 6;   // [QSTG]
   uint64_t* s_full = bars + 10;  // [2]
+  // [2], one per TMEM buffer: the score MMAs of block i+1 are issued before the
+  // MMA thread waits for block i's elementwise results, so a fast warp may
+  // already arrive for block i+1 while a slow one still works on block i;
+  // separate barriers keep those arrivals apart.
   uint64_t* ds_full = bars + 12;
-  uint64_t* o_done = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* o_done = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -118,7 +122,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(ds_full, 256);
+    mbar_init(&ds_full[0], 256);
+    mbar_init(&ds_full[1], 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         umma_commit(&q_free[n % QSTG]);
       };
-      uint32_t dscnt = 0;
+      uint32_t dscnt[2] = {0, 0};
       for (int t = 0; t < ntile && ok; ++t) {
         const int64_t k0 = (int64_t)tile_of(t) * 128;
         const int nq = (int)((p.S - k0) / KB_QB);
@@ -240,18 +245,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           scores(n, i & 1);
           if (i & 1) ++scnt1; else ++scnt0;
           if (i > 0) {
-            if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DKDV | 6)) {
+            const int xp = (i - 1) & 1;
+            if (!mbar_wait(&ds_full[xp], dscnt[xp] & 1, abort_flag, p.err, CODE_DKDV | 6)) {
               ok = false;
               break;
             }
-            ++dscnt;
+            ++dscnt[xp];
             tc_fence_after();
             accumulate(n - 1, (i - 1) & 1, i - 1 > 0);
           }
         }
         if (!ok) break;
-        if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DKDV | 6)) break;
-        ++dscnt;
+        const int xl = (nq - 1) & 1;
+        if (!mbar_wait(&ds_full[xl], dscnt[xl] & 1, abort_flag, p.err, CODE_DKDV | 6)) break;
+        ++dscnt[xl];
         tc_fence_after();
         accumulate(qi + nq - 1, (nq - 1) & 1, nq - 1 > 0);
         umma_commit(o_done);
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st16_nowait(cdP, dk2);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(&ds_full[x]);
       }
       if (!alive) break;
       const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DKDV | 10);
@@ -378,10 +385,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* k_full = bars + 2;   // [KSTG]
   uint64_t* k_free = bars + 6;   // [KSTG]
   uint64_t* s_full = bars + 10;  // [2]
+  // [2], one per TMEM buffer: the score MMAs of block i+1 are issued before the
+  // MMA thread waits for block i's elementwise results, so a fast warp may
+  // already arrive for block i+1 while a slow one still works on block i;
+  // separate barriers keep those arrivals apart.
   uint64_t* ds_full = bars + 12;
-  uint64_t* o_done = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* o_done = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -406,7 +417,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(ds_full, 256);
+    mbar_init(&ds_full[0], 256);
+    mbar_init(&ds_full[1], 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -470,7 +482,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, DQ_KB);
       constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // B (K tile) MN-major
-      uint32_t ki = 0, dscnt = 0;
+      uint32_t ki = 0, dscnt[2] = {0, 0};
       bool ok = true;
       auto scores = [&](uint32_t n, int x) {  // S = Q K^T, dP = dO V^T for key block n
         uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
@@ -512,18 +524,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           scores(n, j & 1);
           if (j > 0) {
-            if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DQ | 6)) {
+            const int xp = (j - 1) & 1;
+            if (!mbar_wait(&ds_full[xp], dscnt[xp] & 1, abort_flag, p.err, CODE_DQ | 6)) {
               ok = false;
               break;
             }
-            ++dscnt;
+            ++dscnt[xp];
             tc_fence_after();
             accumulate(n - 1, (j - 1) & 1, j - 1 > 0);
           }
         }
         if (!ok) break;
-        if (!mbar_wait(ds_full, dscnt & 1, abort_flag, p.err, CODE_DQ | 6)) break;
-        ++dscnt;
+        const int xl = (nkb - 1) & 1;
+        if (!mbar_wait(&ds_full[xl], dscnt[xl] & 1, abort_flag, p.err, CODE_DQ | 6)) break;
+        ++dscnt[xl];
         tc_fence_after();
         accumulate(ki + nkb - 1, (nkb - 1) & 1, nkb - 1 > 0);
         umma_commit(o_done);
@@ -577,7 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st16_nowait(cS, dsk);  // dS over the start of this thread's S columns
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(&ds_full[x]);
       }
       if (!alive) break;
       const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DQ | 10);
