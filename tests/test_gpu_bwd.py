@@ -65,3 +65,22 @@ def test_backward_matches_oracle(tsp, cfg):
     check(dx, rdx, "bf16", f"{cfg.name} dx")
     for k in tsp.CANONICAL:
         check(g[k], rg[k], "bf16", f"{cfg.name} d{k}")
+
+
+def test_forward_and_backward_are_bitwise_deterministic(tsp):
+    """No kernel uses atomics, so repeated runs must agree bit for bit; a
+    barrier or ordering race would show up here as run-to-run differences."""
+    import torch
+
+    cfg = LayerConfig("det_D8_s4096", D=8, batch=1, seq=4096, hidden=1024, heads=8, head_dim=128, ffn=1024,
+                      dtype="bf16")
+    inp = synth.layer_inputs(cfg, seed=9, with_dy=True)
+    runs = []
+    for _ in range(3):
+        y, dx, g = run_bwd(tsp, cfg, inp)
+        runs.append((y, dx, g))
+    for y, dx, g in runs[1:]:
+        assert np.array_equal(y, runs[0][0])
+        assert np.array_equal(dx, runs[0][1])
+        for k in g:
+            assert np.array_equal(g[k], runs[0][2][k]), k
