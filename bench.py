@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # counters were taken (one-pass capture of the full-size launch, see
 # profiles/); if the source has changed since, the traffic is reported as null.
 NCU_TRAFFIC = {
-    "gate/up projection": (2.16e9 + 0.927e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "2be9988fc84071f1"),
+    "gate/up projection": (2.16e9 + 0.927e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "44dc85bc6217b676"),
     "attention": (0.841e9 + 0.253e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "1401fedc4fa023e7"),
 }
 
