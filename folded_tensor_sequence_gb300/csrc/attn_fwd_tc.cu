@@ -14,15 +14,18 @@
 // the mirror pair of blocks (G, 2D*nb-1-G), which lie in chunks c and 2D-1-c
 // of the same rank, so every CTA does the same number of key tiles.
 //
-// Per CTA: warp 8 issues TMA loads (both blocks' Q tiles up front, then K_j /
-// V_j^T tiles through a 3-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
+// Per CTA: warp 8 issues TMA loads (a block's Q tiles, then K_j / V_j^T tiles
+// through a 5-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
 // are the softmax warpgroups of tiles A and B.  TMEM (512 columns): S_A, S_B,
 // O_A, O_B, 128 fp32 columns each.  Issue order per key tile j:
 //   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 // so the tensor core works on one tile while the other tile's softmax runs.
+// The softmax warpgroups hand P_x(j) over through named barriers (the MMA
+// warp never waits on an mbarrier inside a block; the handing-over warpgroup
+// has checked the K/V tiles that the following MMAs read).
 // P = exp2(S*log2e/sqrt(dh) - m) is written as packed bf16 back into the first
 // 64 columns of S's TMEM and consumed from there by the PV MMA (A operand in
-// tensor memory), which leaves shared memory for double-buffered Q tiles.  The running max is only
+// tensor memory), which leaves shared memory for a deep K/V ring.  The running max is only
 // raised (and O rescaled in TMEM) when it grows by more than 2^8, which keeps
 // P <= 256 and makes the rescale rare.
 #include "common.cuh"
@@ -35,14 +38,18 @@ namespace {
 constexpr int QT = 128;    // rows per query tile (MMA M)
 constexpr int KT = 128;    // keys per key tile
 constexpr int HD = 128;    // head dim
-constexpr int STAGES = 3;  // K / V^T tile ring
+constexpr int STAGES = 5;  // K / V^T tile ring
 constexpr int THREADS = 320;
 constexpr uint32_t SUB_BYTES = 128 * 64 * 2;     // one [128][64] bf16 swizzled sub-tile
 constexpr uint32_t TILE_BYTES = 2 * SUB_BYTES;   // [128][128]
-constexpr size_t SMEM_BYTES = 1024 + (4 + STAGES) * (size_t)TILE_BYTES + 256;
+constexpr size_t SMEM_BYTES = 1024 + (2 + STAGES) * (size_t)TILE_BYTES + 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Named barriers handing P_x(j) from softmax warpgroup x to the MMA warp,
+// two per tile (alternating with j): A uses 1-2, B uses 3-4.
+constexpr int kBarPA = 1, kBarPB = 3;
+constexpr int kHandoffThreads = 128 + 32;
 
 struct FaParams {
   int B, H, D, nb;  // nb = 256-query blocks per chunk
@@ -140,15 +147,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                        const __grid_constant__ CUtensorMap tmVt, const FaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Qs = smem;                                   // [2 blocks][2 tiles]
-  uint8_t* KVs = smem + 4 * TILE_BYTES;                 // [STAGES] tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (4 + STAGES) * TILE_BYTES);
+  uint8_t* Qs = smem;                                   // [2 tiles], block 0 then block 1
+  uint8_t* KVs = smem + 2 * TILE_BYTES;                 // [STAGES] tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + STAGES) * TILE_BYTES);
   uint64_t* q_full = bars + 0;              // [2] one per block
-  uint64_t* kv_full = bars + 2;             // [STAGES]
+  uint64_t* q_empty = bars + 2;             // block 0's Q tiles no longer read
+  uint64_t* kv_full = bars + 3;             // [STAGES]
   uint64_t* kv_empty = kv_full + STAGES;    // [STAGES]
   uint64_t* s_full = kv_empty + STAGES;     // [2]
-  uint64_t* p_full = s_full + 2;            // [2]
-  uint64_t* o_done = p_full + 2;            // [2]
+  uint64_t* o_done = s_full + 2;            // [2]
   uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -162,13 +169,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&q_full[0], 1);
     mbar_init(&q_full[1], 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 128);
       mbar_init(&o_done[x], 1);
     }
     mbar_init(drain, 1);
@@ -197,18 +204,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t vt_row0 = ((int64_t)b * p.H + head) * HD;    // V^T rows of this head
       uint32_t item = 0;
       bool ok = true;
-      // both blocks' query tiles first (each has its own buffer), so the
-      // second block never waits for the first to drain
-      for (int blk = 0; blk < 2; ++blk) {
-        const BlockGeo g = block_geo(blk_id(blk), p, b);
-        mbar_arrive_expect_tx(&q_full[blk], 2 * TILE_BYTES);
-        for (int x = 0; x < 2; ++x)
-          for (int c = 0; c < 2; ++c)
-            tma_load_2d(Qs + (blk * 2 + x) * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64,
-                        (int)(g.zrow0 + x * QT), &q_full[blk]);
-      }
+      int q_loaded = 0;
       for (int blk = 0; blk < 2 && ok; ++blk) {
         const BlockGeo g = block_geo(blk_id(blk), p, b);
+        // block 1's query tiles go into block 0's buffer once its last S MMA is done
+        if (blk == 1 && !mbar_wait(q_empty, 0, abort_flag, p.err, code | 1)) break;
+        mbar_arrive_expect_tx(&q_full[blk], 2 * TILE_BYTES);
+        ++q_loaded;
+        for (int x = 0; x < 2; ++x)
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)(g.zrow0 + x * QT),
+                        &q_full[blk]);
         for (int j = 0; j < g.nB && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++item) {
             const int s = item % STAGES;
@@ -232,84 +238,76 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t first = item > (uint32_t)STAGES ? item - STAGES : 0;
       volatile int dummy = 0;
       for (uint32_t n = first; n < item; ++n) mbar_wait(&kv_full[n % STAGES], (n / STAGES) & 1, &dummy, p.err, code | 3);
-      mbar_wait(&q_full[0], 0, &dummy, p.err, code | 3);
-      mbar_wait(&q_full[1], 0, &dummy, p.err, code | 3);
+      for (int q = 0; q < q_loaded; ++q) mbar_wait(&q_full[q], 0, &dummy, p.err, code | 3);
     }
   } else if (warp == 9) {
     // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(QT, KT);
-      uint32_t item = 0;
-      uint32_t pcnt0 = 0, pcnt1 = 0;
-      bool ok = true;
-      uint8_t* qbuf = Qs;
-      auto mma_s = [&](int x, int s) {  // S_x = Q_x K^T, K = head dim
-        const uint32_t qa = smem_u32(qbuf + x * TILE_BYTES), kb = smem_u32(KVs + s * TILE_BYTES);
+    // The whole warp walks the schedule (named barriers are warp-aligned);
+    // lane 0 issues.  Inside a block the warp never waits on an mbarrier: the
+    // softmax warpgroup that hands over P_x(j) has also checked that the K/V
+    // tiles the following MMAs read have landed.
+    constexpr uint32_t idesc = idesc_bf16_f32(QT, KT);
+    uint32_t item = 0;
+    bool ok = true;  // warp-uniform: false once this warp gave up waiting
+    auto mma_s = [&](int x, int s) {  // S_x = Q_x K^T, K = head dim
+      const uint32_t qa = smem_u32(Qs + x * TILE_BYTES), kb = smem_u32(KVs + s * TILE_BYTES);
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t a = sdesc_kmajor_sw128(qa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-          const uint64_t bb = sdesc_kmajor_sw128(kb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-          umma_bf16(tmem_base + x * 128, a, bb, idesc, k > 0);
-        }
-      };
-      auto mma_pv = [&](int x, int s, bool acc) {  // O_x += P_x V, K = keys; P_x in TMEM (S_x columns 0-63)
-        const uint32_t vb = smem_u32(KVs + s * TILE_BYTES);
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t a = sdesc_kmajor_sw128(qa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
+        const uint64_t bb = sdesc_kmajor_sw128(kb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
+        umma_bf16(tmem_base + x * 128, a, bb, idesc, k > 0);
+      }
+    };
+    auto mma_pv = [&](int x, int s, bool acc) {  // O_x += P_x V, K = keys; P_x in TMEM (S_x columns 0-63)
+      const uint32_t vb = smem_u32(KVs + s * TILE_BYTES);
 #pragma unroll
-        for (int k = 0; k < KT / 16; ++k) {
-          const uint64_t bb = sdesc_kmajor_sw128(vb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-          umma_bf16_ts(tmem_base + 256 + x * 128, tmem_base + x * 128 + 8 * k, bb, idesc, (acc || k > 0) ? 1u : 0u);
-        }
-      };
-      auto wait_item = [&](uint32_t n) {
-        return mbar_wait(&kv_full[n % STAGES], (n / STAGES) & 1, abort_flag, p.err, code | 4);
-      };
-      auto wait_p = [&](int x) {
-        uint32_t& cnt = x == 0 ? pcnt0 : pcnt1;
-        const bool r = mbar_wait(&p_full[x], cnt & 1, abort_flag, p.err, code | 5);
-        ++cnt;
-        return r;
-      };
-      for (int blk = 0; blk < 2 && ok; ++blk) {
-        const BlockGeo g = block_geo(blk_id(blk), p, b);
-        const int nB = g.nB, nA = g.nB - 1;
-        if (!mbar_wait(&q_full[blk], 0, abort_flag, p.err, code | 6)) break;
-        qbuf = Qs + blk * 2 * TILE_BYTES;
-        tc_fence_after();
-        const uint32_t base = item;  // K_j = base + 2j, V_j = base + 2j + 1
-        if (!wait_item(base)) break;
-        tc_fence_after();
+      for (int k = 0; k < KT / 16; ++k) {
+        const uint64_t bb = sdesc_kmajor_sw128(vb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
+        umma_bf16_ts(tmem_base + 256 + x * 128, tmem_base + x * 128 + 8 * k, bb, idesc, (acc || k > 0) ? 1u : 0u);
+      }
+    };
+    for (int blk = 0; blk < 2; ++blk) {
+      const BlockGeo g = block_geo(blk_id(blk), p, b);
+      const int nB = g.nB, nA = g.nB - 1;
+      const uint32_t base = item;  // K_j = base + 2j, V_j = base + 2j + 1
+      if (ok) {
+        bool w = true;
+        if (lane == 0)
+          w = mbar_wait(&q_full[blk], 0, abort_flag, p.err, code | 6) &&
+              mbar_wait(&kv_full[base % STAGES], (base / STAGES) & 1, abort_flag, p.err, code | 4);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      }
+      tc_fence_after();
+      if (ok && lane == 0) {
         mma_s(0, base % STAGES);
         umma_commit(&s_full[0]);
         mma_s(1, base % STAGES);
         umma_commit(&s_full[1]);
         umma_commit(&kv_empty[base % STAGES]);
-        for (int j = 0; j < nB && ok; ++j) {
-          const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
-          bool k_next_ready = false;
-          if (!wait_item(iv)) { ok = false; break; }
-          if (j < nA) {
-            if (!wait_p(0)) { ok = false; break; }
-            tc_fence_after();
+      }
+      for (int j = 0; j < nB; ++j) {
+        const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+        if (j < nA) {
+          __syncwarp();
+          named_bar_sync(kBarPA + (j & 1), kHandoffThreads);
+          tc_fence_after();
+          if (ok && lane == 0) {
             mma_pv(0, iv % STAGES, j > 0);
             if (j + 1 < nA) {
-              if (!wait_item(ik)) { ok = false; break; }
-              k_next_ready = true;
-              tc_fence_after();
               mma_s(0, ik % STAGES);
               umma_commit(&s_full[0]);
             } else {
               umma_commit(&o_done[0]);
             }
           }
-          if (!wait_p(1)) { ok = false; break; }
-          tc_fence_after();
+        }
+        __syncwarp();
+        named_bar_sync(kBarPB + (j & 1), kHandoffThreads);
+        tc_fence_after();
+        if (ok && lane == 0) {
           mma_pv(1, iv % STAGES, j > 0);
           umma_commit(&kv_empty[iv % STAGES]);
           if (j + 1 < nB) {
-            if (!k_next_ready) {
-              if (!wait_item(ik)) { ok = false; break; }
-              tc_fence_after();
-            }
             mma_s(1, ik % STAGES);
             umma_commit(&s_full[1]);
             umma_commit(&kv_empty[ik % STAGES]);
@@ -317,12 +315,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             umma_commit(&o_done[1]);
           }
         }
-        item = base + 2 * nB;
       }
+      item = base + 2 * nB;
+      // the Q buffer is free for block 1 once every MMA issued so far is done
+      if (blk == 0 && ok && lane == 0) umma_commit(q_empty);
+    }
+    if (lane == 0) {
       umma_commit(drain);
       volatile int dummy = 0;
       mbar_wait(drain, 0, &dummy, p.err, code | 7);
     }
+    __syncwarp();
   } else {
     // ------------------------- softmax warpgroups (warps 0-7) -------------------------
     const int x = warp / 4;  // 0: tile A, 1: tile B
@@ -333,17 +336,36 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tO = tmem_base + lane_off + 256 + x * 128;
     const float sl2 = kLog2e * rsqrtf((float)HD);
     uint32_t scnt = 0;
+    uint32_t item = 0;  // the producer's K/V item numbering
+    bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
+    const bool checker = quad == 0 && lane == 0;
     for (int blk = 0; blk < 2; ++blk) {
       const BlockGeo g = block_geo(blk_id(blk), p, b);
       const int n = g.nB - 1 + x;
+      const uint32_t base = item;
+      item = base + 2 * g.nB;
       float m_used = -INFINITY, l = 0.f;
-      bool alive = true;
+      // Hands P_x(j) to the MMA warp.  Its next MMAs read V_j and, if this
+      // tile has another key tile, K_{j+1}: one thread checks that both have
+      // landed before the warpgroup arrives.  Every warp arrives once per key
+      // tile whatever happened, so the MMA warp's barrier count always
+      // completes.
+      auto hand_off = [&](int jj) {
+        if (checker && alive) {
+          const uint32_t iv = base + 2 * jj + 1;
+          if (mbar_wait(&kv_full[iv % STAGES], (iv / STAGES) & 1, abort_flag, p.err, code | 10) && jj + 1 < n)
+            mbar_wait(&kv_full[(iv + 1) % STAGES], ((iv + 1) / STAGES) & 1, abort_flag, p.err, code | 10);
+        }
+        __syncwarp();
+        named_bar_arrive((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoffThreads);
+      };
       for (int j = 0; j < n; ++j) {
-        const bool got = mbar_wait(&s_full[x], scnt & 1, abort_flag, p.err, code | 8);
+        const bool got = alive && mbar_wait(&s_full[x], scnt & 1, abort_flag, p.err, code | 8);
         ++scnt;
-        if (!__all_sync(0xffffffffu, got)) {
-          alive = false;
-          break;
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) {
+          hand_off(j);
+          continue;
         }
         tc_fence_after();
         const bool diag = (j == n - 1);
@@ -429,11 +451,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st32_nowait(tS + 32, pk + 32);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[x]);
+        hand_off(j);
       }
-      if (!alive) break;
+      if (!alive) continue;
       const bool got = mbar_wait(&o_done[x], blk & 1, abort_flag, p.err, code | 9);
-      if (!__all_sync(0xffffffffu, got)) break;
+      alive = __all_sync(0xffffffffu, got);
+      if (!alive) continue;
       tc_fence_after();
       uint32_t orr[128];
       tmem_ld128(tO, orr);

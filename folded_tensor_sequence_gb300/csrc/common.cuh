@@ -87,6 +87,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Named (hardware) CTA barriers.  Both forms are warp-aligned: every lane of
+// a warp executes them together, and `count` (threads) is a multiple of 32.
+// Used for hand-offs into the MMA-issuing warp: a thread that has just issued
+// tcgen05.mma instructions and then touches shared memory (an mbarrier wait
+// included) stalls until the tensor pipe has drained, while a named barrier
+// does not, so the MMA warp is released by the warps it waits for.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Waits for the phase with `parity` to complete.  Gives up after
 // kWaitTimeoutNs, or as soon as another role of the CTA has set *abort;
 // on its own timeout it sets *abort and records `code`.  Returns false on
