@@ -30,7 +30,16 @@ namespace tsp {
 namespace {
 
 constexpr int HD = 128;
-constexpr int THREADS = 320;  // warps 0-7 elementwise (two per TMEM lane quadrant), 8 TMA, 9 MMA
+constexpr int THREADS = 352;  // warps 0-7 elementwise (two per TMEM lane quadrant), 8 TMA, 9 MMA, 10 relay
+// Named barriers into the MMA warp (which never waits on an mbarrier inside a
+// tile): the relay warp announces each landed stage on kBarStage + (n % 4)
+// (64 threads: relay + MMA), the elementwise warps hand back P/dS of block i
+// on kBarDS + (i % 2) (256 + 32 threads).  A warp arrives without blocking
+// only while the data it hands over keeps it in step with the MMA warp; the
+// relay, and any warp that has given up waiting, uses the blocking form, so
+// no warp can run ahead and complete a barrier phase in the MMA warp's place.
+constexpr int kBarStage = 1, kBarDS = 5;
+constexpr int kStageThreads = 64, kDSThreads = 256 + 32;
 constexpr uint32_t SUB64 = 64 * 64 * 2;     // [64 rows][64 cols] bf16, 8 KB
 constexpr uint32_t SUB128 = 128 * 64 * 2;   // [128 rows][64 cols] bf16, 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -97,11 +106,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* q_full = bars + 2;   // [QSTG]
   uint64_t* q_free = bars + 6;   // [QSTG]
   uint64_t* s_full = bars + 10;  // [2]
-  // [2], one per TMEM buffer: the score MMAs of block i+1 are issued before the
-  // MMA thread waits for block i's elementwise results, so a fast warp may
-  // already arrive for block i+1 while a slow one still works on block i;
-  // separate barriers keep those arrivals apart.
-  uint64_t* ds_full = bars + 12;
   uint64_t* o_done = bars + 14;
   uint64_t* drain = bars + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
@@ -122,8 +126,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(&ds_full[0], 256);
-    mbar_init(&ds_full[1], 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -190,86 +192,93 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_DKDV | 3);
     }
   } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, KB_QB);  // M = keys, N = queries
-      constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // M = keys, N = head dim (B MN-major)
-      uint32_t qi = 0, scnt0 = 0, scnt1 = 0;
-      bool ok = true;
-      auto scores = [&](uint32_t n, int x) {  // S^T = K Q^T, dP^T = V dO^T for query block n
-        uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
+    // ---------------- MMA issuer (whole warp walks the schedule, lane 0 issues) ----------------
+    constexpr uint32_t id_s = idesc_bf16_f32(128, KB_QB);  // M = keys, N = queries
+    constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // M = keys, N = head dim (B MN-major)
+    uint32_t qi = 0;
+    bool ok = true;  // warp-uniform
+    auto scores = [&](uint32_t n, int x) {  // S^T = K Q^T, dP^T = V dO^T for query block n
+      uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
-          const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
-          umma_bf16(tmem_base + 64 * x, ak, bq, id_s, k > 0);
-        }
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
+        umma_bf16(tmem_base + 64 * x, ak, bq, id_s, k > 0);
+      }
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
-          const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
-          umma_bf16(tmem_base + 128 + 64 * x, av, bo, id_s, k > 0);
-        }
-        umma_commit(&s_full[x]);
-      };
-      // dV += P^T dO, dK += dS^T Q for query block n: the Q / dO tiles of the
-      // stage serve as MN-major B operands (rows = queries = K dimension)
-      auto accumulate = [&](uint32_t n, int x, bool acc) {
-        uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
+        umma_bf16(tmem_base + 128 + 64 * x, av, bo, id_s, k > 0);
+      }
+      umma_commit(&s_full[x]);
+    };
+    // dV += P^T dO, dK += dS^T Q for query block n: the Q / dO tiles of the
+    // stage serve as MN-major B operands (rows = queries = K dimension)
+    auto accumulate = [&](uint32_t n, int x, bool acc) {
+      uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
 #pragma unroll
-        for (int k = 0; k < KB_QB / 16; ++k) {
-          const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB64) + 2048 * k, SUB64);
-          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bo, id_o,
-                       (acc || k > 0) ? 1u : 0u);
-        }
+      for (int k = 0; k < KB_QB / 16; ++k) {
+        const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB64) + 2048 * k, SUB64);
+        umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bo, id_o,
+                     (acc || k > 0) ? 1u : 0u);
+      }
 #pragma unroll
-        for (int k = 0; k < KB_QB / 16; ++k) {
-          const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
-          umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * x + 32 * (k / 2) + 8 * (k % 2), bq, id_o,
-                       (acc || k > 0) ? 1u : 0u);
-        }
-        umma_commit(&q_free[n % QSTG]);
-      };
-      uint32_t dscnt[2] = {0, 0};
-      for (int t = 0; t < ntile && ok; ++t) {
-        const int64_t k0 = (int64_t)tile_of(t) * 128;
-        const int nq = (int)((p.S - k0) / KB_QB);
-        if (!mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_DKDV | 4)) break;
-        for (int i = 0; i < nq; ++i) {
-          const uint32_t n = qi + i;
-          if (!mbar_wait(&q_full[n % QSTG], (n / QSTG) & 1, abort_flag, p.err, CODE_DKDV | 5)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          scores(n, i & 1);
-          if (i & 1) ++scnt1; else ++scnt0;
-          if (i > 0) {
-            const int xp = (i - 1) & 1;
-            if (!mbar_wait(&ds_full[xp], dscnt[xp] & 1, abort_flag, p.err, CODE_DKDV | 6)) {
-              ok = false;
-              break;
-            }
-            ++dscnt[xp];
-            tc_fence_after();
-            accumulate(n - 1, (i - 1) & 1, i - 1 > 0);
-          }
-        }
-        if (!ok) break;
-        const int xl = (nq - 1) & 1;
-        if (!mbar_wait(&ds_full[xl], dscnt[xl] & 1, abort_flag, p.err, CODE_DKDV | 6)) break;
-        ++dscnt[xl];
+      for (int k = 0; k < KB_QB / 16; ++k) {
+        const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
+        umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * x + 32 * (k / 2) + 8 * (k % 2), bq, id_o,
+                     (acc || k > 0) ? 1u : 0u);
+      }
+      umma_commit(&q_free[n % QSTG]);
+    };
+    auto sync_ds = [&](int i) {  // elementwise results of block i of the tile are in TMEM
+      __syncwarp();
+      named_bar_sync(kBarDS + (i & 1), kDSThreads);
+      tc_fence_after();
+    };
+    for (int t = 0; t < ntile; ++t) {
+      const int64_t k0 = (int64_t)tile_of(t) * 128;
+      const int nq = (int)((p.S - k0) / KB_QB);
+      if (ok) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_DKDV | 4);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      }
+      for (int i = 0; i < nq; ++i) {
+        const uint32_t n = qi + i;
+        __syncwarp();
+        named_bar_sync(kBarStage + (n & 3), kStageThreads);  // stage n has landed
         tc_fence_after();
+        if (ok && lane == 0) scores(n, i & 1);
+        if (i > 0) {
+          sync_ds(i - 1);
+          if (ok && lane == 0) accumulate(n - 1, (i - 1) & 1, i - 1 > 0);
+        }
+      }
+      sync_ds(nq - 1);
+      if (ok && lane == 0) {
         accumulate(qi + nq - 1, (nq - 1) & 1, nq - 1 > 0);
         umma_commit(o_done);
         umma_commit(kv_free);
-        qi += nq;
       }
-      (void)scnt0;
-      (void)scnt1;
+      qi += nq;
+    }
+    if (lane == 0) {
       umma_commit(drain);
       volatile int dummy = 0;
       mbar_wait(drain, 0, &dummy, p.err, CODE_DKDV | 7);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ---------------- relay: announces each landed stage to the MMA warp ----------------
+    uint32_t n = 0;
+    for (int t = 0; t < ntile; ++t) {
+      const int nq = (int)((p.S - (int64_t)tile_of(t) * 128) / KB_QB);
+      for (int i = 0; i < nq; ++i, ++n) {
+        if (lane == 0) mbar_wait(&q_full[n % QSTG], (n / QSTG) & 1, abort_flag, p.err, CODE_DKDV | 9);
+        __syncwarp();
+        named_bar_sync(kBarStage + (n & 3), kStageThreads);
+      }
     }
   } else {
     // ------- elementwise warps 0-7: one key row, 32 of the 64 query columns per thread -------
@@ -280,18 +289,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float scale = rsqrtf((float)HD);
     uint32_t scnt[2] = {0, 0};
     uint32_t qidx = 0;  // global query-block counter (stage = qidx % QSTG)
-    bool alive = true;
-    for (int t = 0; t < ntile && alive; ++t) {
+    bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
+    for (int t = 0; t < ntile; ++t) {
       const int64_t k0 = (int64_t)tile_of(t) * 128;
       const int nq = (int)((p.S - k0) / KB_QB);
       const int64_t key = k0 + row;
       for (int i = 0; i < nq; ++i) {
         const int x = i & 1;
-        const bool got = mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DKDV | 8);
+        const bool got = alive && mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DKDV | 8);
         ++scnt[x];
-        if (!__all_sync(0xffffffffu, got)) {
-          alive = false;
-          break;
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) {
+          named_bar_sync(kBarDS + (i & 1), kDSThreads);
+          continue;
         }
         tc_fence_after();
         const uint32_t cS = tmem_base + lane_off + 64 * x + 32 * half;
@@ -328,11 +338,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st16_nowait(cdP, dk2);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&ds_full[x]);
+        __syncwarp();
+        named_bar_arrive(kBarDS + (i & 1), kDSThreads);
       }
-      if (!alive) break;
+      if (!alive) continue;
       const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DKDV | 10);
-      if (!__all_sync(0xffffffffu, got)) break;
+      alive = __all_sync(0xffffffffu, got);
+      if (!alive) continue;
       tc_fence_after();
       uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bh * p.S + key) * HD) + 8 * half;
       uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bh * p.S + key) * HD) + 8 * half;
@@ -385,11 +397,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* k_full = bars + 2;   // [KSTG]
   uint64_t* k_free = bars + 6;   // [KSTG]
   uint64_t* s_full = bars + 10;  // [2]
-  // [2], one per TMEM buffer: the score MMAs of block i+1 are issued before the
-  // MMA thread waits for block i's elementwise results, so a fast warp may
-  // already arrive for block i+1 while a slow one still works on block i;
-  // separate barriers keep those arrivals apart.
-  uint64_t* ds_full = bars + 12;
   uint64_t* o_done = bars + 14;
   uint64_t* drain = bars + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
@@ -417,8 +424,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(&ds_full[0], 256);
-    mbar_init(&ds_full[1], 256);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -479,74 +484,88 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (q_armed) mbar_wait(q_full, (q_armed - 1) & 1, &dummy, p.err, CODE_DQ | 3);
     }
   } else if (warp == 9) {
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, DQ_KB);
-      constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // B (K tile) MN-major
-      uint32_t ki = 0, dscnt[2] = {0, 0};
-      bool ok = true;
-      auto scores = [&](uint32_t n, int x) {  // S = Q K^T, dP = dO V^T for key block n
-        uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
+    // ---------------- MMA issuer (whole warp walks the schedule, lane 0 issues) ----------------
+    constexpr uint32_t id_s = idesc_bf16_f32(128, DQ_KB);
+    constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // B (K tile) MN-major
+    uint32_t ki = 0;
+    bool ok = true;  // warp-uniform
+    auto scores = [&](uint32_t n, int x) {  // S = Q K^T, dP = dO V^T for key block n
+      uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t aq = sdesc_kmajor_sw128(smem_u32(Qs + (k / 4) * SUB128)) + 2 * (k % 4);
-          const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
-          umma_bf16(tmem_base + 64 * x, aq, bk, id_s, k > 0);
-        }
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t aq = sdesc_kmajor_sw128(smem_u32(Qs + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
+        umma_bf16(tmem_base + 64 * x, aq, bk, id_s, k > 0);
+      }
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t ao = sdesc_kmajor_sw128(smem_u32(dOs + (k / 4) * SUB128)) + 2 * (k % 4);
-          const uint64_t bv = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
-          umma_bf16(tmem_base + 128 + 64 * x, ao, bv, id_s, k > 0);
-        }
-        umma_commit(&s_full[x]);
-      };
-      auto accumulate = [&](uint32_t n, int x, bool acc) {  // dQ += dS K for key block n (K tile as MN-major B)
-        uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t ao = sdesc_kmajor_sw128(smem_u32(dOs + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bv = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
+        umma_bf16(tmem_base + 128 + 64 * x, ao, bv, id_s, k > 0);
+      }
+      umma_commit(&s_full[x]);
+    };
+    auto accumulate = [&](uint32_t n, int x, bool acc) {  // dQ += dS K for key block n (K tile as MN-major B)
+      uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
 #pragma unroll
-        for (int k = 0; k < DQ_KB / 16; ++k) {
-          const uint64_t bk = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
-          umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bk, id_o,
-                       (acc || k > 0) ? 1u : 0u);
-        }
-        umma_commit(&k_free[n % KSTG]);
-      };
-      for (int t = 0; t < 2 && ok; ++t) {
-        int64_t zrow0, p0;
-        geo(tile_of(t), zrow0, p0);
-        const int nkb = (int)((p0 + 128) / DQ_KB);
-        if (!mbar_wait(q_full, t & 1, abort_flag, p.err, CODE_DQ | 4)) break;
-        for (int j = 0; j < nkb; ++j) {
-          const uint32_t n = ki + j;
-          if (!mbar_wait(&k_full[n % KSTG], (n / KSTG) & 1, abort_flag, p.err, CODE_DQ | 5)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          scores(n, j & 1);
-          if (j > 0) {
-            const int xp = (j - 1) & 1;
-            if (!mbar_wait(&ds_full[xp], dscnt[xp] & 1, abort_flag, p.err, CODE_DQ | 6)) {
-              ok = false;
-              break;
-            }
-            ++dscnt[xp];
-            tc_fence_after();
-            accumulate(n - 1, (j - 1) & 1, j - 1 > 0);
-          }
-        }
-        if (!ok) break;
-        const int xl = (nkb - 1) & 1;
-        if (!mbar_wait(&ds_full[xl], dscnt[xl] & 1, abort_flag, p.err, CODE_DQ | 6)) break;
-        ++dscnt[xl];
+      for (int k = 0; k < DQ_KB / 16; ++k) {
+        const uint64_t bk = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
+        umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bk, id_o,
+                     (acc || k > 0) ? 1u : 0u);
+      }
+      umma_commit(&k_free[n % KSTG]);
+    };
+    auto sync_ds = [&](int j) {  // elementwise results of key block j of the tile are in TMEM
+      __syncwarp();
+      named_bar_sync(kBarDS + (j & 1), kDSThreads);
+      tc_fence_after();
+    };
+    for (int t = 0; t < 2; ++t) {
+      int64_t zrow0, p0;
+      geo(tile_of(t), zrow0, p0);
+      const int nkb = (int)((p0 + 128) / DQ_KB);
+      if (ok) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(q_full, t & 1, abort_flag, p.err, CODE_DQ | 4);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      }
+      for (int j = 0; j < nkb; ++j) {
+        const uint32_t n = ki + j;
+        __syncwarp();
+        named_bar_sync(kBarStage + (n & 3), kStageThreads);  // stage n has landed
         tc_fence_after();
+        if (ok && lane == 0) scores(n, j & 1);
+        if (j > 0) {
+          sync_ds(j - 1);
+          if (ok && lane == 0) accumulate(n - 1, (j - 1) & 1, j - 1 > 0);
+        }
+      }
+      sync_ds(nkb - 1);
+      if (ok && lane == 0) {
         accumulate(ki + nkb - 1, (nkb - 1) & 1, nkb - 1 > 0);
         umma_commit(o_done);
         umma_commit(q_free);
-        ki += nkb;
       }
+      ki += nkb;
+    }
+    if (lane == 0) {
       umma_commit(drain);
       volatile int dummy = 0;
       mbar_wait(drain, 0, &dummy, p.err, CODE_DQ | 7);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ---------------- relay: announces each landed stage to the MMA warp ----------------
+    uint32_t n = 0;
+    for (int t = 0; t < 2; ++t) {
+      int64_t zrow0, p0;
+      geo(tile_of(t), zrow0, p0);
+      const int nkb = (int)((p0 + 128) / DQ_KB);
+      for (int j = 0; j < nkb; ++j, ++n) {
+        if (lane == 0) mbar_wait(&k_full[n % KSTG], (n / KSTG) & 1, abort_flag, p.err, CODE_DQ | 9);
+        __syncwarp();
+        named_bar_sync(kBarStage + (n & 3), kStageThreads);
+      }
     }
   } else {
     // ------- elementwise warps 0-7: one query row, 32 of the 64 key columns per thread -------
@@ -556,8 +575,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float sl2 = kLog2e * rsqrtf((float)HD);
     const float scale = rsqrtf((float)HD);
     uint32_t scnt[2] = {0, 0};
-    bool alive = true;
-    for (int t = 0; t < 2 && alive; ++t) {
+    bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
+    for (int t = 0; t < 2; ++t) {
       int64_t zrow0, p0;
       geo(tile_of(t), zrow0, p0);
       const int nkb = (int)((p0 + 128) / DQ_KB);
@@ -566,11 +585,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float dsr = p.dsum[bh * p.S + qpos];
       for (int j = 0; j < nkb; ++j) {
         const int x = j & 1;
-        const bool got = mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DQ | 8);
+        const bool got = alive && mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DQ | 8);
         ++scnt[x];
-        if (!__all_sync(0xffffffffu, got)) {
-          alive = false;
-          break;
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) {
+          named_bar_sync(kBarDS + (j & 1), kDSThreads);
+          continue;
         }
         tc_fence_after();
         const uint32_t cS = tmem_base + lane_off + 64 * x + 32 * half;
@@ -591,11 +611,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_st16_nowait(cS, dsk);  // dS over the start of this thread's S columns
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&ds_full[x]);
+        __syncwarp();
+        named_bar_arrive(kBarDS + (j & 1), kDSThreads);
       }
-      if (!alive) break;
+      if (!alive) continue;
       const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DQ | 10);
-      if (!__all_sync(0xffffffffu, got)) break;
+      alive = __all_sync(0xffffffffu, got);
+      if (!alive) continue;
       tc_fence_after();
       uint4* dst = reinterpret_cast<uint4*>(p.dq + (zrow0 + row) * p.h + head * HD) + 8 * half;
 #pragma unroll 1

@@ -349,7 +349,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // tile has another key tile, K_{j+1}: one thread checks that both have
       // landed before the warpgroup arrives.  Every warp arrives once per key
       // tile whatever happened, so the MMA warp's barrier count always
-      // completes.
+      // completes; a warp that has given up waiting uses the blocking form,
+      // which keeps it from running ahead and completing a barrier phase in
+      // the MMA warp's place.
       auto hand_off = [&](int jj) {
         if (checker && alive) {
           const uint32_t iv = base + 2 * jj + 1;
@@ -357,7 +359,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(&kv_full[(iv + 1) % STAGES], ((iv + 1) / STAGES) & 1, abort_flag, p.err, code | 10);
         }
         __syncwarp();
-        named_bar_arrive((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoffThreads);
+        if (alive)
+          named_bar_arrive((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoffThreads);
+        else
+          named_bar_sync((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoffThreads);
       };
       for (int j = 0; j < n; ++j) {
         const bool got = alive && mbar_wait(&s_full[x], scnt & 1, abort_flag, p.err, code | 8);
