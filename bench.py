@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from folded_tensor_sequence_gb300.configs import BY_NAME, LAYER_7B_S16K  # noqa: E402
+from folded_tensor_sequence_gb300.replicas import max_over_ranks, rank_env, whole_job_rate  # noqa: E402
 
 METRIC = "TSP layer fwd TFLOP/s & tokens/s (bf16) at 1 GB300; % of dense bf16 tensor peak"
 # (for the training workload the same metric counts the step's model flops, 3x the forward)
@@ -213,10 +214,8 @@ def cpu_baseline(cfg, prefix: int):
 
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    e = rank_env()
+    return e.world_size, e.rank, e.local_rank
 
 
 def run_reference(args, cfg):
@@ -336,15 +335,12 @@ def main():
         barrier()
     ms = ev0.elapsed_time(ev1)
     tsp.tsp_sync_check(stream)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     clocks = clk.summary()
     flops = cfg.fwd_flops() * (3 if cfg.backward else 1)  # training step: model flops = 3x forward
     ms_step = ms / args.steps
-    value = ws * flops * args.steps / (ms / 1e3) / 1e12
-    tokens_s = ws * B * S * args.steps / (ms / 1e3)
+    value = whole_job_rate(ws, flops, args.steps, ms) / 1e12
+    tokens_s = whole_job_rate(ws, B * S, args.steps, ms)
 
     # ---- per-kernel timing (same stream, separate pass) ---------------------
     tsp.tsp_profile_enable(True)
@@ -397,16 +393,12 @@ def main():
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     barrier()
-    ems = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ems], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ems = float(t.item())
+    ems = max_over_ranks(e0.elapsed_time(e1), dev)
     tsp.tsp_sync_check(stream)
-    e2e = {"value": round(ws * flops * args.steps / (ems / 1e3) / 1e12, 2), "unit": UNIT,
+    e2e = {"value": round(whole_job_rate(ws, flops, args.steps, ems) / 1e12, 2), "unit": UNIT,
            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in ins),
            "d2h_bytes_per_step": out.numel() * out.element_size(),
-           "tokens_per_s": round(ws * B * S * args.steps / (ems / 1e3), 1)}
+           "tokens_per_s": round(whole_job_rate(ws, B * S, args.steps, ems), 1)}
 
     if rank == 0:
         line = {
