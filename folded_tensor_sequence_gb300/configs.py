@@ -23,6 +23,7 @@ class LayerConfig:
     ffn: int
     dtype: str  # "f32" or "bf16"
     backward: bool = False
+    kv_heads: int = 0  # K/V heads for grouped-query attention; 0: as many as query heads
 
     @property
     def chunk(self) -> int:
@@ -32,10 +33,23 @@ class LayerConfig:
     def tokens(self) -> int:
         return self.batch * self.seq
 
+    @property
+    def kv_h(self) -> int:
+        """Number of K/V heads."""
+        return self.kv_heads or self.heads
+
+    @property
+    def kv_hidden(self) -> int:
+        """Width of K and V (K/V heads x head_dim)."""
+        return self.kv_h * self.head_dim
+
     def fwd_flops(self) -> int:
-        """Algorithmic forward flops: B*S*(8h^2 + 6hF) + 4*B*H*dh*S(S+1)/2 (causal triangle only)."""
-        B, S, h, F = self.batch, self.seq, self.hidden, self.ffn
-        return B * S * (8 * h * h + 6 * h * F) + 4 * B * self.heads * self.head_dim * S * (S + 1) // 2
+        """Algorithmic forward flops: B*S*2*(h*(h + 2hk) + h^2 + 3hF) + 4*B*H*dh*S(S+1)/2
+        (Q/K/V, output and MLP projections, causal triangle only; hk = h for multi-head
+        attention, which gives the familiar B*S*(8h^2 + 6hF))."""
+        B, S, h, F, hk = self.batch, self.seq, self.hidden, self.ffn, self.kv_hidden
+        return (B * S * 2 * (h * (h + 2 * hk) + h * h + 3 * h * F)
+                + 4 * B * self.heads * self.head_dim * S * (S + 1) // 2)
 
     def with_(self, **kw) -> "LayerConfig":
         return replace(self, **kw)
@@ -56,5 +70,12 @@ TRAIN_7B_S8K = LayerConfig("bf16_fwdbwd_D8_b1_s8192_h4096", D=8, batch=1, seq=81
 TRAIN_7B_S16K = LayerConfig("bf16_fwdbwd_D8_b2_s16384_h4096", D=8, batch=2, seq=16384, hidden=4096, heads=32,
                             head_dim=128, ffn=14336, dtype="bf16", backward=True)
 
-ALL = [TINY_F32, MID_BF16, LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_S8K, TRAIN_7B_S16K]
+# Grouped-query attention: 8 K/V heads for the 32 query heads (one K/V head per rank at D = 8).
+LAYER_7B_GQA8_S16K = LayerConfig("bf16_gqa8_D8_b2_s16384_h4096", D=8, batch=2, seq=16384, hidden=4096, heads=32,
+                                 head_dim=128, ffn=14336, dtype="bf16", kv_heads=8)
+TRAIN_7B_GQA8_S8K = LayerConfig("bf16_fwdbwd_gqa8_D8_b1_s8192_h4096", D=8, batch=1, seq=8192, hidden=4096,
+                                heads=32, head_dim=128, ffn=14336, dtype="bf16", backward=True, kv_heads=8)
+
+ALL = [TINY_F32, MID_BF16, LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_S8K, TRAIN_7B_S16K, LAYER_7B_GQA8_S16K,
+       TRAIN_7B_GQA8_S8K]
 BY_NAME = {c.name: c for c in ALL}

@@ -122,14 +122,17 @@ def layer_inputs(cfg, seed: int = 0, with_dy: bool = False, only=None) -> dict:
     """All inputs of one TSP layer workload as fp64 arrays (values rounded to ``cfg.dtype``).
 
     Canonical weight layout, row-vector convention y = x @ W:
-    Wq, Wk, Wv, Wo: [h, h]; Wg, Wu: [h, F]; Wd: [F, h]; x (and dY): [B, S, h].
+    Wq, Wo: [h, h]; Wk, Wv: [h, hk] (hk = K/V heads * head_dim, h unless the
+    workload uses grouped-query attention); Wg, Wu: [h, F]; Wd: [F, h];
+    x (and dY): [B, S, h].
     """
     h, F = cfg.hidden, cfg.ffn
+    hk = cfg.kv_hidden
     spec = {
         "x": ((cfg.batch, cfg.seq, h), 1.0),
         "Wq": ((h, h), h ** -0.5),
-        "Wk": ((h, h), h ** -0.5),
-        "Wv": ((h, h), h ** -0.5),
+        "Wk": ((h, hk), h ** -0.5),
+        "Wv": ((h, hk), h ** -0.5),
         "Wo": ((h, h), h ** -0.5),
         "Wg": ((h, F), h ** -0.5),
         "Wu": ((h, F), h ** -0.5),

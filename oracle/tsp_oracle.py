@@ -34,6 +34,13 @@ What it computes (plain definitions, fp64, numpy):
   XW = X1W1 + X2W2, r007 chapter, section "Тензорный параллелизм").
 * Causal key-visit counts per rank and the forward communication-volume model
   behind the break-even B*S > 8h ("The Practicality of Trade-offs").
+* Grouped-query attention: K and V may have fewer heads than Q (Wk, Wv of
+  shape [h, Hk*dh]); the r007 chapter names GQA, with the K/V head count
+  often cut to 8, as what bounds a head-split degree ("Параллелизм по
+  контексту: Ring Attention против Ulysses").  Reading where the pages are
+  silent: query head e reads K/V head e // (H/Hk) (consecutive query heads
+  share one K/V head), and a TSP shard owns H/D query heads and Hk/D K/V
+  heads, so Hk must be divisible by D.  Hk = H is plain multi-head attention.
 
 Readings where the pages are silent are stated next to each function.
 Every function is pinned by tests/test_oracle_*.py against closed forms,
@@ -105,18 +112,28 @@ def silu_grad(z):
     return s * (1.0 + z * (1.0 - s))
 
 
+def kv_head_slice(e: int, heads: int, kv_heads: int, dh: int) -> slice:
+    """Columns of K/V read by query head e: K/V head e // (heads / kv_heads)."""
+    if heads % kv_heads:
+        raise ValueError("heads must be a multiple of kv_heads")
+    g = e // (heads // kv_heads)
+    return slice(g * dh, (g + 1) * dh)
+
+
 def causal_attention(Q, K, V, heads: int, rows=None, row_block: int = 1024):
     """Causal softmax attention per head, natural positions.
 
-    Q, K, V: [S, h] for one batch element (h = heads * dh).  ``rows`` selects
-    the query positions to evaluate (default: all).  Key j is visible to query
-    i iff j <= i (global positions, diagonal included); scale 1/sqrt(dh).
-    Returns (O [len(rows), h], lse [heads, len(rows)]) with lse the natural
-    log-sum-exp of the scaled, masked scores.  Rows are processed in blocks
-    only to bound memory; each row is computed on its own.
+    Q: [S, h] for one batch element (h = heads * dh); K, V: [S, Hk*dh] with
+    Hk K/V heads (Hk = heads for multi-head attention, fewer for GQA).
+    ``rows`` selects the query positions to evaluate (default: all).  Key j is
+    visible to query i iff j <= i (global positions, diagonal included); scale
+    1/sqrt(dh).  Returns (O [len(rows), h], lse [heads, len(rows)]) with lse
+    the natural log-sum-exp of the scaled, masked scores.  Rows are processed
+    in blocks only to bound memory; each row is computed on its own.
     """
-    S, h = K.shape
+    S, h = Q.shape
     dh = h // heads
+    kv_heads = K.shape[1] // dh
     rows = np.arange(S) if rows is None else np.asarray(rows, dtype=np.int64)
     O = np.zeros((len(rows), h))
     lse = np.zeros((heads, len(rows)))
@@ -124,15 +141,16 @@ def causal_attention(Q, K, V, heads: int, rows=None, row_block: int = 1024):
     keys = np.arange(S)
     for e in range(heads):
         sl = slice(e * dh, (e + 1) * dh)
+        kv = kv_head_slice(e, heads, kv_heads, dh)
         for b0 in range(0, len(rows), row_block):
             rb = rows[b0:b0 + row_block]
-            s = (Q[rb, sl] @ K[:, sl].T) * scale
+            s = (Q[rb, sl] @ K[:, kv].T) * scale
             visible = keys[None, :] <= rb[:, None]
             s = np.where(visible, s, -np.inf)
             m = s.max(axis=1, keepdims=True)
             p = np.exp(s - m)
             l = p.sum(axis=1, keepdims=True)
-            O[b0:b0 + len(rb), sl] = (p / l) @ V[:, sl]
+            O[b0:b0 + len(rb), sl] = (p / l) @ V[:, kv]
             lse[e, b0:b0 + len(rb)] = (m + np.log(l))[:, 0]
     return O, lse
 
@@ -145,7 +163,8 @@ def gated_mlp(Hm, w):
 def layer_fwd(x, w, heads: int, rows=None):
     """Unsharded layer forward in fp64.
 
-    x: [B, S, h]; w: dict with Wq, Wk, Wv, Wo [h, h], Wg, Wu [h, F], Wd [F, h].
+    x: [B, S, h]; w: dict with Wq, Wo [h, h], Wk, Wv [h, Hk*dh] (Hk = heads
+    unless the layer uses grouped-query attention), Wg, Wu [h, F], Wd [F, h].
     ``rows`` (optional) restricts every per-token output to those natural
     positions (K and V are still computed for all tokens, since attention needs
     them).  Returns dict of [B, R, .] arrays:
@@ -177,9 +196,10 @@ def layer_fwd(x, w, heads: int, rows=None):
     return {k: np.stack(v) for k, v in out.items()}
 
 
-def _head_probs(Q, K, sl, scale, mask):
-    """Causal softmax probabilities of one head (rows: queries, columns: keys)."""
-    s = np.where(mask, (Q[:, sl] @ K[:, sl].T) * scale, -np.inf)
+def _head_probs(Q, K, sl, kv, scale, mask):
+    """Causal softmax probabilities of one head (rows: queries, columns: keys);
+    sl: the head's Q columns, kv: its K columns."""
+    s = np.where(mask, (Q[:, sl] @ K[:, kv].T) * scale, -np.inf)
     p = np.exp(s - s.max(axis=1, keepdims=True))
     return p / p.sum(axis=1, keepdims=True)
 
@@ -195,9 +215,12 @@ def layer_bwd(x, w, heads: int, dY, return_y: bool = False):
       dWo = O^T dH; dO = dH Wo^T; per head: dV = P^T dO, dP = dO V^T,
       dS = P * (dP - rowsum(dP * P)), dQ = dS K / sqrt(dh), dK = dS^T Q / sqrt(dh);
       dWq = x^T dQ (likewise K, V); dx = dH + dQ Wq^T + dK Wk^T + dV Wv^T.
+    With grouped-query attention a K/V head's dK and dV are the sums over the
+    query heads that read it.
     """
     B, S, h = x.shape
     dh = h // heads
+    kv_heads = w["Wk"].shape[1] // dh
     scale = 1.0 / math.sqrt(dh)
     grads = {k: np.zeros_like(v) for k, v in w.items()}
     dx = np.zeros_like(x)
@@ -209,7 +232,8 @@ def layer_bwd(x, w, heads: int, dY, return_y: bool = False):
         O = np.zeros((S, h))
         for e in range(heads):
             sl = slice(e * dh, (e + 1) * dh)
-            O[:, sl] = _head_probs(Q, K, sl, scale, mask) @ V[:, sl]
+            kv = kv_head_slice(e, heads, kv_heads, dh)
+            O[:, sl] = _head_probs(Q, K, sl, kv, scale, mask) @ V[:, kv]
         Hb = xb + O @ w["Wo"]
         G, U = Hb @ w["Wg"], Hb @ w["Wu"]
         M = silu(G) * U
@@ -226,16 +250,17 @@ def layer_bwd(x, w, heads: int, dY, return_y: bool = False):
         grads["Wo"] += O.T @ dH
         dO = dH @ w["Wo"].T
         dQ = np.zeros((S, h))
-        dK = np.zeros((S, h))
-        dV = np.zeros((S, h))
+        dK = np.zeros_like(K)
+        dV = np.zeros_like(V)
         for e in range(heads):
             sl = slice(e * dh, (e + 1) * dh)
-            p = _head_probs(Q, K, sl, scale, mask)  # recomputed per head to bound memory
-            dV[:, sl] = p.T @ dO[:, sl]
-            dP = dO[:, sl] @ V[:, sl].T
+            kv = kv_head_slice(e, heads, kv_heads, dh)
+            p = _head_probs(Q, K, sl, kv, scale, mask)  # recomputed per head to bound memory
+            dV[:, kv] += p.T @ dO[:, sl]
+            dP = dO[:, sl] @ V[:, kv].T
             dS = p * (dP - (dP * p).sum(axis=1, keepdims=True))
-            dQ[:, sl] = dS @ K[:, sl] * scale
-            dK[:, sl] = dS.T @ Q[:, sl] * scale
+            dQ[:, sl] = dS @ K[:, kv] * scale
+            dK[:, kv] += dS.T @ Q[:, sl] * scale
         grads["Wq"] += xb.T @ dQ
         grads["Wk"] += xb.T @ dK
         grads["Wv"] += xb.T @ dV
@@ -250,14 +275,18 @@ def layer_bwd(x, w, heads: int, dY, return_y: bool = False):
 # ---------------------------------------------------------------------------
 
 def attention_shard(w, s: int, D: int):
-    """Packed attention shard s: Q/K/V columns and W_O rows of heads s*H/D .. (s+1)*H/D-1.
+    """Packed attention shard s: Q columns and W_O rows of query heads
+    s*H/D .. (s+1)*H/D-1, K/V columns of K/V heads s*Hk/D .. (s+1)*Hk/D-1.
 
     Reading: attention weights are sharded by head (softmax needs whole rows,
     so a head cannot be split; bowenzhou.top "张量并行", 机制：行切与列切).
+    With GQA the shard's query heads read exactly its own K/V heads, since
+    consecutive query heads share a K/V head.
     """
-    h = w["Wq"].shape[0]
+    h, hk = w["Wq"].shape[0], w["Wk"].shape[1]
     lo, hi = s * h // D, (s + 1) * h // D
-    return w["Wq"][:, lo:hi], w["Wk"][:, lo:hi], w["Wv"][:, lo:hi], w["Wo"][lo:hi, :]
+    klo, khi = s * hk // D, (s + 1) * hk // D
+    return w["Wq"][:, lo:hi], w["Wk"][:, klo:khi], w["Wv"][:, klo:khi], w["Wo"][lo:hi, :]
 
 
 def mlp_shard(w, j: int, D: int):
@@ -280,9 +309,10 @@ def tsp_layer_fwd_sharded(x, w, heads: int, D: int):
     Returns natural-order A, H, MLP, Y (same keys as ``layer_fwd``).
     """
     B, S, h = x.shape
-    if heads % D or h % D or w["Wg"].shape[1] % D:
-        raise ValueError("heads, hidden and ffn must be divisible by D")
     dh = h // heads
+    kv_heads = w["Wk"].shape[1] // dh
+    if heads % D or kv_heads % D or h % D or w["Wg"].shape[1] % D:
+        raise ValueError("heads, kv heads, hidden and ffn must be divisible by D")
     pos = zigzag_positions(S, D)
     xz = zigzag_permute(x, D)  # [D, B, 2C, h]
     twoC = xz.shape[2]
@@ -294,8 +324,8 @@ def tsp_layer_fwd_sharded(x, w, heads: int, D: int):
         Qs = [xz[r] @ Wq_s for r in range(D)]          # local projections
         Ks = [xz[r] @ Wk_s for r in range(D)]
         Vs = [xz[r] @ Wv_s for r in range(D)]
-        Kfull = np.zeros((B, S, h // D))                # all-gather + zigzag reorder
-        Vfull = np.zeros((B, S, h // D))
+        Kfull = np.zeros((B, S, Wk_s.shape[1]))         # all-gather + zigzag reorder
+        Vfull = np.zeros((B, S, Wv_s.shape[1]))
         for r in range(D):
             Kfull[:, pos[r]] = Ks[r]
             Vfull[:, pos[r]] = Vs[r]
@@ -304,11 +334,12 @@ def tsp_layer_fwd_sharded(x, w, heads: int, D: int):
             for b in range(B):
                 for e in range(hps):
                     sl = slice(e * dh, (e + 1) * dh)
-                    sc = (Qs[r][b, :, sl] @ Kfull[b, :, sl].T) * scale
+                    kv = kv_head_slice(e, hps, kv_heads // D, dh)  # within the shard
+                    sc = (Qs[r][b, :, sl] @ Kfull[b, :, kv].T) * scale
                     sc = np.where(np.arange(S)[None, :] <= pos[r][:, None], sc, -np.inf)
                     p = np.exp(sc - sc.max(axis=1, keepdims=True))
                     p /= p.sum(axis=1, keepdims=True)
-                    Os[b, :, sl] = p @ Vfull[b, :, sl]
+                    Os[b, :, sl] = p @ Vfull[b, :, kv]
             Az[r] += Os @ Wo_s                          # partial output stays on rank r
     Hz = xz + Az
     MLPz = np.zeros_like(xz)
@@ -330,19 +361,21 @@ def tsp_layer_fwd_sharded(x, w, heads: int, D: int):
 # Communication-volume model (forward, per rank, elements)
 # ---------------------------------------------------------------------------
 
-def forward_comm_elements(B: int, S: int, h: int, F: int, D: int, scheme: str) -> float:
+def forward_comm_elements(B: int, S: int, h: int, F: int, D: int, scheme: str, kv_hidden: int | None = None) -> float:
     """Elements each rank receives in one layer forward.
 
-    tsp: attention weights of the D-1 remote shards (4 h * h/D each), the MLP
-    ring's D-1 hops (3 h * F/D each) and the K/V all-gather (2 * B*S*h/D
-    elements from each of the other D-1 ranks, head-sharded: 2 B S h (D-1)/D^2
-    per shard step, summed over D shard steps).
+    tsp: attention weights of the D-1 remote shards ((2 h*h + 2 h*hk)/D each,
+    hk = Hk*dh the K/V width, h for multi-head attention), the MLP ring's D-1
+    hops (3 h * F/D each) and the K/V all-gather (2 * B*S*hk/D elements from
+    each of the other D-1 ranks, head-sharded: 2 B S hk (D-1)/D^2 per shard
+    step, summed over D shard steps).
     tp: two ring all-reduces of the full activation, 2 (D-1)/D * B*S*h each
     (bowenzhou.top "张量并行"; r007 chapter, "Тензорный параллелизм").
     """
+    hk = h if kv_hidden is None else kv_hidden
     if scheme == "tsp":
-        weights = (D - 1) * (4 * h * h // D + 3 * h * F // D)
-        kv = 2 * B * S * h * (D - 1) / D
+        weights = (D - 1) * ((2 * h * h + 2 * h * hk) // D + 3 * h * F // D)
+        kv = 2 * B * S * hk * (D - 1) / D
         return weights + kv
     if scheme == "tp":
         return 2 * 2 * (D - 1) / D * B * S * h
