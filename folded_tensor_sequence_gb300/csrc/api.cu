@@ -8,7 +8,9 @@
 //   2. attention: for every weight shard s, every rank projects its local
 //      tokens with {W_Q, W_K, W_V}^s, K/V are all-gathered into natural
 //      order, causal attention runs, and O_s W_O^s is accumulated locally.
-//      Here: one projection GEMM over all shards (N = 3h) whose epilogue does
+//      Here: one projection GEMM over all shards (N = h + 2hk, hk the K/V
+//      width: h for multi-head attention, less with grouped-query attention,
+//      where a shard owns H/D query heads and Hk/D K/V heads) whose epilogue does
 //      the gather, the zigzag-balanced attention kernel, and one output GEMM
 //      whose K loop is the sum over shards (+ residual);
 //   3. gated MLP ring: each rank accumulates SiLU(H W_g^j)(H W_u^j) W_d^j over
@@ -82,6 +84,8 @@ size_t esize(const tsp_plan* p) { return p->dtype == TSP_BF16 ? 2 : 4; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int kv_hidden(const tsp_plan* p) { return p->kv_heads * p->head_dim; }
+
 // Offsets of the layer's activations inside one buffer (the `saved` buffer
 // for the backward and the forward's workspace share this layout).
 struct Layout {
@@ -98,10 +102,11 @@ Layout layer_layout(const tsp_plan* p, int batch) {
     o = align256(o + bytes);
     return at;
   };
+  const size_t hk = kv_hidden(p);
   L.xz = take(T * h * e);
   L.qz = take(T * h * e);
-  L.k = take(T * h * e);
-  L.v = take(T * h * e);
+  L.k = take(T * hk * e);
+  L.v = take(T * hk * e);
   L.oz = take(T * h * e);
   L.lse = take((size_t)batch * p->heads * p->seq * 4);
   L.hz = take(T * h * e);
@@ -130,13 +135,14 @@ BwdLayout bwd_layout(const tsp_plan* p, int batch) {
   L.dgu = take(T * 2 * F * e);
   L.dhz = take(T * h * e);
   L.doz = take(T * h * e);
+  const size_t hk = kv_hidden(p);
   L.dq = take(T * h * e);
-  L.dk = take(T * h * e);
-  L.dv = take(T * h * e);
+  L.dk = take(T * hk * e);
+  L.dv = take(T * hk * e);
   L.dsum = take((size_t)batch * p->heads * p->seq * 4);
-  L.dqkv = take(T * 3 * h * e);
+  L.dqkv = take(T * (h + 2 * hk) * e);
   L.dxz = take(T * h * e);
-  L.vnat = take(T * h * e);  // V in [B][H][S][dh] when the forward saved it transposed
+  L.vnat = take(T * hk * e);  // V in [B][Hk][S][dh] when the forward saved it transposed
   L.end = o;
   return L;
 }
@@ -237,6 +243,7 @@ EpiParams base_epi(const tsp_plan* p, int batch) {
   ep.S = (int)p->seq;
   ep.C = (int)p->chunk;
   ep.H = p->heads;
+  ep.Hk = p->kv_heads;
   ep.dh = p->head_dim;
   ep.h = p->hidden;
   ep.err = dev_error_word();
@@ -276,7 +283,7 @@ tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const ts
   ep.v = v;
   ep.v_transposed = use_tc_attention(p);
   ep.a_natural = x_natural;
-  tsp_status s = run_gemm(p, xz, h, w->qkv, h, T, 3 * h, h, EPI_QKV, ep, st, "QKV projection");
+  tsp_status s = run_gemm(p, xz, h, w->qkv, h, T, h + 2 * kv_hidden(p), h, EPI_QKV, ep, st, "QKV projection");
   if (s != TSP_OK) return s;
   AttnParams ap;
   ap.q = qz;
@@ -287,6 +294,7 @@ tsp_status attention_impl(const tsp_plan* p, int batch, const void* xz, const ts
   ap.D = p->D;
   ap.B = batch;
   ap.H = p->heads;
+  ap.Hk = p->kv_heads;
   ap.dh = p->head_dim;
   ap.S = p->seq;
   ap.C = p->chunk;
@@ -393,6 +401,11 @@ void tsp_debug_fail_next(tsp_status status, int count) {
 
 tsp_status tsp_plan_create(int D, int64_t seq, int hidden, int heads, int head_dim, int ffn, tsp_dtype dtype,
                            tsp_plan** out) {
+  return tsp_plan_create_gqa(D, seq, hidden, heads, heads, head_dim, ffn, dtype, out);
+}
+
+tsp_status tsp_plan_create_gqa(int D, int64_t seq, int hidden, int heads, int kv_heads, int head_dim, int ffn,
+                               tsp_dtype dtype, tsp_plan** out) {
   if (!out) return fail(TSP_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (D < 1) return fail(TSP_ERR_INVALID_ARG, "D = %d < 1", D);
@@ -403,6 +416,10 @@ tsp_status tsp_plan_create(int D, int64_t seq, int hidden, int heads, int head_d
   if (head_dim != 32 && head_dim != 64 && head_dim != 128)
     return fail(TSP_ERR_INVALID_ARG, "head_dim %d not in {32, 64, 128}", head_dim);
   if (heads % D) return fail(TSP_ERR_INVALID_ARG, "heads %d not divisible by D %d", heads, D);
+  if (kv_heads < 1 || heads % kv_heads)
+    return fail(TSP_ERR_INVALID_ARG, "kv_heads %d does not divide heads %d", kv_heads, heads);
+  if (kv_heads % D)
+    return fail(TSP_ERR_INVALID_ARG, "kv_heads %d not divisible by D %d (a shard owns whole K/V heads)", kv_heads, D);
   if (ffn < 1 || ffn % D) return fail(TSP_ERR_INVALID_ARG, "ffn %d not a positive multiple of D %d", ffn, D);
   if (hidden % 8) return fail(TSP_ERR_INVALID_ARG, "hidden %d not a multiple of 8", hidden);
   if (ffn % 128) return fail(TSP_ERR_INVALID_ARG, "ffn %d not a multiple of 128", ffn);
@@ -414,6 +431,7 @@ tsp_status tsp_plan_create(int D, int64_t seq, int hidden, int heads, int head_d
   p->seq = seq;
   p->hidden = hidden;
   p->heads = heads;
+  p->kv_heads = kv_heads;
   p->head_dim = head_dim;
   p->ffn = ffn;
   p->dtype = dtype;
@@ -495,7 +513,7 @@ tsp_status tsp_kv_gather(const tsp_plan* p, int batch, const void* kz, const voi
   if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
   if (batch == 0) return TSP_OK;
   if ((s = check_ptrs({kz, vz, k, v}, "tsp_kv_gather")) != TSP_OK) return s;
-  return cuda_status(launch_kv_gather(kz, vz, k, v, (int)esize(p), p->D, batch, p->seq, p->heads, p->head_dim,
+  return cuda_status(launch_kv_gather(kz, vz, k, v, (int)esize(p), p->D, batch, p->seq, p->kv_heads, p->head_dim,
                                       as_stream(stream)),
                      "kv gather");
 }
@@ -592,6 +610,9 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     return s;
   if (p->dtype != TSP_BF16) return fail(TSP_ERR_UNSUPPORTED, "layer backward is implemented for bf16 plans");
   if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
+  if (p->kv_heads != p->heads && !attn_bwd_tc_supported(p->head_dim, p->chunk))
+    return fail(TSP_ERR_UNSUPPORTED, "grouped-query backward needs chunk %% 128 == 0 (got %lld)",
+                (long long)p->chunk);
   const int64_t T64 = (int64_t)batch * p->seq;
   if (T64 % 64) return fail(TSP_ERR_UNSUPPORTED, "backward needs batch*seq %% 64 == 0 (got %lld)", (long long)T64);
   const BwdLayout L = bwd_layout(p, batch);
@@ -600,7 +621,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   cudaStream_t st = as_stream(stream);
   const char* sv = static_cast<const char*>(saved);
   char* wb = static_cast<char*>(ws);
-  const int T = (int)T64, h = p->hidden, F = p->ffn;
+  const int T = (int)T64, h = p->hidden, F = p->ffn, W3 = h + 2 * kv_hidden(p);
   const int64_t eb = (int64_t)esize(p);
   // transposes `nmat` consecutive [rows][cols] matrices into workspace
   auto tr = [&](const void* src, size_t dst_off, int64_t rows, int64_t cols, const char* what, int nmat = 1) {
@@ -670,7 +691,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   // attention core backward
   const void* v_nat = sv + A.v;
   if (use_tc_attention(p)) {
-    TSP_TRY(tr(sv + A.v, L.vnat, p->head_dim, p->seq, "transpose V^T", batch * p->heads));
+    TSP_TRY(tr(sv + A.v, L.vnat, p->head_dim, p->seq, "transpose V^T", batch * p->kv_heads));
     v_nat = wb + L.vnat;
   }
   if (attn_bwd_tc_supported(p->head_dim, p->chunk)) {
@@ -693,6 +714,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     ab.D = p->D;
     ab.B = batch;
     ab.H = p->heads;
+    ab.Hk = p->kv_heads;
     ab.dh = p->head_dim;
     ab.S = p->seq;
     ab.C = p->chunk;
@@ -732,7 +754,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   {
     Prof pr_asm("assemble dQKV", st);
     TSP_TRY(cuda_status(launch_assemble_dqkv(wb + L.dq, wb + L.dk, wb + L.dv, wb + L.dqkv, p->D, batch, p->seq,
-                                             p->heads, p->head_dim, st),
+                                             p->heads, p->kv_heads, p->head_dim, st),
                         "assemble dQKV"));
   }
   {
@@ -741,15 +763,15 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     e.ldo = h;
     e.resid = wb + L.dhz;
     e.ldr = h;
-    // dx = dH + dQKV Wqkv: B = packed qkv [3h][h] read MN-major
-    TSP_TRY(run_gemm(p, wb + L.dqkv, 3 * h, w->qkv, h, T, h, 3 * h, EPI_RESID, e, st, "dx", false, true));
+    // dx = dH + dQKV Wqkv: B = packed qkv [h + 2hk][h] read MN-major
+    TSP_TRY(run_gemm(p, wb + L.dqkv, W3, w->qkv, h, T, h, W3, EPI_RESID, e, st, "dx", false, true));
   }
   {
     EpiParams e = base_epi(p, batch);
     e.out = dw->qkv;
     e.ldo = h;
-    // dWqkv = dQKV^T xz: A = dQKV [T][3h], B = xz [T][h], both MN-major
-    TSP_TRY(run_gemm(p, wb + L.dqkv, 3 * h, sv + A.xz, h, 3 * h, h, T, EPI_STORE, e, st, "dW_QKV", true, true));
+    // dWqkv = dQKV^T xz: A = dQKV [T][h + 2hk], B = xz [T][h], both MN-major
+    TSP_TRY(run_gemm(p, wb + L.dqkv, W3, sv + A.xz, h, W3, h, T, EPI_STORE, e, st, "dW_QKV", true, true));
   }
   Prof pr_dx("unpermute dx", st);
   return cuda_status(launch_zigzag_rows(wb + L.dxz, dx, h * eb, p->D, batch, p->seq, false, st), "unpermute dx");

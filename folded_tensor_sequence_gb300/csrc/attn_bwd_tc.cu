@@ -48,6 +48,7 @@ constexpr unsigned CODE_DQ = (KID_ATTN_BWD << 8) | 0x80;
 
 struct BwdTcParams {
   int B, H, D;
+  int Hk;  // K/V heads; query head `head` reads K/V head head / (H / Hk)
   int64_t S, C;
   int h;
   const float* lse;   // [B][H][S], natural log
@@ -112,8 +113,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int head = blockIdx.y, b = blockIdx.z;
-  const int64_t bh = (int64_t)b * p.H + head;
+  // blockIdx.y is a K/V head; the `grp` query heads that read it stream through
+  // one after another (their dK, dV contributions add up in tensor memory)
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int grp = p.H / p.Hk;
+  const int64_t bkv = (int64_t)b * p.Hk + kvh;
   auto tile_of = [&](int t) { return t == 0 ? (int)blockIdx.x : nk - 1 - (int)blockIdx.x; };
   const int ntile = (nk - 1 - (int)blockIdx.x == (int)blockIdx.x) ? 1 : 2;
 
@@ -164,11 +168,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(kv_full, 4 * SUB128);
         ++kv_armed;
         for (int c = 0; c < 2; ++c) {
-          tma_load_2d(Ks + c * SUB128, &tmK, c * 64, (int)(bh * p.S + k0), kv_full);
-          tma_load_2d(Vs + c * SUB128, &tmV, c * 64, (int)(bh * p.S + k0), kv_full);
+          tma_load_2d(Ks + c * SUB128, &tmK, c * 64, (int)(bkv * p.S + k0), kv_full);
+          tma_load_2d(Vs + c * SUB128, &tmV, c * 64, (int)(bkv * p.S + k0), kv_full);
         }
         const int nq = (int)((p.S - k0) / KB_QB);
-        for (int i = 0; i < nq; ++i, ++qi) {
+        for (int u = 0; u < grp * nq; ++u, ++qi) {
+          const int i = u % nq;
+          const int head = kvh * grp + u / nq;
+          const int64_t bh = (int64_t)b * p.H + head;
           const int s = qi % QSTG;
           if (!mbar_wait(&q_free[s], ((qi / QSTG) & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 2)) {
             ok = false;
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     for (int t = 0; t < ntile; ++t) {
       const int64_t k0 = (int64_t)tile_of(t) * 128;
-      const int nq = (int)((p.S - k0) / KB_QB);
+      const int nq = grp * (int)((p.S - k0) / KB_QB);  // query blocks of all the group's heads
       if (ok) {
         bool w = true;
         if (lane == 0) w = mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_DKDV | 4);
@@ -273,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- relay: announces each landed stage to the MMA warp ----------------
     uint32_t n = 0;
     for (int t = 0; t < ntile; ++t) {
-      const int nq = (int)((p.S - (int64_t)tile_of(t) * 128) / KB_QB);
+      const int nq = grp * (int)((p.S - (int64_t)tile_of(t) * 128) / KB_QB);
       for (int i = 0; i < nq; ++i, ++n) {
         if (lane == 0) mbar_wait(&q_full[n % QSTG], (n / QSTG) & 1, abort_flag, p.err, CODE_DKDV | 9);
         __syncwarp();
@@ -294,13 +301,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t k0 = (int64_t)tile_of(t) * 128;
       const int nq = (int)((p.S - k0) / KB_QB);
       const int64_t key = k0 + row;
-      for (int i = 0; i < nq; ++i) {
-        const int x = i & 1;
+      for (int u = 0; u < grp * nq; ++u) {
+        const int i = u % nq;  // query block within the head
+        const int x = u & 1;
         const bool got = alive && mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DKDV | 8);
         ++scnt[x];
         alive = __all_sync(0xffffffffu, got);
         if (!alive) {
-          named_bar_sync(kBarDS + (i & 1), kDSThreads);
+          named_bar_sync(kBarDS + (u & 1), kDSThreads);
           continue;
         }
         tc_fence_after();
@@ -339,15 +347,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        named_bar_arrive(kBarDS + (i & 1), kDSThreads);
+        named_bar_arrive(kBarDS + (u & 1), kDSThreads);
       }
       if (!alive) continue;
       const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DKDV | 10);
       alive = __all_sync(0xffffffffu, got);
       if (!alive) continue;
       tc_fence_after();
-      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bh * p.S + key) * HD) + 8 * half;
-      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bh * p.S + key) * HD) + 8 * half;
+      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bkv * p.S + key) * HD) + 8 * half;
+      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bkv * p.S + key) * HD) + 8 * half;
 #pragma unroll 1
       for (int c32 = 0; c32 < 2; ++c32) {
         float a[32], d[32];
@@ -405,6 +413,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int head = blockIdx.y, b = blockIdx.z;
   const int64_t bh = (int64_t)b * p.H + head;
+  const int64_t bkv = (int64_t)b * p.Hk + head / (p.H / p.Hk);  // the K/V head this query head reads
   const int total_tiles = 2 * p.D * n_tiles;
   auto tile_of = [&](int t) { return t == 0 ? total_tiles - 1 - (int)blockIdx.x : (int)blockIdx.x; };
   auto geo = [&](int g, int64_t& zrow0, int64_t& p0) {
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           uint8_t* st = stg + s * DQ_STAGE_BYTES;
           mbar_arrive_expect_tx(&k_full[s], DQ_STAGE_BYTES);
-          const int krow = (int)(bh * p.S + (int64_t)j * DQ_KB);
+          const int krow = (int)(bkv * p.S + (int64_t)j * DQ_KB);
           for (int c = 0; c < 2; ++c) {
             tma_load_2d(st + c * SUB64, &tmK, c * 64, krow, &k_full[s]);
             tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmV, c * 64, krow, &k_full[s]);
@@ -651,7 +660,7 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
   if ((int64_t)a.B * a.S == 0) return TSP_OK;
   const int64_t T = (int64_t)a.B * a.S;
   const int h = a.H * HD;
-  const int64_t kv_rows = (int64_t)a.B * a.H * a.S;
+  const int64_t kv_rows = (int64_t)a.B * a.Hk * a.S;
   CUtensorMap mK128, mV128, mQ64, mdO64, mQ128, mdO128, mK64, mV64;
   if (!make_tma_2d_bf16(&mK128, a.k, kv_rows, HD, HD, 128) || !make_tma_2d_bf16(&mV128, a.v, kv_rows, HD, HD, 128) ||
       !make_tma_2d_bf16(&mQ64, a.q, T, h, h, 64) || !make_tma_2d_bf16(&mdO64, a.dO, T, h, h, 64) ||
@@ -670,6 +679,7 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
   BwdTcParams p;
   p.B = a.B;
   p.H = a.H;
+  p.Hk = a.Hk;
   p.D = a.D;
   p.S = a.S;
   p.C = a.C;
@@ -681,7 +691,7 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = dev_error_word();
   const int nk = (int)(a.S / 128);
-  dim3 g1((nk + 1) / 2, a.H, a.B);
+  dim3 g1((nk + 1) / 2, a.Hk, a.B);
   if (which & 1) {
     attn_dkdv_tc_kernel<<<g1, THREADS, DKDV_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk);
     if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;

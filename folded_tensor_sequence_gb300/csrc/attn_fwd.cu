@@ -44,8 +44,9 @@ __global__ void attn_fwd_f32_kernel(AttnParams p) {
   for (int d = lane; d < dh; d += 32) qs[d] = q[d];
   __syncwarp();
   const float scale = 1.0f / sqrtf((float)dh);
-  const float* K = static_cast<const float*>(p.k) + ((b * p.H + head) * p.S) * dh;
-  const float* V = static_cast<const float*>(p.v) + ((b * p.H + head) * p.S) * dh;
+  const int kvh = head / (p.H / p.Hk);  // K/V head read by this query head
+  const float* K = static_cast<const float*>(p.k) + ((b * p.Hk + kvh) * p.S) * dh;
+  const float* V = static_cast<const float*>(p.v) + ((b * p.Hk + kvh) * p.S) * dh;
   float m = -INFINITY, l = 0.0f;
   float o[4] = {0.f, 0.f, 0.f, 0.f};  // dims lane + 32 i
   for (int64_t j0 = 0; j0 <= qpos; j0 += 32) {
@@ -107,8 +108,9 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_fwd_bf16_kernel(AttnParams p
   const int64_t C = p.C, S = p.S;
   const int h = p.H * DH;
   const float sl2 = kLog2e / sqrtf((float)DH);
-  const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + ((int64_t)b * p.H + head) * S * DH;
-  const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(p.v) + ((int64_t)b * p.H + head) * S * DH;
+  const int kvh = head / (p.H / p.Hk);  // K/V head read by this query head
+  const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(p.k) + ((int64_t)b * p.Hk + kvh) * S * DH;
+  const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(p.v) + ((int64_t)b * p.Hk + kvh) * S * DH;
   const int total_tiles = 2 * D * n_tiles;
 
   for (int which = 0; which < 2; ++which) {

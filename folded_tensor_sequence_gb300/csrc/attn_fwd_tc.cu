@@ -2,8 +2,9 @@
 // (tcgen05 + TMEM), zigzag token layout, head_dim 128, bf16 in, fp32 softmax.
 //
 // Queries come from the zigzag rows of the rank that owns them; keys and
-// values from the gathered natural-order tensors (K as [B][H][S][128], V
-// transposed as [B][H][128][S]) -- the K/V all-gather of the TSP attention
+// values from the gathered natural-order tensors (K as [B][Hk][S][128], V
+// transposed as [B][Hk][128][S]; with grouped-query attention Hk < H and a
+// query head reads K/V head head / (H / Hk)) -- the K/V all-gather of the TSP attention
 // schedule (ai-trends.today TSP article, "How to Fold a Book").  Online
 // softmax as in FlashAttention / ring attention (r007 chapter, "Параллелизм по
 // контексту: Ring Attention против Ulysses").
@@ -53,6 +54,7 @@ constexpr int kHandoffThreads = 128 + 32;
 
 struct FaParams {
   int B, H, D, nb;  // nb = 256-query blocks per chunk
+  int Hk;           // K/V heads; query head `head` reads K/V head head / (H / Hk)
   int64_t S, C;
   int h;
   __nv_bfloat16* o;
@@ -200,8 +202,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 8) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
-      const int64_t kv_row0 = ((int64_t)b * p.H + head) * p.S;   // K rows of this head
-      const int64_t vt_row0 = ((int64_t)b * p.H + head) * HD;    // V^T rows of this head
+      const int kvh = head / (p.H / p.Hk);                        // the K/V head this query head reads
+      const int64_t kv_row0 = ((int64_t)b * p.Hk + kvh) * p.S;   // K rows of that head
+      const int64_t vt_row0 = ((int64_t)b * p.Hk + kvh) * HD;    // V^T rows of that head
       uint32_t item = 0;
       bool ok = true;
       int q_loaded = 0;
@@ -499,8 +502,8 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   const int h = a.H * HD;
   CUtensorMap mq, mk, mv;
   if (!make_tma_2d_bf16(&mq, a.q, T, h, h, 128) ||
-      !make_tma_2d_bf16(&mk, a.k, (int64_t)a.B * a.H * a.S, HD, HD, 128) ||
-      !make_tma_2d_bf16(&mv, a.v, (int64_t)a.B * a.H * HD, a.S, a.S, 128))
+      !make_tma_2d_bf16(&mk, a.k, (int64_t)a.B * a.Hk * a.S, HD, HD, 128) ||
+      !make_tma_2d_bf16(&mv, a.v, (int64_t)a.B * a.Hk * HD, a.S, a.S, 128))
     return TSP_ERR_CUDA;
   static bool configured = false;
   if (!configured) {
@@ -512,6 +515,7 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   FaParams p;
   p.B = a.B;
   p.H = a.H;
+  p.Hk = a.Hk;
   p.D = a.D;
   p.nb = (int)(a.C / (2 * QT));
   p.S = a.S;

@@ -57,12 +57,13 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
       } else if (epi == EPI_RESID) {
         v += static_cast<const float*>(ep.resid)[m * ep.ldr + n];
         static_cast<float*>(ep.out)[m * ep.ldo + n] = v;
-      } else {  // EPI_QKV
-        const int hs = ep.h / ep.D;
-        const int s = (int)(n / (3 * hs));
-        const int within = (int)(n - (int64_t)s * 3 * hs);
-        const int which = within / hs, cin = within % hs;
-        const int head = s * (ep.H / ep.D) + cin / ep.dh, d = cin % ep.dh;
+      } else {  // EPI_QKV: a shard's packed columns are Q (h/D) | K (Hk*dh/D) | V (Hk*dh/D)
+        const int hs = ep.h / ep.D, ks = ep.Hk * ep.dh / ep.D;
+        const int s = (int)(n / (hs + 2 * ks));
+        const int within = (int)(n - (int64_t)s * (hs + 2 * ks));
+        const int which = within < hs ? 0 : (within < hs + ks ? 1 : 2);
+        const int cin = within - (which == 0 ? 0 : hs + (which - 1) * ks);
+        const int head = s * ((which == 0 ? ep.H : ep.Hk) / ep.D) + cin / ep.dh, d = cin % ep.dh;
         if (which == 0) {
           static_cast<float*>(ep.q)[m * ep.h + head * ep.dh + d] = v;
         } else {
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
           const int64_t r = m / per_rank, rem = m % per_rank, b = rem / twoC, k = rem % twoC;
           const int64_t p = k < ep.C ? r * ep.C + k : (2 * ep.D - 1 - r) * ep.C + (k - ep.C);
           float* dst = static_cast<float*>(which == 1 ? ep.k : ep.v);
-          dst[((b * ep.H + head) * ep.S + p) * ep.dh + d] = v;
+          dst[((b * ep.Hk + head) * ep.S + p) * ep.dh + d] = v;
         }
       }
     }

@@ -2,7 +2,7 @@
 //
 // C[M][N] = sum_k A[m][k] * B[n][k], both operands K-major bf16, fp32
 // accumulation in tensor memory, fused epilogues for the TSP layer:
-//   - QKV projection over all weight shards at once (N = 3h): the epilogue
+//   - QKV projection over all weight shards at once (N = h + 2*Hk*dh): the epilogue
 //     writes Q in zigzag token order and scatters K/V straight into gathered
 //     natural order per head, which is the zigzag K/V all-gather of the TSP
 //     attention schedule done for free (ai-trends.today TSP article, "How to
@@ -295,23 +295,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < 32; ++i) v[i] += r[i];
             store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + (ep.out_natural ? nat : m) * ep.ldo + n, v);
           } else if constexpr (EPI == EPI_QKV) {
-            // packed column n -> (shard s, which of q/k/v, head, d)
-            const int hs = ep.h / ep.D;  // columns of one projection in one shard
-            const int s = (int)(n / (3 * hs));
-            const int within = (int)(n - (int64_t)s * 3 * hs);
-            const int which = within / hs;
-            const int cin = within - which * hs;
-            const int head = s * (ep.H / ep.D) + cin / ep.dh;
+            // packed column n -> (shard s, which of q/k/v, head, d); a shard's
+            // columns are Q (h/D) | K (Hk*dh/D) | V (Hk*dh/D)
+            const int hs = ep.h / ep.D, ks = ep.Hk * ep.dh / ep.D;
+            const int s = (int)(n / (hs + 2 * ks));
+            const int within = (int)(n - (int64_t)s * (hs + 2 * ks));
+            const int which = within < hs ? 0 : (within < hs + ks ? 1 : 2);
+            const int cin = within - (which == 0 ? 0 : hs + (which - 1) * ks);
+            const int head = s * ((which == 0 ? ep.H : ep.Hk) / ep.D) + cin / ep.dh;
             const int d = cin % ep.dh;
             if (which == 0) {
               store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.q) + m * ep.h + head * ep.dh + d, v);
             } else if (which == 1 || !ep.v_transposed) {
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 1 ? ep.k : ep.v);
-              store32_bf16(dst + (((int64_t)b * ep.H + head) * ep.S + p) * ep.dh + d, v);
+              store32_bf16(dst + (((int64_t)b * ep.Hk + head) * ep.S + p) * ep.dh + d, v);
             } else {
-              // V^T [B][H][dh][S]: lanes hold consecutive positions, so each store is coalesced
+              // V^T [B][Hk][dh][S]: lanes hold consecutive positions, so each store is coalesced
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(ep.v) +
-                                   (((int64_t)b * ep.H + head) * ep.dh + d) * ep.S + p;
+                                   (((int64_t)b * ep.Hk + head) * ep.dh + d) * ep.S + p;
 #pragma unroll
               for (int i = 0; i < 32; ++i) dst[(int64_t)i * ep.S] = __float2bfloat16_rn(v[i]);
             }

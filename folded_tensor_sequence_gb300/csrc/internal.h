@@ -12,6 +12,7 @@ struct tsp_plan {
   int64_t seq;
   int hidden;
   int heads;
+  int kv_heads;  // K/V heads (== heads for multi-head attention, fewer for grouped-query attention)
   int head_dim;
   int ffn;
   tsp_dtype dtype;
@@ -24,7 +25,7 @@ namespace tsp {
 enum EpiKind : int {
   EPI_STORE = 0,    // out[m][n] = acc
   EPI_RESID = 1,    // out[m][n] = resid[m][n] + acc
-  EPI_QKV = 2,      // scatter packed Q|K|V columns: Q to zigzag rows, K/V gathered per head
+  EPI_QKV = 2,      // scatter packed Q|K|V columns: Q to zigzag rows, K/V gathered per K/V head
   EPI_SWIGLU = 3,   // gate/up 128-column blocks -> out[m][f] = SiLU(g) * u; optional raw copy to aux
   EPI_DSWIGLU = 4,  // acc = dM[m][f]; reads saved G/U (resid, packed gate_up order) -> dGU to out
 };
@@ -40,8 +41,9 @@ struct EpiParams {
   void* k = nullptr;
   void* v = nullptr;
   int D = 1, B = 1, S = 0, C = 0, H = 1, dh = 1, h = 0;
+  int Hk = 1;                   // EPI_QKV: K/V heads; a shard's packed columns are Q (h/D) | K (Hk*dh/D) | V
   unsigned int* err = nullptr;  // device error word
-  bool v_transposed = false;    // EPI_QKV: write V as [B][H][dh][S] instead of [B][H][S][dh]
+  bool v_transposed = false;    // EPI_QKV: write V as [B][Hk][dh][S] instead of [B][Hk][S][dh]
   // Zigzag row m <-> natural row remapping (uses D, B, S, C; needs C % 128 == 0):
   //   a_natural:     the A operand is natural-order rows; tile rows of zigzag
   //                  rows m0.. are read from natural row nat(m0)..
@@ -84,24 +86,27 @@ cudaError_t launch_pack_weights(const tsp_plan* p, const void* const c[7], const
                                 cudaStream_t stream);
 
 // Attention.
+// Query head `head` reads K/V head head / (H / Hk) (grouped-query attention;
+// Hk == H is multi-head attention).
 struct AttnParams {
   const void* q;  // zigzag rows [T][h]
-  const void* k;  // [B][H][S][dh]
+  const void* k;  // [B][Hk][S][dh]
   const void* v;
   void* o;        // zigzag rows [T][h]
   float* lse;     // [B][H][S] natural log, may be null
   int D, B, H, dh;
   int64_t S, C;
+  int Hk;
 };
 tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream);
 tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream);
-// tcgen05 attention (V given transposed, [B][H][dh][S]); needs head_dim 128 and chunk % 256 == 0.
+// tcgen05 attention (V given transposed, [B][Hk][dh][S]); needs head_dim 128 and chunk % 256 == 0.
 bool attn_tc_supported(int head_dim, int64_t chunk);
 tsp_status attn_fwd_bf16_tc(const AttnParams& p, cudaStream_t stream);
 
 struct AttnBwdParams {
   const void* q;   // zigzag [T][h]
-  const void* k;   // [B][H][S][dh]
+  const void* k;   // [B][H][S][dh] (multi-head attention only)
   const void* v;
   const void* o;   // zigzag [T][h]
   const void* dO;  // zigzag [T][h]
@@ -121,23 +126,25 @@ cudaError_t launch_attn_dsum(const void* o, const void* dO, float* dsum, int D, 
 // tcgen05 attention backward (head_dim 128, chunk % 128 == 0).
 struct AttnBwdTcArgs {
   const void* q;    // zigzag [T][h]
-  const void* k;    // [B][H][S][dh]
-  const void* v;    // [B][H][S][dh]
+  const void* k;    // [B][Hk][S][dh]
+  const void* v;    // [B][Hk][S][dh]
   const void* dO;   // zigzag [T][h]
   const float* lse;
   const float* dsum;
   void* dq;
-  void* dk;
+  void* dk;         // [B][Hk][S][dh]: summed over the query heads that read the K/V head
   void* dv;
   int D, B, H, dh;
   int64_t S, C;
+  int Hk;
 };
 bool attn_bwd_tc_supported(int head_dim, int64_t chunk);
 // which: 1 = the dK/dV kernel, 2 = the dQ kernel, 3 = both.
 tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int which = 3);
 
 // Backward helpers.
+// dqkv [T][h + 2*Hk*dh] in the packed column order <- dq zigzag [T][h], dk/dv [B][Hk][S][dh].
 cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
-                                 int64_t S, int H, int dh, cudaStream_t stream);
+                                 int64_t S, int H, int Hk, int dh, cudaStream_t stream);
 
 }  // namespace tsp

@@ -54,7 +54,7 @@ __global__ void zigzag_rows_kernel(const uint4* __restrict__ src, uint4* __restr
   }
 }
 
-// Gathered [B][H][S][dh] <- zigzag [T][h]; iterates over destination vectors.
+// Gathered [B][H][S][dh] <- zigzag [T][H*dh] (H: the K/V head count); iterates over destination vectors.
 __global__ void kv_gather_kernel(const uint4* __restrict__ kz, const uint4* __restrict__ vz, uint4* __restrict__ k,
                                  uint4* __restrict__ v, int vec_per_head, int D, int B, int64_t S, int H) {
   const int64_t C = S / (2 * D);
@@ -77,11 +77,12 @@ __global__ void kv_gather_kernel(const uint4* __restrict__ kz, const uint4* __re
   }
 }
 
-// dqkv [T][3h] in packed column order <- dq zigzag [T][h], dk/dv gathered [B][H][S][dh].
+// dqkv [T][h + 2hk] in packed column order <- dq zigzag [T][h], dk/dv gathered
+// [B][Hk][S][dh] (hk = Hk*dh; a shard's columns are Q h/D | K hk/D | V hk/D).
 // One CTA per zigzag row: the row's (rank, batch, position) is decoded once.
 __global__ void assemble_dqkv_kernel(const uint4* __restrict__ dq, const uint4* __restrict__ dk,
                                      const uint4* __restrict__ dv, uint4* __restrict__ out, int vec_per_head, int D,
-                                     int B, int64_t S, int H) {
+                                     int B, int64_t S, int H, int Hk) {
   const int64_t C = S / (2 * D);
   const int64_t twoC = 2 * C;
   const int64_t zrow = blockIdx.x;
@@ -90,23 +91,23 @@ __global__ void assemble_dqkv_kernel(const uint4* __restrict__ dq, const uint4* 
   const int64_t b = rem / twoC;
   const int64_t kk = rem - b * twoC;
   const int64_t p = zigzag_pos(r, kk, C, D);
-  const int hpv = H / D;                       // heads per shard
-  const int proj = hpv * vec_per_head;         // vectors of one projection in one shard
-  const int vec_per_proj = H * vec_per_head;   // vectors of h columns
-  const uint4* dq_row = dq + zrow * vec_per_proj;
-  uint4* out_row = out + zrow * 3 * (int64_t)vec_per_proj;
-  for (int cv = threadIdx.x; cv < 3 * vec_per_proj; cv += blockDim.x) {
-    const int s = cv / (3 * proj);
-    const int within = cv - s * 3 * proj;
-    const int which = within / proj;
-    const int cin = within - which * proj;
-    const int head = s * hpv + cin / vec_per_head;
+  const int qs = (H / D) * vec_per_head;       // Q vectors of one shard
+  const int ks = (Hk / D) * vec_per_head;      // K (and V) vectors of one shard
+  const int row_vecs = (H + 2 * Hk) * vec_per_head;
+  const uint4* dq_row = dq + zrow * (int64_t)H * vec_per_head;
+  uint4* out_row = out + zrow * (int64_t)row_vecs;
+  for (int cv = threadIdx.x; cv < row_vecs; cv += blockDim.x) {
+    const int s = cv / (qs + 2 * ks);
+    const int within = cv - s * (qs + 2 * ks);
+    const int which = within < qs ? 0 : (within < qs + ks ? 1 : 2);
+    const int cin = within - (which == 0 ? 0 : qs + (which - 1) * ks);
     const int d = cin % vec_per_head;
     uint4 v;
     if (which == 0) {
-      v = __ldg(&dq_row[head * vec_per_head + d]);
+      v = __ldg(&dq_row[(s * (H / D) + cin / vec_per_head) * vec_per_head + d]);
     } else {
-      const int64_t g = ((b * H + head) * S + p) * vec_per_head + d;
+      const int head = s * (Hk / D) + cin / vec_per_head;
+      const int64_t g = ((b * Hk + head) * S + p) * vec_per_head + d;
       v = __ldg(which == 1 ? &dk[g] : &dv[g]);
     }
     out_row[cv] = v;
@@ -197,20 +198,26 @@ template <typename T>
 __global__ void pack_kernel(const T* __restrict__ Wq, const T* __restrict__ Wk, const T* __restrict__ Wv,
                             const T* __restrict__ Wo, const T* __restrict__ Wg, const T* __restrict__ Wu,
                             const T* __restrict__ Wd, T* __restrict__ Pqkv, T* __restrict__ Po,
-                            T* __restrict__ Pgu, T* __restrict__ Pd, int h, int F, int D, bool unpack) {
-  const int64_t n_qkv = 3LL * h * h, n_o = (int64_t)h * h, n_gu = 2LL * F * h, n_d = (int64_t)h * F;
+                            T* __restrict__ Pgu, T* __restrict__ Pd, int h, int hk, int F, int D, bool unpack) {
+  const int64_t n_qkv = (int64_t)(h + 2 * hk) * h, n_o = (int64_t)h * h, n_gu = 2LL * F * h, n_d = (int64_t)h * F;
   const int64_t total = n_qkv + n_o + n_gu + n_d;
-  const int hs = h / D;
+  const int hs = h / D, ks = hk / D;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     T* packed;
     const T* canon;
     int64_t pidx, cidx;
     if (i < n_qkv) {
-      const int64_t n = i / h, k = i % h;  // packed row n, column k
-      const int64_t s = n / (3 * hs), within = n % (3 * hs);
-      const int64_t which = within / hs, col = s * hs + within % hs;
-      canon = which == 0 ? Wq : (which == 1 ? Wk : Wv);
-      cidx = k * h + col;
+      // packed row n (shard s: Q h/D rows | K hk/D | V hk/D), column k
+      const int64_t n = i / h, k = i % h;
+      const int64_t s = n / (hs + 2 * ks), within = n % (hs + 2 * ks);
+      if (within < hs) {
+        canon = Wq;
+        cidx = k * h + s * hs + within;
+      } else {
+        const int64_t kv = within - hs;
+        canon = kv < ks ? Wk : Wv;
+        cidx = k * hk + s * ks + (kv < ks ? kv : kv - ks);
+      }
       packed = Pqkv;
       pidx = i;
     } else if (i < n_qkv + n_o) {
@@ -272,13 +279,13 @@ cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, i
 }
 
 cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
-                                 int64_t S, int H, int dh, cudaStream_t stream) {
+                                 int64_t S, int H, int Hk, int dh, cudaStream_t stream) {
   const int vph = dh * 2 / 16;
   const int64_t T = (int64_t)B * S;
   if (T == 0) return cudaSuccess;
   assemble_dqkv_kernel<<<(unsigned)T, 256, 0, stream>>>(static_cast<const uint4*>(dq), static_cast<const uint4*>(dk),
                                                          static_cast<const uint4*>(dv), static_cast<uint4*>(dqkv),
-                                                         vph, D, B, S, H);
+                                                         vph, D, B, S, H, Hk);
   return cudaGetLastError();
 }
 
@@ -313,18 +320,18 @@ cudaError_t launch_swiglu_f32(const float* gu, float* m, int64_t T, int F, cudaS
 
 cudaError_t launch_pack_weights(const tsp_plan* p, const void* const c[7], const tsp_weight_grads* w, bool unpack,
                                 cudaStream_t stream) {
-  const int h = p->hidden, F = p->ffn, D = p->D;
-  const int64_t total = 4LL * h * h + 3LL * h * F;
+  const int h = p->hidden, F = p->ffn, D = p->D, hk = p->kv_heads * p->head_dim;
+  const int64_t total = (int64_t)(h + 2 * hk) * h + (int64_t)h * h + 3LL * h * F;
   if (p->dtype == TSP_BF16)
     pack_kernel<uint16_t><<<grid_for(total, 256), 256, 0, stream>>>(
         (const uint16_t*)c[0], (const uint16_t*)c[1], (const uint16_t*)c[2], (const uint16_t*)c[3],
         (const uint16_t*)c[4], (const uint16_t*)c[5], (const uint16_t*)c[6], (uint16_t*)w->qkv, (uint16_t*)w->o,
-        (uint16_t*)w->gate_up, (uint16_t*)w->down, h, F, D, unpack);
+        (uint16_t*)w->gate_up, (uint16_t*)w->down, h, hk, F, D, unpack);
   else
     pack_kernel<uint32_t><<<grid_for(total, 256), 256, 0, stream>>>(
         (const uint32_t*)c[0], (const uint32_t*)c[1], (const uint32_t*)c[2], (const uint32_t*)c[3],
         (const uint32_t*)c[4], (const uint32_t*)c[5], (const uint32_t*)c[6], (uint32_t*)w->qkv, (uint32_t*)w->o,
-        (uint32_t*)w->gate_up, (uint32_t*)w->down, h, F, D, unpack);
+        (uint32_t*)w->gate_up, (uint32_t*)w->down, h, hk, F, D, unpack);
   return cudaGetLastError();
 }
 

@@ -25,7 +25,7 @@ EXPORTS = [
     "tsp_last_error_message", "tsp_pack_weights", "tsp_unpack_weights", "tsp_zigzag_permute",
     "tsp_zigzag_unpermute", "tsp_kv_gather", "tsp_attention_fwd", "tsp_gated_mlp_fwd", "tsp_layer_fwd",
     "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next", "tsp_profile_enable", "tsp_profile_report",
-    "tsp_attention_fwd_static", "tsp_debug_wait_timeout",
+    "tsp_attention_fwd_static", "tsp_debug_wait_timeout", "tsp_plan_create_gqa",
 ]
 
 
@@ -57,6 +57,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(path)
         vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
         L.tsp_plan_create.argtypes = [i32, i64, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+        L.tsp_plan_create_gqa.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
         L.tsp_plan_destroy.argtypes = [vp]
         L.tsp_plan_destroy.restype = None
         L.tsp_workspace_bytes.argtypes = [vp, i32, i32]
@@ -120,10 +121,15 @@ def _stream(stream) -> int | None:
 class Plan:
     """Owns a tsp_plan*; mirrors its shape fields."""
 
-    def __init__(self, handle: int, D, seq, hidden, heads, head_dim, ffn, dtype):
+    def __init__(self, handle: int, D, seq, hidden, heads, head_dim, ffn, dtype, kv_heads=None):
         self.handle = handle
         self.D, self.seq, self.hidden, self.heads, self.head_dim, self.ffn = D, seq, hidden, heads, head_dim, ffn
+        self.kv_heads = heads if kv_heads is None else kv_heads
         self.dtype = dtype
+
+    @property
+    def kv_hidden(self) -> int:
+        return self.kv_heads * self.head_dim
 
     @property
     def torch_dtype(self):
@@ -141,6 +147,21 @@ def tsp_plan_create(D: int, seq: int, hidden: int, heads: int, head_dim: int, ff
     out = ctypes.c_void_p()
     _check(lib().tsp_plan_create(D, seq, hidden, heads, head_dim, ffn, dtype, ctypes.byref(out)), "tsp_plan_create")
     return Plan(out.value, D, seq, hidden, heads, head_dim, ffn, dtype)
+
+
+def tsp_plan_create_gqa(D: int, seq: int, hidden: int, heads: int, kv_heads: int, head_dim: int, ffn: int,
+                        dtype) -> Plan:
+    if isinstance(dtype, str):
+        dtype = TSP_BF16 if dtype == "bf16" else TSP_F32
+    out = ctypes.c_void_p()
+    _check(lib().tsp_plan_create_gqa(D, seq, hidden, heads, kv_heads, head_dim, ffn, dtype, ctypes.byref(out)),
+           "tsp_plan_create_gqa")
+    return Plan(out.value, D, seq, hidden, heads, head_dim, ffn, dtype, kv_heads)
+
+
+def plan_for(cfg) -> Plan:
+    """Plan of a workload description (fields D, seq, hidden, heads, head_dim, ffn, dtype, kv_h)."""
+    return tsp_plan_create_gqa(cfg.D, cfg.seq, cfg.hidden, cfg.heads, cfg.kv_h, cfg.head_dim, cfg.ffn, cfg.dtype)
 
 
 def tsp_workspace_bytes(plan: Plan, batch: int, op: int) -> int:
@@ -200,7 +221,7 @@ class PackedWeights:
 def empty_packed(plan: Plan, device="cuda") -> PackedWeights:
     h, F, dt = plan.hidden, plan.ffn, plan.torch_dtype
     return PackedWeights(
-        qkv=torch.empty(3 * h, h, dtype=dt, device=device),
+        qkv=torch.empty(h + 2 * plan.kv_hidden, h, dtype=dt, device=device),
         o=torch.empty(h, h, dtype=dt, device=device),
         gate_up=torch.empty(2 * F, h, dtype=dt, device=device),
         down=torch.empty(h, F, dtype=dt, device=device),

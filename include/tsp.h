@@ -41,17 +41,27 @@
  *   - tsp_last_error_message() gives a thread-local description of the last
  *     non-OK status.
  *
- * Layouts (T = batch * seq tokens, C = seq / (2D), h = heads * head_dim)
+ * Grouped-query attention (plans from tsp_plan_create_gqa): K and V have
+ * Hk <= H heads, Wk and Wv are [h][hk] with hk = Hk * head_dim, and query
+ * head e reads K/V head e / (H / Hk).  The r007 chapter (section
+ * "Параллелизм по контексту: Ring Attention против Ulysses") names GQA, with
+ * the K/V head count often cut to 8, as what bounds a head split; here a
+ * weight shard owns H/D query heads and Hk/D K/V heads, so Hk % D == 0.
+ * Multi-head attention is the case Hk == H.
+ *
+ * Layouts (T = batch * seq tokens, C = seq / (2D), h = heads * head_dim,
+ * hk = kv_heads * head_dim, equal to h for multi-head attention)
  *   natural   x[b][p][h]               (row b*seq + p)
  *   zigzag    xz[r][b][k][h]            (row (r*batch + b)*2C + k) holding
  *             natural position pos(r,k) = r*C + k for k < C, and
  *             (2D-1-r)*C + (k-C) for k >= C
- *   gathered  K[b][head][p][head_dim], V likewise (natural positions)
+ *   gathered  K[b][kv_head][p][head_dim], V likewise (natural positions)
  *   lse       lse[b][head][p] fp32: natural log of sum_j exp(score_pj)
  *   packed weights (each row holds one output column, contiguous over the
  *   input dimension, i.e. the transposed weight, ready as a K-major operand):
- *     qkv     [3h][h]: for shard s = 0..D-1: the Q, then K, then V columns
- *             of heads s*H/D .. (s+1)*H/D-1 (h/D rows each);
+ *     qkv     [h+2hk][h]: for shard s = 0..D-1: the Q columns of query
+ *             heads s*H/D .. (s+1)*H/D-1 (h/D rows), then the K, then the
+ *             V columns of K/V heads s*Hk/D .. (s+1)*Hk/D-1 (hk/D rows each);
  *     o       [h][h]:  row n = column n of W_O (input rows of shard s are
  *             input indices s*h/D .. (s+1)*h/D-1);
  *     gate_up [2F][h]: blocks of 256 rows; block j holds gate columns
@@ -114,6 +124,13 @@ typedef struct {
  * TSP_ERR_UNSUPPORTED.  *out receives a new plan (free with tsp_plan_destroy). */
 tsp_status tsp_plan_create(int D, int64_t seq, int hidden, int heads, int head_dim, int ffn,
                            tsp_dtype dtype, tsp_plan** out);
+/* The same with grouped-query attention: kv_heads K/V heads shared by the
+ * `heads` query heads (consecutive groups of heads/kv_heads).  Extra rules:
+ * kv_heads >= 1, heads % kv_heads == 0, kv_heads % D == 0 (TSP_ERR_INVALID_ARG
+ * otherwise).  tsp_layer_bwd of such a plan also needs seq/(2D) % 128 == 0
+ * (TSP_ERR_UNSUPPORTED otherwise).  kv_heads == heads gives tsp_plan_create. */
+tsp_status tsp_plan_create_gqa(int D, int64_t seq, int hidden, int heads, int kv_heads, int head_dim, int ffn,
+                               tsp_dtype dtype, tsp_plan** out);
 void tsp_plan_destroy(tsp_plan* plan);
 
 /* Workspace bytes needed by `op` for `batch` sequences (0 on invalid input). */
@@ -140,8 +157,8 @@ tsp_status tsp_unpack_weights(const tsp_plan* plan, const tsp_weights* packed,
 tsp_status tsp_zigzag_permute(const tsp_plan* plan, int batch, const void* x, void* xz, void* stream);
 /* xz zigzag -> x natural. */
 tsp_status tsp_zigzag_unpermute(const tsp_plan* plan, int batch, const void* xz, void* x, void* stream);
-/* The K/V all-gather with zigzag reorder: kz, vz zigzag [D][batch][2C][h]
- * (head-major columns) -> k, v gathered [batch][heads][seq][head_dim]. */
+/* The K/V all-gather with zigzag reorder: kz, vz zigzag [D][batch][2C][hk]
+ * (head-major columns) -> k, v gathered [batch][kv_heads][seq][head_dim]. */
 tsp_status tsp_kv_gather(const tsp_plan* plan, int batch, const void* kz, const void* vz,
                          void* k, void* v, void* stream);
 

@@ -117,3 +117,34 @@ def test_wait_probe_validates_on_host(tsp):
     L = tsp.lib()
     assert L.tsp_debug_wait_timeout(0, None) == tsp.TSP_ERR_INVALID_ARG
     assert L.tsp_debug_wait_timeout(20000000, None) == tsp.TSP_ERR_INVALID_ARG
+
+
+def test_gqa_plan_validation_and_sizes(tsp):
+    p = tsp.tsp_plan_create_gqa(8, 16384, 4096, 32, 8, 128, 14336, "bf16")
+    assert p.kv_heads == 8 and p.kv_hidden == 1024
+    mha = tsp.tsp_plan_create(8, 16384, 4096, 32, 128, 14336, "bf16")
+    # K and V (and their gradients) shrink with the K/V head count
+    assert tsp.tsp_saved_bytes(p, 2) < tsp.tsp_saved_bytes(mha, 2)
+    assert tsp.tsp_workspace_bytes(p, 2, tsp.TSP_OP_LAYER_BWD) < tsp.tsp_workspace_bytes(mha, 2, tsp.TSP_OP_LAYER_BWD)
+    # kv_heads == heads is the multi-head plan
+    same = tsp.tsp_plan_create_gqa(8, 16384, 4096, 32, 32, 128, 14336, "bf16")
+    assert tsp.tsp_saved_bytes(same, 2) == tsp.tsp_saved_bytes(mha, 2)
+    bad = [
+        (2, 1024, 512, 4, 3, 128, 512),   # kv_heads does not divide heads
+        (4, 1024, 1024, 8, 2, 128, 512),  # kv_heads % D (a shard must own whole K/V heads)
+        (2, 1024, 512, 4, 0, 128, 512),   # kv_heads < 1
+    ]
+    for args in bad:
+        with pytest.raises(tsp.TspError) as ei:
+            tsp.tsp_plan_create_gqa(*args, "bf16")
+        assert ei.value.status == tsp.TSP_ERR_INVALID_ARG
+
+
+def test_gqa_backward_needs_128_query_chunks(tsp):
+    L = tsp.lib()
+    w = tsp._Weights(0x1000, 0x2000, 0x3000, 0x4000)
+    p = tsp.tsp_plan_create_gqa(2, 640, 512, 4, 2, 128, 512, "bf16")  # chunk 160
+    st = L.tsp_layer_bwd(p.handle, 1, 0x1000, ctypes.byref(w), 0x2000, 0x3000, 0x4000, ctypes.byref(w), 0x5000,
+                         1 << 40, None)
+    assert st == tsp.TSP_ERR_UNSUPPORTED
+    assert "grouped-query" in tsp.tsp_last_error_message()

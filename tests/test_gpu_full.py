@@ -9,6 +9,8 @@
   over the whole output.
 * 8K tokens forward + backward: the full fp64 oracle gradient (dx and all
   seven weight gradients) against the GPU.
+* The same checks with grouped-query attention (8 K/V heads for 32 query
+  heads) at 16K tokens (sampled rows) and 8K tokens (full backward).
 
 Inputs are drawn by the seeded generator (torch integer recipe on the host)
 once and handed to both sides.
@@ -17,15 +19,16 @@ import numpy as np
 import pytest
 
 from folded_tensor_sequence_gb300 import synth
-from folded_tensor_sequence_gb300.configs import LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_S8K, TRAIN_7B_S16K
+from folded_tensor_sequence_gb300.configs import (LAYER_7B_GQA8_S16K, LAYER_7B_S16K, LAYER_7B_S64K, TRAIN_7B_GQA8_S8K,
+                                                  TRAIN_7B_S8K, TRAIN_7B_S16K)
 from oracle import tsp_oracle as O
 
 from helpers import check, rel_frob, to_np
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = lambda h, F: {"Wq": (h, h), "Wk": (h, h), "Wv": (h, h), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F),
-                       "Wd": (F, h)}
+SHAPES = lambda h, F, hk: {"Wq": (h, h), "Wk": (h, hk), "Wv": (h, hk), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F),
+                           "Wd": (F, h)}
 
 
 @pytest.fixture(scope="module")
@@ -42,7 +45,7 @@ def draw(cfg, with_dy=False):
     """bf16 host tensors of one workload (same values go to the GPU and, as fp64, to the oracle)."""
     h, F = cfg.hidden, cfg.ffn
     t = {k: synth.tensor_torch(k, s, (F if k == "Wd" else h) ** -0.5, "bf16", 0, "cpu")
-         for k, s in SHAPES(h, F).items()}
+         for k, s in SHAPES(h, F, cfg.kv_hidden).items()}
     t["x"] = synth.tensor_torch("x", (cfg.batch, cfg.seq, h), 1.0, "bf16", 0, "cpu")
     if with_dy:
         t["dY"] = synth.tensor_torch("dY", (cfg.batch, cfg.seq, h), 1.0, "bf16", 0, "cpu")
@@ -64,7 +67,7 @@ def gpu_forward(tsp, cfg, t, D=None):
     import torch
 
     D = D or cfg.D
-    plan = tsp.tsp_plan_create(D, cfg.seq, cfg.hidden, cfg.heads, cfg.head_dim, cfg.ffn, "bf16")
+    plan = tsp.plan_for(cfg.with_(D=D))
     canon = {k: t[k].cuda() for k in tsp.CANONICAL}
     packed = tsp.empty_packed(plan)
     tsp.tsp_pack_weights(plan, canon, packed)
@@ -83,7 +86,7 @@ def gpu_forward(tsp, cfg, t, D=None):
     return y, az
 
 
-@pytest.mark.parametrize("cfg", [LAYER_7B_S16K, LAYER_7B_S64K], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [LAYER_7B_S16K, LAYER_7B_S64K, LAYER_7B_GQA8_S16K], ids=lambda c: c.name)
 def test_full_size_sampled_rows(tsp, cfg):
     t = draw(cfg)
     y, a = gpu_forward(tsp, cfg, t)
@@ -113,13 +116,13 @@ def test_full_size_cross_D(tsp):
         assert rel_frob(to_np(yD), ref) <= 2e-2, D
 
 
-def test_training_workload_backward(tsp):
+@pytest.mark.parametrize("cfg", [TRAIN_7B_S8K, TRAIN_7B_GQA8_S8K], ids=lambda c: c.name)
+def test_training_workload_backward(tsp, cfg):
     import torch
 
-    cfg = TRAIN_7B_S8K
     t = draw(cfg, with_dy=True)
     B = cfg.batch
-    plan = tsp.tsp_plan_create(cfg.D, cfg.seq, cfg.hidden, cfg.heads, cfg.head_dim, cfg.ffn, "bf16")
+    plan = tsp.plan_for(cfg)
     canon = {k: t[k].cuda() for k in tsp.CANONICAL}
     packed = tsp.empty_packed(plan)
     tsp.tsp_pack_weights(plan, canon, packed)
@@ -135,17 +138,17 @@ def test_training_workload_backward(tsp):
     tsp.tsp_sync_check()
     w = {k: t[k].double().numpy() for k in tsp.CANONICAL}
     rdx, rg, ry = O.layer_bwd(t["x"].double().numpy(), w, cfg.heads, t["dY"].double().numpy(), return_y=True)
-    check(to_np(y), ry, "bf16", "Y")
-    check(to_np(dx), rdx, "bf16", "dx")
+    check(to_np(y), ry, "bf16", f"{cfg.name} Y")
+    check(to_np(dx), rdx, "bf16", f"{cfg.name} dx")
     for k in tsp.CANONICAL:
-        check(to_np(g[k]), rg[k], "bf16", f"d{k}")
+        check(to_np(g[k]), rg[k], "bf16", f"{cfg.name} d{k}")
 
 
 def gpu_backward(tsp, cfg, t, D):
     import torch
 
     B = cfg.batch
-    plan = tsp.tsp_plan_create(D, cfg.seq, cfg.hidden, cfg.heads, cfg.head_dim, cfg.ffn, "bf16")
+    plan = tsp.plan_for(cfg.with_(D=D))
     canon = {k: t[k].cuda() for k in tsp.CANONICAL}
     packed = tsp.empty_packed(plan)
     tsp.tsp_pack_weights(plan, canon, packed)
