@@ -75,11 +75,13 @@ def step_work(cfg):
     B, S, h, F, H, dh = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
     T = B * S
     e = 2 if cfg.dtype == "bf16" else 4
+    hk = cfg.kv_hidden       # K/V width (h unless grouped-query attention)
+    W3 = h + 2 * hk          # packed Q|K|V width
     attn = 4 * B * H * dh * S * (S + 1) // 2
     w = {
         "zigzag permute": (0, 2 * T * h * e, 1),
-        "QKV projection": (2 * T * h * 3 * h, (T * h + 3 * h * h + 3 * T * h) * e, 1),
-        "attention": (attn, 4 * T * h * e, 1),
+        "QKV projection": (2 * T * h * W3, (T * h + W3 * h + T * W3) * e, 1),
+        "attention": (attn, (2 * T * h + 2 * T * hk) * e, 1),
         "output projection": (2 * T * h * h, (3 * T * h + h * h) * e, 1),
         "gate/up projection": (2 * T * h * 2 * F, (T * h + 2 * F * h + T * F) * e, 1),
         "down projection": (2 * T * F * h, (T * F + F * h + 2 * T * h) * e, 1),
@@ -94,14 +96,14 @@ def step_work(cfg):
             "dW_gate_up": (2 * 2 * F * h * T, (2 * T * F + T * h + 2 * F * h) * e, 1),
             "dO": (2 * T * h * h, (2 * T * h + h * h) * e, 1),
             "dW_O": (2 * h * h * T, (2 * T * h + h * h) * e, 1),
-            "transpose V^T": (0, 2 * T * h * e, 1),
-            "attention bwd": (2 * attn, 7 * T * h * e, 3),
+            "transpose V^T": (0, 2 * T * hk * e, 1),
+            "attention bwd": (2 * attn, (4 * T * h + 4 * T * hk) * e, 3),
             "attention bwd dsum": (0, 2 * T * h * e, 1),
-            "attention bwd dK/dV": (attn, 6 * T * h * e, 1),
-            "attention bwd dQ": (attn // 2, 5 * T * h * e, 1),
-            "assemble dQKV": (0, 6 * T * h * e, 1),
-            "dx": (2 * T * 3 * h * h, (3 * T * h + 3 * h * h + 2 * T * h) * e, 1),
-            "dW_QKV": (2 * 3 * h * h * T, (3 * T * h + T * h + 3 * h * h) * e, 1),
+            "attention bwd dK/dV": (attn, (2 * T * h + 4 * T * hk) * e, 1),
+            "attention bwd dQ": (attn // 2, (3 * T * h + 2 * T * hk) * e, 1),
+            "assemble dQKV": (0, 2 * T * W3 * e, 1),
+            "dx": (2 * T * W3 * h, (T * W3 + W3 * h + 2 * T * h) * e, 1),
+            "dW_QKV": (2 * W3 * h * T, (T * W3 + T * h + W3 * h) * e, 1),
             "unpermute dx": (0, 2 * T * h * e, 1),
         })
     return w
