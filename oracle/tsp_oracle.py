@@ -34,6 +34,10 @@ What it computes (plain definitions, fp64, numpy):
   XW = X1W1 + X2W2, r007 chapter, section "Тензорный параллелизм").
 * Causal key-visit counts per rank and the forward communication-volume model
   behind the break-even B*S > 8h ("The Practicality of Trade-offs").
+* A decode step against a key/value cache (``decode_step``) and its
+  attention computed the TSP way over a cache sharded by the zigzag rule,
+  with per-rank partial softmax results merged by log-sum-exp
+  (``decode_attention_by_rank``).
 * Grouped-query attention: K and V may have fewer heads than Q (Wk, Wv of
   shape [h, Hk*dh]); the r007 chapter names GQA, with the K/V head count
   often cut to 8, as what bounds a head-split degree ("Параллелизм по
@@ -355,6 +359,76 @@ def tsp_layer_fwd_sharded(x, w, heads: int, D: int):
         "MLP": zigzag_unpermute(MLPz, D),
         "Y": zigzag_unpermute(Yz, D),
     }
+
+
+# ---------------------------------------------------------------------------
+# Decoding (one new token per sequence against a key/value cache)
+# ---------------------------------------------------------------------------
+
+def decode_step(x_new, w, heads: int, K_cache, V_cache, pos: int):
+    """One decode step of the layer, fp64.
+
+    The posts present TSP for inference as well as training ("for both
+    training and inference workloads", ai-trends.today TSP article,
+    introduction; the 7B model is "a reference for decoding", "Memory and
+    Processing Results").  Plainest reading of a decode step: each of the B
+    sequences holds ``pos`` cached tokens (positions 0..pos-1) and appends the
+    token x_new at position ``pos``; that token attends to every cached key
+    and to itself (all are at earlier or equal positions).
+
+    x_new: [B, h]; K_cache, V_cache: [B, >= pos, hk] (row p = key/value of
+    position p, hk = Hk*dh); only rows < pos are read.  Returns
+    (Y [B, h], k_new [B, hk], v_new [B, hk]).
+    """
+    B, h = x_new.shape
+    dh = h // heads
+    q, k, v = x_new @ w["Wq"], x_new @ w["Wk"], x_new @ w["Wv"]
+    Y = np.zeros((B, h))
+    for b in range(B):
+        K = np.concatenate([K_cache[b, :pos], k[b:b + 1]], axis=0)
+        V = np.concatenate([V_cache[b, :pos], v[b:b + 1]], axis=0)
+        Q = np.zeros((pos + 1, h))
+        Q[pos] = q[b]
+        O, _ = causal_attention(Q, K, V, heads, rows=[pos])
+        Hb = x_new[b] + O[0] @ w["Wo"]
+        Y[b] = Hb + gated_mlp(Hb[None, :], w)[0]
+    return Y, k, v
+
+
+def decode_attention_by_rank(q, K, V, heads: int, pos: int, D: int):
+    """Attention of one new query (position pos) the TSP way: the cache of
+    2D*C positions is sharded over D ranks by the zigzag rule (rank r holds
+    chunks r and 2D-1-r); every rank computes, per head, the running max m_r,
+    the sum l_r of exp(score - m_r) and the unnormalised output O_r over its
+    own cached keys with position <= pos; the partial results are merged with
+    the log-sum-exp rule m = max m_r, l = sum l_r e^(m_r - m),
+    O = sum O_r e^(m_r - m) / l (the combination FlashAttention's online
+    softmax uses; r007 chapter, "Параллелизм по контексту: Ring Attention
+    против Ulysses").  q: [h]; K, V: [S, hk] with S = 2DC.  Returns O [h].
+    """
+    S, _ = K.shape
+    h = q.shape[0]
+    dh = h // heads
+    kv_heads = K.shape[1] // dh
+    pos_of = zigzag_positions(S, D)
+    scale = 1.0 / math.sqrt(dh)
+    out = np.zeros(h)
+    for e in range(heads):
+        sl = slice(e * dh, (e + 1) * dh)
+        kv = kv_head_slice(e, heads, kv_heads, dh)
+        parts = []
+        for r in range(D):
+            keys = pos_of[r][pos_of[r] <= pos]
+            if len(keys) == 0:
+                continue
+            s = (K[keys, kv] @ q[sl]) * scale
+            m = s.max()
+            p = np.exp(s - m)
+            parts.append((m, p.sum(), p @ V[keys, kv]))
+        m = max(pm for pm, _, _ in parts)
+        l = sum(pl * math.exp(pm - m) for pm, pl, _ in parts)
+        out[sl] = sum(po * math.exp(pm - m) for pm, _, po in parts) / l
+    return out
 
 
 # ---------------------------------------------------------------------------
