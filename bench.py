@@ -87,6 +87,15 @@ def step_work(cfg):
         "down projection": (2 * T * F * h, (T * F + F * h + 2 * T * h) * e, 1),
         "zigzag unpermute": (0, 2 * T * h * e, 1),
     }
+    if cfg.decode:
+        # one token per sequence: every projection streams its weight, attention streams the cache
+        return {
+            "decode QKV projection": (0, (h * W3 + B * h + B * W3) * e, 1),
+            "decode attention": (0, (2 * B * S * hk + 2 * B * h) * e, 2),
+            "decode output projection": (0, (h * h + 3 * B * h) * e, 1),
+            "decode gate/up projection": (0, (2 * F * h + B * h + B * F) * e, 1),
+            "decode down projection": (0, (h * F + B * F + 2 * B * h) * e, 1),
+        }
     if cfg.backward:
         w.update({
             "permute dy": (0, 2 * T * h * e, 1),
@@ -161,8 +170,13 @@ class ClockSampler:
 
 
 def sample_flops(cfg, prefix: int) -> int:
-    h, F, H, dh = cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
-    return prefix * (8 * h * h + 6 * h * F) + 4 * H * dh * prefix * (prefix + 1) // 2
+    """Algorithmic flops of the oracle's sample: the causal prefix of `prefix`
+    positions of one sequence, or for a decode workload one decode step of one
+    sequence (`prefix` unused)."""
+    h, F, H, dh, hk = cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim, cfg.kv_hidden
+    if cfg.decode:
+        return cfg.with_(batch=1).decode_flops()
+    return prefix * 2 * (h * (h + 2 * hk) + h * h + 3 * h * F) + 4 * H * dh * prefix * (prefix + 1) // 2
 
 
 def run_oracle_sample(cfg, prefix: int, repeats: int, timeout: float = 1800.0):
@@ -182,17 +196,29 @@ from folded_tensor_sequence_gb300 import synth
 from folded_tensor_sequence_gb300.configs import BY_NAME
 from oracle import tsp_oracle as O
 cfg = BY_NAME[{cfg.name!r}]
-h, F, P = cfg.hidden, cfg.ffn, {prefix}
-shapes = {{"Wq": (h, h), "Wk": (h, h), "Wv": (h, h), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}}
+h, F, P, hk = cfg.hidden, cfg.ffn, {prefix}, cfg.kv_hidden
+shapes = {{"Wq": (h, h), "Wk": (h, hk), "Wv": (h, hk), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}}
 w = {{k: synth.tensor_torch(k, s, (F if k == "Wd" else h) ** -0.5, cfg.dtype, 0, "cpu").double().numpy()
       for k, s in shapes.items()}}
-x = synth.tensor_torch("x", (1, P, h), 1.0, cfg.dtype, 0, "cpu").double().numpy()
 secs = []
-for _ in range({repeats}):
-    t0 = time.perf_counter()
-    out = O.layer_fwd(x, w, cfg.heads)
-    secs.append(time.perf_counter() - t0)
-    assert np.isfinite(out["Y"]).all()
+if cfg.decode:
+    # one decode step of sequence 0 at position seq-1 against a seeded N(0,1) cache
+    gen = torch.Generator().manual_seed(0)
+    kc = torch.randn(1, cfg.seq, hk, generator=gen).to(torch.bfloat16).float().numpy()
+    vc = torch.randn(1, cfg.seq, hk, generator=gen).to(torch.bfloat16).float().numpy()
+    x = synth.tensor_torch("x", (1, h), 1.0, cfg.dtype, 0, "cpu").double().numpy()
+    for _ in range({repeats}):
+        t0 = time.perf_counter()
+        y, _, _ = O.decode_step(x, w, cfg.heads, kc, vc, cfg.seq - 1)
+        secs.append(time.perf_counter() - t0)
+        assert np.isfinite(y).all()
+else:
+    x = synth.tensor_torch("x", (1, P, h), 1.0, cfg.dtype, 0, "cpu").double().numpy()
+    for _ in range({repeats}):
+        t0 = time.perf_counter()
+        out = O.layer_fwd(x, w, cfg.heads)
+        secs.append(time.perf_counter() - t0)
+        assert np.isfinite(out["Y"]).all()
 print(json.dumps({{"seconds": secs}}))
 """
     try:
@@ -210,9 +236,10 @@ def cpu_baseline(cfg, prefix: int):
         return None, err
     fl = sample_flops(cfg, prefix)
     return {"value": round(fl / secs[0] / 1e12, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, 1 thread, positions 0..{prefix - 1} of batch 0 "
-                      f"({fl / 1e9:.1f} GFLOP algorithmic, {secs[0]:.1f} s)",
-            "tokens_per_s": round(prefix / secs[0], 2)}, None
+            "sample": (f"fp64 numpy oracle, 1 thread, one decode step of sequence 0 at position {cfg.seq - 1} "
+                       if cfg.decode else f"fp64 numpy oracle, 1 thread, positions 0..{prefix - 1} of batch 0 ")
+                      + f"({fl / 1e9:.1f} GFLOP algorithmic, {secs[0]:.1f} s)",
+            "tokens_per_s": round((1 if cfg.decode else prefix) / secs[0], 2)}, None
 
 
 def dist_env():
@@ -239,9 +266,12 @@ def run_reference(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "D": cfg.D, "batch": cfg.batch, "seq": cfg.seq, "hidden": cfg.hidden,
                    "heads": cfg.heads, "head_dim": cfg.head_dim, "ffn": cfg.ffn,
-                   "sample": f"each step: positions 0..{prefix - 1} of batch 0 (causal prefix, exact slice)"},
+                   "sample": (f"each step: one decode step of sequence 0 at position {cfg.seq - 1}" if cfg.decode
+                              else f"each step: positions 0..{prefix - 1} of batch 0 (causal prefix, exact slice)")},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"fp64 numpy oracle, 1 thread, causal prefix of {prefix} tokens per step"},
+                         "sample": (f"fp64 numpy oracle, 1 thread, one decode step of sequence 0 per step"
+                                    if cfg.decode else
+                                    f"fp64 numpy oracle, 1 thread, causal prefix of {prefix} tokens per step")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -289,18 +319,32 @@ def main():
     g.build()
     from folded_tensor_sequence_gb300 import synth, tsp
 
-    B, S, h, F = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn
-    plan = tsp.tsp_plan_create(cfg.D, S, h, cfg.heads, cfg.head_dim, F, cfg.dtype)
-    shapes = {"Wq": (h, h), "Wk": (h, h), "Wv": (h, h), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}
+    B, S, h, F, hk = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn, cfg.kv_hidden
+    plan = tsp.plan_for(cfg)
+    shapes = {"Wq": (h, h), "Wk": (h, hk), "Wv": (h, hk), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}
     canon = {k: synth.tensor_torch(k, s, (F if k == "Wd" else h) ** -0.5, cfg.dtype, 0, dev) for k, s in shapes.items()}
     packed = tsp.empty_packed(plan, dev)
     tsp.tsp_pack_weights(plan, canon, packed)
     del canon
-    x = synth.tensor_torch("x", (B, S, h), 1.0, cfg.dtype, 0, dev)
-    y = torch.empty_like(x)
-    work = tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD, dev)
     stream = torch.cuda.current_stream(dev)
-    if cfg.backward:
+    if cfg.decode:
+        # one decode step per sequence at the last position of a full cache (seeded N(0,1) contents)
+        gen = torch.Generator(device=dev).manual_seed(0)
+        kc = torch.randn(B, cfg.kv_h, S, cfg.head_dim, generator=gen, device=dev).to(torch.bfloat16)
+        vc = torch.randn(B, cfg.kv_h, S, cfg.head_dim, generator=gen, device=dev).to(torch.bfloat16)
+        x = synth.tensor_torch("x", (B, h), 1.0, cfg.dtype, 0, dev)
+        y = torch.empty_like(x)
+        dwork = tsp.workspace(plan, B, tsp.TSP_OP_DECODE, dev)
+
+        def step():
+            tsp.tsp_decode_step(plan, B, S - 1, x, packed, kc, vc, y, dwork, stream)
+    else:
+        x = synth.tensor_torch("x", (B, S, h), 1.0, cfg.dtype, 0, dev)
+        y = torch.empty_like(x)
+        work = tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD, dev)
+    if cfg.decode:
+        pass
+    elif cfg.backward:
         # training step (no optimizer): forward keeping activations, then the full backward
         dy = synth.tensor_torch("dY", (B, S, h), 1.0, cfg.dtype, 0, dev)
         dx = torch.empty_like(x)
@@ -339,10 +383,12 @@ def main():
     tsp.tsp_sync_check(stream)
     ms = max_over_ranks(ms, dev)
     clocks = clk.summary()
-    flops = cfg.fwd_flops() * (3 if cfg.backward else 1)  # training step: model flops = 3x forward
+    # training step: model flops = 3x forward; decode: the step's projections and attention
+    flops = cfg.decode_flops() if cfg.decode else cfg.fwd_flops() * (3 if cfg.backward else 1)
+    tokens_per_step = B if cfg.decode else B * S
     ms_step = ms / args.steps
     value = whole_job_rate(ws, flops, args.steps, ms) / 1e12
-    tokens_s = whole_job_rate(ws, B * S, args.steps, ms)
+    tokens_s = whole_job_rate(ws, tokens_per_step, args.steps, ms)
 
     # ---- per-kernel timing (same stream, separate pass) ---------------------
     tsp.tsp_profile_enable(True)
@@ -379,8 +425,8 @@ def main():
                 "frac": round(ach / peak, 4), "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
 
     # ---- end to end through the API with host buffers -----------------------
-    ins = [x, dy] if cfg.backward else [x]          # per-step inputs copied in
-    out = dx if cfg.backward else y                   # per-step result copied out
+    ins = [x, dy] if cfg.backward and not cfg.decode else [x]  # per-step inputs copied in
+    out = dx if cfg.backward and not cfg.decode else y          # per-step result copied out
     ins_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
     for th, t in zip(ins_host, ins):
         th.copy_(t)
@@ -400,7 +446,7 @@ def main():
     e2e = {"value": round(whole_job_rate(ws, flops, args.steps, ems) / 1e12, 2), "unit": UNIT,
            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in ins),
            "d2h_bytes_per_step": out.numel() * out.element_size(),
-           "tokens_per_s": round(whole_job_rate(ws, B * S, args.steps, ems), 1)}
+           "tokens_per_s": round(whole_job_rate(ws, tokens_per_step, args.steps, ems), 1)}
 
     if rank == 0:
         line = {
@@ -412,9 +458,13 @@ def main():
                             "sustained": round(value / ws / peaks["bf16_tflops_sustained"], 4),
                             "source": peak_src},
             "config": {"workload": cfg.name, "D": cfg.D, "batch": B, "seq": S, "hidden": h, "heads": cfg.heads,
-                       "head_dim": cfg.head_dim, "ffn": F, "parallelism": f"replicas x{ws}" if ws > 1 else "single",
-                       "l2": "inputs larger than L2 (x %d MB, packed weights %d MB)" % (
-                           x.numel() * x.element_size() >> 20,
+                       "kv_heads": cfg.kv_h, "head_dim": cfg.head_dim, "ffn": F,
+                       "step": ("decode: one token per sequence at position seq-1 of a full K/V cache"
+                                if cfg.decode else ("layer forward + backward" if cfg.backward else "layer forward")),
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single",
+                       "l2": "inputs larger than L2 (%s %d MB, packed weights %d MB)" % (
+                           "K/V cache" if cfg.decode else "x",
+                           (2 * kc.numel() * kc.element_size() if cfg.decode else x.numel() * x.element_size()) >> 20,
                            sum(t.numel() * t.element_size() for t in (packed.qkv, packed.o, packed.gate_up,
                                                                         packed.down)) >> 20)},
             "roofline": roof,

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtsp.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
-SOURCES = ["api.cu", "layout.cu", "gemm_simt.cu", "gemm_tc.cu", "attn_fwd.cu", "attn_fwd_tc.cu", "attn_bwd.cu", "attn_bwd_tc.cu", "attn_static.cu"]
+SOURCES = ["api.cu", "layout.cu", "gemm_simt.cu", "gemm_tc.cu", "attn_fwd.cu", "attn_fwd_tc.cu", "attn_bwd.cu", "attn_bwd_tc.cu", "attn_static.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

@@ -234,6 +234,8 @@ struct Prof {
   }
 };
 
+thread_local std::vector<Prof*> t_prof_stack;
+
 // ---- the layer pieces ------------------------------------------------------
 
 EpiParams base_epi(const tsp_plan* p, int batch) {
@@ -350,6 +352,14 @@ tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weig
 
 tsp_status report_error(tsp_status s, const char* msg) { return fail(s, "%s", msg); }
 
+void prof_begin(const char* name, cudaStream_t st) { t_prof_stack.push_back(new Prof(name, st)); }
+
+void prof_end(cudaStream_t) {
+  if (t_prof_stack.empty()) return;
+  delete t_prof_stack.back();  // records the closing event
+  t_prof_stack.pop_back();
+}
+
 unsigned int* dev_error_word() {
   static unsigned int* ptrs[64] = {};
   int dev = 0;
@@ -449,6 +459,7 @@ size_t tsp_workspace_bytes(const tsp_plan* p, int batch, tsp_op op) {
     case TSP_OP_GATED_MLP_FWD: return mlp_ws_bytes(p, batch);
     case TSP_OP_LAYER_FWD: return layer_layout(p, batch).fwd_end;
     case TSP_OP_LAYER_BWD: return bwd_layout(p, batch).end;
+    case TSP_OP_DECODE: return decode_ws_bytes(p, batch);
   }
   return 0;
 }
@@ -776,6 +787,30 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   Prof pr_dx("unpermute dx", st);
   return cuda_status(launch_zigzag_rows(wb + L.dxz, dx, h * eb, p->D, batch, p->seq, false, st), "unpermute dx");
 #undef TSP_TRY
+}
+
+tsp_status tsp_decode_step(const tsp_plan* p, int batch, int64_t pos, const void* x_new, const tsp_weights* w,
+                           void* k_cache, void* v_cache, void* y_new, void* ws, size_t ws_bytes, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if (!p) return fail(TSP_ERR_INVALID_ARG, "plan is NULL");
+  if (batch < 1 || batch > 8) return fail(TSP_ERR_INVALID_ARG, "decode batch %d not in [1, 8]", batch);
+  if (pos < 0 || pos >= p->seq)
+    return fail(TSP_ERR_INVALID_ARG, "pos %lld not in [0, seq = %lld)", (long long)pos, (long long)p->seq);
+  if (!w) return fail(TSP_ERR_INVALID_ARG, "weights is NULL");
+  if ((s = check_ptrs({x_new, k_cache, v_cache, y_new, w->qkv, w->o, w->gate_up, w->down, ws}, "tsp_decode_step")) !=
+      TSP_OK)
+    return s;
+  if (p->dtype != TSP_BF16) return fail(TSP_ERR_UNSUPPORTED, "decode is implemented for bf16 plans");
+  if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
+  const int g = p->heads / p->kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return fail(TSP_ERR_UNSUPPORTED, "decode needs heads / kv_heads in {1, 2, 4, 8} (got %d)", g);
+  if (ws_bytes < decode_ws_bytes(p, batch))
+    return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, decode_ws_bytes(p, batch));
+  s = decode_step_bf16(p, batch, pos, x_new, w, k_cache, v_cache, y_new, ws, as_stream(stream));
+  if (s != TSP_OK) return fail(s, "decode step failed: %s", tsp_status_string(s));
+  return TSP_OK;
 }
 
 tsp_status tsp_debug_wait_timeout(unsigned int timeout_us, void* stream) {

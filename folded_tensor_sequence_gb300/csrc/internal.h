@@ -147,4 +147,15 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
 cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
                                  int64_t S, int H, int Hk, int dh, cudaStream_t stream);
 
+// Decode step (bf16; batch 1..8; head_dim 128; H / Hk in {1, 2, 4, 8}).
+size_t decode_ws_bytes(const tsp_plan* p, int batch);
+int decode_split(int D, int Hk, int B, int64_t C);
+tsp_status decode_step_bf16(const tsp_plan* p, int batch, int64_t pos, const void* x_new, const tsp_weights* w,
+                            void* k_cache, void* v_cache, void* y_new, void* ws, cudaStream_t st);
+
+// Optional per-step timing (tsp_profile_*): CUDA events around enqueued work,
+// summed per name.  No-ops unless profiling is enabled; calls nest like braces.
+void prof_begin(const char* name, cudaStream_t st);
+void prof_end(cudaStream_t st);
+
 }  // namespace tsp

@@ -18,14 +18,14 @@ from . import build as _build
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT, TSP_ERR_WORKSPACE = range(6)
 TSP_F32, TSP_BF16 = 0, 1
-TSP_OP_ATTENTION_FWD, TSP_OP_GATED_MLP_FWD, TSP_OP_LAYER_FWD, TSP_OP_LAYER_BWD = range(4)
+TSP_OP_ATTENTION_FWD, TSP_OP_GATED_MLP_FWD, TSP_OP_LAYER_FWD, TSP_OP_LAYER_BWD, TSP_OP_DECODE = range(5)
 
 EXPORTS = [
     "tsp_plan_create", "tsp_plan_destroy", "tsp_workspace_bytes", "tsp_saved_bytes", "tsp_status_string",
     "tsp_last_error_message", "tsp_pack_weights", "tsp_unpack_weights", "tsp_zigzag_permute",
     "tsp_zigzag_unpermute", "tsp_kv_gather", "tsp_attention_fwd", "tsp_gated_mlp_fwd", "tsp_layer_fwd",
     "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next", "tsp_profile_enable", "tsp_profile_report",
-    "tsp_attention_fwd_static", "tsp_debug_wait_timeout", "tsp_plan_create_gqa",
+    "tsp_attention_fwd_static", "tsp_debug_wait_timeout", "tsp_plan_create_gqa", "tsp_decode_step",
 ]
 
 
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.tsp_layer_fwd.argtypes = [vp, i32, vp, ctypes.POINTER(_Weights), vp, vp, vp, sz, vp]
         L.tsp_layer_bwd.argtypes = [vp, i32, vp, ctypes.POINTER(_Weights), vp, vp, vp, ctypes.POINTER(_Weights), vp,
                                     sz, vp]
+        L.tsp_decode_step.argtypes = [vp, i32, i64, vp, ctypes.POINTER(_Weights), vp, vp, vp, vp, sz, vp]
         L.tsp_sync_check.argtypes = [vp]
         L.tsp_debug_fail_next.argtypes = [i32, i32]
         L.tsp_debug_fail_next.restype = None
@@ -302,6 +303,14 @@ def tsp_layer_bwd(plan: Plan, batch: int, x, weights: PackedWeights, saved, dy, 
     wp, wn = _ws_args(workspace)
     _check(lib().tsp_layer_bwd(plan.handle, batch, _ptr(x), ctypes.byref(w), _ptr(saved), _ptr(dy), _ptr(dx),
                                ctypes.byref(g), wp, wn, _stream(stream)), "tsp_layer_bwd")
+
+
+def tsp_decode_step(plan: Plan, batch: int, pos: int, x_new, weights: PackedWeights, k_cache, v_cache, y_new,
+                    workspace, stream=None):
+    w = weights.c()
+    wp, wn = _ws_args(workspace)
+    _check(lib().tsp_decode_step(plan.handle, batch, pos, _ptr(x_new), ctypes.byref(w), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(y_new), wp, wn, _stream(stream)), "tsp_decode_step")
 
 
 def workspace(plan: Plan, batch: int, op: int, device="cuda") -> torch.Tensor:

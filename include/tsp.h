@@ -93,7 +93,8 @@ typedef enum {
   TSP_OP_ATTENTION_FWD = 0,
   TSP_OP_GATED_MLP_FWD = 1,
   TSP_OP_LAYER_FWD = 2,
-  TSP_OP_LAYER_BWD = 3
+  TSP_OP_LAYER_BWD = 3,
+  TSP_OP_DECODE = 4
 } tsp_op;
 
 /* Opaque, host-only, immutable after creation; safe to share between threads. */
@@ -190,6 +191,27 @@ tsp_status tsp_layer_fwd(const tsp_plan* plan, int batch, const void* x, const t
 tsp_status tsp_layer_bwd(const tsp_plan* plan, int batch, const void* x, const tsp_weights* weights,
                          const void* saved, const void* dy, void* dx, const tsp_weight_grads* dw,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- decoding ---------------------------------------------------------------- */
+
+/* One decode step: each of `batch` sequences (1..8) holds `pos` cached tokens
+ * (positions 0..pos-1) and appends x_new[b] at position `pos` (0 <= pos <
+ * seq; the plan's seq is the cache capacity).  The step writes the new
+ * token's key and value into row `pos` of the caches and y_new[b] = the
+ * layer's output for that token, which attends to positions 0..pos.
+ *   x_new, y_new      [batch][h] bf16
+ *   k_cache, v_cache  [batch][kv_heads][seq][head_dim] bf16, natural positions;
+ *                     rows >= pos are not read (row pos is overwritten)
+ * TSP reading (ai-trends.today TSP article: the scheme serves inference as
+ * well as training): the cache is sharded over the D virtual ranks by the
+ * zigzag rule, each rank computes a partial softmax of the new query over
+ * its own cached positions, and the partials are merged by log-sum-exp; the
+ * projections stream every packed weight shard once.  bf16 plans only,
+ * head_dim 128, heads / kv_heads in {1, 2, 4, 8} (else TSP_ERR_UNSUPPORTED);
+ * workspace: tsp_workspace_bytes(plan, batch, TSP_OP_DECODE). */
+tsp_status tsp_decode_step(const tsp_plan* plan, int batch, int64_t pos, const void* x_new,
+                           const tsp_weights* weights, void* k_cache, void* v_cache, void* y_new,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- status ---------------------------------------------------------------- */
 

@@ -382,15 +382,21 @@ def decode_step(x_new, w, heads: int, K_cache, V_cache, pos: int):
     """
     B, h = x_new.shape
     dh = h // heads
+    kv_heads = w["Wk"].shape[1] // dh
+    scale = 1.0 / math.sqrt(dh)
     q, k, v = x_new @ w["Wq"], x_new @ w["Wk"], x_new @ w["Wv"]
     Y = np.zeros((B, h))
     for b in range(B):
-        K = np.concatenate([K_cache[b, :pos], k[b:b + 1]], axis=0)
-        V = np.concatenate([V_cache[b, :pos], v[b:b + 1]], axis=0)
-        Q = np.zeros((pos + 1, h))
-        Q[pos] = q[b]
-        O, _ = causal_attention(Q, K, V, heads, rows=[pos])
-        Hb = x_new[b] + O[0] @ w["Wo"]
+        O = np.zeros(h)
+        for e in range(heads):
+            sl = slice(e * dh, (e + 1) * dh)
+            kv = kv_head_slice(e, heads, kv_heads, dh)
+            # scores against the cached positions 0..pos-1 and the new token itself
+            s = np.append(K_cache[b, :pos, kv] @ q[b, sl], k[b, kv] @ q[b, sl]) * scale
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            O[sl] = p[:pos] @ V_cache[b, :pos, kv] + p[pos] * v[b, kv]
+        Hb = x_new[b] + O @ w["Wo"]
         Y[b] = Hb + gated_mlp(Hb[None, :], w)[0]
     return Y, k, v
 
