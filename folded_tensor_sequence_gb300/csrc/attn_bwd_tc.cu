@@ -383,6 +383,350 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ===========================================================================
+// dK, dV with 128-query blocks
+// ===========================================================================
+// Every MMA is 128 x 128 x 16 (full rate) and a block needs 32 of them for
+// 128 queries, against 48 for two 64-query blocks; the hand-offs per query
+// halve.  TMEM holds S^T, dP^T (128 columns each, single-buffered), dV and
+// dK.  The elementwise warps work in two phases per block -- P^T (feeds
+// dV += P^T dO) and then dS^T (feeds dK += dS^T Q) -- and the MMA order
+//   S(n), dP(n), [P(n)] dV(n), S(n+1), [dS(n)] dK(n), dP(n+1), ...
+// keeps the tensor core on the next block's scores while they work.
+constexpr int QB2 = 128;
+constexpr int QSTG2 = 2;
+constexpr uint32_t STG2_DATA = 4 * SUB128;            // Q (2 sub-tiles [128][64]), dO (2)
+constexpr uint32_t STG2_BYTES = STG2_DATA + 1024;     // + lse, dsum of the block (512 B each)
+constexpr size_t DKDV2_SMEM = 1024 + 4 * (size_t)SUB128 + QSTG2 * (size_t)STG2_BYTES + 256;
+constexpr int kBarP2 = 5, kBarDS2 = 6;                 // P and dS hand-offs (256 + 32 threads)
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_dkdv128_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                           const BwdTcParams p, int nk) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ks = smem;                    // 2 x SUB128
+  uint8_t* Vs = smem + 2 * SUB128;       // 2 x SUB128
+  uint8_t* stg = smem + 4 * SUB128;      // [QSTG2] stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + QSTG2 * STG2_BYTES);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_free = bars + 1;
+  uint64_t* q_full = bars + 2;   // [QSTG2]
+  uint64_t* q_free = bars + 4;   // [QSTG2]
+  uint64_t* s_full = bars + 6;   // S^T of the current block is in TMEM
+  uint64_t* dp_full = bars + 7;  // dP^T of the current block is in TMEM
+  uint64_t* o_done = bars + 8;
+  uint64_t* drain = bars + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // blockIdx.y is a K/V head; the `grp` query heads that read it stream through
+  // one after another (their dK, dV contributions add up in tensor memory)
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int grp = p.H / p.Hk;
+  const int64_t bkv = (int64_t)b * p.Hk + kvh;
+  auto tile_of = [&](int t) { return t == 0 ? (int)blockIdx.x : nk - 1 - (int)blockIdx.x; };
+  const int ntile = (nk - 1 - (int)blockIdx.x == (int)blockIdx.x) ? 1 : 2;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_free, 1);
+    for (int s = 0; s < QSTG2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_free[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmdO);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // TMEM columns: S^T at 0, dP^T at 128, dV at 256, dK at 384.  P^T (bf16
+  // pairs) goes over the first 32 columns of each 64-column half of S^T (the
+  // half whose scores the writing thread read), dS^T likewise over dP^T.
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t qi = 0;
+      int kv_armed = 0;
+      bool ok = true;
+      for (int t = 0; t < ntile && ok; ++t) {
+        const int64_t k0 = (int64_t)tile_of(t) * 128;
+        if (!mbar_wait(kv_free, (t & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 1)) break;
+        mbar_arrive_expect_tx(kv_full, 4 * SUB128);
+        ++kv_armed;
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(Ks + c * SUB128, &tmK, c * 64, (int)(bkv * p.S + k0), kv_full);
+          tma_load_2d(Vs + c * SUB128, &tmV, c * 64, (int)(bkv * p.S + k0), kv_full);
+        }
+        const int nq = (int)((p.S - k0) / QB2);
+        for (int u = 0; u < grp * nq; ++u, ++qi) {
+          const int i = u % nq;
+          const int head = kvh * grp + u / nq;
+          const int64_t bh = (int64_t)b * p.H + head;
+          const int s = qi % QSTG2;
+          if (!mbar_wait(&q_free[s], ((qi / QSTG2) & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 2)) {
+            ok = false;
+            break;
+          }
+          const int64_t q0 = k0 + (int64_t)i * QB2;
+          const int64_t zr = zz_row(q0, p.C, p.D, p.B, b);  // a 128-query block never crosses a chunk
+          uint8_t* st = stg + s * STG2_BYTES;
+          mbar_arrive_expect_tx(&q_full[s], STG2_DATA + 2 * QB2 * 4);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(st + c * SUB128, &tmQ, head * HD + c * 64, (int)zr, &q_full[s]);
+            tma_load_2d(st + 2 * SUB128 + c * SUB128, &tmdO, head * HD + c * 64, (int)zr, &q_full[s]);
+          }
+          bulk_load(st + STG2_DATA, p.lse + bh * p.S + q0, QB2 * 4, &q_full[s]);
+          bulk_load(st + STG2_DATA + QB2 * 4, p.dsum + bh * p.S + q0, QB2 * 4, &q_full[s]);
+        }
+      }
+      volatile int dummy = 0;
+      const uint32_t first = qi > QSTG2 ? qi - QSTG2 : 0;
+      for (uint32_t n = first; n < qi; ++n) mbar_wait(&q_full[n % QSTG2], (n / QSTG2) & 1, &dummy, p.err, CODE_DKDV | 3);
+      if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_DKDV | 3);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer (whole warp walks the schedule, lane 0 issues) ----------------
+    constexpr uint32_t id_s = idesc_bf16_f32(128, QB2);              // M = keys, N = queries
+    constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // M = keys, N = head dim (B MN-major)
+    uint32_t qi = 0;
+    bool ok = true;  // warp-uniform
+    auto stage = [&](uint32_t n) { return stg + (n % QSTG2) * STG2_BYTES; };
+    auto scores = [&](uint32_t n) {  // S^T = K Q^T
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB128)) + 2 * (k % 4);
+        umma_bf16(tmem_base, ak, bq, id_s, k > 0);
+      }
+      umma_commit(s_full);
+    };
+    auto dpscores = [&](uint32_t n) {  // dP^T = V dO^T
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB128 + (k / 4) * SUB128)) + 2 * (k % 4);
+        umma_bf16(tmem_base + 128, av, bo, id_s, k > 0);
+      }
+      umma_commit(dp_full);
+    };
+    // dV += P^T dO and dK += dS^T Q: the stage's dO / Q tiles as MN-major B
+    // operands (rows = queries = K dimension; 64-column chunks SUB128 apart)
+    auto accum_v = [&](uint32_t n, bool acc) {
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < QB2 / 16; ++k) {
+        const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB128) + 2048 * k, SUB128);
+        umma_bf16_ts(tmem_base + 256, tmem_base + 64 * (k / 4) + 8 * (k % 4), bo, id_o, (acc || k > 0) ? 1u : 0u);
+      }
+    };
+    auto accum_k = [&](uint32_t n, bool acc) {
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < QB2 / 16; ++k) {
+        const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB128);
+        umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * (k / 4) + 8 * (k % 4), bq, id_o,
+                     (acc || k > 0) ? 1u : 0u);
+      }
+      umma_commit(&q_free[n % QSTG2]);
+    };
+    auto sync_on = [&](int id, int count) {
+      __syncwarp();
+      named_bar_sync(id, count);
+      tc_fence_after();
+    };
+    for (int t = 0; t < ntile; ++t) {
+      const int64_t k0 = (int64_t)tile_of(t) * 128;
+      const int nq = grp * (int)((p.S - k0) / QB2);  // query blocks of all the group's heads
+      if (ok) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_DKDV | 4);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      }
+      sync_on(kBarStage + (qi & 3), kStageThreads);
+      if (ok && lane == 0) {
+        scores(qi);
+        dpscores(qi);
+      }
+      for (int i = 0; i < nq; ++i) {
+        const uint32_t n = qi + i;
+        sync_on(kBarP2, kDSThreads);  // P^T(n) in TMEM
+        if (ok && lane == 0) accum_v(n, i > 0);
+        if (i + 1 < nq) {
+          sync_on(kBarStage + ((n + 1) & 3), kStageThreads);
+          if (ok && lane == 0) scores(n + 1);
+        }
+        sync_on(kBarDS2, kDSThreads);  // dS^T(n) in TMEM
+        if (ok && lane == 0) {
+          accum_k(n, i > 0);
+          if (i + 1 < nq) dpscores(n + 1);
+        }
+      }
+      if (ok && lane == 0) {
+        umma_commit(o_done);
+        umma_commit(kv_free);
+      }
+      qi += nq;
+    }
+    if (lane == 0) {
+      umma_commit(drain);
+      volatile int dummy = 0;
+      mbar_wait(drain, 0, &dummy, p.err, CODE_DKDV | 7);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ---------------- relay: announces each landed stage to the MMA warp ----------------
+    uint32_t n = 0;
+    for (int t = 0; t < ntile; ++t) {
+      const int nq = grp * (int)((p.S - (int64_t)tile_of(t) * 128) / QB2);
+      for (int i = 0; i < nq; ++i, ++n) {
+        if (lane == 0) mbar_wait(&q_full[n % QSTG2], (n / QSTG2) & 1, abort_flag, p.err, CODE_DKDV | 9);
+        __syncwarp();
+        named_bar_sync(kBarStage + (n & 3), kStageThreads);
+      }
+    }
+  } else {
+    // ------- elementwise warps 0-7: one key row, 64 of the 128 query columns per thread -------
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = kLog2e * rsqrtf((float)HD);
+    const float scale = rsqrtf((float)HD);
+    uint32_t cnt = 0;  // blocks processed (phase of s_full / dp_full; stage = cnt % QSTG2)
+    bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
+    const uint32_t cS = tmem_base + lane_off + 64 * half;
+    const uint32_t cdP = tmem_base + lane_off + 128 + 64 * half;
+    for (int t = 0; t < ntile; ++t) {
+      const int64_t k0 = (int64_t)tile_of(t) * 128;
+      const int nqh = (int)((p.S - k0) / QB2);
+      const int64_t key = k0 + row;
+      for (int u = 0; u < grp * nqh; ++u, ++cnt) {
+        const int i = u % nqh;  // query block within the head
+        // ---- P phase ----
+        bool got = alive && mbar_wait(s_full, cnt & 1, abort_flag, p.err, CODE_DKDV | 8);
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) {
+          named_bar_sync(kBarP2, kDSThreads);
+          named_bar_sync(kBarDS2, kDSThreads);
+          continue;
+        }
+        tc_fence_after();
+        uint32_t sa[32], sb[32];
+        tmem_ld32_issue(cS, sa);
+        tmem_ld32_issue(cS + 32, sb);
+        const float4* lse4 = reinterpret_cast<const float4*>(stg + (cnt % QSTG2) * STG2_BYTES + STG2_DATA) + 16 * half;
+        const float4* ds4 = lse4 + QB2 / 4;
+        const int64_t q0 = k0 + (int64_t)i * QB2 + 64 * half;  // query of this thread's first column
+        const bool diag = i == 0;
+        float pv[64];
+        tmem_wait_ld32(sa);
+        tmem_wait_ld32(sb);
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = lse4[c4];
+          const float lv[4] = {l4.x * kLog2e, l4.y * kLog2e, l4.z * kLog2e, l4.w * kLog2e};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 * 4 + e;
+            const float sc = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]);
+            float pe = ex2f(fmaf(sc, sl2, -lv[e]));
+            if (diag && q0 + c < key) pe = 0.f;
+            pv[c] = pe;
+          }
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+        tmem_st32_nowait(cS, pk);  // P^T over the start of this thread's S^T columns
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        named_bar_arrive(kBarP2, kDSThreads);
+        // ---- dS phase ----
+        got = mbar_wait(dp_full, cnt & 1, abort_flag, p.err, CODE_DKDV | 11);
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) {
+          named_bar_sync(kBarDS2, kDSThreads);
+          continue;
+        }
+        tc_fence_after();
+        tmem_ld32_issue(cdP, sa);
+        tmem_ld32_issue(cdP + 32, sb);
+        tmem_wait_ld32(sa);
+        tmem_wait_ld32(sb);
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 d4 = ds4[c4];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 * 4 + e;
+            const float dp = __uint_as_float(c < 32 ? sa[c] : sb[c - 32]);
+            pv[c] = pv[c] * (dp - dv[e]);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+        tmem_st32_nowait(cdP, pk);  // dS^T over the start of this thread's dP^T columns
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        named_bar_arrive(kBarDS2, kDSThreads);
+      }
+      if (!alive) continue;
+      const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DKDV | 10);
+      alive = __all_sync(0xffffffffu, got);
+      if (!alive) continue;
+      tc_fence_after();
+      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bkv * p.S + key) * HD) + 8 * half;
+      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bkv * p.S + key) * HD) + 8 * half;
+#pragma unroll 1
+      for (int c32 = 0; c32 < 2; ++c32) {
+        float a[32], d[32];
+        tmem_ld32(tmem_base + lane_off + 256 + 64 * half + 32 * c32, a);
+        tmem_ld32(tmem_base + lane_off + 384 + 64 * half + 32 * c32, d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dvrow[c32 * 4 + q] = make_uint4(pack_bf16x2(a[q * 8 + 0], a[q * 8 + 1]), pack_bf16x2(a[q * 8 + 2], a[q * 8 + 3]),
+                                          pack_bf16x2(a[q * 8 + 4], a[q * 8 + 5]), pack_bf16x2(a[q * 8 + 6], a[q * 8 + 7]));
+          dkrow[c32 * 4 + q] = make_uint4(
+              pack_bf16x2(d[q * 8 + 0] * scale, d[q * 8 + 1] * scale), pack_bf16x2(d[q * 8 + 2] * scale, d[q * 8 + 3] * scale),
+              pack_bf16x2(d[q * 8 + 4] * scale, d[q * 8 + 5] * scale), pack_bf16x2(d[q * 8 + 6] * scale, d[q * 8 + 7] * scale));
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ===========================================================================
 // dQ
 // ===========================================================================
 constexpr int DQ_KB = 64;  // keys per block
@@ -671,6 +1015,8 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
   if (!configured) {
     if (cudaFuncSetAttribute(attn_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DKDV_SMEM) !=
             cudaSuccess ||
+        cudaFuncSetAttribute(attn_dkdv128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DKDV2_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
             cudaSuccess)
       return TSP_ERR_CUDA;
@@ -693,7 +1039,7 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
   const int nk = (int)(a.S / 128);
   dim3 g1((nk + 1) / 2, a.Hk, a.B);
   if (which & 1) {
-    attn_dkdv_tc_kernel<<<g1, THREADS, DKDV_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk);
+    attn_dkdv128_tc_kernel<<<g1, THREADS, DKDV2_SMEM, stream>>>(mK128, mV128, mQ128, mdO128, p, nk);
     if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
   }
   if (!(which & 2)) return TSP_OK;
