@@ -6,22 +6,22 @@
 //   dV = P^T dO,  dK = dS^T Q / sqrt(dh),  dQ = dS K / sqrt(dh).
 // Two kernels, no atomics; every tensor-core operand arrives by TMA:
 //   dK/dV: one CTA per mirror pair of 128-key tiles (j, nk-1-j: together they
-//     see a constant number of query blocks).  K and V of the tile stay in
-//     shared memory; query blocks of 64 stream through a 4-stage ring holding
-//     Q and dO, read as K-major operands by S^T = K Q^T, dP^T = V dO^T and as
-//     MN-major operands by dV += P^T dO, dK += dS^T Q.  TMEM: S^T and dP^T
-//     double-buffered (4 x 64 columns), dV and dK accumulators (2 x 128).
+//     see a constant number of query blocks) of one K/V head.  K and V of the
+//     tile stay in shared memory; 128-query blocks of Q and dO (of every query
+//     head reading the K/V head) stream through a 2-stage ring, read K-major by
+//     S^T = K Q^T, dP^T = V dO^T and MN-major by dV += P^T dO, dK += dS^T Q.
+//     TMEM: S^T, dP^T (single-buffered), dV and dK accumulators.
 //   dQ: one CTA per mirror pair of 128-query tiles (the forward's zigzag
 //     pairing: both tiles on the same rank).  Q and dO stay in shared memory;
 //     key blocks of 64 stream K and V (4-stage ring) for S = Q K^T,
 //     dP = dO V^T, with the K tile read again as the MN-major operand of
 //     dQ += dS K.  TMEM: S and dP double-buffered, dQ accumulator.
 // In both, warps 0-7 turn scores into P and dS (a TMEM lane = a row, split
-// over two threads of 32 columns each) and write them back into tensor memory
-// as packed bf16, where the accumulating MMAs read them as their A operand;
-// lse and dsum of each query block come in with the stage by bulk copy.
-// Warp 8 issues TMA, warp 9 issues tcgen05.mma from one thread; the tensor core computes block i+1's scores
-// while the elementwise warps work on block i.
+// over two threads) and write them back into tensor memory as packed bf16,
+// where the accumulating MMAs read them as their A operand; lse and dsum of
+// each query block come in with the stage by bulk copy (dK/dV) or are read
+// once per tile (dQ).  Warp 8 issues TMA, warp 9 issues tcgen05.mma from one
+// thread, warp 10 relays landed stages to warp 9.
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,8 +33,9 @@ constexpr int HD = 128;
 constexpr int THREADS = 352;  // warps 0-7 elementwise (two per TMEM lane quadrant), 8 TMA, 9 MMA, 10 relay
 // Named barriers into the MMA warp (which never waits on an mbarrier inside a
 // tile): the relay warp announces each landed stage on kBarStage + (n % 4)
-// (64 threads: relay + MMA), the elementwise warps hand back P/dS of block i
-// on kBarDS + (i % 2) (256 + 32 threads).  A warp arrives without blocking
+// (64 threads: relay + MMA), the elementwise warps hand back dS of block i
+// on kBarDS + (i % 2) in the dQ kernel, P and dS on kBarP2 / kBarDS2 in the
+// dK/dV kernel (256 + 32 threads).  A warp arrives without blocking
 // only while the data it hands over keeps it in step with the MMA warp; the
 // relay, and any warp that has given up waiting, uses the blocking form, so
 // no warp can run ahead and complete a barrier phase in the MMA warp's place.
@@ -69,317 +70,6 @@ __device__ __forceinline__ int64_t zz_row(int64_t pos, int64_t C, int D, int B, 
   const int64_t c = pos / C, off = pos - c * C;
   const int64_t r = c < D ? c : 2 * D - 1 - c;
   return (r * B + b) * 2 * C + (c < D ? off : C + off);
-}
-
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  float a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    v[i] = a[i];
-    v[32 + i] = b[i];
-  }
-}
-
-// ===========================================================================
-// dK, dV
-// ===========================================================================
-constexpr int KB_QB = 64;  // queries per block
-// stage: Q, dO (2 sub-tiles each), then lse and dsum of the block (256 B each)
-constexpr int QSTG = 4;
-constexpr uint32_t KV_STAGE_DATA = 4 * SUB64;
-constexpr uint32_t KV_STAGE_BYTES = KV_STAGE_DATA + 1024;  // keeps stages 1024-byte aligned
-constexpr size_t DKDV_SMEM = 1024 + 2 * 2 * SUB128 + QSTG * (size_t)KV_STAGE_BYTES + 256;
-
-__global__ void __launch_bounds__(THREADS, 1)
-    attn_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-                        const BwdTcParams p, int nk) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Ks = smem;                    // 2 x SUB128
-  uint8_t* Vs = smem + 2 * SUB128;       // 2 x SUB128
-  uint8_t* stg = smem + 4 * SUB128;      // [QSTG] stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + QSTG * KV_STAGE_BYTES);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* kv_free = bars + 1;
-  uint64_t* q_full = bars + 2;   // [QSTG]
-  uint64_t* q_free = bars + 6;   // [QSTG]
-  uint64_t* s_full = bars + 10;  // [2]
-  uint64_t* o_done = bars + 14;
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // blockIdx.y is a K/V head; the `grp` query heads that read it stream through
-  // one after another (their dK, dV contributions add up in tensor memory)
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int grp = p.H / p.Hk;
-  const int64_t bkv = (int64_t)b * p.Hk + kvh;
-  auto tile_of = [&](int t) { return t == 0 ? (int)blockIdx.x : nk - 1 - (int)blockIdx.x; };
-  const int ntile = (nk - 1 - (int)blockIdx.x == (int)blockIdx.x) ? 1 : 2;
-
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(kv_free, 1);
-    for (int s = 0; s < QSTG; ++s) {
-      mbar_init(&q_full[s], 1);
-      mbar_init(&q_free[s], 1);
-    }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(o_done, 1);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbarrier_init();
-  }
-  if (warp == 8 && lane == 0) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmdO);
-  }
-  if (warp == 9) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // TMEM columns: S^T[x] at 64x, dP^T[x] at 128 + 64x, dV at 256, dK at 384.
-  // P^T (bf16 pairs) is written over the first 32 columns of S^T[x] and dS^T
-  // over dP^T[x]; the accumulating MMAs read them from there (A operand in
-  // tensor memory).  The next score MMAs into buffer x are issued after those
-  // MMAs, and one CTA's tcgen05 MMAs execute in issue order.
-
-  if (warp == 8) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      uint32_t qi = 0;
-      int kv_armed = 0;
-      bool ok = true;
-      for (int t = 0; t < ntile && ok; ++t) {
-        const int kt = tile_of(t);
-        const int64_t k0 = (int64_t)kt * 128;
-        if (!mbar_wait(kv_free, (t & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 1)) break;
-        mbar_arrive_expect_tx(kv_full, 4 * SUB128);
-        ++kv_armed;
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(Ks + c * SUB128, &tmK, c * 64, (int)(bkv * p.S + k0), kv_full);
-          tma_load_2d(Vs + c * SUB128, &tmV, c * 64, (int)(bkv * p.S + k0), kv_full);
-        }
-        const int nq = (int)((p.S - k0) / KB_QB);
-        for (int u = 0; u < grp * nq; ++u, ++qi) {
-          const int i = u % nq;
-          const int head = kvh * grp + u / nq;
-          const int64_t bh = (int64_t)b * p.H + head;
-          const int s = qi % QSTG;
-          if (!mbar_wait(&q_free[s], ((qi / QSTG) & 1) ^ 1, abort_flag, p.err, CODE_DKDV | 2)) {
-            ok = false;
-            break;
-          }
-          const int64_t zr = zz_row(k0 + (int64_t)i * KB_QB, p.C, p.D, p.B, b);
-          uint8_t* st = stg + s * KV_STAGE_BYTES;
-          const int64_t q0 = k0 + (int64_t)i * KB_QB;
-          mbar_arrive_expect_tx(&q_full[s], KV_STAGE_DATA + 2 * KB_QB * 4);
-          for (int c = 0; c < 2; ++c) {
-            tma_load_2d(st + c * SUB64, &tmQ, head * HD + c * 64, (int)zr, &q_full[s]);
-            tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmdO, head * HD + c * 64, (int)zr, &q_full[s]);
-          }
-          bulk_load(st + KV_STAGE_DATA, p.lse + bh * p.S + q0, KB_QB * 4, &q_full[s]);
-          bulk_load(st + KV_STAGE_DATA + KB_QB * 4, p.dsum + bh * p.S + q0, KB_QB * 4, &q_full[s]);
-        }
-      }
-      volatile int dummy = 0;
-      const uint32_t first = qi > QSTG ? qi - QSTG : 0;
-      for (uint32_t n = first; n < qi; ++n) mbar_wait(&q_full[n % QSTG], (n / QSTG) & 1, &dummy, p.err, CODE_DKDV | 3);
-      if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_DKDV | 3);
-    }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer (whole warp walks the schedule, lane 0 issues) ----------------
-    constexpr uint32_t id_s = idesc_bf16_f32(128, KB_QB);  // M = keys, N = queries
-    constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // M = keys, N = head dim (B MN-major)
-    uint32_t qi = 0;
-    bool ok = true;  // warp-uniform
-    auto scores = [&](uint32_t n, int x) {  // S^T = K Q^T, dP^T = V dO^T for query block n
-      uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
-#pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
-        const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
-        umma_bf16(tmem_base + 64 * x, ak, bq, id_s, k > 0);
-      }
-#pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
-        const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
-        umma_bf16(tmem_base + 128 + 64 * x, av, bo, id_s, k > 0);
-      }
-      umma_commit(&s_full[x]);
-    };
-    // dV += P^T dO, dK += dS^T Q for query block n: the Q / dO tiles of the
-    // stage serve as MN-major B operands (rows = queries = K dimension)
-    auto accumulate = [&](uint32_t n, int x, bool acc) {
-      uint8_t* st = stg + (n % QSTG) * KV_STAGE_BYTES;
-#pragma unroll
-      for (int k = 0; k < KB_QB / 16; ++k) {
-        const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB64) + 2048 * k, SUB64);
-        umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bo, id_o,
-                     (acc || k > 0) ? 1u : 0u);
-      }
-#pragma unroll
-      for (int k = 0; k < KB_QB / 16; ++k) {
-        const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
-        umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * x + 32 * (k / 2) + 8 * (k % 2), bq, id_o,
-                     (acc || k > 0) ? 1u : 0u);
-      }
-      umma_commit(&q_free[n % QSTG]);
-    };
-    auto sync_ds = [&](int i) {  // elementwise results of block i of the tile are in TMEM
-      __syncwarp();
-      named_bar_sync(kBarDS + (i & 1), kDSThreads);
-      tc_fence_after();
-    };
-    for (int t = 0; t < ntile; ++t) {
-      const int64_t k0 = (int64_t)tile_of(t) * 128;
-      const int nq = grp * (int)((p.S - k0) / KB_QB);  // query blocks of all the group's heads
-      if (ok) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_DKDV | 4);
-        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-      }
-      for (int i = 0; i < nq; ++i) {
-        const uint32_t n = qi + i;
-        __syncwarp();
-        named_bar_sync(kBarStage + (n & 3), kStageThreads);  // stage n has landed
-        tc_fence_after();
-        if (ok && lane == 0) scores(n, i & 1);
-        if (i > 0) {
-          sync_ds(i - 1);
-          if (ok && lane == 0) accumulate(n - 1, (i - 1) & 1, i - 1 > 0);
-        }
-      }
-      sync_ds(nq - 1);
-      if (ok && lane == 0) {
-        accumulate(qi + nq - 1, (nq - 1) & 1, nq - 1 > 0);
-        umma_commit(o_done);
-        umma_commit(kv_free);
-      }
-      qi += nq;
-    }
-    if (lane == 0) {
-      umma_commit(drain);
-      volatile int dummy = 0;
-      mbar_wait(drain, 0, &dummy, p.err, CODE_DKDV | 7);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ---------------- relay: announces each landed stage to the MMA warp ----------------
-    uint32_t n = 0;
-    for (int t = 0; t < ntile; ++t) {
-      const int nq = grp * (int)((p.S - (int64_t)tile_of(t) * 128) / KB_QB);
-      for (int i = 0; i < nq; ++i, ++n) {
-        if (lane == 0) mbar_wait(&q_full[n % QSTG], (n / QSTG) & 1, abort_flag, p.err, CODE_DKDV | 9);
-        __syncwarp();
-        named_bar_sync(kBarStage + (n & 3), kStageThreads);
-      }
-    }
-  } else {
-    // ------- elementwise warps 0-7: one key row, 32 of the 64 query columns per thread -------
-    const int quad = warp & 3, half = warp >> 2;
-    const int row = quad * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const float sl2 = kLog2e * rsqrtf((float)HD);
-    const float scale = rsqrtf((float)HD);
-    uint32_t scnt[2] = {0, 0};
-    uint32_t qidx = 0;  // global query-block counter (stage = qidx % QSTG)
-    bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
-    for (int t = 0; t < ntile; ++t) {
-      const int64_t k0 = (int64_t)tile_of(t) * 128;
-      const int nq = (int)((p.S - k0) / KB_QB);
-      const int64_t key = k0 + row;
-      for (int u = 0; u < grp * nq; ++u) {
-        const int i = u % nq;  // query block within the head
-        const int x = u & 1;
-        const bool got = alive && mbar_wait(&s_full[x], scnt[x] & 1, abort_flag, p.err, CODE_DKDV | 8);
-        ++scnt[x];
-        alive = __all_sync(0xffffffffu, got);
-        if (!alive) {
-          named_bar_sync(kBarDS + (u & 1), kDSThreads);
-          continue;
-        }
-        tc_fence_after();
-        const uint32_t cS = tmem_base + lane_off + 64 * x + 32 * half;
-        const uint32_t cdP = tmem_base + lane_off + 128 + 64 * x + 32 * half;
-        float sv[32], dp[32];
-        tmem_ld32(cS, sv);
-        tmem_ld32(cdP, dp);
-        const int64_t q0 = k0 + (int64_t)i * KB_QB + 32 * half;  // first query of this thread's columns
-        const bool diag = i < 2;
-        // lse and dsum of this query block arrived with the stage (bulk copies)
-        const float4* lse4 = reinterpret_cast<const float4*>(stg + (qidx % QSTG) * KV_STAGE_BYTES + KV_STAGE_DATA) + 8 * half;
-        const float4* ds4 = lse4 + KB_QB / 4;
-        uint32_t pk[16], dk2[16];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = lse4[c4], d4 = ds4[c4];
-          const float lv[4] = {l4.x * kLog2e, l4.y * kLog2e, l4.z * kLog2e, l4.w * kLog2e};
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c4 * 4 + e;
-            pv[e] = ex2f(fmaf(sv[c], sl2, -lv[e]));
-            if (diag && q0 + c < key) pv[e] = 0.f;
-          }
-          pk[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-          pk[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-          dk2[2 * c4] = pack_bf16x2(pv[0] * (dp[c4 * 4] - dv[0]), pv[1] * (dp[c4 * 4 + 1] - dv[1]));
-          dk2[2 * c4 + 1] = pack_bf16x2(pv[2] * (dp[c4 * 4 + 2] - dv[2]), pv[3] * (dp[c4 * 4 + 3] - dv[3]));
-        }
-        ++qidx;
-        // P^T over the start of this thread's S^T columns, dS^T over its dP^T columns
-        tmem_st16_nowait(cS, pk);
-        tmem_st16_nowait(cdP, dk2);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        named_bar_arrive(kBarDS + (u & 1), kDSThreads);
-      }
-      if (!alive) continue;
-      const bool got = mbar_wait(o_done, t & 1, abort_flag, p.err, CODE_DKDV | 10);
-      alive = __all_sync(0xffffffffu, got);
-      if (!alive) continue;
-      tc_fence_after();
-      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bkv * p.S + key) * HD) + 8 * half;
-      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bkv * p.S + key) * HD) + 8 * half;
-#pragma unroll 1
-      for (int c32 = 0; c32 < 2; ++c32) {
-        float a[32], d[32];
-        tmem_ld32(tmem_base + lane_off + 256 + 64 * half + 32 * c32, a);
-        tmem_ld32(tmem_base + lane_off + 384 + 64 * half + 32 * c32, d);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          dvrow[c32 * 4 + q] = make_uint4(pack_bf16x2(a[q * 8 + 0], a[q * 8 + 1]), pack_bf16x2(a[q * 8 + 2], a[q * 8 + 3]),
-                                          pack_bf16x2(a[q * 8 + 4], a[q * 8 + 5]), pack_bf16x2(a[q * 8 + 6], a[q * 8 + 7]));
-          dkrow[c32 * 4 + q] = make_uint4(
-              pack_bf16x2(d[q * 8 + 0] * scale, d[q * 8 + 1] * scale), pack_bf16x2(d[q * 8 + 2] * scale, d[q * 8 + 3] * scale),
-              pack_bf16x2(d[q * 8 + 4] * scale, d[q * 8 + 5] * scale), pack_bf16x2(d[q * 8 + 6] * scale, d[q * 8 + 7] * scale));
-        }
-      }
-      tc_fence_before();
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
-  }
 }
 
 // ===========================================================================
@@ -1013,9 +703,7 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
     return TSP_ERR_CUDA;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(attn_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DKDV_SMEM) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(attn_dkdv128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_dkdv128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)DKDV2_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
             cudaSuccess)
