@@ -113,7 +113,10 @@ def step_work(cfg):
             "transpose V^T": (0, 2 * T * hk * e, 1),
             "attention bwd": (2 * attn, (4 * T * h + 4 * T * hk) * e, 3),
             "attention bwd dsum": (0, 2 * T * h * e, 1),
-            "attention bwd dK/dV": (attn, (2 * T * h + 4 * T * hk) * e, 1),
+            # model flops of the backward attention (2 x the forward's) split between the kernels:
+            # dK/dV computes dP, dV and dK; dQ computes dQ.  The S recompute (both kernels) and the
+            # dQ kernel's second dP are not counted.
+            "attention bwd dK/dV": (3 * attn // 2, (2 * T * h + 4 * T * hk) * e, 1),
             "attention bwd dQ": (attn // 2, (3 * T * h + 2 * T * hk) * e, 1),
             "assemble dQKV": (0, 2 * T * W3 * e, 1),
             "dx": (2 * T * W3 * h, (T * W3 + W3 * h + 2 * T * h) * e, 1),
