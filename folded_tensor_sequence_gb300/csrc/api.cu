@@ -372,6 +372,21 @@ unsigned int* dev_error_word() {
   return ptrs[dev];
 }
 
+namespace {
+unsigned long long device_bit() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  return 1ull << dev;
+}
+}  // namespace
+
+bool needs_setup(const std::atomic<unsigned long long>& done) {
+  const unsigned long long bit = device_bit();
+  return bit == 0 || (done.load() & bit) == 0;
+}
+
+void mark_setup_done(std::atomic<unsigned long long>& done) { done.fetch_or(device_bit()); }
+
 int num_sms() {
   static int cache[64] = {};
   int dev = 0;

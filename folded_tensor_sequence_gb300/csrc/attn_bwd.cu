@@ -387,14 +387,14 @@ cudaError_t launch_attn_dsum(const void* o, const void* dO, float* dsum, int D, 
 tsp_status attn_bwd_bf16(const AttnBwdParams& p, cudaStream_t stream) {
   if (p.dh != DH) return TSP_ERR_UNSUPPORTED;
   if (p.B * p.S == 0) return TSP_OK;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // devices set up
+  if (needs_setup(configured)) {
     if (cudaFuncSetAttribute(attn_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DKV_SMEM) !=
             cudaSuccess ||
         cudaFuncSetAttribute(attn_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
             cudaSuccess)
       return TSP_ERR_CUDA;
-    configured = true;
+    mark_setup_done(configured);
   }
   const int64_t rows = (int64_t)p.B * p.H * p.S;
   dsum_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(p.o),

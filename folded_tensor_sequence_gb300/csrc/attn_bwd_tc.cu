@@ -701,14 +701,14 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
       !make_tma_2d_bf16(&mQ128, a.q, T, h, h, 128) || !make_tma_2d_bf16(&mdO128, a.dO, T, h, h, 128) ||
       !make_tma_2d_bf16(&mK64, a.k, kv_rows, HD, HD, 64) || !make_tma_2d_bf16(&mV64, a.v, kv_rows, HD, HD, 64))
     return TSP_ERR_CUDA;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // devices set up
+  if (needs_setup(configured)) {
     if (cudaFuncSetAttribute(attn_dkdv128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)DKDV2_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
             cudaSuccess)
       return TSP_ERR_CUDA;
-    configured = true;
+    mark_setup_done(configured);
   }
   BwdTcParams p;
   p.B = a.B;

@@ -283,12 +283,12 @@ tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream) {
 tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream) {
   if (p.dh != DH) return TSP_ERR_UNSUPPORTED;
   if (p.B * p.S == 0) return TSP_OK;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // devices set up
+  if (needs_setup(configured)) {
     if (cudaFuncSetAttribute(attn_fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ATT_SMEM) !=
         cudaSuccess)
       return TSP_ERR_CUDA;
-    configured = true;
+    mark_setup_done(configured);
   }
   const int n_tiles = (int)((p.C + BQ - 1) / BQ);
   dim3 grid(p.D * n_tiles, p.H, p.B);

@@ -505,12 +505,12 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
       !make_tma_2d_bf16(&mk, a.k, (int64_t)a.B * a.Hk * a.S, HD, HD, 128) ||
       !make_tma_2d_bf16(&mv, a.v, (int64_t)a.B * a.Hk * HD, a.S, a.S, 128))
     return TSP_ERR_CUDA;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // devices set up
+  if (needs_setup(configured)) {
     if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
         cudaSuccess)
       return TSP_ERR_CUDA;
-    configured = true;
+    mark_setup_done(configured);
   }
   FaParams p;
   p.B = a.B;

@@ -432,10 +432,19 @@ tsp_status decode_step_bf16(const tsp_plan* pl, int batch, int64_t pos, const vo
     case 1: decode_attn_partial_kernel<1><<<grid, DA_THREADS, smem, st>>>(ap); break;
     case 2: decode_attn_partial_kernel<2><<<grid, DA_THREADS, smem, st>>>(ap); break;
     case 4: decode_attn_partial_kernel<4><<<grid, DA_THREADS, smem, st>>>(ap); break;
-    case 8:
-      cudaFuncSetAttribute(decode_attn_partial_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    case 8: {
+      static std::atomic<unsigned long long> configured{0};  // devices set up
+      if (needs_setup(configured)) {
+        if (cudaFuncSetAttribute(decode_attn_partial_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)((size_t)16 * 8 * (HD + 2) * 4)) != cudaSuccess) {
+          prof_end(st);
+          return TSP_ERR_CUDA;
+        }
+        mark_setup_done(configured);
+      }
       decode_attn_partial_kernel<8><<<grid, DA_THREADS, smem, st>>>(ap);
       break;
+    }
     default: prof_end(st); return TSP_ERR_UNSUPPORTED;
   }
   e = cudaGetLastError();

@@ -393,12 +393,12 @@ namespace {
 template <int EPI, bool AMN, bool BMN>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& s, const EpiParams& ep,
                        cudaStream_t stream) {
-  static bool configured = false;  // per-process; attribute is per function
-  if (!configured) {
+  static std::atomic<unsigned long long> configured{0};  // devices set up for this instantiation
+  if (needs_setup(configured)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, AMN, BMN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured = true;
+    mark_setup_done(configured);
   }
   const int grid = s.num_tiles < num_sms() ? s.num_tiles : num_sms();
   gemm_bf16_tc_kernel<EPI, AMN, BMN><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, s, ep);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/tsp.h"
 
 struct tsp_plan {
@@ -53,6 +55,11 @@ struct EpiParams {
 };
 
 int num_sms();
+// One-time setup per device (kernel attributes such as the dynamic shared-memory
+// limit are per device): needs_setup() is true until mark_setup_done() has been
+// called on the current device.  Devices 0..63.
+bool needs_setup(const std::atomic<unsigned long long>& done);
+void mark_setup_done(std::atomic<unsigned long long>& done);
 // Records `msg` as this thread's tsp_last_error_message() and returns `s`.
 tsp_status report_error(tsp_status s, const char* msg);
 unsigned int* dev_error_word();  // device address of this device's error word (nullptr on failure)
