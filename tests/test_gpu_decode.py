@@ -145,3 +145,19 @@ def test_decode_full_context(tsp, cfg):
         check(vc[:, :, pos].float().reshape(B, -1).cpu().numpy(), v_new, "bf16", "appended v")
         del kc, vc, k0, v0
         torch.cuda.empty_cache()
+
+
+def test_decode_agrees_across_D(tsp):
+    """The rank split of the cache only partitions the keys: D = 1, 2, 4 give the same step."""
+    base = LayerConfig("dec_xD", D=1, batch=2, seq=1024, hidden=1024, heads=8, head_dim=128, ffn=512, dtype="bf16",
+                       kv_heads=4)
+    inp = synth.layer_inputs(base, seed=45)
+    x_new = synth.tensor("x", (base.batch, base.hidden), 1.0, "bf16", 46)
+    outs = {}
+    for D in (1, 2, 4):
+        y, kc, vc, _, _ = run_decode(tsp, base.with_(D=D), inp, x_new, 700, seed=300)
+        outs[D] = (y, to_np(kc[:, :, 700]), to_np(vc[:, :, 700]))
+    for D in (2, 4):
+        assert np.array_equal(outs[D][1], outs[1][1]) and np.array_equal(outs[D][2], outs[1][2])  # same K/V row
+        err = np.linalg.norm(outs[D][0] - outs[1][0]) / np.linalg.norm(outs[1][0])
+        assert err <= 2e-2, (D, err)
