@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 9) {
     // ------------------------------ MMA issuer ------------------------------
-    // The whole warp walks the schedule (named barriers are warp-aligned);
-    // lane 0 issues.  Inside a block the warp never waits on an mbarrier: the
+    // The whole warp walks the schedule (named barriers are warp-aligned) and
+    // issues through the warp-collective MMA helpers (one elected lane
+    // issues).  Inside a block the warp never waits on an mbarrier: the
     // softmax warpgroup that hands over P_x(j) has also checked that the K/V
     // tiles the following MMAs read have landed.
     constexpr uint32_t idesc = idesc_bf16_f32(QT, KT);
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; k < HD / 16; ++k) {
         const uint64_t a = sdesc_kmajor_sw128(qa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
         const uint64_t bb = sdesc_kmajor_sw128(kb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-        umma_bf16(tmem_base + x * 128, a, bb, idesc, k > 0);
+        umma_bf16_warp(tmem_base + x * 128, a, bb, idesc, k > 0);
       }
     };
     auto mma_pv = [&](int x, int s, bool acc) {  // O_x += P_x V, K = keys; P_x in TMEM (S_x columns 0-63)
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int k = 0; k < KT / 16; ++k) {
         const uint64_t bb = sdesc_kmajor_sw128(vb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-        umma_bf16_ts(tmem_base + 256 + x * 128, tmem_base + x * 128 + 8 * k, bb, idesc, (acc || k > 0) ? 1u : 0u);
+        umma_bf16_ts_warp(tmem_base + 256 + x * 128, tmem_base + x * 128 + 8 * k, bb, idesc, (acc || k > 0) ? 1u : 0u);
       }
     };
     for (int blk = 0; blk < 2; ++blk) {
@@ -281,12 +282,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       }
       tc_fence_after();
-      if (ok && lane == 0) {
+      if (ok) {
         mma_s(0, base % STAGES);
-        umma_commit(&s_full[0]);
+        umma_commit_warp(&s_full[0]);
         mma_s(1, base % STAGES);
-        umma_commit(&s_full[1]);
-        umma_commit(&kv_empty[base % STAGES]);
+        umma_commit_warp(&s_full[1]);
+        umma_commit_warp(&kv_empty[base % STAGES]);
       }
       for (int j = 0; j < nB; ++j) {
         const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
@@ -294,37 +295,37 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
           named_bar_sync(kBarPA + (j & 1), kHandoffThreads);
           tc_fence_after();
-          if (ok && lane == 0) {
+          if (ok) {
             mma_pv(0, iv % STAGES, j > 0);
             if (j + 1 < nA) {
               mma_s(0, ik % STAGES);
-              umma_commit(&s_full[0]);
+              umma_commit_warp(&s_full[0]);
             } else {
-              umma_commit(&o_done[0]);
+              umma_commit_warp(&o_done[0]);
             }
           }
         }
         __syncwarp();
         named_bar_sync(kBarPB + (j & 1), kHandoffThreads);
         tc_fence_after();
-        if (ok && lane == 0) {
+        if (ok) {
           mma_pv(1, iv % STAGES, j > 0);
-          umma_commit(&kv_empty[iv % STAGES]);
+          umma_commit_warp(&kv_empty[iv % STAGES]);
           if (j + 1 < nB) {
             mma_s(1, ik % STAGES);
-            umma_commit(&s_full[1]);
-            umma_commit(&kv_empty[ik % STAGES]);
+            umma_commit_warp(&s_full[1]);
+            umma_commit_warp(&kv_empty[ik % STAGES]);
           } else {
-            umma_commit(&o_done[1]);
+            umma_commit_warp(&o_done[1]);
           }
         }
       }
       item = base + 2 * nB;
       // the Q buffer is free for block 1 once every MMA issued so far is done
-      if (blk == 0 && ok && lane == 0) umma_commit(q_empty);
+      if (blk == 0 && ok) umma_commit_warp(q_empty);
     }
+    umma_commit_warp(drain);
     if (lane == 0) {
-      umma_commit(drain);
       volatile int dummy = 0;
       mbar_wait(drain, 0, &dummy, p.err, code | 7);
     }
