@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_DKDV | 3);
     }
   } else if (warp == 9) {
-    // ---------------- MMA issuer (whole warp walks the schedule, lane 0 issues) ----------------
+    // ---------------- MMA issuer (whole warp walks the schedule and issues; one elected lane) ----------------
     constexpr uint32_t id_s = idesc_bf16_f32(128, QB2);              // M = keys, N = queries
     constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // M = keys, N = head dim (B MN-major)
     uint32_t qi = 0;
@@ -206,9 +206,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; k < HD / 16; ++k) {
         const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
         const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB128)) + 2 * (k % 4);
-        umma_bf16(tmem_base, ak, bq, id_s, k > 0);
+        umma_bf16_warp(tmem_base, ak, bq, id_s, k > 0);
       }
-      umma_commit(s_full);
+      umma_commit_warp(s_full);
     };
     auto dpscores = [&](uint32_t n) {  // dP^T = V dO^T
       uint8_t* st = stage(n);
@@ -216,9 +216,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; k < HD / 16; ++k) {
         const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
         const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB128 + (k / 4) * SUB128)) + 2 * (k % 4);
-        umma_bf16(tmem_base + 128, av, bo, id_s, k > 0);
+        umma_bf16_warp(tmem_base + 128, av, bo, id_s, k > 0);
       }
-      umma_commit(dp_full);
+      umma_commit_warp(dp_full);
     };
     // dV += P^T dO and dK += dS^T Q: the stage's dO / Q tiles as MN-major B
     // operands (rows = queries = K dimension; 64-column chunks SUB128 apart)
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int k = 0; k < QB2 / 16; ++k) {
         const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB128) + 2048 * k, SUB128);
-        umma_bf16_ts(tmem_base + 256, tmem_base + 64 * (k / 4) + 8 * (k % 4), bo, id_o, (acc || k > 0) ? 1u : 0u);
+        umma_bf16_ts_warp(tmem_base + 256, tmem_base + 64 * (k / 4) + 8 * (k % 4), bo, id_o, (acc || k > 0) ? 1u : 0u);
       }
     };
     auto accum_k = [&](uint32_t n, bool acc) {
@@ -235,10 +235,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int k = 0; k < QB2 / 16; ++k) {
         const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB128);
-        umma_bf16_ts(tmem_base + 384, tmem_base + 128 + 64 * (k / 4) + 8 * (k % 4), bq, id_o,
+        umma_bf16_ts_warp(tmem_base + 384, tmem_base + 128 + 64 * (k / 4) + 8 * (k % 4), bq, id_o,
                      (acc || k > 0) ? 1u : 0u);
       }
-      umma_commit(&q_free[n % QSTG2]);
+      umma_commit_warp(&q_free[n % QSTG2]);
     };
     auto sync_on = [&](int id, int count) {
       __syncwarp();
@@ -254,32 +254,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       }
       sync_on(kBarStage + (qi & 3), kStageThreads);
-      if (ok && lane == 0) {
+      if (ok) {
         scores(qi);
         dpscores(qi);
       }
       for (int i = 0; i < nq; ++i) {
         const uint32_t n = qi + i;
         sync_on(kBarP2, kDSThreads);  // P^T(n) in TMEM
-        if (ok && lane == 0) accum_v(n, i > 0);
+        if (ok) accum_v(n, i > 0);
         if (i + 1 < nq) {
           sync_on(kBarStage + ((n + 1) & 3), kStageThreads);
-          if (ok && lane == 0) scores(n + 1);
+          if (ok) scores(n + 1);
         }
         sync_on(kBarDS2, kDSThreads);  // dS^T(n) in TMEM
-        if (ok && lane == 0) {
+        if (ok) {
           accum_k(n, i > 0);
           if (i + 1 < nq) dpscores(n + 1);
         }
       }
-      if (ok && lane == 0) {
-        umma_commit(o_done);
-        umma_commit(kv_free);
+      if (ok) {
+        umma_commit_warp(o_done);
+        umma_commit_warp(kv_free);
       }
       qi += nq;
     }
+    umma_commit_warp(drain);
     if (lane == 0) {
-      umma_commit(drain);
       volatile int dummy = 0;
       mbar_wait(drain, 0, &dummy, p.err, CODE_DKDV | 7);
     }
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (q_armed) mbar_wait(q_full, (q_armed - 1) & 1, &dummy, p.err, CODE_DQ | 3);
     }
   } else if (warp == 9) {
-    // ---------------- MMA issuer (whole warp walks the schedule, lane 0 issues) ----------------
+    // ---------------- MMA issuer (whole warp walks the schedule and issues; one elected lane) ----------------
     constexpr uint32_t id_s = idesc_bf16_f32(128, DQ_KB);
     constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);  // B (K tile) MN-major
     uint32_t ki = 0;
@@ -538,25 +538,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; k < HD / 16; ++k) {
         const uint64_t aq = sdesc_kmajor_sw128(smem_u32(Qs + (k / 4) * SUB128)) + 2 * (k % 4);
         const uint64_t bk = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
-        umma_bf16(tmem_base + 64 * x, aq, bk, id_s, k > 0);
+        umma_bf16_warp(tmem_base + 64 * x, aq, bk, id_s, k > 0);
       }
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k) {
         const uint64_t ao = sdesc_kmajor_sw128(smem_u32(dOs + (k / 4) * SUB128)) + 2 * (k % 4);
         const uint64_t bv = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
-        umma_bf16(tmem_base + 128 + 64 * x, ao, bv, id_s, k > 0);
+        umma_bf16_warp(tmem_base + 128 + 64 * x, ao, bv, id_s, k > 0);
       }
-      umma_commit(&s_full[x]);
+      umma_commit_warp(&s_full[x]);
     };
     auto accumulate = [&](uint32_t n, int x, bool acc) {  // dQ += dS K for key block n (K tile as MN-major B)
       uint8_t* st = stg + (n % KSTG) * DQ_STAGE_BYTES;
 #pragma unroll
       for (int k = 0; k < DQ_KB / 16; ++k) {
         const uint64_t bk = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
-        umma_bf16_ts(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bk, id_o,
+        umma_bf16_ts_warp(tmem_base + 256, tmem_base + 64 * x + 32 * (k / 2) + 8 * (k % 2), bk, id_o,
                      (acc || k > 0) ? 1u : 0u);
       }
-      umma_commit(&k_free[n % KSTG]);
+      umma_commit_warp(&k_free[n % KSTG]);
     };
     auto sync_ds = [&](int j) {  // elementwise results of key block j of the tile are in TMEM
       __syncwarp();
@@ -577,22 +577,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         named_bar_sync(kBarStage + (n & 3), kStageThreads);  // stage n has landed
         tc_fence_after();
-        if (ok && lane == 0) scores(n, j & 1);
+        if (ok) scores(n, j & 1);
         if (j > 0) {
           sync_ds(j - 1);
-          if (ok && lane == 0) accumulate(n - 1, (j - 1) & 1, j - 1 > 0);
+          if (ok) accumulate(n - 1, (j - 1) & 1, j - 1 > 0);
         }
       }
       sync_ds(nkb - 1);
-      if (ok && lane == 0) {
+      if (ok) {
         accumulate(ki + nkb - 1, (nkb - 1) & 1, nkb - 1 > 0);
-        umma_commit(o_done);
-        umma_commit(q_free);
+        umma_commit_warp(o_done);
+        umma_commit_warp(q_free);
       }
       ki += nkb;
     }
+    umma_commit_warp(drain);
     if (lane == 0) {
-      umma_commit(drain);
       volatile int dummy = 0;
       mbar_wait(drain, 0, &dummy, p.err, CODE_DQ | 7);
     }
