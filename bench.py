@@ -75,8 +75,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def step_work(cfg):
-    """Algorithmic work per launch of each step: (flops, bytes, kernels launched)."""
+def step_work(cfg, cfg_det=False):
+    """Algorithmic work per launch of each step: (flops, bytes, kernels launched);
+    cfg_det: the backward runs the split (deterministic) attention kernels."""
     B, S, h, F, H, dh = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
     T = B * S
     e = 2 if cfg.dtype == "bf16" else 4
@@ -112,13 +113,16 @@ def step_work(cfg):
             "dW_O": (2 * h * h * T, (2 * T * h + h * h) * e, 1),
             "transpose V^T": (0, 2 * T * hk * e, 1),
             "attention bwd": (2 * attn, (4 * T * h + 4 * T * hk) * e, 3),
-            "attention bwd dsum": (0, 2 * T * h * e, 1),
-            # model flops of the backward attention (2 x the forward's) split between the kernels:
-            # dK/dV computes dP, dV and dK; dQ computes dQ.  The S recompute (both kernels) and the
-            # dQ kernel's second dP are not counted.
+            # rowsum(dO * O); zeroes the fp32 dQ accumulator when the fused kernel follows
+            "attention bwd dsum": (0, 2 * T * h * e + (0 if cfg_det else 4 * T * h), 1),
+            # model flops of the backward attention: 2 x the forward's (dP, dV, dK, dQ; the S
+            # recompute is not counted).  Fused: one kernel, dQ added into the fp32 accumulator.
+            "attention bwd fused": (2 * attn, (2 * T * h + 4 * T * hk) * e + 4 * T * h, 1),
+            # split (deterministic): dK/dV computes dP, dV and dK; dQ computes dQ.  The S
+            # recompute (both kernels) and the dQ kernel's second dP are not counted.
             "attention bwd dK/dV": (3 * attn // 2, (2 * T * h + 4 * T * hk) * e, 1),
-            "attention bwd dQ": (attn // 2, (3 * T * h + 2 * T * hk) * e, 1),
-            "assemble dQKV": (0, 2 * T * W3 * e, 1),
+            "attention bwd dQ": (attn // 2, (2 * T * h + 2 * T * hk) * e + 4 * T * h, 1),
+            "assemble dQKV": (0, (T * W3 + 2 * T * hk) * e + 4 * T * h, 1),
             "dx": (2 * T * W3 * h, (T * W3 + W3 * h + 2 * T * h) * e, 1),
             "dW_QKV": (2 * W3 * h * T, (T * W3 + T * h + W3 * h) * e, 1),
             "unpermute dx": (0, 2 * T * h * e, 1),
@@ -297,6 +301,8 @@ def main():
     ap.add_argument("--cpu-prefix", type=int, default=512, help="tokens of the oracle's CPU baseline sample")
     ap.add_argument("--ref-prefix", type=int, default=64, help="tokens per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="backward: split bitwise-reproducible kernels instead of the fused one")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = BY_NAME[args.config]
@@ -329,6 +335,7 @@ def main():
 
     B, S, h, F, hk = cfg.batch, cfg.seq, cfg.hidden, cfg.ffn, cfg.kv_hidden
     plan = tsp.plan_for(cfg)
+    tsp.tsp_plan_set_deterministic(plan, 1 if args.deterministic else 0)
     shapes = {"Wq": (h, h), "Wk": (h, hk), "Wv": (h, hk), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}
     canon = {k: synth.tensor_torch(k, s, (F if k == "Wd" else h) ** -0.5, cfg.dtype, 0, dev) for k, s in shapes.items()}
     packed = tsp.empty_packed(plan, dev)
@@ -404,7 +411,7 @@ def main():
         step()
     rows = tsp.tsp_profile_report()
     tsp.tsp_profile_enable(False)
-    wk = step_work(cfg)
+    wk = step_work(cfg, args.deterministic)
     kernels = {}
     launches_per_step = 0
     for name, tot, cnt in rows:
@@ -469,6 +476,8 @@ def main():
                        "kv_heads": cfg.kv_h, "head_dim": cfg.head_dim, "ffn": F,
                        "step": ("decode: one token per sequence at position seq-1 of a full K/V cache"
                                 if cfg.decode else ("layer forward + backward" if cfg.backward else "layer forward")),
+                       **({"attention_backward": "split, bitwise reproducible" if args.deterministic
+                           else "fused (dQ by fp32 L2 reductions)"} if cfg.backward and not cfg.decode else {}),
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single",
                        "l2": "inputs larger than L2 (%s %d MB, packed weights %d MB)" % (
                            "K/V cache" if cfg.decode else "x",

@@ -22,6 +22,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cmath>
 #include <initializer_list>
 #include <mutex>
 #include <new>
@@ -136,7 +137,7 @@ BwdLayout bwd_layout(const tsp_plan* p, int batch) {
   L.dhz = take(T * h * e);
   L.doz = take(T * h * e);
   const size_t hk = kv_hidden(p);
-  L.dq = take(T * h * e);
+  L.dq = take(T * h * 4);  // fp32 dQ accumulator [B][H][S][dh] (bf16 zigzag [T][h] on the warp-MMA path)
   L.dk = take(T * hk * e);
   L.dv = take(T * hk * e);
   L.dsum = take((size_t)batch * p->heads * p->seq * 4);
@@ -467,6 +468,16 @@ tsp_status tsp_plan_create_gqa(int D, int64_t seq, int hidden, int heads, int kv
 
 void tsp_plan_destroy(tsp_plan* plan) { delete plan; }
 
+tsp_status tsp_plan_set_deterministic(tsp_plan* plan, int deterministic) {
+  if (!plan) return fail(TSP_ERR_INVALID_ARG, "plan is NULL");
+  if (deterministic != 0 && deterministic != 1)
+    return fail(TSP_ERR_INVALID_ARG, "deterministic = %d (0 or 1)", deterministic);
+  plan->deterministic = deterministic;
+  return TSP_OK;
+}
+
+int tsp_plan_get_deterministic(const tsp_plan* plan) { return plan ? plan->deterministic : -1; }
+
 size_t tsp_workspace_bytes(const tsp_plan* p, int batch, tsp_op op) {
   if (!p || batch < 0) return 0;
   switch (op) {
@@ -720,11 +731,15 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     TSP_TRY(tr(sv + A.v, L.vnat, p->head_dim, p->seq, "transpose V^T", batch * p->kv_heads));
     v_nat = wb + L.vnat;
   }
-  if (attn_bwd_tc_supported(p->head_dim, p->chunk)) {
+  const bool tc_bwd = attn_bwd_tc_supported(p->head_dim, p->chunk);
+  if (tc_bwd) {
+    const bool fused = !p->deterministic;
     {
       Prof pr("attention bwd dsum", st);
+      // the fused kernel adds dQ partial sums into the accumulator: zero it in the same pass
       TSP_TRY(cuda_status(launch_attn_dsum(sv + A.oz, wb + L.doz, reinterpret_cast<float*>(wb + L.dsum), p->D, batch,
-                                         p->heads, p->seq, p->chunk, st),
+                                         p->heads, p->seq, p->chunk, st,
+                                         fused ? reinterpret_cast<float*>(wb + L.dq) : nullptr),
                           "attention dsum"));
     }
     AttnBwdTcArgs ab;
@@ -734,7 +749,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     ab.dO = wb + L.doz;
     ab.lse = reinterpret_cast<const float*>(sv + A.lse);
     ab.dsum = reinterpret_cast<const float*>(wb + L.dsum);
-    ab.dq = wb + L.dq;
+    ab.dq_acc = reinterpret_cast<float*>(wb + L.dq);
     ab.dk = wb + L.dk;
     ab.dv = wb + L.dv;
     ab.D = p->D;
@@ -744,13 +759,18 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     ab.dh = p->head_dim;
     ab.S = p->seq;
     ab.C = p->chunk;
-    {
-      Prof pr("attention bwd dK/dV", st);
-      s = attn_bwd_bf16_tc(ab, st, 1);
-    }
-    if (s == TSP_OK) {
-      Prof pr("attention bwd dQ", st);
-      s = attn_bwd_bf16_tc(ab, st, 2);
+    if (fused) {
+      Prof pr("attention bwd fused", st);
+      s = attn_bwd_bf16_tc(ab, st, 4);
+    } else {
+      {
+        Prof pr("attention bwd dK/dV", st);
+        s = attn_bwd_bf16_tc(ab, st, 1);
+      }
+      if (s == TSP_OK) {
+        Prof pr("attention bwd dQ", st);
+        s = attn_bwd_bf16_tc(ab, st, 2);
+      }
     }
     if (s != TSP_OK) return fail(s, "attention backward (tensor cores) failed: %s", tsp_status_string(s));
   } else {
@@ -779,9 +799,16 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   }
   {
     Prof pr_asm("assemble dQKV", st);
-    TSP_TRY(cuda_status(launch_assemble_dqkv(wb + L.dq, wb + L.dk, wb + L.dv, wb + L.dqkv, p->D, batch, p->seq,
-                                             p->heads, p->kv_heads, p->head_dim, st),
-                        "assemble dQKV"));
+    if (tc_bwd)
+      TSP_TRY(cuda_status(launch_assemble_dqkv_f32q(reinterpret_cast<const float*>(wb + L.dq),
+                                                    1.0f / std::sqrt((float)p->head_dim), wb + L.dk, wb + L.dv,
+                                                    wb + L.dqkv, p->D, batch, p->seq, p->heads, p->kv_heads,
+                                                    p->head_dim, st),
+                          "assemble dQKV"));
+    else
+      TSP_TRY(cuda_status(launch_assemble_dqkv(wb + L.dq, wb + L.dk, wb + L.dv, wb + L.dqkv, p->D, batch, p->seq,
+                                               p->heads, p->kv_heads, p->head_dim, st),
+                          "assemble dQKV"));
   }
   {
     EpiParams e = base_epi(p, batch);

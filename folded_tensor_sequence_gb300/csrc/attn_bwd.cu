@@ -49,7 +49,8 @@ __device__ __forceinline__ void load_zz_rows(__nv_bfloat16* sm, const __nv_bfloa
 }
 
 __global__ void dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-                            float* __restrict__ dsum, int D, int B, int H, int64_t S, int64_t C) {
+                            float* __restrict__ dsum, int D, int B, int H, int64_t S, int64_t C,
+                            float* __restrict__ dq_zero) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + warp;  // over (b, head, pos)
   if (w >= (int64_t)B * H * S) return;
@@ -64,6 +65,8 @@ __global__ void dsum_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bflo
   float s = a0.x * c0.x + a0.y * c0.y + a1.x * c1.x + a1.y * c1.y;
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (lane == 0) dsum[w] = s;
+  // the same (b, head, pos) row of the fp32 dQ accumulator, 128 floats
+  if (dq_zero != nullptr) reinterpret_cast<float4*>(dq_zero + w * DH)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -375,12 +378,12 @@ __global__ void __launch_bounds__(BT) attn_dq_kernel(AttnBwdParams p, int n_tile
 }  // namespace
 
 cudaError_t launch_attn_dsum(const void* o, const void* dO, float* dsum, int D, int B, int H, int64_t S, int64_t C,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float* dq_zero) {
   const int64_t rows = (int64_t)B * H * S;
   if (rows == 0) return cudaSuccess;
   dsum_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                               static_cast<const __nv_bfloat16*>(dO), dsum, D, B, H,
-                                                              S, C);
+                                                              S, C, dq_zero);
   return cudaGetLastError();
 }
 
@@ -399,7 +402,7 @@ tsp_status attn_bwd_bf16(const AttnBwdParams& p, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.B * p.H * p.S;
   dsum_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(p.o),
                                                               static_cast<const __nv_bfloat16*>(p.dO), p.dsum, p.D,
-                                                              p.B, p.H, p.S, p.C);
+                                                              p.B, p.H, p.S, p.C, nullptr);
   const int nk = (int)((p.S + KT - 1) / KT);
   dim3 g1((nk + 1) / 2, p.H, p.B);
   attn_dkdv_kernel<<<g1, BT, DKV_SMEM, stream>>>(p, nk);

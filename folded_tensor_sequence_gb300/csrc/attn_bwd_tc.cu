@@ -46,6 +46,7 @@ constexpr uint32_t SUB128 = 128 * 64 * 2;   // [128 rows][64 cols] bf16, 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned CODE_DKDV = KID_ATTN_BWD << 8;
 constexpr unsigned CODE_DQ = (KID_ATTN_BWD << 8) | 0x80;
+constexpr unsigned CODE_FUSED = (KID_ATTN_BWD << 8) | 0x40;
 
 struct BwdTcParams {
   int B, H, D;
@@ -54,7 +55,7 @@ struct BwdTcParams {
   int h;
   const float* lse;   // [B][H][S], natural log
   const float* dsum;  // [B][H][S]
-  __nv_bfloat16* dq;  // zigzag [T][h]
+  float* dq_acc;      // [B][H][S][dh] fp32, unscaled dS K sums
   __nv_bfloat16* dk;  // [B][H][S][dh]
   __nv_bfloat16* dv;
   unsigned int* err;
@@ -417,6 +418,412 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ===========================================================================
+// Fused dK, dV and dQ with 64-query blocks
+// ===========================================================================
+// Five MMA groups per block instead of the seven of the two kernels above
+// (scores and dP are not recomputed for dQ) and one exponential per score:
+//   S^T = K Q^T, dP^T = V dO^T            (M = 128 keys, N = 64 queries)
+//   dV += P^T dO, dK += dS^T Q            (P^T, dS^T from TMEM; N = head dim)
+//   dQ^T = K^T dS^T                       (M = head dim, N = 64 queries; K tile
+//                                          and dS^T both read MN-major from
+//                                          shared memory)
+// The dQ^T of a block is a partial sum over this CTA's 128 keys: the
+// elementwise warps read it out of TMEM and add it into an fp32 accumulator
+// [B][H][S][dh] with L2 reductions (zeroed beforehand; scaled by 1/sqrt(dh)
+// when it is assembled), so the summation order, and the last bit of dQ,
+// varies from run to run.  TMEM: S^T at 0 (P^T over its start), dP^T at 64,
+// dQ^T at 128, dS^T at 192, dV at 256, dK at 384.  MMA order per block
+//   [P(n)] dV(n), S(n+1), [dS(n)] dP(n+1), dK(n), dQ(n)
+// puts the next block's dP right behind the dS hand-off, so the elementwise
+// warps compute dS(n+1) while dK(n) and dQ(n) run; before they overwrite
+// dS^T (TMEM and shared memory) and read dQ^T(n) out they wait for the
+// commit that follows dQ(n), and they hand dS(n+1) over before adding
+// dQ^T(n) into memory.  The MMA warp is then limited by its own issue rate.
+constexpr int QBF = 64;
+constexpr int NSTGF = 4;
+constexpr uint32_t STGF_BYTES = 4 * SUB64;   // Q (2 sub-tiles [64][64]), dO (2)
+constexpr uint32_t LDF_BYTES = 2 * QBF * 4;  // lse, dsum of the block
+constexpr size_t FUSED_SMEM =
+    1024 + 4 * (size_t)SUB128 + NSTGF * (size_t)STGF_BYTES + SUB128 + NSTGF * (size_t)LDF_BYTES + 256;
+constexpr int kBarPF = 5, kBarDSF = 6;  // P and dS hand-offs (256 + 32 threads)
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_fused_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                             const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                             const BwdTcParams p, int nk) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ks = smem;                          // 2 x SUB128
+  uint8_t* Vs = smem + 2 * SUB128;             // 2 x SUB128
+  uint8_t* stg = smem + 4 * SUB128;            // [NSTGF] stages
+  uint8_t* dSs = stg + NSTGF * STGF_BYTES;     // dS^T [128 keys][64 queries], 128-byte swizzle
+  uint8_t* ldr = dSs + SUB128;                 // [NSTGF] lse, dsum
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ldr + NSTGF * LDF_BYTES);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_free = bars + 1;
+  uint64_t* q_full = bars + 2;   // [NSTGF]
+  uint64_t* q_free = bars + 6;   // [NSTGF]
+  uint64_t* s_full = bars + 10;  // S^T of the current block is in TMEM
+  uint64_t* dp_full = bars + 11; // dP^T of the current block is in TMEM
+  uint64_t* dq_full = bars + 12; // dQ^T of a block is in TMEM (and every earlier MMA is done)
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int grp = p.H / p.Hk;
+  const int64_t bkv = (int64_t)b * p.Hk + kvh;
+  auto tile_of = [&](int t) { return t == 0 ? (int)blockIdx.x : nk - 1 - (int)blockIdx.x; };
+  const int ntile = (nk - 1 - (int)blockIdx.x == (int)blockIdx.x) ? 1 : 2;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_free, 1);
+    for (int s = 0; s < NSTGF; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_free[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmdO);
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t qi = 0;
+      int kv_armed = 0;
+      bool ok = true;
+      for (int t = 0; t < ntile && ok; ++t) {
+        const int64_t k0 = (int64_t)tile_of(t) * 128;
+        if (!mbar_wait(kv_free, (t & 1) ^ 1, abort_flag, p.err, CODE_FUSED | 1)) break;
+        mbar_arrive_expect_tx(kv_full, 4 * SUB128);
+        ++kv_armed;
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(Ks + c * SUB128, &tmK, c * 64, (int)(bkv * p.S + k0), kv_full);
+          tma_load_2d(Vs + c * SUB128, &tmV, c * 64, (int)(bkv * p.S + k0), kv_full);
+        }
+        const int nq = (int)((p.S - k0) / QBF);
+        for (int u = 0; u < grp * nq; ++u, ++qi) {
+          const int i = u % nq;
+          const int head = kvh * grp + u / nq;
+          const int64_t bh = (int64_t)b * p.H + head;
+          const int s = qi % NSTGF;
+          if (!mbar_wait(&q_free[s], ((qi / NSTGF) & 1) ^ 1, abort_flag, p.err, CODE_FUSED | 2)) {
+            ok = false;
+            break;
+          }
+          const int64_t q0 = k0 + (int64_t)i * QBF;
+          const int64_t zr = zz_row(q0, p.C, p.D, p.B, b);  // a 64-query block never crosses a chunk
+          uint8_t* st = stg + s * STGF_BYTES;
+          uint8_t* ld = ldr + s * LDF_BYTES;
+          mbar_arrive_expect_tx(&q_full[s], STGF_BYTES + LDF_BYTES);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(st + c * SUB64, &tmQ, head * HD + c * 64, (int)zr, &q_full[s]);
+            tma_load_2d(st + 2 * SUB64 + c * SUB64, &tmdO, head * HD + c * 64, (int)zr, &q_full[s]);
+          }
+          bulk_load(ld, p.lse + bh * p.S + q0, QBF * 4, &q_full[s]);
+          bulk_load(ld + QBF * 4, p.dsum + bh * p.S + q0, QBF * 4, &q_full[s]);
+        }
+      }
+      volatile int dummy = 0;
+      const uint32_t first = qi > NSTGF ? qi - NSTGF : 0;
+      for (uint32_t n = first; n < qi; ++n)
+        mbar_wait(&q_full[n % NSTGF], (n / NSTGF) & 1, &dummy, p.err, CODE_FUSED | 3);
+      if (kv_armed) mbar_wait(kv_full, (kv_armed - 1) & 1, &dummy, p.err, CODE_FUSED | 3);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer (whole warp walks the schedule and issues; one elected lane) ----------------
+    constexpr uint32_t id_s = idesc_bf16_f32(128, QBF);                // M = keys, N = queries
+    constexpr uint32_t id_o = idesc_bf16_f32(128, HD, false, true);    // M = keys, N = head dim (B MN-major)
+    constexpr uint32_t id_q = idesc_bf16_f32(HD, QBF, true, true);     // M = head dim, N = queries (A, B MN-major)
+    uint32_t qi = 0;
+    bool ok = true;  // warp-uniform
+    auto stage = [&](uint32_t n) { return stg + (n % NSTGF) * STGF_BYTES; };
+    auto scores = [&](uint32_t n) {  // S^T = K Q^T
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
+        umma_bf16_warp(tmem_base, ak, bq, id_s, k > 0);
+      }
+      umma_commit_warp(s_full);
+    };
+    auto dpscores = [&](uint32_t n) {  // dP^T = V dO^T
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
+        const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
+        umma_bf16_warp(tmem_base + 64, av, bo, id_s, k > 0);
+      }
+      umma_commit_warp(dp_full);
+    };
+    // dV += P^T dO and dK += dS^T Q: the stage's dO / Q tiles as MN-major B
+    // operands (rows = queries = K dimension; 64-column chunks SUB64 apart).
+    // P^T of queries 32x..32x+31 sits in columns 32x..32x+15 of the S^T region;
+    // dS^T is packed contiguously (queries 2c, 2c+1 in column 192 + c).
+    auto accum_v = [&](uint32_t n, bool acc) {
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < QBF / 16; ++k) {
+        const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB64) + 2048 * k, SUB64);
+        umma_bf16_ts_warp(tmem_base + 256, tmem_base + 32 * (k / 2) + 8 * (k % 2), bo, id_o,
+                          (acc || k > 0) ? 1u : 0u);
+      }
+    };
+    auto accum_kq = [&](uint32_t n, bool acc) {
+      uint8_t* st = stage(n);
+#pragma unroll
+      for (int k = 0; k < QBF / 16; ++k) {
+        const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
+        umma_bf16_ts_warp(tmem_base + 384, tmem_base + 192 + 8 * k, bq, id_o, (acc || k > 0) ? 1u : 0u);
+      }
+      // dQ^T = K^T dS^T: the K tile (rows = keys, head-dim chunks SUB128 apart) as
+      // the MN-major A operand, dS^T (rows = keys, 64 queries) as the MN-major B
+#pragma unroll
+      for (int k = 0; k < 128 / 16; ++k) {
+        const uint64_t ak = sdesc_mn_sw128(smem_u32(Ks) + 2048 * k, SUB128);
+        const uint64_t bs = sdesc_mn_sw128(smem_u32(dSs) + 2048 * k, SUB128);
+        umma_bf16_warp(tmem_base + 128, ak, bs, id_q, k > 0);
+      }
+      umma_commit_warp(dq_full);
+      umma_commit_warp(&q_free[n % NSTGF]);
+    };
+    auto sync_on = [&](int id, int count) {
+      __syncwarp();
+      named_bar_sync(id, count);
+      tc_fence_after();
+    };
+    for (int t = 0; t < ntile; ++t) {
+      const int64_t k0 = (int64_t)tile_of(t) * 128;
+      const int nq = grp * (int)((p.S - k0) / QBF);  // query blocks of all the group's heads
+      if (ok) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(kv_full, t & 1, abort_flag, p.err, CODE_FUSED | 4);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      }
+      sync_on(kBarStage + (qi & 3), kStageThreads);
+      if (ok) {
+        scores(qi);
+        dpscores(qi);
+      }
+      for (int i = 0; i < nq; ++i) {
+        const uint32_t n = qi + i;
+        sync_on(kBarPF, kDSThreads);  // P^T(n) in TMEM
+        if (ok) accum_v(n, i > 0);
+        if (i + 1 < nq) {
+          sync_on(kBarStage + ((n + 1) & 3), kStageThreads);
+          if (ok) scores(n + 1);
+        }
+        sync_on(kBarDSF, kDSThreads);  // dS^T(n) in TMEM and shared memory, dQ^T(n-1) read out
+        if (ok) {
+          if (i + 1 < nq) dpscores(n + 1);
+          accum_kq(n, i > 0);
+        }
+      }
+      if (ok) umma_commit_warp(kv_free);
+      qi += nq;
+    }
+    umma_commit_warp(drain);
+    if (lane == 0) {
+      volatile int dummy = 0;
+      mbar_wait(drain, 0, &dummy, p.err, CODE_FUSED | 7);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ---------------- relay: announces each landed stage to the MMA warp ----------------
+    uint32_t n = 0;
+    for (int t = 0; t < ntile; ++t) {
+      const int nq = grp * (int)((p.S - (int64_t)tile_of(t) * 128) / QBF);
+      for (int i = 0; i < nq; ++i, ++n) {
+        if (lane == 0) mbar_wait(&q_full[n % NSTGF], (n / NSTGF) & 1, abort_flag, p.err, CODE_FUSED | 9);
+        __syncwarp();
+        named_bar_sync(kBarStage + (n & 3), kStageThreads);
+      }
+    }
+  } else {
+    // ------- elementwise warps 0-7: one key row, 32 of the 64 query columns per thread -------
+    // (for dQ^T the TMEM lane is a head-dim index instead: the thread adds
+    // column d = its row of the 32 queries it covers)
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t cS = tmem_base + lane_off + 32 * half;
+    const uint32_t cdP = tmem_base + lane_off + 64 + 32 * half;
+    const uint32_t cdQ = tmem_base + lane_off + 128 + 32 * half;
+    const uint32_t cdS = tmem_base + lane_off + 192 + 16 * half;
+    const float sl2 = kLog2e * rsqrtf((float)HD);
+    const float scale = rsqrtf((float)HD);
+    uint8_t* ds_row = dSs + row * 128;
+    uint32_t cnt = 0;   // blocks processed (phase of s_full / dp_full; ring slot = cnt % NSTGF)
+    bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
+    auto add_dq = [&](float* dst, const float (&a)[32]) {  // a block's dQ^T column -> fp32 accumulator
+#pragma unroll
+      for (int c = 0; c < 32; ++c) red_add_f32(dst + (int64_t)c * HD, a[c]);
+    };
+    for (int t = 0; t < ntile; ++t) {
+      const int64_t k0 = (int64_t)tile_of(t) * 128;
+      const int nqh = (int)((p.S - k0) / QBF);
+      const int64_t key = k0 + row;
+      float* dq_prev = nullptr;  // accumulator column of the previous block of this tile
+      for (int u = 0; u < grp * nqh; ++u, ++cnt) {
+        const int i = u % nqh;  // query block within the head
+        const int head = kvh * grp + u / nqh;
+        const int64_t q0 = k0 + (int64_t)i * QBF + 32 * half;  // query of this thread's first column
+        // ---- P phase ----
+        bool got = alive && mbar_wait(s_full, cnt & 1, abort_flag, p.err, CODE_FUSED | 8);
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) {
+          named_bar_sync(kBarPF, kDSThreads);
+          named_bar_sync(kBarDSF, kDSThreads);
+          continue;
+        }
+        tc_fence_after();
+        uint32_t sa[32];
+        tmem_ld32_issue(cS, sa);
+        const float4* lse4 = reinterpret_cast<const float4*>(ldr + (cnt % NSTGF) * LDF_BYTES) + 8 * half;
+        const float4* ds4 = lse4 + QBF / 4;
+        const bool diag = i < 2;  // the two blocks that overlap the key tile
+        float pv[32];
+        tmem_wait_ld32(sa);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = lse4[c4];
+          const float lv[4] = {l4.x * kLog2e, l4.y * kLog2e, l4.z * kLog2e, l4.w * kLog2e};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 * 4 + e;
+            float pe = ex2f(fmaf(__uint_as_float(sa[c]), sl2, -lv[e]));
+            if (diag && q0 + c < key) pe = 0.f;
+            pv[c] = pe;
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+        tmem_st16_nowait(cS, pk);  // P^T over the start of this thread's S^T columns
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        named_bar_arrive(kBarPF, kDSThreads);
+        // ---- dS phase ----
+        got = mbar_wait(dp_full, cnt & 1, abort_flag, p.err, CODE_FUSED | 11);
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) {
+          named_bar_sync(kBarDSF, kDSThreads);
+          continue;
+        }
+        tc_fence_after();
+        tmem_ld32_issue(cdP, sa);
+        tmem_wait_ld32(sa);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = ds4[c4];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 * 4 + e;
+            pv[c] = pv[c] * (__uint_as_float(sa[c]) - dv[e]);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+        // dK(n-1) and dQ(n-1) must be done with dS^T(n-1) before it is overwritten
+        float qa[32];
+        if (dq_prev != nullptr) {
+          got = mbar_wait(dq_full, (cnt - 1) & 1, abort_flag, p.err, CODE_FUSED | 12);
+          alive = __all_sync(0xffffffffu, got);
+          if (!alive) {
+            named_bar_sync(kBarDSF, kDSThreads);
+            continue;
+          }
+          tc_fence_after();
+          tmem_ld32(cdQ, qa);  // dQ^T(n-1), added to memory after the hand-off
+        }
+        tmem_st16_nowait(cdS, pk);
+        // dS^T row for the dQ MMA: 16-byte chunks 4*half..4*half+3 of the
+        // key's 128-byte row, XOR-swizzled by the row within its 8-row group
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int chunk = 4 * half + j;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        named_bar_arrive(kBarDSF, kDSThreads);
+        if (dq_prev != nullptr) add_dq(dq_prev, qa);
+        dq_prev = p.dq_acc + (((int64_t)b * p.H + head) * p.S + q0) * HD + row;
+      }
+      if (!alive) continue;
+      // the tile's last dQ (its commit also covers the last dK, dV)
+      const bool got = mbar_wait(dq_full, (cnt - 1) & 1, abort_flag, p.err, CODE_FUSED | 10);
+      alive = __all_sync(0xffffffffu, got);
+      if (!alive) continue;
+      tc_fence_after();
+      {
+        float qa[32];
+        tmem_ld32(cdQ, qa);
+        add_dq(dq_prev, qa);
+      }
+      uint4* dvrow = reinterpret_cast<uint4*>(p.dv + (bkv * p.S + key) * HD) + 8 * half;
+      uint4* dkrow = reinterpret_cast<uint4*>(p.dk + (bkv * p.S + key) * HD) + 8 * half;
+#pragma unroll 1
+      for (int c32 = 0; c32 < 2; ++c32) {
+        float a[32], d[32];
+        tmem_ld32(tmem_base + lane_off + 256 + 64 * half + 32 * c32, a);
+        tmem_ld32(tmem_base + lane_off + 384 + 64 * half + 32 * c32, d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dvrow[c32 * 4 + q] = make_uint4(pack_bf16x2(a[q * 8 + 0], a[q * 8 + 1]), pack_bf16x2(a[q * 8 + 2], a[q * 8 + 3]),
+                                          pack_bf16x2(a[q * 8 + 4], a[q * 8 + 5]), pack_bf16x2(a[q * 8 + 6], a[q * 8 + 7]));
+          dkrow[c32 * 4 + q] = make_uint4(
+              pack_bf16x2(d[q * 8 + 0] * scale, d[q * 8 + 1] * scale), pack_bf16x2(d[q * 8 + 2] * scale, d[q * 8 + 3] * scale),
+              pack_bf16x2(d[q * 8 + 4] * scale, d[q * 8 + 5] * scale), pack_bf16x2(d[q * 8 + 6] * scale, d[q * 8 + 7] * scale));
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ===========================================================================
 // dQ
 // ===========================================================================
 constexpr int DQ_KB = 64;  // keys per block
@@ -616,7 +1023,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = kLog2e * rsqrtf((float)HD);
-    const float scale = rsqrtf((float)HD);
     uint32_t scnt[2] = {0, 0};
     bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
     for (int t = 0; t < 2; ++t) {
@@ -662,16 +1068,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       alive = __all_sync(0xffffffffu, got);
       if (!alive) continue;
       tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(p.dq + (zrow0 + row) * p.h + head * HD) + 8 * half;
+      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (bh * p.S + qpos) * HD + 64 * half);
 #pragma unroll 1
       for (int c32 = 0; c32 < 2; ++c32) {
         float a[32];
         tmem_ld32(tmem_base + lane_off + 256 + 64 * half + 32 * c32, a);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[c32 * 4 + q] = make_uint4(
-              pack_bf16x2(a[q * 8 + 0] * scale, a[q * 8 + 1] * scale), pack_bf16x2(a[q * 8 + 2] * scale, a[q * 8 + 3] * scale),
-              pack_bf16x2(a[q * 8 + 4] * scale, a[q * 8 + 5] * scale), pack_bf16x2(a[q * 8 + 6] * scale, a[q * 8 + 7] * scale));
+        for (int q = 0; q < 8; ++q) dst[c32 * 8 + q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
       }
       tc_fence_before();
     }
@@ -706,7 +1109,9 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
     if (cudaFuncSetAttribute(attn_dkdv128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)DKDV2_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(attn_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)FUSED_SMEM) != cudaSuccess)
       return TSP_ERR_CUDA;
     mark_setup_done(configured);
   }
@@ -720,12 +1125,16 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
   p.h = h;
   p.lse = a.lse;
   p.dsum = a.dsum;
-  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.dq_acc = a.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = dev_error_word();
   const int nk = (int)(a.S / 128);
   dim3 g1((nk + 1) / 2, a.Hk, a.B);
+  if (which & 4) {
+    attn_bwd_fused_tc_kernel<<<g1, THREADS, FUSED_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk);
+    if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
+  }
   if (which & 1) {
     attn_dkdv128_tc_kernel<<<g1, THREADS, DKDV2_SMEM, stream>>>(mK128, mV128, mQ128, mdO128, p, nk);
     if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;

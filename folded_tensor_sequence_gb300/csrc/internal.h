@@ -19,6 +19,7 @@ struct tsp_plan {
   int ffn;
   tsp_dtype dtype;
   int64_t chunk;  // seq / (2D)
+  int deterministic = 0;  // backward: split dK/dV and dQ kernels (bitwise reproducible) instead of the fused one
 };
 
 namespace tsp {
@@ -127,8 +128,9 @@ struct AttnBwdParams {
 };
 tsp_status attn_bwd_bf16(const AttnBwdParams& p, cudaStream_t stream);
 // dsum[b][head][p] = rowsum(dO * O) (fp32), the softmax-Jacobian row term of the backward.
+// dq_zero (optional): an fp32 [B][H][S][dh] buffer zeroed in the same pass.
 cudaError_t launch_attn_dsum(const void* o, const void* dO, float* dsum, int D, int B, int H, int64_t S, int64_t C,
-                             cudaStream_t stream);
+                             cudaStream_t stream, float* dq_zero = nullptr);
 
 // tcgen05 attention backward (head_dim 128, chunk % 128 == 0).
 struct AttnBwdTcArgs {
@@ -138,7 +140,8 @@ struct AttnBwdTcArgs {
   const void* dO;   // zigzag [T][h]
   const float* lse;
   const float* dsum;
-  void* dq;
+  float* dq_acc;    // [B][H][S][dh] fp32, unscaled sum of dS K (1/sqrt(dh) is applied when assembled);
+                    // the fused kernel adds into it (zero it first), the dQ kernel overwrites it
   void* dk;         // [B][Hk][S][dh]: summed over the query heads that read the K/V head
   void* dv;
   int D, B, H, dh;
@@ -146,13 +149,18 @@ struct AttnBwdTcArgs {
   int Hk;
 };
 bool attn_bwd_tc_supported(int head_dim, int64_t chunk);
-// which: 1 = the dK/dV kernel, 2 = the dQ kernel, 3 = both.
+// which: 1 = the dK/dV kernel, 2 = the dQ kernel (3 = both: bitwise reproducible),
+// 4 = the fused dK/dV/dQ kernel (dQ summed with fp32 L2 reductions).
 tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int which = 3);
 
 // Backward helpers.
 // dqkv [T][h + 2*Hk*dh] in the packed column order <- dq zigzag [T][h], dk/dv [B][Hk][S][dh].
 cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv, void* dqkv, int D, int B,
                                  int64_t S, int H, int Hk, int dh, cudaStream_t stream);
+// The same with dQ taken from the tensor-core backward's fp32 accumulator
+// [B][H][S][dh] (times `scale`) instead of a bf16 zigzag [T][h] buffer.
+cudaError_t launch_assemble_dqkv_f32q(const float* dq_acc, float scale, const void* dk, const void* dv, void* dqkv,
+                                      int D, int B, int64_t S, int H, int Hk, int dh, cudaStream_t stream);
 
 // Decode step (bf16; batch 1..8; head_dim 128; H / Hk in {1, 2, 4, 8}).
 size_t decode_ws_bytes(const tsp_plan* p, int batch);

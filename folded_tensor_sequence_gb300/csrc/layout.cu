@@ -114,6 +114,44 @@ __global__ void assemble_dqkv_kernel(const uint4* __restrict__ dq, const uint4* 
   }
 }
 
+// As above with dQ read from an fp32 [B][H][S][dh] accumulator and scaled.
+__global__ void assemble_dqkv_f32q_kernel(const float4* __restrict__ dq, float scale, const uint4* __restrict__ dk,
+                                          const uint4* __restrict__ dv, uint4* __restrict__ out, int vec_per_head,
+                                          int D, int B, int64_t S, int H, int Hk) {
+  const int64_t C = S / (2 * D);
+  const int64_t twoC = 2 * C;
+  const int64_t zrow = blockIdx.x;
+  const int64_t r = zrow / (B * twoC);
+  const int64_t rem = zrow - r * (B * twoC);
+  const int64_t b = rem / twoC;
+  const int64_t kk = rem - b * twoC;
+  const int64_t p = zigzag_pos(r, kk, C, D);
+  const int qs = (H / D) * vec_per_head;
+  const int ks = (Hk / D) * vec_per_head;
+  const int row_vecs = (H + 2 * Hk) * vec_per_head;
+  uint4* out_row = out + zrow * (int64_t)row_vecs;
+  for (int cv = threadIdx.x; cv < row_vecs; cv += blockDim.x) {
+    const int s = cv / (qs + 2 * ks);
+    const int within = cv - s * (qs + 2 * ks);
+    const int which = within < qs ? 0 : (within < qs + ks ? 1 : 2);
+    const int cin = within - (which == 0 ? 0 : qs + (which - 1) * ks);
+    const int d = cin % vec_per_head;
+    uint4 v;
+    if (which == 0) {
+      const int head = s * (H / D) + cin / vec_per_head;
+      const float4* src = dq + (((b * H + head) * S + p) * vec_per_head + d) * 2;  // 8 floats per vector
+      const float4 lo = __ldg(src), hi = __ldg(src + 1);
+      v = make_uint4(pack_bf16x2(lo.x * scale, lo.y * scale), pack_bf16x2(lo.z * scale, lo.w * scale),
+                     pack_bf16x2(hi.x * scale, hi.y * scale), pack_bf16x2(hi.z * scale, hi.w * scale));
+    } else {
+      const int head = s * (Hk / D) + cin / vec_per_head;
+      const int64_t g = ((b * Hk + head) * S + p) * vec_per_head + d;
+      v = __ldg(which == 1 ? &dk[g] : &dv[g]);
+    }
+    out_row[cv] = v;
+  }
+}
+
 // 32x32 tiles through shared memory, element type T (used for 4-byte elements).
 template <typename T>
 __global__ void transpose_kernel(const T* __restrict__ src, T* __restrict__ dst, int64_t rows, int64_t cols) {
@@ -286,6 +324,18 @@ cudaError_t launch_assemble_dqkv(const void* dq, const void* dk, const void* dv,
   assemble_dqkv_kernel<<<(unsigned)T, 256, 0, stream>>>(static_cast<const uint4*>(dq), static_cast<const uint4*>(dk),
                                                          static_cast<const uint4*>(dv), static_cast<uint4*>(dqkv),
                                                          vph, D, B, S, H, Hk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assemble_dqkv_f32q(const float* dq_acc, float scale, const void* dk, const void* dv, void* dqkv,
+                                      int D, int B, int64_t S, int H, int Hk, int dh, cudaStream_t stream) {
+  const int vph = dh * 2 / 16;
+  const int64_t T = (int64_t)B * S;
+  if (T == 0) return cudaSuccess;
+  assemble_dqkv_f32q_kernel<<<(unsigned)T, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc), scale,
+                                                              static_cast<const uint4*>(dk),
+                                                              static_cast<const uint4*>(dv),
+                                                              static_cast<uint4*>(dqkv), vph, D, B, S, H, Hk);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ EXPORTS = [
     "tsp_zigzag_unpermute", "tsp_kv_gather", "tsp_attention_fwd", "tsp_gated_mlp_fwd", "tsp_layer_fwd",
     "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next", "tsp_profile_enable", "tsp_profile_report",
     "tsp_attention_fwd_static", "tsp_debug_wait_timeout", "tsp_plan_create_gqa", "tsp_decode_step",
+    "tsp_plan_set_deterministic", "tsp_plan_get_deterministic",
 ]
 
 
@@ -60,6 +61,9 @@ def lib() -> ctypes.CDLL:
         L.tsp_plan_create_gqa.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
         L.tsp_plan_destroy.argtypes = [vp]
         L.tsp_plan_destroy.restype = None
+        L.tsp_plan_set_deterministic.argtypes = [vp, i32]
+        L.tsp_plan_get_deterministic.argtypes = [vp]
+        L.tsp_plan_get_deterministic.restype = i32
         L.tsp_workspace_bytes.argtypes = [vp, i32, i32]
         L.tsp_workspace_bytes.restype = sz
         L.tsp_saved_bytes.argtypes = [vp, i32]
@@ -158,6 +162,14 @@ def tsp_plan_create_gqa(D: int, seq: int, hidden: int, heads: int, kv_heads: int
     _check(lib().tsp_plan_create_gqa(D, seq, hidden, heads, kv_heads, head_dim, ffn, dtype, ctypes.byref(out)),
            "tsp_plan_create_gqa")
     return Plan(out.value, D, seq, hidden, heads, head_dim, ffn, dtype, kv_heads)
+
+
+def tsp_plan_set_deterministic(plan: Plan, deterministic: int) -> None:
+    _check(lib().tsp_plan_set_deterministic(plan.handle, deterministic), "tsp_plan_set_deterministic")
+
+
+def tsp_plan_get_deterministic(plan: Plan) -> int:
+    return lib().tsp_plan_get_deterministic(plan.handle)
 
 
 def plan_for(cfg) -> Plan:

@@ -97,7 +97,8 @@ typedef enum {
   TSP_OP_DECODE = 4
 } tsp_op;
 
-/* Opaque, host-only, immutable after creation; safe to share between threads. */
+/* Opaque and host-only.  Configure it (tsp_plan_set_deterministic) before
+ * sharing it; from then on it is read-only and safe to share between threads. */
 typedef struct tsp_plan tsp_plan;
 
 /* Packed weights (device pointers, layouts above). */
@@ -133,6 +134,17 @@ tsp_status tsp_plan_create(int D, int64_t seq, int hidden, int heads, int head_d
 tsp_status tsp_plan_create_gqa(int D, int64_t seq, int hidden, int heads, int kv_heads, int head_dim, int ffn,
                                tsp_dtype dtype, tsp_plan** out);
 void tsp_plan_destroy(tsp_plan* plan);
+/* Attention backward algorithm of tsp_layer_bwd (tensor-core path: bf16,
+ * head_dim 128, seq/(2D) % 128 == 0).  0 (the default): one fused kernel per
+ * 128-key tile computes dK, dV and the tile's share of dQ, and the shares are
+ * summed with fp32 reductions in L2, whose order varies, so dQ -- and dx and
+ * the Q rows of dW_QKV through it -- can differ in the last bits from run to
+ * run.  1: separate dK/dV and dQ kernels (the dQ kernel recomputes the scores
+ * and dP), slower but bitwise reproducible.  Anything else:
+ * TSP_ERR_INVALID_ARG.  Not thread-safe: call before the plan is shared. */
+tsp_status tsp_plan_set_deterministic(tsp_plan* plan, int deterministic);
+/* The setting above (0 or 1), or -1 for a NULL plan. */
+int tsp_plan_get_deterministic(const tsp_plan* plan);
 
 /* Workspace bytes needed by `op` for `batch` sequences (0 on invalid input). */
 size_t tsp_workspace_bytes(const tsp_plan* plan, int batch, tsp_op op);

@@ -148,3 +148,21 @@ def test_gqa_backward_needs_128_query_chunks(tsp):
                          1 << 40, None)
     assert st == tsp.TSP_ERR_UNSUPPORTED
     assert "grouped-query" in tsp.tsp_last_error_message()
+
+
+def test_deterministic_setting(tsp):
+    p = tsp.tsp_plan_create(8, 16384, 4096, 32, 128, 14336, "bf16")
+    assert tsp.tsp_plan_get_deterministic(p) == 0  # fused backward by default
+    tsp.tsp_plan_set_deterministic(p, 1)
+    assert tsp.tsp_plan_get_deterministic(p) == 1
+    for bad in (-1, 2, 7):
+        with pytest.raises(tsp.TspError) as ei:
+            tsp.tsp_plan_set_deterministic(p, bad)
+        assert ei.value.status == tsp.TSP_ERR_INVALID_ARG
+    assert tsp.tsp_plan_get_deterministic(p) == 1
+    L = tsp.lib()
+    assert L.tsp_plan_set_deterministic(None, 1) == tsp.TSP_ERR_INVALID_ARG
+    assert L.tsp_plan_get_deterministic(None) == -1
+    # the backward workspace holds the fp32 dQ accumulator (T x h x 4 bytes) either way
+    T, h = 2 * 16384, 4096
+    assert tsp.tsp_workspace_bytes(p, 2, tsp.TSP_OP_LAYER_BWD) >= T * h * 4

@@ -6,7 +6,7 @@ from folded_tensor_sequence_gb300 import synth
 from folded_tensor_sequence_gb300.configs import LayerConfig
 from oracle import tsp_oracle as O
 
-from helpers import check, to_dev, to_np
+from helpers import check, rel_frob, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -21,11 +21,12 @@ def tsp():
     return T
 
 
-def run_bwd(tsp, cfg, inp):
+def run_bwd(tsp, cfg, inp, deterministic=0):
     import torch
 
     B = cfg.batch
     plan = tsp.tsp_plan_create(cfg.D, cfg.seq, cfg.hidden, cfg.heads, cfg.head_dim, cfg.ffn, cfg.dtype)
+    tsp.tsp_plan_set_deterministic(plan, deterministic)
     canon = {k: to_dev(inp[k], cfg.dtype) for k in tsp.CANONICAL}
     packed = tsp.empty_packed(plan)
     tsp.tsp_pack_weights(plan, canon, packed)
@@ -54,11 +55,20 @@ BWD_CASES = [
 ]
 
 
-@pytest.mark.parametrize("cfg", BWD_CASES, ids=lambda c: c.name)
-def test_backward_matches_oracle(tsp, cfg):
+def tc_case(cfg):
+    """Chunks that are multiples of 128 take the tensor-core backward (fused or split)."""
+    return (cfg.seq // (2 * cfg.D)) % 128 == 0
+
+
+# (case, deterministic): the tensor-core cases run both backward algorithms
+MODE_CASES = [(c, m) for c in BWD_CASES for m in ((0, 1) if tc_case(c) else (0,))]
+
+
+@pytest.mark.parametrize("cfg,det", MODE_CASES, ids=lambda v: v.name if hasattr(v, "name") else f"det{v}")
+def test_backward_matches_oracle(tsp, cfg, det):
     inp = synth.layer_inputs(cfg, seed=5, with_dy=True)
     w = {k: inp[k] for k in tsp.CANONICAL}
-    y, dx, g = run_bwd(tsp, cfg, inp)
+    y, dx, g = run_bwd(tsp, cfg, inp, deterministic=det)
     ref_y = O.layer_fwd(inp["x"], w, cfg.heads)["Y"]
     check(y, ref_y, "bf16", f"{cfg.name} Y")
     rdx, rg = O.layer_bwd(inp["x"], w, cfg.heads, inp["dY"])
@@ -67,20 +77,40 @@ def test_backward_matches_oracle(tsp, cfg):
         check(g[k], rg[k], "bf16", f"{cfg.name} d{k}")
 
 
-def test_forward_and_backward_are_bitwise_deterministic(tsp):
-    """No kernel uses atomics, so repeated runs must agree bit for bit; a
-    barrier or ordering race would show up here as run-to-run differences."""
-    import torch
-
-    cfg = LayerConfig("det_D8_s4096", D=8, batch=1, seq=4096, hidden=1024, heads=8, head_dim=128, ffn=1024,
+DET_CFG = LayerConfig("det_D8_s4096", D=8, batch=1, seq=4096, hidden=1024, heads=8, head_dim=128, ffn=1024,
                       dtype="bf16")
-    inp = synth.layer_inputs(cfg, seed=9, with_dy=True)
-    runs = []
-    for _ in range(3):
-        y, dx, g = run_bwd(tsp, cfg, inp)
-        runs.append((y, dx, g))
+
+
+def test_forward_and_backward_are_bitwise_deterministic(tsp):
+    """With the split backward no kernel uses atomics, so repeated runs must
+    agree bit for bit; a barrier or ordering race would show up here as
+    run-to-run differences."""
+    inp = synth.layer_inputs(DET_CFG, seed=9, with_dy=True)
+    runs = [run_bwd(tsp, DET_CFG, inp, deterministic=1) for _ in range(3)]
     for y, dx, g in runs[1:]:
         assert np.array_equal(y, runs[0][0])
         assert np.array_equal(dx, runs[0][1])
         for k in g:
             assert np.array_equal(g[k], runs[0][2][k]), k
+
+
+def test_fused_backward_repeats(tsp):
+    """The fused backward sums dQ with fp32 reductions in varying order: what
+    does not depend on dQ (Y, dK, dV and so dWk, dWv, and the MLP and output
+    projection gradients) must still repeat bit for bit, dx and dWq only up
+    to rounding; and the two algorithms must agree."""
+    inp = synth.layer_inputs(DET_CFG, seed=9, with_dy=True)
+    runs = [run_bwd(tsp, DET_CFG, inp, deterministic=0) for _ in range(3)]
+    exact = ["Wk", "Wv", "Wo", "Wg", "Wu", "Wd"]
+    for y, dx, g in runs[1:]:
+        assert np.array_equal(y, runs[0][0])
+        for k in exact:
+            assert np.array_equal(g[k], runs[0][2][k]), k
+        assert rel_frob(dx, runs[0][1]) <= 1e-3
+        assert rel_frob(g["Wq"], runs[0][2]["Wq"]) <= 1e-3
+    y1, dx1, g1 = run_bwd(tsp, DET_CFG, inp, deterministic=1)
+    assert rel_frob(dx1, runs[0][1]) <= 5e-3
+    for k in g1:
+        e = rel_frob(g1[k], runs[0][2][k])
+        print(f"PARITY fused vs split d{k}: relative Frobenius {e:.3e}")
+        assert e <= 5e-3, (k, e)

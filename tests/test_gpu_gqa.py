@@ -26,11 +26,12 @@ def tsp():
     return T
 
 
-def run(tsp, cfg, inp, backward=False):
+def run(tsp, cfg, inp, backward=False, deterministic=0):
     import torch
 
     B = cfg.batch
     plan = tsp.plan_for(cfg)
+    tsp.tsp_plan_set_deterministic(plan, deterministic)
     canon = {k: to_dev(inp[k], cfg.dtype) for k in tsp.CANONICAL}
     packed = tsp.empty_packed(plan)
     tsp.tsp_pack_weights(plan, canon, packed)
@@ -96,11 +97,12 @@ BWD = [
 ]
 
 
+@pytest.mark.parametrize("det", [0, 1], ids=["fused", "split"])
 @pytest.mark.parametrize("cfg", BWD, ids=lambda c: c.name)
-def test_gqa_backward_matches_oracle(tsp, cfg):
+def test_gqa_backward_matches_oracle(tsp, cfg, det):
     inp = synth.layer_inputs(cfg, seed=22, with_dy=True)
     w = {k: inp[k] for k in tsp.CANONICAL}
-    got = run(tsp, cfg, inp, backward=True)
+    got = run(tsp, cfg, inp, backward=True, deterministic=det)
     rdx, rg, ry = O.layer_bwd(inp["x"], w, cfg.heads, inp["dY"], return_y=True)
     check(got["Y"], ry, "bf16", f"{cfg.name} Y")
     check(got["dx"], rdx, "bf16", f"{cfg.name} dx")
