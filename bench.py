@@ -47,6 +47,7 @@ NCU_TRAFFIC = {
     "gate/up projection": (2.16e9 + 0.927e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "44dc85bc6217b676"),
     "attention": (0.844e9 + 0.254e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "0592c9391e74232b"),
     # training step at batch 2 x 16384 tokens
+    "attention bwd fused": (0.0, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "pending"),
     "attention bwd dK/dV": (1.09e9 + 0.506e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "c7f7236ef083c6e7"),
     "attention bwd dQ": (1.09e9 + 0.251e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "c7f7236ef083c6e7"),
     # decode step, batch 1, 128K-token cache
