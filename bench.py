@@ -44,14 +44,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # counters were taken (one-pass capture of the full-size launch, see
 # profiles/); if the source has changed since, the traffic is reported as null.
 NCU_TRAFFIC = {
-    "gate/up projection": (2.16e9 + 0.927e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "44dc85bc6217b676"),
-    "attention": (0.844e9 + 0.254e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "0592c9391e74232b"),
+    # layer forward at batch 2 x 16384 tokens
+    "gate/up projection": (2.16e9 + 0.924e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "17ccb880b0bf301b"),
+    "attention": (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
     # training step at batch 2 x 16384 tokens
-    "attention bwd fused": (0.0, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "pending"),
-    "attention bwd dK/dV": (1.09e9 + 0.506e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "c7f7236ef083c6e7"),
-    "attention bwd dQ": (1.09e9 + 0.251e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "c7f7236ef083c6e7"),
+    "attention bwd fused": (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "b2445bd5bb872aae"),
     # decode step, batch 1, 128K-token cache
-    "decode attention": (2.148e9 + 0.0034e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "7843f3cdd81c9f5e"),
+    "decode attention": (2.15e9 + 0.00315e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "25dde6d76c0177c8"),
 }
 
 
