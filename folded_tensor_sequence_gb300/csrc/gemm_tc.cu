@@ -245,6 +245,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       tile_coords(t, shape, mt, nt);
       const int acc = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
+      if constexpr (EPI == EPI_DSWIGLU) {
+        // The tile's 256 dM columns are two packed 128-column gate/up blocks:
+        // 1 KB of saved G|U per row, contiguous.  Pull it into L2 while the
+        // tile's main loop runs.
+        const int64_t mp = (int64_t)mt * BM + row;
+        if (mp < shape.M) {
+          const char* src = reinterpret_cast<const char*>(reinterpret_cast<const __nv_bfloat16*>(ep.resid) +
+                                                          mp * ep.ldr + (int64_t)nt * 2 * BN);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * i));
+        }
+      }
       // Warp-uniform decision: tcgen05.ld below needs every lane of the warp.
       const bool got = mbar_wait(&tfull[acc], aph, abort_flag, ep.err, (KID_GEMM_TC << 8) | 6);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -269,6 +281,70 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < 32; ++i) o[i] = silu_f(g[i]) * u[i];
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + (int64_t)nt * (BN / 2);
             store32_bf16(out + c * 32, o);
+          }
+        }
+      } else if constexpr (EPI == EPI_DSWIGLU) {
+        // acc = dM[m][f]; dG = dM * u * s * (1 + g (1 - s)), dU = dM * g * s with s = sigmoid(g),
+        // read from and written to the packed gate_up order.  Chunk c+1's G/U
+        // are loaded before chunk c is computed.
+        const __nv_bfloat16* gu = reinterpret_cast<const __nv_bfloat16*>(ep.resid) + m * ep.ldr;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo;
+        auto gcol_of = [&](int c) {
+          const int64_t n = (int64_t)nt * BN + c * 32;
+          return (n / 128) * 256 + n % 128;
+        };
+        uint4 gcur[4], ucur[4];
+        if (valid) {
+          const uint4* gs = reinterpret_cast<const uint4*>(gu + gcol_of(0));
+          const uint4* us = reinterpret_cast<const uint4*>(gu + gcol_of(0) + 128);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            gcur[i] = gs[i];
+            ucur[i] = us[i];
+          }
+        }
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          if (!valid) continue;
+          uint4 gnx[4], unx[4];
+          if (c + 1 < BN / 32) {
+            const uint4* gs = reinterpret_cast<const uint4*>(gu + gcol_of(c + 1));
+            const uint4* us = reinterpret_cast<const uint4*>(gu + gcol_of(c + 1) + 128);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              gnx[i] = gs[i];
+              unx[i] = us[i];
+            }
+          }
+          float dg[32], du[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t gw[4] = {gcur[i].x, gcur[i].y, gcur[i].z, gcur[i].w};
+            const uint32_t uw[4] = {ucur[i].x, ucur[i].y, ucur[i].z, ucur[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 g2 = unpack_bf16x2(gw[j]), u2 = unpack_bf16x2(uw[j]);
+              const float gg[2] = {g2.x, g2.y}, uu[2] = {u2.x, u2.y};
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int k = 8 * i + 2 * j + e;
+                const float sg = 1.0f / (1.0f + __expf(-gg[e]));
+                du[k] = v[k] * gg[e] * sg;
+                dg[k] = v[k] * uu[e] * sg * (1.0f + gg[e] * (1.0f - sg));
+              }
+            }
+          }
+          const int64_t gcol = gcol_of(c);
+          store32_bf16(out + gcol, dg);
+          store32_bf16(out + gcol + 128, du);
+          if (c + 1 < BN / 32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              gcur[i] = gnx[i];
+              ucur[i] = unx[i];
+            }
           }
         }
       } else {
@@ -316,24 +392,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) dst[(int64_t)i * ep.S] = __float2bfloat16_rn(v[i]);
             }
-          } else if constexpr (EPI == EPI_DSWIGLU) {
-            // n indexes F; the saved G/U and the dGU output use the packed gate_up order.
-            const int64_t blk = n / 128, off = n % 128;
-            const int64_t gcol = blk * 256 + off, ucol = gcol + 128;
-            const __nv_bfloat16* gu = reinterpret_cast<const __nv_bfloat16*>(ep.resid) + m * ep.ldr;
-            float g[32], u[32], dg[32], du[32];
-            load32_bf16(gu + gcol, g);
-            load32_bf16(gu + ucol, u);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float sg = 1.0f / (1.0f + __expf(-g[i]));
-              const float sl = g[i] * sg;
-              du[i] = v[i] * sl;
-              dg[i] = v[i] * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
-            }
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo;
-            store32_bf16(out + gcol, dg);
-            store32_bf16(out + ucol, du);
           }
         }
       }
