@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/); if the source has changed since, the traffic is reported as null.
 NCU_TRAFFIC = {
     # layer forward at batch 2 x 16384 tokens
-    "gate/up projection": (2.16e9 + 0.924e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "17ccb880b0bf301b"),
+    "gate/up projection": (2.16e9 + 0.926e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "abab59fbc329b85d"),
     "attention": (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
     # training step at batch 2 x 16384 tokens
     "attention bwd fused": (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "b2445bd5bb872aae"),
