@@ -39,23 +39,26 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch
-# of a step's kernel on the default workload (D=8, batch 2, seq 16384), with
-# the kernel source file and the first 16 hex digits of its sha256 when the
-# counters were taken (one-pass capture of the full-size launch, see
-# profiles/); if the source has changed since, the traffic is reported as null.
+# of a step's kernel, keyed by (step, workload), with the kernel source file
+# and the first 16 hex digits of its sha256 when the counters were taken
+# (one-pass capture of the full-size launch, see profiles/).  A workload
+# without its own capture, or a source changed since, reports null.
 NCU_TRAFFIC = {
-    # layer forward at batch 2 x 16384 tokens
-    "gate/up projection": (2.16e9 + 0.926e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "abab59fbc329b85d"),
-    "attention": (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
-    # training step at batch 2 x 16384 tokens
-    "attention bwd fused": (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "b2445bd5bb872aae"),
-    # decode step, batch 1, 128K-token cache
-    "decode attention": (2.15e9 + 0.00315e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "25dde6d76c0177c8"),
+    ("gate/up projection", "bf16_D8_b2_s16384_h4096"):
+        (2.16e9 + 0.926e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "abab59fbc329b85d"),
+    ("attention", "bf16_D8_b2_s16384_h4096"):
+        (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
+    ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
+        (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "b2445bd5bb872aae"),
+    ("decode attention", "bf16_decode_D8_b1_ctx131072_h4096"):
+        (0.0, "folded_tensor_sequence_gb300/csrc/decode.cu", "pending"),
+    ("decode attention", "bf16_decode_gqa8_D8_b4_ctx131072_h4096"):
+        (0.0, "folded_tensor_sequence_gb300/csrc/decode.cu", "pending"),
 }
 
 
-def ncu_traffic(step: str):
-    ent = NCU_TRAFFIC.get(step)
+def ncu_traffic(step: str, workload: str):
+    ent = NCU_TRAFFIC.get((step, workload))
     if not ent:
         return None
     import hashlib
@@ -425,7 +428,7 @@ def main():
     dname, dtot, dcnt = dom
     dfl, dby, _ = wk.get(dname, (0, 0, 1))
     davg_s = dtot / dcnt / 1e3
-    traffic = ncu_traffic(dname)
+    traffic = ncu_traffic(dname, cfg.name)
     if dfl:
         peak = peaks["bf16_tflops_sustained"]
         ach = dfl / davg_s / 1e12

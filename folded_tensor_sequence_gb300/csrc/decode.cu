@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "warp_mma.cuh"
 
 namespace tsp {
 
@@ -188,7 +189,9 @@ struct DecAttnParams {
 // head blockIdx.y, over piece blockIdx.x % split of rank blockIdx.x / split's
 // cached keys (its chunks r and 2D-1-r, positions <= pos).  Half-warps take
 // keys in turn (16 lanes x 8 dims per key), keep an online softmax per query
-// head, and the CTA merges its 16 half-warp states at the end.
+// head, and the CTA merges its 16 half-warp states at the end.  Used for one
+// query head per K/V head; with several, the per-key scalar arithmetic
+// grows with G and decode_attn_mma_kernel takes over.
 template <int G>
 __global__ void __launch_bounds__(DA_THREADS) decode_attn_partial_kernel(const DecAttnParams p) {
   extern __shared__ float sm[];  // [16 half-warps][G][HD + 2]
@@ -216,12 +219,9 @@ __global__ void __launch_bounds__(DA_THREADS) decode_attn_partial_kernel(const D
   auto position = [&](int64_t k) { return k < p.C ? r * p.C + k : (2 * p.D - 1 - r) * p.C + (k - p.C); };
   // Half-warp hw takes keys k_lo + hw + 16 * (U * t + u).  Each warp walks its
   // own block loop from k_lo + 2 * (its warp index), so both halves of a warp
-  // always run the same iterations, as the full-warp shuffles need.  With several query
-  // heads per key (G >= 4) the per-key arithmetic is long enough that the
-  // next block's loads are issued before the current block is consumed; with
-  // one or two, more CTAs per SM (fewer registers) hide the latency better.
-  constexpr int U = G >= 4 ? 2 : 4;
-  constexpr bool kPrefetch = G >= 4;
+  // always run the same iterations, as the full-warp shuffles need.  Many
+  // CTAs per SM (few registers) hide the load latency.
+  constexpr int U = 4;
   uint4 kv[U], vv[U];
   bool use[U];
   auto fetch = [&](int64_t kb, uint4 (&kd)[U], uint4 (&vd)[U], bool (&ud)[U]) {
@@ -239,14 +239,8 @@ __global__ void __launch_bounds__(DA_THREADS) decode_attn_partial_kernel(const D
     }
   };
   const int64_t kw = k_lo + (hw & ~1);  // this warp's first key
-  if (kPrefetch) fetch(kw, kv, vv, use);
   for (int64_t kb = kw; kb < k_hi; kb += 16 * U) {
-    uint4 kn[U], vn[U];
-    bool un[U];
-    if (kPrefetch)
-      fetch(kb + 16 * U, kn, vn, un);
-    else
-      fetch(kb, kv, vv, use);
+    fetch(kb, kv, vv, use);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       // the two half-warps may differ in `use[u]`: the whole warp computes and
@@ -273,14 +267,6 @@ __global__ void __launch_bounds__(DA_THREADS) decode_attn_partial_kernel(const D
 #pragma unroll
           for (int d = 0; d < 8; ++d) o[j][d] = fmaf(o[j][d], corr, e * vf[d]);
         }
-      }
-    }
-    if (kPrefetch) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        kv[u] = kn[u];
-        vv[u] = vn[u];
-        use[u] = un[u];
       }
     }
   }
@@ -314,6 +300,189 @@ __global__ void __launch_bounds__(DA_THREADS) decode_attn_partial_kernel(const D
     }
     const int head = kvh * G + j;
     const int64_t slot = ((int64_t)b * p.H + head) * P + blockIdx.x;
+    p.part_o[slot * HD + d] = O;
+    if (d == 0) {
+      p.part_ml[slot * 2] = M;
+      p.part_ml[slot * 2 + 1] = L;
+    }
+  }
+}
+
+// Partial attention for G = 2, 4 or 8 query heads per K/V head, on the warp
+// tensor cores.  The same split and output as decode_attn_partial_kernel,
+// but the G query rows (padded to 16) are multiplied against 16 keys per
+// warp and step: S = Q K^T and O += P V with mma.sync m16n8k16 (the score
+// accumulators become P's A fragments in registers), K and V arriving in
+// 64-key blocks through a 3-stage cp.async ring of swizzled shared-memory
+// tiles.  Each warp keeps an online softmax over its 16 keys of every block;
+// the CTA merges the four warps at the end.  Still bound by streaming the
+// cache: the tensor cores only remove the per-key scalar arithmetic that
+// limits the half-warp kernel once several query heads share a key.
+constexpr int DM_THREADS = 128;
+constexpr int DM_KB = 64;      // keys per block (16 per warp)
+constexpr int DM_STAGES = 3;
+constexpr size_t DM_STAGE_ELEMS = 2 * (size_t)DM_KB * HD;  // K tile then V tile
+constexpr size_t DM_SMEM = DM_STAGES * DM_STAGE_ELEMS * 2;
+
+template <int G>
+__global__ void __launch_bounds__(DM_THREADS) decode_attn_mma_kernel(const DecAttnParams p) {
+  extern __shared__ __align__(128) uint8_t dm_smem[];
+  __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(dm_smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;  // fragment row / column pair
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int r = blockIdx.x / p.split, piece = blockIdx.x % p.split;
+  const int64_t twoC = 2 * p.C;
+  const int64_t k_lo = twoC * piece / p.split, k_hi = twoC * (piece + 1) / p.split;
+  const int nblk = (int)((k_hi - k_lo + DM_KB - 1) / DM_KB);
+  const float sl2 = rsqrtf((float)HD) * kLog2e;
+  const __nv_bfloat16* kbase = p.kc + ((int64_t)b * p.Hk + kvh) * p.S * HD;
+  const __nv_bfloat16* vbase = p.vc + ((int64_t)b * p.Hk + kvh) * p.S * HD;
+  auto position = [&](int64_t k) { return k < p.C ? r * p.C + k : (2 * p.D - 1 - r) * p.C + (k - p.C); };
+  auto key_ok = [&](int64_t k) { return k < k_hi && position(k) <= p.pos; };
+
+  // K and V rows of block j -> stage j % DM_STAGES (missing rows zero-filled)
+  auto load_block = [&](int j) {
+    __nv_bfloat16* kt = tiles + (size_t)(j % DM_STAGES) * DM_STAGE_ELEMS;
+    __nv_bfloat16* vt = kt + (size_t)DM_KB * HD;
+    const uint32_t ks = smem_u32(kt), vs = smem_u32(vt);
+    for (int i = tid; i < DM_KB * wm::CHUNKS; i += DM_THREADS) {
+      const int row = i / wm::CHUNKS, c = i % wm::CHUNKS;
+      const int64_t k = k_lo + (int64_t)j * DM_KB + row;
+      const bool ok = key_ok(k);
+      const int64_t off = ok ? position(k) * HD + c * 8 : 0;
+      wm::cp_async16(ks + wm::swz(row, c * 8) * 2, kbase + off, ok);
+      wm::cp_async16(vs + wm::swz(row, c * 8) * 2, vbase + off, ok);
+    }
+  };
+
+  // Q rows g < G as A fragments (rows 8..15 and G..7 are zero)
+  uint32_t qa[HD / 16][2];
+  {
+    const uint32_t* qrow =
+        reinterpret_cast<const uint32_t*>(p.q + ((int64_t)b * p.H + (int64_t)kvh * G + (g < G ? g : 0)) * HD);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      qa[kk][0] = g < G ? qrow[(16 * kk + 2 * t) / 2] : 0u;
+      qa[kk][1] = g < G ? qrow[(16 * kk + 8 + 2 * t) / 2] : 0u;
+    }
+  }
+  float o[HD / 8][2];  // row g, head dims 8*dt + 2t, +1
+#pragma unroll
+  for (int dt = 0; dt < HD / 8; ++dt) o[dt][0] = o[dt][1] = 0.f;
+  float m_run = -INFINITY, l_part = 0.f;  // l_part: this thread's columns only
+
+  for (int j = 0; j < DM_STAGES - 1 && j < nblk; ++j) {
+    load_block(j);
+    wm::cp_commit();
+  }
+  for (int j = 0; j < nblk; ++j) {
+    if (j + 1 < nblk)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      wm::cp_wait_all();
+    __syncthreads();  // block j landed for every thread; stage (j + 2) % 3 is free
+    if (j + DM_STAGES - 1 < nblk) {
+      load_block(j + DM_STAGES - 1);
+      wm::cp_commit();
+    }
+    const __nv_bfloat16* kt = tiles + (size_t)(j % DM_STAGES) * DM_STAGE_ELEMS;
+    const __nv_bfloat16* vt = kt + (size_t)DM_KB * HD;
+    const uint32_t ks = smem_u32(kt), vs = smem_u32(vt);
+    // S = Q K^T for this warp's keys 16*warp .. +15 (two n-tiles of 8)
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const int krow = 16 * warp + 8 * nt + (lane & 7);
+#pragma unroll
+      for (int kp = 0; kp < HD / 32; ++kp) {  // pairs of 16-wide k steps
+        uint32_t b0, b1, b2, b3;
+        wm::ldsm_x4(ks + wm::swz(krow, (4 * kp + (lane >> 3)) * 8) * 2, b0, b1, b2, b3);
+        const uint32_t a0[4] = {qa[2 * kp][0], 0u, qa[2 * kp][1], 0u};
+        const uint32_t a1[4] = {qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u};
+        wm::mma16816(s[nt], a0, b0, b1);
+        wm::mma16816(s[nt], a1, b2, b3);
+      }
+    }
+    // online softmax of row g over the 16 keys (c0, c1 of each n-tile; rows g + 8 are padding)
+    const int64_t kbase_blk = k_lo + (int64_t)j * DM_KB + 16 * warp;
+    float x[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int64_t k = kbase_blk + 8 * nt + 2 * t + e;
+        x[2 * nt + e] = key_ok(k) ? s[nt][e] * sl2 : -INFINITY;
+      }
+    float mb = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const float m_new = fmaxf(m_run, mb);
+    if (m_new == -INFINITY) continue;  // nothing visible yet in this warp's keys (uniform per row group)
+    const float corr = ex2f(m_run - m_new);
+    m_run = m_new;
+    float pv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pv[i] = ex2f(x[i] - m_new);
+    l_part = l_part * corr + (pv[0] + pv[1]) + (pv[2] + pv[3]);
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt) {
+      o[dt][0] *= corr;
+      o[dt][1] *= corr;
+    }
+    const uint32_t pa[4] = {pack_bf16x2(pv[0], pv[1]), 0u, pack_bf16x2(pv[2], pv[3]), 0u};
+    // O += P V: V rows = this warp's keys, two head-dim n-tiles per ldmatrix
+    const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int dp = 0; dp < HD / 16; ++dp) {
+      uint32_t b0, b1, b2, b3;
+      wm::ldsm_x4_t(vs + wm::swz(vrow, (2 * dp + (lane >> 4)) * 8) * 2, b0, b1, b2, b3);
+      float acc0[4] = {o[2 * dp][0], o[2 * dp][1], 0.f, 0.f};
+      float acc1[4] = {o[2 * dp + 1][0], o[2 * dp + 1][1], 0.f, 0.f};
+      wm::mma16816(acc0, pa, b0, b1);
+      wm::mma16816(acc1, pa, b2, b3);
+      o[2 * dp][0] = acc0[0];
+      o[2 * dp][1] = acc0[1];
+      o[2 * dp + 1][0] = acc1[0];
+      o[2 * dp + 1][1] = acc1[1];
+    }
+  }
+  // row sums over the four lanes of a row, then the CTA merge of the four warps
+  float l_row = l_part + __shfl_xor_sync(0xffffffffu, l_part, 1);
+  l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+  __syncthreads();  // every warp is done with the stage tiles
+  constexpr int ST = HD + 2;
+  float* ms = reinterpret_cast<float*>(dm_smem);  // [4 warps][G][ST]
+  if (g < G) {
+    float* row = ms + (warp * G + g) * ST;
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt) {
+      row[8 * dt + 2 * t] = o[dt][0];
+      row[8 * dt + 2 * t + 1] = o[dt][1];
+    }
+    if (t == 0) {
+      row[HD] = m_run;
+      row[HD + 1] = l_row;
+    }
+  }
+  __syncthreads();
+  const int P = p.D * p.split;
+  for (int idx = tid; idx < G * HD; idx += DM_THREADS) {
+    const int jh = idx / HD, d = idx % HD;
+    float M = -INFINITY;
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, ms[(w * G + jh) * ST + HD]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < 4; ++w) {
+        const float* row = ms + (w * G + jh) * ST;
+        if (row[HD + 1] == 0.f) continue;
+        const float c = exp2f(row[HD] - M);
+        L = fmaf(row[HD + 1], c, L);
+        O = fmaf(row[d], c, O);
+      }
+    }
+    const int64_t slot = ((int64_t)b * p.H + (int64_t)kvh * G + jh) * P + blockIdx.x;
     p.part_o[slot * HD + d] = O;
     if (d == 0) {
       p.part_ml[slot * 2] = M;
@@ -357,18 +526,41 @@ cudaError_t launch_gemv(const GemvParams& p, cudaStream_t st) {
 
 }  // namespace
 
-int decode_split(int D, int Hk, int B, int64_t C) {
-  // enough CTAs to keep every SM streaming (about 4 per SM), pieces of >= 64 keys
-  const int64_t target = 4LL * num_sms();
-  int64_t split = (target + (int64_t)D * Hk * B - 1) / ((int64_t)D * Hk * B);
-  const int64_t max_split = (2 * C) / 64 > 0 ? (2 * C) / 64 : 1;
-  if (split > max_split) split = max_split;
-  return split < 1 ? 1 : (int)split;
+int decode_split(int D, int H, int Hk, int B, int64_t C) {
+  const int64_t base = (int64_t)D * Hk * B;  // CTAs per piece of every rank
+  const int64_t max_split = (2 * C) / 64 > 0 ? (2 * C) / 64 : 1;  // pieces of >= 64 keys
+  if (H / Hk == 1) {
+    // half-warp kernel: enough CTAs to keep every SM streaming (about 4 per SM)
+    const int64_t target = 4LL * num_sms();
+    int64_t split = (target + base - 1) / base;
+    if (split > max_split) split = max_split;
+    return split < 1 ? 1 : (int)split;
+  }
+  // tensor-core kernel: two CTAs per SM and equal pieces, so whole waves
+  // matter; take the smallest split that fills one wave and leaves the last
+  // wave at least 95 % full (else the fullest within eight times that)
+  const int64_t slots = 2LL * num_sms();
+  int64_t first = (slots + base - 1) / base;
+  if (first > max_split) first = max_split;
+  if (first < 1) first = 1;
+  int64_t best = first;
+  double best_eff = 0.0;
+  for (int64_t split = first; split <= max_split && split <= 8 * first; ++split) {
+    const int64_t n = base * split;
+    const int64_t waves = (n + slots - 1) / slots;
+    const double eff = (double)n / (double)(waves * slots);
+    if (eff >= 0.95) return (int)split;
+    if (eff > best_eff) {
+      best_eff = eff;
+      best = split;
+    }
+  }
+  return (int)best;
 }
 
 size_t decode_ws_bytes(const tsp_plan* p, int batch) {
   const size_t B = batch, h = p->hidden, F = p->ffn, H = p->heads;
-  const size_t P = (size_t)p->D * decode_split(p->D, p->kv_heads, batch, p->chunk);
+  const size_t P = (size_t)p->D * decode_split(p->D, p->heads, p->kv_heads, batch, p->chunk);
   auto a = [](size_t x) { return (x + 255) & ~size_t(255); };
   return a(B * h * 2) * 3 + a(B * F * 2) + a(B * H * P * HD * 4) + a(B * H * P * 2 * 4);
 }
@@ -377,7 +569,7 @@ tsp_status decode_step_bf16(const tsp_plan* pl, int batch, int64_t pos, const vo
                             void* k_cache, void* v_cache, void* y_new, void* ws, cudaStream_t st) {
   const int B = batch, h = pl->hidden, F = pl->ffn, H = pl->heads, Hk = pl->kv_heads, D = pl->D;
   const int hk = Hk * pl->head_dim;
-  const int split = decode_split(D, Hk, B, pl->chunk);
+  const int split = decode_split(D, H, Hk, B, pl->chunk);
   const int P = D * split;
   auto a = [](size_t x) { return (x + 255) & ~size_t(255); };
   char* base = static_cast<char*>(ws);
@@ -426,26 +618,33 @@ tsp_status decode_step_bf16(const tsp_plan* pl, int batch, int64_t pos, const vo
   ap.pos = pos;
   const int G = H / Hk;
   const dim3 grid(P, Hk, B);
-  const size_t smem = (size_t)16 * G * (HD + 2) * 4;
   prof_begin("decode attention", st);
-  switch (G) {
-    case 1: decode_attn_partial_kernel<1><<<grid, DA_THREADS, smem, st>>>(ap); break;
-    case 2: decode_attn_partial_kernel<2><<<grid, DA_THREADS, smem, st>>>(ap); break;
-    case 4: decode_attn_partial_kernel<4><<<grid, DA_THREADS, smem, st>>>(ap); break;
-    case 8: {
-      static std::atomic<unsigned long long> configured{0};  // devices set up
-      if (needs_setup(configured)) {
-        if (cudaFuncSetAttribute(decode_attn_partial_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)((size_t)16 * 8 * (HD + 2) * 4)) != cudaSuccess) {
-          prof_end(st);
-          return TSP_ERR_CUDA;
-        }
-        mark_setup_done(configured);
+  if (G == 1) {
+    decode_attn_partial_kernel<1><<<grid, DA_THREADS, (size_t)16 * (HD + 2) * 4, st>>>(ap);
+  } else if (G == 2 || G == 4 || G == 8) {
+    // several query heads per cached key: tensor-core partials
+    static std::atomic<unsigned long long> configured{0};  // devices set up
+    if (needs_setup(configured)) {
+      if (cudaFuncSetAttribute(decode_attn_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)DM_SMEM) != cudaSuccess ||
+          cudaFuncSetAttribute(decode_attn_mma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)DM_SMEM) != cudaSuccess ||
+          cudaFuncSetAttribute(decode_attn_mma_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)DM_SMEM) != cudaSuccess) {
+        prof_end(st);
+        return TSP_ERR_CUDA;
       }
-      decode_attn_partial_kernel<8><<<grid, DA_THREADS, smem, st>>>(ap);
-      break;
+      mark_setup_done(configured);
     }
-    default: prof_end(st); return TSP_ERR_UNSUPPORTED;
+    if (G == 2)
+      decode_attn_mma_kernel<2><<<grid, DM_THREADS, DM_SMEM, st>>>(ap);
+    else if (G == 4)
+      decode_attn_mma_kernel<4><<<grid, DM_THREADS, DM_SMEM, st>>>(ap);
+    else
+      decode_attn_mma_kernel<8><<<grid, DM_THREADS, DM_SMEM, st>>>(ap);
+  } else {
+    prof_end(st);
+    return TSP_ERR_UNSUPPORTED;
   }
   e = cudaGetLastError();
   if (e == cudaSuccess) {

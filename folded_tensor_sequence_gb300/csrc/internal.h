@@ -164,7 +164,7 @@ cudaError_t launch_assemble_dqkv_f32q(const float* dq_acc, float scale, const vo
 
 // Decode step (bf16; batch 1..8; head_dim 128; H / Hk in {1, 2, 4, 8}).
 size_t decode_ws_bytes(const tsp_plan* p, int batch);
-int decode_split(int D, int Hk, int B, int64_t C);
+int decode_split(int D, int H, int Hk, int B, int64_t C);
 tsp_status decode_step_bf16(const tsp_plan* p, int batch, int64_t pos, const void* x_new, const tsp_weights* w,
                             void* k_cache, void* v_cache, void* y_new, void* ws, cudaStream_t st);
 
