@@ -51,9 +51,9 @@ NCU_TRAFFIC = {
     ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
         (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "b2445bd5bb872aae"),
     ("decode attention", "bf16_decode_D8_b1_ctx131072_h4096"):
-        (0.0, "folded_tensor_sequence_gb300/csrc/decode.cu", "pending"),
+        (2.15e9 + 0.00295e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "d8f12475d8af56f2"),
     ("decode attention", "bf16_decode_gqa8_D8_b4_ctx131072_h4096"):
-        (0.0, "folded_tensor_sequence_gb300/csrc/decode.cu", "pending"),
+        (2.15e9 + 0.00623e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "d8f12475d8af56f2"),
 }
 
 
