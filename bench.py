@@ -354,8 +354,8 @@ def main():
         y = torch.empty_like(x)
         dwork = tsp.workspace(plan, B, tsp.TSP_OP_DECODE, dev)
 
-        def step():
-            tsp.tsp_decode_step(plan, B, S - 1, x, packed, kc, vc, y, dwork, stream)
+        def step_io(ins, out):
+            tsp.tsp_decode_step(plan, B, S - 1, ins[0], packed, kc, vc, out, dwork, stream)
     else:
         x = synth.tensor_torch("x", (B, S, h), 1.0, cfg.dtype, 0, dev)
         y = torch.empty_like(x)
@@ -370,12 +370,18 @@ def main():
         saved = torch.empty(tsp.tsp_saved_bytes(plan, B), dtype=torch.uint8, device=dev)
         bwork = tsp.workspace(plan, B, tsp.TSP_OP_LAYER_BWD, dev)
 
-        def step():
-            tsp.tsp_layer_fwd(plan, B, x, packed, y, saved, work, stream)
-            tsp.tsp_layer_bwd(plan, B, x, packed, saved, dy, dx, grads, bwork, stream)
+        def step_io(ins, out):
+            tsp.tsp_layer_fwd(plan, B, ins[0], packed, y, saved, work, stream)
+            tsp.tsp_layer_bwd(plan, B, ins[0], packed, saved, ins[1], out, grads, bwork, stream)
     else:
-        def step():
-            tsp.tsp_layer_fwd(plan, B, x, packed, y, None, work, stream)
+        def step_io(ins, out):
+            tsp.tsp_layer_fwd(plan, B, ins[0], packed, out, None, work, stream)
+
+    ins = [x, dy] if cfg.backward and not cfg.decode else [x]  # per-step inputs
+    out = dx if cfg.backward and not cfg.decode else y          # per-step result
+
+    def step():
+        step_io(ins, out)
 
     for _ in range(args.warmup):
         step()
@@ -443,21 +449,49 @@ def main():
                 "frac": round(ach / peak, 4), "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
 
     # ---- end to end through the API with host buffers -----------------------
-    ins = [x, dy] if cfg.backward and not cfg.decode else [x]  # per-step inputs copied in
-    out = dx if cfg.backward and not cfg.decode else y          # per-step result copied out
+    # Every step's inputs come from pinned host memory and its result goes back
+    # to it.  As a caller overlapping I/O with the layer would, a copy stream
+    # brings step i+1's inputs in and takes step i's result out while step i
+    # computes (device inputs and outputs double-buffered, events ordering the
+    # reuse of each buffer).  Timed from the first input copy to the last
+    # result copy.
     ins_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
     for th, t in zip(ins_host, ins):
         th.copy_(t)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dins = [ins, [torch.empty_like(t) for t in ins]]
+    douts = [out, torch.empty_like(out)]
+    cs = torch.cuda.Stream(dev)
+    h2d = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    d2h = [torch.cuda.Event() for _ in range(2)]
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        for t, th in zip(ins, ins_host):
+    with torch.cuda.stream(cs):
+        e0.record(cs)
+        for t, th in zip(dins[0], ins_host):
             t.copy_(th, non_blocking=True)
-        step()
-        out_host.copy_(out, non_blocking=True)
-    e1.record(stream)
+        h2d[0].record(cs)
+    for i in range(args.steps):
+        k = i % 2
+        stream.wait_event(h2d[k])
+        if i >= 2:
+            stream.wait_event(d2h[k])  # douts[k] has been read back
+        step_io(dins[k], douts[k])
+        done[k].record(stream)
+        with torch.cuda.stream(cs):
+            if i + 1 < args.steps:
+                nk = (i + 1) % 2
+                if i >= 1:
+                    cs.wait_event(done[nk])  # dins[nk] no longer read by step i-1
+                for t, th in zip(dins[nk], ins_host):
+                    t.copy_(th, non_blocking=True)
+                h2d[nk].record(cs)
+            cs.wait_event(done[k])
+            out_host.copy_(douts[k], non_blocking=True)
+            d2h[k].record(cs)
+    with torch.cuda.stream(cs):
+        e1.record(cs)
     barrier()
     ems = max_over_ranks(e0.elapsed_time(e1), dev)
     tsp.tsp_sync_check(stream)
