@@ -457,7 +457,7 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 __global__ void __launch_bounds__(THREADS, 1)
     attn_bwd_fused_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                              const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-                             const BwdTcParams p, int nk) {
+                             const BwdTcParams p, int nk, int paired) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Ks = smem;                          // 2 x SUB128
@@ -478,11 +478,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  // paired: grid (mirror pair, K/V head, batch), two key tiles of equal total
+  // work per CTA; otherwise grid (K/V head, batch, key tile), one tile per
+  // CTA, heaviest tiles (the earliest keys see the most queries) launched first
+  const int kvh = paired ? (int)blockIdx.y : (int)blockIdx.x;
+  const int b = paired ? (int)blockIdx.z : (int)blockIdx.y;
   const int grp = p.H / p.Hk;
   const int64_t bkv = (int64_t)b * p.Hk + kvh;
-  auto tile_of = [&](int t) { return t == 0 ? (int)blockIdx.x : nk - 1 - (int)blockIdx.x; };
-  const int ntile = (nk - 1 - (int)blockIdx.x == (int)blockIdx.x) ? 1 : 2;
+  auto tile_of = [&](int t) {
+    return paired ? (t == 0 ? (int)blockIdx.x : nk - 1 - (int)blockIdx.x) : (int)blockIdx.z;
+  };
+  const int ntile = paired ? ((nk - 1 - (int)blockIdx.x == (int)blockIdx.x) ? 1 : 2) : 1;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -1132,7 +1138,18 @@ tsp_status attn_bwd_bf16_tc(const AttnBwdTcArgs& a, cudaStream_t stream, int whi
   const int nk = (int)(a.S / 128);
   dim3 g1((nk + 1) / 2, a.Hk, a.B);
   if (which & 4) {
-    attn_bwd_fused_tc_kernel<<<g1, THREADS, FUSED_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk);
+    // Mirror pairs give every CTA the same work; when their count leaves the
+    // last wave on the SMs mostly empty (few K/V heads, short sequences),
+    // single tiles in decreasing order of work balance better.
+    const int64_t pairs = (int64_t)g1.x * g1.y * g1.z;
+    const int64_t sms = num_sms();
+    const double pair_eff = (double)pairs / (double)(((pairs + sms - 1) / sms) * sms);
+    if (pair_eff >= 0.9) {
+      attn_bwd_fused_tc_kernel<<<g1, THREADS, FUSED_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p, nk, 1);
+    } else {
+      attn_bwd_fused_tc_kernel<<<dim3(a.Hk, a.B, nk), THREADS, FUSED_SMEM, stream>>>(mK128, mV128, mQ64, mdO64, p,
+                                                                                     nk, 0);
+    }
     if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
   }
   if (which & 1) {
