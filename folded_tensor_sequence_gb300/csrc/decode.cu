@@ -29,7 +29,6 @@ namespace tsp {
 namespace {
 
 constexpr int GV_WARPS = 4;   // warps per GEMV CTA
-constexpr int GV_ROWS = 4;    // weight rows per warp
 constexpr int DA_THREADS = 256;
 constexpr int HD = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -84,16 +83,21 @@ struct GemvParams {
   int64_t S, pos;
 };
 
-// out[b][n] = sum_k x[b][k] w[n][k] with an epilogue.  Each warp owns four
-// weight rows (for SwiGLU: two gate rows and the matching two up rows of the
-// packed gate/up layout) and streams them once for all B tokens.
-template <int KIND, int NB>
+// out[b][n] = sum_k x[b][k] w[n][k] with an epilogue.  Each warp owns R
+// weight rows (for SwiGLU R = 4: two gate rows and the matching two up rows of
+// the packed gate/up layout) and streams them once for all B tokens, U
+// 256-element chunks of every row in flight per step.  Bytes in flight over
+// the whole GPU are about rows x U x 512 B, so small weights take U = 4 and
+// one row per warp (more warps) to keep HBM busy.
+template <int KIND, int NB, int R, int U>
 __global__ void __launch_bounds__(GV_WARPS * 32) gemv_bf16_kernel(const GemvParams p) {
+  constexpr int GV_ROWS = R;
+  static_assert(KIND != GV_SWIGLU || R == 4, "SwiGLU pairs two gate rows with two up rows");
   const int lane = threadIdx.x & 31;
   const int64_t wg = (int64_t)blockIdx.x * GV_WARPS + (threadIdx.x >> 5);
   int64_t row[GV_ROWS];
   bool valid[GV_ROWS];
-  if (KIND == GV_SWIGLU) {
+  if constexpr (KIND == GV_SWIGLU) {
     const int64_t f0 = wg * 2;  // outputs f0, f0 + 1
     const int64_t blk = f0 / 128, i = f0 % 128;
     row[0] = blk * 256 + i;
@@ -114,18 +118,20 @@ __global__ void __launch_bounds__(GV_WARPS * 32) gemv_bf16_kernel(const GemvPara
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
   const int64_t K = p.K;
-  for (int64_t k0 = lane * 8; k0 < K; k0 += 512) {
-    uint4 wv[2][GV_ROWS];
-    const bool second = k0 + 256 < K;
+  for (int64_t k0 = lane * 8; k0 < K; k0 += 256 * U) {
+    uint4 wv[U][GV_ROWS];
 #pragma unroll
-    for (int r = 0; r < GV_ROWS; ++r) {
-      const int64_t rr = valid[r] ? row[r] : row[0];
-      wv[0][r] = ld_stream16(p.w + rr * K + k0);
-      if (second) wv[1][r] = ld_stream16(p.w + rr * K + k0 + 256);
+    for (int u = 0; u < U; ++u) {
+      if (k0 + 256 * u >= K) break;
+#pragma unroll
+      for (int r = 0; r < GV_ROWS; ++r) {
+        const int64_t rr = valid[r] ? row[r] : row[0];
+        wv[u][r] = ld_stream16(p.w + rr * K + k0 + 256 * u);
+      }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (u == 1 && !second) break;
+    for (int u = 0; u < U; ++u) {
+      if (k0 + 256 * u >= K) break;
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         if (b >= p.B) break;
@@ -149,13 +155,13 @@ __global__ void __launch_bounds__(GV_WARPS * 32) gemv_bf16_kernel(const GemvPara
       if (lane != r * NB + b || b >= p.B || !valid[r]) continue;
       const float v = acc[r][b];
       const int64_t n = row[r];
-      if (KIND == GV_RESID) {
+      if constexpr (KIND == GV_RESID) {
         const float res = p.resid ? __bfloat162float(p.resid[(int64_t)b * p.rows + n]) : 0.f;
         p.out[(int64_t)b * p.rows + n] = __float2bfloat16_rn(v + res);
-      } else if (KIND == GV_SWIGLU) {
+      } else if constexpr (KIND == GV_SWIGLU) {
         if (r < 2) {
           const int64_t f = wg * 2 + r;
-          p.out[(int64_t)b * (p.rows / 2) + f] = __float2bfloat16_rn(silu_f(v) * acc[r + 2][b]);
+          p.out[(int64_t)b * (p.rows / 2) + f] = __float2bfloat16_rn(silu_f(v) * acc[(r + 2) % R][b]);
         }
       } else {  // GV_QKV
         const int hs = p.h / p.D, ks = p.Hk * p.dh / p.D;
@@ -510,18 +516,26 @@ __global__ void decode_attn_combine_kernel(const float* __restrict__ part_o, con
   out[((int64_t)b * H + head) * HD + d] = __float2bfloat16_rn(O / L);
 }
 
-template <int KIND>
-cudaError_t launch_gemv(const GemvParams& p, cudaStream_t st) {
-  const int64_t warps = KIND == GV_SWIGLU ? (p.rows / 2 + 1) / 2 : (p.rows + GV_ROWS - 1) / GV_ROWS;
+template <int KIND, int R, int U>
+cudaError_t launch_gemv_ru(const GemvParams& p, cudaStream_t st) {
+  const int64_t warps = KIND == GV_SWIGLU ? (p.rows / 2 + 1) / 2 : (p.rows + R - 1) / R;
   const unsigned grid = (unsigned)((warps + GV_WARPS - 1) / GV_WARPS);
   switch (p.B) {
-    case 1: gemv_bf16_kernel<KIND, 1><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
-    case 2: gemv_bf16_kernel<KIND, 2><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
+    case 1: gemv_bf16_kernel<KIND, 1, R, U><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
+    case 2: gemv_bf16_kernel<KIND, 2, R, U><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
     case 3:
-    case 4: gemv_bf16_kernel<KIND, 4><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
-    default: gemv_bf16_kernel<KIND, 8><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
+    case 4: gemv_bf16_kernel<KIND, 4, R, U><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
+    default: gemv_bf16_kernel<KIND, 8, R, U><<<grid, GV_WARPS * 32, 0, st>>>(p); break;
   }
   return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t launch_gemv(const GemvParams& p, cudaStream_t st) {
+  if constexpr (KIND == GV_SWIGLU)
+    return launch_gemv_ru<KIND, 4, 2>(p, st);
+  else
+    return launch_gemv_ru<KIND, 1, 4>(p, st);
 }
 
 }  // namespace
