@@ -49,11 +49,11 @@ NCU_TRAFFIC = {
     ("attention", "bf16_D8_b2_s16384_h4096"):
         (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
-        (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "b2445bd5bb872aae"),
+        (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
     ("decode attention", "bf16_decode_D8_b1_ctx131072_h4096"):
-        (2.15e9 + 0.00295e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "d8f12475d8af56f2"),
+        (2.15e9 + 0.00311e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "1544c105bc1c9031"),
     ("decode attention", "bf16_decode_gqa8_D8_b4_ctx131072_h4096"):
-        (2.15e9 + 0.00623e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "d8f12475d8af56f2"),
+        (2.15e9 + 0.00612e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "1544c105bc1c9031"),
 }
 
 
