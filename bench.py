@@ -51,9 +51,9 @@ NCU_TRAFFIC = {
     ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
         (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
     ("decode attention", "bf16_decode_D8_b1_ctx131072_h4096"):
-        (2.15e9 + 0.00311e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "1544c105bc1c9031"),
+        (2.15e9 + 0.00292e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "3bfb1d17f6da32df"),
     ("decode attention", "bf16_decode_gqa8_D8_b4_ctx131072_h4096"):
-        (2.15e9 + 0.00612e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "1544c105bc1c9031"),
+        (2.15e9 + 0.00627e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "3bfb1d17f6da32df"),
 }
 
 
