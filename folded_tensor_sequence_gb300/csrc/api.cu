@@ -158,6 +158,11 @@ size_t mlp_ws_bytes(const tsp_plan* p, int batch) {
   return align256(T * F * e) + align256(T * 2 * F * e);
 }
 
+// bf16 plans whose chunks are whole 128-row tiles move natural-order
+// activations through remapped GEMM rows instead of zigzag copies: x and y in
+// inference, y and dx in training.
+bool folded_io(const tsp_plan* p) { return p->dtype == TSP_BF16 && p->chunk % 128 == 0; }
+
 tsp_status check_plan_batch(const tsp_plan* p, int batch) {
   if (!p) return fail(TSP_ERR_INVALID_ARG, "plan is NULL");
   if (batch < 0) return fail(TSP_ERR_INVALID_ARG, "batch %d < 0", batch);
@@ -607,7 +612,7 @@ tsp_status tsp_layer_fwd(const tsp_plan* p, int batch, const void* x, const tsp_
   char* act = saved ? static_cast<char*>(saved) : wsb;  // where the saved activations go
   char* xz = act + L.xz;
   char* yz = wsb + L.yz;
-  if (!saved && p->dtype == TSP_BF16 && p->chunk % 128 == 0) {
+  if (!saved && folded_io(p)) {
     // The zigzag permute and unpermute ride on the GEMMs: every 128-row tile
     // of zigzag rows is one contiguous run of natural rows, so the QKV GEMM
     // reads x through remapped TMA coordinates, the output projection adds x
@@ -626,6 +631,10 @@ tsp_status tsp_layer_fwd(const tsp_plan* p, int batch, const void* x, const tsp_
   s = attention_impl(p, batch, xz, w, act + L.hz, xz, saved ? reinterpret_cast<float*>(act + L.lse) : nullptr,
                      act + L.qz, act + L.k, act + L.v, act + L.oz, st);
   if (s != TSP_OK) return s;
+  // Training (the backward's weight gradients read x as a zigzag copy, which
+  // they stream faster than remapped natural rows): x is permuted and saved,
+  // y still leaves in natural order through the down projection.
+  if (folded_io(p)) return mlp_impl(p, batch, act + L.hz, w, y, act + L.hz, act + L.mz, act + L.gu, true, st, true);
   s = mlp_impl(p, batch, act + L.hz, w, yz, act + L.hz, act + L.mz, act + L.gu, saved != nullptr, st);
   if (s != TSP_OK) return s;
   Prof pr("zigzag unpermute", st);
@@ -669,11 +678,14 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   do {                             \
     if ((s = (expr)) != TSP_OK) return s; \
   } while (0)
-  // MLP backward
+  // dy enters through a zigzag copy (the weight gradients stream it faster
+  // than remapped natural rows); dx leaves in natural order through the dx GEMM.
+  const bool fold = folded_io(p);
   {
     Prof pr("permute dy", st);
     TSP_TRY(cuda_status(launch_zigzag_rows(dy, wb + L.dyz, h * eb, p->D, batch, p->seq, true, st), "permute dy"));
   }
+  // MLP backward
   // Every weight and activation is read in the layout it is stored in: the
   // GEMM takes operands stored [K][M] / [K][N] (MN-major) where the product
   // needs their transpose.
@@ -812,8 +824,9 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   }
   {
     EpiParams e = base_epi(p, batch);
-    e.out = wb + L.dxz;
+    e.out = fold ? dx : wb + L.dxz;
     e.ldo = h;
+    e.out_natural = fold;
     e.resid = wb + L.dhz;
     e.ldr = h;
     // dx = dH + dQKV Wqkv: B = packed qkv [h + 2hk][h] read MN-major
@@ -826,6 +839,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
     // dWqkv = dQKV^T xz: A = dQKV [T][h + 2hk], B = xz [T][h], both MN-major
     TSP_TRY(run_gemm(p, wb + L.dqkv, W3, sv + A.xz, h, W3, h, T, EPI_STORE, e, st, "dW_QKV", true, true));
   }
+  if (fold) return TSP_OK;
   Prof pr_dx("unpermute dx", st);
   return cuda_status(launch_zigzag_rows(wb + L.dxz, dx, h * eb, p->D, batch, p->seq, false, st), "unpermute dx");
 #undef TSP_TRY
