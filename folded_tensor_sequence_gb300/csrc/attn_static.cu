@@ -60,6 +60,8 @@ void* scratch_on_current_device(cudaError_t* err) {
 extern "C" tsp_status tsp_attention_fwd_static(const tsp_plan* plan, int batch, const void* xz,
                                                const tsp_weights* weights, void* a_out, void* lse, void* stream) {
   if (!plan) return tsp::report_error(TSP_ERR_INVALID_ARG, "tsp_attention_fwd_static: plan is NULL");
+  // an empty (or negative) batch needs no scratch: validated and answered without touching the device
+  if (batch <= 0) return tsp_attention_fwd(plan, batch, xz, weights, a_out, lse, nullptr, 0, stream);
   const size_t need = tsp_workspace_bytes(plan, batch, TSP_OP_ATTENTION_FWD);
   if (need > kStaticScratchBytes) {
     char msg[200];

@@ -40,6 +40,9 @@
  *     as TSP_ERR_TIMEOUT.
  *   - tsp_last_error_message() gives a thread-local description of the last
  *     non-OK status.
+ *   - batch = 0 (no tokens) is valid for every call that takes a batch of
+ *     sequences except tsp_decode_step: it returns TSP_OK, reads no pointer
+ *     and enqueues nothing; the workspace and saved sizes for it are 0.
  *
  * Grouped-query attention (plans from tsp_plan_create_gqa): K and V have
  * Hk <= H heads, Wk and Wv are [h][hk] with hk = Hk * head_dim, and query

@@ -166,3 +166,29 @@ def test_deterministic_setting(tsp):
     # the backward workspace holds the fp32 dQ accumulator (T x h x 4 bytes) either way
     T, h = 2 * 16384, 4096
     assert tsp.tsp_workspace_bytes(p, 2, tsp.TSP_OP_LAYER_BWD) >= T * h * 4
+
+
+def test_empty_batch_is_a_no_op(tsp):
+    """batch 0 (no tokens) is valid for every entry point that takes a batch of
+    sequences: it returns TSP_OK without reading a pointer or touching the
+    device (this runs without a GPU, with every pointer NULL).  Decode batches
+    are 1..8 sequences and reject 0."""
+    L = tsp.lib()
+    for dt in ("bf16", "f32"):
+        p = tsp.tsp_plan_create(2, 256, 256, 2, 128, 512, dt)
+        h = p.handle
+        assert L.tsp_zigzag_permute(h, 0, None, None, None) == tsp.TSP_OK
+        assert L.tsp_zigzag_unpermute(h, 0, None, None, None) == tsp.TSP_OK
+        assert L.tsp_kv_gather(h, 0, None, None, None, None, None) == tsp.TSP_OK
+        assert L.tsp_attention_fwd(h, 0, None, None, None, None, None, 0, None) == tsp.TSP_OK
+        assert L.tsp_attention_fwd_static(h, 0, None, None, None, None, None) == tsp.TSP_OK
+        assert L.tsp_gated_mlp_fwd(h, 0, None, None, None, None, 0, None) == tsp.TSP_OK
+        assert L.tsp_layer_fwd(h, 0, None, None, None, None, None, 0, None) == tsp.TSP_OK
+        assert L.tsp_layer_bwd(h, 0, None, None, None, None, None, None, None, 0, None) == tsp.TSP_OK
+        assert tsp.tsp_saved_bytes(p, 0) == 0
+        for op in (tsp.TSP_OP_ATTENTION_FWD, tsp.TSP_OP_GATED_MLP_FWD, tsp.TSP_OP_LAYER_FWD, tsp.TSP_OP_LAYER_BWD):
+            assert tsp.tsp_workspace_bytes(p, 0, op) == 0
+        # a negative batch is still an error, on the static entry point too
+        assert L.tsp_attention_fwd_static(h, -1, None, None, None, None, None) == tsp.TSP_ERR_INVALID_ARG
+    p = tsp.tsp_plan_create(2, 256, 256, 2, 128, 512, "bf16")
+    assert L.tsp_decode_step(p.handle, 0, 0, None, None, None, None, None, None, 0, None) == tsp.TSP_ERR_INVALID_ARG
