@@ -414,6 +414,17 @@ def main():
     value = whole_job_rate(ws, flops, args.steps, ms) / 1e12
     tokens_s = whole_job_rate(ws, tokens_per_step, args.steps, ms)
 
+    # ---- spread of single steps (same stream, separate pass): min / median ---
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for ea, eb in evs:
+        ea.record(stream)
+        step()
+        eb.record(stream)
+    torch.cuda.synchronize(dev)
+    per = sorted(ea.elapsed_time(eb) for ea, eb in evs)
+    spread = {"min": round(per[0], 4), "median": round(statistics.median(per), 4), "max": round(per[-1], 4),
+              "n": len(per), "note": "rank 0, one event pair per step, after the timed region"}
+
     # ---- per-kernel timing (same stream, separate pass) ---------------------
     tsp.tsp_profile_enable(True)
     for _ in range(args.steps):
@@ -503,7 +514,8 @@ def main():
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "step_ms": spread,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (splitmix64 + Box-Muller, seed 0)",
             "tokens_per_s": round(tokens_s, 1),
             "pct_of_peak": {"burst": round(value / ws / peaks["bf16_tflops"], 4),
