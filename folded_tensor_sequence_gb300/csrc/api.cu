@@ -18,10 +18,14 @@
 //      gate/up GEMM with the SiLU*up epilogue and one down GEMM whose K loop is
 //      the ring's sum over shards (+ residual);
 //   4. unpermute back to natural order.
+// For bf16 plans whose chunks are whole 128-row tiles the permute of x and
+// the unpermute of y (and, in training, of dx) are not separate passes: the
+// GEMMs read and write those rows through remapped row coordinates.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <cmath>
 #include <initializer_list>
 #include <mutex>
@@ -234,7 +238,10 @@ struct Prof {
     ProfState& P = prof();
     std::lock_guard<std::mutex> g(P.mu);
     cudaEvent_t b = P.get();
-    if (!b) return;
+    if (!b) {
+      P.pool.push_back(a);  // no closing event: the step goes unrecorded, the event is reused
+      return;
+    }
     cudaEventRecord(b, st);
     P.recs.push_back({name, a, b});
   }
@@ -366,16 +373,21 @@ void prof_end(cudaStream_t) {
   t_prof_stack.pop_back();
 }
 
+// Per-device caches below are filled on first use by whichever host thread
+// gets there; every thread computes the same value, so a relaxed atomic store
+// is enough.
 unsigned int* dev_error_word() {
-  static unsigned int* ptrs[64] = {};
+  static std::atomic<unsigned int*> ptrs[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
+  unsigned int* p = ptrs[dev].load(std::memory_order_relaxed);
+  if (!p) {
     void* a = nullptr;
     if (cudaGetSymbolAddress(&a, g_dev_error_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<unsigned int*>(a);
+    p = static_cast<unsigned int*>(a);
+    ptrs[dev].store(p, std::memory_order_relaxed);
   }
-  return ptrs[dev];
+  return p;
 }
 
 namespace {
@@ -394,15 +406,15 @@ bool needs_setup(const std::atomic<unsigned long long>& done) {
 void mark_setup_done(std::atomic<unsigned long long>& done) { done.fetch_or(device_bit()); }
 
 int num_sms() {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (!cache[dev]) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 }  // namespace tsp
