@@ -7,6 +7,7 @@ Each .cu file compiles in parallel with nvcc; the objects are linked into
 
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -48,6 +49,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    # One build at a time (several processes may ask at once, e.g. parallel
+    # test workers): the others wait on the lock and then find the library
+    # up to date.
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return LIB
+            return _compile(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _compile(verbose: bool) -> str:
     nvcc = _nvcc()
     procs = []
     for src in SOURCES:
