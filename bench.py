@@ -45,11 +45,21 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # without its own capture, or a source changed since, reports null.
 NCU_TRAFFIC = {
     ("gate/up projection", "bf16_D8_b2_s16384_h4096"):
-        (2.16e9 + 0.926e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "abab59fbc329b85d"),
+        (2.16e9 + 0.9264e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "ab6f317c285c597d"),
+    ("gate/up projection", "bf16_gqa8_D8_b2_s16384_h4096"):
+        (2.16e9 + 0.9268e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "ab6f317c285c597d"),
+    ("gate/up projection", "bf16_D4_s4096_h2048"):
+        (62.96e6 + 10.44e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "ab6f317c285c597d"),
     ("attention", "bf16_D8_b2_s16384_h4096"):
         (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
+    ("attention", "bf16_D8_b1_s65536_h4096"):
+        (2.19e9 + 0.5294e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
         (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
+    ("attention bwd fused", "bf16_fwdbwd_D8_b1_s8192_h4096"):
+        (407.27e6 + 221.83e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
+    ("attention bwd fused", "bf16_fwdbwd_gqa8_D8_b1_s8192_h4096"):
+        (652.95e6 + 290.93e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
     ("decode attention", "bf16_decode_D8_b1_ctx131072_h4096"):
         (2.15e9 + 0.00292e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "3bfb1d17f6da32df"),
     ("decode attention", "bf16_decode_gqa8_D8_b4_ctx131072_h4096"):
