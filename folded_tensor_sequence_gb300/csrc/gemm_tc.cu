@@ -39,6 +39,14 @@ constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+// SwiGLU-derivative epilogue: G and U of 32 rows x 32 columns (bf16, 64-byte
+// rows) per chunk, two chunks per epilogue warp, in shared memory behind the
+// stage ring (1 KB of barriers between them).
+constexpr uint32_t EPI_CHUNK_BYTES = 2 * 32 * 64;
+constexpr uint32_t EPI_BUF_BYTES = 4 * 2 * EPI_CHUNK_BYTES;
+template <int EPI>
+constexpr size_t smem_bytes() { return SMEM_BYTES + (EPI == EPI_DSWIGLU ? 1024 + EPI_BUF_BYTES : 0); }
+static_assert(SMEM_BYTES + 1024 + EPI_BUF_BYTES <= 227 * 1024, "shared memory");
 // Raster: tiles are visited in bands of group_m m-tiles (all n-tiles of a band
 // before the next band), group_m chosen so one band of A is ~32 MB and stays
 // in L2 while the B operand streams past it.
@@ -83,6 +91,25 @@ __device__ __forceinline__ void load32_bf16(const void* src, float (&v)[32]) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
+// TMA tensor store shared -> global (bulk-group completion).  c0 * 2 bytes
+// must be a multiple of 16; rows beyond the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int c0, int c1, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(c0), "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until every committed bulk store of this thread has read its shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Packed gate_up column of dM column n: 128-column gate blocks interleaved
+// with their up blocks (the up column is this + 128).
+__device__ __forceinline__ int gu_col(int n) { return (n / 128) * 256 + n % 128; }
+
 // Zigzag row m of [D][B][2C] -> natural row b*S + pos.
 __device__ __forceinline__ int64_t zigzag_row_to_natural(int64_t m, const EpiParams& ep) {
   const int64_t twoC = 2 * (int64_t)ep.C;
@@ -112,6 +139,7 @@ __device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep
 template <int EPI, bool AMN, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmDG,
                         const GemmShape shape, const EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -122,7 +150,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* gbar = drain + 1;  // [4 warps][2] SwiGLU-derivative staging buffers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + 8);
+  uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // EPI_BUF_BYTES, EPI_DSWIGLU only
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -138,12 +168,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], 128);
     }
     mbar_init(drain, 1);
+    if constexpr (EPI == EPI_DSWIGLU)
+      for (int i = 0; i < 8; ++i) mbar_init(&gbar[i], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (EPI == EPI_DSWIGLU) {
+      tma_prefetch_desc(&tmG);
+      tma_prefetch_desc(&tmDG);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -239,24 +275,37 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- epilogue: warps 2..5 ----------------
     const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
     const int row = quad * 32 + lane;
+    // SwiGLU derivative: the warp's G|U chunks (its 32 rows x 32 columns of G
+    // and of U) stream through two staging buffers; chunk q (counted over all
+    // of the CTA's tiles) uses buffer q & 1.  Lane 0 issues the TMA loads two
+    // chunks ahead and the TMA stores of dG|dU.
+    uint8_t* gbuf = gstage + quad * 2 * EPI_CHUNK_BYTES;
+    uint64_t* gb_full = gbar + quad * 2;
+    uint32_t q_issued = 0, q_done = 0;
+    auto issue_gu = [&](int tt, int c) {  // lane 0: G|U of chunk c of tile tt
+      int mq, nq;
+      tile_coords(tt, shape, mq, nq);
+      const int b = q_issued & 1;
+      uint8_t* dst = gbuf + b * EPI_CHUNK_BYTES;
+      const int gcol = gu_col(nq * BN + c * 32), r0 = mq * BM + quad * 32;
+      mbar_arrive_expect_tx(&gb_full[b], EPI_CHUNK_BYTES);
+      tma_load_2d(dst, &tmG, gcol, r0, &gb_full[b]);
+      tma_load_2d(dst + EPI_CHUNK_BYTES / 2, &tmG, gcol + 128, r0, &gb_full[b]);
+      ++q_issued;
+    };
+    if constexpr (EPI == EPI_DSWIGLU) {
+      if (lane == 0) {
+        issue_gu(blockIdx.x, 0);
+        issue_gu(blockIdx.x, 1);
+      }
+    }
+    bool epi_ok = true;
     uint32_t tl = 0;
-    for (int t = blockIdx.x; t < shape.num_tiles; t += gridDim.x, ++tl) {
+    for (int t = blockIdx.x; t < shape.num_tiles && epi_ok; t += gridDim.x, ++tl) {
       int mt, nt;
       tile_coords(t, shape, mt, nt);
       const int acc = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
-      if constexpr (EPI == EPI_DSWIGLU) {
-        // The tile's 256 dM columns are two packed 128-column gate/up blocks:
-        // 1 KB of saved G|U per row, contiguous.  Pull it into L2 while the
-        // tile's main loop runs.
-        const int64_t mp = (int64_t)mt * BM + row;
-        if (mp < shape.M) {
-          const char* src = reinterpret_cast<const char*>(reinterpret_cast<const __nv_bfloat16*>(ep.resid) +
-                                                          mp * ep.ldr + (int64_t)nt * 2 * BN);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 128 * i));
-        }
-      }
       // Warp-uniform decision: tcgen05.ld below needs every lane of the warp.
       const bool got = mbar_wait(&tfull[acc], aph, abort_flag, ep.err, (KID_GEMM_TC << 8) | 6);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -284,45 +333,38 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else if constexpr (EPI == EPI_DSWIGLU) {
-        // acc = dM[m][f]; dG = dM * u * s * (1 + g (1 - s)), dU = dM * g * s with s = sigmoid(g),
-        // read from and written to the packed gate_up order.  Chunk c+1's G/U
-        // are loaded before chunk c is computed.
-        const __nv_bfloat16* gu = reinterpret_cast<const __nv_bfloat16*>(ep.resid) + m * ep.ldr;
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo;
-        auto gcol_of = [&](int c) {
-          const int64_t n = (int64_t)nt * BN + c * 32;
-          return (n / 128) * 256 + n % 128;
-        };
-        uint4 gcur[4], ucur[4];
-        if (valid) {
-          const uint4* gs = reinterpret_cast<const uint4*>(gu + gcol_of(0));
-          const uint4* us = reinterpret_cast<const uint4*>(gu + gcol_of(0) + 128);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            gcur[i] = gs[i];
-            ucur[i] = us[i];
-          }
-        }
+        // acc = dM[m][f]; dG = dM * u * s * (1 + g (1 - s)), dU = dM * g * s with
+        // s = sigmoid(g), in the packed gate_up order.  The thread's row of G and
+        // U is read from the staging buffer (64-byte rows, 64-byte swizzle: 16-byte
+        // unit j of row r sits at unit j ^ ((r >> 1) & 3)), dG and dU are written
+        // over it, and the buffer goes back to global memory by TMA.  Rows past
+        // M load as zeros and are not stored.
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < BN / 32; ++c, ++q_done) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
-          if (!valid) continue;
-          uint4 gnx[4], unx[4];
-          if (c + 1 < BN / 32) {
-            const uint4* gs = reinterpret_cast<const uint4*>(gu + gcol_of(c + 1));
-            const uint4* us = reinterpret_cast<const uint4*>(gu + gcol_of(c + 1) + 128);
+          const int gb = q_done & 1;
+          const bool landed =
+              mbar_wait(&gb_full[gb], (q_done >> 1) & 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 7);
+          if (!__all_sync(0xffffffffu, landed)) {
+            epi_ok = false;
+            break;
+          }
+          uint8_t* gs = gbuf + gb * EPI_CHUNK_BYTES;
+          uint8_t* us = gs + EPI_CHUNK_BYTES / 2;
+          uint32_t off[4];
+          uint4 g4[4], u4[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              gnx[i] = gs[i];
-              unx[i] = us[i];
-            }
+          for (int j = 0; j < 4; ++j) {
+            off[j] = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+            g4[j] = *reinterpret_cast<const uint4*>(gs + off[j]);
+            u4[j] = *reinterpret_cast<const uint4*>(us + off[j]);
           }
           float dg[32], du[32];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t gw[4] = {gcur[i].x, gcur[i].y, gcur[i].z, gcur[i].w};
-            const uint32_t uw[4] = {ucur[i].x, ucur[i].y, ucur[i].z, ucur[i].w};
+            const uint32_t gw[4] = {g4[i].x, g4[i].y, g4[i].z, g4[i].w};
+            const uint32_t uw[4] = {u4[i].x, u4[i].y, u4[i].z, u4[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float2 g2 = unpack_bf16x2(gw[j]), u2 = unpack_bf16x2(uw[j]);
@@ -336,17 +378,33 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
-          const int64_t gcol = gcol_of(c);
-          store32_bf16(out + gcol, dg);
-          store32_bf16(out + gcol + 128, du);
-          if (c + 1 < BN / 32) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              gcur[i] = gnx[i];
-              ucur[i] = unx[i];
-            }
+          for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<uint4*>(gs + off[j]) =
+                make_uint4(pack_bf16x2(dg[8 * j + 0], dg[8 * j + 1]), pack_bf16x2(dg[8 * j + 2], dg[8 * j + 3]),
+                           pack_bf16x2(dg[8 * j + 4], dg[8 * j + 5]), pack_bf16x2(dg[8 * j + 6], dg[8 * j + 7]));
+            *reinterpret_cast<uint4*>(us + off[j]) =
+                make_uint4(pack_bf16x2(du[8 * j + 0], du[8 * j + 1]), pack_bf16x2(du[8 * j + 2], du[8 * j + 3]),
+                           pack_bf16x2(du[8 * j + 4], du[8 * j + 5]), pack_bf16x2(du[8 * j + 6], du[8 * j + 7]));
           }
+          fence_proxy_async_smem();  // the stores below read what the threads wrote
+          __syncwarp();
+          if (lane == 0) {
+            const int gcol = gu_col(nt * BN + c * 32), r0 = mt * BM + quad * 32;
+            if (r0 < shape.M) {  // a box starting past the last row has nothing to store
+              tma_store_2d(&tmDG, gcol, r0, gs);
+              tma_store_2d(&tmDG, gcol + 128, r0, us);
+              bulk_commit();
+            }
+            bulk_wait_read_all();  // the buffer is free once the stores have read it
+            if (c + 2 < BN / 32)
+              issue_gu(t, c + 2);
+            else if (t + (int)gridDim.x < shape.num_tiles)
+              issue_gu(t + (int)gridDim.x, c + 2 - BN / 32);
+          }
+          __syncwarp();
         }
+        if (!epi_ok) break;
       } else {
         int b = 0;
         int64_t p = 0, nat = m;
@@ -398,6 +456,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
+    if constexpr (EPI == EPI_DSWIGLU) {
+      // Before leaving: every dG|dU store complete, and (on the abort path) every
+      // G|U load still in flight landed (bounded).
+      if (lane == 0) {
+        bulk_wait_all();
+        volatile int dummy = 0;
+        for (uint32_t q = q_done; q < q_issued; ++q)
+          mbar_wait(&gb_full[q & 1], (q >> 1) & 1, &dummy, ep.err, (KID_GEMM_TC << 8) | 8);
+      }
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
@@ -448,18 +517,33 @@ bool make_tma_2d_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t co
 
 namespace {
 
+// 2-D bf16 map of the SwiGLU-derivative epilogue's G|U / dG|dU matrices
+// ([rows][cols], row stride ld elements): box 32 columns x 32 rows, 64-byte
+// swizzle.
+bool make_tma_epi(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI, bool AMN, bool BMN>
-cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& s, const EpiParams& ep,
-                       cudaStream_t stream) {
+cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg, const CUtensorMap& tdg,
+                       const GemmShape& s, const EpiParams& ep, cudaStream_t stream) {
   static std::atomic<unsigned long long> configured{0};  // devices set up for this instantiation
   if (needs_setup(configured)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, AMN, BMN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<EPI>());
     if (e != cudaSuccess) return e;
     mark_setup_done(configured);
   }
   const int grid = s.num_tiles < num_sms() ? s.num_tiles : num_sms();
-  gemm_bf16_tc_kernel<EPI, AMN, BMN><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, s, ep);
+  gemm_bf16_tc_kernel<EPI, AMN, BMN><<<grid, THREADS, smem_bytes<EPI>(), stream>>>(ta, tb, tg, tdg, s, ep);
   return cudaGetLastError();
 }
 
@@ -475,6 +559,15 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   const bool ok_a = a_mn ? make_tma_2d_bf16(&ta, A, K, M, lda, 64) : make_tma_2d_bf16(&ta, A, M, K, lda, BM);
   const bool ok_b = b_mn ? make_tma_2d_bf16(&tb, B, K, N, ldb, 64) : make_tma_2d_bf16(&tb, B, N, K, ldb, BN);
   if (!ok_a || !ok_b) return TSP_ERR_CUDA;
+  // G|U in and dG|dU out of the SwiGLU-derivative epilogue, moved by TMA
+  CUtensorMap tg{}, tdg{};
+  if (epi == EPI_DSWIGLU) {
+    if (!ep.resid || !ep.out || ((reinterpret_cast<uintptr_t>(ep.resid) | reinterpret_cast<uintptr_t>(ep.out)) & 15) ||
+        ep.ldr % 8 || ep.ldo % 8 || ep.ldr < 2 * (int64_t)N || ep.ldo < 2 * (int64_t)N)
+      return TSP_ERR_INVALID_ARG;
+    if (!make_tma_epi(&tg, ep.resid, M, 2 * (int64_t)N, ep.ldr) || !make_tma_epi(&tdg, ep.out, M, 2 * (int64_t)N, ep.ldo))
+      return TSP_ERR_CUDA;
+  }
   GemmShape s;
   s.M = M;
   s.N = N;
@@ -491,15 +584,15 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   cudaError_t e;
   const int mode = (a_mn ? 2 : 0) | (b_mn ? 1 : 0);
   switch (epi * 4 + mode) {
-    case EPI_STORE * 4 + 0: e = launch_epi<EPI_STORE, false, false>(ta, tb, s, ep, stream); break;
-    case EPI_STORE * 4 + 1: e = launch_epi<EPI_STORE, false, true>(ta, tb, s, ep, stream); break;
-    case EPI_STORE * 4 + 3: e = launch_epi<EPI_STORE, true, true>(ta, tb, s, ep, stream); break;
-    case EPI_RESID * 4 + 0: e = launch_epi<EPI_RESID, false, false>(ta, tb, s, ep, stream); break;
-    case EPI_RESID * 4 + 1: e = launch_epi<EPI_RESID, false, true>(ta, tb, s, ep, stream); break;
-    case EPI_QKV * 4 + 0: e = launch_epi<EPI_QKV, false, false>(ta, tb, s, ep, stream); break;
-    case EPI_SWIGLU * 4 + 0: e = launch_epi<EPI_SWIGLU, false, false>(ta, tb, s, ep, stream); break;
-    case EPI_DSWIGLU * 4 + 0: e = launch_epi<EPI_DSWIGLU, false, false>(ta, tb, s, ep, stream); break;
-    case EPI_DSWIGLU * 4 + 1: e = launch_epi<EPI_DSWIGLU, false, true>(ta, tb, s, ep, stream); break;
+    case EPI_STORE * 4 + 0: e = launch_epi<EPI_STORE, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_STORE * 4 + 1: e = launch_epi<EPI_STORE, false, true>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_STORE * 4 + 3: e = launch_epi<EPI_STORE, true, true>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_RESID * 4 + 0: e = launch_epi<EPI_RESID, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_RESID * 4 + 1: e = launch_epi<EPI_RESID, false, true>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_QKV * 4 + 0: e = launch_epi<EPI_QKV, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_SWIGLU * 4 + 0: e = launch_epi<EPI_SWIGLU, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_DSWIGLU * 4 + 0: e = launch_epi<EPI_DSWIGLU, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_DSWIGLU * 4 + 1: e = launch_epi<EPI_DSWIGLU, false, true>(ta, tb, tg, tdg, s, ep, stream); break;
     default: return TSP_ERR_UNSUPPORTED;
   }
   return e == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;

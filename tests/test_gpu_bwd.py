@@ -46,6 +46,8 @@ def run_bwd(tsp, cfg, inp, deterministic=0):
 
 BWD_CASES = [
     LayerConfig("bwd_D2_s256", D=2, batch=1, seq=256, hidden=256, heads=2, head_dim=128, ffn=512, dtype="bf16"),
+    # ragged: chunks of 80 queries, T = 320 tokens leaves a 64-row tail in every token-major GEMM
+    LayerConfig("bwd_D2_s320", D=2, batch=1, seq=320, hidden=256, heads=2, head_dim=128, ffn=512, dtype="bf16"),
     LayerConfig("bwd_D4_b2_s1024", D=4, batch=2, seq=1024, hidden=512, heads=4, head_dim=128, ffn=768, dtype="bf16"),
     LayerConfig("bwd_D8_s2048", D=8, batch=1, seq=2048, hidden=1024, heads=8, head_dim=128, ffn=1024, dtype="bf16"),
     LayerConfig("bwd_D3_s1152", D=3, batch=1, seq=1152, hidden=768, heads=6, head_dim=128, ffn=1536, dtype="bf16"),
