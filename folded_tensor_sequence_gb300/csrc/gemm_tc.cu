@@ -39,14 +39,20 @@ constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
-// SwiGLU-derivative epilogue: G and U of 32 rows x 32 columns (bf16, 64-byte
-// rows) per chunk, two chunks per epilogue warp, in shared memory behind the
-// stage ring (1 KB of barriers between them).
+// Epilogue staging in shared memory behind the stage ring (1 KB of barriers
+// between them), 32 rows x 32 columns of bf16 (64-byte rows) per matrix:
+//   SwiGLU derivative: G and U of a chunk, two chunks per epilogue warp;
+//   SwiGLU: the chunk's G, U (kept for the backward) and SiLU(G)*U outputs.
 constexpr uint32_t EPI_CHUNK_BYTES = 2 * 32 * 64;
-constexpr uint32_t EPI_BUF_BYTES = 4 * 2 * EPI_CHUNK_BYTES;
+constexpr uint32_t DSW_STAGE_BYTES = 4 * 2 * EPI_CHUNK_BYTES;
+constexpr uint32_t SWG_WARP_BYTES = 3 * 32 * 64;
+constexpr uint32_t SWG_STAGE_BYTES = 4 * SWG_WARP_BYTES;
 template <int EPI>
-constexpr size_t smem_bytes() { return SMEM_BYTES + (EPI == EPI_DSWIGLU ? 1024 + EPI_BUF_BYTES : 0); }
-static_assert(SMEM_BYTES + 1024 + EPI_BUF_BYTES <= 227 * 1024, "shared memory");
+constexpr size_t smem_bytes() {
+  return SMEM_BYTES + (EPI == EPI_DSWIGLU ? 1024 + DSW_STAGE_BYTES : EPI == EPI_SWIGLU ? 1024 + SWG_STAGE_BYTES : 0);
+}
+static_assert(SMEM_BYTES + 1024 + DSW_STAGE_BYTES <= 227 * 1024, "shared memory");
+static_assert(SMEM_BYTES + 1024 + SWG_STAGE_BYTES <= 227 * 1024, "shared memory");
 // Raster: tiles are visited in bands of group_m m-tiles (all n-tiles of a band
 // before the next band), group_m chosen so one band of A is ~32 MB and stays
 // in L2 while the B operand streams past it.
@@ -136,10 +142,13 @@ __device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep
 // AMN / BMN: the operand is MN-major (global [K][M] / [K][N], M / N
 // contiguous), loaded as 64-wide boxes of [64 K rows][64 elements] into 8 KB
 // chunks and described with the MN-major 128-byte-swizzle descriptor.
+// tmE0 / tmE1: epilogue tensor maps (32 x 32 boxes, 64-byte swizzle):
+//   EPI_DSWIGLU: saved G|U (read) / dG|dU (written);
+//   EPI_SWIGLU:  the G|U copy kept for the backward / SiLU(G)*U.
 template <int EPI, bool AMN, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmDG,
+                        const __grid_constant__ CUtensorMap tmE0, const __grid_constant__ CUtensorMap tmE1,
                         const GemmShape shape, const EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -152,7 +161,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = tempty + 2;
   uint64_t* gbar = drain + 1;  // [4 warps][2] SwiGLU-derivative staging buffers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + 8);
-  uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // EPI_BUF_BYTES, EPI_DSWIGLU only
+  uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // epilogue staging (EPI_DSWIGLU, EPI_SWIGLU)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -176,9 +185,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (EPI == EPI_DSWIGLU) {
-      tma_prefetch_desc(&tmG);
-      tma_prefetch_desc(&tmDG);
+    if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_SWIGLU) {
+      if (EPI == EPI_DSWIGLU || ep.aux) tma_prefetch_desc(&tmE0);  // the SwiGLU map exists only with aux
+      tma_prefetch_desc(&tmE1);
     }
   }
   if (warp == 1) {
@@ -289,8 +298,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint8_t* dst = gbuf + b * EPI_CHUNK_BYTES;
       const int gcol = gu_col(nq * BN + c * 32), r0 = mq * BM + quad * 32;
       mbar_arrive_expect_tx(&gb_full[b], EPI_CHUNK_BYTES);
-      tma_load_2d(dst, &tmG, gcol, r0, &gb_full[b]);
-      tma_load_2d(dst + EPI_CHUNK_BYTES / 2, &tmG, gcol + 128, r0, &gb_full[b]);
+      tma_load_2d(dst, &tmE0, gcol, r0, &gb_full[b]);
+      tma_load_2d(dst + EPI_CHUNK_BYTES / 2, &tmE0, gcol + 128, r0, &gb_full[b]);
       ++q_issued;
     };
     if constexpr (EPI == EPI_DSWIGLU) {
@@ -314,22 +323,50 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = m < shape.M;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       if constexpr (EPI == EPI_SWIGLU) {
+        // The tile's 256 columns are a 128-column gate block and its up block.
+        // Per 32-column chunk the warp stages its 32 rows of SiLU(G)*U (and, for
+        // the backward, of G and U) in shared memory (64-byte rows, 64-byte
+        // swizzle: 16-byte unit j of row r at unit j ^ ((r >> 1) & 3)) and one
+        // lane stores them by TMA; rows past M are not written.
+        uint8_t* sg = gstage + quad * SWG_WARP_BYTES;
+        uint8_t* su = sg + 2048;
+        uint8_t* so = sg + 4096;
+        const bool keep = ep.aux != nullptr;
+        const int r0 = mt * BM + quad * 32;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float g[32], u[32];
           tmem_ld32(tbase + c * 32, g);
           tmem_ld32(tbase + 128 + c * 32, u);
-          if (valid) {
-            if (ep.aux) {
-              __nv_bfloat16* aux = reinterpret_cast<__nv_bfloat16*>(ep.aux) + m * ep.ldx + (int64_t)nt * BN;
-              store32_bf16(aux + c * 32, g);
-              store32_bf16(aux + 128 + c * 32, u);
-            }
-            float o[32];
+          float o[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = silu_f(g[i]) * u[i];
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + (int64_t)nt * (BN / 2);
-            store32_bf16(out + c * 32, o);
+          for (int i = 0; i < 32; ++i) o[i] = silu_f(g[i]) * u[i];
+          if (lane == 0) bulk_wait_read_all();  // the previous chunk's stores have read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+            if (keep) {
+              *reinterpret_cast<uint4*>(sg + off) =
+                  make_uint4(pack_bf16x2(g[8 * j + 0], g[8 * j + 1]), pack_bf16x2(g[8 * j + 2], g[8 * j + 3]),
+                             pack_bf16x2(g[8 * j + 4], g[8 * j + 5]), pack_bf16x2(g[8 * j + 6], g[8 * j + 7]));
+              *reinterpret_cast<uint4*>(su + off) =
+                  make_uint4(pack_bf16x2(u[8 * j + 0], u[8 * j + 1]), pack_bf16x2(u[8 * j + 2], u[8 * j + 3]),
+                             pack_bf16x2(u[8 * j + 4], u[8 * j + 5]), pack_bf16x2(u[8 * j + 6], u[8 * j + 7]));
+            }
+            *reinterpret_cast<uint4*>(so + off) =
+                make_uint4(pack_bf16x2(o[8 * j + 0], o[8 * j + 1]), pack_bf16x2(o[8 * j + 2], o[8 * j + 3]),
+                           pack_bf16x2(o[8 * j + 4], o[8 * j + 5]), pack_bf16x2(o[8 * j + 6], o[8 * j + 7]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && r0 < shape.M) {
+            if (keep) {
+              tma_store_2d(&tmE0, nt * BN + c * 32, r0, sg);
+              tma_store_2d(&tmE0, nt * BN + 128 + c * 32, r0, su);
+            }
+            tma_store_2d(&tmE1, nt * (BN / 2) + c * 32, r0, so);
+            bulk_commit();
           }
         }
       } else if constexpr (EPI == EPI_DSWIGLU) {
@@ -392,8 +429,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0) {
             const int gcol = gu_col(nt * BN + c * 32), r0 = mt * BM + quad * 32;
             if (r0 < shape.M) {  // a box starting past the last row has nothing to store
-              tma_store_2d(&tmDG, gcol, r0, gs);
-              tma_store_2d(&tmDG, gcol + 128, r0, us);
+              tma_store_2d(&tmE1, gcol, r0, gs);
+              tma_store_2d(&tmE1, gcol + 128, r0, us);
               bulk_commit();
             }
             bulk_wait_read_all();  // the buffer is free once the stores have read it
@@ -455,6 +492,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
+    }
+    if constexpr (EPI == EPI_SWIGLU) {
+      if (lane == 0) bulk_wait_all();  // every staged store complete before leaving
+      __syncwarp();
     }
     if constexpr (EPI == EPI_DSWIGLU) {
       // Before leaving: every dG|dU store complete, and (on the abort path) every
@@ -559,8 +600,16 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   const bool ok_a = a_mn ? make_tma_2d_bf16(&ta, A, K, M, lda, 64) : make_tma_2d_bf16(&ta, A, M, K, lda, BM);
   const bool ok_b = b_mn ? make_tma_2d_bf16(&tb, B, K, N, ldb, 64) : make_tma_2d_bf16(&tb, B, N, K, ldb, BN);
   if (!ok_a || !ok_b) return TSP_ERR_CUDA;
-  // G|U in and dG|dU out of the SwiGLU-derivative epilogue, moved by TMA
+  // Epilogue tensor maps: G|U in and dG|dU out of the SwiGLU-derivative
+  // epilogue; the G|U copy and SiLU(G)*U out of the SwiGLU epilogue.
   CUtensorMap tg{}, tdg{};
+  if (epi == EPI_SWIGLU) {
+    if (!ep.out || (reinterpret_cast<uintptr_t>(ep.out) & 15) || ep.ldo % 8 || ep.ldo < N / 2 ||
+        (ep.aux && ((reinterpret_cast<uintptr_t>(ep.aux) & 15) || ep.ldx % 8 || ep.ldx < (int64_t)N)))
+      return TSP_ERR_INVALID_ARG;
+    if ((ep.aux && !make_tma_epi(&tg, ep.aux, M, N, ep.ldx)) || !make_tma_epi(&tdg, ep.out, M, N / 2, ep.ldo))
+      return TSP_ERR_CUDA;
+  }
   if (epi == EPI_DSWIGLU) {
     if (!ep.resid || !ep.out || ((reinterpret_cast<uintptr_t>(ep.resid) | reinterpret_cast<uintptr_t>(ep.out)) & 15) ||
         ep.ldr % 8 || ep.ldo % 8 || ep.ldr < 2 * (int64_t)N || ep.ldo < 2 * (int64_t)N)
