@@ -42,17 +42,29 @@ constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 // Epilogue staging in shared memory behind the stage ring (1 KB of barriers
 // between them), 32 rows x 32 columns of bf16 (64-byte rows) per matrix:
 //   SwiGLU derivative: G and U of a chunk, two chunks per epilogue warp;
+//   residual: the chunk's residual (the sum written over it), two chunks per warp;
 //   SwiGLU: the chunk's G, U (kept for the backward) and SiLU(G)*U outputs.
-constexpr uint32_t EPI_CHUNK_BYTES = 2 * 32 * 64;
-constexpr uint32_t DSW_STAGE_BYTES = 4 * 2 * EPI_CHUNK_BYTES;
-constexpr uint32_t SWG_WARP_BYTES = 3 * 32 * 64;
-constexpr uint32_t SWG_STAGE_BYTES = 4 * SWG_WARP_BYTES;
+constexpr uint32_t MAT_BYTES = 32 * 64;
 template <int EPI>
-constexpr size_t smem_bytes() {
-  return SMEM_BYTES + (EPI == EPI_DSWIGLU ? 1024 + DSW_STAGE_BYTES : EPI == EPI_SWIGLU ? 1024 + SWG_STAGE_BYTES : 0);
+__host__ __device__ constexpr uint32_t chunk_bytes() {  // one staged chunk of the streamed (loaded) epilogues
+  return EPI == EPI_DSWIGLU ? 2 * MAT_BYTES : EPI == EPI_RESID ? MAT_BYTES : 0;
 }
-static_assert(SMEM_BYTES + 1024 + DSW_STAGE_BYTES <= 227 * 1024, "shared memory");
-static_assert(SMEM_BYTES + 1024 + SWG_STAGE_BYTES <= 227 * 1024, "shared memory");
+// Epilogues that stream loaded chunks through the staging buffers (and own
+// the 8 staging barriers).
+template <int EPI>
+__host__ __device__ constexpr bool streamed_epi() { return chunk_bytes<EPI>() != 0; }
+constexpr uint32_t SWG_WARP_BYTES = 3 * MAT_BYTES;
+template <int EPI>
+__host__ __device__ constexpr size_t stage_bytes() {
+  return EPI == EPI_SWIGLU ? 4 * SWG_WARP_BYTES : 4 * 2 * chunk_bytes<EPI>();
+}
+template <int EPI>
+__host__ __device__ constexpr size_t smem_bytes() {
+  return SMEM_BYTES + (stage_bytes<EPI>() ? 1024 + stage_bytes<EPI>() : 0);
+}
+static_assert(smem_bytes<EPI_DSWIGLU>() <= 227 * 1024 && smem_bytes<EPI_SWIGLU>() <= 227 * 1024 &&
+                  smem_bytes<EPI_RESID>() <= 227 * 1024,
+              "shared memory");
 // Raster: tiles are visited in bands of group_m m-tiles (all n-tiles of a band
 // before the next band), group_m chosen so one band of A is ~32 MB and stays
 // in L2 while the B operand streams past it.
@@ -81,17 +93,6 @@ __device__ __forceinline__ void store32_bf16(void* dst, const float (&v)[32]) {
   for (int i = 0; i < 4; ++i) {
     d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-  }
-}
-
-__device__ __forceinline__ void load32_bf16(const void* src, float (&v)[32]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 u = s[i];
-    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
-    v[8 * i + 0] = a.x; v[8 * i + 1] = a.y; v[8 * i + 2] = b.x; v[8 * i + 3] = b.y;
-    v[8 * i + 4] = c.x; v[8 * i + 5] = c.y; v[8 * i + 6] = d.x; v[8 * i + 7] = d.y;
   }
 }
 
@@ -144,6 +145,7 @@ __device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep
 // chunks and described with the MN-major 128-byte-swizzle descriptor.
 // tmE0 / tmE1: epilogue tensor maps (32 x 32 boxes, 64-byte swizzle):
 //   EPI_DSWIGLU: saved G|U (read) / dG|dU (written);
+//   EPI_RESID:   the residual (read) / the sum (written);
 //   EPI_SWIGLU:  the G|U copy kept for the backward / SiLU(G)*U.
 template <int EPI, bool AMN, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -159,9 +161,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* gbar = drain + 1;  // [4 warps][2] SwiGLU-derivative staging buffers
+  uint64_t* gbar = drain + 1;  // [4 warps][2] staging buffers of the streamed epilogues
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + 8);
-  uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // epilogue staging (EPI_DSWIGLU, EPI_SWIGLU)
+  uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // epilogue staging (EPI_DSWIGLU, EPI_RESID, EPI_SWIGLU)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], 128);
     }
     mbar_init(drain, 1);
-    if constexpr (EPI == EPI_DSWIGLU)
+    if constexpr (streamed_epi<EPI>())
       for (int i = 0; i < 8; ++i) mbar_init(&gbar[i], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -185,8 +187,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_SWIGLU) {
-      if (EPI == EPI_DSWIGLU || ep.aux) tma_prefetch_desc(&tmE0);  // the SwiGLU map exists only with aux
+    if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_SWIGLU || EPI == EPI_RESID) {
+      if (EPI != EPI_SWIGLU || ep.aux) tma_prefetch_desc(&tmE0);  // the SwiGLU map exists only with aux
       tma_prefetch_desc(&tmE1);
     }
   }
@@ -284,28 +286,38 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- epilogue: warps 2..5 ----------------
     const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
     const int row = quad * 32 + lane;
-    // SwiGLU derivative: the warp's G|U chunks (its 32 rows x 32 columns of G
-    // and of U) stream through two staging buffers; chunk q (counted over all
-    // of the CTA's tiles) uses buffer q & 1.  Lane 0 issues the TMA loads two
-    // chunks ahead and the TMA stores of dG|dU.
-    uint8_t* gbuf = gstage + quad * 2 * EPI_CHUNK_BYTES;
+    // Streamed epilogues (SwiGLU derivative: the warp's 32 rows x 32 columns
+    // of G and of U; residual: of the residual) pass each chunk through two
+    // staging buffers; chunk q (counted over all of the CTA's tiles) uses
+    // buffer q & 1.  Lane 0 issues the TMA loads two chunks ahead and the TMA
+    // stores of the results, which the threads write over the loaded data.
+    constexpr uint32_t CH = chunk_bytes<EPI>();
+    uint8_t* gbuf = gstage + quad * 2 * CH;
     uint64_t* gb_full = gbar + quad * 2;
     uint32_t q_issued = 0, q_done = 0;
-    auto issue_gu = [&](int tt, int c) {  // lane 0: G|U of chunk c of tile tt
+    auto issue_chunk = [&](int tt, int c) {  // lane 0: the loaded data of chunk c of tile tt
       int mq, nq;
       tile_coords(tt, shape, mq, nq);
       const int b = q_issued & 1;
-      uint8_t* dst = gbuf + b * EPI_CHUNK_BYTES;
-      const int gcol = gu_col(nq * BN + c * 32), r0 = mq * BM + quad * 32;
-      mbar_arrive_expect_tx(&gb_full[b], EPI_CHUNK_BYTES);
-      tma_load_2d(dst, &tmE0, gcol, r0, &gb_full[b]);
-      tma_load_2d(dst + EPI_CHUNK_BYTES / 2, &tmE0, gcol + 128, r0, &gb_full[b]);
+      uint8_t* dst = gbuf + b * CH;
+      const int r0 = mq * BM + quad * 32;
+      mbar_arrive_expect_tx(&gb_full[b], CH);
+      if constexpr (EPI == EPI_DSWIGLU) {
+        const int gcol = gu_col(nq * BN + c * 32);
+        tma_load_2d(dst, &tmE0, gcol, r0, &gb_full[b]);
+        tma_load_2d(dst + MAT_BYTES, &tmE0, gcol + 128, r0, &gb_full[b]);
+      } else {
+        // 32 zigzag rows of a chunk of 128-row multiples are 32 consecutive natural rows
+        const int rr = (ep.resid_natural && r0 < shape.M) ? (int)zigzag_row_to_natural(r0, ep) : r0;
+        tma_load_2d(dst, &tmE0, nq * BN + c * 32, rr, &gb_full[b]);
+      }
       ++q_issued;
     };
-    if constexpr (EPI == EPI_DSWIGLU) {
+    constexpr bool streamed = streamed_epi<EPI>();
+    if constexpr (streamed) {
       if (lane == 0) {
-        issue_gu(blockIdx.x, 0);
-        issue_gu(blockIdx.x, 1);
+        issue_chunk(blockIdx.x, 0);
+        issue_chunk(blockIdx.x, 1);
       }
     }
     bool epi_ok = true;
@@ -387,8 +399,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             epi_ok = false;
             break;
           }
-          uint8_t* gs = gbuf + gb * EPI_CHUNK_BYTES;
-          uint8_t* us = gs + EPI_CHUNK_BYTES / 2;
+          uint8_t* gs = gbuf + gb * CH;
+          uint8_t* us = gs + MAT_BYTES;
           uint32_t off[4];
           uint4 g4[4], u4[4];
 #pragma unroll
@@ -435,21 +447,65 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             bulk_wait_read_all();  // the buffer is free once the stores have read it
             if (c + 2 < BN / 32)
-              issue_gu(t, c + 2);
+              issue_chunk(t, c + 2);
             else if (t + (int)gridDim.x < shape.num_tiles)
-              issue_gu(t + (int)gridDim.x, c + 2 - BN / 32);
+              issue_chunk(t + (int)gridDim.x, c + 2 - BN / 32);
+          }
+          __syncwarp();
+        }
+        if (!epi_ok) break;
+      } else if constexpr (EPI == EPI_RESID) {
+        // out = resid + acc: the chunk's residual arrives by TMA in the staging
+        // buffer (64-byte swizzle), the sum is written over it and stored by
+        // TMA.  Residual and output rows follow the natural order when asked
+        // (32 zigzag rows of a chunk of 128-row multiples are 32 consecutive
+        // natural rows); rows past M are not stored.
+        const int r0 = mt * BM + quad * 32;
+        const int orow = (ep.out_natural && r0 < shape.M) ? (int)zigzag_row_to_natural(r0, ep) : r0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c, ++q_done) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          const int gb = q_done & 1;
+          const bool landed =
+              mbar_wait(&gb_full[gb], (q_done >> 1) & 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 7);
+          if (!__all_sync(0xffffffffu, landed)) {
+            epi_ok = false;
+            break;
+          }
+          uint8_t* rs = gbuf + gb * CH;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4* cell = reinterpret_cast<uint4*>(rs + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
+            const uint4 w = *cell;
+            const float2 a = unpack_bf16x2(w.x), bb = unpack_bf16x2(w.y), cc = unpack_bf16x2(w.z),
+                         dd = unpack_bf16x2(w.w);
+            *cell = make_uint4(pack_bf16x2(v[8 * j + 0] + a.x, v[8 * j + 1] + a.y),
+                               pack_bf16x2(v[8 * j + 2] + bb.x, v[8 * j + 3] + bb.y),
+                               pack_bf16x2(v[8 * j + 4] + cc.x, v[8 * j + 5] + cc.y),
+                               pack_bf16x2(v[8 * j + 6] + dd.x, v[8 * j + 7] + dd.y));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (r0 < shape.M) {
+              tma_store_2d(&tmE1, nt * BN + c * 32, orow, rs);
+              bulk_commit();
+            }
+            bulk_wait_read_all();
+            if (c + 2 < BN / 32)
+              issue_chunk(t, c + 2);
+            else if (t + (int)gridDim.x < shape.num_tiles)
+              issue_chunk(t + (int)gridDim.x, c + 2 - BN / 32);
           }
           __syncwarp();
         }
         if (!epi_ok) break;
       } else {
         int b = 0;
-        int64_t p = 0, nat = m;
+        int64_t p = 0;
         if constexpr (EPI == EPI_QKV) {
           if (valid) zigzag_row_to_pos(m, ep, b, p);
-        }
-        if constexpr (EPI == EPI_RESID) {
-          if (valid && (ep.resid_natural || ep.out_natural)) nat = zigzag_row_to_natural(m, ep);
         }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -459,12 +515,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int64_t n = (int64_t)nt * BN + c * 32;
           if constexpr (EPI == EPI_STORE) {
             store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + n, v);
-          } else if constexpr (EPI == EPI_RESID) {
-            float r[32];
-            load32_bf16(reinterpret_cast<const __nv_bfloat16*>(ep.resid) + (ep.resid_natural ? nat : m) * ep.ldr + n, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += r[i];
-            store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + (ep.out_natural ? nat : m) * ep.ldo + n, v);
           } else if constexpr (EPI == EPI_QKV) {
             // packed column n -> (shard s, which of q/k/v, head, d); a shard's
             // columns are Q (h/D) | K (Hk*dh/D) | V (Hk*dh/D)
@@ -497,9 +547,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) bulk_wait_all();  // every staged store complete before leaving
       __syncwarp();
     }
-    if constexpr (EPI == EPI_DSWIGLU) {
-      // Before leaving: every dG|dU store complete, and (on the abort path) every
-      // G|U load still in flight landed (bounded).
+    if constexpr (streamed) {
+      // Before leaving: every staged store complete, and (on the abort path)
+      // every load still in flight landed (bounded).
       if (lane == 0) {
         bulk_wait_all();
         volatile int dummy = 0;
@@ -609,6 +659,12 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
       return TSP_ERR_INVALID_ARG;
     if ((ep.aux && !make_tma_epi(&tg, ep.aux, M, N, ep.ldx)) || !make_tma_epi(&tdg, ep.out, M, N / 2, ep.ldo))
       return TSP_ERR_CUDA;
+  }
+  if (epi == EPI_RESID) {
+    if (!ep.resid || !ep.out || ((reinterpret_cast<uintptr_t>(ep.resid) | reinterpret_cast<uintptr_t>(ep.out)) & 15) ||
+        ep.ldr % 8 || ep.ldo % 8 || ep.ldr < (int64_t)N || ep.ldo < (int64_t)N)
+      return TSP_ERR_INVALID_ARG;
+    if (!make_tma_epi(&tg, ep.resid, M, N, ep.ldr) || !make_tma_epi(&tdg, ep.out, M, N, ep.ldo)) return TSP_ERR_CUDA;
   }
   if (epi == EPI_DSWIGLU) {
     if (!ep.resid || !ep.out || ((reinterpret_cast<uintptr_t>(ep.resid) | reinterpret_cast<uintptr_t>(ep.out)) & 15) ||
