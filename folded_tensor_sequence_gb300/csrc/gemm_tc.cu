@@ -43,7 +43,8 @@ constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 // between them), 32 rows x 32 columns of bf16 (64-byte rows) per matrix:
 //   SwiGLU derivative: G and U of a chunk, two chunks per epilogue warp;
 //   residual: the chunk's residual (the sum written over it), two chunks per warp;
-//   SwiGLU: the chunk's G, U (kept for the backward) and SiLU(G)*U outputs.
+//   SwiGLU: the chunk's G, U (kept for the backward) and SiLU(G)*U outputs;
+//   QKV: the chunk's Q, K or V (V^T: transposed) block, one buffer per warp.
 constexpr uint32_t MAT_BYTES = 32 * 64;
 template <int EPI>
 __host__ __device__ constexpr uint32_t chunk_bytes() {  // one staged chunk of the streamed (loaded) epilogues
@@ -56,14 +57,14 @@ __host__ __device__ constexpr bool streamed_epi() { return chunk_bytes<EPI>() !=
 constexpr uint32_t SWG_WARP_BYTES = 3 * MAT_BYTES;
 template <int EPI>
 __host__ __device__ constexpr size_t stage_bytes() {
-  return EPI == EPI_SWIGLU ? 4 * SWG_WARP_BYTES : 4 * 2 * chunk_bytes<EPI>();
+  return EPI == EPI_SWIGLU ? 4 * SWG_WARP_BYTES : EPI == EPI_QKV ? 4 * MAT_BYTES : 4 * 2 * chunk_bytes<EPI>();
 }
 template <int EPI>
 __host__ __device__ constexpr size_t smem_bytes() {
   return SMEM_BYTES + (stage_bytes<EPI>() ? 1024 + stage_bytes<EPI>() : 0);
 }
 static_assert(smem_bytes<EPI_DSWIGLU>() <= 227 * 1024 && smem_bytes<EPI_SWIGLU>() <= 227 * 1024 &&
-                  smem_bytes<EPI_RESID>() <= 227 * 1024,
+                  smem_bytes<EPI_RESID>() <= 227 * 1024 && smem_bytes<EPI_QKV>() <= 227 * 1024,
               "shared memory");
 // Raster: tiles are visited in bands of group_m m-tiles (all n-tiles of a band
 // before the next band), group_m chosen so one band of A is ~32 MB and stays
@@ -146,11 +147,14 @@ __device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep
 // tmE0 / tmE1: epilogue tensor maps (32 x 32 boxes, 64-byte swizzle):
 //   EPI_DSWIGLU: saved G|U (read) / dG|dU (written);
 //   EPI_RESID:   the residual (read) / the sum (written);
-//   EPI_SWIGLU:  the G|U copy kept for the backward / SiLU(G)*U.
+//   EPI_SWIGLU:  the G|U copy kept for the backward / SiLU(G)*U;
+//   EPI_QKV:     Q [T][h] / K [B*Hk*S][dh] / tmE2: V, [B*Hk*S][dh] or V^T
+//                [B*Hk*dh][S] (only when the chunk length is a multiple of 32).
 template <int EPI, bool AMN, bool BMN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmE0, const __grid_constant__ CUtensorMap tmE1,
+                        const __grid_constant__ CUtensorMap tmE2,
                         const GemmShape shape, const EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = tempty + 2;
   uint64_t* gbar = drain + 1;  // [4 warps][2] staging buffers of the streamed epilogues
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + 8);
-  uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // epilogue staging (EPI_DSWIGLU, EPI_RESID, EPI_SWIGLU)
+  uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // epilogue staging (all but EPI_STORE)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -190,6 +194,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_SWIGLU || EPI == EPI_RESID) {
       if (EPI != EPI_SWIGLU || ep.aux) tma_prefetch_desc(&tmE0);  // the SwiGLU map exists only with aux
       tma_prefetch_desc(&tmE1);
+    }
+    if constexpr (EPI == EPI_QKV) {
+      if (ep.C % 32 == 0) {  // the maps exist only then
+        tma_prefetch_desc(&tmE0);
+        tma_prefetch_desc(&tmE1);
+        tma_prefetch_desc(&tmE2);
+      }
     }
   }
   if (warp == 1) {
@@ -501,6 +512,63 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
         }
         if (!epi_ok) break;
+      } else if (EPI == EPI_QKV && ep.C % 32 == 0) {
+        // Q|K|V scatter by TMA.  A 32-column chunk lies in one head of one of Q,
+        // K, V (a shard's Q, K and V blocks are multiples of 128 columns), and
+        // the warp's 32 zigzag rows lie in one chunk of the sequence, i.e. are 32
+        // consecutive positions p0.. of one sequence b.  The warp stages the
+        // 32 x 32 block (64-byte rows, 64-byte swizzle; V^T transposed: rows are
+        // head dims, columns positions) and one lane stores it as one box.
+        uint8_t* sb = gstage + quad * MAT_BYTES;
+        const int r0 = mt * BM + quad * 32;
+        int b0 = 0;
+        int64_t p0 = 0;
+        if (r0 < shape.M) zigzag_row_to_pos(r0, ep, b0, p0);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          const int n = nt * BN + c * 32;
+          const int hs = ep.h / ep.D, ks = ep.Hk * ep.dh / ep.D;
+          const int sh = n / (hs + 2 * ks);
+          const int within = n - sh * (hs + 2 * ks);
+          const int which = within < hs ? 0 : (within < hs + ks ? 1 : 2);
+          const int cin = within - (which == 0 ? 0 : hs + (which - 1) * ks);
+          const int head = sh * ((which == 0 ? ep.H : ep.Hk) / ep.D) + cin / ep.dh;
+          const int d0 = cin % ep.dh;
+          const bool vt = which == 2 && ep.v_transposed;
+          if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the buffer
+          __syncwarp();
+          if (vt) {
+            // element (head dim i, position lane): row i, 16-byte unit lane / 8
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(
+                  sb + i * 64 + (((lane >> 3) ^ ((i >> 1) & 3)) << 4) + (lane & 7) * 2);
+              *e = __float2bfloat16_rn(v[i]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(sb + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                             pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && r0 < shape.M) {
+            const int kvrow = ((int)b0 * ep.Hk + head) * ep.S + (int)p0;  // K / V row of position p0
+            if (which == 0)
+              tma_store_2d(&tmE0, head * ep.dh + d0, r0, sb);
+            else if (which == 1)
+              tma_store_2d(&tmE1, d0, kvrow, sb);
+            else if (!vt)
+              tma_store_2d(&tmE2, d0, kvrow, sb);
+            else
+              tma_store_2d(&tmE2, (int)p0, ((int)b0 * ep.Hk + head) * ep.dh + d0, sb);
+            bulk_commit();
+          }
+        }
       } else {
         int b = 0;
         int64_t p = 0;
@@ -543,8 +611,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
-    if constexpr (EPI == EPI_SWIGLU) {
-      if (lane == 0) bulk_wait_all();  // every staged store complete before leaving
+    if constexpr (EPI == EPI_SWIGLU || EPI == EPI_QKV) {
+      if (lane == 0) bulk_wait_all();  // every staged store complete before leaving (none on the per-row path)
       __syncwarp();
     }
     if constexpr (streamed) {
@@ -625,7 +693,7 @@ bool make_tma_epi(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, 
 
 template <int EPI, bool AMN, bool BMN>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg, const CUtensorMap& tdg,
-                       const GemmShape& s, const EpiParams& ep, cudaStream_t stream) {
+                       const CUtensorMap& te2, const GemmShape& s, const EpiParams& ep, cudaStream_t stream) {
   static std::atomic<unsigned long long> configured{0};  // devices set up for this instantiation
   if (needs_setup(configured)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, AMN, BMN>,
@@ -634,7 +702,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     mark_setup_done(configured);
   }
   const int grid = s.num_tiles < num_sms() ? s.num_tiles : num_sms();
-  gemm_bf16_tc_kernel<EPI, AMN, BMN><<<grid, THREADS, smem_bytes<EPI>(), stream>>>(ta, tb, tg, tdg, s, ep);
+  gemm_bf16_tc_kernel<EPI, AMN, BMN><<<grid, THREADS, smem_bytes<EPI>(), stream>>>(ta, tb, tg, tdg, te2, s, ep);
   return cudaGetLastError();
 }
 
@@ -652,7 +720,20 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   if (!ok_a || !ok_b) return TSP_ERR_CUDA;
   // Epilogue tensor maps: G|U in and dG|dU out of the SwiGLU-derivative
   // epilogue; the G|U copy and SiLU(G)*U out of the SwiGLU epilogue.
-  CUtensorMap tg{}, tdg{};
+  CUtensorMap tg{}, tdg{}, te2{};
+  if (epi == EPI_QKV && ep.C % 32 == 0) {
+    // Q [M][h] (zigzag rows), K [B*Hk*S][dh], V likewise or V^T [B*Hk*dh][S]
+    const int64_t kv_rows = (int64_t)ep.B * ep.Hk * ep.S;
+    if (!ep.q || !ep.k || !ep.v ||
+        ((reinterpret_cast<uintptr_t>(ep.q) | reinterpret_cast<uintptr_t>(ep.k) | reinterpret_cast<uintptr_t>(ep.v)) &
+         15) ||
+        ep.dh % 32 || ep.h % 32 || ep.S % 32 || kv_rows * (ep.v_transposed ? ep.dh : 1) > INT32_MAX)
+      return TSP_ERR_INVALID_ARG;
+    const bool ok = make_tma_epi(&tg, ep.q, M, ep.h, ep.h) && make_tma_epi(&tdg, ep.k, kv_rows, ep.dh, ep.dh) &&
+                    (ep.v_transposed ? make_tma_epi(&te2, ep.v, (int64_t)ep.B * ep.Hk * ep.dh, ep.S, ep.S)
+                                     : make_tma_epi(&te2, ep.v, kv_rows, ep.dh, ep.dh));
+    if (!ok) return TSP_ERR_CUDA;
+  }
   if (epi == EPI_SWIGLU) {
     if (!ep.out || (reinterpret_cast<uintptr_t>(ep.out) & 15) || ep.ldo % 8 || ep.ldo < N / 2 ||
         (ep.aux && ((reinterpret_cast<uintptr_t>(ep.aux) & 15) || ep.ldx % 8 || ep.ldx < (int64_t)N)))
@@ -689,15 +770,15 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   cudaError_t e;
   const int mode = (a_mn ? 2 : 0) | (b_mn ? 1 : 0);
   switch (epi * 4 + mode) {
-    case EPI_STORE * 4 + 0: e = launch_epi<EPI_STORE, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_STORE * 4 + 1: e = launch_epi<EPI_STORE, false, true>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_STORE * 4 + 3: e = launch_epi<EPI_STORE, true, true>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_RESID * 4 + 0: e = launch_epi<EPI_RESID, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_RESID * 4 + 1: e = launch_epi<EPI_RESID, false, true>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_QKV * 4 + 0: e = launch_epi<EPI_QKV, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_SWIGLU * 4 + 0: e = launch_epi<EPI_SWIGLU, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_DSWIGLU * 4 + 0: e = launch_epi<EPI_DSWIGLU, false, false>(ta, tb, tg, tdg, s, ep, stream); break;
-    case EPI_DSWIGLU * 4 + 1: e = launch_epi<EPI_DSWIGLU, false, true>(ta, tb, tg, tdg, s, ep, stream); break;
+    case EPI_STORE * 4 + 0: e = launch_epi<EPI_STORE, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_STORE * 4 + 1: e = launch_epi<EPI_STORE, false, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_STORE * 4 + 3: e = launch_epi<EPI_STORE, true, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_RESID * 4 + 0: e = launch_epi<EPI_RESID, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_RESID * 4 + 1: e = launch_epi<EPI_RESID, false, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_QKV * 4 + 0: e = launch_epi<EPI_QKV, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_SWIGLU * 4 + 0: e = launch_epi<EPI_SWIGLU, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_DSWIGLU * 4 + 0: e = launch_epi<EPI_DSWIGLU, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    case EPI_DSWIGLU * 4 + 1: e = launch_epi<EPI_DSWIGLU, false, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
     default: return TSP_ERR_UNSUPPORTED;
   }
   return e == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
