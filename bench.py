@@ -45,11 +45,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # without its own capture, or a source changed since, reports null.
 NCU_TRAFFIC = {
     ("gate/up projection", "bf16_D8_b2_s16384_h4096"):
-        (2.16e9 + 0.9264e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "ab6f317c285c597d"),
+        (2.16e9 + 0.92808e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "1c44a2a1014d92e7"),
     ("gate/up projection", "bf16_gqa8_D8_b2_s16384_h4096"):
-        (2.16e9 + 0.9268e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "ab6f317c285c597d"),
+        (2.16e9 + 0.92766e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "1c44a2a1014d92e7"),
     ("gate/up projection", "bf16_D4_s4096_h2048"):
-        (62.96e6 + 10.44e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "ab6f317c285c597d"),
+        (62.96e6 + 16.29e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "1c44a2a1014d92e7"),
     ("attention", "bf16_D8_b2_s16384_h4096"):
         (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
     ("attention", "bf16_D8_b1_s65536_h4096"):
