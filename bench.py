@@ -471,28 +471,28 @@ def main():
 
     # ---- end to end through the API with host buffers -----------------------
     # Every step's inputs come from pinned host memory and its result goes back
-    # to it.  As a caller overlapping I/O with the layer would, a copy stream
-    # brings step i+1's inputs in and takes step i's result out while step i
-    # computes (device inputs and outputs double-buffered, events ordering the
-    # reuse of each buffer).  Timed from the first input copy to the last
-    # result copy.
+    # to it.  As a caller overlapping I/O with the layer would, one copy stream
+    # brings step i+1's inputs in and another takes step i's result out while
+    # step i computes (the host link is full duplex; device inputs and outputs
+    # are double-buffered, events order the reuse of each buffer).  Timed from
+    # the first input copy to the last result copy.
     ins_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
     for th, t in zip(ins_host, ins):
         th.copy_(t)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     dins = [ins, [torch.empty_like(t) for t in ins]]
     douts = [out, torch.empty_like(out)]
-    cs = torch.cuda.Stream(dev)
+    cs_in, cs_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     h2d = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
     d2h = [torch.cuda.Event() for _ in range(2)]
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(cs):
-        e0.record(cs)
+    e0.record(cs_in)
+    with torch.cuda.stream(cs_in):
         for t, th in zip(dins[0], ins_host):
             t.copy_(th, non_blocking=True)
-        h2d[0].record(cs)
+        h2d[0].record(cs_in)
     for i in range(args.steps):
         k = i % 2
         stream.wait_event(h2d[k])
@@ -500,19 +500,19 @@ def main():
             stream.wait_event(d2h[k])  # douts[k] has been read back
         step_io(dins[k], douts[k])
         done[k].record(stream)
-        with torch.cuda.stream(cs):
-            if i + 1 < args.steps:
-                nk = (i + 1) % 2
+        if i + 1 < args.steps:
+            nk = (i + 1) % 2
+            with torch.cuda.stream(cs_in):
                 if i >= 1:
-                    cs.wait_event(done[nk])  # dins[nk] no longer read by step i-1
+                    cs_in.wait_event(done[nk])  # dins[nk] no longer read by step i-1
                 for t, th in zip(dins[nk], ins_host):
                     t.copy_(th, non_blocking=True)
-                h2d[nk].record(cs)
-            cs.wait_event(done[k])
+                h2d[nk].record(cs_in)
+        with torch.cuda.stream(cs_out):
+            cs_out.wait_event(done[k])
             out_host.copy_(douts[k], non_blocking=True)
-            d2h[k].record(cs)
-    with torch.cuda.stream(cs):
-        e1.record(cs)
+            d2h[k].record(cs_out)
+    e1.record(cs_out)
     barrier()
     ems = max_over_ranks(e0.elapsed_time(e1), dev)
     tsp.tsp_sync_check(stream)
