@@ -194,6 +194,7 @@ tsp_status check_bf16_shapes(const tsp_plan* p) {
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+
 // ---- optional per-step timing (tsp_profile_*) --------------------------------
 // When enabled, each launched step is bracketed by two CUDA events on its
 // stream; tsp_profile_report() sums the elapsed times per step name.
@@ -365,6 +366,20 @@ tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weig
 
 tsp_status report_error(tsp_status s, const char* msg) { return fail(s, "%s", msg); }
 
+// Every device address the library looks up (error word, static scratch, SM
+// count, kernel attributes) is the current device's, so the work must be
+// enqueued on a stream of that device.
+tsp_status check_stream_device(void* stream, const char* what) {
+  int cur = 0, sdev = 0;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e == cudaSuccess) e = cudaStreamGetDevice(as_stream(stream), &sdev);
+  if (e != cudaSuccess) return fail(TSP_ERR_CUDA, "%s: device of the stream: %s", what, cudaGetErrorString(e));
+  if (sdev != cur)
+    return fail(TSP_ERR_INVALID_ARG, "%s: the stream belongs to device %d but device %d is current", what, sdev,
+                cur);
+  return TSP_OK;
+}
+
 void prof_begin(const char* name, cudaStream_t st) { t_prof_stack.push_back(new Prof(name, st)); }
 
 void prof_end(cudaStream_t) {
@@ -521,6 +536,7 @@ tsp_status tsp_pack_weights(const tsp_plan* p, const void* const canonical[7], c
                        canonical[6], packed->qkv, packed->o, packed->gate_up, packed->down},
                       "tsp_pack_weights")) != TSP_OK)
     return s;
+  if ((s = check_stream_device(stream, "tsp_pack_weights")) != TSP_OK) return s;
   return cuda_status(launch_pack_weights(p, canonical, packed, false, as_stream(stream)), "pack weights");
 }
 
@@ -532,6 +548,7 @@ tsp_status tsp_unpack_weights(const tsp_plan* p, const tsp_weights* packed, void
                        canonical[6], packed->qkv, packed->o, packed->gate_up, packed->down},
                       "tsp_unpack_weights")) != TSP_OK)
     return s;
+  if ((s = check_stream_device(stream, "tsp_unpack_weights")) != TSP_OK) return s;
   tsp_weight_grads w{const_cast<void*>(packed->qkv), const_cast<void*>(packed->o), const_cast<void*>(packed->gate_up),
                      const_cast<void*>(packed->down)};
   return cuda_status(launch_pack_weights(p, const_cast<const void* const*>(canonical), &w, true, as_stream(stream)),
@@ -544,6 +561,8 @@ tsp_status tsp_zigzag_permute(const tsp_plan* p, int batch, const void* x, void*
   if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
   if (batch == 0) return TSP_OK;
   if ((s = check_ptrs({x, xz}, "tsp_zigzag_permute")) != TSP_OK) return s;
+  if ((s = check_stream_device(stream, "tsp_zigzag_permute")) != TSP_OK) return s;
+  Prof pr("zigzag permute", as_stream(stream));
   return cuda_status(
       launch_zigzag_rows(x, xz, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, true, as_stream(stream)),
       "zigzag permute");
@@ -555,6 +574,8 @@ tsp_status tsp_zigzag_unpermute(const tsp_plan* p, int batch, const void* xz, vo
   if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
   if (batch == 0) return TSP_OK;
   if ((s = check_ptrs({x, xz}, "tsp_zigzag_unpermute")) != TSP_OK) return s;
+  if ((s = check_stream_device(stream, "tsp_zigzag_unpermute")) != TSP_OK) return s;
+  Prof pr("zigzag unpermute", as_stream(stream));
   return cuda_status(
       launch_zigzag_rows(xz, x, (int64_t)p->hidden * esize(p), p->D, batch, p->seq, false, as_stream(stream)),
       "zigzag unpermute");
@@ -567,6 +588,8 @@ tsp_status tsp_kv_gather(const tsp_plan* p, int batch, const void* kz, const voi
   if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
   if (batch == 0) return TSP_OK;
   if ((s = check_ptrs({kz, vz, k, v}, "tsp_kv_gather")) != TSP_OK) return s;
+  if ((s = check_stream_device(stream, "tsp_kv_gather")) != TSP_OK) return s;
+  Prof pr("kv gather", as_stream(stream));
   return cuda_status(launch_kv_gather(kz, vz, k, v, (int)esize(p), p->D, batch, p->seq, p->kv_heads, p->head_dim,
                                       as_stream(stream)),
                      "kv gather");
@@ -584,6 +607,7 @@ tsp_status tsp_attention_fwd(const tsp_plan* p, int batch, const void* xz, const
   if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
   if (ws_bytes < attn_ws_bytes(p, batch))
     return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, attn_ws_bytes(p, batch));
+  if ((s = check_stream_device(stream, "tsp_attention_fwd")) != TSP_OK) return s;
   const size_t blk = attn_ws_bytes(p, batch) / 4;
   char* base = static_cast<char*>(ws);
   return attention_impl(p, batch, xz, w, a_out, nullptr, static_cast<float*>(lse), base, base + blk, base + 2 * blk,
@@ -601,6 +625,7 @@ tsp_status tsp_gated_mlp_fwd(const tsp_plan* p, int batch, const void* hz, const
   if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
   if (ws_bytes < mlp_ws_bytes(p, batch))
     return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, mlp_ws_bytes(p, batch));
+  if ((s = check_stream_device(stream, "tsp_gated_mlp_fwd")) != TSP_OK) return s;
   const size_t T = (size_t)batch * p->seq;
   char* mz = static_cast<char*>(ws);
   char* gu = mz + align256(T * p->ffn * esize(p));
@@ -619,6 +644,7 @@ tsp_status tsp_layer_fwd(const tsp_plan* p, int batch, const void* x, const tsp_
   if ((s = check_bf16_shapes(p)) != TSP_OK) return s;
   const Layout L = layer_layout(p, batch);
   if (ws_bytes < L.fwd_end) return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, L.fwd_end);
+  if ((s = check_stream_device(stream, "tsp_layer_fwd")) != TSP_OK) return s;
   cudaStream_t st = as_stream(stream);
   char* wsb = static_cast<char*>(ws);
   char* act = saved ? static_cast<char*>(saved) : wsb;  // where the saved activations go
@@ -675,6 +701,7 @@ tsp_status tsp_layer_bwd(const tsp_plan* p, int batch, const void* x, const tsp_
   if (T64 % 64) return fail(TSP_ERR_UNSUPPORTED, "backward needs batch*seq %% 64 == 0 (got %lld)", (long long)T64);
   const BwdLayout L = bwd_layout(p, batch);
   if (ws_bytes < L.end) return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, L.end);
+  if ((s = check_stream_device(stream, "tsp_layer_bwd")) != TSP_OK) return s;
   const Layout A = layer_layout(p, batch);
   cudaStream_t st = as_stream(stream);
   const char* sv = static_cast<const char*>(saved);
@@ -876,6 +903,7 @@ tsp_status tsp_decode_step(const tsp_plan* p, int batch, int64_t pos, const void
     return fail(TSP_ERR_UNSUPPORTED, "decode needs heads / kv_heads in {1, 2, 4, 8} (got %d)", g);
   if (ws_bytes < decode_ws_bytes(p, batch))
     return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, decode_ws_bytes(p, batch));
+  if ((s = check_stream_device(stream, "tsp_decode_step")) != TSP_OK) return s;
   s = decode_step_bf16(p, batch, pos, x_new, w, k_cache, v_cache, y_new, ws, as_stream(stream));
   if (s != TSP_OK) return fail(s, "decode step failed: %s", tsp_status_string(s));
   return TSP_OK;
@@ -886,6 +914,7 @@ tsp_status tsp_debug_wait_timeout(unsigned int timeout_us, void* stream) {
   if (injected(&s)) return s;
   if (timeout_us == 0 || timeout_us > 10000000u)
     return fail(TSP_ERR_INVALID_ARG, "timeout_us %u not in (0, 10 s]", timeout_us);
+  if ((s = check_stream_device(stream, "tsp_debug_wait_timeout")) != TSP_OK) return s;
   unsigned int* err = dev_error_word();
   if (!err) return fail(TSP_ERR_CUDA, "device error word unavailable");
   wait_probe_kernel<<<1, 32, 0, as_stream(stream)>>>(err, (unsigned long long)timeout_us * 1000ull);

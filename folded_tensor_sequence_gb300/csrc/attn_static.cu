@@ -71,6 +71,9 @@ extern "C" tsp_status tsp_attention_fwd_static(const tsp_plan* plan, int batch, 
              need, kStaticScratchBytes);
     return tsp::report_error(TSP_ERR_WORKSPACE, msg);
   }
+  // the array's address is looked up for the current device, so the work must go to that device's stream
+  const tsp_status sd = tsp::check_stream_device(stream, "tsp_attention_fwd_static");
+  if (sd != TSP_OK) return sd;
   cudaError_t err = cudaSuccess;
   void* scratch = scratch_on_current_device(&err);
   if (!scratch) {

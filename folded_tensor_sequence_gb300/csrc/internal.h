@@ -63,6 +63,9 @@ bool needs_setup(const std::atomic<unsigned long long>& done);
 void mark_setup_done(std::atomic<unsigned long long>& done);
 // Records `msg` as this thread's tsp_last_error_message() and returns `s`.
 tsp_status report_error(tsp_status s, const char* msg);
+// TSP_OK if `stream` belongs to the current device; TSP_ERR_INVALID_ARG (with a
+// message naming both devices) if not, TSP_ERR_CUDA if either cannot be read.
+tsp_status check_stream_device(void* stream, const char* what);
 unsigned int* dev_error_word();  // device address of this device's error word (nullptr on failure)
 
 // bf16 tcgen05 GEMM: C[M][N] = sum_k A[m][k] B[n][k] with fp32 accumulation in

@@ -8,7 +8,7 @@
 // pos(r,k) = r*C + k (k < C) or (2D-1-r)*C + (k-C) (k >= C).
 //
 // All copies move 16-byte vectors, consecutive threads touching consecutive
-// vectors of one row, over a grid of (SM count x 8) CTAs striding the work.
+// vectors, over a grid of at most (SM count x 8) CTAs striding the work.
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,60 +20,96 @@ __device__ __forceinline__ int64_t zigzag_pos(int64_t r, int64_t k, int64_t C, i
   return k < C ? r * C + k : (2 * D - 1 - r) * C + (k - C);
 }
 
-// Natural position p -> (rank, local index).
-__device__ __forceinline__ void pos_to_zigzag(int64_t p, int64_t C, int D, int64_t& r, int64_t& k) {
-  const int64_t c = p / C;
-  const int64_t off = p - c * C;
-  if (c < D) {
-    r = c;
-    k = off;
-  } else {
-    r = 2 * D - 1 - c;
-    k = C + off;
+// Vectors each thread keeps in flight in the copy kernels below (loads issued
+// back to back, then the stores): 2048 threads x 4 x 16 B = 128 KB per SM,
+// well above what HBM latency times bandwidth per SM asks for.
+constexpr int kCopyUnroll = 4;
+constexpr int kCopyThreads = 256;
+
+// Copies `nvec` 16-byte vectors src[i] -> dst[i], i in [first, nvec), the
+// calling CTA taking every `stride`-th group of kCopyThreads*kCopyUnroll.
+__device__ __forceinline__ void copy_span(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t nvec,
+                                          int64_t first, int64_t stride) {
+  for (int64_t v0 = first + threadIdx.x; v0 < nvec; v0 += stride) {
+    uint4 t[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t i = v0 + (int64_t)u * kCopyThreads;
+      if (i < nvec) t[u] = __ldcs(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t i = v0 + (int64_t)u * kCopyThreads;
+      if (i < nvec) __stcs(dst + i, t[u]);
+    }
   }
 }
 
-// One 16-byte vector per thread-iteration; rows of `vecs_per_row` vectors.
-__global__ void zigzag_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t vecs_per_row,
-                                   int D, int B, int64_t S, bool to_zigzag) {
+// Zigzag permute / unpermute.  Each of the 2*D*B chunk copies is contiguous on
+// both sides: half e of rank r's rows of sequence b (C zigzag rows from
+// (r*B + b)*2C + e*C) is natural chunk c = r (e = 0) or 2D-1-r (e = 1) of that
+// sequence (C rows from b*S + c*C).  Work item w = (chunk copy, part): `parts`
+// CTAs share one chunk copy, so the grid needs no per-vector index arithmetic.
+__global__ void __launch_bounds__(kCopyThreads) zigzag_rows_kernel(const uint4* __restrict__ src,
+                                                                   uint4* __restrict__ dst, int64_t vecs_per_row,
+                                                                   int D, int B, int64_t S, int parts,
+                                                                   bool to_zigzag) {
   const int64_t C = S / (2 * D);
-  const int64_t twoC = 2 * C;
-  const int64_t total = (int64_t)B * S * vecs_per_row;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t zrow = i / vecs_per_row;  // zigzag row index
-    const int64_t v = i - zrow * vecs_per_row;
-    const int64_t r = zrow / (B * twoC);
-    const int64_t rem = zrow - r * (B * twoC);
-    const int64_t b = rem / twoC;
-    const int64_t k = rem - b * twoC;
-    const int64_t nrow = b * S + zigzag_pos(r, k, C, D);  // natural row
-    if (to_zigzag)
-      dst[zrow * vecs_per_row + v] = __ldg(&src[nrow * vecs_per_row + v]);
-    else
-      dst[nrow * vecs_per_row + v] = __ldg(&src[zrow * vecs_per_row + v]);
+  const int64_t seg_vecs = C * vecs_per_row;
+  const int items = 2 * D * B * parts;
+  for (int w = blockIdx.x; w < items; w += gridDim.x) {
+    const int seg = w / parts, part = w - seg * parts;
+    const int e = seg & 1, rb = seg >> 1;  // rb = r*B + b
+    const int r = rb / B, b = rb - r * B;
+    const int64_t c = e == 0 ? r : 2 * D - 1 - r;
+    const int64_t zrow0 = (int64_t)rb * 2 * C + e * C;
+    const int64_t nrow0 = (int64_t)b * S + c * C;
+    const uint4* s0 = src + (to_zigzag ? nrow0 : zrow0) * vecs_per_row;
+    uint4* d0 = dst + (to_zigzag ? zrow0 : nrow0) * vecs_per_row;
+    copy_span(s0, d0, seg_vecs, (int64_t)part * kCopyThreads * kCopyUnroll,
+              (int64_t)parts * kCopyThreads * kCopyUnroll);
   }
 }
 
-// Gathered [B][H][S][dh] <- zigzag [T][H*dh] (H: the K/V head count); iterates over destination vectors.
-__global__ void kv_gather_kernel(const uint4* __restrict__ kz, const uint4* __restrict__ vz, uint4* __restrict__ k,
-                                 uint4* __restrict__ v, int vec_per_head, int D, int B, int64_t S, int H) {
+// K/V all-gather into natural order: gathered [B][Hk][S][dh] <- zigzag
+// [T][Hk*dh].  Work item = (tensor K or V, sequence b, K/V head, chunk c):
+// natural positions c*C .. c*C+C-1 of that head are C consecutive rows of
+// dh*e bytes in the destination, read from C consecutive zigzag rows of rank
+// r(c) (row stride Hk*dh*e bytes) at the head's column offset.  vph = vectors
+// per head row, a power of two (dh * elem_bytes / 16 with dh in {32, 64, 128}).
+__global__ void __launch_bounds__(kCopyThreads) kv_gather_kernel(const uint4* __restrict__ kz,
+                                                                 const uint4* __restrict__ vz, uint4* __restrict__ k,
+                                                                 uint4* __restrict__ v, int lg_vph, int D, int B,
+                                                                 int64_t S, int H) {
   const int64_t C = S / (2 * D);
-  const int64_t twoC = 2 * C;
-  const int64_t vec_per_row = (int64_t)H * vec_per_head;
-  const int64_t total = (int64_t)B * H * S * vec_per_head;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t dv = i % vec_per_head;
-    const int64_t rest = i / vec_per_head;
-    const int64_t p = rest % S;
-    const int64_t bh = rest / S;
-    const int64_t head = bh % H;
-    const int64_t b = bh / H;
-    int64_t r, kk;
-    pos_to_zigzag(p, C, D, r, kk);
-    const int64_t zrow = (r * B + b) * twoC + kk;
-    const int64_t s_idx = zrow * vec_per_row + head * vec_per_head + dv;
-    k[i] = __ldg(&kz[s_idx]);
-    v[i] = __ldg(&vz[s_idx]);
+  const int vph = 1 << lg_vph;
+  const int64_t vec_per_row = (int64_t)H * vph;
+  const int64_t seg_vecs = C << lg_vph;
+  const int64_t items = 2LL * B * H * 2 * D;
+  for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
+    const int c = (int)(w % (2 * D));
+    int64_t rest = w / (2 * D);
+    const int head = (int)(rest % H);
+    rest /= H;
+    const int b = (int)(rest % B);
+    const int tensor = (int)(rest / B);
+    const int64_t r = c < D ? c : 2 * D - 1 - c;
+    const int64_t zrow0 = (r * B + b) * 2 * C + (c < D ? 0 : C);
+    const uint4* src = (tensor == 0 ? kz : vz) + zrow0 * vec_per_row + (int64_t)head * vph;
+    uint4* dst = (tensor == 0 ? k : v) + (((int64_t)b * H + head) * S + (int64_t)c * C) * vph;
+    for (int64_t v0 = threadIdx.x; v0 < seg_vecs; v0 += kCopyThreads * kCopyUnroll) {
+      uint4 t[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = v0 + u * kCopyThreads;
+        if (i < seg_vecs) t[u] = __ldcs(src + (i >> lg_vph) * vec_per_row + (i & (vph - 1)));
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t i = v0 + u * kCopyThreads;
+        if (i < seg_vecs) __stcs(dst + i, t[u]);
+      }
+    }
   }
 }
 
@@ -298,21 +334,34 @@ int grid_for(int64_t work, int threads) {
 cudaError_t launch_zigzag_rows(const void* src, void* dst, int64_t row_bytes, int D, int B, int64_t S,
                                bool to_zigzag, cudaStream_t stream) {
   const int64_t vpr = row_bytes / 16;
-  const int64_t total = (int64_t)B * S * vpr;
-  if (total == 0) return cudaSuccess;
-  zigzag_rows_kernel<<<grid_for(total, 256), 256, 0, stream>>>(static_cast<const uint4*>(src),
-                                                               static_cast<uint4*>(dst), vpr, D, B, S, to_zigzag);
+  const int64_t seg_vecs = S / (2 * D) * vpr;
+  if ((int64_t)B * S * vpr == 0) return cudaSuccess;
+  // about 8 resident CTAs per SM, spread evenly over the 2*D*B chunk copies
+  const int64_t nseg = 2LL * D * B;
+  const int64_t want = (int64_t)num_sms() * 8;
+  const int64_t max_parts = (seg_vecs + kCopyThreads * kCopyUnroll - 1) / (kCopyThreads * kCopyUnroll);
+  int64_t parts = (want + nseg - 1) / nseg;
+  if (parts > max_parts) parts = max_parts;
+  if (parts < 1) parts = 1;
+  const int64_t items = nseg * parts;
+  const int grid = (int)(items < want ? items : want);
+  zigzag_rows_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                        vpr, D, B, S, (int)parts, to_zigzag);
   return cudaGetLastError();
 }
 
 cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
                              int64_t S, int H, int dh, cudaStream_t stream) {
   const int vph = dh * elem_bytes / 16;
-  const int64_t total = (int64_t)B * H * S * vph;
-  if (total == 0) return cudaSuccess;
-  kv_gather_kernel<<<grid_for(total, 256), 256, 0, stream>>>(static_cast<const uint4*>(kz),
-                                                             static_cast<const uint4*>(vz), static_cast<uint4*>(k),
-                                                             static_cast<uint4*>(v), vph, D, B, S, H);
+  int lg = 0;
+  while ((1 << lg) < vph) ++lg;
+  if ((1 << lg) != vph) return cudaErrorInvalidValue;  // dh * elem_bytes is 64, 128, 256 or 512
+  const int64_t items = 2LL * B * H * 2 * D;
+  if ((int64_t)B * H * S == 0) return cudaSuccess;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  kv_gather_kernel<<<(int)(items < cap ? items : cap), kCopyThreads, 0, stream>>>(
+      static_cast<const uint4*>(kz), static_cast<const uint4*>(vz), static_cast<uint4*>(k), static_cast<uint4*>(v),
+      lg, D, B, S, H);
   return cudaGetLastError();
 }
 

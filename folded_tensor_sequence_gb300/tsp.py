@@ -19,6 +19,7 @@ from . import build as _build
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT, TSP_ERR_WORKSPACE = range(6)
 TSP_F32, TSP_BF16 = 0, 1
 TSP_OP_ATTENTION_FWD, TSP_OP_GATED_MLP_FWD, TSP_OP_LAYER_FWD, TSP_OP_LAYER_BWD, TSP_OP_DECODE = range(5)
+TSP_STATIC_SCRATCH_BYTES = 32 << 20  # size of the static scratch array behind tsp_attention_fwd_static
 
 EXPORTS = [
     "tsp_plan_create", "tsp_plan_destroy", "tsp_workspace_bytes", "tsp_saved_bytes", "tsp_status_string",

@@ -31,8 +31,12 @@
  *     as a workspace of tsp_workspace_bytes() bytes.
  *   - Element type is the plan's dtype (fp32 or bf16) unless stated; lse is
  *     always fp32.  Every pointer must be 16-byte aligned.
- *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
- *     enqueue work; they return before it runs.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream) of the
+ *     CURRENT device (cudaSetDevice): the library's per-device state (error
+ *     word, static scratch, kernel set-up) is looked up for the current
+ *     device, so a stream of another device is refused with
+ *     TSP_ERR_INVALID_ARG before anything is enqueued.  Calls only enqueue
+ *     work; they return before it runs.
  *   - Arguments are validated on the host before any launch; an invalid call
  *     enqueues nothing and returns a status.  A launch failure returns
  *     TSP_ERR_CUDA.  Kernels never trap: a device-side wait that exceeds its

@@ -6,7 +6,7 @@ from folded_tensor_sequence_gb300 import synth
 from folded_tensor_sequence_gb300.configs import LayerConfig
 from oracle import tsp_oracle as O
 
-from helpers import check, rel_frob, to_dev, to_np
+from helpers import Guarded, check, guarded_like, guarded_packed, guarded_workspace, rel_frob, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -22,6 +22,8 @@ def tsp():
 
 
 def run_bwd(tsp, cfg, inp, deterministic=0):
+    """Forward (keeping activations) and backward; every output, the saved buffer and both
+    workspaces sit between guard bands that must be intact afterwards."""
     import torch
 
     B = cfg.batch
@@ -32,16 +34,21 @@ def run_bwd(tsp, cfg, inp, deterministic=0):
     tsp.tsp_pack_weights(plan, canon, packed)
     x = to_dev(inp["x"], cfg.dtype)
     dy = to_dev(inp["dY"], cfg.dtype)
-    y = torch.empty_like(x)
-    saved = torch.empty(tsp.tsp_saved_bytes(plan, B), dtype=torch.uint8, device="cuda")
-    tsp.tsp_layer_fwd(plan, B, x, packed, y, saved, tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD))
-    dx = torch.empty_like(x)
-    grads = tsp.empty_packed(plan)
-    tsp.tsp_layer_bwd(plan, B, x, packed, saved, dy, dx, grads, tsp.workspace(plan, B, tsp.TSP_OP_LAYER_BWD))
+    y = guarded_like(x)
+    saved = Guarded((tsp.tsp_saved_bytes(plan, B),), torch.uint8, fill=None)
+    wf = guarded_workspace(tsp, plan, B, tsp.TSP_OP_LAYER_FWD)
+    tsp.tsp_layer_fwd(plan, B, x, packed, y.t, saved.t, wf.t)
+    dx = guarded_like(x)
+    grads, gguards = guarded_packed(tsp, plan)
+    wb = guarded_workspace(tsp, plan, B, tsp.TSP_OP_LAYER_BWD)
+    tsp.tsp_layer_bwd(plan, B, x, packed, saved.t, dy, dx.t, grads, wb.t)
     canon_g = {k: torch.empty_like(v) for k, v in canon.items()}
     tsp.tsp_unpack_weights(plan, grads, canon_g)
     tsp.tsp_sync_check()
-    return to_np(y), to_np(dx), {k: to_np(v) for k, v in canon_g.items()}
+    for g, what in ((y, "y"), (saved, "saved"), (wf, "forward workspace"), (dx, "dx"), (wb, "backward workspace"),
+                    *zip(gguards, ("dW_qkv", "dW_o", "dW_gate_up", "dW_down"))):
+        g.check(f"{cfg.name} {what}")
+    return to_np(y.t), to_np(dx.t), {k: to_np(v) for k, v in canon_g.items()}
 
 
 BWD_CASES = [

@@ -12,7 +12,7 @@ from folded_tensor_sequence_gb300 import synth
 from folded_tensor_sequence_gb300.configs import LayerConfig
 from oracle import tsp_oracle as O
 
-from helpers import check, to_dev, to_np
+from helpers import Guarded, check, guarded_like, guarded_workspace, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -28,16 +28,17 @@ def tsp():
 
 
 def make_cache(cfg, pos, seed):
-    """[B][Hk][S][dh] bf16 on the GPU: N(0,1) rows < pos, sentinel 30.0 from pos on."""
+    """[B][Hk][S][dh] bf16 on the GPU between guard bands: N(0,1) rows < pos, sentinel 30.0 from pos on."""
     import torch
 
     gen = torch.Generator(device="cuda").manual_seed(seed)
     shape = (cfg.batch, cfg.kv_h, cfg.seq, cfg.head_dim)
-    k = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
-    v = torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
-    k[:, :, pos:] = 30.0
-    v[:, :, pos:] = 30.0
-    return k, v
+    kg, vg = Guarded(shape, torch.bfloat16, fill=None), Guarded(shape, torch.bfloat16, fill=None)
+    kg.t.copy_(torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16))
+    vg.t.copy_(torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16))
+    kg.t[:, :, pos:] = 30.0
+    vg.t[:, :, pos:] = 30.0
+    return kg, vg
 
 
 def as_oracle_cache(c):
@@ -47,19 +48,22 @@ def as_oracle_cache(c):
 
 
 def run_decode(tsp, cfg, inp, x_new, pos, seed=5):
-    import torch
-
+    """One decode step; the caches, the output and the workspace sit between guard bands."""
     plan = tsp.plan_for(cfg)
     canon = {k: to_dev(inp[k], "bf16") for k in tsp.CANONICAL}
     packed = tsp.empty_packed(plan)
     tsp.tsp_pack_weights(plan, canon, packed)
-    kc, vc = make_cache(cfg, pos, seed)
+    kg, vg = make_cache(cfg, pos, seed)
+    kc, vc = kg.t, vg.t
     k0, v0 = kc.clone(), vc.clone()
     xd = to_dev(x_new, "bf16")
-    y = torch.empty_like(xd)
-    tsp.tsp_decode_step(plan, cfg.batch, pos, xd, packed, kc, vc, y, tsp.workspace(plan, cfg.batch, tsp.TSP_OP_DECODE))
+    y = guarded_like(xd)
+    ws = guarded_workspace(tsp, plan, cfg.batch, tsp.TSP_OP_DECODE)
+    tsp.tsp_decode_step(plan, cfg.batch, pos, xd, packed, kc, vc, y.t, ws.t)
     tsp.tsp_sync_check()
-    return to_np(y), kc, vc, k0, v0
+    for g, what in ((kg, "k cache"), (vg, "v cache"), (y, "y_new"), (ws, "decode workspace")):
+        g.check(f"{cfg.name} pos={pos} {what}")
+    return to_np(y.t), kc, vc, k0, v0
 
 
 def oracle_step(cfg, inp, x_new, k0, v0, pos):

@@ -94,3 +94,46 @@ def test_pack_layout_and_roundtrip(tsp, D, h, H, F, dt):
     torch.cuda.synchronize()
     for k in canon:
         assert torch.equal(back[k], canon[k]), k
+
+
+FULL_LAYOUT = [  # D, B, S, K/V heads, head_dim: the 16K-token x 2 and 64K-token workloads, and 8 K/V heads
+    (8, 2, 16384, 32, 128),
+    (8, 1, 65536, 32, 128),
+    (8, 2, 16384, 8, 128),
+]
+
+
+@pytest.mark.parametrize("D,B,S,Hk,dh", FULL_LAYOUT)
+def test_layout_full_size_bit_exact(tsp, D, B, S, Hk, dh):
+    """Permute, unpermute and K/V gather at the full workload sizes (the launch
+    configuration the benchmark times), every element compared with the
+    oracle's zigzag position map applied by plain indexing."""
+    import torch
+
+    h = 32 * dh
+    plan = tsp.tsp_plan_create_gqa(D, S, h, 32, Hk, dh, 128 * D, "bf16")
+    gen = torch.Generator(device="cuda").manual_seed(D + S)
+    x = torch.randn(B, S, h, generator=gen, device="cuda").to(torch.bfloat16)
+    pos = torch.from_numpy(O.zigzag_positions(S, D).astype(np.int64)).to("cuda")  # [D, 2C]
+    xz = torch.empty_like(x)
+    tsp.tsp_zigzag_permute(plan, B, x, xz)
+    back = torch.empty_like(x)
+    tsp.tsp_zigzag_unpermute(plan, B, xz, back)
+    torch.cuda.synchronize()
+    want = x[:, pos.reshape(-1)].reshape(B, D, -1, h).transpose(0, 1)  # [D, B, 2C, h]
+    assert torch.equal(xz.view(D, B, -1, h), want)
+    assert torch.equal(back, x)
+    del want, back
+    hk = Hk * dh
+    kz = torch.randn(B * S, hk, generator=gen, device="cuda").to(torch.bfloat16)
+    vz = torch.randn(B * S, hk, generator=gen, device="cuda").to(torch.bfloat16)
+    k = torch.empty(B, Hk, S, dh, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    tsp.tsp_kv_gather(plan, B, kz, vz, k, v)
+    torch.cuda.synchronize()
+    inv = torch.empty(S, dtype=torch.int64, device="cuda")  # natural position -> (rank, local index)
+    inv[pos.reshape(-1)] = torch.arange(S, device="cuda")
+    for src, out in ((kz, k), (vz, v)):
+        zz = src.view(D, B, -1, hk).transpose(0, 1).reshape(B, S, hk)  # [B][rank-major zigzag][hk]
+        nat = zz[:, inv]                                                 # natural order
+        assert torch.equal(out, nat.view(B, S, Hk, dh).transpose(1, 2))

@@ -11,7 +11,7 @@ from folded_tensor_sequence_gb300 import synth
 from folded_tensor_sequence_gb300.configs import MID_BF16, TINY_F32, LayerConfig
 from oracle import tsp_oracle as O
 
-from helpers import check, rel_frob, to_dev, to_np
+from helpers import Guarded, check, guarded_like, guarded_workspace, rel_frob, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -39,34 +39,42 @@ def setup(tsp, cfg, inp=None, seed=0):
 
 
 def run_pieces(tsp, cfg, plan, packed, x):
-    """Runs attention_fwd, gated_mlp_fwd and layer_fwd; returns natural-order A, MLP(H_ref-free), Y, lse."""
+    """Runs attention_fwd, gated_mlp_fwd and layer_fwd; returns natural-order A, MLP(H_ref-free), Y, lse.
+
+    Every output and workspace sits between guard bands that must be intact afterwards."""
     import torch
 
     B = cfg.batch
-    xz = torch.empty_like(x)
-    tsp.tsp_zigzag_permute(plan, B, x, xz)
-    a = torch.empty_like(x)
-    lse = torch.empty(B, cfg.heads, cfg.seq, dtype=torch.float32, device="cuda")
-    tsp.tsp_attention_fwd(plan, B, xz, packed, a, lse, tsp.workspace(plan, B, tsp.TSP_OP_ATTENTION_FWD))
-    y = torch.empty_like(x)
-    tsp.tsp_layer_fwd(plan, B, x, packed, y, None, tsp.workspace(plan, B, tsp.TSP_OP_LAYER_FWD))
+    xz = guarded_like(x)
+    tsp.tsp_zigzag_permute(plan, B, x, xz.t)
+    a = guarded_like(x)
+    lse = Guarded((B, cfg.heads, cfg.seq), torch.float32)
+    wa = guarded_workspace(tsp, plan, B, tsp.TSP_OP_ATTENTION_FWD)
+    tsp.tsp_attention_fwd(plan, B, xz.t, packed, a.t, lse.t, wa.t)
+    y = guarded_like(x)
+    wl = guarded_workspace(tsp, plan, B, tsp.TSP_OP_LAYER_FWD)
+    tsp.tsp_layer_fwd(plan, B, x, packed, y.t, None, wl.t)
     tsp.tsp_sync_check()
-    a_nat = O.zigzag_unpermute(to_np(a).reshape(cfg.D, B, -1, cfg.hidden), cfg.D)
-    return a_nat, to_np(y), to_np(lse)
+    for g, what in ((xz, "xz"), (a, "a_out"), (lse, "lse"), (y, "y"), (wa, "attention workspace"),
+                    (wl, "layer workspace")):
+        g.check(f"{cfg.name} {what}")
+    a_nat = O.zigzag_unpermute(to_np(a.t).reshape(cfg.D, B, -1, cfg.hidden), cfg.D)
+    return a_nat, to_np(y.t), to_np(lse.t)
 
 
 def mlp_piece(tsp, cfg, plan, packed, H_np):
     """gated_mlp_fwd on the given natural-order H (values exact in the plan dtype)."""
-    import torch
-
     B = cfg.batch
     Hd = to_dev(H_np, cfg.dtype)
-    hz = torch.empty_like(Hd)
-    tsp.tsp_zigzag_permute(plan, B, Hd, hz)
-    m = torch.empty_like(Hd)
-    tsp.tsp_gated_mlp_fwd(plan, B, hz, packed, m, tsp.workspace(plan, B, tsp.TSP_OP_GATED_MLP_FWD))
+    hz = guarded_like(Hd)
+    tsp.tsp_zigzag_permute(plan, B, Hd, hz.t)
+    m = guarded_like(Hd)
+    wm = guarded_workspace(tsp, plan, B, tsp.TSP_OP_GATED_MLP_FWD)
+    tsp.tsp_gated_mlp_fwd(plan, B, hz.t, packed, m.t, wm.t)
     tsp.tsp_sync_check()
-    return O.zigzag_unpermute(to_np(m).reshape(cfg.D, B, -1, cfg.hidden), cfg.D)
+    for g, what in ((hz, "hz"), (m, "m_out"), (wm, "mlp workspace")):
+        g.check(f"{cfg.name} {what}")
+    return O.zigzag_unpermute(to_np(m.t).reshape(cfg.D, B, -1, cfg.hidden), cfg.D)
 
 
 def round_to(a, dtype):
