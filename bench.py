@@ -64,9 +64,9 @@ NCU_TRAFFIC = {
     ("attention bwd fused", "bf16_fwdbwd_gqa8_D8_b1_s8192_h4096"):
         (652.95e6 + 290.93e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
     ("kv gather (standalone)", "bf16_D8_b2_s16384_h4096"):
-        (536.909e6 + 486.555e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "e1cfd23fddcaefb4"),
+        (536.903e6 + 486.071e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "535fa8a09df460cd"),
     ("zigzag permute (standalone)", "bf16_D8_b2_s16384_h4096"):
-        (268.449e6 + 216.701e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "e1cfd23fddcaefb4"),
+        (268.449e6 + 217.227e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "535fa8a09df460cd"),
     ("decode attention", "bf16_decode_D8_b1_ctx131072_h4096"):
         (2.15e9 + 0.00292e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "3bfb1d17f6da32df"),
     ("decode attention", "bf16_decode_gqa8_D8_b4_ctx131072_h4096"):
@@ -188,6 +188,10 @@ def step_work(cfg, cfg_det=False):
     return w
 
 
+# The layout calls timed on their own after the layer (kernel table names get " (standalone)").
+LAYOUT_STEPS = ("zigzag permute", "kv gather", "zigzag unpermute")
+
+
 def time_layout(cfg, plan, x, steps: int, warmup: int, hbm_peak: float, dev):
     """The zigzag permute, the K/V all-gather and the unpermute called on their
     own through the C ABI at the workload's full size (inputs larger than L2),
@@ -234,6 +238,66 @@ def time_layout(cfg, plan, x, steps: int, warmup: int, hbm_peak: float, dev):
                      "bytes": nbytes[name], "launches": cnt}
     del xz, xu, kz, vz, k, v
     return out
+
+
+def time_rank_compute(cfg, plan, packed, x, steps: int, warmup: int, dev, layer_ms: float):
+    """One rank's compute in a D-GPU TSP layer (tsp_rank_* calls), shards
+    already in local memory: for every attention shard the projection of the
+    rank's tokens, attention over the gathered K/V and the output projection,
+    then the D steps of the MLP ring.  Timed with CUDA events for rank 0 and
+    rank D-1 (the zigzag split gives every rank the same causal work).  The
+    exchanges between GPUs are not part of it."""
+    import torch
+
+    from folded_tensor_sequence_gb300 import tsp, tsp_rank
+
+    D, B = cfg.D, cfg.batch
+    stream = torch.cuda.current_stream(dev)
+    attn = [torch.empty(tsp.tsp_rank_shard_bytes(plan, tsp.TSP_SHARD_ATTENTION), dtype=torch.uint8, device=dev)
+            for _ in range(D)]
+    mlp = [torch.empty(tsp.tsp_rank_shard_bytes(plan, tsp.TSP_SHARD_MLP), dtype=torch.uint8, device=dev)
+           for _ in range(D)]
+    for s_ in range(D):
+        tsp.tsp_rank_extract_shard(plan, packed, s_, tsp.TSP_SHARD_ATTENTION, attn[s_], stream)
+        tsp.tsp_rank_extract_shard(plan, packed, s_, tsp.TSP_SHARD_MLP, mlp[s_], stream)
+    xz = torch.empty_like(x)
+    tsp.tsp_zigzag_permute(plan, B, x, xz, stream)
+    xr = xz.view(D, -1, cfg.hidden)
+    out = {}
+    for r in sorted({0, D - 1}):
+        layer = tsp_rank.RankLayer(plan, r, B, dev, stream)
+        gen = torch.Generator(device=dev).manual_seed(2)
+        layer.kv_all.copy_(torch.randn(layer.kv_all.shape, generator=gen, device=dev).to(layer.kv_all.dtype))
+
+        def rank_step():
+            for s_ in range(D):
+                layer.project(xr[r], attn[s_])
+                layer.attend(attn[s_], xr[r] if s_ == 0 else layer.h)
+            for t in range(D):
+                layer.mlp(mlp[(r - t) % D], layer.h if t == 0 else layer.y)
+
+        for _ in range(warmup):
+            rank_step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            rank_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        tsp.tsp_profile_enable(True)
+        rank_step()
+        parts = {n: round(t, 4) for n, t, _ in tsp.tsp_profile_report()}
+        tsp.tsp_profile_enable(False)
+        out[f"rank {r}"] = {"ms": round(ms, 4), "tflops": round(cfg.fwd_flops() / D / ms / 1e9, 1),
+                            "steps_ms": parts}
+        del layer
+    tsp.tsp_sync_check(stream)
+    return {"per_rank": out, "ideal_ms": round(layer_ms / D, 4),
+            "note": ("compute of one rank of a D-GPU TSP layer on this GPU (its 1/D of the tokens against every "
+                     "weight shard, shards already local); ideal_ms = the one-GPU layer's time / D; the "
+                     "broadcasts, the K/V all-gather and the ring hops between GPUs are not included")}
 
 
 class ClockSampler:
@@ -407,6 +471,7 @@ def main():
     ap.add_argument("--cpu-prefix", type=int, default=512, help="tokens of the oracle's CPU baseline sample")
     ap.add_argument("--ref-prefix", type=int, default=64, help="tokens per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rank-compute", action="store_true", help="skip timing one rank of a D-GPU TSP layer")
     ap.add_argument("--deterministic", action="store_true",
                     help="backward: split bitwise-reproducible kernels instead of the fused one")
     args = ap.parse_args()
@@ -586,6 +651,14 @@ def main():
                     "peak_source": f"{peak_src} HBM copy (torch copy_ of 2 GiB)",
                     "algorithmic": f"{hent['bytes'] / 1e9:.3f} GB per launch (read + write)"}
 
+    # ---- one rank of a D-GPU TSP layer (compute only) ------------------------
+    rank_compute = None
+    if not cfg.decode and not cfg.backward and cfg.D > 1 and not args.no_rank_compute:
+        try:
+            rank_compute = time_rank_compute(cfg, plan, packed, x, args.steps, args.warmup, dev, ms_step)
+        except Exception as e:  # noqa: BLE001 -- e.g. a shape the per-rank calls do not take
+            rank_compute = {"unavailable": str(e)[:300]}
+
     # ---- end to end through the API with host buffers -----------------------
     # Every step's inputs come from pinned host memory and its result goes back
     # to it.  As a caller overlapping I/O with the layer would, one copy stream
@@ -665,6 +738,7 @@ def main():
             "roofline": roof,
             "roofline_hbm": roof_hbm,
             "layout_kernels": layout,
+            "tsp_rank_compute": rank_compute,
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,

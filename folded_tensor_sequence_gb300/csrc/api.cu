@@ -362,6 +362,70 @@ tsp_status mlp_impl(const tsp_plan* p, int batch, const void* hz, const tsp_weig
   return run_gemm(p, mz, F, w->down, F, T, h, F, resid ? EPI_RESID : EPI_STORE, ed, st, "down projection");
 }
 
+// ---- one rank of a multi-GPU layer (tsp_rank_*) --------------------------------
+
+struct RankDims {
+  int64_t L;       // local rows: batch * 2C
+  int hs, ks, fs;  // h/D, hk/D, F/D
+};
+
+RankDims rank_dims(const tsp_plan* p, int batch) {
+  return RankDims{(int64_t)batch * 2 * p->chunk, p->hidden / p->D, kv_hidden(p) / p->D, p->ffn / p->D};
+}
+
+// Element offsets of the second matrix in each shard buffer (o_s, down_j).
+size_t attn_shard_o_offset(const tsp_plan* p) {
+  const RankDims d = rank_dims(p, 0);
+  return (size_t)(d.hs + 2 * d.ks) * p->hidden;
+}
+size_t mlp_shard_down_offset(const tsp_plan* p) { return (size_t)2 * (p->ffn / p->D) * p->hidden; }
+
+tsp_status check_rank_shapes(const tsp_plan* p, const char* what) {
+  const RankDims d = rank_dims(p, 0);
+  const size_t e = esize(p);
+  if (d.fs % 128)
+    return fail(TSP_ERR_UNSUPPORTED, "%s: ffn/D = %d is not a multiple of 128 (a shard holds whole gate/up blocks)",
+                what, d.fs);
+  if ((d.hs * e) % 16 || (2 * d.ks * e) % 16)
+    return fail(TSP_ERR_UNSUPPORTED, "%s: hidden/D and 2*kv_hidden/D rows must be multiples of 16 bytes", what);
+  if (p->dtype == TSP_BF16) {
+    tsp_status s = check_bf16_shapes(p);
+    if (s != TSP_OK) return s;
+    if (d.hs % 256 || (2 * d.ks) % 256)
+      return fail(TSP_ERR_UNSUPPORTED, "%s: bf16 needs hidden/D %% 256 == 0 and 2*kv_hidden/D %% 256 == 0 (got %d, %d)",
+                  what, d.hs, 2 * d.ks);
+  }
+  return TSP_OK;
+}
+
+struct RankAttnLayout {
+  size_t k, v, vt, o, end;
+};
+
+RankAttnLayout rank_attn_layout(const tsp_plan* p, int batch) {
+  const RankDims d = rank_dims(p, batch);
+  const size_t e = esize(p), kvb = (size_t)batch * p->seq * d.ks * e;
+  RankAttnLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.k = take(kvb);
+  L.v = take(kvb);
+  L.vt = use_tc_attention(p) ? take(kvb) : L.v;
+  L.o = take((size_t)d.L * d.hs * e);
+  L.end = o;
+  return L;
+}
+
+size_t rank_mlp_ws_bytes(const tsp_plan* p, int batch) {
+  const RankDims d = rank_dims(p, batch);
+  const size_t e = esize(p);
+  return align256((size_t)d.L * d.fs * e) + (p->dtype == TSP_BF16 ? 0 : align256((size_t)d.L * 2 * d.fs * e));
+}
+
 }  // namespace
 
 tsp_status report_error(tsp_status s, const char* msg) { return fail(s, "%s", msg); }
@@ -518,6 +582,8 @@ size_t tsp_workspace_bytes(const tsp_plan* p, int batch, tsp_op op) {
     case TSP_OP_LAYER_FWD: return layer_layout(p, batch).fwd_end;
     case TSP_OP_LAYER_BWD: return bwd_layout(p, batch).end;
     case TSP_OP_DECODE: return decode_ws_bytes(p, batch);
+    case TSP_OP_RANK_ATTENTION: return rank_attn_layout(p, batch).end;
+    case TSP_OP_RANK_MLP: return rank_mlp_ws_bytes(p, batch);
   }
   return 0;
 }
@@ -907,6 +973,184 @@ tsp_status tsp_decode_step(const tsp_plan* p, int batch, int64_t pos, const void
   s = decode_step_bf16(p, batch, pos, x_new, w, k_cache, v_cache, y_new, ws, as_stream(stream));
   if (s != TSP_OK) return fail(s, "decode step failed: %s", tsp_status_string(s));
   return TSP_OK;
+}
+
+size_t tsp_rank_shard_bytes(const tsp_plan* p, tsp_shard_kind kind) {
+  if (!p) return 0;
+  const RankDims d = rank_dims(p, 0);
+  const size_t e = esize(p), h = p->hidden;
+  if (kind == TSP_SHARD_ATTENTION) return ((size_t)(d.hs + 2 * d.ks) * h + h * d.hs) * e;
+  if (kind == TSP_SHARD_MLP) return ((size_t)2 * d.fs * h + h * d.fs) * e;
+  return 0;
+}
+
+tsp_status tsp_rank_extract_shard(const tsp_plan* p, const tsp_weights* w, int shard, tsp_shard_kind kind, void* out,
+                                  void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if (!p || !w) return fail(TSP_ERR_INVALID_ARG, "tsp_rank_extract_shard: NULL plan or weights");
+  if (shard < 0 || shard >= p->D) return fail(TSP_ERR_INVALID_ARG, "shard %d not in [0, D = %d)", shard, p->D);
+  if (kind != TSP_SHARD_ATTENTION && kind != TSP_SHARD_MLP)
+    return fail(TSP_ERR_INVALID_ARG, "unknown shard kind %d", (int)kind);
+  if ((s = check_rank_shapes(p, "tsp_rank_extract_shard")) != TSP_OK) return s;
+  const void* a = kind == TSP_SHARD_ATTENTION ? w->qkv : w->gate_up;
+  const void* b = kind == TSP_SHARD_ATTENTION ? w->o : w->down;
+  if ((s = check_ptrs({a, b, out}, "tsp_rank_extract_shard")) != TSP_OK) return s;
+  if ((s = check_stream_device(stream, "tsp_rank_extract_shard")) != TSP_OK) return s;
+  const RankDims d = rank_dims(p, 0);
+  const int64_t e = (int64_t)esize(p), h = p->hidden;
+  cudaStream_t st = as_stream(stream);
+  char* dst = static_cast<char*>(out);
+  cudaError_t ce;
+  if (kind == TSP_SHARD_ATTENTION) {
+    const int64_t rows = d.hs + 2 * d.ks;  // the shard's rows of packed qkv, then its input rows of W_O
+    ce = launch_copy_rows(static_cast<const char*>(a) + shard * rows * h * e, h * e, dst, h * e, rows, h * e, st);
+    if (ce == cudaSuccess)
+      ce = launch_copy_rows(static_cast<const char*>(b) + (int64_t)shard * d.hs * e, h * e,
+                            dst + attn_shard_o_offset(p) * e, d.hs * e, h, d.hs * e, st);
+  } else {
+    const int64_t F = p->ffn;
+    ce = launch_copy_rows(static_cast<const char*>(a) + (int64_t)shard * 2 * d.fs * h * e, h * e, dst, h * e,
+                          2 * d.fs, h * e, st);
+    if (ce == cudaSuccess)
+      ce = launch_copy_rows(static_cast<const char*>(b) + (int64_t)shard * d.fs * e, F * e,
+                            dst + mlp_shard_down_offset(p) * e, d.fs * e, h, d.fs * e, st);
+  }
+  return cuda_status(ce, "extract shard");
+}
+
+tsp_status tsp_rank_qkv(const tsp_plan* p, int batch, const void* x_local, const void* attn_shard, void* q_local,
+                        void* kv_local, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if ((s = check_ptrs({x_local, attn_shard, q_local, kv_local}, "tsp_rank_qkv")) != TSP_OK) return s;
+  if ((s = check_rank_shapes(p, "tsp_rank_qkv")) != TSP_OK) return s;
+  if ((s = check_stream_device(stream, "tsp_rank_qkv")) != TSP_OK) return s;
+  const RankDims d = rank_dims(p, batch);
+  const int h = p->hidden;
+  cudaStream_t st = as_stream(stream);
+  EpiParams eq = base_epi(p, batch);
+  eq.out = q_local;
+  eq.ldo = d.hs;
+  if ((s = run_gemm(p, x_local, h, attn_shard, h, (int)d.L, d.hs, h, EPI_STORE, eq, st, "rank Q projection")) !=
+      TSP_OK)
+    return s;
+  EpiParams ekv = base_epi(p, batch);
+  ekv.out = kv_local;
+  ekv.ldo = 2 * d.ks;
+  const char* wkv = static_cast<const char*>(attn_shard) + (size_t)d.hs * h * esize(p);
+  return run_gemm(p, x_local, h, wkv, h, (int)d.L, 2 * d.ks, h, EPI_STORE, ekv, st, "rank K/V projection");
+}
+
+tsp_status tsp_rank_attention(const tsp_plan* p, int rank, int batch, const void* q_local, const void* kv_all,
+                              const void* attn_shard, const void* resid, void* h_out, void* ws, size_t ws_bytes,
+                              void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (rank < 0 || rank >= p->D) return fail(TSP_ERR_INVALID_ARG, "rank %d not in [0, D = %d)", rank, p->D);
+  if (batch == 0) return TSP_OK;
+  if ((s = check_ptrs({q_local, kv_all, attn_shard, h_out, ws}, "tsp_rank_attention")) != TSP_OK) return s;
+  if (resid && !aligned16(resid)) return fail(TSP_ERR_INVALID_ARG, "tsp_rank_attention: resid not 16-byte aligned");
+  if ((s = check_rank_shapes(p, "tsp_rank_attention")) != TSP_OK) return s;
+  const RankAttnLayout W = rank_attn_layout(p, batch);
+  if (ws_bytes < W.end) return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, W.end);
+  if ((s = check_stream_device(stream, "tsp_rank_attention")) != TSP_OK) return s;
+  const RankDims d = rank_dims(p, batch);
+  const int h = p->hidden, hk_heads = p->kv_heads / p->D;
+  const size_t e = esize(p);
+  cudaStream_t st = as_stream(stream);
+  char* wb = static_cast<char*>(ws);
+  {
+    // the all-gathered rows [D][L][2 ks] (K columns, then V) into natural positions [B][Hk/D][S][dh]
+    Prof pr("rank K/V reorder", st);
+    s = cuda_status(launch_kv_gather_ld(kv_all, static_cast<const char*>(kv_all) + (size_t)d.ks * e, wb + W.k,
+                                        wb + W.v, (int)e, p->D, batch, p->seq, hk_heads, p->head_dim, 2 * d.ks, st),
+                    "rank K/V reorder");
+  }
+  if (s != TSP_OK) return s;
+  const bool tc = use_tc_attention(p);
+  if (tc) {
+    Prof pr("rank V transpose", st);
+    s = cuda_status(launch_transpose(wb + W.v, wb + W.vt, p->seq, p->head_dim, (int)e, st, batch * hk_heads),
+                    "rank V transpose");
+    if (s != TSP_OK) return s;
+  }
+  AttnParams ap;
+  ap.q = q_local;
+  ap.k = wb + W.k;
+  ap.v = wb + W.vt;
+  ap.o = wb + W.o;
+  ap.lse = nullptr;
+  ap.D = p->D;
+  ap.B = batch;
+  ap.H = p->heads / p->D;
+  ap.Hk = hk_heads;
+  ap.dh = p->head_dim;
+  ap.S = p->seq;
+  ap.C = p->chunk;
+  ap.rank = rank;
+  {
+    Prof pr("rank attention", st);
+    s = p->dtype != TSP_BF16 ? attn_fwd_f32(ap, st) : (tc ? attn_fwd_bf16_tc(ap, st) : attn_fwd_bf16(ap, st));
+  }
+  if (s != TSP_OK) return fail(s, "rank attention kernel failed: %s", tsp_status_string(s));
+  EpiParams eo = base_epi(p, batch);
+  eo.out = h_out;
+  eo.ldo = h;
+  eo.resid = resid;
+  eo.ldr = h;
+  const char* wo = static_cast<const char*>(attn_shard) + attn_shard_o_offset(p) * e;
+  return run_gemm(p, wb + W.o, d.hs, wo, d.hs, (int)d.L, h, d.hs, resid ? EPI_RESID : EPI_STORE, eo, st,
+                  "rank output projection");
+}
+
+tsp_status tsp_rank_mlp(const tsp_plan* p, int batch, const void* h_local, const void* mlp_shard, const void* resid,
+                        void* y_out, void* ws, size_t ws_bytes, void* stream) {
+  tsp_status s;
+  if (injected(&s)) return s;
+  if ((s = check_plan_batch(p, batch)) != TSP_OK) return s;
+  if (batch == 0) return TSP_OK;
+  if ((s = check_ptrs({h_local, mlp_shard, y_out, ws}, "tsp_rank_mlp")) != TSP_OK) return s;
+  if (resid && !aligned16(resid)) return fail(TSP_ERR_INVALID_ARG, "tsp_rank_mlp: resid not 16-byte aligned");
+  if ((s = check_rank_shapes(p, "tsp_rank_mlp")) != TSP_OK) return s;
+  if (ws_bytes < rank_mlp_ws_bytes(p, batch))
+    return fail(TSP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, rank_mlp_ws_bytes(p, batch));
+  if ((s = check_stream_device(stream, "tsp_rank_mlp")) != TSP_OK) return s;
+  const RankDims d = rank_dims(p, batch);
+  const int h = p->hidden;
+  const size_t e = esize(p);
+  cudaStream_t st = as_stream(stream);
+  char* mz = static_cast<char*>(ws);
+  if (p->dtype == TSP_BF16) {
+    EpiParams eg = base_epi(p, batch);
+    eg.out = mz;
+    eg.ldo = d.fs;
+    s = run_gemm(p, h_local, h, mlp_shard, h, (int)d.L, 2 * d.fs, h, EPI_SWIGLU, eg, st, "rank gate/up projection");
+  } else {
+    char* gu = mz + align256((size_t)d.L * d.fs * e);
+    EpiParams eg = base_epi(p, batch);
+    eg.out = gu;
+    eg.ldo = 2 * d.fs;
+    s = run_gemm(p, h_local, h, mlp_shard, h, (int)d.L, 2 * d.fs, h, EPI_STORE, eg, st, "rank gate/up projection");
+    if (s == TSP_OK) {
+      Prof pr("rank swiglu", st);
+      s = cuda_status(launch_swiglu_f32(reinterpret_cast<const float*>(gu), reinterpret_cast<float*>(mz), d.L, d.fs,
+                                        st),
+                      "rank swiglu");
+    }
+  }
+  if (s != TSP_OK) return s;
+  EpiParams ed = base_epi(p, batch);
+  ed.out = y_out;
+  ed.ldo = h;
+  ed.resid = resid;
+  ed.ldr = h;
+  const char* wd = static_cast<const char*>(mlp_shard) + mlp_shard_down_offset(p) * e;
+  return run_gemm(p, mz, d.fs, wd, d.fs, (int)d.L, h, d.fs, resid ? EPI_RESID : EPI_STORE, ed, st,
+                  "rank down projection");
 }
 
 tsp_status tsp_debug_wait_timeout(unsigned int timeout_us, void* stream) {

@@ -30,13 +30,14 @@ using namespace wm;
 __global__ void attn_fwd_f32_kernel(AttnParams p) {
   extern __shared__ float qs_all[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t T = (int64_t)p.B * p.S;
+  const int64_t twoC = 2 * p.C, per_rank = (int64_t)p.B * twoC;
+  const int64_t T = p.rank < 0 ? (int64_t)p.B * p.S : per_rank;  // rows of q and o
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + warp;
   if (w >= T * p.H) return;
-  const int64_t zrow = w / p.H;
+  const int64_t zrow = w / p.H;  // row of q and o
   const int head = (int)(w % p.H);
-  const int64_t twoC = 2 * p.C, per_rank = (int64_t)p.B * twoC;
-  const int64_t r = zrow / per_rank, rem = zrow % per_rank, b = rem / twoC, kk = rem % twoC;
+  const int64_t r = p.rank < 0 ? zrow / per_rank : p.rank, rem = p.rank < 0 ? zrow % per_rank : zrow;
+  const int64_t b = rem / twoC, kk = rem % twoC;
   const int64_t qpos = kk < p.C ? r * p.C + kk : (2 * p.D - 1 - r) * p.C + (kk - p.C);
   const int dh = p.dh, h = p.H * dh;
   float* qs = qs_all + warp * dh;
@@ -113,15 +114,18 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_fwd_bf16_kernel(AttnParams p
   const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(p.v) + ((int64_t)b * p.Hk + kvh) * S * DH;
   const int total_tiles = 2 * D * n_tiles;
 
+  // one rank's queries: that rank's light tiles only, q and o holding its rows alone
+  const int light = (p.rank < 0 ? 0 : p.rank * n_tiles) + (int)blockIdx.x;
+  const int64_t row_off = p.rank < 0 ? 0 : (int64_t)p.rank * p.B * 2 * C;
   for (int which = 0; which < 2; ++which) {
     // heavy tile of the mirror pair first
-    const int gt = which == 0 ? total_tiles - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const int gt = which == 0 ? total_tiles - 1 - light : light;
     const int c = gt / n_tiles, i = gt % n_tiles;
     const int64_t off = (int64_t)i * BQ;
     const int nrows = (int)min64(BQ, C - off);
     const int64_t r = c < D ? c : 2 * D - 1 - c;
     const int64_t k0 = c < D ? off : C + off;
-    const int64_t zrow0 = (r * p.B + b) * 2 * C + k0;
+    const int64_t zrow0 = (r * p.B + b) * 2 * C + k0 - row_off;
     const int64_t p0 = (int64_t)c * C + off;  // global position of the tile's first query
     const int64_t qlast = p0 + nrows - 1;
     const int nkt = (int)(qlast / BKV) + 1;
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_fwd_bf16_kernel(AttnParams p
 }  // namespace
 
 tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream) {
-  const int64_t warps = (int64_t)p.B * p.S * p.H;
+  const int64_t warps = (p.rank < 0 ? (int64_t)p.B * p.S : (int64_t)p.B * 2 * p.C) * p.H;
   if (warps == 0) return TSP_OK;
   if (p.dh > 128) return TSP_ERR_UNSUPPORTED;
   const int wpb = 8;
@@ -291,7 +295,7 @@ tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream) {
     mark_setup_done(configured);
   }
   const int n_tiles = (int)((p.C + BQ - 1) / BQ);
-  dim3 grid(p.D * n_tiles, p.H, p.B);
+  dim3 grid(p.rank < 0 ? p.D * n_tiles : n_tiles, p.H, p.B);
   attn_fwd_bf16_kernel<<<grid, ATT_THREADS, ATT_SMEM, stream>>>(p, n_tiles);
   return cudaGetLastError() == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
 }

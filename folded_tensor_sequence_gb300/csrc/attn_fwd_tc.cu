@@ -57,6 +57,8 @@ struct FaParams {
   int Hk;           // K/V heads; query head `head` reads K/V head head / (H / Hk)
   int64_t S, C;
   int h;
+  int g_off;        // first light block of the grid (rank * nb when one rank's queries run)
+  int64_t row_off;  // zigzag row held by row 0 of Q and O (rank * B * 2C likewise)
   __nv_bfloat16* o;
   float* lse;
   unsigned int* err;
@@ -138,7 +140,7 @@ __device__ __forceinline__ BlockGeo block_geo(int G, const FaParams& p, int b) {
   const int64_t r = c < p.D ? c : 2 * p.D - 1 - c;
   const int64_t k0 = (c < p.D ? 0 : p.C) + (int64_t)i * 2 * QT;
   BlockGeo g;
-  g.zrow0 = (r * p.B + b) * 2 * p.C + k0;
+  g.zrow0 = (r * p.B + b) * 2 * p.C + k0 - p.row_off;
   g.p0 = (int64_t)c * p.C + (int64_t)i * 2 * QT;
   g.nB = (int)(g.p0 / KT) + 2;
   return g;
@@ -166,7 +168,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int head = blockIdx.y, b = blockIdx.z;
   const int total_blocks = 2 * p.D * p.nb;
   // the CTA's two blocks: heavy (late in the sequence) first, then its mirror
-  auto blk_id = [&](int blk) { return blk == 0 ? total_blocks - 1 - (int)blockIdx.x : (int)blockIdx.x; };
+  const int light = p.g_off + (int)blockIdx.x;
+  auto blk_id = [&](int blk) { return blk == 0 ? total_blocks - 1 - light : light; };
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full[0], 1);
@@ -499,7 +502,8 @@ bool attn_tc_supported(int head_dim, int64_t chunk) { return head_dim == HD && c
 tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   if (!attn_tc_supported(a.dh, a.C)) return TSP_ERR_UNSUPPORTED;
   if (a.B * a.S == 0) return TSP_OK;
-  const int64_t T = (int64_t)a.B * a.S;
+  // Q / O rows: every rank's, or one rank's B * 2C
+  const int64_t T = a.rank < 0 ? (int64_t)a.B * a.S : (int64_t)a.B * 2 * a.C;
   const int h = a.H * HD;
   CUtensorMap mq, mk, mv;
   if (!make_tma_2d_bf16(&mq, a.q, T, h, h, 128) ||
@@ -525,7 +529,9 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.err = dev_error_word();
-  dim3 grid(a.D * p.nb, a.H, a.B);
+  p.g_off = a.rank < 0 ? 0 : a.rank * p.nb;
+  p.row_off = a.rank < 0 ? 0 : (int64_t)a.rank * a.B * 2 * a.C;
+  dim3 grid(a.rank < 0 ? a.D * p.nb : p.nb, a.H, a.B);
   attn_fwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
 }

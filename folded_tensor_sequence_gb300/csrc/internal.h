@@ -90,6 +90,12 @@ cudaError_t launch_zigzag_rows(const void* src, void* dst, int64_t row_bytes, in
                                bool to_zigzag, cudaStream_t stream);
 cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
                              int64_t S, int H, int dh, cudaStream_t stream);
+// The same with source rows src_ld elements apart (a multiple of 16 bytes).
+cudaError_t launch_kv_gather_ld(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
+                                int64_t S, int H, int dh, int64_t src_ld, cudaStream_t stream);
+// 2-D copy of `rows` rows of row_bytes (pitches and row_bytes multiples of 16).
+cudaError_t launch_copy_rows(const void* src, int64_t src_pitch_bytes, void* dst, int64_t dst_pitch_bytes,
+                             int64_t rows, int64_t row_bytes, cudaStream_t stream);
 cudaError_t launch_swiglu_f32(const float* gu, float* m, int64_t T, int F, cudaStream_t stream);
 cudaError_t launch_transpose(const void* src, void* dst, int64_t rows, int64_t cols, int elem_bytes,
                              cudaStream_t stream, int batch = 1);
@@ -108,6 +114,9 @@ struct AttnParams {
   int D, B, H, dh;
   int64_t S, C;
   int Hk;
+  // -1: the queries of every rank.  r >= 0: only rank r's queries; q and o
+  // then hold just that rank's zigzag rows ([B][2C][H*dh], row b*2C + k).
+  int rank = -1;
 };
 tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream);
 tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream);

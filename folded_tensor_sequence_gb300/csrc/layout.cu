@@ -72,18 +72,18 @@ __global__ void __launch_bounds__(kCopyThreads) zigzag_rows_kernel(const uint4* 
 }
 
 // K/V all-gather into natural order: gathered [B][Hk][S][dh] <- zigzag
-// [T][Hk*dh].  Work item = (tensor K or V, sequence b, K/V head, chunk c):
-// natural positions c*C .. c*C+C-1 of that head are C consecutive rows of
-// dh*e bytes in the destination, read from C consecutive zigzag rows of rank
-// r(c) (row stride Hk*dh*e bytes) at the head's column offset.  vph = vectors
-// per head row, a power of two (dh * elem_bytes / 16 with dh in {32, 64, 128}).
+// [T][Hk*dh] (source rows `vec_per_row` vectors apart).  Work item = (tensor
+// K or V, sequence b, K/V head, chunk c): natural positions c*C .. c*C+C-1 of
+// that head are C consecutive rows of dh*e bytes in the destination, read
+// from C consecutive zigzag rows of rank r(c) at the head's column offset.
+// vph = vectors per head row, a power of two (dh * elem_bytes / 16 with dh in
+// {32, 64, 128}).
 __global__ void __launch_bounds__(kCopyThreads) kv_gather_kernel(const uint4* __restrict__ kz,
                                                                  const uint4* __restrict__ vz, uint4* __restrict__ k,
                                                                  uint4* __restrict__ v, int lg_vph, int D, int B,
-                                                                 int64_t S, int H) {
+                                                                 int64_t S, int H, int64_t vec_per_row) {
   const int64_t C = S / (2 * D);
   const int vph = 1 << lg_vph;
-  const int64_t vec_per_row = (int64_t)H * vph;
   const int64_t seg_vecs = C << lg_vph;
   const int64_t items = 2LL * B * H * 2 * D;
   for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
@@ -110,6 +110,18 @@ __global__ void __launch_bounds__(kCopyThreads) kv_gather_kernel(const uint4* __
         if (i < seg_vecs) __stcs(dst + i, t[u]);
       }
     }
+  }
+}
+
+// 2-D copy: `rows` rows of `row_vecs` 16-byte vectors, source rows
+// `src_pitch` vectors apart, destination rows `dst_pitch` vectors apart.
+__global__ void __launch_bounds__(kCopyThreads) copy_rows_kernel(const uint4* __restrict__ src, int64_t src_pitch,
+                                                                 uint4* __restrict__ dst, int64_t dst_pitch,
+                                                                 int64_t rows, int64_t row_vecs) {
+  const int64_t total = rows * row_vecs;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / row_vecs, c = i - r * row_vecs;
+    dst[r * dst_pitch + c] = __ldg(&src[r * src_pitch + c]);
   }
 }
 
@@ -352,6 +364,11 @@ cudaError_t launch_zigzag_rows(const void* src, void* dst, int64_t row_bytes, in
 
 cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
                              int64_t S, int H, int dh, cudaStream_t stream) {
+  return launch_kv_gather_ld(kz, vz, k, v, elem_bytes, D, B, S, H, dh, (int64_t)H * dh, stream);
+}
+
+cudaError_t launch_kv_gather_ld(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
+                                int64_t S, int H, int dh, int64_t src_ld, cudaStream_t stream) {
   const int vph = dh * elem_bytes / 16;
   int lg = 0;
   while ((1 << lg) < vph) ++lg;
@@ -361,7 +378,18 @@ cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, i
   const int64_t cap = (int64_t)num_sms() * 8;
   kv_gather_kernel<<<(int)(items < cap ? items : cap), kCopyThreads, 0, stream>>>(
       static_cast<const uint4*>(kz), static_cast<const uint4*>(vz), static_cast<uint4*>(k), static_cast<uint4*>(v),
-      lg, D, B, S, H);
+      lg, D, B, S, H, src_ld * elem_bytes / 16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_rows(const void* src, int64_t src_pitch_bytes, void* dst, int64_t dst_pitch_bytes,
+                             int64_t rows, int64_t row_bytes, cudaStream_t stream) {
+  if (rows == 0 || row_bytes == 0) return cudaSuccess;
+  if ((src_pitch_bytes | dst_pitch_bytes | row_bytes) % 16) return cudaErrorInvalidValue;
+  const int64_t total = rows * (row_bytes / 16);
+  copy_rows_kernel<<<grid_for(total, kCopyThreads), kCopyThreads, 0, stream>>>(
+      static_cast<const uint4*>(src), src_pitch_bytes / 16, static_cast<uint4*>(dst), dst_pitch_bytes / 16, rows,
+      row_bytes / 16);
   return cudaGetLastError();
 }
 

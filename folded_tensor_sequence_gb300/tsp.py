@@ -18,7 +18,9 @@ from . import build as _build
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT, TSP_ERR_WORKSPACE = range(6)
 TSP_F32, TSP_BF16 = 0, 1
-TSP_OP_ATTENTION_FWD, TSP_OP_GATED_MLP_FWD, TSP_OP_LAYER_FWD, TSP_OP_LAYER_BWD, TSP_OP_DECODE = range(5)
+(TSP_OP_ATTENTION_FWD, TSP_OP_GATED_MLP_FWD, TSP_OP_LAYER_FWD, TSP_OP_LAYER_BWD, TSP_OP_DECODE,
+ TSP_OP_RANK_ATTENTION, TSP_OP_RANK_MLP) = range(7)
+TSP_SHARD_ATTENTION, TSP_SHARD_MLP = 0, 1
 TSP_STATIC_SCRATCH_BYTES = 32 << 20  # size of the static scratch array behind tsp_attention_fwd_static
 
 EXPORTS = [
@@ -27,7 +29,8 @@ EXPORTS = [
     "tsp_zigzag_unpermute", "tsp_kv_gather", "tsp_attention_fwd", "tsp_gated_mlp_fwd", "tsp_layer_fwd",
     "tsp_layer_bwd", "tsp_sync_check", "tsp_debug_fail_next", "tsp_profile_enable", "tsp_profile_report",
     "tsp_attention_fwd_static", "tsp_debug_wait_timeout", "tsp_plan_create_gqa", "tsp_decode_step",
-    "tsp_plan_set_deterministic", "tsp_plan_get_deterministic",
+    "tsp_plan_set_deterministic", "tsp_plan_get_deterministic", "tsp_rank_shard_bytes", "tsp_rank_extract_shard",
+    "tsp_rank_qkv", "tsp_rank_attention", "tsp_rank_mlp",
 ]
 
 
@@ -89,6 +92,12 @@ def lib() -> ctypes.CDLL:
         L.tsp_debug_fail_next.restype = None
         L.tsp_debug_wait_timeout.argtypes = [ctypes.c_uint, vp]
         L.tsp_attention_fwd_static.argtypes = [vp, i32, vp, ctypes.POINTER(_Weights), vp, vp, vp]
+        L.tsp_rank_shard_bytes.argtypes = [vp, i32]
+        L.tsp_rank_shard_bytes.restype = sz
+        L.tsp_rank_extract_shard.argtypes = [vp, ctypes.POINTER(_Weights), i32, i32, vp, vp]
+        L.tsp_rank_qkv.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+        L.tsp_rank_attention.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.tsp_rank_mlp.argtypes = [vp, i32, vp, vp, vp, vp, vp, sz, vp]
         L.tsp_profile_enable.argtypes = [i32]
         L.tsp_profile_enable.restype = None
         L.tsp_profile_report.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
@@ -324,6 +333,36 @@ def tsp_decode_step(plan: Plan, batch: int, pos: int, x_new, weights: PackedWeig
     wp, wn = _ws_args(workspace)
     _check(lib().tsp_decode_step(plan.handle, batch, pos, _ptr(x_new), ctypes.byref(w), _ptr(k_cache), _ptr(v_cache),
                                  _ptr(y_new), wp, wn, _stream(stream)), "tsp_decode_step")
+
+
+# ---- one rank of a multi-GPU layer ------------------------------------------------
+
+def tsp_rank_shard_bytes(plan: Plan, kind: int) -> int:
+    return lib().tsp_rank_shard_bytes(plan.handle, kind)
+
+
+def tsp_rank_extract_shard(plan: Plan, packed: PackedWeights, shard: int, kind: int, out, stream=None) -> None:
+    w = packed.c()
+    _check(lib().tsp_rank_extract_shard(plan.handle, ctypes.byref(w), shard, kind, _ptr(out), _stream(stream)),
+           "tsp_rank_extract_shard")
+
+
+def tsp_rank_qkv(plan: Plan, batch: int, x_local, attn_shard, q_local, kv_local, stream=None) -> None:
+    _check(lib().tsp_rank_qkv(plan.handle, batch, _ptr(x_local), _ptr(attn_shard), _ptr(q_local), _ptr(kv_local),
+                              _stream(stream)), "tsp_rank_qkv")
+
+
+def tsp_rank_attention(plan: Plan, rank: int, batch: int, q_local, kv_all, attn_shard, resid, h_out, workspace,
+                       stream=None) -> None:
+    wp, wn = _ws_args(workspace)
+    _check(lib().tsp_rank_attention(plan.handle, rank, batch, _ptr(q_local), _ptr(kv_all), _ptr(attn_shard),
+                                    _ptr(resid), _ptr(h_out), wp, wn, _stream(stream)), "tsp_rank_attention")
+
+
+def tsp_rank_mlp(plan: Plan, batch: int, h_local, mlp_shard, resid, y_out, workspace, stream=None) -> None:
+    wp, wn = _ws_args(workspace)
+    _check(lib().tsp_rank_mlp(plan.handle, batch, _ptr(h_local), _ptr(mlp_shard), _ptr(resid), _ptr(y_out), wp, wn,
+                              _stream(stream)), "tsp_rank_mlp")
 
 
 def workspace(plan: Plan, batch: int, op: int, device="cuda") -> torch.Tensor:

@@ -101,8 +101,14 @@ typedef enum {
   TSP_OP_GATED_MLP_FWD = 1,
   TSP_OP_LAYER_FWD = 2,
   TSP_OP_LAYER_BWD = 3,
-  TSP_OP_DECODE = 4
+  TSP_OP_DECODE = 4,
+  TSP_OP_RANK_ATTENTION = 5, /* tsp_rank_attention */
+  TSP_OP_RANK_MLP = 6        /* tsp_rank_mlp */
 } tsp_op;
+
+/* The two kinds of weight shard that travel between ranks in a multi-GPU TSP
+ * layer (tsp_rank_*). */
+typedef enum { TSP_SHARD_ATTENTION = 0, TSP_SHARD_MLP = 1 } tsp_shard_kind;
 
 /* Opaque and host-only.  Configure it (tsp_plan_set_deterministic) before
  * sharing it; from then on it is read-only and safe to share between threads. */
@@ -231,6 +237,73 @@ tsp_status tsp_layer_bwd(const tsp_plan* plan, int batch, const void* x, const t
 tsp_status tsp_decode_step(const tsp_plan* plan, int batch, int64_t pos, const void* x_new,
                            const tsp_weights* weights, void* k_cache, void* v_cache, void* y_new,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- one rank of a multi-GPU TSP layer ------------------------------------ */
+/*
+ * The calls above run all D ranks of a layer on one GPU.  The calls below are
+ * ONE rank's compute steps of the same layer when each of D GPUs is a rank
+ * and holds 1/D of the tokens and 1/D of the weights (ai-trends.today TSP
+ * article, "How to Fold a Book"); the exchanges between them (broadcast of an
+ * attention shard by its owner, all-gather of K/V, the MLP ring) are the
+ * caller's, e.g. NCCL.  Every pointer is local device memory of the calling
+ * rank's GPU: a shard that came from another rank has already been received
+ * into a local buffer.  Rank r's layer, with x_r its local zigzag rows:
+ *
+ *   H_r = x_r;  for s = 0..D-1 (owner s broadcasts attention shard s):
+ *       tsp_rank_qkv(x_r, shard s)          -> q_r, kv_r
+ *       all-gather kv_r over the ranks      -> kv_all (rank order)
+ *       tsp_rank_attention(rank r, q_r, kv_all, shard s, resid = H_r) -> H_r
+ *   Y_r = H_r;  for t = 0..D-1, j = (r - t) mod D (the ring; at t = 0 the
+ *       rank's own MLP shard, then the one received from rank r-1):
+ *       tsp_rank_mlp(H_r, shard j, resid = Y_r) -> Y_r
+ *
+ * after which Y_r equals rows of rank r of tsp_layer_fwd's output (zigzag
+ * rows (r*batch + b)*2C + k) up to rounding.  There is no output all-reduce.
+ *
+ * Local layouts (L = batch * 2C local rows, row b*2C + k holding natural
+ * position pos(r, k) of sequence b; hs = h/D, ks = hk/D, fs = ffn/D):
+ *   x_r, H_r, Y_r [L][h];  q_r [L][hs];  kv_r [L][2*ks] (the shard's K
+ *   columns then its V columns);  kv_all [D][L][2*ks] (rank r' at r'*L rows).
+ * Shard layouts (one contiguous buffer each, tsp_rank_shard_bytes bytes):
+ *   attention shard s:  qkv_s [hs + 2*ks][h]  = rows of packed qkv for shard
+ *                       s (Q columns of its H/D heads, then K, then V), then
+ *                       o_s [h][hs] with o_s[n][i] = W_O[s*hs + i][n];
+ *   MLP shard j:        gu_j [2*fs][h] = rows j*2*fs .. of packed gate_up
+ *                       (its 128-column gate/up blocks), then
+ *                       down_j [h][fs] with down_j[n][i] = W_down[j*fs + i][n].
+ * Shape rules on top of the plan's: ffn/D % 128 == 0 (a shard holds whole
+ * gate/up blocks); for bf16 also hidden/D % 256 == 0 and 2*kv_hidden/D % 256
+ * == 0 (TSP_ERR_UNSUPPORTED otherwise).
+ */
+
+/* Bytes of one shard of `kind` in the layout above (0 for a NULL plan). */
+size_t tsp_rank_shard_bytes(const tsp_plan* plan, tsp_shard_kind kind);
+
+/* Writes shard `shard` (0..D-1) of `kind` from the whole packed weights into
+ * `out` (tsp_rank_shard_bytes bytes): what the rank owning that shard holds. */
+tsp_status tsp_rank_extract_shard(const tsp_plan* plan, const tsp_weights* packed, int shard, tsp_shard_kind kind,
+                                  void* out, void* stream);
+
+/* Projection of the rank's tokens by one attention shard: q_r = x_r Wq_s,
+ * kv_r = x_r [Wk_s | Wv_s] (kv_r is what the rank contributes to the K/V
+ * all-gather). */
+tsp_status tsp_rank_qkv(const tsp_plan* plan, int batch, const void* x_local, const void* attn_shard,
+                        void* q_local, void* kv_local, void* stream);
+
+/* Causal attention of rank `rank`'s queries (its H/D heads of the shard) over
+ * the gathered K/V of every rank, then h_out = resid + O_s Wo_s.  kv_all is
+ * reordered into natural positions inside the call.  resid may equal h_out
+ * (accumulation in place); resid NULL means 0.  Workspace:
+ * tsp_workspace_bytes(plan, batch, TSP_OP_RANK_ATTENTION). */
+tsp_status tsp_rank_attention(const tsp_plan* plan, int rank, int batch, const void* q_local, const void* kv_all,
+                              const void* attn_shard, const void* resid, void* h_out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* One step of the MLP ring: y_out = resid + (SiLU(H_r Wg_j) * (H_r Wu_j)) Wd_j.
+ * resid may equal y_out (in place); NULL means 0.  Workspace:
+ * tsp_workspace_bytes(plan, batch, TSP_OP_RANK_MLP). */
+tsp_status tsp_rank_mlp(const tsp_plan* plan, int batch, const void* h_local, const void* mlp_shard,
+                        const void* resid, void* y_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- status ---------------------------------------------------------------- */
 

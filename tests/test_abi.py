@@ -192,3 +192,53 @@ def test_empty_batch_is_a_no_op(tsp):
         assert L.tsp_attention_fwd_static(h, -1, None, None, None, None, None) == tsp.TSP_ERR_INVALID_ARG
     p = tsp.tsp_plan_create(2, 256, 256, 2, 128, 512, "bf16")
     assert L.tsp_decode_step(p.handle, 0, 0, None, None, None, None, None, None, 0, None) == tsp.TSP_ERR_INVALID_ARG
+
+
+def test_rank_shard_sizes_and_validation(tsp):
+    """Shard sizes follow the documented layouts; bad ranks, shards, shapes and workspaces are refused
+    on the host before anything is enqueued."""
+    D, S, h, H, dh, F = 8, 16384, 4096, 32, 128, 14336
+    p = tsp.tsp_plan_create(D, S, h, H, dh, F, "bf16")
+    hs, fs = h // D, F // D
+    assert tsp.tsp_rank_shard_bytes(p, tsp.TSP_SHARD_ATTENTION) == ((hs + 2 * hs) * h + h * hs) * 2
+    assert tsp.tsp_rank_shard_bytes(p, tsp.TSP_SHARD_MLP) == (2 * fs * h + h * fs) * 2
+    assert tsp.lib().tsp_rank_shard_bytes(None, 0) == 0
+    g = tsp.tsp_plan_create_gqa(D, S, h, H, 8, dh, F, "bf16")
+    assert tsp.tsp_rank_shard_bytes(g, tsp.TSP_SHARD_ATTENTION) == ((hs + 2 * 128) * h + h * hs) * 2
+    # workspaces: K, V, V^T of the shard's heads over the whole sequence, and the rank's attention output
+    B = 2
+    L = B * S // D
+    assert tsp.tsp_workspace_bytes(p, B, tsp.TSP_OP_RANK_ATTENTION) >= (3 * B * S * hs + L * hs) * 2
+    assert tsp.tsp_workspace_bytes(p, B, tsp.TSP_OP_RANK_MLP) >= L * fs * 2
+    w = tsp._Weights(0x1000, 0x2000, 0x3000, 0x4000)
+    L_ = tsp.lib()
+    big = 1 << 40
+    ws_ok = tsp.tsp_workspace_bytes(p, B, tsp.TSP_OP_RANK_ATTENTION)
+    cases = [
+        (L_.tsp_rank_attention(p.handle, D, B, 0x1000, 0x2000, 0x3000, None, 0x4000, 0x5000, big, None),
+         tsp.TSP_ERR_INVALID_ARG),  # rank == D
+        (L_.tsp_rank_attention(p.handle, -1, B, 0x1000, 0x2000, 0x3000, None, 0x4000, 0x5000, big, None),
+         tsp.TSP_ERR_INVALID_ARG),
+        (L_.tsp_rank_attention(p.handle, 0, B, 0x1000, 0x2000, 0x3000, None, 0x4000, 0x5000, ws_ok - 1, None),
+         tsp.TSP_ERR_WORKSPACE),
+        (L_.tsp_rank_attention(p.handle, 0, B, 0x1000, 0x2000, 0x3000, 0x3008, 0x4000, 0x5000, big, None),
+         tsp.TSP_ERR_INVALID_ARG),  # misaligned resid
+        (L_.tsp_rank_qkv(p.handle, B, 0x1000, None, 0x2000, 0x3000, None), tsp.TSP_ERR_INVALID_ARG),
+        (L_.tsp_rank_mlp(p.handle, B, 0x1000, 0x2000, None, 0x3000, 0x4000, 0, None), tsp.TSP_ERR_WORKSPACE),
+        (L_.tsp_rank_extract_shard(p.handle, ctypes.byref(w), D, 0, 0x5000, None), tsp.TSP_ERR_INVALID_ARG),
+        (L_.tsp_rank_extract_shard(p.handle, ctypes.byref(w), 0, 7, 0x5000, None), tsp.TSP_ERR_INVALID_ARG),
+    ]
+    for got, want in cases:
+        assert got == want, (got, want, tsp.tsp_last_error_message())
+    # a shard must hold whole 128-column gate/up blocks: ffn / D = 1152 / 8 = 144
+    odd = tsp.tsp_plan_create(8, 2048, 2048, 16, 128, 1152, "bf16")
+    st = L_.tsp_rank_mlp(odd.handle, 1, 0x1000, 0x2000, None, 0x3000, 0x4000, big, None)
+    assert st == tsp.TSP_ERR_UNSUPPORTED and "128" in tsp.tsp_last_error_message()
+    # bf16 needs hidden / D % 256 == 0 (2048 / 16 = 128)
+    narrow = tsp.tsp_plan_create(16, 4096, 2048, 16, 128, 4096, "bf16")
+    st = L_.tsp_rank_qkv(narrow.handle, 1, 0x1000, 0x2000, 0x3000, 0x4000, None)
+    assert st == tsp.TSP_ERR_UNSUPPORTED
+    # an empty batch is a no-op that reads no pointer
+    assert L_.tsp_rank_qkv(p.handle, 0, None, None, None, None, None) == tsp.TSP_OK
+    assert L_.tsp_rank_attention(p.handle, 0, 0, None, None, None, None, None, None, 0, None) == tsp.TSP_OK
+    assert L_.tsp_rank_mlp(p.handle, 0, None, None, None, None, None, 0, None) == tsp.TSP_OK
