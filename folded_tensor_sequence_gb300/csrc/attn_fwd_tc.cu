@@ -9,11 +9,15 @@
 // softmax as in FlashAttention / ring attention (r007 chapter, "Параллелизм по
 // контексту: Ring Attention против Ulysses").
 //
-// Work unit: a 256-query block (two 128-row tiles A and B) of one (batch,
-// head).  Block G needs key tiles 0..2G+1 (tile A stops one earlier); only
-// each tile's last key tile crosses the diagonal and is masked.  A CTA takes
-// the mirror pair of blocks (G, 2D*nb-1-G), which lie in chunks c and 2D-1-c
-// of the same rank, so every CTA does the same number of key tiles.
+// Work unit: a block of two 128-row query tiles A and B of one (batch,
+// head); only each tile's last key tile crosses the diagonal and is masked.
+// Chunks of whole 256-query blocks: a block is 256 consecutive queries (tile
+// A stops one key tile before B), and a CTA takes the mirror pair of blocks
+// (G, 2D*nb-1-G), which lie in chunks c and 2D-1-c of the same rank.  Chunks
+// of an odd number of 128-query tiles: a CTA's one block is the mirror pair
+// of tiles itself (tile A the light one in chunk c, tile B the heavy one in
+// chunk 2D-1-c); A runs out of key tiles first and B finishes alone.  Either
+// way every CTA does the same number of key tiles.
 //
 // Per CTA: warp 8 issues TMA loads (a block's Q tiles, then K_j / V_j^T tiles
 // through a 5-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
@@ -53,7 +57,8 @@ constexpr int kBarPA = 1, kBarPB = 3;
 constexpr int kHandoffThreads = 128 + 32;
 
 struct FaParams {
-  int B, H, D, nb;  // nb = 256-query blocks per chunk
+  int B, H, D, nb;  // nb = blocks per chunk: 256-query blocks (nblk 2) or 128-query tiles (nblk 1)
+  int nblk;         // blocks per CTA: 2 (a mirror pair of 256-query blocks) or 1 (a mirror pair of tiles)
   int Hk;           // K/V heads; query head `head` reads K/V head head / (H / Hk)
   int64_t S, C;
   int h;
@@ -130,19 +135,35 @@ __device__ __forceinline__ void exp_pack_quarter(const uint32_t (&h)[32], uint32
 }
 
 struct BlockGeo {
-  int64_t zrow0;  // zigzag row of the block's first query
-  int64_t p0;     // global position of the block's first query
-  int nB;         // key tiles for tile B (tile A uses nB - 1)
+  int64_t zrow[2];  // row of Q / O holding tile x's first query
+  int64_t p0[2];    // global position of tile x's first query
+  int n[2];         // key tiles of tile x (the last one is its diagonal tile)
 };
 
-__device__ __forceinline__ BlockGeo block_geo(int G, const FaParams& p, int b) {
-  const int c = G / p.nb, i = G % p.nb;
+// Zigzag row and position of the 128-query tile starting `off` queries into chunk c.
+__device__ __forceinline__ void tile_at(int c, int64_t off, const FaParams& p, int b, int64_t& zrow, int64_t& p0) {
   const int64_t r = c < p.D ? c : 2 * p.D - 1 - c;
-  const int64_t k0 = (c < p.D ? 0 : p.C) + (int64_t)i * 2 * QT;
+  zrow = (r * p.B + b) * 2 * p.C + (c < p.D ? 0 : p.C) + off - p.row_off;
+  p0 = (int64_t)c * p.C + off;
+}
+
+// blk: the CTA's block index (0: heavy, 1: light when nblk == 2).
+__device__ __forceinline__ BlockGeo block_geo(int blk, int light, const FaParams& p, int b) {
   BlockGeo g;
-  g.zrow0 = (r * p.B + b) * 2 * p.C + k0 - p.row_off;
-  g.p0 = (int64_t)c * p.C + (int64_t)i * 2 * QT;
-  g.nB = (int)(g.p0 / KT) + 2;
+  const int total = 2 * p.D * p.nb;
+  if (p.nblk == 2) {
+    const int G = blk == 0 ? total - 1 - light : light;
+    const int c = G / p.nb, i = G % p.nb;
+    tile_at(c, (int64_t)i * 2 * QT, p, b, g.zrow[0], g.p0[0]);
+    g.zrow[1] = g.zrow[0] + QT;
+    g.p0[1] = g.p0[0] + QT;
+  } else {
+    const int GH = total - 1 - light;  // tile B: the heavy mirror of the light tile A
+    tile_at(light / p.nb, (int64_t)(light % p.nb) * QT, p, b, g.zrow[0], g.p0[0]);
+    tile_at(GH / p.nb, (int64_t)(GH % p.nb) * QT, p, b, g.zrow[1], g.p0[1]);
+  }
+  g.n[0] = (int)(g.p0[0] / KT) + 1;
+  g.n[1] = (int)(g.p0[1] / KT) + 1;
   return g;
 }
 
@@ -166,10 +187,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int head = blockIdx.y, b = blockIdx.z;
-  const int total_blocks = 2 * p.D * p.nb;
-  // the CTA's two blocks: heavy (late in the sequence) first, then its mirror
+  // light block (or tile) of the CTA's mirror pair; with two blocks the heavy one goes first
   const int light = p.g_off + (int)blockIdx.x;
-  auto blk_id = [&](int blk) { return blk == 0 ? total_blocks - 1 - light : light; };
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full[0], 1);
@@ -211,17 +230,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t item = 0;
       bool ok = true;
       int q_loaded = 0;
-      for (int blk = 0; blk < 2 && ok; ++blk) {
-        const BlockGeo g = block_geo(blk_id(blk), p, b);
+      for (int blk = 0; blk < p.nblk && ok; ++blk) {
+        const BlockGeo g = block_geo(blk, light, p, b);
         // block 1's query tiles go into block 0's buffer once its last S MMA is done
         if (blk == 1 && !mbar_wait(q_empty, 0, abort_flag, p.err, code | 1)) break;
         mbar_arrive_expect_tx(&q_full[blk], 2 * TILE_BYTES);
         ++q_loaded;
         for (int x = 0; x < 2; ++x)
           for (int c = 0; c < 2; ++c)
-            tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)(g.zrow0 + x * QT),
-                        &q_full[blk]);
-        for (int j = 0; j < g.nB && ok; ++j) {
+            tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)g.zrow[x], &q_full[blk]);
+        for (int j = 0; j < g.n[1] && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++item) {
             const int s = item % STAGES;
             if (!mbar_wait(&kv_empty[s], ((item / STAGES) & 1) ^ 1, abort_flag, p.err, code | 2)) {
@@ -273,9 +291,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         umma_bf16_ts_warp(tmem_base + 256 + x * 128, tmem_base + x * 128 + 8 * k, bb, idesc, (acc || k > 0) ? 1u : 0u);
       }
     };
-    for (int blk = 0; blk < 2; ++blk) {
-      const BlockGeo g = block_geo(blk_id(blk), p, b);
-      const int nB = g.nB, nA = g.nB - 1;
+    for (int blk = 0; blk < p.nblk; ++blk) {
+      const BlockGeo g = block_geo(blk, light, p, b);
+      const int nB = g.n[1], nA = g.n[0];  // tile A never has more key tiles than tile B
       const uint32_t base = item;  // K_j = base + 2j, V_j = base + 2j + 1
       if (ok) {
         bool w = true;
@@ -325,7 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       item = base + 2 * nB;
       // the Q buffer is free for block 1 once every MMA issued so far is done
-      if (blk == 0 && ok) umma_commit_warp(q_empty);
+      if (blk == 0 && p.nblk == 2 && ok) umma_commit_warp(q_empty);
     }
     umma_commit_warp(drain);
     if (lane == 0) {
@@ -346,11 +364,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t item = 0;  // the producer's K/V item numbering
     bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
     const bool checker = quad == 0 && lane == 0;
-    for (int blk = 0; blk < 2; ++blk) {
-      const BlockGeo g = block_geo(blk_id(blk), p, b);
-      const int n = g.nB - 1 + x;
+    for (int blk = 0; blk < p.nblk; ++blk) {
+      const BlockGeo g = block_geo(blk, light, p, b);
+      const int n = x ? g.n[1] : g.n[0];  // selects, not a runtime index into the struct's arrays
       const uint32_t base = item;
-      item = base + 2 * g.nB;
+      item = base + 2 * g.n[1];
       float m_used = -INFINITY, l = 0.f;
       // Hands P_x(j) to the MMA warp.  Its next MMAs read V_j and, if this
       // tile has another key tile, K_{j+1}: one thread checks that both have
@@ -473,7 +491,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t orr[128];
       tmem_ld128(tO, orr);
       const float inv = 1.0f / l;
-      const int64_t zrow = g.zrow0 + x * QT + row;
+      const int64_t zrow = (x ? g.zrow[1] : g.zrow[0]) + row;
       uint4* dst = reinterpret_cast<uint4*>(p.o + zrow * p.h + head * HD);
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
@@ -482,7 +500,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             pack_bf16x2(__uint_as_float(orr[q * 8 + 4]) * inv, __uint_as_float(orr[q * 8 + 5]) * inv),
                             pack_bf16x2(__uint_as_float(orr[q * 8 + 6]) * inv, __uint_as_float(orr[q * 8 + 7]) * inv));
       }
-      if (p.lse) p.lse[((int64_t)b * p.H + head) * p.S + g.p0 + x * QT + row] = (m_used + __log2f(l)) * kLn2;
+      if (p.lse)
+        p.lse[((int64_t)b * p.H + head) * p.S + (x ? g.p0[1] : g.p0[0]) + row] = (m_used + __log2f(l)) * kLn2;
       tc_fence_before();
     }
   }
@@ -497,7 +516,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-bool attn_tc_supported(int head_dim, int64_t chunk) { return head_dim == HD && chunk % (2 * QT) == 0; }
+bool attn_tc_supported(int head_dim, int64_t chunk) { return head_dim == HD && chunk % QT == 0; }
 
 tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   if (!attn_tc_supported(a.dh, a.C)) return TSP_ERR_UNSUPPORTED;
@@ -522,7 +541,8 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   p.H = a.H;
   p.Hk = a.Hk;
   p.D = a.D;
-  p.nb = (int)(a.C / (2 * QT));
+  p.nblk = a.C % (2 * QT) == 0 ? 2 : 1;
+  p.nb = (int)(a.C / (p.nblk * QT));
   p.S = a.S;
   p.C = a.C;
   p.h = h;

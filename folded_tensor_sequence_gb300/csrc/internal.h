@@ -120,7 +120,7 @@ struct AttnParams {
 };
 tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream);
 tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream);
-// tcgen05 attention (V given transposed, [B][Hk][dh][S]); needs head_dim 128 and chunk % 256 == 0.
+// tcgen05 attention (V given transposed, [B][Hk][dh][S]); needs head_dim 128 and chunk % 128 == 0.
 bool attn_tc_supported(int head_dim, int64_t chunk);
 tsp_status attn_fwd_bf16_tc(const AttnParams& p, cudaStream_t stream);
 

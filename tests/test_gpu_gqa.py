@@ -73,6 +73,9 @@ FWD = [
                 dtype="bf16", kv_heads=2),
     LayerConfig("gqa_bf16_D1_s1024_mqa", D=1, batch=1, seq=1024, hidden=512, heads=4, head_dim=128, ffn=512,
                 dtype="bf16", kv_heads=1),
+    # chunks of 128: the tcgen05 forward on mirror pairs of 128-query tiles
+    LayerConfig("gqa_bf16_D4_s1024_c128", D=4, batch=1, seq=1024, hidden=1024, heads=8, head_dim=128, ffn=1024,
+                dtype="bf16", kv_heads=4),
 ]
 
 

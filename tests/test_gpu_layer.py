@@ -110,8 +110,11 @@ SMALL_BF16 = [
     LayerConfig("bf16_D2_s320", D=2, batch=1, seq=320, hidden=256, heads=2, head_dim=128, ffn=512, dtype="bf16"),
     # several tiles in every GEMM dimension, two batches
     LayerConfig("bf16_D4_b2_s1024", D=4, batch=2, seq=1024, hidden=512, heads=4, head_dim=128, ffn=768, dtype="bf16"),
-    # D = 8 with one head per shard
+    # D = 8 with one head per shard; chunks of 128 queries: the tcgen05 attention on mirror pairs of 128-query tiles
     LayerConfig("bf16_D8_s2048", D=8, batch=1, seq=2048, hidden=1024, heads=8, head_dim=128, ffn=1024, dtype="bf16"),
+    # chunks of 384 queries (three 128-query tiles): tcgen05 attention, tile mirror pairs, two sequences
+    LayerConfig("bf16_D2_b2_s1536", D=2, batch=2, seq=1536, hidden=512, heads=4, head_dim=128, ffn=512,
+                dtype="bf16"),
     # odd D, chunk not a multiple of the 128-row query tile
     LayerConfig("bf16_D3_s1152", D=3, batch=1, seq=1152, hidden=768, heads=6, head_dim=128, ffn=1536, dtype="bf16"),
     # chunks of 256 and 512 queries: the tcgen05 attention kernel (256-query blocks)
