@@ -136,3 +136,19 @@ def test_traffic_table_names_existing_sources_and_steps():
         assert os.path.exists(os.path.join(ROOT, path))
         assert (step in bench.step_work(BY_NAME[workload])
                 or step.removesuffix(" (standalone)") in bench.LAYOUT_STEPS), step
+
+
+def test_nominal_peak_is_the_clock_derived_tensor_rate():
+    # 8192 flops per SM cycle (one 128 x 256 x 16 bf16 MMA every 128 cycles) x 152 SMs x clock
+    assert bench.nominal_bf16_tflops(152, 2070.0) == pytest.approx(8192 * 152 * 2.07e9 / 1e12)
+    assert bench.nominal_bf16_tflops(152, 2070.0) == pytest.approx(2577.5, abs=0.1)
+    # at about 1.8 GHz it is the 2.25 PFLOP/s nominal figure
+    assert bench.nominal_bf16_tflops(152, 1807.0) == pytest.approx(2250.0, rel=1e-3)
+    assert bench.nominal_bf16_tflops(152, None) is None
+
+
+def test_host_description_names_cpus_and_model():
+    h = bench.host_cpu()
+    assert h["nproc"] == os.cpu_count() and h["nproc"] >= 1
+    assert isinstance(h["cpu_model"], str) and h["cpu_model"]
+    assert h["machine"]
