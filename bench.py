@@ -54,9 +54,9 @@ NCU_TRAFFIC = {
     ("gate/up projection", "bf16_D4_s4096_h2048"):
         (62.96e6 + 16.29e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "1c44a2a1014d92e7"),
     ("attention", "bf16_D8_b2_s16384_h4096"):
-        (0.844e9 + 0.248e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
+        (849.534e6 + 254.581e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "f3ebf6c44e68df52"),
     ("attention", "bf16_D8_b1_s65536_h4096"):
-        (2.19e9 + 0.5294e9, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "d9e4078a1ead8069"),
+        (2152.43e6 + 536.669e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "f3ebf6c44e68df52"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
         (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b1_s8192_h4096"):
