@@ -399,7 +399,7 @@ tsp_status check_rank_shapes(const tsp_plan* p, const char* what) {
 }
 
 struct RankAttnLayout {
-  size_t k, v, vt, o, end;
+  size_t k, v, vt, o, split, end;  // split: parts of the attention kernel's key split (tcgen05 path)
 };
 
 RankAttnLayout rank_attn_layout(const tsp_plan* p, int batch) {
@@ -416,6 +416,7 @@ RankAttnLayout rank_attn_layout(const tsp_plan* p, int batch) {
   L.v = take(kvb);
   L.vt = use_tc_attention(p) ? take(kvb) : L.v;
   L.o = take((size_t)d.L * d.hs * e);
+  L.split = use_tc_attention(p) ? take(attn_tc_split_bytes(d.L, p->heads / p->D)) : L.o;
   L.end = o;
   return L;
 }
@@ -1092,6 +1093,10 @@ tsp_status tsp_rank_attention(const tsp_plan* p, int rank, int batch, const void
   ap.S = p->seq;
   ap.C = p->chunk;
   ap.rank = rank;
+  if (tc) {  // one rank's queries of one shard rarely fill the GPU: room for the key split
+    ap.split_ws = wb + W.split;
+    ap.split_ws_bytes = W.end - W.split;
+  }
   {
     Prof pr("rank attention", st);
     s = p->dtype != TSP_BF16 ? attn_fwd_f32(ap, st) : (tc ? attn_fwd_bf16_tc(ap, st) : attn_fwd_bf16(ap, st));

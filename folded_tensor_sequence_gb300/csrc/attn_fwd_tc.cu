@@ -64,6 +64,15 @@ struct FaParams {
   int h;
   int g_off;        // first light block of the grid (rank * nb when one rank's queries run)
   int64_t row_off;  // zigzag row held by row 0 of Q and O (rank * B * 2C likewise)
+  // Key split: nsplit CTAs share a mirror pair, part sp taking key tiles
+  // [n*sp/nsplit, n*(sp+1)/nsplit) of each block (n = the block's tile-B key
+  // tiles), and write unnormalised O and (max, sum) per row to part_o /
+  // part_ml ([nsplit][rows of Q][H][...]) for attn_combine_kernel; nsplit 1
+  // writes O and lse directly.
+  int nsplit;
+  int64_t part_rows;
+  float* part_o;
+  float2* part_ml;
   __nv_bfloat16* o;
   float* lse;
   unsigned int* err;
@@ -167,6 +176,9 @@ __device__ __forceinline__ BlockGeo block_geo(int blk, int light, const FaParams
   return g;
 }
 
+// SPLIT: the key-split instantiation (parts written for attn_combine_kernel);
+// without it the kernel takes every key tile and writes O and lse itself.
+template <bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmVt, const FaParams p) {
@@ -188,7 +200,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int head = blockIdx.y, b = blockIdx.z;
   // light block (or tile) of the CTA's mirror pair; with two blocks the heavy one goes first
-  const int light = p.g_off + (int)blockIdx.x;
+  const int nsplit = SPLIT ? p.nsplit : 1;
+  const int light = p.g_off + (int)blockIdx.x / nsplit;
+  const int sp = SPLIT ? (int)blockIdx.x % nsplit : 0;  // part of the key range (key split)
+  // key tiles [lo, hiB) of this part of a block; tile A takes [lo, hiA), empty if hiA <= lo
+  auto key_part = [&](const BlockGeo& g, int& lo, int& hiA, int& hiB) {
+    if constexpr (SPLIT) {
+      lo = (int)((int64_t)g.n[1] * sp / nsplit);
+      hiB = (int)((int64_t)g.n[1] * (sp + 1) / nsplit);
+      hiA = g.n[0] < hiB ? g.n[0] : hiB;
+    } else {
+      lo = 0;
+      hiB = g.n[1];
+      hiA = g.n[0];
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full[0], 1);
@@ -239,7 +265,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int x = 0; x < 2; ++x)
           for (int c = 0; c < 2; ++c)
             tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)g.zrow[x], &q_full[blk]);
-        for (int j = 0; j < g.n[1] && ok; ++j) {
+        int lo, hiA, hiB;
+        key_part(g, lo, hiA, hiB);
+        for (int j = lo; j < hiB && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++item) {
             const int s = item % STAGES;
             if (!mbar_wait(&kv_empty[s], ((item / STAGES) & 1) ^ 1, abort_flag, p.err, code | 2)) {
@@ -293,31 +321,35 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     for (int blk = 0; blk < p.nblk; ++blk) {
       const BlockGeo g = block_geo(blk, light, p, b);
-      const int nB = g.n[1], nA = g.n[0];  // tile A never has more key tiles than tile B
-      const uint32_t base = item;  // K_j = base + 2j, V_j = base + 2j + 1
+      int lo, nA, nB;  // this part's key tiles: [lo, nB) for tile B, [lo, nA) for tile A (possibly none)
+      key_part(g, lo, nA, nB);
+      const bool actA = lo < nA;
+      const uint32_t base = item - 2 * lo;  // K_j = base + 2j, V_j = base + 2j + 1
       if (ok) {
         bool w = true;
         if (lane == 0)
           w = mbar_wait(&q_full[blk], 0, abort_flag, p.err, code | 6) &&
-              mbar_wait(&kv_full[base % STAGES], (base / STAGES) & 1, abort_flag, p.err, code | 4);
+              mbar_wait(&kv_full[item % STAGES], (item / STAGES) & 1, abort_flag, p.err, code | 4);
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       }
       tc_fence_after();
       if (ok) {
-        mma_s(0, base % STAGES);
-        umma_commit_warp(&s_full[0]);
-        mma_s(1, base % STAGES);
+        if (actA) {
+          mma_s(0, item % STAGES);
+          umma_commit_warp(&s_full[0]);
+        }
+        mma_s(1, item % STAGES);
         umma_commit_warp(&s_full[1]);
-        umma_commit_warp(&kv_empty[base % STAGES]);
+        umma_commit_warp(&kv_empty[item % STAGES]);
       }
-      for (int j = 0; j < nB; ++j) {
+      for (int j = lo; j < nB; ++j) {
         const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
         if (j < nA) {
           __syncwarp();
           named_bar_sync(kBarPA + (j & 1), kHandoffThreads);
           tc_fence_after();
           if (ok) {
-            mma_pv(0, iv % STAGES, j > 0);
+            mma_pv(0, iv % STAGES, j > lo);
             if (j + 1 < nA) {
               mma_s(0, ik % STAGES);
               umma_commit_warp(&s_full[0]);
@@ -330,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         named_bar_sync(kBarPB + (j & 1), kHandoffThreads);
         tc_fence_after();
         if (ok) {
-          mma_pv(1, iv % STAGES, j > 0);
+          mma_pv(1, iv % STAGES, j > lo);
           umma_commit_warp(&kv_empty[iv % STAGES]);
           if (j + 1 < nB) {
             mma_s(1, ik % STAGES);
@@ -361,14 +393,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tO = tmem_base + lane_off + 256 + x * 128;
     const float sl2 = kLog2e * rsqrtf((float)HD);
     uint32_t scnt = 0;
+    uint32_t ocnt = 0;  // completed phases of o_done[x] (a tile with no key tile in its part has none)
     uint32_t item = 0;  // the producer's K/V item numbering
     bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
     const bool checker = quad == 0 && lane == 0;
     for (int blk = 0; blk < p.nblk; ++blk) {
       const BlockGeo g = block_geo(blk, light, p, b);
       const int n = x ? g.n[1] : g.n[0];  // selects, not a runtime index into the struct's arrays
-      const uint32_t base = item;
-      item = base + 2 * g.n[1];
+      int lo, hiA, hiB;
+      key_part(g, lo, hiA, hiB);
+      const int hi = x ? hiB : hiA;  // this tile's key tiles in this part: [lo, hi)
+      const uint32_t base = item - 2 * lo;
+      item = item + 2 * (hiB - lo);
       float m_used = -INFINITY, l = 0.f;
       // Hands P_x(j) to the MMA warp.  Its next MMAs read V_j and, if this
       // tile has another key tile, K_{j+1}: one thread checks that both have
@@ -380,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto hand_off = [&](int jj) {
         if (checker && alive) {
           const uint32_t iv = base + 2 * jj + 1;
-          if (mbar_wait(&kv_full[iv % STAGES], (iv / STAGES) & 1, abort_flag, p.err, code | 10) && jj + 1 < n)
+          if (mbar_wait(&kv_full[iv % STAGES], (iv / STAGES) & 1, abort_flag, p.err, code | 10) && jj + 1 < hi)
             mbar_wait(&kv_full[(iv + 1) % STAGES], ((iv + 1) / STAGES) & 1, abort_flag, p.err, code | 10);
         }
         __syncwarp();
@@ -389,7 +425,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         else
           named_bar_sync((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoffThreads);
       };
-      for (int j = 0; j < n; ++j) {
+      for (int j = lo; j < hi; ++j) {
         const bool got = alive && mbar_wait(&s_full[x], scnt & 1, abort_flag, p.err, code | 8);
         ++scnt;
         alive = __all_sync(0xffffffffu, got);
@@ -408,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // (speculation); only if this tile raises the max by more than the
         // threshold are O rescaled and P recomputed from S (still in TMEM).
         uint32_t pk[64];
-        if (j == 0) {  // first key tile of the block: the max has to come first
+        if (j == lo) {  // first key tile of the block (or its part): the max has to come first
           float mx = -INFINITY;
 #pragma unroll 1
           for (int k = 0; k < 4; ++k) {
@@ -456,7 +492,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           again = __any_sync(0xffffffffu, need);
           if (again) {
             const float factor = need ? ex2f(m_used - m_new) : 1.0f;
-            if (j > 0) {
+            if (j > lo) {
 #pragma unroll 1
               for (int c4 = 0; c4 < 4; ++c4) {
                 float ov[32];
@@ -484,14 +520,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         hand_off(j);
       }
       if (!alive) continue;
-      const bool got = mbar_wait(&o_done[x], blk & 1, abort_flag, p.err, code | 9);
+      const int64_t zrow = (x ? g.zrow[1] : g.zrow[0]) + row;
+      if constexpr (SPLIT) {
+        // unnormalised O and (max, sum) of this part; a tile with no key tile in it adds nothing
+        float4* po = reinterpret_cast<float4*>(p.part_o + (((int64_t)sp * p.part_rows + zrow) * p.H + head) * HD);
+        const int64_t mli = ((int64_t)sp * p.part_rows + zrow) * p.H + head;
+        if (lo >= hi) {
+#pragma unroll 4
+          for (int q = 0; q < HD / 4; ++q) po[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.part_ml[mli] = make_float2(-INFINITY, 0.f);
+          continue;
+        }
+        const bool got = mbar_wait(&o_done[x], ocnt & 1, abort_flag, p.err, code | 9);
+        ++ocnt;
+        alive = __all_sync(0xffffffffu, got);
+        if (!alive) continue;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float ov[32];
+          tmem_ld32(tO + c4 * 32, ov);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) po[c4 * 8 + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+        }
+        p.part_ml[mli] = make_float2(m_used, l);
+        tc_fence_before();
+        continue;
+      }
+      const bool got = mbar_wait(&o_done[x], ocnt & 1, abort_flag, p.err, code | 9);
+      ++ocnt;
       alive = __all_sync(0xffffffffu, got);
       if (!alive) continue;
       tc_fence_after();
       uint32_t orr[128];
       tmem_ld128(tO, orr);
       const float inv = 1.0f / l;
-      const int64_t zrow = (x ? g.zrow[1] : g.zrow[0]) + row;
       uint4* dst = reinterpret_cast<uint4*>(p.o + zrow * p.h + head * HD);
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
@@ -514,9 +577,43 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Merges the key-split parts: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s with
+// M = max_s m_s (m in log2 units), one warp per (row, head), four head dims per lane.
+__global__ void attn_combine_kernel(const float4* __restrict__ part_o, const float2* __restrict__ part_ml, int nsplit,
+                                    int64_t rows, int H, __nv_bfloat16* __restrict__ o, int h) {
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (w >= rows * H) return;
+  const int64_t row = w / H;
+  const int head = (int)(w - row * H);
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_ml[s * rows * H + w].x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < nsplit; ++s) {
+    const float2 ml = part_ml[s * rows * H + w];
+    const float f = ex2f(ml.x - M);  // 0 for a part with no key tile (m = -inf)
+    L += f * ml.y;
+    const float4 v = part_o[(s * rows * H + w) * (HD / 4) + lane];
+    acc.x += f * v.x;
+    acc.y += f * v.y;
+    acc.z += f * v.z;
+    acc.w += f * v.w;
+  }
+  const float inv = 1.0f / L;
+  uint2 out;
+  out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(o + row * h + head * HD + 4 * lane) = out;
+}
+
 }  // namespace
 
 bool attn_tc_supported(int head_dim, int64_t chunk) { return head_dim == HD && chunk % QT == 0; }
+
+size_t attn_tc_split_bytes(int64_t rows, int H) {
+  return 2 * (size_t)rows * H * HD * sizeof(float) + 2 * (size_t)rows * H * sizeof(float2) + 256;
+}
 
 tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   if (!attn_tc_supported(a.dh, a.C)) return TSP_ERR_UNSUPPORTED;
@@ -531,8 +628,10 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
     return TSP_ERR_CUDA;
   static std::atomic<unsigned long long> configured{0};  // devices set up
   if (needs_setup(configured)) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
       return TSP_ERR_CUDA;
     mark_setup_done(configured);
   }
@@ -551,9 +650,32 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
   p.err = dev_error_word();
   p.g_off = a.rank < 0 ? 0 : a.rank * p.nb;
   p.row_off = a.rank < 0 ? 0 : (int64_t)a.rank * a.B * 2 * a.C;
-  dim3 grid(a.rank < 0 ? a.D * p.nb : p.nb, a.H, a.B);
-  attn_fwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
+  const int pairs = a.rank < 0 ? a.D * p.nb : p.nb;
+  // A grid under one wave (one rank's queries of one weight shard) splits every
+  // CTA's key range in two when the caller gave room for the parts (no lse then).
+  p.nsplit = 1;
+  p.part_rows = T;
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
+  if (a.split_ws && !a.lse && a.split_ws_bytes >= attn_tc_split_bytes(T, a.H) &&
+      (int64_t)pairs * a.H * a.B < num_sms()) {
+    p.nsplit = 2;
+    p.part_o = static_cast<float*>(a.split_ws);
+    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(a.split_ws) + 2 * (size_t)T * a.H * HD * sizeof(float));
+  }
+  dim3 grid(pairs * p.nsplit, a.H, a.B);
+  if (p.nsplit > 1)
+    attn_fwd_tc_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  else
+    attn_fwd_tc_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
+  if (p.nsplit > 1) {
+    const int64_t warps = T * a.H;
+    attn_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(p.part_o), p.part_ml, p.nsplit, T, a.H, p.o, h);
+    if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
+  }
+  return TSP_OK;
 }
 
 }  // namespace tsp

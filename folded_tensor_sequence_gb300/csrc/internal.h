@@ -117,12 +117,18 @@ struct AttnParams {
   // -1: the queries of every rank.  r >= 0: only rank r's queries; q and o
   // then hold just that rank's zigzag rows ([B][2C][H*dh], row b*2C + k).
   int rank = -1;
+  // Optional scratch for the tcgen05 kernel's key split (attn_tc_split_bytes):
+  // used, with lse NULL, when the grid would not fill the GPU once.
+  void* split_ws = nullptr;
+  size_t split_ws_bytes = 0;
 };
 tsp_status attn_fwd_bf16(const AttnParams& p, cudaStream_t stream);
 tsp_status attn_fwd_f32(const AttnParams& p, cudaStream_t stream);
 // tcgen05 attention (V given transposed, [B][Hk][dh][S]); needs head_dim 128 and chunk % 128 == 0.
 bool attn_tc_supported(int head_dim, int64_t chunk);
 tsp_status attn_fwd_bf16_tc(const AttnParams& p, cudaStream_t stream);
+// Scratch bytes of the tcgen05 kernel's two-way key split for `rows` query rows of H heads.
+size_t attn_tc_split_bytes(int64_t rows, int H);
 
 struct AttnBwdParams {
   const void* q;   // zigzag [T][h]
