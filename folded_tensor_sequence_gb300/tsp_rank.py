@@ -194,13 +194,21 @@ class DistComm:
         return self.dist.get_global_rank(self.group, r) if self.group is not None else r
 
     def check_peers(self, what: str):
-        """Raises TspError(TSP_ERR_TIMEOUT) if another rank has given up."""
-        if self.store.check([ABORT_KEY]):
-            who = self.store.get(ABORT_KEY).decode(errors="replace")
+        """Raises TspError(TSP_ERR_TIMEOUT) if another rank has given up (or
+        the store that would say so cannot be reached)."""
+        try:
+            gone = self.store.check([ABORT_KEY])
+            who = self.store.get(ABORT_KEY).decode(errors="replace") if gone else None
+        except RuntimeError as e:  # the store's host is gone: so is the group
+            raise TspError(TSP_ERR_TIMEOUT, what, f"store unreachable ({str(e).splitlines()[0][:120]})") from e
+        if gone:
             raise TspError(TSP_ERR_TIMEOUT, what, f"rank {who} gave up; not starting the exchange")
 
     def give_up(self, what: str, detail: str):
-        self.store.set(ABORT_KEY, str(self.rank))
+        try:
+            self.store.set(ABORT_KEY, str(self.rank))
+        except RuntimeError:
+            pass  # the others then find out from their own bounded waits
         raise TspError(TSP_ERR_TIMEOUT, what, f"rank {self.rank}: wait gave up ({detail.splitlines()[0][:160]})")
 
     def broadcast(self, buf, src: int):

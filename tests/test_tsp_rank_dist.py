@@ -198,3 +198,31 @@ def test_dropped_ring_message_times_out_on_every_rank():
         if out[r]["status"] == 0:
             assert out[r]["err"] <= 1e-12, out[r]
     assert codes == [0] * world
+
+
+class _DeadStore:
+    """A store whose host is gone: every call fails as a lost connection does."""
+
+    def check(self, keys):
+        raise RuntimeError("Connection reset by peer")
+
+    def get(self, key):
+        raise RuntimeError("Connection reset by peer")
+
+    def set(self, key, value):
+        raise RuntimeError("Broken pipe")
+
+
+def test_unreachable_store_reads_as_a_timeout():
+    from folded_tensor_sequence_gb300.tsp import TSP_ERR_TIMEOUT, TspError
+    from folded_tensor_sequence_gb300.tsp_rank import DistComm
+
+    comm = DistComm.__new__(DistComm)  # no process group needed for the store paths
+    comm.rank, comm.store = 3, _DeadStore()
+    for call in (lambda: comm.check_peers("K/V all-gather"), lambda: comm.give_up("MLP ring step 2", "timed out")):
+        try:
+            call()
+        except TspError as e:
+            assert e.status == TSP_ERR_TIMEOUT
+        else:
+            raise AssertionError("no error raised")
