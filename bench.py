@@ -48,11 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # without its own capture, or a source changed since, reports null.
 NCU_TRAFFIC = {
     ("gate/up projection", "bf16_D8_b2_s16384_h4096"):
-        (2.16e9 + 0.92808e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "1c44a2a1014d92e7"),
+        (2162.50e6 + 928.24e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "f1fbc4e5fcda0324"),
+    # the same launch (M, N, K and kernel) as the multi-head workload's gate/up projection
     ("gate/up projection", "bf16_gqa8_D8_b2_s16384_h4096"):
-        (2.16e9 + 0.92766e9, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "1c44a2a1014d92e7"),
-    ("gate/up projection", "bf16_D4_s4096_h2048"):
-        (62.96e6 + 16.29e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "1c44a2a1014d92e7"),
+        (2162.50e6 + 928.24e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "f1fbc4e5fcda0324"),
     ("attention", "bf16_D8_b2_s16384_h4096"):
         (849.534e6 + 254.581e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "f3ebf6c44e68df52"),
     ("attention", "bf16_D8_b1_s65536_h4096"):

@@ -413,8 +413,9 @@ RankAttnLayout rank_attn_layout(const tsp_plan* p, int batch) {
     return at;
   };
   L.k = take(kvb);
+  // natural V for the warp-MMA kernel, V^T (gathered straight into it) for the tcgen05 kernel
   L.v = take(kvb);
-  L.vt = use_tc_attention(p) ? take(kvb) : L.v;
+  L.vt = L.v;
   L.o = take((size_t)d.L * d.hs * e);
   L.split = use_tc_attention(p) ? take(attn_tc_split_bytes(d.L, p->heads / p->D)) : L.o;
   L.end = o;
@@ -1032,17 +1033,16 @@ tsp_status tsp_rank_qkv(const tsp_plan* p, int batch, const void* x_local, const
   const RankDims d = rank_dims(p, batch);
   const int h = p->hidden;
   cudaStream_t st = as_stream(stream);
-  EpiParams eq = base_epi(p, batch);
-  eq.out = q_local;
-  eq.ldo = d.hs;
-  if ((s = run_gemm(p, x_local, h, attn_shard, h, (int)d.L, d.hs, h, EPI_STORE, eq, st, "rank Q projection")) !=
-      TSP_OK)
-    return s;
-  EpiParams ekv = base_epi(p, batch);
-  ekv.out = kv_local;
-  ekv.ldo = 2 * d.ks;
-  const char* wkv = static_cast<const char*>(attn_shard) + (size_t)d.hs * h * esize(p);
-  return run_gemm(p, x_local, h, wkv, h, (int)d.L, 2 * d.ks, h, EPI_STORE, ekv, st, "rank K/V projection");
+  // one GEMM over the shard's Q|K|V rows (they share the A operand); its
+  // epilogue sends the Q columns to q_local and the K|V columns to kv_local
+  EpiParams e = base_epi(p, batch);
+  e.out = q_local;
+  e.ldo = d.hs;
+  e.aux = kv_local;
+  e.ldx = 2 * d.ks;
+  e.split_col = d.hs;
+  return run_gemm(p, x_local, h, attn_shard, h, (int)d.L, d.hs + 2 * d.ks, h, EPI_STORE, e, st,
+                  "rank QKV projection");
 }
 
 tsp_status tsp_rank_attention(const tsp_plan* p, int rank, int batch, const void* q_local, const void* kv_all,
@@ -1064,21 +1064,21 @@ tsp_status tsp_rank_attention(const tsp_plan* p, int rank, int batch, const void
   const size_t e = esize(p);
   cudaStream_t st = as_stream(stream);
   char* wb = static_cast<char*>(ws);
+  // the all-gathered rows [D][L][2 ks] (K columns, then V) into natural positions:
+  // K [B][Hk/D][S][dh]; V likewise, or for the tcgen05 kernel straight into V^T [B][Hk/D][dh][S]
+  const bool tc = use_tc_attention(p);
   {
-    // the all-gathered rows [D][L][2 ks] (K columns, then V) into natural positions [B][Hk/D][S][dh]
     Prof pr("rank K/V reorder", st);
     s = cuda_status(launch_kv_gather_ld(kv_all, static_cast<const char*>(kv_all) + (size_t)d.ks * e, wb + W.k,
-                                        wb + W.v, (int)e, p->D, batch, p->seq, hk_heads, p->head_dim, 2 * d.ks, st),
+                                        tc ? nullptr : wb + W.v, (int)e, p->D, batch, p->seq, hk_heads,
+                                        p->head_dim, 2 * d.ks, st, tc ? 1 : 2),
                     "rank K/V reorder");
+    if (s == TSP_OK && tc)
+      s = cuda_status(launch_kv_gather_vt(kv_all, 2 * d.ks, d.ks, wb + W.vt, p->D, batch, p->seq, hk_heads,
+                                          p->head_dim, st),
+                      "rank V^T gather");
   }
   if (s != TSP_OK) return s;
-  const bool tc = use_tc_attention(p);
-  if (tc) {
-    Prof pr("rank V transpose", st);
-    s = cuda_status(launch_transpose(wb + W.v, wb + W.vt, p->seq, p->head_dim, (int)e, st, batch * hk_heads),
-                    "rank V transpose");
-    if (s != TSP_OK) return s;
-  }
   AttnParams ap;
   ap.q = q_local;
   ap.k = wb + W.k;

@@ -53,7 +53,10 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
       if (n >= N) continue;
       float v = acc[i][j];
       if (epi == EPI_STORE) {
-        static_cast<float*>(ep.out)[m * ep.ldo + n] = v;
+        if (ep.split_col > 0 && n >= ep.split_col)
+          static_cast<float*>(ep.aux)[m * ep.ldx + (n - ep.split_col)] = v;
+        else
+          static_cast<float*>(ep.out)[m * ep.ldo + n] = v;
       } else if (epi == EPI_RESID) {
         v += static_cast<const float*>(ep.resid)[m * ep.ldr + n];
         static_cast<float*>(ep.out)[m * ep.ldo + n] = v;

@@ -582,7 +582,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!valid) continue;
           const int64_t n = (int64_t)nt * BN + c * 32;
           if constexpr (EPI == EPI_STORE) {
-            store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + n, v);
+            if (ep.split_col > 0 && n >= ep.split_col)
+              store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.aux) + m * ep.ldx + (n - ep.split_col), v);
+            else
+              store32_bf16(reinterpret_cast<__nv_bfloat16*>(ep.out) + m * ep.ldo + n, v);
           } else if constexpr (EPI == EPI_QKV) {
             // packed column n -> (shard s, which of q/k/v, head, d); a shard's
             // columns are Q (h/D) | K (Hk*dh/D) | V (Hk*dh/D)

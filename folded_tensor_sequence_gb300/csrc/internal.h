@@ -53,6 +53,9 @@ struct EpiParams {
   //   resid_natural: EPI_RESID reads resid row nat(m)
   //   out_natural:   EPI_RESID writes out row nat(m)
   bool a_natural = false, resid_natural = false, out_natural = false;
+  // EPI_STORE: columns n >= split_col (> 0, a multiple of 32) go to aux[m][n - split_col]
+  // (row stride ldx) instead of out -- two outputs of one GEMM that shares its A operand.
+  int64_t split_col = 0;
 };
 
 int num_sms();
@@ -90,9 +93,14 @@ cudaError_t launch_zigzag_rows(const void* src, void* dst, int64_t row_bytes, in
                                bool to_zigzag, cudaStream_t stream);
 cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
                              int64_t S, int H, int dh, cudaStream_t stream);
-// The same with source rows src_ld elements apart (a multiple of 16 bytes).
+// The same with source rows src_ld elements apart (a multiple of 16 bytes);
+// ntens 1 gathers K only (vz and v unused).
 cudaError_t launch_kv_gather_ld(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
-                                int64_t S, int H, int dh, int64_t src_ld, cudaStream_t stream);
+                                int64_t S, int H, int dh, int64_t src_ld, cudaStream_t stream, int ntens = 2);
+// 16-bit V of zigzag rows [T][ld] (head e at columns v_col0 + e*dh) -> vt
+// [B][H][dh][S] in natural positions; needs seq/(2D) % 64 == 0 and dh % 64 == 0.
+cudaError_t launch_kv_gather_vt(const void* src, int64_t ld, int64_t v_col0, void* vt, int D, int B, int64_t S,
+                                int H, int dh, cudaStream_t stream);
 // 2-D copy of `rows` rows of row_bytes (pitches and row_bytes multiples of 16).
 cudaError_t launch_copy_rows(const void* src, int64_t src_pitch_bytes, void* dst, int64_t dst_pitch_bytes,
                              int64_t rows, int64_t row_bytes, cudaStream_t stream);

@@ -81,11 +81,11 @@ __global__ void __launch_bounds__(kCopyThreads) zigzag_rows_kernel(const uint4* 
 __global__ void __launch_bounds__(kCopyThreads) kv_gather_kernel(const uint4* __restrict__ kz,
                                                                  const uint4* __restrict__ vz, uint4* __restrict__ k,
                                                                  uint4* __restrict__ v, int lg_vph, int D, int B,
-                                                                 int64_t S, int H, int64_t vec_per_row) {
+                                                                 int64_t S, int H, int64_t vec_per_row, int ntens) {
   const int64_t C = S / (2 * D);
   const int vph = 1 << lg_vph;
   const int64_t seg_vecs = C << lg_vph;
-  const int64_t items = 2LL * B * H * 2 * D;
+  const int64_t items = (int64_t)ntens * B * H * 2 * D;  // ntens 1: K only
   for (int64_t w = blockIdx.x; w < items; w += gridDim.x) {
     const int c = (int)(w % (2 * D));
     int64_t rest = w / (2 * D);
@@ -122,6 +122,59 @@ __global__ void __launch_bounds__(kCopyThreads) copy_rows_kernel(const uint4* __
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / row_vecs, c = i - r * row_vecs;
     dst[r * dst_pitch + c] = __ldg(&src[r * src_pitch + c]);
+  }
+}
+
+// V of the all-gathered rows straight into the transposed natural layout the
+// tcgen05 attention reads: vt [B][H][dh][S] <- src zigzag rows [T][ld] (V of
+// head e in columns v_col0 + e*dh ..).  One CTA per 64 positions x 64 head
+// dims: the 64 positions lie in one chunk (C % 64 == 0), i.e. 64 consecutive
+// zigzag rows of one rank; through a 64 x 64 shared tile whose 16-byte chunk c
+// of row r sits at c ^ ((r / 8) % 8), as in transpose_b16_kernel.
+__global__ void __launch_bounds__(256) kv_gather_vt_kernel(const uint16_t* __restrict__ src, int64_t ld,
+                                                           int64_t v_col0, uint16_t* __restrict__ vt, int D, int B,
+                                                           int64_t S, int H, int dh) {
+  __shared__ __align__(16) uint16_t tile[64 * 64];
+  const int64_t C = S / (2 * D);
+  const int64_t ptiles = S / 64, dtiles = dh / 64;
+  const int64_t ntiles = (int64_t)B * H * ptiles * dtiles;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t dt = t % dtiles;
+    int64_t rest = t / dtiles;
+    const int64_t pt = rest % ptiles;
+    rest /= ptiles;
+    const int head = (int)(rest % H);
+    const int b = (int)(rest / H);
+    const int64_t p0 = pt * 64, d0 = dt * 64;
+    const int64_t c = p0 / C, off = p0 - c * C;
+    const int64_t r = c < D ? c : 2 * D - 1 - c;
+    const int64_t zrow0 = (r * B + b) * 2 * C + (c < D ? 0 : C) + off;
+    const uint16_t* s0 = src + zrow0 * ld + v_col0 + (int64_t)head * dh + d0;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int idx = threadIdx.x + it * 256;  // 64 positions x 8 chunks of 8 dims
+      const int rr = idx / 8, cv = idx % 8;
+      const uint4 val = __ldg(reinterpret_cast<const uint4*>(s0 + (int64_t)rr * ld + cv * 8));
+      *reinterpret_cast<uint4*>(&tile[rr * 64 + ((cv ^ ((rr / 8) & 7)) * 8)]) = val;
+    }
+    __syncthreads();
+    uint16_t* d0p = vt + (((int64_t)b * H + head) * dh + d0) * S + p0;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int idx = threadIdx.x + it * 256;  // 64 dims x 8 chunks of 8 positions
+      const int cc = idx / 8, rv = idx % 8;    // head dim d0 + cc, positions rv*8 .. rv*8+7
+      const int pos = (((cc / 8) ^ rv) * 8) + (cc % 8);
+      uint16_t e[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) e[k] = tile[(rv * 8 + k) * 64 + pos];
+      uint4 val;
+      val.x = e[0] | (uint32_t(e[1]) << 16);
+      val.y = e[2] | (uint32_t(e[3]) << 16);
+      val.z = e[4] | (uint32_t(e[5]) << 16);
+      val.w = e[6] | (uint32_t(e[7]) << 16);
+      *reinterpret_cast<uint4*>(d0p + (int64_t)cc * S + rv * 8) = val;
+    }
+    __syncthreads();
   }
 }
 
@@ -367,18 +420,30 @@ cudaError_t launch_kv_gather(const void* kz, const void* vz, void* k, void* v, i
   return launch_kv_gather_ld(kz, vz, k, v, elem_bytes, D, B, S, H, dh, (int64_t)H * dh, stream);
 }
 
+cudaError_t launch_kv_gather_vt(const void* src, int64_t ld, int64_t v_col0, void* vt, int D, int B, int64_t S,
+                                int H, int dh, cudaStream_t stream) {
+  const int64_t C = S / (2 * D);
+  if (C % 64 || dh % 64 || ld % 8 || v_col0 % 8) return cudaErrorInvalidValue;
+  const int64_t ntiles = (int64_t)B * H * (S / 64) * (dh / 64);
+  if (ntiles == 0) return cudaSuccess;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  kv_gather_vt_kernel<<<(int)(ntiles < cap ? ntiles : cap), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(src), ld, v_col0, static_cast<uint16_t*>(vt), D, B, S, H, dh);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_kv_gather_ld(const void* kz, const void* vz, void* k, void* v, int elem_bytes, int D, int B,
-                                int64_t S, int H, int dh, int64_t src_ld, cudaStream_t stream) {
+                                int64_t S, int H, int dh, int64_t src_ld, cudaStream_t stream, int ntens) {
   const int vph = dh * elem_bytes / 16;
   int lg = 0;
   while ((1 << lg) < vph) ++lg;
   if ((1 << lg) != vph) return cudaErrorInvalidValue;  // dh * elem_bytes is 64, 128, 256 or 512
-  const int64_t items = 2LL * B * H * 2 * D;
+  const int64_t items = (int64_t)ntens * B * H * 2 * D;
   if ((int64_t)B * H * S == 0) return cudaSuccess;
   const int64_t cap = (int64_t)num_sms() * 8;
   kv_gather_kernel<<<(int)(items < cap ? items : cap), kCopyThreads, 0, stream>>>(
       static_cast<const uint4*>(kz), static_cast<const uint4*>(vz), static_cast<uint4*>(k), static_cast<uint4*>(v),
-      lg, D, B, S, H, src_ld * elem_bytes / 16);
+      lg, D, B, S, H, src_ld * elem_bytes / 16, ntens);
   return cudaGetLastError();
 }
 
