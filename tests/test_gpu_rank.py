@@ -8,17 +8,18 @@
   gives every rank's output rows; stitched together they must match the
   oracle (fp32: max relative 1e-4; bf16: relative Frobenius 2e-2) and the
   single-GPU tsp_layer_fwd (which sums the same shards in another order).
-* At the 16K-token x 2, D = 8 workload the stitched output is compared with
-  tsp_layer_fwd over every element.
-Every rank's buffers are checked for NaN (they start as NaN-free garbage, so
-the check is on the result only) and the outputs of tsp_rank_* are also
-guarded against writes outside them.
+* At the 16K-token x 2, D = 8 workload (32 and 8 K/V heads) the stitched
+  output is compared with tsp_layer_fwd over every element.  One rank's
+  attention there runs with the key split (two CTAs per mirror pair and a
+  log-sum-exp combine), as it does in every small tcgen05 case here.
+* One rank's three calls write nothing outside their outputs and workspaces
+  (guard bands) and produce finite values.
 """
 import numpy as np
 import pytest
 
 from folded_tensor_sequence_gb300 import synth
-from folded_tensor_sequence_gb300.configs import LAYER_7B_S16K, LayerConfig
+from folded_tensor_sequence_gb300.configs import LAYER_7B_GQA8_S16K, LAYER_7B_S16K, LayerConfig
 from oracle import tsp_oracle as O
 
 from helpers import check, guarded_like, guarded_workspace, rel_frob, to_dev, to_np
@@ -165,14 +166,15 @@ def test_rank_entry_outputs_stay_in_bounds(tsp):
         assert torch.isfinite(g.t.float()).all()
 
 
-def test_rank_schedule_full_size_matches_layer(tsp):
-    """D = 8 ranks, 2 x 16384 tokens, hidden 4096: the stitched per-rank output against tsp_layer_fwd
-    over every element (the layer itself is pinned to the oracle on sampled rows at this size)."""
+@pytest.mark.parametrize("cfg", [LAYER_7B_S16K, LAYER_7B_GQA8_S16K], ids=lambda c: c.name)
+def test_rank_schedule_full_size_matches_layer(tsp, cfg):
+    """D = 8 ranks, 2 x 16384 tokens, hidden 4096 (32 K/V heads, and 8): the stitched per-rank output
+    against tsp_layer_fwd over every element (the layer itself is pinned to the oracle on sampled rows
+    at this size)."""
     import torch
 
-    cfg = LAYER_7B_S16K
-    h, F = cfg.hidden, cfg.ffn
-    shapes = {"Wq": (h, h), "Wk": (h, h), "Wv": (h, h), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}
+    h, F, hk = cfg.hidden, cfg.ffn, cfg.kv_hidden
+    shapes = {"Wq": (h, h), "Wk": (h, hk), "Wv": (h, hk), "Wo": (h, h), "Wg": (h, F), "Wu": (h, F), "Wd": (F, h)}
     inp = {k: synth.tensor_torch(k, s, (F if k == "Wd" else h) ** -0.5, "bf16", 0, "cpu").double().numpy()
            for k, s in shapes.items()}
     inp["x"] = synth.tensor_torch("x", (cfg.batch, cfg.seq, h), 1.0, "bf16", 0, "cpu").double().numpy()
