@@ -63,9 +63,9 @@ NCU_TRAFFIC = {
     ("attention bwd fused", "bf16_fwdbwd_gqa8_D8_b1_s8192_h4096"):
         (652.95e6 + 290.93e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
     ("kv gather (standalone)", "bf16_D8_b2_s16384_h4096"):
-        (536.903e6 + 486.071e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "535fa8a09df460cd"),
+        (536.906e6 + 485.511e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "b3e6ab7624313095"),
     ("zigzag permute (standalone)", "bf16_D8_b2_s16384_h4096"):
-        (268.449e6 + 217.227e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "535fa8a09df460cd"),
+        (268.450e6 + 216.774e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "b3e6ab7624313095"),
     ("decode attention", "bf16_decode_D8_b1_ctx131072_h4096"):
         (2.15e9 + 0.00292e9, "folded_tensor_sequence_gb300/csrc/decode.cu", "3bfb1d17f6da32df"),
     ("decode attention", "bf16_decode_gqa8_D8_b4_ctx131072_h4096"):

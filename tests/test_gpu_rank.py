@@ -186,3 +186,39 @@ def test_rank_schedule_full_size_matches_layer(tsp, cfg):
     e = float((y.float() - y1.float()).norm() / y1.float().norm())
     print(f"PARITY full-size per-rank vs tsp_layer_fwd: relative Frobenius {e:.3e}")
     assert e <= 2e-2
+
+
+def test_rank_calls_without_residual(tsp):
+    """resid NULL means 0: the attention and MLP steps store their product, equal to adding it to zeros."""
+    import torch
+
+    cfg = CASES[2]  # grouped-query attention, two sequences, tcgen05 attention with the key split
+    inp = synth.layer_inputs(cfg, seed=27)
+    plan = tsp.plan_for(cfg)
+    packed = _packed(tsp, plan, inp, cfg.dtype)
+    D, L, h = cfg.D, cfg.batch * 2 * cfg.chunk, cfg.hidden
+    hs, ks = h // D, cfg.kv_hidden // D
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn(L, h, generator=gen, device="cuda").to(torch.bfloat16)
+    kv_all = torch.randn(D, L, 2 * ks, generator=gen, device="cuda").to(torch.bfloat16)
+    shard = torch.empty(tsp.tsp_rank_shard_bytes(plan, tsp.TSP_SHARD_ATTENTION), dtype=torch.uint8, device="cuda")
+    mshard = torch.empty(tsp.tsp_rank_shard_bytes(plan, tsp.TSP_SHARD_MLP), dtype=torch.uint8, device="cuda")
+    tsp.tsp_rank_extract_shard(plan, packed, 2, tsp.TSP_SHARD_ATTENTION, shard)
+    tsp.tsp_rank_extract_shard(plan, packed, 3, tsp.TSP_SHARD_MLP, mshard)
+    q = torch.empty(L, hs, dtype=torch.bfloat16, device="cuda")
+    kv = torch.empty(L, 2 * ks, dtype=torch.bfloat16, device="cuda")
+    tsp.tsp_rank_qkv(plan, cfg.batch, x, shard, q, kv)
+    wa = tsp.workspace(plan, cfg.batch, tsp.TSP_OP_RANK_ATTENTION)
+    wm = tsp.workspace(plan, cfg.batch, tsp.TSP_OP_RANK_MLP)
+    zeros = torch.zeros_like(x)
+    for r in (0, D - 1):
+        a0, a1 = torch.empty_like(x), torch.empty_like(x)
+        tsp.tsp_rank_attention(plan, r, cfg.batch, q, kv_all, shard, None, a0, wa)
+        tsp.tsp_rank_attention(plan, r, cfg.batch, q, kv_all, shard, zeros, a1, wa)
+        m0, m1 = torch.empty_like(x), torch.empty_like(x)
+        tsp.tsp_rank_mlp(plan, cfg.batch, x, mshard, None, m0, wm)
+        tsp.tsp_rank_mlp(plan, cfg.batch, x, mshard, zeros, m1, wm)
+        tsp.tsp_sync_check()
+        assert torch.isfinite(a0.float()).all() and float(a0.float().abs().max()) > 0
+        assert torch.equal(a0, a1), f"rank {r}: attention output with resid NULL differs from resid 0"
+        assert torch.equal(m0, m1), f"rank {r}: MLP output with resid NULL differs from resid 0"
