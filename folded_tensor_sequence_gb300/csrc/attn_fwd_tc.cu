@@ -19,20 +19,29 @@
 // chunk 2D-1-c); A runs out of key tiles first and B finishes alone.  Either
 // way every CTA does the same number of key tiles.
 //
-// Per CTA: warp 8 issues TMA loads (a block's Q tiles, then K_j / V_j^T tiles
-// through a 5-stage ring), warp 9 issues tcgen05.mma from one thread, warps 0-3 and 4-7
-// are the softmax warpgroups of tiles A and B.  TMEM (512 columns): S_A, S_B,
-// O_A, O_B, 128 fp32 columns each.  Issue order per key tile j:
+// Per CTA: warp 16 issues TMA loads (a block's Q tiles, then K_j / V_j^T
+// tiles through a 5-stage ring), warp 17 issues tcgen05.mma from one thread,
+// and warps 0-15 run the softmax: for each tile and TMEM lane quadrant two
+// warps, each on half of the row's 128 key columns.  TMEM (512 columns): S_A,
+// S_B, O_A, O_B, 128 fp32 columns each.  Issue order per key tile j:
 //   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 // so the tensor core works on one tile while the other tile's softmax runs.
-// The softmax warpgroups hand P_x(j) over through named barriers (the MMA
-// warp never waits on an mbarrier inside a block; the handing-over warpgroup
-// has checked the K/V tiles that the following MMAs read).
-// P = exp2(S*log2e/sqrt(dh) - m) is written as packed bf16 back into the first
-// 64 columns of S's TMEM and consumed from there by the PV MMA (A operand in
-// tensor memory), which leaves shared memory for a deep K/V ring.  The running max is only
-// raised (and O rescaled in TMEM) when it grows by more than 2^8, which keeps
-// P <= 256 and makes the rescale rare.
+// The softmax warps hand P_x(j) over through named barriers (the MMA warp
+// never waits on an mbarrier inside a block; one softmax thread has checked
+// the K/V tiles that the following MMAs read).
+// P = exp2(S*log2e/sqrt(dh) - m) is written as packed bf16 back into S's TMEM
+// (each half over the first 32 of its 64 columns) and consumed from there by
+// the PV MMA (A operand in tensor memory), which leaves shared memory for a
+// deep K/V ring.  The running max is only raised (and O rescaled in TMEM)
+// when it grows by more than 2^8, which keeps P <= 256 and makes the rescale
+// rare; the test for it is the half-row's sum of P, not a max.
+//
+// Why two warps per row and no per-tile max: the MMA warp shares its SM
+// sub-partition with softmax warps, and every softmax instruction issued
+// there delays its MMA issue (measured: a key-tile step takes 2230 cycles
+// with no softmax arithmetic, 3140 with the one-warp softmax and its max
+// tree, 2790 now).  Fewer softmax instructions per score, not shorter
+// softmax latency, is what keeps the tensor pipe fed.
 #include "common.cuh"
 #include "internal.h"
 
@@ -44,17 +53,25 @@ constexpr int QT = 128;    // rows per query tile (MMA M)
 constexpr int KT = 128;    // keys per key tile
 constexpr int HD = 128;    // head dim
 constexpr int STAGES = 5;  // K / V^T tile ring
-constexpr int THREADS = 320;
 constexpr uint32_t SUB_BYTES = 128 * 64 * 2;     // one [128][64] bf16 swizzled sub-tile
 constexpr uint32_t TILE_BYTES = 2 * SUB_BYTES;   // [128][128]
-constexpr size_t SMEM_BYTES = 1024 + (2 + STAGES) * (size_t)TILE_BYTES + 256;
+// Softmax warps 0-15 (two per query tile and TMEM lane quadrant, each taking
+// half of a row's 128 key columns), then the TMA warp and the MMA warp.
+constexpr int THREADS = 576;
+constexpr int kTmaWarp = 16, kMmaWarp = 17;
+constexpr int kHandoff = 256 + 32;  // a tile's softmax threads + the MMA warp
+// Q tiles, K/V ring, mbarriers, one fp32 per row of both tiles (the row sums
+// the two halves exchange).
+constexpr size_t SMEM_BYTES = 1024 + (2 + STAGES) * (size_t)TILE_BYTES + 256 + 2 * 128 * sizeof(float);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// Named barriers handing P_x(j) from softmax warpgroup x to the MMA warp,
-// two per tile (alternating with j): A uses 1-2, B uses 3-4.
-constexpr int kBarPA = 1, kBarPB = 3;
-constexpr int kHandoffThreads = 128 + 32;
+constexpr float kRescaleSum = 256.0f;      // 2^kRescaleThreshold
+// Named barriers handing P_x(j) from the softmax warps of tile x to the MMA
+// warp, two per tile (alternating with j): A uses 1-2, B uses 3-4.  Barriers
+// 5-12 pair the two warps that share the rows of one TMEM lane quadrant of one
+// tile (5 + 4x + quadrant).
+constexpr int kBarPA = 1, kBarPB = 3, kBarPair = 5;
 
 struct FaParams {
   int B, H, D, nb;  // nb = blocks per chunk: 256-query blocks (nblk 2) or 128-query tiles (nblk 1)
@@ -143,6 +160,70 @@ __device__ __forceinline__ void exp_pack_quarter(const uint32_t (&h)[32], uint32
   }
 }
 
+// 16-column forms of the mask and max helpers above.
+__device__ __forceinline__ void mask16(uint32_t (&h)[16], int c0, int row) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    if (c0 + c > row) h[c] = __float_as_uint(-INFINITY);
+}
+__device__ __forceinline__ float max16(const uint32_t (&h)[16], float m) {
+  const float a0 = fmax3(__uint_as_float(h[0]), __uint_as_float(h[1]), __uint_as_float(h[2]));
+  const float a1 = fmax3(__uint_as_float(h[3]), __uint_as_float(h[4]), __uint_as_float(h[5]));
+  const float a2 = fmax3(__uint_as_float(h[6]), __uint_as_float(h[7]), __uint_as_float(h[8]));
+  const float a3 = fmax3(__uint_as_float(h[9]), __uint_as_float(h[10]), __uint_as_float(h[11]));
+  const float a4 = fmax3(__uint_as_float(h[12]), __uint_as_float(h[13]), __uint_as_float(h[14]));
+  return fmax3(fmax3(a0, a1, a2), fmax3(a3, a4, __uint_as_float(h[15])), m);
+}
+// The two 32-bit words of a K-major 128-byte-swizzle descriptor (as
+// sdesc_kmajor_sw128 builds it): the high word is the same for every tile, the
+// low word is the start address >> 4 plus the leading-byte-offset field.
+// Advancing K by 16 elements adds 2 (32 bytes) within a 64-element sub-tile
+// and SUB_BYTES >> 4 between the two sub-tiles; no carry leaves the 14-bit
+// address field for any shared-memory address.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+__host__ __device__ constexpr uint32_t kstep_lo(int k) { return (k / 4) * (SUB_BYTES >> 4) + 2 * (k % 4); }
+
+// Warp-collective MMAs (one elected lane issues) from descriptor low words:
+// A and B from shared memory, or A from tensor memory.
+__device__ __forceinline__ void mma_ss_lo(uint32_t d, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n"
+      ".reg .b64 ad, bd;\n"
+      ".reg .pred p, e;\n"
+      "mov.b64 ad, {%1, %5};\n"
+      "mov.b64 bd, {%2, %5};\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n"
+      "}\n" ::"r"(d),
+      "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_lo(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n"
+      ".reg .b64 bd;\n"
+      ".reg .pred p, e;\n"
+      "mov.b64 bd, {%2, %5};\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n"
+      "}\n" ::"r"(d),
+      "r"(a_tmem), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi)
+      : "memory");
+}
+// Warp-collective commit to the mbarrier at shared address `bar`.
+__device__ __forceinline__ void commit_to(uint32_t bar) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar)
+      : "memory");
+}
+
 struct BlockGeo {
   int64_t zrow[2];  // row of Q / O holding tile x's first query
   int64_t p0[2];    // global position of tile x's first query
@@ -196,6 +277,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* lx = reinterpret_cast<float*>(smem + (2 + STAGES) * TILE_BYTES + 256);  // [2 tiles][128 rows]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int head = blockIdx.y, b = blockIdx.z;
@@ -232,12 +314,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmVt);
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -247,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const unsigned code = KID_ATTN_FWD << 8;
 
-  if (warp == 8) {
+  if (warp == kTmaWarp) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
       const int kvh = head / (p.H / p.Hk);                        // the K/V head this query head reads
@@ -292,7 +374,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (uint32_t n = first; n < item; ++n) mbar_wait(&kv_full[n % STAGES], (n / STAGES) & 1, &dummy, p.err, code | 3);
       for (int q = 0; q < q_loaded; ++q) mbar_wait(&q_full[q], 0, &dummy, p.err, code | 3);
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
     // The whole warp walks the schedule (named barriers are warp-aligned) and
     // issues through the warp-collective MMA helpers (one elected lane
@@ -302,21 +384,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(QT, KT);
     uint32_t item = 0;
     bool ok = true;  // warp-uniform: false once this warp gave up waiting
-    auto mma_s = [&](int x, int s) {  // S_x = Q_x K^T, K = head dim
-      const uint32_t qa = smem_u32(Qs + x * TILE_BYTES), kb = smem_u32(KVs + s * TILE_BYTES);
+    // The MMA warp shares its SM sub-partition with softmax warps that keep
+    // it from issuing; its own stream is kept short: descriptor low words per
+    // tile and stage computed once, K/V stages advanced incrementally.
+    const uint32_t q_lo = sdesc_lo(smem_u32(Qs));     // tile x: + x * (TILE_BYTES >> 4)
+    const uint32_t kv_lo = sdesc_lo(smem_u32(KVs));   // stage s: + s * (TILE_BYTES >> 4)
+    const uint32_t kv_empty_at = smem_u32(kv_empty);  // stage s: + 8 s
+    const uint32_t s_full_at = smem_u32(s_full), o_done_at = smem_u32(o_done);
+    auto next_stage = [](uint32_t s) { return s == STAGES - 1 ? 0u : s + 1; };
+    auto mma_s = [&](int x, uint32_t s) {  // S_x = Q_x K^T, K = head dim
+      const uint32_t alo = q_lo + x * (TILE_BYTES >> 4), blo = kv_lo + s * (TILE_BYTES >> 4);
 #pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint64_t a = sdesc_kmajor_sw128(qa + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-        const uint64_t bb = sdesc_kmajor_sw128(kb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-        umma_bf16_warp(tmem_base + x * 128, a, bb, idesc, k > 0);
-      }
+      for (int k = 0; k < HD / 16; ++k)
+        mma_ss_lo(tmem_base + x * 128, alo + kstep_lo(k), blo + kstep_lo(k), idesc, k > 0);
     };
-    auto mma_pv = [&](int x, int s, bool acc) {  // O_x += P_x V, K = keys; P_x in TMEM (S_x columns 0-63)
-      const uint32_t vb = smem_u32(KVs + s * TILE_BYTES);
+    // O_x += P_x V, K = keys; P_x in TMEM over S_x's columns: keys 16k..16k+15
+    // are the 8 packed columns at 64*(k/4) + 8*(k%4) (each half's P over the
+    // first 32 of its own 64 columns)
+    auto mma_pv = [&](int x, uint32_t s, bool acc) {
+      const uint32_t blo = kv_lo + s * (TILE_BYTES >> 4);
 #pragma unroll
       for (int k = 0; k < KT / 16; ++k) {
-        const uint64_t bb = sdesc_kmajor_sw128(vb + (k / 4) * SUB_BYTES) + 2 * (k % 4);
-        umma_bf16_ts_warp(tmem_base + 256 + x * 128, tmem_base + x * 128 + 8 * k, bb, idesc, (acc || k > 0) ? 1u : 0u);
+        const uint32_t pcol = 64 * (k / 4) + 8 * (k % 4);
+        mma_ts_lo(tmem_base + 256 + x * 128, tmem_base + x * 128 + pcol, blo + kstep_lo(k), idesc,
+                  (acc || k > 0) ? 1u : 0u);
       }
     };
     for (int blk = 0; blk < p.nblk; ++blk) {
@@ -333,45 +424,48 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       }
       tc_fence_after();
+      const uint32_t s0 = item % STAGES;  // stage of K_lo
       if (ok) {
         if (actA) {
-          mma_s(0, item % STAGES);
-          umma_commit_warp(&s_full[0]);
+          mma_s(0, s0);
+          commit_to(s_full_at);
         }
-        mma_s(1, item % STAGES);
-        umma_commit_warp(&s_full[1]);
-        umma_commit_warp(&kv_empty[item % STAGES]);
+        mma_s(1, s0);
+        commit_to(s_full_at + 8);
+        commit_to(kv_empty_at + 8 * s0);
       }
+      uint32_t sv = next_stage(s0);  // stage of V_j
       for (int j = lo; j < nB; ++j) {
-        const uint32_t iv = base + 2 * j + 1, ik = base + 2 * j + 2;
+        const uint32_t sk = next_stage(sv);  // stage of K_{j+1}
         if (j < nA) {
           __syncwarp();
-          named_bar_sync(kBarPA + (j & 1), kHandoffThreads);
+          named_bar_sync(kBarPA + (j & 1), kHandoff);
           tc_fence_after();
           if (ok) {
-            mma_pv(0, iv % STAGES, j > lo);
+            mma_pv(0, sv, j > lo);
             if (j + 1 < nA) {
-              mma_s(0, ik % STAGES);
-              umma_commit_warp(&s_full[0]);
+              mma_s(0, sk);
+              commit_to(s_full_at);
             } else {
-              umma_commit_warp(&o_done[0]);
+              commit_to(o_done_at);
             }
           }
         }
         __syncwarp();
-        named_bar_sync(kBarPB + (j & 1), kHandoffThreads);
+        named_bar_sync(kBarPB + (j & 1), kHandoff);
         tc_fence_after();
         if (ok) {
-          mma_pv(1, iv % STAGES, j > lo);
-          umma_commit_warp(&kv_empty[iv % STAGES]);
+          mma_pv(1, sv, j > lo);
+          commit_to(kv_empty_at + 8 * sv);
           if (j + 1 < nB) {
-            mma_s(1, ik % STAGES);
-            umma_commit_warp(&s_full[1]);
-            umma_commit_warp(&kv_empty[ik % STAGES]);
+            mma_s(1, sk);
+            commit_to(s_full_at + 8);
+            commit_to(kv_empty_at + 8 * sk);
           } else {
-            umma_commit_warp(&o_done[1]);
+            commit_to(o_done_at + 8);
           }
         }
+        sv = next_stage(sk);
       }
       item = base + 2 * nB;
       // the Q buffer is free for block 1 once every MMA issued so far is done
@@ -384,35 +478,78 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------- softmax warpgroups (warps 0-7) -------------------------
-    const int x = warp / 4;  // 0: tile A, 1: tile B
-    const int quad = warp % 4;
-    const int row = quad * 32 + lane;  // TMEM lane == row of the tile
+    // -------------- softmax, two warps per tile and lane quadrant (warps 0-15) --------------
+    // Warp w: tile x = (w / 4) % 2, rows of TMEM lane quadrant w % 4, key
+    // columns [64 hf, 64 hf + 64) with hf = w / 8.  Both halves of a row keep
+    // the same running max m_used (a block's first key tile and every raise
+    // take the max over the whole row, which both compute alike).  Per key
+    // tile no max is taken: an exponential above 2^8 (the max grew by more
+    // than the threshold) makes the half's sum of P exceed 2^8, and the two
+    // halves vote on that on their pair barrier; only then is the row's max
+    // read to decide the raise.  Half hf writes its P over the first 32 of its
+    // own 64 columns, rescales and stores O's columns [64 hf, 64 hf + 64), and
+    // the halves add their row sums through shared memory at the end of a block.
+    const int x = (warp / 4) & 1;
+    const int hf = warp / 8;
+    const int quad = warp % 4;  // the TMEM lane quadrant a warp may access
+    const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem_base + lane_off + x * 128;
-    const uint32_t tO = tmem_base + lane_off + 256 + x * 128;
+    const uint32_t tSx = tmem_base + lane_off + x * 128;  // the whole row of S_x
+    const uint32_t tS = tSx + 64 * hf;                    // this half's columns
+    const uint32_t tO = tmem_base + lane_off + 256 + x * 128 + 64 * hf;
+    const int pbar = kBarPair + 4 * x + quad;
     const float sl2 = kLog2e * rsqrtf((float)HD);
-    uint32_t scnt = 0;
-    uint32_t ocnt = 0;  // completed phases of o_done[x] (a tile with no key tile in its part has none)
-    uint32_t item = 0;  // the producer's K/V item numbering
-    bool alive = true;  // warp-uniform; once false the warp only keeps the hand-off count
-    const bool checker = quad == 0 && lane == 0;
+    uint32_t scnt = 0, ocnt = 0, item = 0;
+    bool alive = true;
+    const bool checker = hf == 0 && quad == 0 && lane == 0;
+    // Raw max of the row's 128 scores (masked on the diagonal tile).  With
+    // 18 warps the kernel has 96 registers a thread, so the TMEM loads here
+    // and below are not double-buffered; what costs the tensor pipe is the
+    // number of softmax instructions, not their latency.
+    auto row_max = [&](bool diag) {
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k) {
+        uint32_t bf[16];
+        tmem_ld16_issue(tSx + 16 * k, bf);
+        tmem_wait_ld16(bf);
+        if (diag) mask16(bf, 16 * k, row);
+        mx = max16(bf, mx);
+      }
+      return mx;
+    };
+    // P = 2^(s sl2 - m) over this half's 64 columns, packed into pk; returns
+    // the row sum of P in sum
+    auto half_exp = [&](bool diag, float m, uint32_t (&pk)[32], float& sum) {
+      const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-m, -m);
+      uint64_t acc[2] = {0, 0};
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t bf[32];
+        tmem_ld32_issue(tS + 32 * k, bf);
+        tmem_wait_ld32(bf);
+        if (diag) mask_quarter(bf, 64 * hf + 32 * k, row);
+        exp_pack_quarter(bf, pk + 16 * k, sl2x2, negm2, acc);
+      }
+      float a0, a1, a2, a3;
+      f2unpack(acc[0], a0, a1);
+      f2unpack(acc[1], a2, a3);
+      sum = (a0 + a1) + (a2 + a3);
+    };
     for (int blk = 0; blk < p.nblk; ++blk) {
       const BlockGeo g = block_geo(blk, light, p, b);
-      const int n = x ? g.n[1] : g.n[0];  // selects, not a runtime index into the struct's arrays
+      const int n = x ? g.n[1] : g.n[0];
       int lo, hiA, hiB;
       key_part(g, lo, hiA, hiB);
-      const int hi = x ? hiB : hiA;  // this tile's key tiles in this part: [lo, hi)
+      const int hi = x ? hiB : hiA;
       const uint32_t base = item - 2 * lo;
       item = item + 2 * (hiB - lo);
       float m_used = -INFINITY, l = 0.f;
-      // Hands P_x(j) to the MMA warp.  Its next MMAs read V_j and, if this
-      // tile has another key tile, K_{j+1}: one thread checks that both have
-      // landed before the warpgroup arrives.  Every warp arrives once per key
-      // tile whatever happened, so the MMA warp's barrier count always
-      // completes; a warp that has given up waiting uses the blocking form,
-      // which keeps it from running ahead and completing a barrier phase in
-      // the MMA warp's place.
+      // Every warp arrives once per key tile whatever happened, so the MMA
+      // warp's barrier count always completes; the checker first makes sure
+      // V_j and K_{j+1} have landed (the MMAs that follow read them).  A warp
+      // that has given up waiting uses the blocking form, which keeps it from
+      // running ahead and completing a barrier phase in the MMA warp's place.
       auto hand_off = [&](int jj) {
         if (checker && alive) {
           const uint32_t iv = base + 2 * jj + 1;
@@ -421,114 +558,79 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         if (alive)
-          named_bar_arrive((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoffThreads);
+          named_bar_arrive((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoff);
         else
-          named_bar_sync((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoffThreads);
+          named_bar_sync((x == 0 ? kBarPA : kBarPB) + (jj & 1), kHandoff);
       };
       for (int j = lo; j < hi; ++j) {
         const bool got = alive && mbar_wait(&s_full[x], scnt & 1, abort_flag, p.err, code | 8);
         ++scnt;
         alive = __all_sync(0xffffffffu, got);
         if (!alive) {
+          named_bar_red_or(pbar, 64, false);  // one vote per key tile whatever happened
           hand_off(j);
           continue;
         }
         tc_fence_after();
         const bool diag = (j == n - 1);
-        // Columns 0-63 are loaded and waited; columns 64-127 load while the
-        // first half is exponentiated.  Exponentials use the running max from
-        // earlier key tiles (speculation); only if this tile raises the max by
-        // more than the threshold are O rescaled and P recomputed from S.
-        // Four 32-column quarters of S: quarter k+1 loads while quarter k is
-        // processed.  Exponentials use the running max from earlier key tiles
-        // (speculation); only if this tile raises the max by more than the
-        // threshold are O rescaled and P recomputed from S (still in TMEM).
-        uint32_t pk[64];
-        if (j == lo) {  // first key tile of the block (or its part): the max has to come first
-          float mx = -INFINITY;
+        if (j == lo) m_used = row_max(diag) * sl2;  // a block's (or part's) first key tile: the exact max
+        uint32_t pk[32];
+        float sum;
+        half_exp(diag, m_used, pk, sum);
+        // exponentials against the running max (exact on the first tile, so
+        // the sum there is at most 64); the row's max is read only when some
+        // half of the pair's rows summed above 2^8 (NaN sums count too)
+        if (named_bar_red_or(pbar, 64, !(sum <= kRescaleSum))) {
+          const float m_new = row_max(diag) * sl2;
+          const bool up = m_new > m_used + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, up)) {
+            const float factor = up ? ex2f(m_used - m_new) : 1.0f;
 #pragma unroll 1
-          for (int k = 0; k < 4; ++k) {
-            uint32_t hq[32];
-            tmem_ld32_issue(tS + 32 * k, hq);
-            tmem_wait_ld32(hq);
-            if (diag) mask_quarter(hq, 32 * k, row);
-            mx = fmaxf(mx, max_quarter(hq));
-          }
-          m_used = mx * sl2;
-        }
-        float sum = 0.f;
-        bool again = true;
-        for (int pass = 0; pass < 2 && again; ++pass) {
-          const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-m_used, -m_used);
-          uint64_t acc[2] = {0, 0};
-          float mx = -INFINITY;
-          uint32_t hq0[32], hq1[32];
-          tmem_ld32_issue(tS, hq0);
-          tmem_wait_ld32(hq0);
-          tmem_ld32_issue(tS + 32, hq1);
-          if (diag) mask_quarter(hq0, 0, row);
-          mx = max_quarter(hq0);
-          exp_pack_quarter(hq0, pk, sl2x2, negm2, acc);
-          tmem_wait_ld32(hq1);
-          tmem_ld32_issue(tS + 64, hq0);
-          if (diag) mask_quarter(hq1, 32, row);
-          mx = fmaxf(mx, max_quarter(hq1));
-          exp_pack_quarter(hq1, pk + 16, sl2x2, negm2, acc);
-          tmem_wait_ld32(hq0);
-          tmem_ld32_issue(tS + 96, hq1);
-          if (diag) mask_quarter(hq0, 64, row);
-          mx = fmaxf(mx, max_quarter(hq0));
-          exp_pack_quarter(hq0, pk + 32, sl2x2, negm2, acc);
-          tmem_wait_ld32(hq1);
-          if (diag) mask_quarter(hq1, 96, row);
-          mx = fmaxf(mx, max_quarter(hq1));
-          exp_pack_quarter(hq1, pk + 48, sl2x2, negm2, acc);
-          float a0, a1, a2, a3;
-          f2unpack(acc[0], a0, a1);
-          f2unpack(acc[1], a2, a3);
-          sum = (a0 + a1) + (a2 + a3);
-          const float m_new = mx * sl2;
-          const bool need = m_new > m_used + kRescaleThreshold;
-          again = __any_sync(0xffffffffu, need);
-          if (again) {
-            const float factor = need ? ex2f(m_used - m_new) : 1.0f;
-            if (j > lo) {
-#pragma unroll 1
-              for (int c4 = 0; c4 < 4; ++c4) {
-                float ov[32];
-                uint32_t part[32];
-                tmem_ld32(tO + c4 * 32, ov);
+            for (int c2 = 0; c2 < 2; ++c2) {
+              float ov[32];
+              uint32_t part[32];
+              tmem_ld32(tO + c2 * 32, ov);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) part[c] = __float_as_uint(ov[c] * factor);
-                tmem_st32(tO + c4 * 32, part);
-              }
+              for (int c = 0; c < 32; ++c) part[c] = __float_as_uint(ov[c] * factor);
+              tmem_st32(tO + c2 * 32, part);
             }
-            if (need) {
+            if (up) {
               l *= factor;
               m_used = m_new;
             }
+            half_exp(diag, m_used, pk, sum);
           }
         }
         l += sum;
-        // P over S's first 64 columns; the next S MMA into this buffer is
-        // issued after the PV MMA that reads P, and tensor-core MMAs of one
-        // CTA execute in issue order.
+        // P over this half's first 32 columns (already read); the next S MMA
+        // into S_x is issued after the PV MMA that reads P.
         tmem_st32_nowait(tS, pk);
-        tmem_st32_nowait(tS + 32, pk + 32);
         tmem_wait_st();
         tc_fence_before();
         hand_off(j);
       }
+      // the row sum over both halves (both warps of the pair take part whatever happened)
+      if (lo < hi) {
+        float* slot = lx + x * 128 + row;
+        if (hf == 1) *slot = l;
+        named_bar_sync(pbar, 64);
+        if (hf == 0) {
+          l += *slot;
+          *slot = l;
+        }
+        named_bar_sync(pbar, 64);
+        if (hf == 1) l = *slot;
+      }
       if (!alive) continue;
       const int64_t zrow = (x ? g.zrow[1] : g.zrow[0]) + row;
       if constexpr (SPLIT) {
-        // unnormalised O and (max, sum) of this part; a tile with no key tile in it adds nothing
-        float4* po = reinterpret_cast<float4*>(p.part_o + (((int64_t)sp * p.part_rows + zrow) * p.H + head) * HD);
+        float4* po =
+            reinterpret_cast<float4*>(p.part_o + (((int64_t)sp * p.part_rows + zrow) * p.H + head) * HD + 64 * hf);
         const int64_t mli = ((int64_t)sp * p.part_rows + zrow) * p.H + head;
         if (lo >= hi) {
 #pragma unroll 4
-          for (int q = 0; q < HD / 4; ++q) po[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          p.part_ml[mli] = make_float2(-INFINITY, 0.f);
+          for (int q = 0; q < 16; ++q) po[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (hf == 0) p.part_ml[mli] = make_float2(-INFINITY, 0.f);
           continue;
         }
         const bool got = mbar_wait(&o_done[x], ocnt & 1, abort_flag, p.err, code | 9);
@@ -537,13 +639,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!alive) continue;
         tc_fence_after();
 #pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c2 = 0; c2 < 2; ++c2) {
           float ov[32];
-          tmem_ld32(tO + c4 * 32, ov);
+          tmem_ld32(tO + c2 * 32, ov);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) po[c4 * 8 + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+          for (int q = 0; q < 8; ++q) po[c2 * 8 + q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
         }
-        p.part_ml[mli] = make_float2(m_used, l);
+        if (hf == 0) p.part_ml[mli] = make_float2(m_used, l);
         tc_fence_before();
         continue;
       }
@@ -552,18 +654,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       alive = __all_sync(0xffffffffu, got);
       if (!alive) continue;
       tc_fence_after();
-      uint32_t orr[128];
-      tmem_ld128(tO, orr);
+      uint32_t orr[64];
+      tmem_ld64_issue(tO, orr);
+      tmem_wait_ld64(orr);
       const float inv = 1.0f / l;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + zrow * p.h + head * HD);
+      uint4* dst = reinterpret_cast<uint4*>(p.o + zrow * p.h + head * HD + 64 * hf);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < 8; ++q) {
         dst[q] = make_uint4(pack_bf16x2(__uint_as_float(orr[q * 8 + 0]) * inv, __uint_as_float(orr[q * 8 + 1]) * inv),
                             pack_bf16x2(__uint_as_float(orr[q * 8 + 2]) * inv, __uint_as_float(orr[q * 8 + 3]) * inv),
                             pack_bf16x2(__uint_as_float(orr[q * 8 + 4]) * inv, __uint_as_float(orr[q * 8 + 5]) * inv),
                             pack_bf16x2(__uint_as_float(orr[q * 8 + 6]) * inv, __uint_as_float(orr[q * 8 + 7]) * inv));
       }
-      if (p.lse)
+      if (p.lse && hf == 0)
         p.lse[((int64_t)b * p.H + head) * p.S + (x ? g.p0[1] : g.p0[0]) + row] = (m_used + __log2f(l)) * kLn2;
       tc_fence_before();
     }
@@ -571,7 +674,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
