@@ -570,57 +570,53 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr uint32_t id_q = idesc_bf16_f32(HD, QBF, true, true);     // M = head dim, N = queries (A, B MN-major)
     uint32_t qi = 0;
     bool ok = true;  // warp-uniform
-    auto stage = [&](uint32_t n) { return stg + (n % NSTGF) * STGF_BYTES; };
+    // Descriptor low words computed once (the issuing stream stays short;
+    // the elementwise warps' instructions on this sub-partition delay every
+    // MMA issue): K-major tiles for S^T and dP^T, MN-major for dV, dK, dQ^T.
+    // A stage adds s * (STGF_BYTES >> 4); K step k of a K-major [rows][128]
+    // tile in two 64-column sub-tiles adds (k / 4) * (sub-tile >> 4) + 2 (k % 4),
+    // of an MN-major tile 2048 k >> 4 = 128 k.
+    const uint32_t k_lo = sdesc_lo(smem_u32(Ks)), v_lo = sdesc_lo(smem_u32(Vs));
+    const uint32_t stg_lo = sdesc_lo(smem_u32(stg)), stg_mn = sdesc_mn_lo(smem_u32(stg), SUB64);
+    const uint32_t k_mn = sdesc_mn_lo(smem_u32(Ks), SUB128), ds_mn = sdesc_mn_lo(smem_u32(dSs), SUB128);
+    const uint32_t s_full_at = smem_u32(s_full), dp_full_at = smem_u32(dp_full), dq_full_at = smem_u32(dq_full);
+    const uint32_t q_free_at = smem_u32(q_free);  // stage s: + 8 s
+    auto stage_off = [](uint32_t n) { return (n % NSTGF) * (STGF_BYTES >> 4); };
+    auto kstep128 = [](int k) { return (uint32_t)((k / 4) * (SUB128 >> 4) + 2 * (k % 4)); };
+    auto kstep64 = [](int k) { return (uint32_t)((k / 4) * (SUB64 >> 4) + 2 * (k % 4)); };
     auto scores = [&](uint32_t n) {  // S^T = K Q^T
-      uint8_t* st = stage(n);
+      const uint32_t q = stg_lo + stage_off(n);
 #pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint64_t ak = sdesc_kmajor_sw128(smem_u32(Ks + (k / 4) * SUB128)) + 2 * (k % 4);
-        const uint64_t bq = sdesc_kmajor_sw128(smem_u32(st + (k / 4) * SUB64)) + 2 * (k % 4);
-        umma_bf16_warp(tmem_base, ak, bq, id_s, k > 0);
-      }
-      umma_commit_warp(s_full);
+      for (int k = 0; k < HD / 16; ++k) mma_ss_lo(tmem_base, k_lo + kstep128(k), q + kstep64(k), id_s, k > 0);
+      commit_to(s_full_at);
     };
     auto dpscores = [&](uint32_t n) {  // dP^T = V dO^T
-      uint8_t* st = stage(n);
+      const uint32_t o = stg_lo + stage_off(n) + ((2 * SUB64) >> 4);
 #pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint64_t av = sdesc_kmajor_sw128(smem_u32(Vs + (k / 4) * SUB128)) + 2 * (k % 4);
-        const uint64_t bo = sdesc_kmajor_sw128(smem_u32(st + 2 * SUB64 + (k / 4) * SUB64)) + 2 * (k % 4);
-        umma_bf16_warp(tmem_base + 64, av, bo, id_s, k > 0);
-      }
-      umma_commit_warp(dp_full);
+      for (int k = 0; k < HD / 16; ++k) mma_ss_lo(tmem_base + 64, v_lo + kstep128(k), o + kstep64(k), id_s, k > 0);
+      commit_to(dp_full_at);
     };
     // dV += P^T dO and dK += dS^T Q: the stage's dO / Q tiles as MN-major B
     // operands (rows = queries = K dimension; 64-column chunks SUB64 apart).
     // P^T of queries 32x..32x+31 sits in columns 32x..32x+15 of the S^T region;
     // dS^T is packed contiguously (queries 2c, 2c+1 in column 192 + c).
     auto accum_v = [&](uint32_t n, bool acc) {
-      uint8_t* st = stage(n);
+      const uint32_t o = stg_mn + stage_off(n) + ((2 * SUB64) >> 4);
 #pragma unroll
-      for (int k = 0; k < QBF / 16; ++k) {
-        const uint64_t bo = sdesc_mn_sw128(smem_u32(st + 2 * SUB64) + 2048 * k, SUB64);
-        umma_bf16_ts_warp(tmem_base + 256, tmem_base + 32 * (k / 2) + 8 * (k % 2), bo, id_o,
-                          (acc || k > 0) ? 1u : 0u);
-      }
+      for (int k = 0; k < QBF / 16; ++k)
+        mma_ts_lo(tmem_base + 256, tmem_base + 32 * (k / 2) + 8 * (k % 2), o + 128 * k, id_o, (acc || k > 0) ? 1u : 0u);
     };
     auto accum_kq = [&](uint32_t n, bool acc) {
-      uint8_t* st = stage(n);
+      const uint32_t q = stg_mn + stage_off(n);
 #pragma unroll
-      for (int k = 0; k < QBF / 16; ++k) {
-        const uint64_t bq = sdesc_mn_sw128(smem_u32(st) + 2048 * k, SUB64);
-        umma_bf16_ts_warp(tmem_base + 384, tmem_base + 192 + 8 * k, bq, id_o, (acc || k > 0) ? 1u : 0u);
-      }
+      for (int k = 0; k < QBF / 16; ++k)
+        mma_ts_lo(tmem_base + 384, tmem_base + 192 + 8 * k, q + 128 * k, id_o, (acc || k > 0) ? 1u : 0u);
       // dQ^T = K^T dS^T: the K tile (rows = keys, head-dim chunks SUB128 apart) as
       // the MN-major A operand, dS^T (rows = keys, 64 queries) as the MN-major B
 #pragma unroll
-      for (int k = 0; k < 128 / 16; ++k) {
-        const uint64_t ak = sdesc_mn_sw128(smem_u32(Ks) + 2048 * k, SUB128);
-        const uint64_t bs = sdesc_mn_sw128(smem_u32(dSs) + 2048 * k, SUB128);
-        umma_bf16_warp(tmem_base + 128, ak, bs, id_q, k > 0);
-      }
-      umma_commit_warp(dq_full);
-      umma_commit_warp(&q_free[n % NSTGF]);
+      for (int k = 0; k < 128 / 16; ++k) mma_ss_lo(tmem_base + 128, k_mn + 128 * k, ds_mn + 128 * k, id_q, k > 0);
+      commit_to(dq_full_at);
+      commit_to(q_free_at + 8 * (n % NSTGF));
     };
     auto sync_on = [&](int id, int count) {
       __syncwarp();
@@ -686,6 +682,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t cdQ = tmem_base + lane_off + 128 + 32 * half;
     const uint32_t cdS = tmem_base + lane_off + 192 + 16 * half;
     const float sl2 = kLog2e * rsqrtf((float)HD);
+    const uint64_t sl2x2 = f2pack(sl2, sl2), nlog2e2 = f2pack(-kLog2e, -kLog2e);
     const float scale = rsqrtf((float)HD);
     uint8_t* ds_row = dSs + row * 128;
     uint32_t cnt = 0;   // blocks processed (phase of s_full / dp_full; ring slot = cnt % NSTGF)
@@ -717,23 +714,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float4* lse4 = reinterpret_cast<const float4*>(ldr + (cnt % NSTGF) * LDF_BYTES) + 8 * half;
         const float4* ds4 = lse4 + QBF / 4;
         const bool diag = i < 2;  // the two blocks that overlap the key tile
-        float pv[32];
+        // P = 2^(s sl2 - lse log2e) in packed pairs (one f32x2 multiply and
+        // one f32x2 FMA per two scores)
+        uint64_t pv2[16];
+        uint32_t pk[16];
         tmem_wait_ld32(sa);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 l4 = lse4[c4];
-          const float lv[4] = {l4.x * kLog2e, l4.y * kLog2e, l4.z * kLog2e, l4.w * kLog2e};
+          float a[4];
+          f2unpack(f2fma(f2pack(__uint_as_float(sa[4 * c4]), __uint_as_float(sa[4 * c4 + 1])), sl2x2,
+                         f2mul(f2pack(l4.x, l4.y), nlog2e2)),
+                   a[0], a[1]);
+          f2unpack(f2fma(f2pack(__uint_as_float(sa[4 * c4 + 2]), __uint_as_float(sa[4 * c4 + 3])), sl2x2,
+                         f2mul(f2pack(l4.z, l4.w), nlog2e2)),
+                   a[2], a[3]);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int c = c4 * 4 + e;
-            float pe = ex2f(fmaf(__uint_as_float(sa[c]), sl2, -lv[e]));
-            if (diag && q0 + c < key) pe = 0.f;
-            pv[c] = pe;
+            a[e] = ex2f(a[e]);
+            if (diag && q0 + 4 * c4 + e < key) a[e] = 0.f;
           }
+          pv2[2 * c4] = f2pack(a[0], a[1]);
+          pv2[2 * c4 + 1] = f2pack(a[2], a[3]);
+          pk[2 * c4] = pack_bf16x2(a[0], a[1]);
+          pk[2 * c4 + 1] = pack_bf16x2(a[2], a[3]);
         }
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
         tmem_st16_nowait(cS, pk);  // P^T over the start of this thread's S^T columns
         tmem_wait_st();
         tc_fence_before();
@@ -749,18 +754,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         tmem_ld32_issue(cdP, sa);
         tmem_wait_ld32(sa);
+        // dS = P (dP - dsum) in packed pairs
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = ds4[c4];
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c4 * 4 + e;
-            pv[c] = pv[c] * (__uint_as_float(sa[c]) - dv[e]);
-          }
+          float g[4];
+          f2unpack(f2mul(pv2[2 * c4], f2sub(f2pack(__uint_as_float(sa[4 * c4]), __uint_as_float(sa[4 * c4 + 1])),
+                                            f2pack(d4.x, d4.y))),
+                   g[0], g[1]);
+          f2unpack(f2mul(pv2[2 * c4 + 1], f2sub(f2pack(__uint_as_float(sa[4 * c4 + 2]), __uint_as_float(sa[4 * c4 + 3])),
+                                                f2pack(d4.z, d4.w))),
+                   g[2], g[3]);
+          pk[2 * c4] = pack_bf16x2(g[0], g[1]);
+          pk[2 * c4 + 1] = pack_bf16x2(g[2], g[3]);
         }
-#pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
         // dK(n-1) and dQ(n-1) must be done with dS^T(n-1) before it is overwritten
         float qa[32];
         if (dq_prev != nullptr) {

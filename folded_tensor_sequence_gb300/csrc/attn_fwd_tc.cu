@@ -101,26 +101,6 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// ---- packed fp32 pairs (f32x2 instructions) -----------------------------------
-__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -174,55 +154,9 @@ __device__ __forceinline__ float max16(const uint32_t (&h)[16], float m) {
   const float a4 = fmax3(__uint_as_float(h[12]), __uint_as_float(h[13]), __uint_as_float(h[14]));
   return fmax3(fmax3(a0, a1, a2), fmax3(a3, a4, __uint_as_float(h[15])), m);
 }
-// The two 32-bit words of a K-major 128-byte-swizzle descriptor (as
-// sdesc_kmajor_sw128 builds it): the high word is the same for every tile, the
-// low word is the start address >> 4 plus the leading-byte-offset field.
-// Advancing K by 16 elements adds 2 (32 bytes) within a 64-element sub-tile
-// and SUB_BYTES >> 4 between the two sub-tiles; no carry leaves the 14-bit
-// address field for any shared-memory address.
-constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
-__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+// Low-word offset of the K step k (16 elements) in a [128][128] tile of two
+// 64-column sub-tiles: 2 (32 bytes) within a sub-tile, SUB_BYTES >> 4 between them.
 __host__ __device__ constexpr uint32_t kstep_lo(int k) { return (k / 4) * (SUB_BYTES >> 4) + 2 * (k % 4); }
-
-// Warp-collective MMAs (one elected lane issues) from descriptor low words:
-// A and B from shared memory, or A from tensor memory.
-__device__ __forceinline__ void mma_ss_lo(uint32_t d, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n"
-      ".reg .b64 ad, bd;\n"
-      ".reg .pred p, e;\n"
-      "mov.b64 ad, {%1, %5};\n"
-      "mov.b64 bd, {%2, %5};\n"
-      "elect.sync _|e, 0xffffffff;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n"
-      "}\n" ::"r"(d),
-      "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi)
-      : "memory");
-}
-__device__ __forceinline__ void mma_ts_lo(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n"
-      ".reg .b64 bd;\n"
-      ".reg .pred p, e;\n"
-      "mov.b64 bd, {%2, %5};\n"
-      "elect.sync _|e, 0xffffffff;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n"
-      "}\n" ::"r"(d),
-      "r"(a_tmem), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi)
-      : "memory");
-}
-// Warp-collective commit to the mbarrier at shared address `bar`.
-__device__ __forceinline__ void commit_to(uint32_t bar) {
-  asm volatile(
-      "{\n"
-      ".reg .pred e;\n"
-      "elect.sync _|e, 0xffffffff;\n"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
-      "}\n" ::"r"(bar)
-      : "memory");
-}
 
 struct BlockGeo {
   int64_t zrow[2];  // row of Q / O holding tile x's first query

@@ -54,6 +54,40 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
+// Packed fp32 pairs (f32x2 instructions: one issue for two lanes' worth of
+// arithmetic)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -271,6 +305,62 @@ __device__ __forceinline__ void umma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tm
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The two 32-bit words of a 128-byte-swizzle descriptor (as
+// sdesc_kmajor_sw128 / sdesc_mn_sw128 build them): the high word (stride byte
+// offset 1024, version 1, swizzle mode) is the same for every tile; the low
+// word is the start address >> 4 plus the leading-byte-offset field.  Moving
+// the start address by a few KB only adds to the low word: the 14-bit address
+// field cannot carry for any shared-memory address.  Kernels that issue many
+// MMAs per step keep low words precomputed, which keeps the issuing warp's
+// instruction stream short.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+// MN-major tile whose 64-element MN chunks are mn_chunk_bytes apart (the
+// leading byte offset).
+__device__ __forceinline__ uint32_t sdesc_mn_lo(uint32_t saddr, uint32_t mn_chunk_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | ((mn_chunk_bytes >> 4) << 16);
+}
+
+// Warp-collective MMAs (one elected lane issues) from descriptor low words:
+// A and B from shared memory, or A from tensor memory.
+__device__ __forceinline__ void mma_ss_lo(uint32_t d, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n"
+      ".reg .b64 ad, bd;\n"
+      ".reg .pred p, e;\n"
+      "mov.b64 ad, {%1, %5};\n"
+      "mov.b64 bd, {%2, %5};\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n"
+      "}\n" ::"r"(d),
+      "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_lo(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n"
+      ".reg .b64 bd;\n"
+      ".reg .pred p, e;\n"
+      "mov.b64 bd, {%2, %5};\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n"
+      "}\n" ::"r"(d),
+      "r"(a_tmem), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi)
+      : "memory");
+}
+// Warp-collective commit to the mbarrier at shared address `bar`.
+__device__ __forceinline__ void commit_to(uint32_t bar) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05.mma the electing lane issued so far has completed.
 __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
   asm volatile(
