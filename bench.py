@@ -53,15 +53,15 @@ NCU_TRAFFIC = {
     ("gate/up projection", "bf16_gqa8_D8_b2_s16384_h4096"):
         (2162.50e6 + 928.24e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "f1fbc4e5fcda0324"),
     ("attention", "bf16_D8_b2_s16384_h4096"):
-        (849.534e6 + 254.581e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "f3ebf6c44e68df52"),
+        (841.452e6 + 256.905e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "7ed87788d4fc8471"),
     ("attention", "bf16_D8_b1_s65536_h4096"):
-        (2152.43e6 + 536.669e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "f3ebf6c44e68df52"),
+        (2192.78e6 + 551.372e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "7ed87788d4fc8471"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
-        (1.64e9 + 1.04e9, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
+        (1647.83e6 + 1044.21e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "11a1e0ec7314427b"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b1_s8192_h4096"):
-        (407.27e6 + 221.83e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
+        (408.127e6 + 222.500e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "11a1e0ec7314427b"),
     ("attention bwd fused", "bf16_fwdbwd_gqa8_D8_b1_s8192_h4096"):
-        (652.95e6 + 290.93e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "d4b28b5bd4c6d69e"),
+        (634.187e6 + 291.365e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "11a1e0ec7314427b"),
     ("kv gather (standalone)", "bf16_D8_b2_s16384_h4096"):
         (536.906e6 + 485.511e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "b3e6ab7624313095"),
     ("zigzag permute (standalone)", "bf16_D8_b2_s16384_h4096"):
