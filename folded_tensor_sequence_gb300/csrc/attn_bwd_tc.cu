@@ -22,6 +22,8 @@
 // each query block come in with the stage by bulk copy (dK/dV) or are read
 // once per tile (dQ).  Warp 8 issues TMA, warp 9 issues tcgen05.mma from one
 // thread, warp 10 relays landed stages to warp 9.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -719,26 +721,36 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint64_t pv2[16];
         uint32_t pk[16];
         tmem_wait_ld32(sa);
+        // The causal mask only touches the two blocks that overlap the key
+        // tile; the others take the loop without the per-score test (a
+        // warp-uniform branch, so it is not turned into selects).
+        auto p_phase = [&](auto masked) {
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = lse4[c4];
-          float a[4];
-          f2unpack(f2fma(f2pack(__uint_as_float(sa[4 * c4]), __uint_as_float(sa[4 * c4 + 1])), sl2x2,
-                         f2mul(f2pack(l4.x, l4.y), nlog2e2)),
-                   a[0], a[1]);
-          f2unpack(f2fma(f2pack(__uint_as_float(sa[4 * c4 + 2]), __uint_as_float(sa[4 * c4 + 3])), sl2x2,
-                         f2mul(f2pack(l4.z, l4.w), nlog2e2)),
-                   a[2], a[3]);
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 l4 = lse4[c4];
+            float a[4];
+            f2unpack(f2fma(f2pack(__uint_as_float(sa[4 * c4]), __uint_as_float(sa[4 * c4 + 1])), sl2x2,
+                           f2mul(f2pack(l4.x, l4.y), nlog2e2)),
+                     a[0], a[1]);
+            f2unpack(f2fma(f2pack(__uint_as_float(sa[4 * c4 + 2]), __uint_as_float(sa[4 * c4 + 3])), sl2x2,
+                           f2mul(f2pack(l4.z, l4.w), nlog2e2)),
+                     a[2], a[3]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            a[e] = ex2f(a[e]);
-            if (diag && q0 + 4 * c4 + e < key) a[e] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+              a[e] = ex2f(a[e]);
+              if constexpr (decltype(masked)::value)
+                if (q0 + 4 * c4 + e < key) a[e] = 0.f;
+            }
+            pv2[2 * c4] = f2pack(a[0], a[1]);
+            pv2[2 * c4 + 1] = f2pack(a[2], a[3]);
+            pk[2 * c4] = pack_bf16x2(a[0], a[1]);
+            pk[2 * c4 + 1] = pack_bf16x2(a[2], a[3]);
           }
-          pv2[2 * c4] = f2pack(a[0], a[1]);
-          pv2[2 * c4 + 1] = f2pack(a[2], a[3]);
-          pk[2 * c4] = pack_bf16x2(a[0], a[1]);
-          pk[2 * c4 + 1] = pack_bf16x2(a[2], a[3]);
-        }
+        };
+        if (diag)
+          p_phase(std::true_type{});
+        else
+          p_phase(std::false_type{});
         tmem_st16_nowait(cS, pk);  // P^T over the start of this thread's S^T columns
         tmem_wait_st();
         tc_fence_before();
