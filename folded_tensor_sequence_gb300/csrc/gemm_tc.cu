@@ -68,17 +68,32 @@ static_assert(smem_bytes<EPI_DSWIGLU>() <= 227 * 1024 && smem_bytes<EPI_SWIGLU>(
               "shared memory");
 // Raster: tiles are visited in bands of group_m m-tiles (all n-tiles of a band
 // before the next band), group_m chosen so one band of A is ~32 MB and stays
-// in L2 while the B operand streams past it.
+// in L2 while the B operand streams past it; or, when B is the smaller
+// operand (N < M), in bands of group_n n-tiles (kBBandTiles, at most
+// kBBandBytes of B) that stay in L2 while A streams past them.
 constexpr size_t kBandBytes = size_t(32) << 20;
+constexpr size_t kBBandBytes = size_t(64) << 20;
+constexpr int kBBandTiles = 16;
 constexpr uint32_t TMEM_COLS = 512;
 
 struct GemmShape {
   int M, N, K;
   int num_m, num_n, num_tiles, kblocks;
-  int group_m;
+  int group_m;  // > 0: bands of group_m m-tiles (A resident, B streams)
+  int group_n;  // > 0: bands of group_n n-tiles (B resident, A streams)
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmShape& s, int& mt, int& nt) {
+  if (s.group_n > 0) {
+    const int per_group = s.group_n * s.num_m;
+    const int group = t / per_group;
+    const int first_n = group * s.group_n;
+    const int gsz = min(s.num_n - first_n, s.group_n);
+    const int in_g = t - group * per_group;
+    nt = first_n + in_g % gsz;
+    mt = in_g / gsz;
+    return;
+  }
   const int per_group = s.group_m * s.num_n;
   const int group = t / per_group;
   const int first_m = group * s.group_m;
@@ -769,6 +784,20 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
     const size_t band_rows = kBandBytes / ((size_t)K * 2);
     int gm = (int)(band_rows / BM);
     s.group_m = gm < 1 ? 1 : (gm > s.num_m ? s.num_m : gm);
+    s.group_n = 0;
+    if (N < M) {
+      // B is the smaller operand: bands of 16 of B's n-tiles (at most 64 MB)
+      // stay in L2 while A streams past them.  Measured at 2 x 16K tokens:
+      // gate/up, QKV and output projection 2-4 % faster than with A bands,
+      // and the down projection (K = 14336, 8 n-tiles per band) reads 3.9 GB
+      // from DRAM instead of 5.2 (its 117 MB weight was re-read every wave).
+      // Larger B bands (64, 96 MB of gate/up's B) and L2 eviction hints on
+      // the streaming operand were slower.
+      const size_t band_cols = kBBandBytes / ((size_t)K * 2);
+      int gn = (int)(band_cols / BN);
+      gn = gn > kBBandTiles ? kBBandTiles : gn;
+      s.group_n = gn < 1 ? 1 : (gn > s.num_n ? s.num_n : gn);
+    }
   }
   cudaError_t e;
   const int mode = (a_mn ? 2 : 0) | (b_mn ? 1 : 0);
