@@ -144,3 +144,56 @@ def test_outputs_agree_across_D(tsp):
         ys[D] = y
     for D in (2, 4, 8):
         assert rel_frob(ys[D], ys[1]) <= 2e-2
+
+
+def test_attention_rescale_path_matches_oracle(tsp):
+    """Scores that grow along the sequence, so that a row's maximum rises above its first key
+    tile's by more than 2^8 (8 in log2 units): the tcgen05 softmax then leaves its common path
+    (the two half-row warps vote on their pair barrier, read the row's maximum, rescale O in
+    tensor memory and recompute P).  Built from the seeded inputs: x becomes x / 2 + c(p) u with u a
+    fixed unit vector and c rising from -8 to 8 along the sequence, and W_K = W_Q, so every score
+    gains c(i) c(j) |u W_Q|^2 / sqrt(dh): late keys win the late rows, early keys lose them (and
+    the scores stay below 8, where the bf16 comparison is as tight as in the other tests)."""
+    import torch
+
+    cfg = LayerConfig("bf16_rescale_D2_s1024", D=2, batch=1, seq=1024, hidden=256, heads=2, head_dim=128,
+                      ffn=512, dtype="bf16")
+    inp = dict(synth.layer_inputs(cfg, seed=5))
+    S, h, dh = cfg.seq, cfg.hidden, cfg.head_dim
+    u = np.ones(h) / np.sqrt(h)
+    c = 8.0 * (2.0 * np.arange(S) / (S - 1) - 1.0)
+    inp["x"] = synth.round_bf16(0.5 * inp["x"] + c[None, :, None] * u[None, None, :])
+    inp["Wk"] = inp["Wq"].copy()
+    # the precondition, from fp64 scores: many rows' running max grows by > 8 (log2) after key tile 0
+    x0 = inp["x"][0]
+    Qm, Km = x0 @ inp["Wq"], x0 @ inp["Wk"]
+    causal = np.tril(np.ones((S, S), dtype=bool))
+    smax = 0.0
+    for hd in range(cfg.heads):
+        sl = slice(hd * dh, (hd + 1) * dh)
+        s = (Qm[:, sl] @ Km[:, sl].T) / np.sqrt(dh)
+        smax = max(smax, float(np.max(np.abs(s[causal]))))
+        s2 = np.where(causal, s * np.log2(np.e), -np.inf)
+        first, later = s2[:, :128].max(axis=1), s2[:, 128:].max(axis=1)
+        assert int(np.sum(later > first + 8)) >= 64, "too few rows take the rescale path"
+    plan, packed, x, _ = setup(tsp, cfg, inp=inp)
+    w = {k: inp[k] for k in tsp.CANONICAL}
+    ref = O.layer_fwd(inp["x"], w, cfg.heads)
+    B = cfg.batch
+    xz = guarded_like(x)
+    tsp.tsp_zigzag_permute(plan, B, x, xz.t)
+    a = guarded_like(x)
+    lse = Guarded((B, cfg.heads, cfg.seq), torch.float32)
+    wa = guarded_workspace(tsp, plan, B, tsp.TSP_OP_ATTENTION_FWD)
+    tsp.tsp_attention_fwd(plan, B, xz.t, packed, a.t, lse.t, wa.t)
+    tsp.tsp_sync_check()
+    for g, what in ((a, "a_out"), (lse, "lse"), (wa, "attention workspace")):
+        g.check(f"{cfg.name} {what}")
+    a_nat = O.zigzag_unpermute(to_np(a.t).reshape(cfg.D, B, -1, cfg.hidden), cfg.D)
+    check(a_nat, ref["A"], "bf16", f"{cfg.name} A")
+    # Q and K are rounded to bf16 on the GPU (2^-8 relative each), so a score of size |s| moves by
+    # up to about 2^-7 |s|, and the log-sum-exp by at most the largest such move
+    assert smax < 8.0
+    err = float(np.max(np.abs(to_np(lse.t) - ref["lse"])))
+    print(f"PARITY {cfg.name} lse: max abs {err:.3e} (largest |score| {smax:.2f})")
+    assert err <= 2 ** -7 * smax + 1e-2
