@@ -36,6 +36,11 @@
 // when it grows by more than 2^8, which keeps P <= 256 and makes the rescale
 // rare; the test for it is the half-row's sum of P, not a max.
 //
+// Without the key split the CTAs are persistent (one per SM, units taken
+// round-robin): the next block's Q tiles load as soon as a block's last S MMA
+// is done, and TMEM allocation and barrier set-up happen once per CTA (8K
+// tokens: 0.409 -> 0.403 ms; no change at 2 x 16K tokens).
+//
 // Why two warps per row and no per-tile max: the MMA warp shares its SM
 // sub-partition with softmax warps, and every softmax instruction issued
 // there delays its MMA issue (measured: a key-tile step takes 2230 cycles
@@ -80,6 +85,11 @@ struct FaParams {
   int64_t S, C;
   int h;
   int g_off;        // first light block of the grid (rank * nb when one rank's queries run)
+  // Without the key split the CTAs are persistent: CTA c takes units c, c +
+  // gridDim.x, ... of the npairs * H * B units (mirror pair u % npairs, head
+  // (u / npairs) % H, batch u / (npairs * H)).
+  int npairs;
+  int nunits;
   int64_t row_off;  // zigzag row held by row 0 of Q and O (rank * B * 2C likewise)
   // Key split: nsplit CTAs share a mirror pair, part sp taking key tiles
   // [n*sp/nsplit, n*(sp+1)/nsplit) of each block (n = the block's tile-B key
@@ -202,8 +212,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* Qs = smem;                                   // [2 tiles], block 0 then block 1
   uint8_t* KVs = smem + 2 * TILE_BYTES;                 // [STAGES] tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + STAGES) * TILE_BYTES);
-  uint64_t* q_full = bars + 0;              // [2] one per block
-  uint64_t* q_empty = bars + 2;             // block 0's Q tiles no longer read
+  uint64_t* q_full = bars + 0;              // a block's Q tiles landed (one phase per block)
+  uint64_t* q_empty = bars + 2;             // a block's last S MMA done: the Q buffer may be refilled
   uint64_t* kv_full = bars + 3;             // [STAGES]
   uint64_t* kv_empty = kv_full + STAGES;    // [STAGES]
   uint64_t* s_full = kv_empty + STAGES;     // [2]
@@ -214,11 +224,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   float* lx = reinterpret_cast<float*>(smem + (2 + STAGES) * TILE_BYTES + 256);  // [2 tiles][128 rows]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int head = blockIdx.y, b = blockIdx.z;
-  // light block (or tile) of the CTA's mirror pair; with two blocks the heavy one goes first
   const int nsplit = SPLIT ? p.nsplit : 1;
-  const int light = p.g_off + (int)blockIdx.x / nsplit;
   const int sp = SPLIT ? (int)blockIdx.x % nsplit : 0;  // part of the key range (key split)
+  // The CTA's units: with the key split, the one of its grid position;
+  // otherwise (persistent) u = blockIdx.x, blockIdx.x + gridDim.x, ...  A unit
+  // is (light block or tile of a mirror pair, head, batch); with two blocks the
+  // heavy one goes first.
+  const int u_first = SPLIT ? 0 : (int)blockIdx.x;
+  const int u_end = SPLIT ? 1 : p.nunits;
+  const int u_step = SPLIT ? 1 : (int)gridDim.x;
+  auto unit_of = [&](int u, int& light, int& head, int& b) {
+    if constexpr (SPLIT) {
+      head = (int)blockIdx.y;
+      b = (int)blockIdx.z;
+      light = p.g_off + (int)blockIdx.x / nsplit;
+    } else {
+      head = (u / p.npairs) % p.H;
+      b = u / (p.npairs * p.H);
+      light = p.g_off + u % p.npairs;
+    }
+  };
   // key tiles [lo, hiB) of this part of a block; tile A takes [lo, hiA), empty if hiA <= lo
   auto key_part = [&](const BlockGeo& g, int& lo, int& hiA, int& hiB) {
     if constexpr (SPLIT) {
@@ -233,8 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   };
 
   if (threadIdx.x == 0) {
-    mbar_init(&q_full[0], 1);
-    mbar_init(&q_full[1], 1);
+    mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -266,21 +290,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == kTmaWarp) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
+      uint32_t item = 0, kb = 0;  // K/V tiles and blocks loaded so far
+      bool ok = true;
+      for (int u = u_first; u < u_end && ok; u += u_step) {
+      int light, head, b;
+      unit_of(u, light, head, b);
       const int kvh = head / (p.H / p.Hk);                        // the K/V head this query head reads
       const int64_t kv_row0 = ((int64_t)b * p.Hk + kvh) * p.S;   // K rows of that head
       const int64_t vt_row0 = ((int64_t)b * p.Hk + kvh) * HD;    // V^T rows of that head
-      uint32_t item = 0;
-      bool ok = true;
-      int q_loaded = 0;
-      for (int blk = 0; blk < p.nblk && ok; ++blk) {
+      for (int blk = 0; blk < p.nblk && ok; ++blk, ++kb) {
         const BlockGeo g = block_geo(blk, light, p, b);
-        // block 1's query tiles go into block 0's buffer once its last S MMA is done
-        if (blk == 1 && !mbar_wait(q_empty, 0, abort_flag, p.err, code | 1)) break;
-        mbar_arrive_expect_tx(&q_full[blk], 2 * TILE_BYTES);
-        ++q_loaded;
+        // a block's query tiles go into the buffer once the previous block's last S MMA is done
+        if (kb > 0 && !mbar_wait(q_empty, (kb - 1) & 1, abort_flag, p.err, code | 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
         for (int x = 0; x < 2; ++x)
           for (int c = 0; c < 2; ++c)
-            tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)g.zrow[x], &q_full[blk]);
+            tma_load_2d(Qs + x * TILE_BYTES + c * SUB_BYTES, &tmQ, head * HD + c * 64, (int)g.zrow[x], q_full);
         int lo, hiA, hiB;
         key_part(g, lo, hiA, hiB);
         for (int j = lo; j < hiB && ok; ++j) {
@@ -302,11 +330,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // wait for the copies still in flight (bounded) before the CTA may exit
+      }
+      // wait for the copies still in flight (bounded) before the CTA may exit;
+      // a block's Q copies completed before any MMA of its could run, except
+      // possibly the last block's if the CTA gave up
       const uint32_t first = item > (uint32_t)STAGES ? item - STAGES : 0;
       volatile int dummy = 0;
       for (uint32_t n = first; n < item; ++n) mbar_wait(&kv_full[n % STAGES], (n / STAGES) & 1, &dummy, p.err, code | 3);
-      for (int q = 0; q < q_loaded; ++q) mbar_wait(&q_full[q], 0, &dummy, p.err, code | 3);
+      if (kb > 0) mbar_wait(q_full, (kb - 1) & 1, &dummy, p.err, code | 3);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
@@ -344,16 +375,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                   (acc || k > 0) ? 1u : 0u);
       }
     };
-    for (int blk = 0; blk < p.nblk; ++blk) {
+    const uint32_t q_empty_at = smem_u32(q_empty);
+    uint32_t kb = 0;  // blocks so far (phase of q_full)
+    for (int u = u_first; u < u_end; u += u_step) {
+    int light, head, b;
+    unit_of(u, light, head, b);
+    for (int blk = 0; blk < p.nblk; ++blk, ++kb) {
       const BlockGeo g = block_geo(blk, light, p, b);
       int lo, nA, nB;  // this part's key tiles: [lo, nB) for tile B, [lo, nA) for tile A (possibly none)
       key_part(g, lo, nA, nB);
       const bool actA = lo < nA;
+      // another block follows in this CTA: its Q tiles may load once this
+      // block's last S MMA (tile B's, issued after tile A's) is done
+      const bool more = blk + 1 < p.nblk || u + u_step < u_end;
       const uint32_t base = item - 2 * lo;  // K_j = base + 2j, V_j = base + 2j + 1
       if (ok) {
         bool w = true;
         if (lane == 0)
-          w = mbar_wait(&q_full[blk], 0, abort_flag, p.err, code | 6) &&
+          w = mbar_wait(q_full, kb & 1, abort_flag, p.err, code | 6) &&
               mbar_wait(&kv_full[item % STAGES], (item / STAGES) & 1, abort_flag, p.err, code | 4);
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       }
@@ -367,6 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_s(1, s0);
         commit_to(s_full_at + 8);
         commit_to(kv_empty_at + 8 * s0);
+        if (more && nB == lo + 1) commit_to(q_empty_at);
       }
       uint32_t sv = next_stage(s0);  // stage of V_j
       for (int j = lo; j < nB; ++j) {
@@ -395,6 +435,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_s(1, sk);
             commit_to(s_full_at + 8);
             commit_to(kv_empty_at + 8 * sk);
+            if (more && j + 2 == nB) commit_to(q_empty_at);
           } else {
             commit_to(o_done_at + 8);
           }
@@ -402,8 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         sv = next_stage(sk);
       }
       item = base + 2 * nB;
-      // the Q buffer is free for block 1 once every MMA issued so far is done
-      if (blk == 0 && p.nblk == 2 && ok) umma_commit_warp(q_empty);
+    }
     }
     umma_commit_warp(drain);
     if (lane == 0) {
@@ -470,6 +510,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       f2unpack(acc[1], a2, a3);
       sum = (a0 + a1) + (a2 + a3);
     };
+    for (int u = u_first; u < u_end; u += u_step) {
+    int light, head, b;
+    unit_of(u, light, head, b);
     for (int blk = 0; blk < p.nblk; ++blk) {
       const BlockGeo g = block_geo(blk, light, p, b);
       const int n = x ? g.n[1] : g.n[0];
@@ -604,6 +647,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         p.lse[((int64_t)b * p.H + head) * p.S + (x ? g.p0[1] : g.p0[0]) + row] = (m_used + __log2f(l)) * kLn2;
       tc_fence_before();
     }
+    }
   }
 
   tc_fence_before();
@@ -700,11 +744,16 @@ tsp_status attn_fwd_bf16_tc(const AttnParams& a, cudaStream_t stream) {
     p.part_o = static_cast<float*>(a.split_ws);
     p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(a.split_ws) + 2 * (size_t)T * a.H * HD * sizeof(float));
   }
-  dim3 grid(pairs * p.nsplit, a.H, a.B);
-  if (p.nsplit > 1)
-    attn_fwd_tc_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
-  else
-    attn_fwd_tc_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  p.npairs = pairs;
+  p.nunits = pairs * a.H * a.B;
+  if (p.nsplit > 1) {
+    attn_fwd_tc_kernel<true><<<dim3(pairs * p.nsplit, a.H, a.B), THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  } else {
+    // persistent: one CTA per SM walks the units (the next block's Q tiles
+    // load while a block finishes, and set-up is paid once per CTA)
+    const int sms = num_sms();
+    attn_fwd_tc_kernel<false><<<(unsigned)(p.nunits < sms ? p.nunits : sms), THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  }
   if (cudaGetLastError() != cudaSuccess) return TSP_ERR_CUDA;
   if (p.nsplit > 1) {
     const int64_t warps = T * a.H;
