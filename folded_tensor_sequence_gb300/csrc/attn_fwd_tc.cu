@@ -9,15 +9,15 @@
 // softmax as in FlashAttention / ring attention (r007 chapter, "Параллелизм по
 // контексту: Ring Attention против Ulysses").
 //
-// Work unit: a block of two 128-row query tiles A and B of one (batch,
-// head); only each tile's last key tile crosses the diagonal and is masked.
-// Chunks of whole 256-query blocks: a block is 256 consecutive queries (tile
-// A stops one key tile before B), and a CTA takes the mirror pair of blocks
-// (G, 2D*nb-1-G), which lie in chunks c and 2D-1-c of the same rank.  Chunks
-// of an odd number of 128-query tiles: a CTA's one block is the mirror pair
-// of tiles itself (tile A the light one in chunk c, tile B the heavy one in
-// chunk 2D-1-c); A runs out of key tiles first and B finishes alone.  Either
-// way every CTA does the same number of key tiles.
+// Block: two 128-row query tiles A and B of one (batch, head); only each
+// tile's last key tile crosses the diagonal and is masked.  Chunks of whole
+// 256-query blocks: a block is 256 consecutive queries (tile A stops one key
+// tile before B), and a work unit is the mirror pair of blocks (G,
+// 2D*nb-1-G), which lie in chunks c and 2D-1-c of the same rank.  Chunks of an
+// odd number of 128-query tiles: a unit's one block is the mirror pair of
+// tiles itself (tile A the light one in chunk c, tile B the heavy one in chunk
+// 2D-1-c); A runs out of key tiles first and B finishes alone.  Either way
+// every unit does the same number of key tiles.
 //
 // Per CTA: warp 16 issues TMA loads (a block's Q tiles, then K_j / V_j^T
 // tiles through a 5-stage ring), warp 17 issues tcgen05.mma from one thread,
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // The whole warp walks the schedule (named barriers are warp-aligned) and
     // issues through the warp-collective MMA helpers (one elected lane
     // issues).  Inside a block the warp never waits on an mbarrier: the
-    // softmax warpgroup that hands over P_x(j) has also checked that the K/V
+    // softmax warps that hand over P_x(j) have also checked that the K/V
     // tiles the following MMAs read have landed.
     constexpr uint32_t idesc = idesc_bf16_f32(QT, KT);
     uint32_t item = 0;
