@@ -48,20 +48,20 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # without its own capture, or a source changed since, reports null.
 NCU_TRAFFIC = {
     ("gate/up projection", "bf16_D8_b2_s16384_h4096"):
-        (2162.50e6 + 928.24e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "f1fbc4e5fcda0324"),
+        (2135.88e6 + 924.70e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "f28b3c78982f3cd7"),
     # the same launch (M, N, K and kernel) as the multi-head workload's gate/up projection
     ("gate/up projection", "bf16_gqa8_D8_b2_s16384_h4096"):
-        (2162.50e6 + 928.24e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "f1fbc4e5fcda0324"),
+        (2135.88e6 + 924.70e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "f28b3c78982f3cd7"),
     ("attention", "bf16_D8_b2_s16384_h4096"):
-        (841.452e6 + 256.905e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "7ed87788d4fc8471"),
+        (833.823e6 + 250.399e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "6c52c6aefe671f3b"),
     ("attention", "bf16_D8_b1_s65536_h4096"):
-        (2192.78e6 + 551.372e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "7ed87788d4fc8471"),
+        (2278.46e6 + 567.390e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "6c52c6aefe671f3b"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b2_s16384_h4096"):
-        (1647.83e6 + 1044.21e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "11a1e0ec7314427b"),
+        (1643.48e6 + 1040.48e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "908c433fee92d1ce"),
     ("attention bwd fused", "bf16_fwdbwd_D8_b1_s8192_h4096"):
-        (408.127e6 + 222.500e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "11a1e0ec7314427b"),
+        (406.761e6 + 222.230e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "908c433fee92d1ce"),
     ("attention bwd fused", "bf16_fwdbwd_gqa8_D8_b1_s8192_h4096"):
-        (634.187e6 + 291.365e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "11a1e0ec7314427b"),
+        (651.287e6 + 289.550e6, "folded_tensor_sequence_gb300/csrc/attn_bwd_tc.cu", "908c433fee92d1ce"),
     ("kv gather (standalone)", "bf16_D8_b2_s16384_h4096"):
         (536.906e6 + 485.511e6, "folded_tensor_sequence_gb300/csrc/layout.cu", "b3e6ab7624313095"),
     ("zigzag permute (standalone)", "bf16_D8_b2_s16384_h4096"):
