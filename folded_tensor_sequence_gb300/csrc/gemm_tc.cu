@@ -21,6 +21,16 @@
 // issuer (and TMEM owner), warps 2..5 = epilogue (one TMEM lane quadrant each).
 // Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
 // tile overlap the main loop of the next.
+//
+// CTA-pair form (CG = 2, K-major operands): a cluster of two CTAs computes a
+// 256 x 256 tile with M = 256 MMAs issued by the first CTA.  Each CTA loads
+// its own 128 rows of A and 128 of the tile's 256 rows of B (the tensor cores
+// of the pair exchange the B halves), so a CTA's stage is 32 KB instead of
+// 48 KB and the ring holds 6 stages; each CTA's epilogue reads its own 128
+// accumulator rows.  The pair's copies complete on the first CTA's "full"
+// barriers, the MMA completions arrive on both CTAs' "empty" and
+// "accumulator full" barriers, and both CTAs' epilogue warps release an
+// accumulator on the first CTA's "accumulator empty" barrier.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -33,12 +43,18 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int THREADS = 192;
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
-constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;  // 32 KB
-constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+// Ring of CG-CTA tiles: B rows held per CTA BN / CG (32 or 16 KB a stage).
+template <int CG>
+__host__ __device__ constexpr int ring_stages() { return CG == 2 ? 6 : 4; }
+template <int CG>
+__host__ __device__ constexpr uint32_t b_stage_bytes() { return (BN / CG) * BK * 2; }
+template <int CG>
+__host__ __device__ constexpr uint32_t ring_stage_bytes() { return A_STAGE_BYTES + b_stage_bytes<CG>(); }
+// Alignment slack, the ring, and its barriers.
+template <int CG>
+__host__ __device__ constexpr size_t ring_smem_bytes() { return 1024 + ring_stages<CG>() * ring_stage_bytes<CG>() + 256; }
 // Epilogue staging in shared memory behind the stage ring (1 KB of barriers
 // between them), 32 rows x 32 columns of bf16 (64-byte rows) per matrix:
 //   SwiGLU derivative: G and U of a chunk, two chunks per epilogue warp;
@@ -59,12 +75,14 @@ template <int EPI>
 __host__ __device__ constexpr size_t stage_bytes() {
   return EPI == EPI_SWIGLU ? 4 * SWG_WARP_BYTES : EPI == EPI_QKV ? 4 * MAT_BYTES : 4 * 2 * chunk_bytes<EPI>();
 }
-template <int EPI>
+template <int EPI, int CG>
 __host__ __device__ constexpr size_t smem_bytes() {
-  return SMEM_BYTES + (stage_bytes<EPI>() ? 1024 + stage_bytes<EPI>() : 0);
+  return ring_smem_bytes<CG>() + (stage_bytes<EPI>() ? 1024 + stage_bytes<EPI>() : 0);
 }
-static_assert(smem_bytes<EPI_DSWIGLU>() <= 227 * 1024 && smem_bytes<EPI_SWIGLU>() <= 227 * 1024 &&
-                  smem_bytes<EPI_RESID>() <= 227 * 1024 && smem_bytes<EPI_QKV>() <= 227 * 1024,
+static_assert(smem_bytes<EPI_DSWIGLU, 1>() <= 227 * 1024 && smem_bytes<EPI_SWIGLU, 1>() <= 227 * 1024 &&
+                  smem_bytes<EPI_RESID, 1>() <= 227 * 1024 && smem_bytes<EPI_QKV, 1>() <= 227 * 1024 &&
+                  smem_bytes<EPI_DSWIGLU, 2>() <= 227 * 1024 && smem_bytes<EPI_SWIGLU, 2>() <= 227 * 1024 &&
+                  smem_bytes<EPI_RESID, 2>() <= 227 * 1024 && smem_bytes<EPI_QKV, 2>() <= 227 * 1024,
               "shared memory");
 // Raster: tiles are visited in bands of group_m m-tiles (all n-tiles of a band
 // before the next band), group_m chosen so one band of A is ~32 MB and stays
@@ -75,6 +93,11 @@ constexpr size_t kBandBytes = size_t(32) << 20;
 constexpr size_t kBBandBytes = size_t(64) << 20;
 constexpr int kBBandTiles = 16;  // 12 and 24 measured: equal and 3 % slower (headline layer)
 constexpr uint32_t TMEM_COLS = 512;
+#ifndef TSP_GEMM_PAIRS
+#define TSP_GEMM_PAIRS 1
+#endif
+// CTA-pair tiles for the K-major GEMMs (0 at build time: one-CTA tiles only).
+constexpr bool kGemmPairs = TSP_GEMM_PAIRS != 0;
 
 struct GemmShape {
   int M, N, K;
@@ -165,12 +188,16 @@ __device__ __forceinline__ void zigzag_row_to_pos(int64_t m, const EpiParams& ep
 //   EPI_SWIGLU:  the G|U copy kept for the backward / SiLU(G)*U;
 //   EPI_QKV:     Q [T][h] / K [B*Hk*S][dh] / tmE2: V, [B*Hk*S][dh] or V^T
 //                [B*Hk*dh][S] (only when the chunk length is a multiple of 32).
-template <int EPI, bool AMN, bool BMN>
+template <int EPI, bool AMN, bool BMN, int CG>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmE0, const __grid_constant__ CUtensorMap tmE1,
                         const __grid_constant__ CUtensorMap tmE2,
                         const GemmShape shape, const EpiParams ep) {
+  static_assert(CG == 1 || (CG == 2 && !AMN && !BMN), "CTA pairs take K-major operands");
+  constexpr int STAGES = ring_stages<CG>();
+  constexpr uint32_t B_STAGE_BYTES = b_stage_bytes<CG>();
+  constexpr uint32_t STAGE_BYTES = ring_stage_bytes<CG>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* smA = smem;
@@ -187,6 +214,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // Tiles of TM rows: this CTA's rows of tile mt start at mt * TM + roff.  The
+  // pair walks its tiles together (first tile t0, stride tstep).
+  constexpr int TM = BM * CG;
+  const uint32_t crank = CG == 2 ? cluster_ctarank() : 0;
+  const int roff = (int)crank * BM;
+  const int t0 = CG == 2 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int tstep = CG == 2 ? (int)gridDim.x / 2 : (int)gridDim.x;
+  const bool leader = crank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -195,7 +230,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      // CTA pairs: one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[a], CG == 2 ? 8 : 128);
     }
     mbar_init(drain, 1);
     if constexpr (streamed_epi<EPI>())
@@ -219,11 +255,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2)
+    cluster_sync_all();  // both CTAs' barriers initialised before any copy or commit reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -232,16 +276,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < shape.num_tiles && ok; t += gridDim.x) {
+      for (int t = t0; t < shape.num_tiles && ok; t += tstep) {
         int mt, nt;
         tile_coords(t, shape, mt, nt);
-        const int arow = ep.a_natural ? (int)zigzag_row_to_natural((int64_t)mt * BM, ep) : mt * BM;
+        // (the second CTA's rows of a pair's last tile may lie past M: zeros)
+        const int64_t r_a = (int64_t)mt * TM + roff;
+        const int arow = (ep.a_natural && r_a < shape.M) ? (int)zigzag_row_to_natural(r_a, ep) : (int)r_a;
         for (int kb = 0; kb < shape.kblocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 1)) {
             ok = false;
             break;
+          }
+          if constexpr (CG == 2) {
+            // the first CTA's barrier counts both CTAs' bytes; the second CTA's
+            // copies complete on it (possibly before this arrival: the
+            // transaction count may go negative within a phase)
+            if (leader) {
+              mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
+              tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, &full[s]);
+              tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
+            } else {
+              const uint32_t fb = cluster_smem_addr(&full[s], 0);
+              tma_load_2d_pair(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, fb);
+              tma_load_2d_pair(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN + BN / 2, fb);
+            }
+            continue;
           }
           mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
           if constexpr (AMN) {
@@ -261,24 +322,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       // Before leaving, make sure every copy this thread issued has landed
-      // (always true on the normal path, bounded on the abort path).
+      // (always true on the normal path, bounded on the abort path).  The
+      // second CTA of a pair cannot wait on the first CTA's barriers; its
+      // copies have landed once the first CTA's MMAs have consumed them, which
+      // the closing cluster barrier orders before either CTA exits.
       const uint32_t issued = it;
       const uint32_t first = issued > (uint32_t)STAGES ? issued - STAGES : 0;
-      for (uint32_t j = first; j < issued; ++j) {
+      for (uint32_t j = first; j < issued && leader; ++j) {
         volatile int dummy = 0;
         mbar_wait(&full[j % STAGES], (j / STAGES) & 1, &dummy, ep.err, (KID_GEMM_TC << 8) | 2);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, AMN, BMN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(TM, BN, AMN, BMN);
       uint32_t it = 0, tl = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < shape.num_tiles && ok; t += gridDim.x, ++tl) {
+      for (int t = t0; t < shape.num_tiles && ok; t += tstep, ++tl) {
         const int acc = tl & 1;
         const uint32_t aph = (tl >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 3)) break;
+        if (!mbar_wait<CG == 2>(&tempty[acc], aph ^ 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 3)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < shape.kblocks; ++kb, ++it) {
@@ -296,15 +360,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             // MN-major: +16 K rows = +2048 bytes.
             const uint64_t adesc = AMN ? sdesc_mn_sw128(sa + 2048 * k, 8192) : sdesc_kmajor_sw128(sa) + 2 * k;
             const uint64_t bdesc = BMN ? sdesc_mn_sw128(sb + 2048 * k, 8192) : sdesc_kmajor_sw128(sb) + 2 * k;
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+            if constexpr (CG == 2)
+              umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+            else
+              umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
           }
-          umma_commit(&empty[s]);
+          if constexpr (CG == 2)
+            umma_commit_pair_mc(&empty[s], 0x3);  // both CTAs' stage s is free
+          else
+            umma_commit(&empty[s]);
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (CG == 2)
+          umma_commit_pair_mc(&tfull[acc], 0x3);
+        else
+          umma_commit(&tfull[acc]);
       }
       // Drain: wait until every MMA issued above has completed before TMEM is freed.
-      umma_commit(drain);
+      if constexpr (CG == 2)
+        umma_commit_pair(drain);
+      else
+        umma_commit(drain);
       volatile int dummy = 0;
       mbar_wait(drain, 0, &dummy, ep.err, (KID_GEMM_TC << 8) | 5);
     }
@@ -326,7 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tile_coords(tt, shape, mq, nq);
       const int b = q_issued & 1;
       uint8_t* dst = gbuf + b * CH;
-      const int r0 = mq * BM + quad * 32;
+      const int r0 = mq * TM + roff + quad * 32;
       mbar_arrive_expect_tx(&gb_full[b], CH);
       if constexpr (EPI == EPI_DSWIGLU) {
         const int gcol = gu_col(nq * BN + c * 32);
@@ -342,13 +418,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr bool streamed = streamed_epi<EPI>();
     if constexpr (streamed) {
       if (lane == 0) {
-        issue_chunk(blockIdx.x, 0);
-        issue_chunk(blockIdx.x, 1);
+        issue_chunk(t0, 0);
+        issue_chunk(t0, 1);
       }
     }
     bool epi_ok = true;
     uint32_t tl = 0;
-    for (int t = blockIdx.x; t < shape.num_tiles && epi_ok; t += gridDim.x, ++tl) {
+    for (int t = t0; t < shape.num_tiles && epi_ok; t += tstep, ++tl) {
       int mt, nt;
       tile_coords(t, shape, mt, nt);
       const int acc = tl & 1;
@@ -357,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool got = mbar_wait(&tfull[acc], aph, abort_flag, ep.err, (KID_GEMM_TC << 8) | 6);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const int64_t m = (int64_t)mt * BM + row;
+      const int64_t m = (int64_t)mt * TM + roff + row;
       const bool valid = m < shape.M;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       if constexpr (EPI == EPI_SWIGLU) {
@@ -370,7 +446,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* su = sg + 2048;
         uint8_t* so = sg + 4096;
         const bool keep = ep.aux != nullptr;
-        const int r0 = mt * BM + quad * 32;
+        const int r0 = mt * TM + roff + quad * 32;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float g[32], u[32];
@@ -465,7 +541,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           fence_proxy_async_smem();  // the stores below read what the threads wrote
           __syncwarp();
           if (lane == 0) {
-            const int gcol = gu_col(nt * BN + c * 32), r0 = mt * BM + quad * 32;
+            const int gcol = gu_col(nt * BN + c * 32), r0 = mt * TM + roff + quad * 32;
             if (r0 < shape.M) {  // a box starting past the last row has nothing to store
               tma_store_2d(&tmE1, gcol, r0, gs);
               tma_store_2d(&tmE1, gcol + 128, r0, us);
@@ -474,8 +550,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             bulk_wait_read_all();  // the buffer is free once the stores have read it
             if (c + 2 < BN / 32)
               issue_chunk(t, c + 2);
-            else if (t + (int)gridDim.x < shape.num_tiles)
-              issue_chunk(t + (int)gridDim.x, c + 2 - BN / 32);
+            else if (t + tstep < shape.num_tiles)
+              issue_chunk(t + tstep, c + 2 - BN / 32);
           }
           __syncwarp();
         }
@@ -486,7 +562,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // TMA.  Residual and output rows follow the natural order when asked
         // (32 zigzag rows of a chunk of 128-row multiples are 32 consecutive
         // natural rows); rows past M are not stored.
-        const int r0 = mt * BM + quad * 32;
+        const int r0 = mt * TM + roff + quad * 32;
         const int orow = (ep.out_natural && r0 < shape.M) ? (int)zigzag_row_to_natural(r0, ep) : r0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c, ++q_done) {
@@ -521,8 +597,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             bulk_wait_read_all();
             if (c + 2 < BN / 32)
               issue_chunk(t, c + 2);
-            else if (t + (int)gridDim.x < shape.num_tiles)
-              issue_chunk(t + (int)gridDim.x, c + 2 - BN / 32);
+            else if (t + tstep < shape.num_tiles)
+              issue_chunk(t + tstep, c + 2 - BN / 32);
           }
           __syncwarp();
         }
@@ -535,7 +611,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // 32 x 32 block (64-byte rows, 64-byte swizzle; V^T transposed: rows are
         // head dims, columns positions) and one lane stores it as one box.
         uint8_t* sb = gstage + quad * MAT_BYTES;
-        const int r0 = mt * BM + quad * 32;
+        const int r0 = mt * TM + roff + quad * 32;
         int b0 = 0;
         int64_t p0 = 0;
         if (r0 < shape.M) zigzag_row_to_pos(r0, ep, b0, p0);
@@ -627,7 +703,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      if constexpr (CG == 2) {
+        // one arrival per warp on the first CTA's barrier (the warp's TMEM
+        // loads have all completed: tcgen05.ld waits inside each load)
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(&tempty[acc]);
+          else
+            mbar_arrive_cluster(cluster_smem_addr(&tempty[acc], 0));
+        }
+      } else {
+        mbar_arrive(&tempty[acc]);
+      }
     }
     if constexpr (EPI == EPI_SWIGLU || EPI == EPI_QKV) {
       if (lane == 0) bulk_wait_all();  // every staged store complete before leaving (none on the per-row path)
@@ -647,10 +735,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    // Neither CTA leaves (or frees TMEM) while the other may still signal its
+    // barriers or the first CTA's MMAs may still write its TMEM.
+    __syncwarp();
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (CG == 2)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -714,14 +812,76 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
                        const CUtensorMap& te2, const GemmShape& s, const EpiParams& ep, cudaStream_t stream) {
   static std::atomic<unsigned long long> configured{0};  // devices set up for this instantiation
   if (needs_setup(configured)) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, AMN, BMN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<EPI>());
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, AMN, BMN, 1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<EPI, 1>());
     if (e != cudaSuccess) return e;
     mark_setup_done(configured);
   }
   const int grid = s.num_tiles < num_sms() ? s.num_tiles : num_sms();
-  gemm_bf16_tc_kernel<EPI, AMN, BMN><<<grid, THREADS, smem_bytes<EPI>(), stream>>>(ta, tb, tg, tdg, te2, s, ep);
+  gemm_bf16_tc_kernel<EPI, AMN, BMN, 1><<<grid, THREADS, smem_bytes<EPI, 1>(), stream>>>(ta, tb, tg, tdg, te2, s, ep);
   return cudaGetLastError();
+}
+
+// CTA-pair kernels: launched as clusters of two, one pair per co-resident
+// cluster slot (at most one tile per pair).
+template <int EPI>
+cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int pairs, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<EPI, 2>();
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Clusters of two the pair kernel can keep resident on the current device
+// (queried once per device), 0 if none.
+template <int EPI>
+int pair_slots() {
+  static std::atomic<int> slots[64];
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (needs_setup(configured)) {
+    int n = 0;
+    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, false, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes<EPI, 2>()) == cudaSuccess) {
+      cudaLaunchAttribute attr[1];
+      const cudaLaunchConfig_t cfg = pair_config<EPI>(attr, num_sms() / 2, nullptr);
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel<EPI, false, false, 2>, &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();  // a refused query leaves the one-SM kernel in use
+    slots[dev].store(n < 0 ? 0 : n);
+    mark_setup_done(configured);
+  }
+  return slots[dev].load();
+}
+
+template <int EPI>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg, const CUtensorMap& tdg,
+                        const CUtensorMap& te2, const GemmShape& s, const EpiParams& ep, int slots,
+                        cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config<EPI>(attr, s.num_tiles < slots ? s.num_tiles : slots, stream);
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<EPI, false, false, 2>, ta, tb, tg, tdg, te2, s, ep);
+}
+
+// Pair slots for the K-major instantiation of `epi` (0: use one-CTA tiles).
+int pair_slots_for(EpiKind epi) {
+  switch (epi) {
+    case EPI_STORE: return pair_slots<EPI_STORE>();
+    case EPI_RESID: return pair_slots<EPI_RESID>();
+    case EPI_QKV: return pair_slots<EPI_QKV>();
+    case EPI_SWIGLU: return pair_slots<EPI_SWIGLU>();
+    case EPI_DSWIGLU: return pair_slots<EPI_DSWIGLU>();
+    default: return 0;
+  }
 }
 
 }  // namespace
@@ -732,9 +892,18 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   if (N % BN || K % BK || lda % 8 || ldb % 8) return TSP_ERR_UNSUPPORTED;
   if (a_mn && M % 64) return TSP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) return TSP_ERR_INVALID_ARG;
+  // CTA pairs (256 x 256 tiles) for K-major operands with more than one
+  // 128-row block of A, where the device can keep pairs resident.  Measured
+  // at 2 x 16K tokens, h = 4096 (same box, interleaved runs): QKV 1.94 ->
+  // 1.91 ms, output projection 0.678 -> 0.668, down projection 2.355 ->
+  // 2.21, gate/up with its G|U copy (training) 4.70 -> 4.37; the inference
+  // gate/up (no copy) 4.38 -> 4.44, so it keeps one-CTA tiles.
+  const bool pair_shape = !a_mn && !b_mn && M > BM && !(epi == EPI_SWIGLU && !ep.aux);
+  const int slots = (kGemmPairs && pair_shape) ? pair_slots_for(epi) : 0;
+  const int CG = slots > 0 ? 2 : 1;
   CUtensorMap ta, tb;
   const bool ok_a = a_mn ? make_tma_2d_bf16(&ta, A, K, M, lda, 64) : make_tma_2d_bf16(&ta, A, M, K, lda, BM);
-  const bool ok_b = b_mn ? make_tma_2d_bf16(&tb, B, K, N, ldb, 64) : make_tma_2d_bf16(&tb, B, N, K, ldb, BN);
+  const bool ok_b = b_mn ? make_tma_2d_bf16(&tb, B, K, N, ldb, 64) : make_tma_2d_bf16(&tb, B, N, K, ldb, BN / CG);
   if (!ok_a || !ok_b) return TSP_ERR_CUDA;
   // Epilogue tensor maps: G|U in and dG|dU out of the SwiGLU-derivative
   // epilogue; the G|U copy and SiLU(G)*U out of the SwiGLU epilogue.
@@ -776,13 +945,13 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   s.M = M;
   s.N = N;
   s.K = K;
-  s.num_m = (M + BM - 1) / BM;
+  s.num_m = (M + BM * CG - 1) / (BM * CG);
   s.num_n = N / BN;
   s.num_tiles = s.num_m * s.num_n;
   s.kblocks = K / BK;
   {
     const size_t band_rows = kBandBytes / ((size_t)K * 2);
-    int gm = (int)(band_rows / BM);
+    int gm = (int)(band_rows / (BM * CG));
     s.group_m = gm < 1 ? 1 : (gm > s.num_m ? s.num_m : gm);
     s.group_n = 0;
     if (N < M) {
@@ -800,6 +969,17 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
     }
   }
   cudaError_t e;
+  if (CG == 2) {
+    switch (epi) {
+      case EPI_STORE: e = launch_pair<EPI_STORE>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
+      case EPI_RESID: e = launch_pair<EPI_RESID>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
+      case EPI_QKV: e = launch_pair<EPI_QKV>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
+      case EPI_SWIGLU: e = launch_pair<EPI_SWIGLU>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
+      case EPI_DSWIGLU: e = launch_pair<EPI_DSWIGLU>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
+      default: return TSP_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
+  }
   const int mode = (a_mn ? 2 : 0) | (b_mn ? 1 : 0);
   switch (epi * 4 + mode) {
     case EPI_STORE * 4 + 0: e = launch_epi<EPI_STORE, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
