@@ -272,6 +272,46 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// Cluster launch control: asks to cancel the launch of a cluster of this grid
+// that has not started, so that this cluster does its work instead.  The
+// 16-byte response is written to `resp` in every CTA of this cluster (same
+// offset), each CTA's mbarrier at `bar`'s offset receiving 16 transaction
+// bytes.  No request may follow a response that cancelled nothing.
+__device__ __forceinline__ void clc_try_cancel_all(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+      "[%0], [%1];" ::"r"(smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+// The same for a grid launched without clusters (each CTA its own cluster):
+// the response goes to this CTA only.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                   smem_u32(resp)),
+               "r"(smem_u32(bar))
+               : "memory");
+}
+// x index of the first CTA of the cluster a response cancelled, or -1 if it
+// cancelled nothing.
+__device__ __forceinline__ int clc_cancelled_x(const void* resp) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n"
+      ".reg .b128 r;\n"
+      ".reg .pred p;\n"
+      "ld.shared.b128 r, [%2];\n"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "mov.u32 %1, 0;\n"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n"
+      "}\n"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_u32(resp))
+      : "memory");
+  return ok ? (int)x : -1;
+}
+
 // CTA-pair forms (every tcgen05 instruction of a kernel uses one CTA-group
 // size).  Allocation and deallocation: one warp of each CTA of the pair,
 // together; the same TMEM columns are then held in both CTAs.

@@ -16,8 +16,10 @@
 //   - gate/up projection with SiLU(gate) * up computed from one TMEM tile that
 //     holds matching gate and up columns.
 //
-// Tile 128 x 256 x 64, 4-stage TMA ring (128-byte swizzle), one CTA per SM,
-// persistent over tiles.  Warp roles: warp 0 = TMA producer, warp 1 = MMA
+// Tile 128 x 256 x 64, 4-stage TMA ring (128-byte swizzle).  The grid has one
+// CTA per tile; the CTAs that start (one per SM) take over the tiles of those
+// that have not started by cancelling their launch (cluster launch control),
+// in tile order, so each SM runs one CTA over many tiles.  Warp roles: warp 0 = TMA producer, warp 1 = MMA
 // issuer (and TMEM owner), warps 2..5 = epilogue (one TMEM lane quadrant each).
 // Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
 // tile overlap the main loop of the next.
@@ -52,9 +54,11 @@ template <int CG>
 __host__ __device__ constexpr uint32_t b_stage_bytes() { return (BN / CG) * BK * 2; }
 template <int CG>
 __host__ __device__ constexpr uint32_t ring_stage_bytes() { return A_STAGE_BYTES + b_stage_bytes<CG>(); }
-// Alignment slack, the ring, and its barriers.
+// Alignment slack, the ring, and its barriers (and the tile-request ring).
 template <int CG>
-__host__ __device__ constexpr size_t ring_smem_bytes() { return 1024 + ring_stages<CG>() * ring_stage_bytes<CG>() + 256; }
+__host__ __device__ constexpr size_t ring_smem_bytes() { return 1024 + ring_stages<CG>() * ring_stage_bytes<CG>() + 512; }
+// Tile requests in flight (slots of the response ring).
+constexpr int kResp = 4;
 // Epilogue staging in shared memory behind the stage ring (1 KB of barriers
 // between them), 32 rows x 32 columns of bf16 (64-byte rows) per matrix:
 //   SwiGLU derivative: G and U of a chunk, two chunks per epilogue warp;
@@ -211,16 +215,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + 8);
   uint8_t* gstage = smem + STAGES * STAGE_BYTES + 1024;  // epilogue staging (all but EPI_STORE)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Tile-request responses (kResp x 16 bytes, 16-byte aligned) and their barriers
+  uint64_t* resp_full = reinterpret_cast<uint64_t*>(tmem_slot + 2);
+  uint64_t* resp_empty = resp_full + kResp;
+  uint8_t* resp = reinterpret_cast<uint8_t*>(resp_empty + kResp);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // Tiles of TM rows: this CTA's rows of tile mt start at mt * TM + roff.  The
-  // pair walks its tiles together (first tile t0, stride tstep).
+  // Tiles of TM rows: this CTA's rows of tile mt start at mt * TM + roff.
+  // The pair walks its tiles together, starting with tile t0.
   constexpr int TM = BM * CG;
   const uint32_t crank = CG == 2 ? cluster_ctarank() : 0;
   const int roff = (int)crank * BM;
   const int t0 = CG == 2 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-  const int tstep = CG == 2 ? (int)gridDim.x / 2 : (int)gridDim.x;
   const bool leader = crank == 0;
 
   if (threadIdx.x == 0) {
@@ -234,6 +241,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], CG == 2 ? 8 : 128);
     }
     mbar_init(drain, 1);
+    for (int r = 0; r < kResp; ++r) {
+      mbar_init(&resp_full[r], 1);
+      // readers: the (first) CTA's producer, MMA thread and 4 epilogue warps,
+      // and a pair's second CTA's producer and 4 epilogue warps
+      mbar_init(&resp_empty[r], CG == 2 ? 11 : 6);
+    }
     if constexpr (streamed_epi<EPI>())
       for (int i = 0; i < 8; ++i) mbar_init(&gbar[i], 1);
     *abort_flag = 0;
@@ -271,12 +284,53 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Tile sequence.  The grid has one CTA (pair: one cluster) per tile, and
+  // step 0 is the CTA's (pair's) own tile.  At the start of step j the
+  // (first CTA's) producer asks for the tile of step j + 1 by cancelling the
+  // launch of a CTA (cluster) that has not started, whose tile is then done
+  // here: the tiles in flight stay a window of consecutive tiles however
+  // the CTAs' speeds differ, and the operands they share meet in L2.  (With
+  // a fixed tile stride the CTAs drift apart over many waves: the CTA-pair
+  // down projection at 2 x 16K tokens read 9.55 GB from DRAM that way, 4.02
+  // GB in this order.)  The response lands in ring slot j % kResp (of both
+  // CTAs of a pair); every role reads its own copy and releases the slot on
+  // the (first) CTA's barrier.
+  // next_tile: (one thread) the tile of step s >= 1, or -1 when none is left.
+  auto next_tile = [&](uint32_t s, unsigned int code) -> int {
+    const uint32_t slot = (s - 1) % kResp;
+    if (!mbar_wait<CG == 2>(&resp_full[slot], ((s - 1) / kResp) & 1, abort_flag, ep.err, code)) return -1;
+    const int x = clc_cancelled_x(resp + slot * 16);
+    if (leader)
+      mbar_arrive(&resp_empty[slot]);
+    else
+      mbar_arrive_cluster(cluster_smem_addr(&resp_empty[slot], 0));
+    return x < 0 ? -1 : x / CG;
+  };
+
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, step = 0;
       bool ok = true;
-      for (int t = t0; t < shape.num_tiles && ok; t += tstep) {
+      for (int t = t0; t >= 0 && ok; t = next_tile(++step, (KID_GEMM_TC << 8) | 10)) {
+        {
+          // ask for the tile of the next step (no request follows one that found none)
+          const uint32_t slot = step % kResp;
+          if (leader) {
+            if (!mbar_wait<CG == 2>(&resp_empty[slot], ((step / kResp) & 1) ^ 1, abort_flag, ep.err,
+                                    (KID_GEMM_TC << 8) | 9)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&resp_full[slot], 16);
+            if constexpr (CG == 2)
+              clc_try_cancel_all(resp + slot * 16, &resp_full[slot]);
+            else
+              clc_try_cancel(resp + slot * 16, &resp_full[slot]);
+          } else {
+            mbar_arrive_expect_tx(&resp_full[slot], 16);
+          }
+        }
         int mt, nt;
         tile_coords(t, shape, mt, nt);
         // (the second CTA's rows of a pair's last tile may lie past M: zeros)
@@ -339,7 +393,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(TM, BN, AMN, BMN);
       uint32_t it = 0, tl = 0;
       bool ok = true;
-      for (int t = t0; t < shape.num_tiles && ok; t += tstep, ++tl) {
+      for (int t = t0; t >= 0 && ok; t = next_tile(tl + 1, (KID_GEMM_TC << 8) | 11), ++tl) {
         const int acc = tl & 1;
         const uint32_t aph = (tl >> 1) & 1;
         if (!mbar_wait<CG == 2>(&tempty[acc], aph ^ 1, abort_flag, ep.err, (KID_GEMM_TC << 8) | 3)) break;
@@ -424,7 +478,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     bool epi_ok = true;
     uint32_t tl = 0;
-    for (int t = t0; t < shape.num_tiles && epi_ok; t += tstep, ++tl) {
+    for (int t = t0, tn = -1; t >= 0 && epi_ok; t = tn, ++tl) {
       int mt, nt;
       tile_coords(t, shape, mt, nt);
       const int acc = tl & 1;
@@ -432,6 +486,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Warp-uniform decision: tcgen05.ld below needs every lane of the warp.
       const bool got = mbar_wait(&tfull[acc], aph, abort_flag, ep.err, (KID_GEMM_TC << 8) | 6);
       if (!__all_sync(0xffffffffu, got)) break;
+      // the tile after this one (lane 0 reads it, the warp shares it)
+      tn = lane == 0 ? next_tile(tl + 1, (KID_GEMM_TC << 8) | 12) : 0;
+      tn = __shfl_sync(0xffffffffu, tn, 0);
       tc_fence_after();
       const int64_t m = (int64_t)mt * TM + roff + row;
       const bool valid = m < shape.M;
@@ -550,8 +607,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             bulk_wait_read_all();  // the buffer is free once the stores have read it
             if (c + 2 < BN / 32)
               issue_chunk(t, c + 2);
-            else if (t + tstep < shape.num_tiles)
-              issue_chunk(t + tstep, c + 2 - BN / 32);
+            else if (tn >= 0)
+              issue_chunk(tn, c + 2 - BN / 32);
           }
           __syncwarp();
         }
@@ -597,8 +654,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             bulk_wait_read_all();
             if (c + 2 < BN / 32)
               issue_chunk(t, c + 2);
-            else if (t + tstep < shape.num_tiles)
-              issue_chunk(t + tstep, c + 2 - BN / 32);
+            else if (tn >= 0)
+              issue_chunk(tn, c + 2 - BN / 32);
           }
           __syncwarp();
         }
@@ -817,13 +874,14 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     if (e != cudaSuccess) return e;
     mark_setup_done(configured);
   }
-  const int grid = s.num_tiles < num_sms() ? s.num_tiles : num_sms();
-  gemm_bf16_tc_kernel<EPI, AMN, BMN, 1><<<grid, THREADS, smem_bytes<EPI, 1>(), stream>>>(ta, tb, tg, tdg, te2, s, ep);
+  // one CTA per tile: the CTAs that start cancel the launch of the others and do their tiles
+  gemm_bf16_tc_kernel<EPI, AMN, BMN, 1><<<s.num_tiles, THREADS, smem_bytes<EPI, 1>(), stream>>>(ta, tb, tg, tdg, te2,
+                                                                                            s, ep);
   return cudaGetLastError();
 }
 
-// CTA-pair kernels: launched as clusters of two, one pair per co-resident
-// cluster slot (at most one tile per pair).
+// CTA-pair kernels: launched as clusters of two, one cluster per tile; the
+// clusters that start cancel the launch of the others and do their tiles.
 template <int EPI>
 cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int pairs, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -865,10 +923,9 @@ int pair_slots() {
 
 template <int EPI>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg, const CUtensorMap& tdg,
-                        const CUtensorMap& te2, const GemmShape& s, const EpiParams& ep, int slots,
-                        cudaStream_t stream) {
+                        const CUtensorMap& te2, const GemmShape& s, const EpiParams& ep, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = pair_config<EPI>(attr, s.num_tiles < slots ? s.num_tiles : slots, stream);
+  const cudaLaunchConfig_t cfg = pair_config<EPI>(attr, s.num_tiles, stream);
   return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<EPI, false, false, 2>, ta, tb, tg, tdg, te2, s, ep);
 }
 
@@ -894,11 +951,10 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) return TSP_ERR_INVALID_ARG;
   // CTA pairs (256 x 256 tiles) for K-major operands with more than one
   // 128-row block of A, where the device can keep pairs resident.  Measured
-  // at 2 x 16K tokens, h = 4096 (same box, interleaved runs): QKV 1.94 ->
-  // 1.91 ms, output projection 0.678 -> 0.668, down projection 2.355 ->
-  // 2.21, gate/up with its G|U copy (training) 4.70 -> 4.37; the inference
-  // gate/up (no copy) 4.38 -> 4.44, so it keeps one-CTA tiles.
-  const bool pair_shape = !a_mn && !b_mn && M > BM && !(epi == EPI_SWIGLU && !ep.aux);
+  // at 2 x 16K tokens, h = 4096, under ncu: QKV 1.70 -> 1.69 ms, output
+  // projection 0.588 -> 0.585, gate/up 4.12 -> 3.91, down 2.18 -> 2.01;
+  // forward step (same box, interleaved) 12.17-12.19 -> 11.88-11.92 ms.
+  const bool pair_shape = !a_mn && !b_mn && M > BM;
   const int slots = (kGemmPairs && pair_shape) ? pair_slots_for(epi) : 0;
   const int CG = slots > 0 ? 2 : 1;
   CUtensorMap ta, tb;
@@ -971,11 +1027,11 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   cudaError_t e;
   if (CG == 2) {
     switch (epi) {
-      case EPI_STORE: e = launch_pair<EPI_STORE>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
-      case EPI_RESID: e = launch_pair<EPI_RESID>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
-      case EPI_QKV: e = launch_pair<EPI_QKV>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
-      case EPI_SWIGLU: e = launch_pair<EPI_SWIGLU>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
-      case EPI_DSWIGLU: e = launch_pair<EPI_DSWIGLU>(ta, tb, tg, tdg, te2, s, ep, slots, stream); break;
+      case EPI_STORE: e = launch_pair<EPI_STORE>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_RESID: e = launch_pair<EPI_RESID>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_QKV: e = launch_pair<EPI_QKV>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_SWIGLU: e = launch_pair<EPI_SWIGLU>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_DSWIGLU: e = launch_pair<EPI_DSWIGLU>(ta, tb, tg, tdg, te2, s, ep, stream); break;
       default: return TSP_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
