@@ -24,8 +24,8 @@
 // Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
 // tile overlap the main loop of the next.
 //
-// CTA-pair form (CG = 2, K-major operands): a cluster of two CTAs computes a
-// 256 x 256 tile with M = 256 MMAs issued by the first CTA.  Each CTA loads
+// CTA-pair form (CG = 2): a cluster of two CTAs computes a 256 x 256 tile
+// with M = 256 MMAs issued by the first CTA.  Each CTA loads
 // its own 128 rows of A and 128 of the tile's 256 rows of B (the tensor cores
 // of the pair exchange the B halves), so a CTA's stage is 32 KB instead of
 // 48 KB and the ring holds 6 stages; each CTA's epilogue reads its own 128
@@ -198,7 +198,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const __grid_constant__ CUtensorMap tmE0, const __grid_constant__ CUtensorMap tmE1,
                         const __grid_constant__ CUtensorMap tmE2,
                         const GemmShape shape, const EpiParams ep) {
-  static_assert(CG == 1 || (CG == 2 && !AMN && !BMN), "CTA pairs take K-major operands");
   constexpr int STAGES = ring_stages<CG>();
   constexpr uint32_t B_STAGE_BYTES = b_stage_bytes<CG>();
   constexpr uint32_t STAGE_BYTES = ring_stage_bytes<CG>();
@@ -347,14 +346,40 @@ __global__ void __launch_bounds__(THREADS, 1)
             // the first CTA's barrier counts both CTAs' bytes; the second CTA's
             // copies complete on it (possibly before this arrival: the
             // transaction count may go negative within a phase)
+            // MN-major operands: 64-wide boxes of this CTA's 128 rows of A / of B
+            const int b0 = nt * BN + (int)crank * (BN / 2);
             if (leader) {
               mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
-              tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, &full[s]);
-              tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN, &full[s]);
+              if constexpr (AMN) {
+#pragma unroll
+                for (int c = 0; c < BM / 64; ++c)
+                  tma_load_2d(smA + s * A_STAGE_BYTES + c * 8192, &tmA, (int)r_a + c * 64, kb * BK, &full[s]);
+              } else {
+                tma_load_2d(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, &full[s]);
+              }
+              if constexpr (BMN) {
+#pragma unroll
+                for (int c = 0; c < BN / 2 / 64; ++c)
+                  tma_load_2d(smB + s * B_STAGE_BYTES + c * 8192, &tmB, b0 + c * 64, kb * BK, &full[s]);
+              } else {
+                tma_load_2d(smB + s * B_STAGE_BYTES, &tmB, kb * BK, b0, &full[s]);
+              }
             } else {
               const uint32_t fb = cluster_smem_addr(&full[s], 0);
-              tma_load_2d_pair(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, fb);
-              tma_load_2d_pair(smB + s * B_STAGE_BYTES, &tmB, kb * BK, nt * BN + BN / 2, fb);
+              if constexpr (AMN) {
+#pragma unroll
+                for (int c = 0; c < BM / 64; ++c)
+                  tma_load_2d_pair(smA + s * A_STAGE_BYTES + c * 8192, &tmA, (int)r_a + c * 64, kb * BK, fb);
+              } else {
+                tma_load_2d_pair(smA + s * A_STAGE_BYTES, &tmA, kb * BK, arow, fb);
+              }
+              if constexpr (BMN) {
+#pragma unroll
+                for (int c = 0; c < BN / 2 / 64; ++c)
+                  tma_load_2d_pair(smB + s * B_STAGE_BYTES + c * 8192, &tmB, b0 + c * 64, kb * BK, fb);
+              } else {
+                tma_load_2d_pair(smB + s * B_STAGE_BYTES, &tmB, kb * BK, b0, fb);
+              }
             }
             continue;
           }
@@ -921,12 +946,19 @@ int pair_slots() {
   return slots[dev].load();
 }
 
-template <int EPI>
+template <int EPI, bool AMN, bool BMN>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg, const CUtensorMap& tdg,
                         const CUtensorMap& te2, const GemmShape& s, const EpiParams& ep, cudaStream_t stream) {
+  static std::atomic<unsigned long long> configured{0};  // devices set up for this instantiation
+  if (needs_setup(configured)) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, AMN, BMN, 2>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<EPI, 2>());
+    if (e != cudaSuccess) return e;
+    mark_setup_done(configured);
+  }
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pair_config<EPI>(attr, s.num_tiles, stream);
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<EPI, false, false, 2>, ta, tb, tg, tdg, te2, s, ep);
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<EPI, AMN, BMN, 2>, ta, tb, tg, tdg, te2, s, ep);
 }
 
 // Pair slots for the K-major instantiation of `epi` (0: use one-CTA tiles).
@@ -949,12 +981,12 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
   if (N % BN || K % BK || lda % 8 || ldb % 8) return TSP_ERR_UNSUPPORTED;
   if (a_mn && M % 64) return TSP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) return TSP_ERR_INVALID_ARG;
-  // CTA pairs (256 x 256 tiles) for K-major operands with more than one
-  // 128-row block of A, where the device can keep pairs resident.  Measured
+  // CTA pairs (256 x 256 tiles) when A has more than one 128-row block and
+  // the device can keep pairs resident.  Measured
   // at 2 x 16K tokens, h = 4096, under ncu: QKV 1.70 -> 1.69 ms, output
   // projection 0.588 -> 0.585, gate/up 4.12 -> 3.91, down 2.18 -> 2.01;
   // forward step (same box, interleaved) 12.17-12.19 -> 11.88-11.92 ms.
-  const bool pair_shape = !a_mn && !b_mn && M > BM;
+  const bool pair_shape = M > BM;
   const int slots = (kGemmPairs && pair_shape) ? pair_slots_for(epi) : 0;
   const int CG = slots > 0 ? 2 : 1;
   CUtensorMap ta, tb;
@@ -1025,18 +1057,24 @@ tsp_status gemm_bf16_tc(const void* A, int64_t lda, const void* B, int64_t ldb, 
     }
   }
   cudaError_t e;
+  const int mode = (a_mn ? 2 : 0) | (b_mn ? 1 : 0);
   if (CG == 2) {
-    switch (epi) {
-      case EPI_STORE: e = launch_pair<EPI_STORE>(ta, tb, tg, tdg, te2, s, ep, stream); break;
-      case EPI_RESID: e = launch_pair<EPI_RESID>(ta, tb, tg, tdg, te2, s, ep, stream); break;
-      case EPI_QKV: e = launch_pair<EPI_QKV>(ta, tb, tg, tdg, te2, s, ep, stream); break;
-      case EPI_SWIGLU: e = launch_pair<EPI_SWIGLU>(ta, tb, tg, tdg, te2, s, ep, stream); break;
-      case EPI_DSWIGLU: e = launch_pair<EPI_DSWIGLU>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+    switch (epi * 4 + mode) {
+      case EPI_STORE * 4 + 0: e = launch_pair<EPI_STORE, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_STORE * 4 + 1: e = launch_pair<EPI_STORE, false, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_STORE * 4 + 3: e = launch_pair<EPI_STORE, true, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_RESID * 4 + 0: e = launch_pair<EPI_RESID, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_RESID * 4 + 1: e = launch_pair<EPI_RESID, false, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_QKV * 4 + 0: e = launch_pair<EPI_QKV, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_SWIGLU * 4 + 0: e = launch_pair<EPI_SWIGLU, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
+      case EPI_DSWIGLU * 4 + 0:
+        e = launch_pair<EPI_DSWIGLU, false, false>(ta, tb, tg, tdg, te2, s, ep, stream);
+        break;
+      case EPI_DSWIGLU * 4 + 1: e = launch_pair<EPI_DSWIGLU, false, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
       default: return TSP_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? TSP_OK : TSP_ERR_CUDA;
   }
-  const int mode = (a_mn ? 2 : 0) | (b_mn ? 1 : 0);
   switch (epi * 4 + mode) {
     case EPI_STORE * 4 + 0: e = launch_epi<EPI_STORE, false, false>(ta, tb, tg, tdg, te2, s, ep, stream); break;
     case EPI_STORE * 4 + 1: e = launch_epi<EPI_STORE, false, true>(ta, tb, tg, tdg, te2, s, ep, stream); break;
