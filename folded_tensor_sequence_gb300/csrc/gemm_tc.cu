@@ -19,8 +19,9 @@
 // Tile 128 x 256 x 64, 4-stage TMA ring (128-byte swizzle).  The grid has one
 // CTA per tile; the CTAs that start (one per SM) take over the tiles of those
 // that have not started by cancelling their launch (cluster launch control),
-// in tile order, so each SM runs one CTA over many tiles.  Warp roles: warp 0 = TMA producer, warp 1 = MMA
-// issuer (and TMEM owner), warps 2..5 = epilogue (one TMEM lane quadrant each).
+// in tile order, so each SM runs one CTA over many tiles.  Warp roles: warp 0
+// = TMA producer, warp 1 = MMA issuer (and TMEM owner), warps 2..5 =
+// epilogue (one TMEM lane quadrant each).
 // Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
 // tile overlap the main loop of the next.
 //
@@ -100,7 +101,7 @@ constexpr uint32_t TMEM_COLS = 512;
 #ifndef TSP_GEMM_PAIRS
 #define TSP_GEMM_PAIRS 1
 #endif
-// CTA-pair tiles for the K-major GEMMs (0 at build time: one-CTA tiles only).
+// CTA-pair tiles for GEMMs of more than 128 rows (0 at build time: one-CTA tiles only).
 constexpr bool kGemmPairs = TSP_GEMM_PAIRS != 0;
 
 struct GemmShape {
@@ -343,10 +344,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           if constexpr (CG == 2) {
-            // the first CTA's barrier counts both CTAs' bytes; the second CTA's
+            // The first CTA's barrier counts both CTAs' bytes; the second CTA's
             // copies complete on it (possibly before this arrival: the
-            // transaction count may go negative within a phase)
-            // MN-major operands: 64-wide boxes of this CTA's 128 rows of A / of B
+            // transaction count may go negative within a phase).  MN-major
+            // operands come as 64-wide boxes of this CTA's 128 rows of A / of B.
             const int b0 = nt * BN + (int)crank * (BN / 2);
             if (leader) {
               mbar_arrive_expect_tx(&full[s], 2 * STAGE_BYTES);
