@@ -48,10 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # without its own capture, or a source changed since, reports null.
 NCU_TRAFFIC = {
     ("gate/up projection", "bf16_D8_b2_s16384_h4096"):
-        (2174.07e6 + 926.63e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "8f99559bd34e4afd"),
+        (2174.07e6 + 926.63e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "16a0278f61e1aa96"),
     # the same launch (M, N, K and kernel) as the multi-head workload's gate/up projection
     ("gate/up projection", "bf16_gqa8_D8_b2_s16384_h4096"):
-        (2174.07e6 + 926.63e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "8f99559bd34e4afd"),
+        (2174.07e6 + 926.63e6, "folded_tensor_sequence_gb300/csrc/gemm_tc.cu", "16a0278f61e1aa96"),
     ("attention", "bf16_D8_b2_s16384_h4096"):
         (833.823e6 + 250.399e6, "folded_tensor_sequence_gb300/csrc/attn_fwd_tc.cu", "6c52c6aefe671f3b"),
     ("attention", "bf16_D8_b1_s65536_h4096"):

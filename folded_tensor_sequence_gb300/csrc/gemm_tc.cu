@@ -934,13 +934,17 @@ int pair_slots() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (needs_setup(configured)) {
     int n = 0;
-    if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, false, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes<EPI, 2>()) == cudaSuccess) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<EPI, false, false, 2>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<EPI, 2>());
+    if (e == cudaSuccess) {
       cudaLaunchAttribute attr[1];
       const cudaLaunchConfig_t cfg = pair_config<EPI>(attr, num_sms() / 2, nullptr);
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel<EPI, false, false, 2>, &cfg) != cudaSuccess) n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel<EPI, false, false, 2>, &cfg);
     }
-    (void)cudaGetLastError();  // a refused query leaves the one-SM kernel in use
+    if (e != cudaSuccess) {
+      n = 0;
+      (void)cudaGetLastError();  // this query's own error: the one-CTA kernel stays in use
+    }
     slots[dev].store(n < 0 ? 0 : n);
     mark_setup_done(configured);
   }
